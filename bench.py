@@ -1,0 +1,473 @@
+"""Benchmark of the MHLA forward pass on GB300 (one JSON line on stdout).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--variant auto|simt|multipass] [--impl mine|reference]
+                    [--all-workloads] [--no-cpu-baseline]
+
+A step is one full forward (block summaries, mixing, output) over one batch
+of the workload's seeded synthetic inputs, already resident in HBM.  The
+metric is tokens*heads per second (B*H*N / step time).  The default workload
+is the video-shaped 3D grid (B=2, H=16, d=64, 16x64x64 tokens, 2x8x8 blocks,
+M=512): its 403 MB of inputs exceed the 126 MB L2, so no flush runs between
+timed steps.  With --all-workloads the other workloads are timed too (with an
+L2 flush between steps, outside the per-step events) and listed under
+"workloads".
+
+--impl reference times the float64 CPU oracle (the only reference there is)
+on the same workload: each step is one (batch, head) unit.
+
+Multi-GPU (torchrun): every rank runs an independent replica of the workload
+(units are independent, no collective on the data path); value = all ranks'
+tokens*heads / the slowest rank's time ("scaling": "weak").
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from token_level_head_phi_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "MHLA fwd tokens*heads/sec (d=64) and % of GB300 HBM/tensor roofline"
+UNIT = "tokens*heads/s"
+PHASES = ["summary", "mix", "output"]
+L2_BYTES = 126 * 1024 * 1024
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            d = json.load(fh)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ----------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="mhla_clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu=timestamp,{self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self, t0: float, t1: float):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        with open(self.path) as fh:
+            for line in fh:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 10:
+                    continue
+                rows.append(parts)
+        os.unlink(self.path)
+        # keep samples taken inside [t0, t1] (wall clock); nvidia-smi stamps are local time
+        def stamp(p):
+            try:
+                return time.mktime(time.strptime(p[0].split(".")[0], "%Y/%m/%d %H:%M:%S")) + \
+                    float("0." + p[0].split(".")[1]) if "." in p[0] else 0.0
+            except Exception:
+                return None
+        inside = [r for r in rows if stamp(r) is not None and t0 - 0.15 <= stamp(r) <= t1 + 0.15]
+        use = inside if inside else rows
+        sm = [float(r[2]) for r in use if r[2].replace(".", "").isdigit()]
+        smax = [float(r[3]) for r in use if r[3].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in use:
+            for name, val in zip(names, r[6:10]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(use), "samples_in_region": len(inside)}
+
+
+# ------------------------------------------------------------ my arm
+
+def phase_bytes(w: wl.Workload, info, variant: int):
+    """Compulsory bytes of each phase kernel: its inputs read once, outputs written once."""
+    import token_level_head_phi_gb300.binding as mb
+    el = 2 if w.dtype == "bf16" else 4
+    U, N, d, M = w.units, w.n_tokens, w.head_dim, w.n_blocks
+    R = d * d + 2 * d
+    st_el = 4 if variant == mb.VARIANT_SIMT else 2
+    rows = M * info.summary_splits
+    io = U * N * d * el
+    stack = U * rows * R * st_el
+    mixed = U * M * R * st_el
+    return {"summary": 2 * io + stack, "mix": stack + mixed + 4 * M * M, "output": io + mixed + io}
+
+
+def traffic_table():
+    """Per-launch DRAM bytes from the committed ncu summary, keyed by
+    (kernel, workload); each entry carries the hash of the kernel source it
+    was captured from and is ignored once that source changes."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    table = {}
+    if not os.path.exists(path):
+        return table
+    for line in open(path):
+        line = line.split("#", 1)[0].strip()
+        if not line:
+            continue
+        parts = line.split()
+        if len(parts) != 4:
+            continue
+        kernel, workload, nbytes, src_hash = parts
+        table[(kernel, workload)] = (float(nbytes), src_hash)
+    return table
+
+
+def source_hash(relpath: str) -> str:
+    h = hashlib.sha256()
+    with open(os.path.join(ROOT, relpath), "rb") as fh:
+        h.update(fh.read())
+    return h.hexdigest()[:12]
+
+
+PHASE_KERNEL = {  # variant -> phase -> (kernel name in ncu, source file)
+    1: {"summary": ("simt_summary_kernel", "token_level_head_phi_gb300/csrc/simt.cu"),
+        "mix": ("simt_mix_kernel", "token_level_head_phi_gb300/csrc/simt.cu"),
+        "output": ("simt_output_kernel", "token_level_head_phi_gb300/csrc/simt.cu")},
+}
+
+
+def run_mine(args, w: wl.Workload, world: int, rank: int, local: int, dist):
+    import torch
+    import token_level_head_phi_gb300.binding as mb
+    from token_level_head_phi_gb300 import build as mbuild
+
+    if rank == 0 or world == 1:
+        mbuild.build()
+    if dist is not None:
+        dist.barrier()
+    mb.load()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+
+    qn, kn, vn = wl.all_device_inputs(w)
+    mcn = wl.make_mc(w)
+
+    def to_dev(a):
+        t = torch.from_numpy(a)
+        if w.dtype == "bf16":
+            t = t.view(torch.bfloat16)
+        return t.to(dev)
+
+    q, k, v = to_dev(qn), to_dev(kn), to_dev(vn)
+    mc = torch.from_numpy(mcn).to(dev)
+    out = torch.empty_like(q)
+    p = mb.make_params(w.batch, w.heads, w.head_dim, w.grid, w.block, w.dtype, "elu1", w.norm, args.variant)
+    info = mb.mhla_plan(p)
+    ws = torch.empty(max(info.workspace_bytes, 1), dtype=torch.uint8, device=dev)
+    ws_bytes = ws.numel()
+    handle = stream.cuda_stream
+    io_bytes = q.numel() * q.element_size()
+    flush = None
+    if io_bytes * 3 < 2 * L2_BYTES:
+        flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+
+    def step():
+        st = mb.mhla_forward_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), mc.data_ptr(), p, out.data_ptr(),
+                                 ws.data_ptr(), ws_bytes, handle)
+        if st != 0:
+            raise mb.MhlaError(st, "mhla_forward")
+
+    for _ in range(args.warmup):
+        if flush is not None:
+            flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    code, detail = mb.mhla_device_status()
+    if code != 0:
+        raise RuntimeError(f"device status {code} during warm-up (detail {detail})")
+
+    # timed region: K steps, per-step phase events, no flush when inputs exceed L2
+    K = args.steps
+    ev_sets = [[torch.cuda.Event(enable_timing=True) for _ in range(mb.NUM_PHASE_EVENTS)] for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local) if rank == 0 else None
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+    t0 = time.time()
+    start.record(stream)
+    for i in range(K):
+        if flush is not None:
+            flush.zero_()
+        mb.mhla_set_phase_events(ev_sets[i])
+        step()
+    end.record(stream)
+    mb.mhla_set_phase_events(None)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    if dist is not None:
+        dist.barrier()
+    clocks = sampler.stop(t0, t1) if sampler else None
+    code, detail = mb.mhla_device_status()
+    if code != 0:
+        raise RuntimeError(f"device status {code} in timed region (detail {detail})")
+
+    phase_ms = {ph: [] for ph in PHASES}
+    for evs in ev_sets:
+        for j, ph in enumerate(PHASES):
+            phase_ms[ph].append(evs[j].elapsed_time(evs[j + 1]))
+    step_ms = [evs[0].elapsed_time(evs[-1]) for evs in ev_sets]
+    if flush is None:
+        total_ms = start.elapsed_time(end)
+    else:
+        total_ms = sum(step_ms)
+    local_ms = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+    if dist is not None:
+        dist.all_reduce(local_ms, op=dist.ReduceOp.MAX)
+    max_ms = float(local_ms.item())
+    ms_per_step = max_ms / K
+    units_tokens = w.units * w.n_tokens
+    value = world * units_tokens * K / (max_ms / 1e3)
+
+    hbm, tf_burst, tf_sust, peak_kind = load_peaks()
+    pbytes = phase_bytes(w, info, info.variant)
+    avg_phase = {ph: statistics.mean(v) for ph, v in phase_ms.items()}
+    dom = max(avg_phase, key=avg_phase.get)
+    achieved = pbytes[dom] / (avg_phase[dom] / 1e3) / 1e9
+    kname, ksrc = PHASE_KERNEL.get(info.variant, {}).get(dom, (dom, None))
+    traffic = None
+    tt = traffic_table().get((kname, w.name))
+    if tt and ksrc and tt[1] == source_hash(ksrc):
+        traffic = tt[0]
+    roof_bytes = wl.roofline_bytes(w)
+    roof_flops = wl.roofline_flops(w)
+    t_hbm = roof_bytes / (hbm * 1e9)
+    t_tc = roof_flops / (tf_sust * 1e12)
+    t_roof = max(t_hbm, t_tc)
+
+    result = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": w.dtype, "data": "synthetic (seeded normals, locality-biased Mc; no dataset, no weights)",
+        "config": dict(wl.describe(w), variant=mb.mhla_plan(p).variant,
+                       variant_name={1: "simt", 2: "multipass"}.get(info.variant, str(info.variant)),
+                       l2="no flush: inputs exceed L2" if flush is None else "L2 flushed (256 MB write) between steps, outside per-step events",
+                       parallelism=f"replicas{world}" if world > 1 else "single GPU"),
+        "roofline": {"bound": "hbm", "kernel": kname, "phase": dom, "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "traffic": traffic, "peak_source": peak_kind,
+                     "algorithmic_bytes_per_launch": pbytes[dom], "avg_launch_ms": avg_phase[dom]},
+        "path_roofline": {"bytes": roof_bytes, "flops": roof_flops, "t_hbm_us": t_hbm * 1e6, "t_tc_us": t_tc * 1e6,
+                          "bound": "hbm" if t_hbm >= t_tc else "tensor", "frac": t_roof / (ms_per_step / 1e3),
+                          "peak_hbm_gbs": hbm, "peak_bf16_tflops_sustained": tf_sust, "peak_source": peak_kind},
+        "phase_ms": avg_phase,
+        "gpu_launches": info.kernels_per_call * K,
+        "clocks": clocks,
+    }
+    return result, (q, k, v, mc, out, p, info, stream)
+
+
+def run_e2e(w: wl.Workload, state, steps: int):
+    """Same metric through mhla_forward_host: pinned host inputs copied in,
+    result copied out, every step."""
+    import torch
+    import token_level_head_phi_gb300.binding as mb
+    q, k, v, mc, out, p, info, stream = state
+    hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
+    hmc = mc.cpu().pin_memory()
+    hout = torch.empty_like(hq).pin_memory()
+    need = mb.mhla_host_buffer_bytes(p)
+    del q, k, v, out
+    torch.cuda.empty_cache()
+    buf = torch.empty(need, dtype=torch.uint8, device=mc.device)
+    lib = mb.load()
+    import ctypes
+
+    def step():
+        st = lib.mhla_forward_host(hq.data_ptr(), hk.data_ptr(), hv.data_ptr(), hmc.data_ptr(), ctypes.byref(p),
+                                   hout.data_ptr(), buf.data_ptr(), need, stream.cuda_stream)
+        if st != 0:
+            raise mb.MhlaError(st, "mhla_forward_host")
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    t1 = time.perf_counter()
+    io = hq.numel() * hq.element_size()
+    return {"value": w.units * w.n_tokens * steps / (t1 - t0), "unit": UNIT,
+            "h2d_bytes_per_step": 3 * io + hmc.numel() * 4, "d2h_bytes_per_step": io,
+            "steps": steps, "ms_per_step": (t1 - t0) * 1e3 / steps}
+
+
+# ------------------------------------------------------ oracle baseline
+
+ORACLE_SNIPPET = r"""
+import json, sys, time
+sys.path.insert(0, {root!r})
+from token_level_head_phi_gb300 import workloads as wl
+from oracle import mhla_oracle as orc
+w = wl.WORKLOADS[{name!r}]
+mc = wl.make_mc(w)
+budget, max_units, per_step = {budget}, {max_units}, {per_step}
+times = []
+units = 0
+t_all = time.perf_counter()
+for step in range(max_units):
+    u = step % w.units
+    q, k, v = wl.head_inputs(w, u)
+    t0 = time.perf_counter()
+    orc.mhla_head64(q, k, v, mc, w.grid, w.block, orc.ELU1, w.norm)
+    times.append(time.perf_counter() - t0)
+    units += 1
+    if not per_step and sum(times) >= budget:
+        break
+print(json.dumps({{"times": times, "units": units}}))
+"""
+
+
+def oracle_run(w: wl.Workload, budget_s: float, max_units: int, per_step: bool):
+    """Runs the oracle in a fresh process (BLAS threads = available cores)."""
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    env = dict(os.environ)
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[var] = str(cores)
+    code = ORACLE_SNIPPET.format(root=ROOT, name=w.name, budget=budget_s, max_units=max_units, per_step=per_step)
+    res = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=1800)
+    if res.returncode != 0:
+        raise RuntimeError(f"oracle run failed: {res.stderr[-2000:]}")
+    d = json.loads(res.stdout.strip().splitlines()[-1])
+    return d["times"], d["units"], cores
+
+
+def cpu_baseline(w: wl.Workload, budget_s: float = 15.0):
+    times, units, cores = oracle_run(w, budget_s, max_units=10 ** 6, per_step=False)
+    total = sum(times)
+    return {"value": units * w.n_tokens / total, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{units} of {w.units} (batch, head) units of {w.name}, float64 NumPy oracle, "
+                      f"{total:.1f} s of CPU time; input generation excluded"}
+
+
+def run_reference(args, w: wl.Workload):
+    """--impl reference: the float64 oracle, each step one (batch, head) unit."""
+    K, W = args.steps, args.warmup
+    times, units, cores = oracle_run(w, 0.0, max_units=W + K, per_step=True)
+    timed = times[W:W + K]
+    total = sum(timed)
+    value = K * w.n_tokens / total
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": K,
+        "warmup": W, "ms_per_step": total * 1e3 / K, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded normals, locality-biased Mc)",
+        "config": dict(wl.describe(w), parallelism="host cores"),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"each step one (batch, head) unit of {w.name} ({w.n_tokens} tokens)"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=wl.BENCH_WORKLOAD, choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--variant", default="auto", choices=["auto", "simt", "multipass"])
+    ap.add_argument("--impl", default="mine", choices=["mine", "reference"])
+    ap.add_argument("--all-workloads", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world, rank, local = dist_env()
+    w = wl.WORKLOADS[args.workload]
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, w)), flush=True)
+        return
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist_mod
+        dist_mod.init_process_group("nccl")
+        dist = dist_mod
+    import torch
+    result, state = run_mine(args, w, world, rank, local, dist)
+    result["e2e"] = run_e2e(w, state, args.e2e_steps)
+    del state
+    torch.cuda.empty_cache()
+    if args.all_workloads:
+        extra = {}
+        for name in sorted(wl.WORKLOADS):
+            if name == w.name or wl.WORKLOADS[name].head_dim != 64 and args.variant == "multipass":
+                continue
+            sub = argparse.Namespace(**vars(args))
+            sub.steps = max(10, min(args.steps, 50))
+            r, st = run_mine(sub, wl.WORKLOADS[name], world, rank, local, dist)
+            del st
+            torch.cuda.empty_cache()
+            extra[name] = {k: r[k] for k in ("value", "ms_per_step", "phase_ms", "path_roofline", "roofline")}
+            extra[name]["config"] = r["config"]
+        result["workloads"] = extra
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(w)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

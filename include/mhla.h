@@ -1,0 +1,177 @@
+/*
+ * mhla.h -- C ABI of libmhla.so: the forward pass of token-level multi-head
+ * linear attention (MHLA) on one NVIDIA GB300 (sm_103a).
+ *
+ * The operation ("MHLA: Restoring Expressivity of Linear Attention via
+ * Token-Level Multi-Head", overall framework, flowchart and key design 2):
+ *   phi(x) = ELU(x) + 1 applied to Q and K;
+ *   the N tokens of a (T, Hg, Wg) grid are split into M non-overlapping
+ *   (bt, bh, bw) blocks; for every block b
+ *       S_b = sum_{j in b} phi(K_j) V_j^T   (d x d)
+ *       z_b = sum_{j in b} phi(K_j)         (d)
+ *   the summaries are mixed per query block i with a coefficient matrix Mc:
+ *       S~_i = sum_b Mc[i,b] S_b,   z~_i = sum_b Mc[i,b] z_b
+ *   and every query q in block i produces
+ *       DIVISIVE: o = phi(q)^T S~_i / phi(q)^T z~_i
+ *       NONE:     o = phi(q)^T S~_i          (normaliser dropped, key design 2)
+ *       MALA:     s = phi(q)^T z~_i, beta = 1 + 1/s, gamma = s / n~_i,
+ *                 o = beta phi(q)^T S~_i - gamma v~_i
+ *   where v~_i = sum_b Mc[i,b] sum_{j in b} V_j and n~_i = sum_b Mc[i,b] |b|
+ *   ("Rectifying Magnitude Neglect in Linear Attention", key designs: the
+ *   linear form of MALA, with each global sum replaced by its mixed
+ *   counterpart; at M = 1 and Mc = [[1]] it is that page's formula).
+ *
+ * Conventions shared by every call:
+ *   - Q, K, V and out are contiguous [B, H, N, d] arrays, d innermost, tokens
+ *     in raster order of the grid: t = (tau * Hg + y) * Wg + x.
+ *   - Blocks are numbered in raster order of the block grid
+ *     (T/bt, Hg/bh, Wg/bw); Mc is a float32 [M, M] row-major array whose row
+ *     is the query block and whose column is the summary block.  One Mc is
+ *     shared by all batches and heads.
+ *   - dtype BF16: Q, K, V, out hold bf16 values; F32: float32.
+ *   - Pointers passed to mhla_forward are device pointers owned by the
+ *     caller; the library never frees them and keeps none of them after the
+ *     call returns.  Q, K, V and out must be 16-byte aligned, the workspace
+ *     256-byte aligned, Mc 4-byte aligned.
+ *   - The stream argument is a cudaStream_t (NULL = legacy default stream).
+ *     Work is enqueued asynchronously; no call synchronises the host unless
+ *     its comment says so.
+ *   - Every argument is checked on the host before anything is enqueued.  An
+ *     invalid argument returns an error status and enqueues nothing.  No
+ *     kernel traps.  A kernel whose bounded wait on the device expires stops
+ *     early and records MHLA_ERR_DEVICE_TIMEOUT, which mhla_device_status
+ *     reports; the output of that call is then undefined.
+ *   - The library keeps per-device state (cached tensor-map encoder, device
+ *     error word); calls from several host threads on the same device are
+ *     safe except mhla_set_phase_events, which is process-wide.
+ */
+#ifndef MHLA_H_
+#define MHLA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MHLA_ABI_VERSION 1
+
+typedef enum mhla_status {
+  MHLA_OK = 0,
+  MHLA_ERR_INVALID_ARG = 1,     /* bad pointer, shape, enum or alignment      */
+  MHLA_ERR_UNSUPPORTED = 2,     /* valid request this build cannot run        */
+  MHLA_ERR_WORKSPACE = 3,       /* workspace missing or smaller than required */
+  MHLA_ERR_CUDA = 4,            /* a CUDA runtime call failed                  */
+  MHLA_ERR_DEVICE_TIMEOUT = 5   /* a kernel's bounded wait expired             */
+} mhla_status;
+
+typedef enum mhla_dtype { MHLA_DTYPE_BF16 = 0, MHLA_DTYPE_F32 = 1 } mhla_dtype;
+
+/* ELU1: phi(x) = x + 1 (x > 0), exp(x) (x <= 0).  IDENTITY: phi(x) = x; for
+ * tests only, the caller keeps the features positive. */
+typedef enum mhla_feature_map { MHLA_FEATURE_ELU1 = 0, MHLA_FEATURE_IDENTITY = 1 } mhla_feature_map;
+
+typedef enum mhla_norm { MHLA_NORM_DIVISIVE = 0, MHLA_NORM_MALA = 1, MHLA_NORM_NONE = 2 } mhla_norm;
+
+/* AUTO picks MULTIPASS for bf16 with d = 64, SIMT otherwise.
+ * SIMT:      CUDA-core kernels, float32 arithmetic, any supported d, both dtypes.
+ * MULTIPASS: tcgen05/TMEM tensor-core kernels fed by TMA (bf16, d = 64):
+ *            block summaries -> mixing GEMM -> output with fused epilogue. */
+typedef enum mhla_variant {
+  MHLA_VARIANT_AUTO = 0,
+  MHLA_VARIANT_SIMT = 1,
+  MHLA_VARIANT_MULTIPASS = 2
+} mhla_variant;
+
+typedef struct mhla_params {
+  int batch;        /* B >= 0                                              */
+  int heads;        /* H >= 0                                              */
+  int head_dim;     /* d in {16, 32, 64, 128}                              */
+  int grid[3];      /* (T, Hg, Wg) token grid, each >= 1; 1D = (1, 1, N)   */
+  int block[3];     /* (bt, bh, bw), each >= 1 and dividing grid[i]        */
+  int dtype;        /* mhla_dtype                                          */
+  int feature_map;  /* mhla_feature_map                                    */
+  int norm;         /* mhla_norm                                           */
+  int variant;      /* mhla_variant                                        */
+} mhla_params;
+
+/* What a call with these parameters will run (for tests and benchmarks). */
+typedef struct mhla_plan_info {
+  int n_tokens;          /* N                                              */
+  int n_blocks;          /* M                                              */
+  int block_tokens;      /* n_b = bt * bh * bw                             */
+  int variant;           /* the variant AUTO resolved to                   */
+  int kernels_per_call;  /* kernel launches one mhla_forward enqueues     */
+  int summary_splits;    /* partial summaries per block (long blocks)      */
+  size_t workspace_bytes;
+} mhla_plan_info;
+
+/* Validates p and fills *info.  Returns MHLA_ERR_INVALID_ARG or
+ * MHLA_ERR_UNSUPPORTED for parameters mhla_forward would reject. */
+mhla_status mhla_plan(const mhla_params* p, mhla_plan_info* info);
+
+/* Device workspace mhla_forward needs for p, in bytes (0 for an empty
+ * problem).  Returns the same errors as mhla_plan. */
+mhla_status mhla_workspace_bytes(const mhla_params* p, size_t* bytes);
+
+/* The MHLA forward pass (see the top of this file).
+ *   q, k, v     device [B, H, N, d] inputs (dtype p->dtype)
+ *   mc          device float32 [M, M] mixing coefficients
+ *   out         device [B, H, N, d] output (dtype p->dtype); must not alias
+ *               q, k, v, mc or the workspace
+ *   workspace   device scratch of at least mhla_workspace_bytes(p) bytes, or
+ *               NULL with workspace_bytes == 0, in which case the library
+ *               takes stream-ordered memory (cudaMallocAsync) on `stream` and
+ *               returns it (cudaFreeAsync) on the same stream
+ *   stream      cudaStream_t the kernels are enqueued on
+ * B * H * N == 0 is a no-op that returns MHLA_OK.  Non-positive Mc rows or
+ * features make the divisive and MALA denominators reach zero; IEEE inf/NaN
+ * then propagate (the pages put no epsilon in them). */
+mhla_status mhla_forward(const void* q, const void* k, const void* v, const float* mc,
+                         const mhla_params* p, void* out, void* workspace,
+                         size_t workspace_bytes, void* stream);
+
+/* Device buffer mhla_forward_host needs: room for Q, K, V, Mc, out and the
+ * workspace, each 256-byte aligned. */
+mhla_status mhla_host_buffer_bytes(const mhla_params* p, size_t* bytes);
+
+/* End-to-end call on HOST arrays: enqueues the host-to-device copies of
+ * q, k, v, mc into dev_buffer, the forward pass, and the device-to-host copy
+ * of the result into out (all on `stream`), then synchronises `stream` and
+ * returns.  Host arrays have the layouts of mhla_forward; page-locked host
+ * memory makes the copies asynchronous DMA transfers.  dev_buffer is a
+ * device allocation of at least mhla_host_buffer_bytes(p) bytes. */
+mhla_status mhla_forward_host(const void* q, const void* k, const void* v, const float* mc,
+                              const mhla_params* p, void* out, void* dev_buffer,
+                              size_t dev_buffer_bytes, void* stream);
+
+/* Reads and clears the device error word of the current device.  Blocks the
+ * host until the device is idle.  *code receives MHLA_OK or the status a
+ * kernel recorded (MHLA_ERR_DEVICE_TIMEOUT); *detail receives a kernel-
+ * specific location code (0 if none).  Either pointer may be NULL. */
+mhla_status mhla_device_status(int* code, int* detail);
+
+/* Timing hook.  With n == MHLA_NUM_PHASE_EVENTS, each later mhla_forward
+ * records events[0] before its first kernel and events[i] after phase i
+ * (1: block summaries, 2: mixing, 3: output) on its stream; phases a
+ * variant does not have record at the same point as the previous one.
+ * events are cudaEvent_t handles owned by the caller.  n == 0 turns the hook
+ * off.  Process-wide; not meant for concurrent callers. */
+#define MHLA_NUM_PHASE_EVENTS 4
+mhla_status mhla_set_phase_events(void* const* events, int n);
+
+/* Static description of a status code; never NULL. */
+const char* mhla_status_string(mhla_status s);
+
+/* Text of the last CUDA error this thread saw inside the library ("" if none). */
+const char* mhla_last_error_string(void);
+
+/* MHLA_ABI_VERSION of the loaded library. */
+int mhla_abi_version(void);
+
+#ifdef __cplusplus
+}  /* extern "C" */
+#endif
+
+#endif  /* MHLA_H_ */

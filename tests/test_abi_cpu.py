@@ -1,0 +1,169 @@
+"""CPU checks of the C ABI: the library builds, loads, exports every symbol
+include/mhla.h declares, and validates arguments on the host before touching
+the device.  No call here reaches a CUDA runtime function."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from token_level_head_phi_gb300 import binding as mb
+from token_level_head_phi_gb300 import build as mbuild
+from token_level_head_phi_gb300 import workloads as wl
+
+HEADER = os.path.join(mbuild.INCLUDE, "mhla.h")
+
+
+@pytest.fixture(scope="session")
+def lib():
+    mbuild.build()
+    return mb.load()
+
+
+def header_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mhla_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_entry_points():
+    names = header_functions()
+    assert "mhla_forward" in names and "mhla_workspace_bytes" in names
+    assert len(names) >= 10
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in header_functions():
+        assert hasattr(lib, name), f"{name} missing from libmhla.so"
+
+
+def test_binding_declares_every_header_function():
+    bound = {s[0] for s in mb.SIGNATURES}
+    assert set(header_functions()) == bound
+
+
+def test_abi_version_and_strings(lib):
+    assert mb.mhla_abi_version() == 1
+    for s in range(6):
+        assert mb.mhla_status_string(s).startswith("MHLA")
+    assert "unknown" in mb.mhla_status_string(42)
+
+
+def _params(w, **kw):
+    opts = dict(dtype=w.dtype, norm=w.norm)
+    opts.update(kw)
+    return mb.make_params(w.batch, w.heads, w.head_dim, w.grid, w.block, **opts)
+
+
+@pytest.mark.parametrize("name", sorted(wl.WORKLOADS))
+def test_plan_matches_workload(lib, name):
+    w = wl.WORKLOADS[name]
+    info = mb.mhla_plan(_params(w, variant="simt"))
+    assert info.n_tokens == w.n_tokens
+    assert info.n_blocks == w.n_blocks
+    assert info.block_tokens == w.block_tokens
+    assert info.variant == mb.VARIANT_SIMT
+    assert info.kernels_per_call >= 1
+    d, R = w.head_dim, w.head_dim ** 2 + 2 * w.head_dim
+    stack = 4 * w.units * w.n_blocks * info.summary_splits * R
+    mixed = 4 * w.units * w.n_blocks * R
+    assert info.workspace_bytes >= stack + mixed
+    assert mb.mhla_workspace_bytes(_params(w, variant="simt")) == info.workspace_bytes
+
+
+BAD = [
+    dict(head_dim=48),
+    dict(head_dim=0),
+    dict(grid=(1, 15, 14)),      # 15 not divisible by 7
+    dict(block=(1, 0, 7)),
+    dict(grid=(0, 14, 14)),
+    dict(batch=-1),
+    dict(dtype=7),
+    dict(feature_map=3),
+    dict(norm=9),
+    dict(variant=11),
+]
+
+
+@pytest.mark.parametrize("bad", BAD)
+def test_invalid_params_rejected(lib, bad):
+    w = wl.WORKLOADS["deit_t"]
+    args = dict(batch=w.batch, heads=w.heads, head_dim=w.head_dim, grid=w.grid, block=w.block)
+    opts = dict(dtype=w.dtype, norm="divisive", feature_map="elu1", variant="auto")
+    for k, v in bad.items():
+        (args if k in args else opts)[k] = v
+    p = mb.make_params(args["batch"], args["heads"], args["head_dim"], args["grid"], args["block"], **opts)
+    info = mb.MhlaPlanInfo()
+    assert lib.mhla_plan(ctypes.byref(p), ctypes.byref(info)) == mb.MHLA_ERR_INVALID_ARG
+    n = ctypes.c_size_t(0)
+    assert lib.mhla_workspace_bytes(ctypes.byref(p), ctypes.byref(n)) == mb.MHLA_ERR_INVALID_ARG
+    # forward rejects the same parameters before looking at any pointer
+    assert lib.mhla_forward(None, None, None, None, ctypes.byref(p), None, None, 0, None) == \
+        mb.MHLA_ERR_INVALID_ARG
+
+
+def test_null_params_rejected(lib):
+    assert lib.mhla_forward(None, None, None, None, None, None, None, 0, None) == mb.MHLA_ERR_INVALID_ARG
+    assert lib.mhla_workspace_bytes(None, None) == mb.MHLA_ERR_INVALID_ARG
+
+
+def test_empty_problem_is_noop(lib):
+    w = wl.WORKLOADS["deit_t"]
+    for batch, heads in ((0, 3), (4, 0)):
+        p = mb.make_params(batch, heads, 64, w.grid, w.block)
+        assert mb.mhla_workspace_bytes(p) == 0
+        assert lib.mhla_forward(None, None, None, None, ctypes.byref(p), None, None, 0, None) == mb.MHLA_OK
+
+
+FAKE = 1 << 40  # never dereferenced: validation fails first
+
+
+def test_pointer_checks(lib):
+    w = wl.WORKLOADS["deit_t"]
+    p = _params(w)
+    io = w.units * w.n_tokens * w.head_dim * 2
+    q, k, v, mc, out, ws = FAKE, FAKE + 2 * io, FAKE + 4 * io, FAKE + 6 * io, FAKE + 8 * io, FAKE + 10 * io
+    need = mb.mhla_workspace_bytes(p)
+    f = lib.mhla_forward
+    # null pointers
+    assert f(None, k, v, mc, ctypes.byref(p), out, ws, need, None) == mb.MHLA_ERR_INVALID_ARG
+    assert f(q, k, v, None, ctypes.byref(p), out, ws, need, None) == mb.MHLA_ERR_INVALID_ARG
+    assert f(q, k, v, mc, ctypes.byref(p), None, ws, need, None) == mb.MHLA_ERR_INVALID_ARG
+    # misaligned tensors / workspace
+    assert f(q + 2, k, v, mc, ctypes.byref(p), out, ws, need, None) == mb.MHLA_ERR_INVALID_ARG
+    assert f(q, k, v, mc + 2, ctypes.byref(p), out, ws, need, None) == mb.MHLA_ERR_INVALID_ARG
+    assert f(q, k, v, mc, ctypes.byref(p), out + 8, ws, need, None) == mb.MHLA_ERR_INVALID_ARG
+    assert f(q, k, v, mc, ctypes.byref(p), out, ws + 16, need, None) == mb.MHLA_ERR_INVALID_ARG
+    # output aliasing an input
+    assert f(q, k, v, mc, ctypes.byref(p), q + 256, ws, need, None) == mb.MHLA_ERR_INVALID_ARG
+    # workspace too small, or sized but null
+    assert f(q, k, v, mc, ctypes.byref(p), out, ws, need - 1, None) == mb.MHLA_ERR_WORKSPACE
+    assert f(q, k, v, mc, ctypes.byref(p), out, None, need, None) == mb.MHLA_ERR_INVALID_ARG
+
+
+def test_host_entry_checks(lib):
+    w = wl.WORKLOADS["tiny_f32"]
+    p = _params(w)
+    need = mb.mhla_host_buffer_bytes(p)
+    io = w.units * w.n_tokens * w.head_dim * 4
+    assert need >= 4 * io + mb.mhla_workspace_bytes(p)
+    h = ctypes.create_string_buffer(io)
+    f = lib.mhla_forward_host
+    assert f(h, h, h, h, ctypes.byref(p), h, None, need, None) == mb.MHLA_ERR_INVALID_ARG
+    assert f(h, h, h, h, ctypes.byref(p), h, FAKE, need - 1, None) == mb.MHLA_ERR_WORKSPACE
+
+
+def test_phase_event_hook_checks(lib):
+    assert lib.mhla_set_phase_events(None, 0) == mb.MHLA_OK
+    assert lib.mhla_set_phase_events(None, mb.NUM_PHASE_EVENTS) == mb.MHLA_ERR_INVALID_ARG
+    arr = (ctypes.c_void_p * 3)(1, 2, 3)
+    assert lib.mhla_set_phase_events(arr, 3) == mb.MHLA_ERR_INVALID_ARG
+    arr = (ctypes.c_void_p * 4)(1, 2, None, 3)
+    assert lib.mhla_set_phase_events(arr, 4) == mb.MHLA_ERR_INVALID_ARG
+
+
+def test_long_blocks_are_split(lib):
+    w = wl.WORKLOADS["seq_32k_m1"]
+    info = mb.mhla_plan(_params(w, variant="simt"))
+    assert info.n_blocks == 1 and info.summary_splits > 1

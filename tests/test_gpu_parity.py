@@ -1,0 +1,172 @@
+"""GPU parity: the CUDA path (through the C ABI) against the float64 oracle.
+
+Measure: max|gpu - oracle| / max|oracle| per (batch, head) unit, at most 5e-3
+for bf16 inputs/outputs with float32 accumulation and 1e-5 in float32 mode.
+Full-size workloads compare every unit the oracle finishes in seconds and a
+sample of units otherwise; edge cases cover ragged blocks, every head
+dimension, a single block, Mc rows with zeros, non-square and 3D grids, every
+norm and both feature maps.
+"""
+
+import zlib
+
+import numpy as np
+import pytest
+
+from oracle import mhla_oracle as orc
+from token_level_head_phi_gb300 import binding as mb
+from token_level_head_phi_gb300 import workloads as wl
+
+from helpers import TOL, download, parity, run_gpu, upload
+
+pytestmark = pytest.mark.gpu
+
+VARIANTS = ["simt"]
+
+FULL = {  # workload -> units the oracle checks (None = all)
+    "tiny_f32": None,
+    "deit_t": None,
+    "image_64x64": None,
+    "video_16x64x64": [0, 17, 31],
+    "seq_32k": [0, 33, 63],
+    "seq_32k_mala": [0, 63],
+    "seq_32k_m1": [0, 40],
+    "seq_32k_m1_mala": [1, 62],
+}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from token_level_head_phi_gb300 import build
+    build.build()
+    mb.load()
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("name", list(FULL))
+def test_workload_parity(name, variant):
+    w = wl.WORKLOADS[name]
+    err = parity(w, w.norm, variant, units=FULL[name])
+    assert err <= TOL[w.dtype], f"{name}/{variant}: rel err {err:.3e}"
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("norm", ["divisive", "none", "mala"])
+@pytest.mark.parametrize("name", ["tiny_f32", "deit_t"])
+def test_norms(name, norm, variant):
+    w = wl.WORKLOADS[name]
+    err = parity(w, norm, variant, units=[0, w.units - 1])
+    assert err <= TOL[w.dtype], f"{name}/{norm}/{variant}: rel err {err:.3e}"
+
+
+EDGE = [
+    # grid, block, d, dtype, batch, heads
+    ((1, 14, 14), (1, 7, 7), 64, "bf16", 1, 2),        # ragged 49-token blocks
+    ((1, 10, 12), (1, 5, 4), 32, "f32", 2, 1),         # non-square blocks, d=32
+    ((3, 8, 8), (3, 4, 8), 16, "f32", 1, 3),           # 3D, bt = T, d=16
+    ((4, 6, 10), (2, 3, 5), 128, "bf16", 1, 1),        # 3D ragged, d=128
+    ((1, 1, 1000), (1, 1, 1000), 64, "bf16", 2, 2),    # one block, N not a multiple of 64
+    ((1, 1, 3000), (1, 1, 1500), 64, "f32", 1, 1),     # two long blocks split into pieces
+    ((1, 1, 4100), (1, 1, 41), 64, "bf16", 1, 1),      # M=100 odd blocks
+    ((1, 9, 1), (1, 3, 1), 64, "bf16", 1, 1),          # column grid
+    ((2, 2, 2), (1, 1, 1), 16, "f32", 1, 1),           # one token per block
+]
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("norm", ["divisive", "mala"])
+@pytest.mark.parametrize("case", EDGE, ids=lambda c: f"{c[0]}-{c[1]}-d{c[2]}-{c[3]}")
+def test_edge_shapes(case, norm, variant):
+    grid, block, d, dtype, batch, heads = case
+    w = wl.random_small(zlib.crc32(repr(case).encode()) % 10000, grid, block, d, batch, heads, dtype)
+    err = parity(w, norm, variant)
+    assert err <= TOL[dtype], f"{case}/{norm}: rel err {err:.3e}"
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_mc_with_zero_entries(variant):
+    w = wl.random_small(5, (1, 16, 16), (1, 4, 4), 64, 2, 2, "bf16")
+    M = w.n_blocks
+    rng = np.random.default_rng(3)
+    mc = rng.uniform(0, 1, (M, M)) * (rng.uniform(0, 1, (M, M)) < 0.3)
+    np.fill_diagonal(mc, 1.0)
+    mc = (mc / mc.sum(1, keepdims=True)).astype(np.float32)
+    for norm in ("divisive", "mala", "none"):
+        err = parity(w, norm, variant, mc=mc)
+        assert err <= TOL["bf16"], f"{norm}: {err:.3e}"
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_linear_decay_mc_and_identity_map(variant):
+    w = wl.random_small(8, (1, 12, 12), (1, 4, 4), 64, 1, 2, "f32", mc="linear_decay")
+    vals, dev = wl.all_inputs(w)
+    vals = [np.abs(a) + 0.1 for a in vals]  # positive features for phi(x) = x
+    dev = [a.astype(np.float32) for a in vals]
+    err = parity(w, "divisive", variant, fmap="identity", inputs=(vals, dev))
+    assert err <= TOL["f32"]
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_output_guard_regions_untouched(variant):
+    torch = pytest.importorskip("torch")
+    w = wl.random_small(9, (1, 14, 14), (1, 7, 7), 64, 2, 3, "bf16")
+    vals, dev = wl.all_inputs(w)
+    tensors = upload(w, dev)
+    n = w.units * w.n_tokens * w.head_dim
+    pad = 4096
+    big = torch.full((n + 2 * pad,), 12345.0, dtype=torch.bfloat16, device="cuda")
+    out = big[pad:pad + n].view(w.batch, w.heads, w.n_tokens, w.head_dim)
+    run_gpu(w, tensors, wl.make_mc(w), "divisive", variant, out=out)
+    assert torch.all(big[:pad] == 12345.0) and torch.all(big[pad + n:] == 12345.0)
+    o = download(out).reshape(w.units, w.n_tokens, w.head_dim)
+    mc = wl.make_mc(w)
+    for u in range(w.units):
+        b, h = divmod(u, w.heads)
+        want = orc.mhla_head64(vals[0][b, h], vals[1][b, h], vals[2][b, h], mc, w.grid, w.block)
+        assert orc.relative_max_error(o[u], want) <= TOL["bf16"]
+
+
+def test_host_entry_matches_device_entry():
+    torch = pytest.importorskip("torch")
+    w = wl.WORKLOADS["deit_t"]
+    vals, dev = wl.all_inputs(w)
+    mc = wl.make_mc(w)
+    tensors = upload(w, dev)
+    d_out = download(run_gpu(w, tensors, mc, "divisive"))
+    host = [torch.from_numpy(a).view(torch.bfloat16).pin_memory() for a in dev]
+    h_out = torch.empty_like(host[0]).pin_memory()
+    mb.mhla_forward_host(*host, torch.from_numpy(mc), w.grid, w.block, out=h_out)
+    np.testing.assert_array_equal(download(h_out), d_out)
+
+
+def test_workspace_allocated_by_library():
+    torch = pytest.importorskip("torch")
+    import ctypes
+    w = wl.WORKLOADS["tiny_f32"]
+    vals, dev = wl.all_inputs(w)
+    q, k, v = upload(w, dev)
+    mc = torch.from_numpy(wl.make_mc(w)).cuda()
+    out = torch.empty_like(q)
+    p = mb.make_params(w.batch, w.heads, w.head_dim, w.grid, w.block, "f32")
+    st = mb.mhla_forward_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), mc.data_ptr(), p, out.data_ptr(), 0, 0,
+                             torch.cuda.current_stream().cuda_stream)
+    assert st == mb.MHLA_OK
+    torch.cuda.synchronize()
+    want = orc.mhla_head64(vals[0][0, 0], vals[1][0, 0], vals[2][0, 0], wl.make_mc(w), w.grid, w.block)
+    assert orc.relative_max_error(download(out)[0, 0], want) <= TOL["f32"]
+    del ctypes
+
+
+def test_phase_events_recorded():
+    torch = pytest.importorskip("torch")
+    w = wl.WORKLOADS["image_64x64"]
+    vals, dev = wl.all_inputs(w)
+    tensors = upload(w, dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(mb.NUM_PHASE_EVENTS)]
+    mb.mhla_set_phase_events(ev)
+    try:
+        run_gpu(w, tensors, wl.make_mc(w), "divisive")
+    finally:
+        mb.mhla_set_phase_events(None)
+    times = [ev[0].elapsed_time(ev[i]) for i in range(1, mb.NUM_PHASE_EVENTS)]
+    assert all(t >= 0 for t in times) and times == sorted(times)

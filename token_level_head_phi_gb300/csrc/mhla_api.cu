@@ -1,0 +1,323 @@
+// C ABI of libmhla.so (declared in include/mhla.h): argument validation,
+// planning, workspace layout and dispatch to the kernels.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "mhla.h"
+#include "plan.h"
+
+namespace mhla {
+namespace {
+
+thread_local std::string g_last_error;
+
+std::mutex g_events_mu;
+cudaEvent_t g_events[MHLA_NUM_PHASE_EVENTS];
+int g_num_events = 0;
+
+// Device error word: [0] status code, [1] location detail.  Kernels with
+// bounded waits write it when a wait expires.
+__device__ unsigned int g_device_error[2];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_err_mu;
+unsigned int* g_err_ptr[kMaxDevices] = {};
+
+constexpr size_t kAlign = 256;
+constexpr int kSimtSplitLen = 1024;
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+mhla_status cuda_fail(cudaError_t e) {
+  g_last_error = cudaGetErrorString(e);
+  return MHLA_ERR_CUDA;
+}
+
+size_t elem_bytes(int dtype) { return dtype == MHLA_DTYPE_BF16 ? 2 : 4; }
+
+mhla_status device_error_ptr(unsigned int** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= kMaxDevices) return MHLA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_err_mu);
+  if (!g_err_ptr[dev]) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_device_error);
+    if (e != cudaSuccess) return cuda_fail(e);
+    g_err_ptr[dev] = static_cast<unsigned int*>(ptr);
+  }
+  *out = g_err_ptr[dev];
+  return MHLA_OK;
+}
+
+// Shape and option checks; fills the plan without touching the device.
+mhla_status make_plan(const mhla_params* prm, Plan* p) {
+  if (!prm || !p) return MHLA_ERR_INVALID_ARG;
+  std::memset(p, 0, sizeof(*p));
+  const int d = prm->head_dim;
+  if (prm->batch < 0 || prm->heads < 0) return MHLA_ERR_INVALID_ARG;
+  if (d != 16 && d != 32 && d != 64 && d != 128) return MHLA_ERR_INVALID_ARG;
+  for (int i = 0; i < 3; ++i) {
+    if (prm->grid[i] < 1 || prm->block[i] < 1) return MHLA_ERR_INVALID_ARG;
+    if (prm->grid[i] % prm->block[i] != 0) return MHLA_ERR_INVALID_ARG;
+  }
+  if (prm->dtype != MHLA_DTYPE_BF16 && prm->dtype != MHLA_DTYPE_F32) return MHLA_ERR_INVALID_ARG;
+  if (prm->feature_map != MHLA_FEATURE_ELU1 && prm->feature_map != MHLA_FEATURE_IDENTITY)
+    return MHLA_ERR_INVALID_ARG;
+  if (prm->norm != MHLA_NORM_DIVISIVE && prm->norm != MHLA_NORM_MALA && prm->norm != MHLA_NORM_NONE)
+    return MHLA_ERR_INVALID_ARG;
+  if (prm->variant != MHLA_VARIANT_AUTO && prm->variant != MHLA_VARIANT_SIMT &&
+      prm->variant != MHLA_VARIANT_MULTIPASS)
+    return MHLA_ERR_INVALID_ARG;
+
+  const int64_t N64 = (int64_t)prm->grid[0] * prm->grid[1] * prm->grid[2];
+  const int64_t BH64 = (int64_t)prm->batch * prm->heads;
+  if (N64 > (1LL << 30) || BH64 > 65535) return MHLA_ERR_UNSUPPORTED;
+  if (BH64 * N64 * d > (1LL << 40)) return MHLA_ERR_UNSUPPORTED;
+
+  p->B = prm->batch;
+  p->H = prm->heads;
+  p->BH = (int)BH64;
+  p->d = d;
+  p->T = prm->grid[0];
+  p->Hg = prm->grid[1];
+  p->Wg = prm->grid[2];
+  p->bt = prm->block[0];
+  p->bh = prm->block[1];
+  p->bw = prm->block[2];
+  p->Mt = p->T / p->bt;
+  p->Mh = p->Hg / p->bh;
+  p->Mw = p->Wg / p->bw;
+  p->N = (int)N64;
+  const int64_t M64 = (int64_t)p->Mt * p->Mh * p->Mw;
+  if (M64 > 65536) return MHLA_ERR_UNSUPPORTED;
+  p->M = (int)M64;
+  p->nb = p->bt * p->bh * p->bw;
+  p->dtype = prm->dtype;
+  p->fmap = prm->feature_map;
+  p->norm = prm->norm;
+
+  int variant = prm->variant;
+  if (variant == MHLA_VARIANT_AUTO) variant = MHLA_VARIANT_SIMT;
+  if (variant == MHLA_VARIANT_MULTIPASS) return MHLA_ERR_UNSUPPORTED;
+  p->variant = variant;
+
+  p->R = d * d + 2 * d;
+  // SIMT path: pieces of at most kSimtSplitLen tokens.
+  p->splits = (p->nb + kSimtSplitLen - 1) / kSimtSplitLen;
+  p->split_len = (p->nb + p->splits - 1) / p->splits;
+  p->kernels = 4;
+
+  if (p->BH == 0) {
+    p->ws_total = 0;
+    p->kernels = 0;
+    return MHLA_OK;
+  }
+  size_t off = 0;
+  p->off_stack = off;
+  off = align_up(off + sizeof(float) * (size_t)p->BH * p->M * p->splits * p->R);
+  p->off_mixed = off;
+  off = align_up(off + sizeof(float) * (size_t)p->BH * p->M * p->R);
+  p->off_rowsum = off;
+  off = align_up(off + sizeof(float) * (size_t)p->M);
+  p->off_aux = off;
+  p->ws_total = off;
+  return MHLA_OK;
+}
+
+bool misaligned(const void* ptr, size_t a) { return ((uintptr_t)ptr) % a != 0; }
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  if (!a || !b || na == 0 || nb == 0) return false;
+  const uintptr_t a0 = (uintptr_t)a, b0 = (uintptr_t)b;
+  return a0 < b0 + nb && b0 < a0 + na;
+}
+
+void record_event(int idx, cudaStream_t s) {
+  std::lock_guard<std::mutex> lock(g_events_mu);
+  if (g_num_events == MHLA_NUM_PHASE_EVENTS) cudaEventRecord(g_events[idx], s);
+}
+
+mhla_status run_plan(const Plan& plan, const void* q, const void* k, const void* v, const float* mc,
+                     void* out, char* ws, cudaStream_t s) {
+  Plan p = plan;
+  mhla_status st = device_error_ptr(&p.err);
+  if (st != MHLA_OK) return st;
+  float* stack = reinterpret_cast<float*>(ws + p.off_stack);
+  float* mixed = reinterpret_cast<float*>(ws + p.off_mixed);
+  float* rowsum = reinterpret_cast<float*>(ws + p.off_rowsum);
+  int e;
+  record_event(0, s);
+  if ((e = launch_mc_rowsum(p, mc, rowsum, s)) != 0) return cuda_fail((cudaError_t)e);
+  if ((e = launch_simt_summary(p, k, v, stack, s)) != 0) return cuda_fail((cudaError_t)e);
+  record_event(1, s);
+  if ((e = launch_simt_mix(p, mc, stack, mixed, s)) != 0) return cuda_fail((cudaError_t)e);
+  record_event(2, s);
+  if ((e = launch_simt_output(p, q, mixed, rowsum, out, s)) != 0) return cuda_fail((cudaError_t)e);
+  record_event(3, s);
+  return MHLA_OK;
+}
+
+}  // namespace
+}  // namespace mhla
+
+using mhla::Plan;
+
+extern "C" {
+
+mhla_status mhla_plan(const mhla_params* p, mhla_plan_info* info) {
+  Plan plan;
+  mhla_status st = mhla::make_plan(p, &plan);
+  if (st != MHLA_OK) return st;
+  if (info) {
+    info->n_tokens = plan.N;
+    info->n_blocks = plan.M;
+    info->block_tokens = plan.nb;
+    info->variant = plan.variant;
+    info->kernels_per_call = plan.kernels;
+    info->summary_splits = plan.splits;
+    info->workspace_bytes = plan.ws_total;
+  }
+  return MHLA_OK;
+}
+
+mhla_status mhla_workspace_bytes(const mhla_params* p, size_t* bytes) {
+  if (!bytes) return MHLA_ERR_INVALID_ARG;
+  Plan plan;
+  mhla_status st = mhla::make_plan(p, &plan);
+  if (st != MHLA_OK) return st;
+  *bytes = plan.ws_total;
+  return MHLA_OK;
+}
+
+mhla_status mhla_forward(const void* q, const void* k, const void* v, const float* mc,
+                         const mhla_params* p, void* out, void* workspace, size_t workspace_bytes,
+                         void* stream) {
+  Plan plan;
+  mhla_status st = mhla::make_plan(p, &plan);
+  if (st != MHLA_OK) return st;
+  if (plan.BH == 0) return MHLA_OK;
+  if (!q || !k || !v || !mc || !out) return MHLA_ERR_INVALID_ARG;
+  if (mhla::misaligned(q, 16) || mhla::misaligned(k, 16) || mhla::misaligned(v, 16) ||
+      mhla::misaligned(out, 16) || mhla::misaligned(mc, 4))
+    return MHLA_ERR_INVALID_ARG;
+  const size_t io_bytes = (size_t)plan.BH * plan.N * plan.d * mhla::elem_bytes(plan.dtype);
+  const size_t mc_bytes = sizeof(float) * (size_t)plan.M * plan.M;
+  if (mhla::overlaps(out, io_bytes, q, io_bytes) || mhla::overlaps(out, io_bytes, k, io_bytes) ||
+      mhla::overlaps(out, io_bytes, v, io_bytes) || mhla::overlaps(out, io_bytes, mc, mc_bytes))
+    return MHLA_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  bool owned = false;
+  if (!workspace) {
+    if (workspace_bytes != 0) return MHLA_ERR_INVALID_ARG;
+    cudaError_t e = cudaMallocAsync(&workspace, plan.ws_total, s);
+    if (e != cudaSuccess) return mhla::cuda_fail(e);
+    owned = true;
+  } else {
+    if (workspace_bytes < plan.ws_total) return MHLA_ERR_WORKSPACE;
+    if (mhla::misaligned(workspace, 256)) return MHLA_ERR_INVALID_ARG;
+    if (mhla::overlaps(out, io_bytes, workspace, plan.ws_total)) return MHLA_ERR_INVALID_ARG;
+  }
+  st = mhla::run_plan(plan, q, k, v, mc, out, static_cast<char*>(workspace), s);
+  if (owned) {
+    cudaError_t e = cudaFreeAsync(workspace, s);
+    if (st == MHLA_OK && e != cudaSuccess) st = mhla::cuda_fail(e);
+  }
+  return st;
+}
+
+mhla_status mhla_host_buffer_bytes(const mhla_params* p, size_t* bytes) {
+  if (!bytes) return MHLA_ERR_INVALID_ARG;
+  Plan plan;
+  mhla_status st = mhla::make_plan(p, &plan);
+  if (st != MHLA_OK) return st;
+  const size_t io = mhla::align_up((size_t)plan.BH * plan.N * plan.d * mhla::elem_bytes(plan.dtype));
+  const size_t mcb = mhla::align_up(sizeof(float) * (size_t)plan.M * plan.M);
+  *bytes = plan.BH == 0 ? 0 : 4 * io + mcb + plan.ws_total;
+  return MHLA_OK;
+}
+
+mhla_status mhla_forward_host(const void* q, const void* k, const void* v, const float* mc,
+                              const mhla_params* p, void* out, void* dev_buffer,
+                              size_t dev_buffer_bytes, void* stream) {
+  Plan plan;
+  mhla_status st = mhla::make_plan(p, &plan);
+  if (st != MHLA_OK) return st;
+  if (plan.BH == 0) return MHLA_OK;
+  if (!q || !k || !v || !mc || !out || !dev_buffer) return MHLA_ERR_INVALID_ARG;
+  if (mhla::misaligned(dev_buffer, 256)) return MHLA_ERR_INVALID_ARG;
+  size_t need = 0;
+  mhla_host_buffer_bytes(p, &need);
+  if (dev_buffer_bytes < need) return MHLA_ERR_WORKSPACE;
+  const size_t io_raw = (size_t)plan.BH * plan.N * plan.d * mhla::elem_bytes(plan.dtype);
+  const size_t io = mhla::align_up(io_raw);
+  const size_t mc_raw = sizeof(float) * (size_t)plan.M * plan.M;
+  const size_t mcb = mhla::align_up(mc_raw);
+  char* base = static_cast<char*>(dev_buffer);
+  char* dq = base;
+  char* dk = dq + io;
+  char* dv = dk + io;
+  char* dmc = dv + io;
+  char* dout = dmc + mcb;
+  char* ws = dout + io;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if ((e = cudaMemcpyAsync(dq, q, io_raw, cudaMemcpyHostToDevice, s)) != cudaSuccess) return mhla::cuda_fail(e);
+  if ((e = cudaMemcpyAsync(dk, k, io_raw, cudaMemcpyHostToDevice, s)) != cudaSuccess) return mhla::cuda_fail(e);
+  if ((e = cudaMemcpyAsync(dv, v, io_raw, cudaMemcpyHostToDevice, s)) != cudaSuccess) return mhla::cuda_fail(e);
+  if ((e = cudaMemcpyAsync(dmc, mc, mc_raw, cudaMemcpyHostToDevice, s)) != cudaSuccess) return mhla::cuda_fail(e);
+  st = mhla::run_plan(plan, dq, dk, dv, reinterpret_cast<const float*>(dmc), dout, ws, s);
+  if (st != MHLA_OK) return st;
+  if ((e = cudaMemcpyAsync(out, dout, io_raw, cudaMemcpyDeviceToHost, s)) != cudaSuccess) return mhla::cuda_fail(e);
+  if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return mhla::cuda_fail(e);
+  return MHLA_OK;
+}
+
+mhla_status mhla_device_status(int* code, int* detail) {
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return mhla::cuda_fail(e);
+  unsigned int h[2] = {0, 0};
+  e = cudaMemcpyFromSymbol(h, mhla::g_device_error, sizeof(h));
+  if (e != cudaSuccess) return mhla::cuda_fail(e);
+  const unsigned int zero[2] = {0, 0};
+  e = cudaMemcpyToSymbol(mhla::g_device_error, zero, sizeof(zero));
+  if (e != cudaSuccess) return mhla::cuda_fail(e);
+  if (code) *code = (int)h[0];
+  if (detail) *detail = (int)h[1];
+  return MHLA_OK;
+}
+
+mhla_status mhla_set_phase_events(void* const* events, int n) {
+  if (n != 0 && n != MHLA_NUM_PHASE_EVENTS) return MHLA_ERR_INVALID_ARG;
+  if (n && !events) return MHLA_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(mhla::g_events_mu);
+  for (int i = 0; i < n; ++i) {
+    if (!events[i]) return MHLA_ERR_INVALID_ARG;
+  }
+  for (int i = 0; i < n; ++i) mhla::g_events[i] = static_cast<cudaEvent_t>(events[i]);
+  mhla::g_num_events = n;
+  return MHLA_OK;
+}
+
+const char* mhla_status_string(mhla_status s) {
+  switch (s) {
+    case MHLA_OK: return "MHLA_OK";
+    case MHLA_ERR_INVALID_ARG: return "MHLA_ERR_INVALID_ARG: invalid pointer, shape, option or alignment";
+    case MHLA_ERR_UNSUPPORTED: return "MHLA_ERR_UNSUPPORTED: valid request this build cannot run";
+    case MHLA_ERR_WORKSPACE: return "MHLA_ERR_WORKSPACE: workspace missing or too small";
+    case MHLA_ERR_CUDA: return "MHLA_ERR_CUDA: a CUDA runtime call failed";
+    case MHLA_ERR_DEVICE_TIMEOUT: return "MHLA_ERR_DEVICE_TIMEOUT: a kernel's bounded wait expired";
+  }
+  return "MHLA: unknown status";
+}
+
+const char* mhla_last_error_string(void) { return mhla::g_last_error.c_str(); }
+
+int mhla_abi_version(void) { return MHLA_ABI_VERSION; }
+
+}  // extern "C"

@@ -1,0 +1,65 @@
+// Internal execution plan shared by the host dispatcher and the kernels.
+//
+// A Plan is a plain struct passed by value to every kernel.  It holds the
+// problem shape, the block partition of the token grid, how long blocks are
+// split into partial summaries, and where each intermediate lives in the
+// caller's workspace.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include "mhla.h"
+
+namespace mhla {
+
+struct Plan {
+  // shape
+  int B, H, BH, d;
+  int T, Hg, Wg;  // token grid
+  int bt, bh, bw; // block shape
+  int Mt, Mh, Mw; // block grid
+  int N, M, nb;   // tokens, blocks, tokens per block
+  // options
+  int dtype, fmap, norm, variant;
+  // long blocks are summarised in `splits` pieces of at most `split_len`
+  // tokens each; the mixing step sums the pieces (every piece of block b
+  // takes the weight Mc[i, b])
+  int splits, split_len;
+  // one stack row per (block, piece): S_b (d*d, row-major over (k, c)),
+  // z_b (d), v_b (d)
+  int R;
+  // number of kernel launches one forward enqueues
+  int kernels;
+  // workspace layout: byte offsets from the 256-aligned base
+  size_t ws_total;
+  size_t off_stack, off_mixed, off_rowsum, off_aux;
+  // device error word (code, detail), set by kernels whose bounded waits
+  // expire
+  unsigned int* err;
+};
+
+// Global token index (within one head) of local token l of block b.  Local
+// tokens run in raster order over the (bt, bh, bw) box; blocks in raster
+// order over the (Mt, Mh, Mw) block grid.
+__host__ __device__ inline int block_token(const Plan& p, int b, int l) {
+  int bx = b % p.Mw;
+  int r = b / p.Mw;
+  int by = r % p.Mh;
+  int bz = r / p.Mh;
+  int x = l % p.bw;
+  r = l / p.bw;
+  int y = r % p.bh;
+  int z = r / p.bh;
+  return ((bz * p.bt + z) * p.Hg + by * p.bh + y) * p.Wg + bx * p.bw + x;
+}
+
+// Launchers implemented by the kernel translation units.  Each returns the
+// cudaError_t of its launch (as int, to keep this header runtime-free).
+int launch_mc_rowsum(const Plan& p, const float* mc, float* rowsum, void* stream);
+int launch_simt_summary(const Plan& p, const void* k, const void* v, float* stack, void* stream);
+int launch_simt_mix(const Plan& p, const float* mc, const float* stack, float* mixed, void* stream);
+int launch_simt_output(const Plan& p, const void* q, const float* mixed, const float* rowsum,
+                       void* out, void* stream);
+
+}  // namespace mhla
