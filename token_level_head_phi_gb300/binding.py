@@ -245,6 +245,9 @@ def mhla_set_phase_events(events) -> None:
     if events is None:
         _check(load().mhla_set_phase_events(None, 0), "mhla_set_phase_events")
         return
+    for e in events:  # torch creates the CUDA event on its first record
+        if not e.cuda_event:
+            e.record()
     arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
     _check(load().mhla_set_phase_events(arr, len(events)), "mhla_set_phase_events")
 
