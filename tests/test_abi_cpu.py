@@ -167,3 +167,25 @@ def test_long_blocks_are_split(lib):
     w = wl.WORKLOADS["seq_32k_m1"]
     info = mb.mhla_plan(_params(w, variant="simt"))
     assert info.n_blocks == 1 and info.summary_splits > 1
+
+
+def test_auto_picks_tensor_cores_for_bf16_d64(lib):
+    w = wl.WORKLOADS["video_16x64x64"]
+    assert mb.mhla_plan(_params(w)).variant == mb.VARIANT_MULTIPASS
+    assert mb.mhla_plan(_params(wl.WORKLOADS["tiny_f32"])).variant == mb.VARIANT_SIMT
+    p = mb.make_params(1, 1, 32, (1, 8, 8), (1, 4, 4), "bf16")
+    assert mb.mhla_plan(p).variant == mb.VARIANT_SIMT
+
+
+def test_multipass_rejects_unsupported(lib):
+    info = mb.MhlaPlanInfo()
+    for dtype, d in (("f32", 64), ("bf16", 32), ("bf16", 128)):
+        p = mb.make_params(1, 1, d, (1, 8, 8), (1, 4, 4), dtype, variant="multipass")
+        assert lib.mhla_plan(ctypes.byref(p), ctypes.byref(info)) == mb.MHLA_ERR_UNSUPPORTED
+
+
+def test_multipass_splits_long_blocks(lib):
+    w = wl.WORKLOADS["seq_32k_m1"]
+    info = mb.mhla_plan(_params(w, variant="multipass"))
+    assert info.summary_splits > 1
+    assert mb.mhla_plan(_params(wl.WORKLOADS["video_16x64x64"], variant="multipass")).summary_splits == 1

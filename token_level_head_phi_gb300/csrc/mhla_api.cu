@@ -9,6 +9,7 @@
 
 #include "mhla.h"
 #include "plan.h"
+#include "tc_host.h"
 
 namespace mhla {
 namespace {
@@ -102,16 +103,34 @@ mhla_status make_plan(const mhla_params* prm, Plan* p) {
   p->fmap = prm->feature_map;
   p->norm = prm->norm;
 
+  const bool tc_ok = prm->dtype == MHLA_DTYPE_BF16 && d == kTcHeadDim;
   int variant = prm->variant;
-  if (variant == MHLA_VARIANT_AUTO) variant = MHLA_VARIANT_SIMT;
-  if (variant == MHLA_VARIANT_MULTIPASS) return MHLA_ERR_UNSUPPORTED;
+  if (variant == MHLA_VARIANT_AUTO) variant = tc_ok ? MHLA_VARIANT_MULTIPASS : MHLA_VARIANT_SIMT;
+  if (variant == MHLA_VARIANT_MULTIPASS && !tc_ok) return MHLA_ERR_UNSUPPORTED;
   p->variant = variant;
-
   p->R = d * d + 2 * d;
-  // SIMT path: pieces of at most kSimtSplitLen tokens.
-  p->splits = (p->nb + kSimtSplitLen - 1) / kSimtSplitLen;
-  p->split_len = (p->nb + p->splits - 1) / p->splits;
   p->kernels = 4;
+
+  if (variant == MHLA_VARIANT_SIMT) {
+    // pieces of at most kSimtSplitLen tokens
+    p->splits = (p->nb + kSimtSplitLen - 1) / kSimtSplitLen;
+    p->split_len = (p->nb + p->splits - 1) / p->splits;
+  } else {
+    // token chunks of <= 128 rows; blocks are cut into pieces only when there
+    // are too few blocks to keep every SM busy for several waves
+    p->chunk = choose_chunk(*p);
+    const int nck = p->chunk.per_block;
+    const int64_t blocks = (int64_t)p->BH * p->M;
+    int splits = 1;
+    if (blocks > 0 && blocks < 8LL * kPlanSms)
+      splits = (int)((8LL * kPlanSms + blocks - 1) / blocks);
+    if (splits > nck) splits = nck;
+    if (splits < 1) splits = 1;
+    p->cpp = (nck + splits - 1) / splits;
+    p->splits = (nck + p->cpp - 1) / p->cpp;
+    p->split_len = p->cpp * p->chunk.rows;
+    p->Qp = (p->M * p->splits + 7) / 8 * 8;
+  }
 
   if (p->BH == 0) {
     p->ws_total = 0;
@@ -119,12 +138,29 @@ mhla_status make_plan(const mhla_params* prm, Plan* p) {
     return MHLA_OK;
   }
   size_t off = 0;
-  p->off_stack = off;
-  off = align_up(off + sizeof(float) * (size_t)p->BH * p->M * p->splits * p->R);
-  p->off_mixed = off;
-  off = align_up(off + sizeof(float) * (size_t)p->BH * p->M * p->R);
-  p->off_rowsum = off;
-  off = align_up(off + sizeof(float) * (size_t)p->M);
+  if (variant == MHLA_VARIANT_SIMT) {
+    p->off_stack = off;
+    off = align_up(off + sizeof(float) * (size_t)p->BH * p->M * p->splits * p->R);
+    p->off_mixed = off;
+    off = align_up(off + sizeof(float) * (size_t)p->BH * p->M * p->R);
+    p->off_rowsum = off;
+    off = align_up(off + sizeof(float) * (size_t)p->M);
+  } else {
+    const size_t stack = 2 * (size_t)p->BH * p->M * p->splits * p->R;
+    const size_t mixed = 2 * (size_t)p->BH * p->M * p->R;
+    p->off_stack = off;
+    off = align_up(off + stack);
+    p->off_stack_lo = off;
+    if (p->norm == MHLA_NORM_MALA) off = align_up(off + stack);
+    p->off_mixed = off;
+    off = align_up(off + mixed);
+    p->off_mixed_lo = off;
+    off = align_up(off + mixed);
+    p->off_mc_exp = off;
+    off = align_up(off + 2 * (size_t)p->M * p->Qp);
+    p->off_rowsum = off;
+    off = align_up(off + sizeof(float) * (size_t)p->M);
+  }
   p->off_aux = off;
   p->ws_total = off;
   return MHLA_OK;
@@ -148,10 +184,29 @@ mhla_status run_plan(const Plan& plan, const void* q, const void* k, const void*
   Plan p = plan;
   mhla_status st = device_error_ptr(&p.err);
   if (st != MHLA_OK) return st;
+  int e;
+  if (p.variant == MHLA_VARIANT_MULTIPASS) {
+    TcBuffers b;
+    b.stack_hi = reinterpret_cast<__nv_bfloat16*>(ws + p.off_stack);
+    b.stack_lo = p.norm == MHLA_NORM_MALA ? reinterpret_cast<__nv_bfloat16*>(ws + p.off_stack_lo) : nullptr;
+    b.mixed_hi = reinterpret_cast<__nv_bfloat16*>(ws + p.off_mixed);
+    b.mixed_lo = reinterpret_cast<__nv_bfloat16*>(ws + p.off_mixed_lo);
+    b.mc_exp = reinterpret_cast<__nv_bfloat16*>(ws + p.off_mc_exp);
+    b.rowsum = reinterpret_cast<float*>(ws + p.off_rowsum);
+    b.Qp = p.Qp;
+    record_event(0, s);
+    if ((e = launch_tc_prep(p, mc, b, s)) != 0) return cuda_fail((cudaError_t)e);
+    if ((e = launch_tc_summary(p, p.chunk, k, v, b, s)) != 0) return cuda_fail((cudaError_t)e);
+    record_event(1, s);
+    if ((e = launch_tc_mix(p, b, s)) != 0) return cuda_fail((cudaError_t)e);
+    record_event(2, s);
+    if ((e = launch_tc_output(p, p.chunk, q, b, out, s)) != 0) return cuda_fail((cudaError_t)e);
+    record_event(3, s);
+    return MHLA_OK;
+  }
   float* stack = reinterpret_cast<float*>(ws + p.off_stack);
   float* mixed = reinterpret_cast<float*>(ws + p.off_mixed);
   float* rowsum = reinterpret_cast<float*>(ws + p.off_rowsum);
-  int e;
   record_event(0, s);
   if ((e = launch_mc_rowsum(p, mc, rowsum, s)) != 0) return cuda_fail((cudaError_t)e);
   if ((e = launch_simt_summary(p, k, v, stack, s)) != 0) return cuda_fail((cudaError_t)e);

@@ -13,6 +13,16 @@
 
 namespace mhla {
 
+// Token tile ("chunk") of the tensor-core path: a (ct, ch, cw) sub-box of a
+// block with ct*ch*cw <= 128 rows that tiles the block exactly.
+struct ChunkShape {
+  int ct, ch, cw;
+  int ncx, ncy, nct;  // chunks per block along x, y, t
+  int per_block;      // ncx * ncy * nct
+  int rows;           // ct * ch * cw
+  int rows_pad;       // rows rounded up to 16 (MMA K granularity)
+};
+
 struct Plan {
   // shape
   int B, H, BH, d;
@@ -26,6 +36,9 @@ struct Plan {
   // tokens each; the mixing step sums the pieces (every piece of block b
   // takes the weight Mc[i, b])
   int splits, split_len;
+  // tensor-core path: token chunk and chunks per piece
+  ChunkShape chunk;
+  int cpp;
   // one stack row per (block, piece): S_b (d*d, row-major over (k, c)),
   // z_b (d), v_b (d)
   int R;
@@ -34,6 +47,9 @@ struct Plan {
   // workspace layout: byte offsets from the 256-aligned base
   size_t ws_total;
   size_t off_stack, off_mixed, off_rowsum, off_aux;
+  // tensor-core path buffers
+  size_t off_stack_lo, off_mixed_lo, off_mc_exp;
+  int Qp;
   // device error word (code, detail), set by kernels whose bounded waits
   // expire
   unsigned int* err;

@@ -18,8 +18,11 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+
+#include "mhla.h"
 
 namespace mhla {
 namespace tc {
@@ -75,22 +78,44 @@ __device__ __forceinline__ void report_timeout(unsigned int* err, unsigned int w
 }
 
 // Waits until the phase of `bar` with parity `parity` has completed.  Gives
-// up after kWaitLimitNs, records the timeout (with `where`) and returns false.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned int* err, unsigned int where) {
+// up after kWaitLimitNs, records the timeout (with `where`), raises the CTA's
+// abort flag and returns false.  Also returns false as soon as another role
+// of the CTA has raised the abort flag.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned int* err, unsigned int where,
+                                          volatile int* abort_flag = nullptr) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0u && globaltimer() - t0 > kWaitLimitNs) {
-      report_timeout(err, where);
-      return false;
+    if ((it & 63u) == 0u) {
+      if (abort_flag && *abort_flag) return false;
+      if (globaltimer() - t0 > kWaitLimitNs) {
+        report_timeout(err, where);
+        if (abort_flag) *abort_flag = 1;
+        return false;
+      }
     }
   }
 }
 
 // Named barrier over `nthreads` threads (a multiple of 32) with id 1..15.
 __device__ __forceinline__ void named_sync(uint32_t id, uint32_t nthreads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+  asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Named barrier that also ANDs `pred` over the participating threads, so a
+// group of threads leaves a loop together when any of them gave up a wait.
+__device__ __forceinline__ bool named_all(uint32_t id, uint32_t nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "barrier.red.and.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
 }
 
 // Makes this thread's generic-proxy shared-memory writes visible to the
@@ -140,6 +165,22 @@ __device__ __forceinline__ void tma_store_5d(const CUtensorMap* map, uint32_t sr
   asm volatile("cp.async.bulk.tensor.5d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5, %6}], [%1];" ::"l"(
                    reinterpret_cast<uint64_t>(map)),
                "r"(src), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
+               : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1,
+                                            uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int c0, int c1) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(src), "r"(c0), "r"(c1)
                : "memory");
 }
 

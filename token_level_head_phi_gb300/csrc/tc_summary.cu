@@ -1,0 +1,389 @@
+// Block summaries on the tensor cores (head dimension 64, bf16 inputs).
+//
+// For every block b of every head ("MHLA: Restoring Expressivity of Linear
+// Attention via Token-Level Multi-Head", overall framework):
+//   S_b = sum_{j in b} phi(K_j) V_j^T,  z_b = sum_{j in b} phi(K_j),
+//   v_b = sum_{j in b} V_j  (the last one feeds the MALA normalisation).
+// All three come out of ONE 128x128 tcgen05 MMA per 16 tokens:
+//   A = [phi(K_b)^T ; 1^T]  (rows 0..63 features of phi(K), rows 64..127 ones)
+//   B = [V_b | 1]           (cols 0..63 features of V, cols 64..127 ones)
+//   D = A B:  D[k][c] = S_b[k][c], D[k][64] = z_b[k], D[64][c] = v_b[c].
+// Both operands are MN-major: the token tile arrives by TMA exactly as it
+// lies in memory ([token][feature], 128-byte rows, 128-byte swizzle) and the
+// ones tiles sit at a fixed shared-memory offset reached through the
+// descriptor's leading-byte offset.  phi = ELU+1 is applied in place to the
+// K tile by a transform warpgroup; padding rows stay zero.
+//
+// Persistent, warp-specialised CTA (one per SM, 384 threads):
+//   warp 0      TMA producer (K and V tiles of one token chunk per stage)
+//   warp 1      TMEM allocation + MMA issue (one elected thread)
+//   warps 4-7   phi(K) transform, one thread per token row
+//   warps 8-11  epilogue: TMEM -> bf16 (hi and, for MALA, lo residual) ->
+//               swizzled staging tile -> TMA store into the summary stack
+// Each CTA walks work units (head, block, piece) with a static stride; long
+// blocks are cut into pieces whose partial summaries the mixing step adds.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstring>
+
+#include "common.cuh"
+#include "tc_common.cuh"
+#include "tc_host.h"
+
+namespace mhla {
+namespace {
+
+using namespace tc;
+
+constexpr int kStages = 4;
+constexpr int kThreads = 384;
+constexpr uint32_t kTile = 128 * 128;                  // 128 rows of 128 bytes
+constexpr uint32_t kStageBytes = 2 * kTile;            // K tile + V tile
+constexpr uint32_t kOnesA = kStages * kStageBytes;     // ones tile of A (rows 64..127)
+constexpr uint32_t kOnesB = kOnesA + kTile;            // ones tile of B (cols 64..127)
+constexpr uint32_t kStaging = kOnesB + kTile;          // 2 buffers x (hi, lo) x (S 8 KB + zv 1 KB)
+constexpr uint32_t kStagePart = 8192 + 1024;
+constexpr uint32_t kStagingBuf = 2 * kStagePart;
+constexpr uint32_t kBars = kStaging + 2 * kStagingBuf;
+constexpr uint32_t kSmemBytes = kBars + 256 + 1024;    // + barriers + alignment slack
+constexpr uint32_t kTmemCols = 256;                    // two 128-column accumulators
+
+struct SummaryArgs {
+  CUtensorMap tmK, tmV;              // 5D (64, Wg, Hg, T, BH), box (64, cw, ch, ct, 1)
+  CUtensorMap tmS_hi, tmZV_hi;       // 2D stack view (64, rows), boxes (64, 64) and (64, 2)
+  CUtensorMap tmS_lo, tmZV_lo;
+  int units, splits, cpp;            // work units, pieces per block, chunks per piece
+  int write_lo;
+  ChunkShape c;
+  unsigned int* err;
+};
+
+__device__ __forceinline__ float phi_fast(float x, int fmap) {
+  if (fmap == MHLA_FEATURE_IDENTITY) return x;
+  return x > 0.f ? x + 1.f : __expf(x);
+}
+
+__device__ __forceinline__ uint32_t phi_pair(uint32_t w, int fmap) {
+  __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162*>(&w);
+  float2 f = __bfloat1622float2(h);
+  return pack_bf16x2(phi_fast(f.x, fmap), phi_fast(f.y, fmap));
+}
+
+struct UnitCoord {
+  int u, b, c0, c1;
+};
+
+__device__ __forceinline__ UnitCoord unit_coord(const Plan& p, const SummaryArgs& a, int w) {
+  UnitCoord r;
+  const int per_head = p.M * a.splits;
+  r.u = w / per_head;
+  const int rem = w % per_head;
+  r.b = rem / a.splits;
+  const int s = rem % a.splits;
+  r.c0 = s * a.cpp;
+  r.c1 = min(a.c.per_block, r.c0 + a.cpp);
+  return r;
+}
+
+// Grid origin of chunk `c` of block `b`.
+__device__ __forceinline__ void chunk_origin(const Plan& p, const ChunkShape& ch, int b, int c, int& x0, int& y0,
+                                             int& t0) {
+  const int bx = b % p.Mw;
+  const int by = (b / p.Mw) % p.Mh;
+  const int bz = b / (p.Mw * p.Mh);
+  const int cx = c % ch.ncx;
+  const int cy = (c / ch.ncx) % ch.ncy;
+  const int cz = c / (ch.ncx * ch.ncy);
+  x0 = bx * p.bw + cx * ch.cw;
+  y0 = by * p.bh + cy * ch.ch;
+  t0 = bz * p.bt + cz * ch.ct;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) tc_summary_kernel(const __grid_constant__ SummaryArgs a, const Plan p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gb = smem_raw + (base - raw);
+  const uint32_t bars = base + kBars;
+  // barrier addresses
+  auto full = [&](int s) { return bars + 8u * s; };
+  auto kready = [&](int s) { return bars + 8u * (kStages + s); };
+  auto empty = [&](int s) { return bars + 8u * (2 * kStages + s); };
+  auto accfull = [&](int x) { return bars + 8u * (3 * kStages + x); };
+  auto accempty = [&](int x) { return bars + 8u * (3 * kStages + 2 + x); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gb + kBars + 8 * (3 * kStages + 4));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gb + kBars + 8 * (3 * kStages + 4) + 8);
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  const int rows = a.c.rows;
+
+  // Stage tiles start zeroed (padding rows must stay zero); the ones tiles
+  // hold 1.0 in every valid row.
+  for (uint32_t off = threadIdx.x * 16u; off < kStaging; off += kThreads * 16u) {
+    uint4 val = make_uint4(0u, 0u, 0u, 0u);
+    if (off >= kOnesA && ((off - kOnesA) % kTile) / 128u < (uint32_t)rows)
+      val = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+    *reinterpret_cast<uint4*>(gb + off) = val;
+  }
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(kready(s), 128);
+      mbar_init(empty(s), 1);
+    }
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(accfull(x), 1);
+      mbar_init(accempty(x), 128);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&a.tmK);
+    tma_prefetch_desc(&a.tmV);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  fence_proxy_async();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------- producer
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      const uint32_t bytes = 2u * (uint32_t)rows * 128u;
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int w = blockIdx.x; w < a.units && ok; w += gridDim.x) {
+        const UnitCoord uc = unit_coord(p, a, w);
+        for (int c = uc.c0; c < uc.c1; ++c) {
+          if (!(ok = mbar_wait(empty(stage), phase ^ 1u, a.err, 0x101, abort_flag))) break;
+          int x0, y0, t0;
+          chunk_origin(p, a.c, uc.b, c, x0, y0, t0);
+          const uint32_t kt = base + (uint32_t)stage * kStageBytes;
+          mbar_arrive_expect_tx(full(stage), bytes);
+          tma_load_5d(kt, &a.tmK, full(stage), 0, x0, y0, t0, uc.u, pol);
+          tma_load_5d(kt + kTile, &a.tmV, full(stage), 0, x0, y0, t0, uc.u, pol);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // --------------------------------------------------------------- MMA
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(128, 128, true, true);
+      const int ksteps = a.c.rows_pad / 16;
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, accph = 0;
+      bool ok = true;
+      for (int w = blockIdx.x; w < a.units && ok; w += gridDim.x) {
+        const UnitCoord uc = unit_coord(p, a, w);
+        if (!(ok = mbar_wait(accempty(acc), accph ^ 1u, a.err, 0x102, abort_flag))) break;
+        tc_fence_after();
+        const uint32_t d = tmem + (uint32_t)acc * 128u;
+        for (int c = uc.c0; c < uc.c1; ++c) {
+          if (!(ok = mbar_wait(kready(stage), phase, a.err, 0x103, abort_flag))) break;
+          tc_fence_after();
+          const uint32_t kt = base + (uint32_t)stage * kStageBytes;
+          const uint32_t vt = kt + kTile;
+          const uint32_t lbo_a = base + kOnesA - kt;
+          const uint32_t lbo_b = base + kOnesB - vt;
+          for (int ks = 0; ks < ksteps; ++ks) {
+            umma_bf16(d, sdesc_sw128(kt + (uint32_t)ks * 2048u, lbo_a, 1024u),
+                      sdesc_sw128(vt + (uint32_t)ks * 2048u, lbo_b, 1024u), idesc,
+                      (c > uc.c0 || ks > 0) ? 1u : 0u);
+          }
+          umma_commit(empty(stage));
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(accfull(acc));
+        if (++acc == 2) {
+          acc = 0;
+          accph ^= 1u;
+        }
+      }
+    }
+  } else if (warp >= 4 && warp < 8) {
+    // ------------------------------------------------ phi(K) transform
+    const int t = threadIdx.x - 128;
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int w = blockIdx.x; w < a.units && ok; w += gridDim.x) {
+      const UnitCoord uc = unit_coord(p, a, w);
+      for (int c = uc.c0; c < uc.c1; ++c) {
+        if (!(ok = mbar_wait(full(stage), phase, a.err, 0x104, abort_flag))) break;
+        if (t < rows) {
+          uint8_t* row = gb + stage * kStageBytes + t * 128;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            uint4* ptr = reinterpret_cast<uint4*>(row + (((j + t) & 7) << 4));
+            uint4 x = *ptr;
+            x.x = phi_pair(x.x, p.fmap);
+            x.y = phi_pair(x.y, p.fmap);
+            x.z = phi_pair(x.z, p.fmap);
+            x.w = phi_pair(x.w, p.fmap);
+            *ptr = x;
+          }
+        }
+        fence_proxy_async();
+        mbar_arrive(kready(stage));
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+  } else if (warp >= 8) {
+    // ------------------------------------------------------------ epilogue
+    const int e = warp - 8;
+    const int et = threadIdx.x - 256;
+    const int r = 32 * e + lane;  // TMEM lane = row of D
+    int acc = 0, it = 0;
+    uint32_t accph = 0;
+    bool ok = true;
+    for (int w = blockIdx.x; w < a.units && ok; w += gridDim.x, ++it) {
+      const UnitCoord uc = unit_coord(p, a, w);
+      ok = mbar_wait(accfull(acc), accph, a.err, 0x105, abort_flag);
+      if (!(ok = named_all(1, 128, ok))) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem + (uint32_t)acc * 128u + ((uint32_t)(32 * e) << 16);
+      float s0[32], s1[32], zz[32];
+      if (e < 3) {
+        tmem_ld32(taddr, s0);
+        tmem_ld32(taddr + 32u, s1);
+      }
+      if (e < 2) tmem_ld32(taddr + 64u, zz);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(accempty(acc));
+      if (++acc == 2) {
+        acc = 0;
+        accph ^= 1u;
+      }
+
+      uint8_t* st_hi = gb + kStaging + (it & 1) * kStagingBuf;
+      uint8_t* st_lo = st_hi + kStagePart;
+      if (et == 0) bulk_wait_read<1>();
+      named_sync(1, 128);
+      if (e < 2) {
+        // row r of S (= summary row k) and z[k]
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float* src = j < 4 ? &s0[8 * j] : &s1[8 * (j - 4)];
+          uint4 hv, lv;
+          uint32_t* hp = &hv.x;
+          uint32_t* lp = &lv.x;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float x0 = src[2 * q], x1 = src[2 * q + 1];
+            hp[q] = pack_bf16x2(x0, x1);
+            if (a.write_lo) {
+              __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162*>(&hp[q]);
+              float2 hf = __bfloat1622float2(h);
+              lp[q] = pack_bf16x2(x0 - hf.x, x1 - hf.y);
+            }
+          }
+          const uint32_t off = (uint32_t)r * 128u + ((uint32_t)((j ^ (r & 7)) & 7) << 4);
+          *reinterpret_cast<uint4*>(st_hi + off) = hv;
+          if (a.write_lo) *reinterpret_cast<uint4*>(st_lo + off) = lv;
+        }
+        const __nv_bfloat16 zh = __float2bfloat16_rn(zz[0]);
+        *reinterpret_cast<__nv_bfloat16*>(st_hi + 8192 + sw128_offset(0, r)) = zh;
+        if (a.write_lo)
+          *reinterpret_cast<__nv_bfloat16*>(st_lo + 8192 + sw128_offset(0, r)) =
+              __float2bfloat16_rn(zz[0] - __bfloat162float(zh));
+      } else if (e == 2 && lane == 0) {
+        // row 64 of D: v_b (every row 64..127 holds the same values)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float* src = j < 4 ? &s0[8 * j] : &s1[8 * (j - 4)];
+          uint4 hv, lv;
+          uint32_t* hp = &hv.x;
+          uint32_t* lp = &lv.x;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float x0 = src[2 * q], x1 = src[2 * q + 1];
+            hp[q] = pack_bf16x2(x0, x1);
+            __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162*>(&hp[q]);
+            float2 hf = __bfloat1622float2(h);
+            lp[q] = pack_bf16x2(x0 - hf.x, x1 - hf.y);
+          }
+          const uint32_t off = 128u + ((uint32_t)((j ^ 1) & 7) << 4);
+          *reinterpret_cast<uint4*>(st_hi + 8192 + off) = hv;
+          if (a.write_lo) *reinterpret_cast<uint4*>(st_lo + 8192 + off) = lv;
+        }
+      }
+      fence_proxy_async();
+      named_sync(1, 128);
+      if (et == 0) {
+        const int row0 = ((uc.u * p.M + uc.b) * a.splits + (uc.c0 / a.cpp)) * 66;
+        tma_store_2d(&a.tmS_hi, smem_u32(st_hi), 0, row0);
+        tma_store_2d(&a.tmZV_hi, smem_u32(st_hi + 8192), 0, row0 + 64);
+        if (a.write_lo) {
+          tma_store_2d(&a.tmS_lo, smem_u32(st_lo), 0, row0);
+          tma_store_2d(&a.tmZV_lo, smem_u32(st_lo + 8192), 0, row0 + 64);
+        }
+        bulk_commit();
+      }
+    }
+    if (et == 0) bulk_wait<0>();
+  }
+  __syncwarp();
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+}  // namespace
+
+int launch_tc_summary(const Plan& p, const ChunkShape& c, const void* k, const void* v, const TcBuffers& b,
+                      cudaStream_t s) {
+  SummaryArgs a;
+  memset(&a, 0, sizeof(a));
+  const uint64_t dims5[5] = {64, (uint64_t)p.Wg, (uint64_t)p.Hg, (uint64_t)p.T, (uint64_t)p.BH};
+  const uint64_t str5[4] = {128, 128ull * p.Wg, 128ull * p.Wg * p.Hg, 128ull * p.N};
+  const uint32_t box5[5] = {64, (uint32_t)c.cw, (uint32_t)c.ch, (uint32_t)c.ct, 1};
+  int e;
+  if ((e = encode_tmap_bf16(&a.tmK, k, 5, dims5, str5, box5)) != 0) return e;
+  if ((e = encode_tmap_bf16(&a.tmV, v, 5, dims5, str5, box5)) != 0) return e;
+  const uint64_t stack_rows = (uint64_t)p.BH * p.M * p.splits * 66ull;
+  const uint64_t dims2[2] = {64, stack_rows};
+  const uint64_t str2[1] = {128};
+  const uint32_t boxS[2] = {64, 64};
+  const uint32_t boxZV[2] = {64, 2};
+  if ((e = encode_tmap_bf16(&a.tmS_hi, b.stack_hi, 2, dims2, str2, boxS)) != 0) return e;
+  if ((e = encode_tmap_bf16(&a.tmZV_hi, b.stack_hi, 2, dims2, str2, boxZV)) != 0) return e;
+  a.write_lo = b.stack_lo != nullptr;
+  const void* lo = a.write_lo ? (const void*)b.stack_lo : (const void*)b.stack_hi;
+  if ((e = encode_tmap_bf16(&a.tmS_lo, lo, 2, dims2, str2, boxS)) != 0) return e;
+  if ((e = encode_tmap_bf16(&a.tmZV_lo, lo, 2, dims2, str2, boxZV)) != 0) return e;
+  a.splits = p.splits;
+  a.cpp = p.cpp;
+  a.units = p.BH * p.M * p.splits;
+  a.c = c;
+  a.err = p.err;
+  cudaError_t ce = cudaFuncSetAttribute(tc_summary_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  if (ce != cudaSuccess) return (int)ce;
+  const int grid = a.units < num_sms() ? a.units : num_sms();
+  tc_summary_kernel<<<grid, kThreads, kSmemBytes, s>>>(a, p);
+  return (int)cudaGetLastError();
+}
+
+}  // namespace mhla

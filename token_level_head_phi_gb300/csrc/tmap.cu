@@ -1,0 +1,82 @@
+// Host helpers of the tensor-core path: TMA tensor-map encoding (through the
+// driver entry point, so the library does not link libcuda directly) and the
+// SM count of the current device.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "tc_host.h"
+
+namespace mhla {
+namespace {
+
+std::once_flag g_enc_once;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_sm_mu;
+int g_sms[kMaxDevices] = {};
+
+}  // namespace
+
+int encode_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                     const uint64_t* strides_bytes, const uint32_t* box) {
+  std::call_once(g_enc_once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (!g_encode) return (int)cudaErrorNotSupported;
+  cuuint64_t gdim[5];
+  cuuint64_t gstride[4];
+  cuuint32_t bdim[5];
+  cuuint32_t estride[5];
+  for (int i = 0; i < rank; ++i) {
+    gdim[i] = dims[i];
+    bdim[i] = box[i];
+    estride[i] = 1;
+    if (i + 1 < rank) gstride[i] = strides_bytes[i];
+  }
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base), gdim,
+                        gstride, bdim, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : (int)cudaErrorInvalidValue;
+}
+
+ChunkShape choose_chunk(const Plan& p) {
+  auto largest_divisor = [](int n, int limit) {
+    for (int d = limit < n ? limit : n; d >= 1; --d)
+      if (n % d == 0) return d;
+    return 1;
+  };
+  ChunkShape c;
+  c.cw = largest_divisor(p.bw, kTcTileRows);
+  c.ch = largest_divisor(p.bh, kTcTileRows / c.cw);
+  c.ct = largest_divisor(p.bt, kTcTileRows / (c.cw * c.ch));
+  c.ncx = p.bw / c.cw;
+  c.ncy = p.bh / c.ch;
+  c.nct = p.bt / c.ct;
+  c.per_block = c.ncx * c.ncy * c.nct;
+  c.rows = c.ct * c.ch * c.cw;
+  c.rows_pad = (c.rows + 15) / 16 * 16;
+  return c;
+}
+
+int num_sms() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
+  std::lock_guard<std::mutex> lock(g_sm_mu);
+  if (!g_sms[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    g_sms[dev] = n;
+  }
+  return g_sms[dev];
+}
+
+}  // namespace mhla
