@@ -158,6 +158,8 @@ mhla_status make_plan(const mhla_params* prm, Plan* p) {
     off = align_up(off + mixed);
     p->off_mc_exp = off;
     off = align_up(off + 2 * (size_t)p->M * p->Qp);
+    p->off_mc_exp_lo = off;
+    off = align_up(off + 2 * (size_t)p->M * p->Qp);
     p->off_rowsum = off;
     off = align_up(off + sizeof(float) * (size_t)p->M);
   }
@@ -192,6 +194,7 @@ mhla_status run_plan(const Plan& plan, const void* q, const void* k, const void*
     b.mixed_hi = reinterpret_cast<__nv_bfloat16*>(ws + p.off_mixed);
     b.mixed_lo = reinterpret_cast<__nv_bfloat16*>(ws + p.off_mixed_lo);
     b.mc_exp = reinterpret_cast<__nv_bfloat16*>(ws + p.off_mc_exp);
+    b.mc_exp_lo = reinterpret_cast<__nv_bfloat16*>(ws + p.off_mc_exp_lo);
     b.rowsum = reinterpret_cast<float*>(ws + p.off_rowsum);
     b.Qp = p.Qp;
     record_event(0, s);

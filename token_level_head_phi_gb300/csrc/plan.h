@@ -48,7 +48,7 @@ struct Plan {
   size_t ws_total;
   size_t off_stack, off_mixed, off_rowsum, off_aux;
   // tensor-core path buffers
-  size_t off_stack_lo, off_mixed_lo, off_mc_exp;
+  size_t off_stack_lo, off_mixed_lo, off_mc_exp, off_mc_exp_lo;
   int Qp;
   // device error word (code, detail), set by kernels whose bounded waits
   // expire

@@ -32,7 +32,8 @@ struct TcBuffers {
   __nv_bfloat16* mixed_hi;  // [BH][M][R]
   __nv_bfloat16* mixed_lo;  // [BH][M][R]
   __nv_bfloat16* mc_exp;    // [M][Qp] bf16(Mc[i][q / splits])
-  float* rowsum;            // [M] sum_b bf16(Mc[i][b])
+  __nv_bfloat16* mc_exp_lo; // [M][Qp] low bf16 residual of the same
+  float* rowsum;            // [M] sum_b (hi + lo)(Mc[i][b])
   int Qp;                   // padded row pitch of mc_exp
 };
 

@@ -29,24 +29,25 @@ namespace {
 
 using namespace tc;
 
-constexpr int kStages = 3;
+constexpr int kMaxStages = 4;
 constexpr int kThreads = 256;
 constexpr uint32_t kAtom = 64 * 128;                // 64 q-rows x 64 r (8 KB)
 constexpr uint32_t kATile = 2 * kAtom;              // 128 r
-constexpr uint32_t kBTileMax = 256 * 128;           // 256 query blocks x 64 q
-constexpr uint32_t kStageBytes = 2 * kATile + kBTileMax;  // A hi, A lo, B
-constexpr uint32_t kBars = kStages * kStageBytes;
+constexpr uint32_t kStageArea = 200 * 1024;         // shared memory for the stages
+constexpr uint32_t kBars = kStageArea;
 constexpr uint32_t kSmemBytes = kBars + 256 + 1024;
 constexpr uint32_t kTmemCols = 512;                 // two accumulators of up to 256 columns
 
 struct MixArgs {
   CUtensorMap tmA_hi, tmA_lo;  // 3D (R, Q, BH), box (64, 64, 1)
-  CUtensorMap tmB;             // 2D (Q, M),     box (64, NT)
+  CUtensorMap tmB_hi, tmB_lo;  // 2D (Q, M),     box (64, NT)
   __nv_bfloat16* mixed_hi;
   __nv_bfloat16* mixed_lo;
   int Q, NT, itiles, rtiles, kchunks, units;
-  int use_lo_in;   // second MMA with the low residual of the stack
+  int use_lo_in;   // extra MMA with the low residual of the stack (MALA)
   int write_lo_s;  // write the low residual of S~ (aux rows always get one)
+  int stages;      // pipeline depth (<= kMaxStages)
+  uint32_t stage_bytes, off_alo, off_bhi, off_blo;
   unsigned int* err;
 };
 
@@ -56,12 +57,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_mix_kernel(const __grid_consta
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gb = smem_raw + (base - raw);
   const uint32_t bars = base + kBars;
+  const int kStages = a.stages;
   auto full = [&](int s) { return bars + 8u * s; };
-  auto empty = [&](int s) { return bars + 8u * (kStages + s); };
-  auto accfull = [&](int x) { return bars + 8u * (2 * kStages + x); };
-  auto accempty = [&](int x) { return bars + 8u * (2 * kStages + 2 + x); };
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gb + kBars + 8 * (2 * kStages + 4));
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(gb + kBars + 8 * (2 * kStages + 4) + 8);
+  auto empty = [&](int s) { return bars + 8u * (kMaxStages + s); };
+  auto accfull = [&](int x) { return bars + 8u * (2 * kMaxStages + x); };
+  auto accempty = [&](int x) { return bars + 8u * (2 * kMaxStages + 2 + x); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gb + kBars + 8 * (2 * kMaxStages + 4));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gb + kBars + 8 * (2 * kMaxStages + 4) + 8);
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -80,7 +82,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_mix_kernel(const __grid_consta
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&a.tmA_hi);
-    tma_prefetch_desc(&a.tmB);
+    tma_prefetch_desc(&a.tmB_hi);
+    tma_prefetch_desc(&a.tmB_lo);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
@@ -97,7 +100,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_mix_kernel(const __grid_consta
       // ---------------------------------------------------------- producer
       const uint64_t pol_a = policy_evict_first();
       const uint64_t pol_b = policy_evict_last();
-      const uint32_t bytes = kATile * (a.use_lo_in ? 2u : 1u) + (uint32_t)a.NT * 128u;
+      const uint32_t bytes = kATile * (a.use_lo_in ? 2u : 1u) + 2u * (uint32_t)a.NT * 128u;
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -108,15 +111,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_mix_kernel(const __grid_consta
         const int i0 = (rem % a.itiles) * a.NT;
         for (int kc = 0; kc < a.kchunks; ++kc) {
           if (!(ok = mbar_wait(empty(stage), phase ^ 1u, a.err, 0x201, abort_flag))) break;
-          const uint32_t st = base + (uint32_t)stage * kStageBytes;
+          const uint32_t st = base + (uint32_t)stage * a.stage_bytes;
           mbar_arrive_expect_tx(full(stage), bytes);
           tma_load_3d(st, &a.tmA_hi, full(stage), r0, kc * 64, u, pol_a);
           tma_load_3d(st + kAtom, &a.tmA_hi, full(stage), r0 + 64, kc * 64, u, pol_a);
           if (a.use_lo_in) {
-            tma_load_3d(st + kATile, &a.tmA_lo, full(stage), r0, kc * 64, u, pol_a);
-            tma_load_3d(st + kATile + kAtom, &a.tmA_lo, full(stage), r0 + 64, kc * 64, u, pol_a);
+            tma_load_3d(st + a.off_alo, &a.tmA_lo, full(stage), r0, kc * 64, u, pol_a);
+            tma_load_3d(st + a.off_alo + kAtom, &a.tmA_lo, full(stage), r0 + 64, kc * 64, u, pol_a);
           }
-          tma_load_2d(st + 2 * kATile, &a.tmB, full(stage), kc * 64, i0, pol_b);
+          tma_load_2d(st + a.off_bhi, &a.tmB_hi, full(stage), kc * 64, i0, pol_b);
+          tma_load_2d(st + a.off_blo, &a.tmB_lo, full(stage), kc * 64, i0, pol_b);
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
@@ -138,14 +142,18 @@ __global__ void __launch_bounds__(kThreads, 1) tc_mix_kernel(const __grid_consta
         for (int kc = 0; kc < a.kchunks; ++kc) {
           if (!(ok = mbar_wait(full(stage), phase, a.err, 0x203, abort_flag))) break;
           tc_fence_after();
-          const uint32_t st = base + (uint32_t)stage * kStageBytes;
-          const uint32_t bt = st + 2 * kATile;
+          const uint32_t st = base + (uint32_t)stage * a.stage_bytes;
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) {
-            const uint64_t bd = sdesc_sw128(bt + (uint32_t)ks * 32u, 0u, 1024u);
-            umma_bf16(d, sdesc_sw128(st + (uint32_t)ks * 2048u, kAtom, 1024u), bd, idesc,
-                      (kc > 0 || ks > 0) ? 1u : 0u);
-            if (a.use_lo_in) umma_bf16(d, sdesc_sw128(st + kATile + (uint32_t)ks * 2048u, kAtom, 1024u), bd, idesc, 1u);
+            // X_hi Mc_hi + X_hi Mc_lo (+ X_lo Mc_hi): Mc carries its low bf16
+            // residual in every norm, the stack only for MALA
+            const uint64_t ahi = sdesc_sw128(st + (uint32_t)ks * 2048u, kAtom, 1024u);
+            const uint64_t bhi = sdesc_sw128(st + a.off_bhi + (uint32_t)ks * 32u, 0u, 1024u);
+            const uint64_t blo = sdesc_sw128(st + a.off_blo + (uint32_t)ks * 32u, 0u, 1024u);
+            umma_bf16(d, ahi, bhi, idesc, (kc > 0 || ks > 0) ? 1u : 0u);
+            umma_bf16(d, ahi, blo, idesc, 1u);
+            if (a.use_lo_in)
+              umma_bf16(d, sdesc_sw128(st + a.off_alo + (uint32_t)ks * 2048u, kAtom, 1024u), bhi, idesc, 1u);
           }
           umma_commit(empty(stage));
           if (++stage == kStages) {
@@ -211,17 +219,26 @@ __global__ void __launch_bounds__(kThreads, 1) tc_mix_kernel(const __grid_consta
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-// One warp per row i of Mc.
+// One warp per row i of Mc: high and low bf16 parts, expanded over pieces,
+// and the row sum of hi + lo in float32.
 __global__ void tc_prep_kernel(int M, int splits, int Q, int Qp, const float* __restrict__ mc,
-                               __nv_bfloat16* __restrict__ mc_exp, float* __restrict__ rowsum) {
+                               __nv_bfloat16* __restrict__ mc_hi, __nv_bfloat16* __restrict__ mc_lo,
+                               float* __restrict__ rowsum) {
   const int i = (blockIdx.x * blockDim.x + threadIdx.x) / 32;
   const int lane = threadIdx.x % 32;
   if (i >= M) return;
   const float* row = mc + (size_t)i * M;
-  for (int q = lane; q < Qp; q += 32)
-    mc_exp[(size_t)i * Qp + q] = q < Q ? __float2bfloat16_rn(row[q / splits]) : __float2bfloat16_rn(0.f);
+  for (int q = lane; q < Qp; q += 32) {
+    const float x = q < Q ? row[q / splits] : 0.f;
+    const __nv_bfloat16 h = __float2bfloat16_rn(x);
+    mc_hi[(size_t)i * Qp + q] = h;
+    mc_lo[(size_t)i * Qp + q] = __float2bfloat16_rn(x - __bfloat162float(h));
+  }
   float s = 0.f;
-  for (int b = lane; b < M; b += 32) s += __bfloat162float(__float2bfloat16_rn(row[b]));
+  for (int b = lane; b < M; b += 32) {
+    const __nv_bfloat16 h = __float2bfloat16_rn(row[b]);
+    s += __bfloat162float(h) + __bfloat162float(__float2bfloat16_rn(row[b] - __bfloat162float(h)));
+  }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
   if (lane == 0) rowsum[i] = s;
@@ -232,7 +249,8 @@ __global__ void tc_prep_kernel(int M, int splits, int Q, int Qp, const float* __
 int launch_tc_prep(const Plan& p, const float* mc, const TcBuffers& b, cudaStream_t s) {
   const int threads = 256;
   const int blocks = (p.M * 32 + threads - 1) / threads;
-  tc_prep_kernel<<<blocks, threads, 0, s>>>(p.M, p.splits, p.M * p.splits, b.Qp, mc, b.mc_exp, b.rowsum);
+  tc_prep_kernel<<<blocks, threads, 0, s>>>(p.M, p.splits, p.M * p.splits, b.Qp, mc, b.mc_exp, b.mc_exp_lo,
+                                             b.rowsum);
   return (int)cudaGetLastError();
 }
 
@@ -252,7 +270,8 @@ int launch_tc_mix(const Plan& p, const TcBuffers& b, cudaStream_t s) {
   const uint64_t dimsB[2] = {(uint64_t)Q, (uint64_t)p.M};
   const uint64_t strB[1] = {2ull * b.Qp};
   const uint32_t boxB[2] = {64, (uint32_t)NT};
-  if ((e = encode_tmap_bf16(&a.tmB, b.mc_exp, 2, dimsB, strB, boxB)) != 0) return e;
+  if ((e = encode_tmap_bf16(&a.tmB_hi, b.mc_exp, 2, dimsB, strB, boxB)) != 0) return e;
+  if ((e = encode_tmap_bf16(&a.tmB_lo, b.mc_exp_lo, 2, dimsB, strB, boxB)) != 0) return e;
   a.mixed_hi = b.mixed_hi;
   a.mixed_lo = b.mixed_lo;
   a.Q = Q;
@@ -262,6 +281,13 @@ int launch_tc_mix(const Plan& p, const TcBuffers& b, cudaStream_t s) {
   a.kchunks = (Q + 63) / 64;
   a.units = p.BH * a.rtiles * a.itiles;
   a.write_lo_s = p.norm == MHLA_NORM_MALA;
+  const uint32_t btile = (uint32_t)NT * 128u;
+  a.off_alo = kATile;
+  a.off_bhi = kATile * (a.use_lo_in ? 2u : 1u);
+  a.off_blo = a.off_bhi + btile;
+  a.stage_bytes = (a.off_blo + btile + 1023u) / 1024u * 1024u;
+  a.stages = (int)(kStageArea / a.stage_bytes);
+  if (a.stages > kMaxStages) a.stages = kMaxStages;
   a.err = p.err;
   cudaError_t ce = cudaFuncSetAttribute(tc_mix_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (ce != cudaSuccess) return (int)ce;

@@ -36,18 +36,24 @@ namespace {
 
 using namespace tc;
 
-constexpr int kStages = 4;
 constexpr int kThreads = 384;
 constexpr uint32_t kTile = 128 * 128;                  // 128 rows of 128 bytes
-constexpr uint32_t kStageBytes = 2 * kTile;            // K tile + V tile
-constexpr uint32_t kOnesA = kStages * kStageBytes;     // ones tile of A (rows 64..127)
-constexpr uint32_t kOnesB = kOnesA + kTile;            // ones tile of B (cols 64..127)
-constexpr uint32_t kStaging = kOnesB + kTile;          // 2 buffers x (hi, lo) x (S 8 KB + zv 1 KB)
-constexpr uint32_t kStagePart = 8192 + 1024;
-constexpr uint32_t kStagingBuf = 2 * kStagePart;
-constexpr uint32_t kBars = kStaging + 2 * kStagingBuf;
-constexpr uint32_t kSmemBytes = kBars + 256 + 1024;    // + barriers + alignment slack
+constexpr uint32_t kStagePart = 8192 + 1024;           // staging: S 8 KB + zv 1 KB
+constexpr uint32_t kStagingBuf = 2 * kStagePart;       // hi and lo
 constexpr uint32_t kTmemCols = 256;                    // two 128-column accumulators
+
+// Shared-memory layout.  kLo adds the low bf16 residual of phi(K) as a third
+// tile per stage (MALA); the stage count shrinks to keep everything resident.
+template <bool kLo>
+struct Layout {
+  static constexpr int kStages = kLo ? 3 : 4;
+  static constexpr uint32_t kStageBytes = (kLo ? 3 : 2) * kTile;  // K, V [, K lo]
+  static constexpr uint32_t kOnesA = kStages * kStageBytes;         // ones tile of A (rows 64..127)
+  static constexpr uint32_t kOnesB = kOnesA + kTile;                // ones tile of B (cols 64..127)
+  static constexpr uint32_t kStaging = kOnesB + kTile;              // 2 staging buffers
+  static constexpr uint32_t kBars = kStaging + 2 * kStagingBuf;
+  static constexpr uint32_t kSmemBytes = kBars + 256 + 1024;        // + barriers + alignment slack
+};
 
 struct SummaryArgs {
   CUtensorMap tmK, tmV;              // 5D (64, Wg, Hg, T, BH), box (64, cw, ch, ct, 1)
@@ -68,6 +74,17 @@ __device__ __forceinline__ uint32_t phi_pair(uint32_t w, int fmap) {
   __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162*>(&w);
   float2 f = __bfloat1622float2(h);
   return pack_bf16x2(phi_fast(f.x, fmap), phi_fast(f.y, fmap));
+}
+
+// phi of two bf16 values as bf16 (returned) plus the low bf16 residual.
+__device__ __forceinline__ uint32_t phi_pair_lo(uint32_t w, int fmap, uint32_t& lo) {
+  __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162*>(&w);
+  float2 f = __bfloat1622float2(h);
+  const float a = phi_fast(f.x, fmap), b = phi_fast(f.y, fmap);
+  const uint32_t hi = pack_bf16x2(a, b);
+  float2 g = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&hi));
+  lo = pack_bf16x2(a - g.x, b - g.y);
+  return hi;
 }
 
 struct UnitCoord {
@@ -100,7 +117,15 @@ __device__ __forceinline__ void chunk_origin(const Plan& p, const ChunkShape& ch
   t0 = bz * p.bt + cz * ch.ct;
 }
 
+template <bool kLo>
 __global__ void __launch_bounds__(kThreads, 1) tc_summary_kernel(const __grid_constant__ SummaryArgs a, const Plan p) {
+  using L = Layout<kLo>;
+  constexpr int kStages = L::kStages;
+  constexpr uint32_t kStageBytes = L::kStageBytes;
+  constexpr uint32_t kOnesA = L::kOnesA;
+  constexpr uint32_t kOnesB = L::kOnesB;
+  constexpr uint32_t kStaging = L::kStaging;
+  constexpr uint32_t kBars = L::kBars;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -200,9 +225,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_summary_kernel(const __grid_co
           const uint32_t lbo_a = base + kOnesA - kt;
           const uint32_t lbo_b = base + kOnesB - vt;
           for (int ks = 0; ks < ksteps; ++ks) {
-            umma_bf16(d, sdesc_sw128(kt + (uint32_t)ks * 2048u, lbo_a, 1024u),
-                      sdesc_sw128(vt + (uint32_t)ks * 2048u, lbo_b, 1024u), idesc,
+            const uint64_t bd = sdesc_sw128(vt + (uint32_t)ks * 2048u, lbo_b, 1024u);
+            umma_bf16(d, sdesc_sw128(kt + (uint32_t)ks * 2048u, lbo_a, 1024u), bd, idesc,
                       (c > uc.c0 || ks > 0) ? 1u : 0u);
+            if (kLo) {
+              // [phi(K) lo ; ones]: rows 64..127 of D collect v_b a second time
+              const uint32_t klo = kt + 2 * kTile;
+              umma_bf16(d, sdesc_sw128(klo + (uint32_t)ks * 2048u, base + kOnesA - klo, 1024u), bd, idesc, 1u);
+            }
           }
           umma_commit(empty(stage));
           if (++stage == kStages) {
@@ -232,12 +262,22 @@ __global__ void __launch_bounds__(kThreads, 1) tc_summary_kernel(const __grid_co
           uint8_t* row = gb + stage * kStageBytes + t * 128;
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
-            uint4* ptr = reinterpret_cast<uint4*>(row + (((j + t) & 7) << 4));
+            const uint32_t off = ((j + t) & 7) << 4;
+            uint4* ptr = reinterpret_cast<uint4*>(row + off);
             uint4 x = *ptr;
-            x.x = phi_pair(x.x, p.fmap);
-            x.y = phi_pair(x.y, p.fmap);
-            x.z = phi_pair(x.z, p.fmap);
-            x.w = phi_pair(x.w, p.fmap);
+            if (kLo) {
+              uint4 lo;
+              x.x = phi_pair_lo(x.x, p.fmap, lo.x);
+              x.y = phi_pair_lo(x.y, p.fmap, lo.y);
+              x.z = phi_pair_lo(x.z, p.fmap, lo.z);
+              x.w = phi_pair_lo(x.w, p.fmap, lo.w);
+              *reinterpret_cast<uint4*>(row + 2 * kTile + off) = lo;
+            } else {
+              x.x = phi_pair(x.x, p.fmap);
+              x.y = phi_pair(x.y, p.fmap);
+              x.z = phi_pair(x.z, p.fmap);
+              x.w = phi_pair(x.w, p.fmap);
+            }
             *ptr = x;
           }
         }
@@ -318,7 +358,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_summary_kernel(const __grid_co
           uint32_t* lp = &lv.x;
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            const float x0 = src[2 * q], x1 = src[2 * q + 1];
+            const float vscale = kLo ? 0.5f : 1.f;  // the lo MMA adds v_b a second time
+            const float x0 = src[2 * q] * vscale, x1 = src[2 * q + 1] * vscale;
             hp[q] = pack_bf16x2(x0, x1);
             __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162*>(&hp[q]);
             float2 hf = __bfloat1622float2(h);
@@ -370,7 +411,7 @@ int launch_tc_summary(const Plan& p, const ChunkShape& c, const void* k, const v
   const uint32_t boxZV[2] = {64, 2};
   if ((e = encode_tmap_bf16(&a.tmS_hi, b.stack_hi, 2, dims2, str2, boxS)) != 0) return e;
   if ((e = encode_tmap_bf16(&a.tmZV_hi, b.stack_hi, 2, dims2, str2, boxZV)) != 0) return e;
-  a.write_lo = b.stack_lo != nullptr;
+  a.write_lo = b.stack_lo != nullptr;  // MALA: phi(K) and the stack carry low residuals
   const void* lo = a.write_lo ? (const void*)b.stack_lo : (const void*)b.stack_hi;
   if ((e = encode_tmap_bf16(&a.tmS_lo, lo, 2, dims2, str2, boxS)) != 0) return e;
   if ((e = encode_tmap_bf16(&a.tmZV_lo, lo, 2, dims2, str2, boxZV)) != 0) return e;
@@ -379,10 +420,18 @@ int launch_tc_summary(const Plan& p, const ChunkShape& c, const void* k, const v
   a.units = p.BH * p.M * p.splits;
   a.c = c;
   a.err = p.err;
-  cudaError_t ce = cudaFuncSetAttribute(tc_summary_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-  if (ce != cudaSuccess) return (int)ce;
   const int grid = a.units < num_sms() ? a.units : num_sms();
-  tc_summary_kernel<<<grid, kThreads, kSmemBytes, s>>>(a, p);
+  if (a.write_lo) {
+    const uint32_t smem = Layout<true>::kSmemBytes;
+    cudaError_t ce = cudaFuncSetAttribute(tc_summary_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (ce != cudaSuccess) return (int)ce;
+    tc_summary_kernel<true><<<grid, kThreads, smem, s>>>(a, p);
+  } else {
+    const uint32_t smem = Layout<false>::kSmemBytes;
+    cudaError_t ce = cudaFuncSetAttribute(tc_summary_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (ce != cudaSuccess) return (int)ce;
+    tc_summary_kernel<false><<<grid, kThreads, smem, s>>>(a, p);
+  }
   return (int)cudaGetLastError();
 }
 
