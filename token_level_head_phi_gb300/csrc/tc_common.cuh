@@ -255,6 +255,42 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 2 consecutive float32 columns of this warp's 32 TMEM lanes.
+__device__ __forceinline__ void tmem_ld2(uint32_t taddr, float& a, float& b) {
+  uint32_t r0, r1;
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0,%1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(taddr));
+  a = __uint_as_float(r0);
+  b = __uint_as_float(r1);
+}
+
+// 16 consecutive float32 columns of this warp's 32 TMEM lanes.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// phi = ELU(x) + 1 written as max(x, 0) + exp(min(x, 0)): x + 1 above zero,
+// exp(x) at and below it, with no branch or select.
+__device__ __forceinline__ float phi_elu1_fast(float x) {
+  return fmaxf(x, 0.f) + __expf(fminf(x, 0.f));
+}
+
+__device__ __forceinline__ float phi_map(float x, int fmap) {
+  return fmap == MHLA_FEATURE_IDENTITY ? x : phi_elu1_fast(x);
+}
+
+// Two bf16 (one 32-bit word) -> float2, exact.
+__device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w) {
+  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+
 // Shared-memory matrix descriptor, 128-byte swizzle (layout type 2),
 // descriptor version 1 (bits 46-47), base offset 0 (tile bases 1024-aligned).
 __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {

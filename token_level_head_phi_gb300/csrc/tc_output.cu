@@ -3,18 +3,23 @@
 // 2; "Rectifying Magnitude Neglect in Linear Attention", key designs).
 //
 // For a token tile of query block i (up to 128 tokens, gathered by one TMA box
-// from the token grid):
-//     D = phi(Q_tile) S~_i            (tcgen05, M = 128 tokens, N = 64, K = 64)
-//     s_t = phi(q_t) . z~_i           (CUDA cores, while phi is applied)
+// from the token grid) one tcgen05 MMA of N = 80 yields numerators and
+// denominators together:
+//     D = phi(Q_tile) [S~_i | z~_i]   (M = 128 tokens, K = 64, N = 64 + 16)
+//     D[t][c] = phi(q_t)^T S~_i[:, c],  s_t = D[t][64] + D[t][65]
+// where the second B atom holds z~_i in two columns (high and low bf16
+// parts) and zeros elsewhere.  The epilogue forms
 //   DIVISIVE o = D / s,  NONE o = D,
 //   MALA     o = (1 + 1/s) D - (s / n~_i) v~_i,   n~_i = n_b sum_b Mc[i, b]
-// then the bf16 result overwrites the Q tile in shared memory and one TMA
-// store scatters it back to the grid positions of the tile.
+// writes the bf16 result over the Q tile in shared memory, and one TMA store
+// scatters it back to the grid positions of the tile.
 //   A = phi(Q) tile: K-major (features contiguous), as TMA delivered it
 //   B = S~_i: MN-major ([k][c], c contiguous), loaded by TMA from the mixed
 //       stack (bf16 high part; MALA adds the low residual as a second MMA)
-// Persistent, warp-specialised CTA (384 threads): warp 0 TMA producer,
-// warp 1 TMEM + MMA, warps 4-7 phi + denominators, warps 8-11 epilogue.
+// Persistent, warp-specialised CTA (640 threads): warp 0 TMA producer,
+// warp 1 TMEM + MMA, warps 4-11 phi(Q) (two threads per token row) and the
+// z~/v~ operands, warps 12-19 epilogue (two warps per TMEM lane quarter,
+// 32 output features each).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -30,20 +35,22 @@ namespace {
 using namespace tc;
 
 constexpr int kStages = 4;
-constexpr int kThreads = 384;
-constexpr uint32_t kQTile = 128 * 128;           // Q / O tile
-constexpr uint32_t kBTile = 64 * 128;            // S~_i, 64 k-rows x 64 c
-constexpr uint32_t kOffBhi = kQTile;
-constexpr uint32_t kOffBlo = kQTile + kBTile;
-constexpr uint32_t kOffDen = kQTile + 2 * kBTile;  // 128 floats
-constexpr uint32_t kOffZ = kOffDen + 512;          // z~ (64 floats)
-constexpr uint32_t kOffV = kOffZ + 256;            // v~ (64 floats)
-constexpr uint32_t kStageBytes = 34 * 1024;
+constexpr int kThreads = 640;
+constexpr int kXfThreads = 256;                    // warps 4..11
+constexpr int kEpiThreads = 256;                   // warps 12..19
+constexpr uint32_t kQTile = 128 * 128;             // Q / O tile
+constexpr uint32_t kBTile = 64 * 128;              // 64 k-rows x 64 columns
+constexpr uint32_t kOffBhi = kQTile;               // S~_i high part
+constexpr uint32_t kOffZt = kOffBhi + kBTile;      // z~_i as columns 0 (hi) and 1 (lo)
+constexpr uint32_t kOffBlo = kOffZt + kBTile;      // S~_i low part (MALA)
+constexpr uint32_t kOffV = kOffBlo + kBTile;       // v~_i, 64 floats (MALA)
+constexpr uint32_t kStageBytes = kOffV + 1024;
 constexpr uint32_t kBars = kStages * kStageBytes;
 constexpr uint32_t kSmemBytes = kBars + 256 + 1024;
-constexpr uint32_t kTmemCols = 256;              // one 64-column accumulator per stage
+constexpr uint32_t kAccStride = 128;               // TMEM columns per stage (80 used)
+constexpr uint32_t kTmemCols = 512;
 
-static_assert(kOffV + 256 <= kStageBytes, "stage layout overflow");
+static_assert(kStageBytes % 1024 == 0, "stage alignment");
 
 struct OutArgs {
   CUtensorMap tmQ, tmO;        // 5D (64, Wg, Hg, T, BH), box (64, cw, ch, ct, 1)
@@ -56,11 +63,6 @@ struct OutArgs {
   ChunkShape c;
   unsigned int* err;
 };
-
-__device__ __forceinline__ float phi_fast(float x, int fmap) {
-  if (fmap == MHLA_FEATURE_IDENTITY) return x;
-  return x > 0.f ? x + 1.f : __expf(x);
-}
 
 __global__ void __launch_bounds__(kThreads, 1) tc_output_kernel(const __grid_constant__ OutArgs a, const Plan p) {
   extern __shared__ uint8_t smem_raw[];
@@ -81,10 +83,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_output_kernel(const __grid_con
   const int nck = a.c.per_block;
   const int per_head = p.M * nck;
 
+  // z~ tiles: every column except 0 and 1 stays zero
+  for (int s = 0; s < kStages; ++s)
+    for (uint32_t off = threadIdx.x * 16u; off < kBTile; off += kThreads * 16u)
+      *reinterpret_cast<uint4*>(gb + s * kStageBytes + kOffZt + off) = make_uint4(0u, 0u, 0u, 0u);
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(full(s), 1);
-      mbar_init(tready(s), 128);
+      mbar_init(tready(s), kXfThreads);
       mbar_init(mmadone(s), 1);
       mbar_init(empty(s), 1);
     }
@@ -100,6 +106,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_output_kernel(const __grid_con
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
+  fence_proxy_async();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -137,19 +144,22 @@ __global__ void __launch_bounds__(kThreads, 1) tc_output_kernel(const __grid_con
   } else if (warp == 1) {
     if (lane == 0) {
       // --------------------------------------------------------------- MMA
-      const uint32_t idesc = idesc_bf16_f32(128, 64, false, true);
+      const uint32_t idesc80 = idesc_bf16_f32(128, 80, false, true);
+      const uint32_t idesc64 = idesc_bf16_f32(128, 64, false, true);
       int stage = 0;
       uint32_t phase = 0;
       for (int w = blockIdx.x; w < a.units; w += gridDim.x) {
         if (!mbar_wait(tready(stage), phase, a.err, 0x302, abort_flag)) break;
         tc_fence_after();
         const uint32_t st = base + (uint32_t)stage * kStageBytes;
-        const uint32_t d = tmem + (uint32_t)stage * 64u;
+        const uint32_t d = tmem + (uint32_t)stage * kAccStride;
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
           const uint64_t ad = sdesc_sw128(st + (uint32_t)ks * 32u, 0u, 1024u);
-          umma_bf16(d, ad, sdesc_sw128(st + kOffBhi + (uint32_t)ks * 2048u, kBTile, 1024u), idesc, ks > 0 ? 1u : 0u);
-          if (a.use_lo) umma_bf16(d, ad, sdesc_sw128(st + kOffBlo + (uint32_t)ks * 2048u, kBTile, 1024u), idesc, 1u);
+          umma_bf16(d, ad, sdesc_sw128(st + kOffBhi + (uint32_t)ks * 2048u, kOffZt - kOffBhi, 1024u), idesc80,
+                    ks > 0 ? 1u : 0u);
+          if (a.use_lo)
+            umma_bf16(d, ad, sdesc_sw128(st + kOffBlo + (uint32_t)ks * 2048u, kBTile, 1024u), idesc64, 1u);
         }
         umma_commit(mmadone(stage));
         if (++stage == kStages) {
@@ -158,43 +168,46 @@ __global__ void __launch_bounds__(kThreads, 1) tc_output_kernel(const __grid_con
         }
       }
     }
-  } else if (warp >= 4 && warp < 8) {
-    // ------------------------------------------- phi(Q) and denominators
+  } else if (warp >= 4 && warp < 12) {
+    // ----------------------------------- phi(Q) and the z~_i / v~_i operands
     const int t = threadIdx.x - 128;
+    const int row = t >> 1;
+    const int half = t & 1;
     int stage = 0;
     uint32_t phase = 0;
     for (int w = blockIdx.x; w < a.units; w += gridDim.x) {
       const int u = w / per_head;
       const int i = (w % per_head) / nck;
-      // z~_i (threads 0..63) and v~_i (threads 64..127), hi + lo parts
-      const size_t aux = ((size_t)u * p.M + i) * p.R + (size_t)p.d * p.d + t;
-      const float zv = __bfloat162float(a.mixed_hi[aux]) + __bfloat162float(a.mixed_lo[aux]);
+      // threads 0..63: z~_i[k] (hi, lo); threads 64..127: v~_i[c] (hi + lo)
+      const size_t aux = ((size_t)u * p.M + i) * p.R + (size_t)p.d * p.d + (t & 127);
+      __nv_bfloat16 zh = __float2bfloat16_rn(0.f), zl = zh;
+      if (t < 128) {
+        zh = a.mixed_hi[aux];
+        zl = a.mixed_lo[aux];
+      }
       const bool ok = mbar_wait(full(stage), phase, a.err, 0x303, abort_flag);
-      if (!named_all(2, 128, ok)) break;
+      if (!named_all(2, kXfThreads, ok)) break;
       uint8_t* st = gb + stage * kStageBytes;
-      float* zs = reinterpret_cast<float*>(st + kOffZ);  // z at [0,64), v at [64,128)
-      zs[t] = zv;
-      named_sync(4, 128);
-      if (t < rows) {
-        uint8_t* row = st + t * 128;
-        float s = 0.f;
+      if (t < 64) {
+        *reinterpret_cast<__nv_bfloat16*>(st + kOffZt + sw128_offset(t, 0)) = zh;
+        *reinterpret_cast<__nv_bfloat16*>(st + kOffZt + sw128_offset(t, 1)) = zl;
+      } else if (t < 128) {
+        reinterpret_cast<float*>(st + kOffV)[t - 64] = __bfloat162float(zh) + __bfloat162float(zl);
+      }
+      if (row < rows) {
+        uint8_t* rp = st + row * 128;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          uint4* ptr = reinterpret_cast<uint4*>(row + (((j ^ t) & 7) << 4));
-          uint4 x = *ptr;
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t off = ((4 * half + j + row) & 7) << 4;
+          uint4 x = *reinterpret_cast<uint4*>(rp + off);
           uint32_t* xp = &x.x;
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162*>(&xp[q]);
-            float2 f = __bfloat1622float2(h);
-            xp[q] = pack_bf16x2(phi_fast(f.x, p.fmap), phi_fast(f.y, p.fmap));
-            float2 g = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&xp[q]));
-            s = fmaf(g.x, zs[8 * j + 2 * q], s);
-            s = fmaf(g.y, zs[8 * j + 2 * q + 1], s);
+            const float2 f = bf16x2_to_float2(xp[q]);
+            xp[q] = pack_bf16x2(phi_map(f.x, p.fmap), phi_map(f.y, p.fmap));
           }
-          *ptr = x;
+          *reinterpret_cast<uint4*>(rp + off) = x;
         }
-        reinterpret_cast<float*>(st + kOffDen)[t] = s;
       }
       fence_proxy_async();
       mbar_arrive(tready(stage));
@@ -203,10 +216,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_output_kernel(const __grid_con
         phase ^= 1u;
       }
     }
-  } else if (warp >= 8) {
+  } else if (warp >= 12) {
     // ------------------------------------------------------------ epilogue
-    const int e = warp - 8;
-    const int t = threadIdx.x - 256;  // token row = TMEM lane
+    const int q4 = warp & 3;            // TMEM lane quarter
+    const int h = (warp - 12) >> 2;     // output features 32h .. 32h+31
+    const int t = 32 * q4 + lane;       // token row = TMEM lane
+    const int et = threadIdx.x - 384;
     int stage = 0, prev = -1;
     uint32_t phase = 0;
     for (int w = blockIdx.x; w < a.units; w += gridDim.x) {
@@ -215,48 +230,48 @@ __global__ void __launch_bounds__(kThreads, 1) tc_output_kernel(const __grid_con
       const int i = rem / nck;
       const int c = rem % nck;
       bool ok = mbar_wait(mmadone(stage), phase, a.err, 0x304, abort_flag);
-      // the transform's shared-memory writes (denominators, z~, v~)
+      // the transform's shared-memory writes (v~)
       ok = ok && mbar_wait(tready(stage), phase, a.err, 0x305, abort_flag);
-      if (!named_all(3, 128, ok)) break;
+      if (!named_all(3, kEpiThreads, ok)) break;
       tc_fence_after();
-      float o0[32], o1[32];
-      const uint32_t taddr = tmem + (uint32_t)stage * 64u + ((uint32_t)(32 * e) << 16);
-      tmem_ld32(taddr, o0);
-      tmem_ld32(taddr + 32u, o1);
+      float o[32], s0, s1;
+      const uint32_t taddr = tmem + (uint32_t)stage * kAccStride + ((uint32_t)(32 * q4) << 16);
+      tmem_ld32(taddr + 32u * h, o);
+      tmem_ld2(taddr + 64u, s0, s1);
       tmem_wait_ld();
       uint8_t* st = gb + stage * kStageBytes;
       if (t < rows) {
-        const float s = reinterpret_cast<const float*>(st + kOffDen)[t];
-        const float* vs = reinterpret_cast<const float*>(st + kOffV);
-        // MALA: beta = 1 + 1/s, gamma = s / n~_i
-        const float beta = 1.f + 1.f / s;
-        const float gamma = p.norm == MHLA_NORM_MALA ? s / ((float)p.nb * a.rowsum[i]) : 0.f;
-        uint8_t* row = st + t * 128;
+        const float s = s0 + s1;
+        float scale = 1.f, gamma = 0.f;
+        if (p.norm == MHLA_NORM_DIVISIVE) {
+          scale = __frcp_rn(s);
+        } else if (p.norm == MHLA_NORM_MALA) {
+          scale = 1.f + __frcp_rn(s);                       // beta
+          gamma = s / ((float)p.nb * a.rowsum[i]);
+        }
+        const float* vs = reinterpret_cast<const float*>(st + kOffV) + 32 * h;
+        uint8_t* rp = st + t * 128;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float* src = j < 4 ? &o0[8 * j] : &o1[8 * (j - 4)];
+        for (int j = 0; j < 4; ++j) {
           uint4 x;
           uint32_t* xp = &x.x;
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            const int cidx = 8 * j + 2 * q;
-            float y0 = src[2 * q], y1 = src[2 * q + 1];
-            if (p.norm == MHLA_NORM_DIVISIVE) {
-              y0 = y0 / s;
-              y1 = y1 / s;
-            } else if (p.norm == MHLA_NORM_MALA) {
-              y0 = beta * y0 - gamma * vs[cidx];
-              y1 = beta * y1 - gamma * vs[cidx + 1];
+            const int cc = 8 * j + 2 * q;
+            float y0 = o[cc] * scale, y1 = o[cc + 1] * scale;
+            if (p.norm == MHLA_NORM_MALA) {
+              y0 -= gamma * vs[cc];
+              y1 -= gamma * vs[cc + 1];
             }
             xp[q] = pack_bf16x2(y0, y1);
           }
-          *reinterpret_cast<uint4*>(row + (((j ^ t) & 7) << 4)) = x;
+          *reinterpret_cast<uint4*>(rp + ((((4 * h + j) ^ t) & 7) << 4)) = x;
         }
       }
       fence_proxy_async();
       tc_fence_before();
-      named_sync(3, 128);
-      if (t == 0) {
+      named_sync(3, kEpiThreads);
+      if (et == 0) {
         const int bx = i % p.Mw, by = (i / p.Mw) % p.Mh, bz = i / (p.Mw * p.Mh);
         const int x0 = bx * p.bw + (c % a.c.ncx) * a.c.cw;
         const int y0 = by * p.bh + ((c / a.c.ncx) % a.c.ncy) * a.c.ch;
@@ -273,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_output_kernel(const __grid_con
         phase ^= 1u;
       }
     }
-    if (t == 0) bulk_wait<0>();
+    if (et == 0) bulk_wait<0>();
   }
   __syncwarp();
 

@@ -4,22 +4,25 @@
 // Attention via Token-Level Multi-Head", overall framework):
 //   S_b = sum_{j in b} phi(K_j) V_j^T,  z_b = sum_{j in b} phi(K_j),
 //   v_b = sum_{j in b} V_j  (the last one feeds the MALA normalisation).
-// All three come out of ONE 128x128 tcgen05 MMA per 16 tokens:
+// All three come out of ONE 128x80 tcgen05 MMA per 16 tokens:
 //   A = [phi(K_b)^T ; 1^T]  (rows 0..63 features of phi(K), rows 64..127 ones)
-//   B = [V_b | 1]           (cols 0..63 features of V, cols 64..127 ones)
+//   B = [V_b | 1]           (cols 0..63 features of V, cols 64..79 ones)
 //   D = A B:  D[k][c] = S_b[k][c], D[k][64] = z_b[k], D[64][c] = v_b[c].
 // Both operands are MN-major: the token tile arrives by TMA exactly as it
 // lies in memory ([token][feature], 128-byte rows, 128-byte swizzle) and the
 // ones tiles sit at a fixed shared-memory offset reached through the
 // descriptor's leading-byte offset.  phi = ELU+1 is applied in place to the
-// K tile by a transform warpgroup; padding rows stay zero.
+// K tile by the transform warps; padding rows stay zero.  For MALA the low
+// bf16 residual of phi(K) goes through a second MMA (its ones rows add v_b a
+// second time, which the epilogue halves).
 //
-// Persistent, warp-specialised CTA (one per SM, 384 threads):
-//   warp 0      TMA producer (K and V tiles of one token chunk per stage)
-//   warp 1      TMEM allocation + MMA issue (one elected thread)
-//   warps 4-7   phi(K) transform, one thread per token row
-//   warps 8-11  epilogue: TMEM -> bf16 (hi and, for MALA, lo residual) ->
-//               swizzled staging tile -> TMA store into the summary stack
+// Persistent, warp-specialised CTA (one per SM, 512 threads):
+//   warp 0       TMA producer (K and V tiles of one token chunk per stage)
+//   warp 1       TMEM allocation + MMA issue (one elected thread)
+//   warps 4-6    epilogue: TMEM rows 0..95 -> bf16 (hi and, for MALA, lo
+//                residual) -> swizzled staging tile -> TMA store into the
+//                summary stack
+//   warps 8-15   phi(K) transform, two threads per token row
 // Each CTA walks work units (head, block, piece) with a static stride; long
 // blocks are cut into pieces whose partial summaries the mixing step adds.
 #include <cuda_bf16.h>
@@ -36,11 +39,14 @@ namespace {
 
 using namespace tc;
 
-constexpr int kThreads = 384;
-constexpr uint32_t kTile = 128 * 128;                  // 128 rows of 128 bytes
-constexpr uint32_t kStagePart = 8192 + 1024;           // staging: S 8 KB + zv 1 KB
-constexpr uint32_t kStagingBuf = 2 * kStagePart;       // hi and lo
-constexpr uint32_t kTmemCols = 256;                    // two 128-column accumulators
+constexpr int kThreads = 512;
+constexpr int kEpiThreads = 96;                         // warps 4..6
+constexpr int kXfThreads = 256;                         // warps 8..15
+constexpr uint32_t kTile = 128 * 128;                   // 128 rows of 128 bytes
+constexpr uint32_t kStagePart = 8192 + 1024;            // staging: S 8 KB + zv 1 KB
+constexpr uint32_t kStagingBuf = 2 * kStagePart;        // hi and lo
+constexpr uint32_t kTmemCols = 256;                     // two 128-column accumulators
+constexpr int kN = 80;                                  // MMA N: 64 value features + 16 ones
 
 // Shared-memory layout.  kLo adds the low bf16 residual of phi(K) as a third
 // tile per stage (MALA); the stage count shrinks to keep everything resident.
@@ -49,7 +55,7 @@ struct Layout {
   static constexpr int kStages = kLo ? 3 : 4;
   static constexpr uint32_t kStageBytes = (kLo ? 3 : 2) * kTile;  // K, V [, K lo]
   static constexpr uint32_t kOnesA = kStages * kStageBytes;         // ones tile of A (rows 64..127)
-  static constexpr uint32_t kOnesB = kOnesA + kTile;                // ones tile of B (cols 64..127)
+  static constexpr uint32_t kOnesB = kOnesA + kTile;                // ones tile of B (cols 64..79)
   static constexpr uint32_t kStaging = kOnesB + kTile;              // 2 staging buffers
   static constexpr uint32_t kBars = kStaging + 2 * kStagingBuf;
   static constexpr uint32_t kSmemBytes = kBars + 256 + 1024;        // + barriers + alignment slack
@@ -64,28 +70,6 @@ struct SummaryArgs {
   ChunkShape c;
   unsigned int* err;
 };
-
-__device__ __forceinline__ float phi_fast(float x, int fmap) {
-  if (fmap == MHLA_FEATURE_IDENTITY) return x;
-  return x > 0.f ? x + 1.f : __expf(x);
-}
-
-__device__ __forceinline__ uint32_t phi_pair(uint32_t w, int fmap) {
-  __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162*>(&w);
-  float2 f = __bfloat1622float2(h);
-  return pack_bf16x2(phi_fast(f.x, fmap), phi_fast(f.y, fmap));
-}
-
-// phi of two bf16 values as bf16 (returned) plus the low bf16 residual.
-__device__ __forceinline__ uint32_t phi_pair_lo(uint32_t w, int fmap, uint32_t& lo) {
-  __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162*>(&w);
-  float2 f = __bfloat1622float2(h);
-  const float a = phi_fast(f.x, fmap), b = phi_fast(f.y, fmap);
-  const uint32_t hi = pack_bf16x2(a, b);
-  float2 g = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&hi));
-  lo = pack_bf16x2(a - g.x, b - g.y);
-  return hi;
-}
 
 struct UnitCoord {
   int u, b, c0, c1;
@@ -117,28 +101,56 @@ __device__ __forceinline__ void chunk_origin(const Plan& p, const ChunkShape& ch
   t0 = bz * p.bt + cz * ch.ct;
 }
 
+// phi of 8 bf16 (one 16-byte chunk), rounded to bf16; optionally also the
+// low bf16 residual.
+template <bool kLo>
+__device__ __forceinline__ void phi_chunk(uint4& x, uint4& lo, int fmap) {
+  uint32_t* xp = &x.x;
+  uint32_t* lp = &lo.x;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float2 f = bf16x2_to_float2(xp[q]);
+    const float a = phi_map(f.x, fmap), b = phi_map(f.y, fmap);
+    xp[q] = pack_bf16x2(a, b);
+    if (kLo) {
+      const float2 g = bf16x2_to_float2(xp[q]);
+      lp[q] = pack_bf16x2(a - g.x, b - g.y);
+    }
+  }
+}
+
+// 8 floats (times scale) -> 8 bf16 (hi) and optionally their low residuals.
+__device__ __forceinline__ void split8(const float* src, uint4& hv, uint4& lv, float scale, bool want_lo) {
+  uint32_t* hp = &hv.x;
+  uint32_t* lp = &lv.x;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float x0 = src[2 * q] * scale, x1 = src[2 * q + 1] * scale;
+    hp[q] = pack_bf16x2(x0, x1);
+    if (want_lo) {
+      const float2 g = bf16x2_to_float2(hp[q]);
+      lp[q] = pack_bf16x2(x0 - g.x, x1 - g.y);
+    }
+  }
+}
+
 template <bool kLo>
 __global__ void __launch_bounds__(kThreads, 1) tc_summary_kernel(const __grid_constant__ SummaryArgs a, const Plan p) {
   using L = Layout<kLo>;
   constexpr int kStages = L::kStages;
   constexpr uint32_t kStageBytes = L::kStageBytes;
-  constexpr uint32_t kOnesA = L::kOnesA;
-  constexpr uint32_t kOnesB = L::kOnesB;
-  constexpr uint32_t kStaging = L::kStaging;
-  constexpr uint32_t kBars = L::kBars;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gb = smem_raw + (base - raw);
-  const uint32_t bars = base + kBars;
-  // barrier addresses
+  const uint32_t bars = base + L::kBars;
   auto full = [&](int s) { return bars + 8u * s; };
   auto kready = [&](int s) { return bars + 8u * (kStages + s); };
   auto empty = [&](int s) { return bars + 8u * (2 * kStages + s); };
   auto accfull = [&](int x) { return bars + 8u * (3 * kStages + x); };
   auto accempty = [&](int x) { return bars + 8u * (3 * kStages + 2 + x); };
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gb + kBars + 8 * (3 * kStages + 4));
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(gb + kBars + 8 * (3 * kStages + 4) + 8);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gb + L::kBars + 8 * (3 * kStages + 4));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gb + L::kBars + 8 * (3 * kStages + 4) + 8);
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -146,21 +158,21 @@ __global__ void __launch_bounds__(kThreads, 1) tc_summary_kernel(const __grid_co
 
   // Stage tiles start zeroed (padding rows must stay zero); the ones tiles
   // hold 1.0 in every valid row.
-  for (uint32_t off = threadIdx.x * 16u; off < kStaging; off += kThreads * 16u) {
+  for (uint32_t off = threadIdx.x * 16u; off < L::kStaging; off += kThreads * 16u) {
     uint4 val = make_uint4(0u, 0u, 0u, 0u);
-    if (off >= kOnesA && ((off - kOnesA) % kTile) / 128u < (uint32_t)rows)
+    if (off >= L::kOnesA && ((off - L::kOnesA) % kTile) / 128u < (uint32_t)rows)
       val = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
     *reinterpret_cast<uint4*>(gb + off) = val;
   }
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(full(s), 1);
-      mbar_init(kready(s), 128);
+      mbar_init(kready(s), kXfThreads);
       mbar_init(empty(s), 1);
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(accfull(x), 1);
-      mbar_init(accempty(x), 128);
+      mbar_init(accempty(x), kEpiThreads);
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -207,7 +219,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_summary_kernel(const __grid_co
   } else if (warp == 1) {
     // --------------------------------------------------------------- MMA
     if (lane == 0) {
-      const uint32_t idesc = idesc_bf16_f32(128, 128, true, true);
+      const uint32_t idesc = idesc_bf16_f32(128, kN, true, true);
       const int ksteps = a.c.rows_pad / 16;
       int stage = 0, acc = 0;
       uint32_t phase = 0, accph = 0;
@@ -222,16 +234,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc_summary_kernel(const __grid_co
           tc_fence_after();
           const uint32_t kt = base + (uint32_t)stage * kStageBytes;
           const uint32_t vt = kt + kTile;
-          const uint32_t lbo_a = base + kOnesA - kt;
-          const uint32_t lbo_b = base + kOnesB - vt;
+          const uint32_t lbo_a = base + L::kOnesA - kt;
+          const uint32_t lbo_b = base + L::kOnesB - vt;
           for (int ks = 0; ks < ksteps; ++ks) {
             const uint64_t bd = sdesc_sw128(vt + (uint32_t)ks * 2048u, lbo_b, 1024u);
             umma_bf16(d, sdesc_sw128(kt + (uint32_t)ks * 2048u, lbo_a, 1024u), bd, idesc,
                       (c > uc.c0 || ks > 0) ? 1u : 0u);
             if (kLo) {
-              // [phi(K) lo ; ones]: rows 64..127 of D collect v_b a second time
               const uint32_t klo = kt + 2 * kTile;
-              umma_bf16(d, sdesc_sw128(klo + (uint32_t)ks * 2048u, base + kOnesA - klo, 1024u), bd, idesc, 1u);
+              umma_bf16(d, sdesc_sw128(klo + (uint32_t)ks * 2048u, base + L::kOnesA - klo, 1024u), bd, idesc, 1u);
             }
           }
           umma_commit(empty(stage));
@@ -248,9 +259,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_summary_kernel(const __grid_co
         }
       }
     }
-  } else if (warp >= 4 && warp < 8) {
+  } else if (warp >= 8) {
     // ------------------------------------------------ phi(K) transform
-    const int t = threadIdx.x - 128;
+    // thread t: row t/2, chunks 4*(t%2) .. +3 at physical positions rotated
+    // by the row so that 8 consecutive threads hit 8 distinct bank groups
+    const int t = threadIdx.x - 256;
+    const int row = t >> 1;
+    const int half = t & 1;
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
@@ -258,27 +273,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_summary_kernel(const __grid_co
       const UnitCoord uc = unit_coord(p, a, w);
       for (int c = uc.c0; c < uc.c1; ++c) {
         if (!(ok = mbar_wait(full(stage), phase, a.err, 0x104, abort_flag))) break;
-        if (t < rows) {
-          uint8_t* row = gb + stage * kStageBytes + t * 128;
+        if (row < rows) {
+          uint8_t* rp = gb + stage * kStageBytes + row * 128;
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const uint32_t off = ((j + t) & 7) << 4;
-            uint4* ptr = reinterpret_cast<uint4*>(row + off);
-            uint4 x = *ptr;
-            if (kLo) {
-              uint4 lo;
-              x.x = phi_pair_lo(x.x, p.fmap, lo.x);
-              x.y = phi_pair_lo(x.y, p.fmap, lo.y);
-              x.z = phi_pair_lo(x.z, p.fmap, lo.z);
-              x.w = phi_pair_lo(x.w, p.fmap, lo.w);
-              *reinterpret_cast<uint4*>(row + 2 * kTile + off) = lo;
-            } else {
-              x.x = phi_pair(x.x, p.fmap);
-              x.y = phi_pair(x.y, p.fmap);
-              x.z = phi_pair(x.z, p.fmap);
-              x.w = phi_pair(x.w, p.fmap);
-            }
-            *ptr = x;
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t off = ((4 * half + j + row) & 7) << 4;
+            uint4 x = *reinterpret_cast<uint4*>(rp + off);
+            uint4 lo;
+            phi_chunk<kLo>(x, lo, p.fmap);
+            *reinterpret_cast<uint4*>(rp + off) = x;
+            if (kLo) *reinterpret_cast<uint4*>(rp + 2 * kTile + off) = lo;
           }
         }
         fence_proxy_async();
@@ -289,10 +293,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_summary_kernel(const __grid_co
         }
       }
     }
-  } else if (warp >= 8) {
+  } else if (warp >= 4 && warp < 7) {
     // ------------------------------------------------------------ epilogue
-    const int e = warp - 8;
-    const int et = threadIdx.x - 256;
+    const int e = warp - 4;
+    const int et = threadIdx.x - 128;
     const int r = 32 * e + lane;  // TMEM lane = row of D
     int acc = 0, it = 0;
     uint32_t accph = 0;
@@ -300,15 +304,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_summary_kernel(const __grid_co
     for (int w = blockIdx.x; w < a.units && ok; w += gridDim.x, ++it) {
       const UnitCoord uc = unit_coord(p, a, w);
       ok = mbar_wait(accfull(acc), accph, a.err, 0x105, abort_flag);
-      if (!(ok = named_all(1, 128, ok))) break;
+      if (!(ok = named_all(1, kEpiThreads, ok))) break;
       tc_fence_after();
       const uint32_t taddr = tmem + (uint32_t)acc * 128u + ((uint32_t)(32 * e) << 16);
-      float s0[32], s1[32], zz[32];
-      if (e < 3) {
-        tmem_ld32(taddr, s0);
-        tmem_ld32(taddr + 32u, s1);
-      }
-      if (e < 2) tmem_ld32(taddr + 64u, zz);
+      float s0[32], s1[32], zval = 0.f, znext;
+      tmem_ld32(taddr, s0);
+      tmem_ld32(taddr + 32u, s1);
+      tmem_ld2(taddr + 64u, zval, znext);
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(accempty(acc));
@@ -317,61 +319,39 @@ __global__ void __launch_bounds__(kThreads, 1) tc_summary_kernel(const __grid_co
         accph ^= 1u;
       }
 
-      uint8_t* st_hi = gb + kStaging + (it & 1) * kStagingBuf;
+      uint8_t* st_hi = gb + L::kStaging + (it & 1) * kStagingBuf;
       uint8_t* st_lo = st_hi + kStagePart;
       if (et == 0) bulk_wait_read<1>();
-      named_sync(1, 128);
+      named_sync(1, kEpiThreads);
       if (e < 2) {
-        // row r of S (= summary row k) and z[k]
+        // row r of S_b and z_b[r]
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          const float* src = j < 4 ? &s0[8 * j] : &s1[8 * (j - 4)];
           uint4 hv, lv;
-          uint32_t* hp = &hv.x;
-          uint32_t* lp = &lv.x;
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const float x0 = src[2 * q], x1 = src[2 * q + 1];
-            hp[q] = pack_bf16x2(x0, x1);
-            if (a.write_lo) {
-              __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162*>(&hp[q]);
-              float2 hf = __bfloat1622float2(h);
-              lp[q] = pack_bf16x2(x0 - hf.x, x1 - hf.y);
-            }
-          }
+          split8(j < 4 ? &s0[8 * j] : &s1[8 * (j - 4)], hv, lv, 1.f, a.write_lo);
           const uint32_t off = (uint32_t)r * 128u + ((uint32_t)((j ^ (r & 7)) & 7) << 4);
           *reinterpret_cast<uint4*>(st_hi + off) = hv;
           if (a.write_lo) *reinterpret_cast<uint4*>(st_lo + off) = lv;
         }
-        const __nv_bfloat16 zh = __float2bfloat16_rn(zz[0]);
+        const __nv_bfloat16 zh = __float2bfloat16_rn(zval);
         *reinterpret_cast<__nv_bfloat16*>(st_hi + 8192 + sw128_offset(0, r)) = zh;
         if (a.write_lo)
           *reinterpret_cast<__nv_bfloat16*>(st_lo + 8192 + sw128_offset(0, r)) =
-              __float2bfloat16_rn(zz[0] - __bfloat162float(zh));
-      } else if (e == 2 && lane == 0) {
-        // row 64 of D: v_b (every row 64..127 holds the same values)
+              __float2bfloat16_rn(zval - __bfloat162float(zh));
+      } else if (lane == 0) {
+        // row 64 of D: v_b (every row 64..127 holds the same values; the
+        // low-residual MMA of MALA adds them twice)
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          const float* src = j < 4 ? &s0[8 * j] : &s1[8 * (j - 4)];
           uint4 hv, lv;
-          uint32_t* hp = &hv.x;
-          uint32_t* lp = &lv.x;
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const float vscale = kLo ? 0.5f : 1.f;  // the lo MMA adds v_b a second time
-            const float x0 = src[2 * q] * vscale, x1 = src[2 * q + 1] * vscale;
-            hp[q] = pack_bf16x2(x0, x1);
-            __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162*>(&hp[q]);
-            float2 hf = __bfloat1622float2(h);
-            lp[q] = pack_bf16x2(x0 - hf.x, x1 - hf.y);
-          }
+          split8(j < 4 ? &s0[8 * j] : &s1[8 * (j - 4)], hv, lv, kLo ? 0.5f : 1.f, true);
           const uint32_t off = 128u + ((uint32_t)((j ^ 1) & 7) << 4);
           *reinterpret_cast<uint4*>(st_hi + 8192 + off) = hv;
           if (a.write_lo) *reinterpret_cast<uint4*>(st_lo + 8192 + off) = lv;
         }
       }
       fence_proxy_async();
-      named_sync(1, 128);
+      named_sync(1, kEpiThreads);
       if (et == 0) {
         const int row0 = ((uc.u * p.M + uc.b) * a.splits + (uc.c0 / a.cpp)) * 66;
         tma_store_2d(&a.tmS_hi, smem_u32(st_hi), 0, row0);
@@ -390,6 +370,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_summary_kernel(const __grid_co
   tc_fence_before();
   __syncthreads();
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+template <bool kLo>
+int launch_variant(const SummaryArgs& a, const Plan& p, cudaStream_t s) {
+  const uint32_t smem = Layout<kLo>::kSmemBytes;
+  cudaError_t ce = cudaFuncSetAttribute(tc_summary_kernel<kLo>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (ce != cudaSuccess) return (int)ce;
+  const int grid = a.units < num_sms() ? a.units : num_sms();
+  tc_summary_kernel<kLo><<<grid, kThreads, smem, s>>>(a, p);
+  return (int)cudaGetLastError();
 }
 
 }  // namespace
@@ -420,19 +410,7 @@ int launch_tc_summary(const Plan& p, const ChunkShape& c, const void* k, const v
   a.units = p.BH * p.M * p.splits;
   a.c = c;
   a.err = p.err;
-  const int grid = a.units < num_sms() ? a.units : num_sms();
-  if (a.write_lo) {
-    const uint32_t smem = Layout<true>::kSmemBytes;
-    cudaError_t ce = cudaFuncSetAttribute(tc_summary_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (ce != cudaSuccess) return (int)ce;
-    tc_summary_kernel<true><<<grid, kThreads, smem, s>>>(a, p);
-  } else {
-    const uint32_t smem = Layout<false>::kSmemBytes;
-    cudaError_t ce = cudaFuncSetAttribute(tc_summary_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (ce != cudaSuccess) return (int)ce;
-    tc_summary_kernel<false><<<grid, kThreads, smem, s>>>(a, p);
-  }
-  return (int)cudaGetLastError();
+  return a.write_lo ? launch_variant<true>(a, p, s) : launch_variant<false>(a, p, s);
 }
 
 }  // namespace mhla
