@@ -133,17 +133,28 @@ class ClockSampler:
 # ------------------------------------------------------------ my arm
 
 def phase_bytes(w: wl.Workload, info, variant: int):
-    """Compulsory bytes of each phase kernel: its inputs read once, outputs written once."""
+    """Compulsory bytes of each phase: its inputs read once, its outputs
+    written once, in the layouts the variant uses (SIMT: float32 stack and
+    mixed summaries; tensor cores: fp16 or bf16 S stack, bf16 hi+lo z/v
+    stack, bf16 mixed summaries with low residuals where the output needs
+    them)."""
     import token_level_head_phi_gb300.binding as mb
     el = 2 if w.dtype == "bf16" else 4
     U, N, d, M = w.units, w.n_tokens, w.head_dim, w.n_blocks
     R = d * d + 2 * d
-    st_el = 4 if variant == mb.VARIANT_SIMT else 2
     rows = M * info.summary_splits
     io = U * N * d * el
-    stack = U * rows * R * st_el
-    mixed = U * M * R * st_el
-    return {"summary": 2 * io + stack, "mix": stack + mixed + 4 * M * M, "output": io + mixed + io}
+    if variant == mb.VARIANT_SIMT:
+        stack = U * rows * R * 4
+        mixed_w = mixed_r = U * M * R * 4
+        mc = 4 * M * M
+    else:
+        mala = w.norm == "mala"
+        stack = U * rows * (d * d * 2 * (2 if mala else 1) + 2 * d * 2 * 2)
+        mixed_w = U * M * (R * 2 + (R if mala else 2 * d) * 2)
+        mixed_r = U * M * (d * d * 2 * (2 if mala else 1) + 2 * d * 2 * 2)
+        mc = 4 * M * M
+    return {"summary": 2 * io + stack, "mix": stack + mixed_w + mc, "output": io + mixed_r + io}
 
 
 def traffic_table():
@@ -177,6 +188,9 @@ PHASE_KERNEL = {  # variant -> phase -> (kernel name in ncu, source file)
     1: {"summary": ("simt_summary_kernel", "token_level_head_phi_gb300/csrc/simt.cu"),
         "mix": ("simt_mix_kernel", "token_level_head_phi_gb300/csrc/simt.cu"),
         "output": ("simt_output_kernel", "token_level_head_phi_gb300/csrc/simt.cu")},
+    2: {"summary": ("tc_summary_kernel", "token_level_head_phi_gb300/csrc/tc_summary.cu"),
+        "mix": ("tc_mix_kernel", "token_level_head_phi_gb300/csrc/tc_mix.cu"),
+        "output": ("tc_output_kernel", "token_level_head_phi_gb300/csrc/tc_output.cu")},
 }
 
 

@@ -63,7 +63,8 @@ typedef enum mhla_status {
   MHLA_ERR_UNSUPPORTED = 2,     /* valid request this build cannot run        */
   MHLA_ERR_WORKSPACE = 3,       /* workspace missing or smaller than required */
   MHLA_ERR_CUDA = 4,            /* a CUDA runtime call failed                  */
-  MHLA_ERR_DEVICE_TIMEOUT = 5   /* a kernel's bounded wait expired             */
+  MHLA_ERR_DEVICE_TIMEOUT = 5,  /* a kernel's bounded wait expired             */
+  MHLA_ERR_OVERFLOW = 6         /* an intermediate left the fp16 range (device) */
 } mhla_status;
 
 typedef enum mhla_dtype { MHLA_DTYPE_BF16 = 0, MHLA_DTYPE_F32 = 1 } mhla_dtype;
@@ -77,7 +78,15 @@ typedef enum mhla_norm { MHLA_NORM_DIVISIVE = 0, MHLA_NORM_MALA = 1, MHLA_NORM_N
 /* AUTO picks MULTIPASS for bf16 with d = 64, SIMT otherwise.
  * SIMT:      CUDA-core kernels, float32 arithmetic, any supported d, both dtypes.
  * MULTIPASS: tcgen05/TMEM tensor-core kernels fed by TMA (bf16, d = 64):
- *            block summaries -> mixing GEMM -> output with fused epilogue. */
+ *            block summaries -> mixing GEMM -> output with fused epilogue.
+ *            For the DIVISIVE and NONE norms the mixing multiplies fp16
+ *            operands: each block summary is scaled by 2^-ceil(log2 n) (n
+ *            tokens per summary piece) and each Mc row by a power of two
+ *            that brings its largest entry into [0.5, 1].  A summary entry
+ *            that still leaves the fp16 range (a single token with
+ *            |phi(K)[k] V[c]| >= 65504) is recorded on the device as
+ *            MHLA_ERR_OVERFLOW (see mhla_device_status); MALA and SIMT have
+ *            no such limit. */
 typedef enum mhla_variant {
   MHLA_VARIANT_AUTO = 0,
   MHLA_VARIANT_SIMT = 1,
@@ -147,9 +156,10 @@ mhla_status mhla_forward_host(const void* q, const void* k, const void* v, const
                               size_t dev_buffer_bytes, void* stream);
 
 /* Reads and clears the device error word of the current device.  Blocks the
- * host until the device is idle.  *code receives MHLA_OK or the status a
- * kernel recorded (MHLA_ERR_DEVICE_TIMEOUT); *detail receives a kernel-
- * specific location code (0 if none).  Either pointer may be NULL. */
+ * host until the device is idle.  *code receives MHLA_OK or the first status
+ * a kernel recorded (MHLA_ERR_DEVICE_TIMEOUT, MHLA_ERR_OVERFLOW); *detail
+ * receives a kernel-specific location code (0 if none).  Either pointer may
+ * be NULL. */
 mhla_status mhla_device_status(int* code, int* detail);
 
 /* Timing hook.  With n == MHLA_NUM_PHASE_EVENTS, each later mhla_forward

@@ -45,7 +45,7 @@ def test_binding_declares_every_header_function():
 
 def test_abi_version_and_strings(lib):
     assert mb.mhla_abi_version() == 1
-    for s in range(6):
+    for s in range(7):
         assert mb.mhla_status_string(s).startswith("MHLA")
     assert "unknown" in mb.mhla_status_string(42)
 

@@ -23,6 +23,7 @@ MHLA_ERR_UNSUPPORTED = 2
 MHLA_ERR_WORKSPACE = 3
 MHLA_ERR_CUDA = 4
 MHLA_ERR_DEVICE_TIMEOUT = 5
+MHLA_ERR_OVERFLOW = 6
 
 DTYPE_BF16 = 0
 DTYPE_F32 = 1

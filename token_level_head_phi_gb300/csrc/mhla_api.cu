@@ -2,6 +2,7 @@
 // planning, workspace layout and dispatch to the kernels.
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -130,6 +131,10 @@ mhla_status make_plan(const mhla_params* prm, Plan* p) {
     p->splits = (nck + p->cpp - 1) / p->cpp;
     p->split_len = p->cpp * p->chunk.rows;
     p->Qp = (p->M * p->splits + 7) / 8 * 8;
+    p->f16_mix = p->norm != MHLA_NORM_MALA;
+    int lg = 0;
+    while ((1 << lg) < p->split_len) ++lg;
+    p->stack_scale = ldexpf(1.f, -lg);
   }
 
   if (p->BH == 0) {
@@ -146,22 +151,34 @@ mhla_status make_plan(const mhla_params* prm, Plan* p) {
     p->off_rowsum = off;
     off = align_up(off + sizeof(float) * (size_t)p->M);
   } else {
-    const size_t stack = 2 * (size_t)p->BH * p->M * p->splits * p->R;
+    const size_t rows = (size_t)p->BH * p->M * p->splits;
+    const size_t stack_s = 2 * rows * d * d;
+    const size_t stack_aux = 2 * rows * 2 * d;
     const size_t mixed = 2 * (size_t)p->BH * p->M * p->R;
+    const size_t mcq = 2 * (size_t)p->M * p->Qp;
     p->off_stack = off;
-    off = align_up(off + stack);
+    off = align_up(off + stack_s);
     p->off_stack_lo = off;
-    if (p->norm == MHLA_NORM_MALA) off = align_up(off + stack);
+    if (p->norm == MHLA_NORM_MALA) off = align_up(off + stack_s);
+    p->off_aux_hi = off;
+    off = align_up(off + stack_aux);
+    p->off_aux_lo = off;
+    off = align_up(off + stack_aux);
     p->off_mixed = off;
     off = align_up(off + mixed);
     p->off_mixed_lo = off;
     off = align_up(off + mixed);
-    p->off_mc_exp = off;
-    off = align_up(off + 2 * (size_t)p->M * p->Qp);
-    p->off_mc_exp_lo = off;
-    off = align_up(off + 2 * (size_t)p->M * p->Qp);
+    p->off_mc_f16 = off;
+    off = align_up(off + mcq);
+    p->off_mc_hi = off;
+    off = align_up(off + mcq);
+    p->off_mc_lo = off;
+    off = align_up(off + mcq);
+    p->off_mc_scale = off;
+    off = align_up(off + sizeof(float) * (size_t)p->M);
     p->off_rowsum = off;
     off = align_up(off + sizeof(float) * (size_t)p->M);
+    p->kernels = 5;
   }
   p->off_aux = off;
   p->ws_total = off;
@@ -189,19 +206,26 @@ mhla_status run_plan(const Plan& plan, const void* q, const void* k, const void*
   int e;
   if (p.variant == MHLA_VARIANT_MULTIPASS) {
     TcBuffers b;
-    b.stack_hi = reinterpret_cast<__nv_bfloat16*>(ws + p.off_stack);
-    b.stack_lo = p.norm == MHLA_NORM_MALA ? reinterpret_cast<__nv_bfloat16*>(ws + p.off_stack_lo) : nullptr;
+    b.stack_s = ws + p.off_stack;
+    b.stack_s_lo = p.norm == MHLA_NORM_MALA ? reinterpret_cast<__nv_bfloat16*>(ws + p.off_stack_lo) : nullptr;
+    b.aux_hi = reinterpret_cast<__nv_bfloat16*>(ws + p.off_aux_hi);
+    b.aux_lo = reinterpret_cast<__nv_bfloat16*>(ws + p.off_aux_lo);
     b.mixed_hi = reinterpret_cast<__nv_bfloat16*>(ws + p.off_mixed);
     b.mixed_lo = reinterpret_cast<__nv_bfloat16*>(ws + p.off_mixed_lo);
-    b.mc_exp = reinterpret_cast<__nv_bfloat16*>(ws + p.off_mc_exp);
-    b.mc_exp_lo = reinterpret_cast<__nv_bfloat16*>(ws + p.off_mc_exp_lo);
+    b.mc_f16 = reinterpret_cast<__half*>(ws + p.off_mc_f16);
+    b.mc_scale = reinterpret_cast<float*>(ws + p.off_mc_scale);
+    b.mc_hi = reinterpret_cast<__nv_bfloat16*>(ws + p.off_mc_hi);
+    b.mc_lo = reinterpret_cast<__nv_bfloat16*>(ws + p.off_mc_lo);
     b.rowsum = reinterpret_cast<float*>(ws + p.off_rowsum);
     b.Qp = p.Qp;
+    b.f16 = p.f16_mix != 0;
+    b.stack_scale = b.f16 ? p.stack_scale : 1.f;
     record_event(0, s);
     if ((e = launch_tc_prep(p, mc, b, s)) != 0) return cuda_fail((cudaError_t)e);
     if ((e = launch_tc_summary(p, p.chunk, k, v, b, s)) != 0) return cuda_fail((cudaError_t)e);
     record_event(1, s);
-    if ((e = launch_tc_mix(p, b, s)) != 0) return cuda_fail((cudaError_t)e);
+    if ((e = launch_tc_mix(p, b, false, s)) != 0) return cuda_fail((cudaError_t)e);
+    if ((e = launch_tc_mix(p, b, true, s)) != 0) return cuda_fail((cudaError_t)e);
     record_event(2, s);
     if ((e = launch_tc_output(p, p.chunk, q, b, out, s)) != 0) return cuda_fail((cudaError_t)e);
     record_event(3, s);
@@ -370,6 +394,7 @@ const char* mhla_status_string(mhla_status s) {
     case MHLA_ERR_WORKSPACE: return "MHLA_ERR_WORKSPACE: workspace missing or too small";
     case MHLA_ERR_CUDA: return "MHLA_ERR_CUDA: a CUDA runtime call failed";
     case MHLA_ERR_DEVICE_TIMEOUT: return "MHLA_ERR_DEVICE_TIMEOUT: a kernel's bounded wait expired";
+    case MHLA_ERR_OVERFLOW: return "MHLA_ERR_OVERFLOW: an intermediate left the fp16 range";
   }
   return "MHLA: unknown status";
 }

@@ -48,8 +48,11 @@ struct Plan {
   size_t ws_total;
   size_t off_stack, off_mixed, off_rowsum, off_aux;
   // tensor-core path buffers
-  size_t off_stack_lo, off_mixed_lo, off_mc_exp, off_mc_exp_lo;
+  size_t off_stack_lo, off_aux_hi, off_aux_lo, off_mixed_lo;
+  size_t off_mc_f16, off_mc_scale, off_mc_hi, off_mc_lo;
   int Qp;
+  int f16_mix;        // S part of the mixing in fp16 (DIVISIVE and NONE)
+  float stack_scale;  // 2^-ceil(log2(tokens per piece))
   // device error word (code, detail), set by kernels whose bounded waits
   // expire
   unsigned int* err;

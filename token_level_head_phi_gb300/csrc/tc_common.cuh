@@ -19,6 +19,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -72,9 +73,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Records a timeout in the device error word (first writer wins).
+// Records a status in the device error word (first writer wins).
+__device__ __forceinline__ void report_error(unsigned int* err, unsigned int code, unsigned int where) {
+  if (err && atomicCAS(err, 0u, code) == 0u) atomicExch(err + 1, where);
+}
+
 __device__ __forceinline__ void report_timeout(unsigned int* err, unsigned int where) {
-  if (err && atomicCAS(err, 0u, kErrTimeout) == 0u) atomicExch(err + 1, where);
+  report_error(err, kErrTimeout, where);
 }
 
 // Waits until the phase of `bar` with parity `parity` has completed.  Gives
@@ -220,7 +225,9 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// D[tmem] (+)= A[smem] * B[smem], bf16 inputs, float32 accumulate.
+// D[tmem] (+)= A[smem] * B[smem] with kind::f16: bf16 or fp16 inputs (as the
+// instruction descriptor says; A and B of one MMA share the type), float32
+// accumulate.
 __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                           uint32_t accumulate) {
   asm volatile(
@@ -308,6 +315,12 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn, bool b_mn) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
          ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// Same for fp16 A/B (format 0).
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, bool a_mn, bool b_mn) {
+  return (1u << 4) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
 }
 
 // Byte offset of element (row, col) (col < 64, bf16) inside a 128-byte

@@ -3,6 +3,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -19,28 +20,43 @@ constexpr int kTcTileRows = 128;
 // size must not depend on the device).
 constexpr int kPlanSms = 152;
 
-int encode_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
-                     const uint64_t* strides_bytes, const uint32_t* box);
+// Tiled TMA tensor map with 128-byte swizzle over 2-byte elements (bf16, or
+// fp16 when f16 is set); dims[0] innermost, strides_bytes[i] is the stride of
+// dims[i + 1].
+int encode_tmap(CUtensorMap* map, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
+                const uint32_t* box, bool f16);
+inline int encode_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                            const uint64_t* strides_bytes, const uint32_t* box) {
+  return encode_tmap(map, base, rank, dims, strides_bytes, box, false);
+}
 int num_sms();
 
 ChunkShape choose_chunk(const Plan& p);
 
-// Workspace pointers of the tensor-core path.
+// Workspace pointers of the tensor-core path.  Stack rows are block pieces
+// (Q = M * splits per head).
 struct TcBuffers {
-  __nv_bfloat16* stack_hi;  // [BH][M*splits][R]
-  __nv_bfloat16* stack_lo;  // same, MALA only (else nullptr)
-  __nv_bfloat16* mixed_hi;  // [BH][M][R]
-  __nv_bfloat16* mixed_lo;  // [BH][M][R]
-  __nv_bfloat16* mc_exp;    // [M][Qp] bf16(Mc[i][q / splits])
-  __nv_bfloat16* mc_exp_lo; // [M][Qp] low bf16 residual of the same
-  float* rowsum;            // [M] sum_b (hi + lo)(Mc[i][b])
-  int Qp;                   // padded row pitch of mc_exp
+  void* stack_s;             // [BH][Q][d*d] S_b: fp16 scaled by stack_scale, or bf16 (MALA)
+  __nv_bfloat16* stack_s_lo; // [BH][Q][d*d] low bf16 residual of S_b (MALA only, else nullptr)
+  __nv_bfloat16* aux_hi;     // [BH][Q][2d]  z_b, v_b (bf16 high parts)
+  __nv_bfloat16* aux_lo;     // [BH][Q][2d]  low residuals
+  __nv_bfloat16* mixed_hi;   // [BH][M][R]   S~_i, z~_i, v~_i high parts
+  __nv_bfloat16* mixed_lo;   // [BH][M][R]   low residuals (S~ part for MALA only)
+  __half* mc_f16;            // [M][Qp] Mc[i][q / splits] * 2^-e_i in fp16
+  float* mc_scale;           // [M] 2^e_i (power of two with max_b |Mc[i][b]| <= 2^e_i)
+  __nv_bfloat16* mc_hi;      // [M][Qp] bf16(Mc[i][q / splits])
+  __nv_bfloat16* mc_lo;      // [M][Qp] low bf16 residual of the same
+  float* rowsum;             // [M] sum_b (hi + lo)(Mc[i][b])
+  int Qp;                    // padded row pitch of the Mc copies
+  bool f16;                  // S part of the stack in fp16 (DIVISIVE and NONE)
+  float stack_scale;         // 2^-ceil(log2(tokens per piece))
 };
 
 int launch_tc_prep(const Plan& p, const float* mc, const TcBuffers& b, cudaStream_t s);
 int launch_tc_summary(const Plan& p, const ChunkShape& c, const void* k, const void* v, const TcBuffers& b,
                       cudaStream_t s);
-int launch_tc_mix(const Plan& p, const TcBuffers& b, cudaStream_t s);
+// Mixing of the S part (fp16 or split bf16) and of the z/v part (split bf16).
+int launch_tc_mix(const Plan& p, const TcBuffers& b, bool aux_part, cudaStream_t s);
 int launch_tc_output(const Plan& p, const ChunkShape& c, const void* q, const TcBuffers& b, void* out,
                      cudaStream_t s);
 

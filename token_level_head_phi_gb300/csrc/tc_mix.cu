@@ -2,20 +2,24 @@
 // Linear Attention via Token-Level Multi-Head", key design 2: the mixing is a
 // single product of Mc with the stack of block summaries).
 //
-// Per head, with the stack X [Q][R] (one row of R = d*d + 2d values per block
-// piece: S_b, z_b, v_b) and McExp [M][Q] (McExp[i][q] = Mc[i][q / splits]):
-//     Mixed[i][r] = sum_q McExp[i][q] X[q][r]
-// computed transposed so that the long R axis fills the 128-row MMA:
+// Per head, with a stack X [Q][W] (one row per block piece) and
+// McExp [M][Q] (McExp[i][q] = Mc[i][q / splits]):
+//     Mixed[i][r0 + r] = sum_q McExp[i][q] X[q][r]
+// computed transposed so that the long r axis fills the 128-row MMA:
 //     D[r][i] = sum_q X^T[r][q] McExp^T[q][i]
 //   A = X^T  : MN-major (r contiguous), two 64-wide atoms per 128-row tile
 //   B = McExp: K-major (q contiguous), N = up to 256 query blocks per tile
-// so every Mc element is read once per (head, 128-row tile) and the epilogue
-// writes Mixed with each warp storing 32 consecutive r of one query block.
-// The MALA norm adds the low bf16 residual of X as a second A operand.
+// Two precisions:
+//   kF16  (S part, DIVISIVE/NONE): X = fp16(S * 2^-s), B = fp16(Mc * 2^-e_i);
+//         one MMA per K step, D rescaled by 2^(s + e_i) in the epilogue.
+//   split (z/v part always, S part for MALA): X and Mc as bf16 high + low
+//         parts, D = Xh Mh + Xh Ml + Xl Mh.
+// The epilogue writes Mixed as bf16 (plus the low residual where the output
+// step needs it), each warp storing 32 consecutive r of one query block.
 //
-// Also here: the small preparation kernel that rounds Mc to bf16, expands it
-// over summary pieces and sums its rows (n~_i = n_b * sum_b bf16(Mc[i,b])).
+// Also here: the small preparation kernel that builds the Mc copies.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <cstring>
@@ -39,18 +43,21 @@ constexpr uint32_t kSmemBytes = kBars + 256 + 1024;
 constexpr uint32_t kTmemCols = 512;                 // two accumulators of up to 256 columns
 
 struct MixArgs {
-  CUtensorMap tmA_hi, tmA_lo;  // 3D (R, Q, BH), box (64, 64, 1)
-  CUtensorMap tmB_hi, tmB_lo;  // 2D (Q, M),     box (64, NT)
+  CUtensorMap tmA, tmA_lo;     // 3D (W, Q, BH), box (64, 64, 1)
+  CUtensorMap tmB, tmB_lo;     // 2D (Q, M),     box (64, NT)
   __nv_bfloat16* mixed_hi;
   __nv_bfloat16* mixed_lo;
+  const float* col_scale;      // kF16: 2^e_i per query block i
+  float inv_stack_scale;       // kF16: 2^s
   int Q, NT, itiles, rtiles, kchunks, units;
-  int use_lo_in;   // extra MMA with the low residual of the stack (MALA)
-  int write_lo_s;  // write the low residual of S~ (aux rows always get one)
-  int stages;      // pipeline depth (<= kMaxStages)
-  uint32_t stage_bytes, off_alo, off_bhi, off_blo;
+  int r_off;                   // column of Mixed where this part starts
+  int write_lo;                // write the low residual of every value
+  int stages;
+  uint32_t stage_bytes, off_alo, off_b, off_blo;
   unsigned int* err;
 };
 
+template <bool kF16>
 __global__ void __launch_bounds__(kThreads, 1) tc_mix_kernel(const __grid_constant__ MixArgs a, const Plan p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -81,9 +88,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_mix_kernel(const __grid_consta
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&a.tmA_hi);
-    tma_prefetch_desc(&a.tmB_hi);
-    tma_prefetch_desc(&a.tmB_lo);
+    tma_prefetch_desc(&a.tmA);
+    tma_prefetch_desc(&a.tmB);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
@@ -100,7 +106,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_mix_kernel(const __grid_consta
       // ---------------------------------------------------------- producer
       const uint64_t pol_a = policy_evict_first();
       const uint64_t pol_b = policy_evict_last();
-      const uint32_t bytes = kATile * (a.use_lo_in ? 2u : 1u) + 2u * (uint32_t)a.NT * 128u;
+      const uint32_t bytes = kF16 ? kATile + (uint32_t)a.NT * 128u : 2u * kATile + 2u * (uint32_t)a.NT * 128u;
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -113,14 +119,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_mix_kernel(const __grid_consta
           if (!(ok = mbar_wait(empty(stage), phase ^ 1u, a.err, 0x201, abort_flag))) break;
           const uint32_t st = base + (uint32_t)stage * a.stage_bytes;
           mbar_arrive_expect_tx(full(stage), bytes);
-          tma_load_3d(st, &a.tmA_hi, full(stage), r0, kc * 64, u, pol_a);
-          tma_load_3d(st + kAtom, &a.tmA_hi, full(stage), r0 + 64, kc * 64, u, pol_a);
-          if (a.use_lo_in) {
+          tma_load_3d(st, &a.tmA, full(stage), r0, kc * 64, u, pol_a);
+          tma_load_3d(st + kAtom, &a.tmA, full(stage), r0 + 64, kc * 64, u, pol_a);
+          tma_load_2d(st + a.off_b, &a.tmB, full(stage), kc * 64, i0, pol_b);
+          if (!kF16) {
             tma_load_3d(st + a.off_alo, &a.tmA_lo, full(stage), r0, kc * 64, u, pol_a);
             tma_load_3d(st + a.off_alo + kAtom, &a.tmA_lo, full(stage), r0 + 64, kc * 64, u, pol_a);
+            tma_load_2d(st + a.off_blo, &a.tmB_lo, full(stage), kc * 64, i0, pol_b);
           }
-          tma_load_2d(st + a.off_bhi, &a.tmB_hi, full(stage), kc * 64, i0, pol_b);
-          tma_load_2d(st + a.off_blo, &a.tmB_lo, full(stage), kc * 64, i0, pol_b);
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
@@ -131,7 +137,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_mix_kernel(const __grid_consta
   } else if (warp == 1) {
     if (lane == 0) {
       // --------------------------------------------------------------- MMA
-      const uint32_t idesc = idesc_bf16_f32(128, a.NT, true, false);
+      const uint32_t idesc = kF16 ? idesc_f16_f32(128, a.NT, true, false) : idesc_bf16_f32(128, a.NT, true, false);
       int stage = 0, acc = 0;
       uint32_t phase = 0, accph = 0;
       bool ok = true;
@@ -145,15 +151,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc_mix_kernel(const __grid_consta
           const uint32_t st = base + (uint32_t)stage * a.stage_bytes;
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) {
-            // X_hi Mc_hi + X_hi Mc_lo (+ X_lo Mc_hi): Mc carries its low bf16
-            // residual in every norm, the stack only for MALA
             const uint64_t ahi = sdesc_sw128(st + (uint32_t)ks * 2048u, kAtom, 1024u);
-            const uint64_t bhi = sdesc_sw128(st + a.off_bhi + (uint32_t)ks * 32u, 0u, 1024u);
-            const uint64_t blo = sdesc_sw128(st + a.off_blo + (uint32_t)ks * 32u, 0u, 1024u);
+            const uint64_t bhi = sdesc_sw128(st + a.off_b + (uint32_t)ks * 32u, 0u, 1024u);
             umma_bf16(d, ahi, bhi, idesc, (kc > 0 || ks > 0) ? 1u : 0u);
-            umma_bf16(d, ahi, blo, idesc, 1u);
-            if (a.use_lo_in)
-              umma_bf16(d, sdesc_sw128(st + a.off_alo + (uint32_t)ks * 2048u, kAtom, 1024u), bhi, idesc, 1u);
+            if (!kF16) {
+              const uint64_t alo = sdesc_sw128(st + a.off_alo + (uint32_t)ks * 2048u, kAtom, 1024u);
+              const uint64_t blo = sdesc_sw128(st + a.off_blo + (uint32_t)ks * 32u, 0u, 1024u);
+              umma_bf16(d, ahi, blo, idesc, 1u);
+              umma_bf16(d, alo, bhi, idesc, 1u);
+            }
           }
           umma_commit(empty(stage));
           if (++stage == kStages) {
@@ -178,10 +184,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_mix_kernel(const __grid_consta
     for (int w = blockIdx.x; w < a.units && ok; w += gridDim.x) {
       const int u = w / per_head;
       const int rem = w % per_head;
-      const int r = (rem / a.itiles) * 128 + 32 * e + lane;
+      const int r = a.r_off + (rem / a.itiles) * 128 + 32 * e + lane;
       const int i0 = (rem % a.itiles) * a.NT;
-      const bool aux = r >= p.d * p.d;
-      const bool lo = a.write_lo_s || aux;
       ok = mbar_wait(accfull(acc), accph, a.err, 0x204, abort_flag);
       if (!(ok = named_all(1, 128, ok))) break;
       tc_fence_after();
@@ -195,11 +199,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_mix_kernel(const __grid_consta
         if (r < p.R) {
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
-            if (i0 + c0 + j < p.M) {
-              const __nv_bfloat16 h = __float2bfloat16_rn(v[j]);
+            const int i = i0 + c0 + j;
+            if (i < p.M) {
+              float x = v[j];
+              if (kF16) x *= a.col_scale[i] * a.inv_stack_scale;
+              const __nv_bfloat16 h = __float2bfloat16_rn(x);
               const size_t off = (size_t)(c0 + j) * p.R;
               dst_hi[off] = h;
-              if (lo) dst_lo[off] = __float2bfloat16_rn(v[j] - __bfloat162float(h));
+              if (a.write_lo) dst_lo[off] = __float2bfloat16_rn(x - __bfloat162float(h));
             }
           }
         }
@@ -219,29 +226,51 @@ __global__ void __launch_bounds__(kThreads, 1) tc_mix_kernel(const __grid_consta
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-// One warp per row i of Mc: high and low bf16 parts, expanded over pieces,
-// and the row sum of hi + lo in float32.
+// One warp per row i of Mc: the fp16 copy scaled by 2^-e_i (largest entry of
+// the row in [0.5, 1]), the bf16 high and low parts, the row scale 2^e_i and
+// the row sum of hi + lo in float32.  Columns are expanded over pieces.
 __global__ void tc_prep_kernel(int M, int splits, int Q, int Qp, const float* __restrict__ mc,
+                               __half* __restrict__ mc_f16, float* __restrict__ mc_scale,
                                __nv_bfloat16* __restrict__ mc_hi, __nv_bfloat16* __restrict__ mc_lo,
                                float* __restrict__ rowsum) {
   const int i = (blockIdx.x * blockDim.x + threadIdx.x) / 32;
   const int lane = threadIdx.x % 32;
   if (i >= M) return;
   const float* row = mc + (size_t)i * M;
+  float s = 0.f, amax = 0.f;
+  for (int b = lane; b < M; b += 32) {
+    const __nv_bfloat16 h = __float2bfloat16_rn(row[b]);
+    s += __bfloat162float(h) + __bfloat162float(__float2bfloat16_rn(row[b] - __bfloat162float(h)));
+    amax = fmaxf(amax, fabsf(row[b]));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    s += __shfl_xor_sync(0xffffffffu, s, o);
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  }
+  int ex = 0;
+  if (amax > 0.f && amax <= 3.0e38f) frexpf(amax, &ex);  // amax = f * 2^ex, f in [0.5, 1)
+  const float down = ldexpf(1.f, -ex);
   for (int q = lane; q < Qp; q += 32) {
     const float x = q < Q ? row[q / splits] : 0.f;
     const __nv_bfloat16 h = __float2bfloat16_rn(x);
     mc_hi[(size_t)i * Qp + q] = h;
     mc_lo[(size_t)i * Qp + q] = __float2bfloat16_rn(x - __bfloat162float(h));
+    mc_f16[(size_t)i * Qp + q] = __float2half_rn(x * down);
   }
-  float s = 0.f;
-  for (int b = lane; b < M; b += 32) {
-    const __nv_bfloat16 h = __float2bfloat16_rn(row[b]);
-    s += __bfloat162float(h) + __bfloat162float(__float2bfloat16_rn(row[b] - __bfloat162float(h)));
+  if (lane == 0) {
+    rowsum[i] = s;
+    mc_scale[i] = ldexpf(1.f, ex);
   }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-  if (lane == 0) rowsum[i] = s;
+}
+
+template <bool kF16>
+int launch_variant(const MixArgs& a, const Plan& p, cudaStream_t s) {
+  cudaError_t ce = cudaFuncSetAttribute(tc_mix_kernel<kF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  if (ce != cudaSuccess) return (int)ce;
+  const int grid = a.units < num_sms() ? a.units : num_sms();
+  tc_mix_kernel<kF16><<<grid, kThreads, kSmemBytes, s>>>(a, p);
+  return (int)cudaGetLastError();
 }
 
 }  // namespace
@@ -249,51 +278,64 @@ __global__ void tc_prep_kernel(int M, int splits, int Q, int Qp, const float* __
 int launch_tc_prep(const Plan& p, const float* mc, const TcBuffers& b, cudaStream_t s) {
   const int threads = 256;
   const int blocks = (p.M * 32 + threads - 1) / threads;
-  tc_prep_kernel<<<blocks, threads, 0, s>>>(p.M, p.splits, p.M * p.splits, b.Qp, mc, b.mc_exp, b.mc_exp_lo,
-                                             b.rowsum);
+  tc_prep_kernel<<<blocks, threads, 0, s>>>(p.M, p.splits, p.M * p.splits, b.Qp, mc, b.mc_f16, b.mc_scale, b.mc_hi,
+                                             b.mc_lo, b.rowsum);
   return (int)cudaGetLastError();
 }
 
-int launch_tc_mix(const Plan& p, const TcBuffers& b, cudaStream_t s) {
+int launch_tc_mix(const Plan& p, const TcBuffers& b, bool aux_part, cudaStream_t s) {
   MixArgs a;
   memset(&a, 0, sizeof(a));
   const int Q = p.M * p.splits;
-  const uint64_t dimsA[3] = {(uint64_t)p.R, (uint64_t)Q, (uint64_t)p.BH};
-  const uint64_t strA[2] = {2ull * p.R, 2ull * p.R * Q};
+  const bool f16 = b.f16 && !aux_part;
+  const int W = aux_part ? 2 * p.d : p.d * p.d;
+  const void* src = aux_part ? (const void*)b.aux_hi : b.stack_s;
+  const void* src_lo = aux_part ? (const void*)b.aux_lo : (const void*)b.stack_s_lo;
+  const uint64_t dimsA[3] = {(uint64_t)W, (uint64_t)Q, (uint64_t)p.BH};
+  const uint64_t strA[2] = {2ull * W, 2ull * W * Q};
   const uint32_t boxA[3] = {64, 64, 1};
   int e;
-  if ((e = encode_tmap_bf16(&a.tmA_hi, b.stack_hi, 3, dimsA, strA, boxA)) != 0) return e;
-  a.use_lo_in = b.stack_lo != nullptr;
-  if ((e = encode_tmap_bf16(&a.tmA_lo, a.use_lo_in ? b.stack_lo : b.stack_hi, 3, dimsA, strA, boxA)) != 0) return e;
+  if ((e = encode_tmap(&a.tmA, src, 3, dimsA, strA, boxA, f16)) != 0) return e;
+  if ((e = encode_tmap_bf16(&a.tmA_lo, src_lo ? src_lo : src, 3, dimsA, strA, boxA)) != 0) return e;
+  const int nt_max = f16 ? 256 : 128;
   int NT = (p.M + 15) / 16 * 16;
-  if (NT > 256) NT = 256;
+  if (NT > nt_max) NT = nt_max;
   const uint64_t dimsB[2] = {(uint64_t)Q, (uint64_t)p.M};
   const uint64_t strB[1] = {2ull * b.Qp};
   const uint32_t boxB[2] = {64, (uint32_t)NT};
-  if ((e = encode_tmap_bf16(&a.tmB_hi, b.mc_exp, 2, dimsB, strB, boxB)) != 0) return e;
-  if ((e = encode_tmap_bf16(&a.tmB_lo, b.mc_exp_lo, 2, dimsB, strB, boxB)) != 0) return e;
+  if (f16) {
+    if ((e = encode_tmap(&a.tmB, b.mc_f16, 2, dimsB, strB, boxB, true)) != 0) return e;
+    a.tmB_lo = a.tmB;
+  } else {
+    if ((e = encode_tmap_bf16(&a.tmB, b.mc_hi, 2, dimsB, strB, boxB)) != 0) return e;
+    if ((e = encode_tmap_bf16(&a.tmB_lo, b.mc_lo, 2, dimsB, strB, boxB)) != 0) return e;
+  }
   a.mixed_hi = b.mixed_hi;
   a.mixed_lo = b.mixed_lo;
+  a.col_scale = b.mc_scale;
+  a.inv_stack_scale = 1.f / b.stack_scale;
   a.Q = Q;
   a.NT = NT;
   a.itiles = (p.M + NT - 1) / NT;
-  a.rtiles = (p.R + 127) / 128;
+  a.rtiles = W / 128;
   a.kchunks = (Q + 63) / 64;
   a.units = p.BH * a.rtiles * a.itiles;
-  a.write_lo_s = p.norm == MHLA_NORM_MALA;
+  a.r_off = aux_part ? p.d * p.d : 0;
+  a.write_lo = aux_part || p.norm == MHLA_NORM_MALA;
   const uint32_t btile = (uint32_t)NT * 128u;
-  a.off_alo = kATile;
-  a.off_bhi = kATile * (a.use_lo_in ? 2u : 1u);
-  a.off_blo = a.off_bhi + btile;
-  a.stage_bytes = (a.off_blo + btile + 1023u) / 1024u * 1024u;
+  if (f16) {
+    a.off_b = kATile;
+    a.stage_bytes = (kATile + btile + 1023u) / 1024u * 1024u;
+  } else {
+    a.off_alo = kATile;
+    a.off_b = 2 * kATile;
+    a.off_blo = a.off_b + btile;
+    a.stage_bytes = (a.off_blo + btile + 1023u) / 1024u * 1024u;
+  }
   a.stages = (int)(kStageArea / a.stage_bytes);
   if (a.stages > kMaxStages) a.stages = kMaxStages;
   a.err = p.err;
-  cudaError_t ce = cudaFuncSetAttribute(tc_mix_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-  if (ce != cudaSuccess) return (int)ce;
-  const int grid = a.units < num_sms() ? a.units : num_sms();
-  tc_mix_kernel<<<grid, kThreads, kSmemBytes, s>>>(a, p);
-  return (int)cudaGetLastError();
+  return f16 ? launch_variant<true>(a, p, s) : launch_variant<false>(a, p, s);
 }
 
 }  // namespace mhla

@@ -19,9 +19,10 @@
 // Persistent, warp-specialised CTA (one per SM, 512 threads):
 //   warp 0       TMA producer (K and V tiles of one token chunk per stage)
 //   warp 1       TMEM allocation + MMA issue (one elected thread)
-//   warps 4-6    epilogue: TMEM rows 0..95 -> bf16 (hi and, for MALA, lo
-//                residual) -> swizzled staging tile -> TMA store into the
-//                summary stack
+//   warps 4-6    epilogue: TMEM rows 0..95 -> S_b as fp16 (scaled by
+//                2^-ceil(log2 n), DIVISIVE/NONE) or bf16 hi + lo (MALA),
+//                z_b and v_b as bf16 hi + lo -> swizzled staging tiles ->
+//                TMA stores into the summary stacks
 //   warps 8-15   phi(K) transform, two threads per token row
 // Each CTA walks work units (head, block, piece) with a static stride; long
 // blocks are cut into pieces whose partial summaries the mixing step adds.
@@ -63,10 +64,11 @@ struct Layout {
 
 struct SummaryArgs {
   CUtensorMap tmK, tmV;              // 5D (64, Wg, Hg, T, BH), box (64, cw, ch, ct, 1)
-  CUtensorMap tmS_hi, tmZV_hi;       // 2D stack view (64, rows), boxes (64, 64) and (64, 2)
-  CUtensorMap tmS_lo, tmZV_lo;
+  CUtensorMap tmS, tmS_lo;           // 2D view (64, BH*Q*64) of the S stack, box (64, 64)
+  CUtensorMap tmZV_hi, tmZV_lo;      // 2D view (64, BH*Q*2) of the z/v stack, box (64, 2)
   int units, splits, cpp;            // work units, pieces per block, chunks per piece
-  int write_lo;
+  int f16;                           // S stored as fp16(S * stack_scale); else bf16 (+ lo)
+  float stack_scale;
   ChunkShape c;
   unsigned int* err;
 };
@@ -325,19 +327,32 @@ __global__ void __launch_bounds__(kThreads, 1) tc_summary_kernel(const __grid_co
       named_sync(1, kEpiThreads);
       if (e < 2) {
         // row r of S_b and z_b[r]
+        bool overflow = false;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
+          const float* src = j < 4 ? &s0[8 * j] : &s1[8 * (j - 4)];
           uint4 hv, lv;
-          split8(j < 4 ? &s0[8 * j] : &s1[8 * (j - 4)], hv, lv, 1.f, a.write_lo);
+          if (a.f16) {
+            uint32_t* hp = &hv.x;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const float x0 = src[2 * q] * a.stack_scale, x1 = src[2 * q + 1] * a.stack_scale;
+              overflow |= fabsf(x0) > 65504.f || fabsf(x1) > 65504.f;
+              __half2 h = __floats2half2_rn(x0, x1);
+              hp[q] = *reinterpret_cast<uint32_t*>(&h);
+            }
+          } else {
+            split8(src, hv, lv, 1.f, kLo);
+          }
           const uint32_t off = (uint32_t)r * 128u + ((uint32_t)((j ^ (r & 7)) & 7) << 4);
           *reinterpret_cast<uint4*>(st_hi + off) = hv;
-          if (a.write_lo) *reinterpret_cast<uint4*>(st_lo + off) = lv;
+          if (kLo) *reinterpret_cast<uint4*>(st_lo + off) = lv;
         }
+        if (overflow) report_error(a.err, MHLA_ERR_OVERFLOW, 0x106);
         const __nv_bfloat16 zh = __float2bfloat16_rn(zval);
         *reinterpret_cast<__nv_bfloat16*>(st_hi + 8192 + sw128_offset(0, r)) = zh;
-        if (a.write_lo)
-          *reinterpret_cast<__nv_bfloat16*>(st_lo + 8192 + sw128_offset(0, r)) =
-              __float2bfloat16_rn(zval - __bfloat162float(zh));
+        *reinterpret_cast<__nv_bfloat16*>(st_lo + 8192 + sw128_offset(0, r)) =
+            __float2bfloat16_rn(zval - __bfloat162float(zh));
       } else if (lane == 0) {
         // row 64 of D: v_b (every row 64..127 holds the same values; the
         // low-residual MMA of MALA adds them twice)
@@ -347,19 +362,17 @@ __global__ void __launch_bounds__(kThreads, 1) tc_summary_kernel(const __grid_co
           split8(j < 4 ? &s0[8 * j] : &s1[8 * (j - 4)], hv, lv, kLo ? 0.5f : 1.f, true);
           const uint32_t off = 128u + ((uint32_t)((j ^ 1) & 7) << 4);
           *reinterpret_cast<uint4*>(st_hi + 8192 + off) = hv;
-          if (a.write_lo) *reinterpret_cast<uint4*>(st_lo + 8192 + off) = lv;
+          *reinterpret_cast<uint4*>(st_lo + 8192 + off) = lv;
         }
       }
       fence_proxy_async();
       named_sync(1, kEpiThreads);
       if (et == 0) {
-        const int row0 = ((uc.u * p.M + uc.b) * a.splits + (uc.c0 / a.cpp)) * 66;
-        tma_store_2d(&a.tmS_hi, smem_u32(st_hi), 0, row0);
-        tma_store_2d(&a.tmZV_hi, smem_u32(st_hi + 8192), 0, row0 + 64);
-        if (a.write_lo) {
-          tma_store_2d(&a.tmS_lo, smem_u32(st_lo), 0, row0);
-          tma_store_2d(&a.tmZV_lo, smem_u32(st_lo + 8192), 0, row0 + 64);
-        }
+        const int srow = (uc.u * p.M + uc.b) * a.splits + (uc.c0 / a.cpp);
+        tma_store_2d(&a.tmS, smem_u32(st_hi), 0, srow * 64);
+        if (kLo) tma_store_2d(&a.tmS_lo, smem_u32(st_lo), 0, srow * 64);
+        tma_store_2d(&a.tmZV_hi, smem_u32(st_hi + 8192), 0, srow * 2);
+        tma_store_2d(&a.tmZV_lo, smem_u32(st_lo + 8192), 0, srow * 2);
         bulk_commit();
       }
     }
@@ -394,23 +407,26 @@ int launch_tc_summary(const Plan& p, const ChunkShape& c, const void* k, const v
   int e;
   if ((e = encode_tmap_bf16(&a.tmK, k, 5, dims5, str5, box5)) != 0) return e;
   if ((e = encode_tmap_bf16(&a.tmV, v, 5, dims5, str5, box5)) != 0) return e;
-  const uint64_t stack_rows = (uint64_t)p.BH * p.M * p.splits * 66ull;
-  const uint64_t dims2[2] = {64, stack_rows};
+  const uint64_t stack_rows = (uint64_t)p.BH * p.M * p.splits;
+  const uint64_t dimsS[2] = {64, stack_rows * 64};
+  const uint64_t dimsA[2] = {64, stack_rows * 2};
   const uint64_t str2[1] = {128};
   const uint32_t boxS[2] = {64, 64};
   const uint32_t boxZV[2] = {64, 2};
-  if ((e = encode_tmap_bf16(&a.tmS_hi, b.stack_hi, 2, dims2, str2, boxS)) != 0) return e;
-  if ((e = encode_tmap_bf16(&a.tmZV_hi, b.stack_hi, 2, dims2, str2, boxZV)) != 0) return e;
-  a.write_lo = b.stack_lo != nullptr;  // MALA: phi(K) and the stack carry low residuals
-  const void* lo = a.write_lo ? (const void*)b.stack_lo : (const void*)b.stack_hi;
-  if ((e = encode_tmap_bf16(&a.tmS_lo, lo, 2, dims2, str2, boxS)) != 0) return e;
-  if ((e = encode_tmap_bf16(&a.tmZV_lo, lo, 2, dims2, str2, boxZV)) != 0) return e;
+  const bool lo = b.stack_s_lo != nullptr;  // MALA: phi(K) and S carry low residuals
+  if ((e = encode_tmap(&a.tmS, b.stack_s, 2, dimsS, str2, boxS, b.f16)) != 0) return e;
+  if ((e = encode_tmap_bf16(&a.tmS_lo, lo ? (const void*)b.stack_s_lo : b.stack_s, 2, dimsS, str2, boxS)) != 0)
+    return e;
+  if ((e = encode_tmap_bf16(&a.tmZV_hi, b.aux_hi, 2, dimsA, str2, boxZV)) != 0) return e;
+  if ((e = encode_tmap_bf16(&a.tmZV_lo, b.aux_lo, 2, dimsA, str2, boxZV)) != 0) return e;
+  a.f16 = b.f16;
+  a.stack_scale = b.stack_scale;
   a.splits = p.splits;
   a.cpp = p.cpp;
   a.units = p.BH * p.M * p.splits;
   a.c = c;
   a.err = p.err;
-  return a.write_lo ? launch_variant<true>(a, p, s) : launch_variant<false>(a, p, s);
+  return lo ? launch_variant<true>(a, p, s) : launch_variant<false>(a, p, s);
 }
 
 }  // namespace mhla
