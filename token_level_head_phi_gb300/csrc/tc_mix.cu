@@ -45,9 +45,9 @@ constexpr uint32_t kTmemCols = 512;                 // two accumulators of up to
 struct MixArgs {
   CUtensorMap tmA, tmA_lo;     // 3D (W, Q, BH), box (64, 64, 1)
   CUtensorMap tmB, tmB_lo;     // 2D (Q, M),     box (64, NT)
-  __nv_bfloat16* mixed_hi;
-  __nv_bfloat16* mixed_lo;
-  const float* col_scale;      // kF16: 2^e_i per query block i
+  __nv_bfloat16* __restrict__ mixed_hi;
+  __nv_bfloat16* __restrict__ mixed_lo;
+  const float* __restrict__ col_scale;  // kF16: 2^e_i per query block i
   float inv_stack_scale;       // kF16: 2^s
   int Q, NT, itiles, rtiles, kchunks, units;
   int r_off;                   // column of Mixed where this part starts
@@ -195,19 +195,20 @@ __global__ void __launch_bounds__(kThreads, 1) tc_mix_kernel(const __grid_consta
       for (int c0 = 0; c0 < a.NT; c0 += 32) {
         float v[32];
         tmem_ld32(taddr + (uint32_t)c0, v);
+        // scale of query block i0 + c0 + lane, broadcast to the warp below
+        float my_scale = 1.f;
+        if (kF16 && i0 + c0 + lane < p.M) my_scale = a.col_scale[i0 + c0 + lane] * a.inv_stack_scale;
         tmem_wait_ld();
-        if (r < p.R) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int i = i0 + c0 + j;
-            if (i < p.M) {
-              float x = v[j];
-              if (kF16) x *= a.col_scale[i] * a.inv_stack_scale;
-              const __nv_bfloat16 h = __float2bfloat16_rn(x);
-              const size_t off = (size_t)(c0 + j) * p.R;
-              dst_hi[off] = h;
-              if (a.write_lo) dst_lo[off] = __float2bfloat16_rn(x - __bfloat162float(h));
-            }
+        for (int j = 0; j < 32; ++j) {
+          const float sc = kF16 ? __shfl_sync(0xffffffffu, my_scale, j) : 1.f;
+          const int i = i0 + c0 + j;
+          if (i < p.M && r < p.R) {
+            const float x = v[j] * sc;
+            const __nv_bfloat16 h = __float2bfloat16_rn(x);
+            const size_t off = (size_t)(c0 + j) * p.R;
+            dst_hi[off] = h;
+            if (a.write_lo) dst_lo[off] = __float2bfloat16_rn(x - __bfloat162float(h));
           }
         }
       }
