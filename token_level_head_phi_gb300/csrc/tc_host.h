@@ -25,6 +25,9 @@ constexpr int kPlanSms = 152;
 // dims[i + 1].
 int encode_tmap(CUtensorMap* map, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
                 const uint32_t* box, bool f16);
+// Same without swizzle (row-major boxes in shared memory), bf16.
+int encode_tmap_plain(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                      const uint64_t* strides_bytes, const uint32_t* box);
 inline int encode_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
                             const uint64_t* strides_bytes, const uint32_t* box) {
   return encode_tmap(map, base, rank, dims, strides_bytes, box, false);

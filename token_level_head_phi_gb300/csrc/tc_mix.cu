@@ -15,7 +15,9 @@
 //   split (z/v part always, S part for MALA): X and Mc as bf16 high + low
 //         parts, D = Xh Mh + Xh Ml + Xl Mh.
 // The epilogue writes Mixed as bf16 (plus the low residual where the output
-// step needs it), each warp storing 32 consecutive r of one query block.
+// step needs it): 32 query blocks x 128 r at a time, transposed through a
+// shared-memory tile and stored by TMA.  In the fp16 case Mixed holds
+// S~_i / 2^(s + e_i); the output step multiplies the scale back.
 //
 // Also here: the small preparation kernel that builds the Mc copies.
 #include <cuda_bf16.h>
@@ -34,21 +36,21 @@ namespace {
 using namespace tc;
 
 constexpr int kMaxStages = 4;
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;                       // 4 control warps + 8 epilogue warps
+constexpr int kEpiGroups = 2;                       // epilogue groups (column halves)
 constexpr uint32_t kAtom = 64 * 128;                // 64 q-rows x 64 r (8 KB)
 constexpr uint32_t kATile = 2 * kAtom;              // 128 r
-constexpr uint32_t kStageArea = 200 * 1024;         // shared memory for the stages
-constexpr uint32_t kBars = kStageArea;
+constexpr uint32_t kStageArea = 192 * 1024;         // shared memory for the stages
+constexpr uint32_t kStagingBytes = 2 * 32 * 256;    // per group: [32 i][128 r] bf16, hi and lo
+constexpr uint32_t kStaging = kStageArea;
+constexpr uint32_t kBars = kStaging + kEpiGroups * kStagingBytes;
 constexpr uint32_t kSmemBytes = kBars + 256 + 1024;
 constexpr uint32_t kTmemCols = 512;                 // two accumulators of up to 256 columns
 
 struct MixArgs {
   CUtensorMap tmA, tmA_lo;     // 3D (W, Q, BH), box (64, 64, 1)
   CUtensorMap tmB, tmB_lo;     // 2D (Q, M),     box (64, NT)
-  __nv_bfloat16* __restrict__ mixed_hi;
-  __nv_bfloat16* __restrict__ mixed_lo;
-  const float* __restrict__ col_scale;  // kF16: 2^e_i per query block i
-  float inv_stack_scale;       // kF16: 2^s
+  CUtensorMap tmO, tmO_lo;     // 3D (R, M, BH) view of Mixed, box (128, 32, 1), no swizzle
   int Q, NT, itiles, rtiles, kchunks, units;
   int r_off;                   // column of Mixed where this part starts
   int write_lo;                // write the low residual of every value
@@ -82,7 +84,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_mix_kernel(const __grid_consta
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(accfull(x), 1);
-      mbar_init(accempty(x), 128);
+      mbar_init(accempty(x), 128 * kEpiGroups);
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -177,39 +179,48 @@ __global__ void __launch_bounds__(kThreads, 1) tc_mix_kernel(const __grid_consta
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ epilogue
-    const int e = warp - 4;
+    // warp 4 + 4g + q: TMEM lane quarter q, query-block columns of half g.
+    // Each 32-column slice goes through a [32 i][128 r] staging tile and
+    // one TMA store (rows of Mixed are contiguous in r).
+    const int q4 = warp & 3;
+    const int g = (warp - 4) >> 2;
+    const int gt = threadIdx.x - 128 - 128 * g;  // 0..127 within the group
+    const int rl = 32 * q4 + lane;               // row of the 128-row tile
+    uint8_t* stg = gb + kStaging + g * kStagingBytes;
+    const uint32_t stg_addr = base + kStaging + g * kStagingBytes;
+    const int half_nt = a.NT / 2;
     int acc = 0;
     uint32_t accph = 0;
     bool ok = true;
     for (int w = blockIdx.x; w < a.units && ok; w += gridDim.x) {
       const int u = w / per_head;
       const int rem = w % per_head;
-      const int r = a.r_off + (rem / a.itiles) * 128 + 32 * e + lane;
+      const int r0 = a.r_off + (rem / a.itiles) * 128;
       const int i0 = (rem % a.itiles) * a.NT;
       ok = mbar_wait(accfull(acc), accph, a.err, 0x204, abort_flag);
-      if (!(ok = named_all(1, 128, ok))) break;
+      if (!(ok = named_all(1 + g, 128, ok))) break;
       tc_fence_after();
-      const uint32_t taddr = tmem + (uint32_t)acc * 256u + ((uint32_t)(32 * e) << 16);
-      __nv_bfloat16* dst_hi = a.mixed_hi + ((size_t)u * p.M + i0) * p.R + r;
-      __nv_bfloat16* dst_lo = a.mixed_lo + ((size_t)u * p.M + i0) * p.R + r;
-      for (int c0 = 0; c0 < a.NT; c0 += 32) {
+      const uint32_t taddr = tmem + (uint32_t)acc * 256u + ((uint32_t)(32 * q4) << 16);
+      for (int c0 = g * half_nt; c0 < (g + 1) * half_nt; c0 += 32) {
         float v[32];
         tmem_ld32(taddr + (uint32_t)c0, v);
-        // scale of query block i0 + c0 + lane, broadcast to the warp below
-        float my_scale = 1.f;
-        if (kF16 && i0 + c0 + lane < p.M) my_scale = a.col_scale[i0 + c0 + lane] * a.inv_stack_scale;
         tmem_wait_ld();
+        // the previous slice's store has finished reading the staging tile
+        if (gt == 0) bulk_wait_read<0>();
+        named_sync(1 + g, 128);
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-          const float sc = kF16 ? __shfl_sync(0xffffffffu, my_scale, j) : 1.f;
-          const int i = i0 + c0 + j;
-          if (i < p.M && r < p.R) {
-            const float x = v[j] * sc;
-            const __nv_bfloat16 h = __float2bfloat16_rn(x);
-            const size_t off = (size_t)(c0 + j) * p.R;
-            dst_hi[off] = h;
-            if (a.write_lo) dst_lo[off] = __float2bfloat16_rn(x - __bfloat162float(h));
-          }
+          const __nv_bfloat16 h = __float2bfloat16_rn(v[j]);
+          reinterpret_cast<__nv_bfloat16*>(stg)[j * 128 + rl] = h;
+          if (a.write_lo)
+            reinterpret_cast<__nv_bfloat16*>(stg + 8192)[j * 128 + rl] = __float2bfloat16_rn(v[j] - __bfloat162float(h));
+        }
+        fence_proxy_async();
+        named_sync(1 + g, 128);
+        if (gt == 0) {
+          tma_store_3d(&a.tmO, stg_addr, r0, i0 + c0, u);
+          if (a.write_lo) tma_store_3d(&a.tmO_lo, stg_addr + 8192, r0, i0 + c0, u);
+          bulk_commit();
         }
       }
       tc_fence_before();
@@ -219,6 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_mix_kernel(const __grid_consta
         accph ^= 1u;
       }
     }
+    if (gt == 0) bulk_wait<0>();
   }
   __syncwarp();
 
@@ -298,8 +310,10 @@ int launch_tc_mix(const Plan& p, const TcBuffers& b, bool aux_part, cudaStream_t
   int e;
   if ((e = encode_tmap(&a.tmA, src, 3, dimsA, strA, boxA, f16)) != 0) return e;
   if ((e = encode_tmap_bf16(&a.tmA_lo, src_lo ? src_lo : src, 3, dimsA, strA, boxA)) != 0) return e;
+  // query-block tile: a multiple of 64 so that each epilogue group stores
+  // whole 32-row boxes that never reach into the next tile
   const int nt_max = f16 ? 256 : 128;
-  int NT = (p.M + 15) / 16 * 16;
+  int NT = (p.M + 63) / 64 * 64;
   if (NT > nt_max) NT = nt_max;
   const uint64_t dimsB[2] = {(uint64_t)Q, (uint64_t)p.M};
   const uint64_t strB[1] = {2ull * b.Qp};
@@ -311,10 +325,11 @@ int launch_tc_mix(const Plan& p, const TcBuffers& b, bool aux_part, cudaStream_t
     if ((e = encode_tmap_bf16(&a.tmB, b.mc_hi, 2, dimsB, strB, boxB)) != 0) return e;
     if ((e = encode_tmap_bf16(&a.tmB_lo, b.mc_lo, 2, dimsB, strB, boxB)) != 0) return e;
   }
-  a.mixed_hi = b.mixed_hi;
-  a.mixed_lo = b.mixed_lo;
-  a.col_scale = b.mc_scale;
-  a.inv_stack_scale = 1.f / b.stack_scale;
+  const uint64_t dimsO[3] = {(uint64_t)p.R, (uint64_t)p.M, (uint64_t)p.BH};
+  const uint64_t strO[2] = {2ull * p.R, 2ull * p.R * p.M};
+  const uint32_t boxO[3] = {128, 32, 1};
+  if ((e = encode_tmap_plain(&a.tmO, b.mixed_hi, 3, dimsO, strO, boxO)) != 0) return e;
+  if ((e = encode_tmap_plain(&a.tmO_lo, b.mixed_lo, 3, dimsO, strO, boxO)) != 0) return e;
   a.Q = Q;
   a.NT = NT;
   a.itiles = (p.M + NT - 1) / NT;

@@ -58,6 +58,8 @@ struct OutArgs {
   const __nv_bfloat16* mixed_hi;
   const __nv_bfloat16* mixed_lo;
   const float* rowsum;
+  const float* col_scale;      // fp16 mixing: Mixed holds S~_i / (2^e_i 2^s); else nullptr
+  float inv_stack_scale;       // 2^s
   int units;
   int use_lo;
   ChunkShape c;
@@ -242,9 +244,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_output_kernel(const __grid_con
       uint8_t* st = gb + stage * kStageBytes;
       if (t < rows) {
         const float s = s0 + s1;
-        float scale = 1.f, gamma = 0.f;
+        const float cs = a.col_scale ? a.col_scale[i] * a.inv_stack_scale : 1.f;
+        float scale = cs, gamma = 0.f;
         if (p.norm == MHLA_NORM_DIVISIVE) {
-          scale = __frcp_rn(s);
+          scale = cs * __frcp_rn(s);
         } else if (p.norm == MHLA_NORM_MALA) {
           scale = 1.f + __frcp_rn(s);                       // beta
           gamma = s / ((float)p.nb * a.rowsum[i]);
@@ -317,6 +320,8 @@ int launch_tc_output(const Plan& p, const ChunkShape& c, const void* q, const Tc
   a.mixed_hi = b.mixed_hi;
   a.mixed_lo = b.mixed_lo;
   a.rowsum = b.rowsum;
+  a.col_scale = b.f16 ? b.mc_scale : nullptr;
+  a.inv_stack_scale = 1.f / b.stack_scale;
   a.units = p.BH * p.M * c.per_block;
   a.use_lo = p.norm == MHLA_NORM_MALA;
   a.c = c;

@@ -21,8 +21,24 @@ int g_sms[kMaxDevices] = {};
 
 }  // namespace
 
+namespace {
+int encode_impl(CUtensorMap* map, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
+                const uint32_t* box, bool f16, bool swizzle);
+}  // namespace
+
 int encode_tmap(CUtensorMap* map, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
                 const uint32_t* box, bool f16) {
+  return encode_impl(map, base, rank, dims, strides_bytes, box, f16, true);
+}
+
+int encode_tmap_plain(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                      const uint64_t* strides_bytes, const uint32_t* box) {
+  return encode_impl(map, base, rank, dims, strides_bytes, box, false, false);
+}
+
+namespace {
+int encode_impl(CUtensorMap* map, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
+                const uint32_t* box, bool f16, bool swizzle) {
   std::call_once(g_enc_once, [] {
     cudaDriverEntryPointQueryResult q;
     void* fn = nullptr;
@@ -43,10 +59,12 @@ int encode_tmap(CUtensorMap* map, const void* base, int rank, const uint64_t* di
     if (i + 1 < rank) gstride[i] = strides_bytes[i];
   }
   CUresult r = g_encode(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base), gdim,
-                        gstride, bdim, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        gstride, bdim, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? 0 : (int)cudaErrorInvalidValue;
 }
+}  // namespace
 
 ChunkShape choose_chunk(const Plan& p) {
   auto largest_divisor = [](int n, int limit) {
