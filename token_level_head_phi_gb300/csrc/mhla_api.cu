@@ -178,6 +178,8 @@ mhla_status make_plan(const mhla_params* prm, Plan* p) {
     off = align_up(off + sizeof(float) * (size_t)p->M);
     p->off_rowsum = off;
     off = align_up(off + sizeof(float) * (size_t)p->M);
+    p->off_blkinfo = off;
+    off = align_up(off + 16 * (size_t)p->M);
     p->kernels = 5;
   }
   p->off_aux = off;
@@ -217,6 +219,7 @@ mhla_status run_plan(const Plan& plan, const void* q, const void* k, const void*
     b.mc_hi = reinterpret_cast<__nv_bfloat16*>(ws + p.off_mc_hi);
     b.mc_lo = reinterpret_cast<__nv_bfloat16*>(ws + p.off_mc_lo);
     b.rowsum = reinterpret_cast<float*>(ws + p.off_rowsum);
+    b.blkinfo = reinterpret_cast<float4*>(ws + p.off_blkinfo);
     b.Qp = p.Qp;
     b.f16 = p.f16_mix != 0;
     b.stack_scale = b.f16 ? p.stack_scale : 1.f;

@@ -31,6 +31,9 @@ namespace tc {
 constexpr unsigned int kErrTimeout = MHLA_ERR_DEVICE_TIMEOUT;
 // Upper bound on any single wait on the device.
 constexpr unsigned long long kWaitLimitNs = 1000ull * 1000ull * 1000ull;
+// Longest a waiting thread stays suspended before it re-checks the abort
+// flag and the time limit.
+constexpr uint32_t kSleepHintNs = 200000u;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -73,6 +76,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait that lets the hardware suspend the thread for up to `hint_ns`
+// nanoseconds (it resumes as soon as the phase completes), so waiting roles
+// do not spin on the issue slots the working roles need.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Records a status in the device error word (first writer wins).
 __device__ __forceinline__ void report_error(unsigned int* err, unsigned int code, unsigned int where) {
   if (err && atomicCAS(err, 0u, code) == 0u) atomicExch(err + 1, where);
@@ -90,15 +108,13 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigne
                                           volatile int* abort_flag = nullptr) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0u) {
-      if (abort_flag && *abort_flag) return false;
-      if (globaltimer() - t0 > kWaitLimitNs) {
-        report_timeout(err, where);
-        if (abort_flag) *abort_flag = 1;
-        return false;
-      }
+  for (;;) {
+    if (mbar_try_wait_sleep(bar, parity, kSleepHintNs)) return true;
+    if (abort_flag && *abort_flag) return false;
+    if (globaltimer() - t0 > kWaitLimitNs) {
+      report_timeout(err, where);
+      if (abort_flag) *abort_flag = 1;
+      return false;
     }
   }
 }
@@ -193,6 +209,14 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t sr
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
                    reinterpret_cast<uint64_t>(map)),
                "r"(src), "r"(c0), "r"(c1)
+               : "memory");
+}
+
+// Plain (untiled) bulk copy global -> shared completing on an mbarrier;
+// 16-byte aligned addresses, size % 16 == 0.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
                : "memory");
 }
 

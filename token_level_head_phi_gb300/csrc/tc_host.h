@@ -50,6 +50,7 @@ struct TcBuffers {
   __nv_bfloat16* mc_hi;      // [M][Qp] bf16(Mc[i][q / splits])
   __nv_bfloat16* mc_lo;      // [M][Qp] low bf16 residual of the same
   float* rowsum;             // [M] sum_b (hi + lo)(Mc[i][b])
+  float4* blkinfo;           // [M] {scale the output step applies to S~_i, n~_i, 0, 0}
   int Qp;                    // padded row pitch of the Mc copies
   bool f16;                  // S part of the stack in fp16 (DIVISIVE and NONE)
   float stack_scale;         // 2^-ceil(log2(tokens per piece))

@@ -245,7 +245,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_mix_kernel(const __grid_consta
 __global__ void tc_prep_kernel(int M, int splits, int Q, int Qp, const float* __restrict__ mc,
                                __half* __restrict__ mc_f16, float* __restrict__ mc_scale,
                                __nv_bfloat16* __restrict__ mc_hi, __nv_bfloat16* __restrict__ mc_lo,
-                               float* __restrict__ rowsum) {
+                               float* __restrict__ rowsum, float4* __restrict__ blkinfo, int f16,
+                               float inv_stack_scale, float nb) {
   const int i = (blockIdx.x * blockDim.x + threadIdx.x) / 32;
   const int lane = threadIdx.x % 32;
   if (i >= M) return;
@@ -274,6 +275,9 @@ __global__ void tc_prep_kernel(int M, int splits, int Q, int Qp, const float* __
   if (lane == 0) {
     rowsum[i] = s;
     mc_scale[i] = ldexpf(1.f, ex);
+    // the fp16 mixing leaves S~_i divided by 2^ex 2^s; the output step
+    // multiplies it back
+    blkinfo[i] = make_float4(f16 ? ldexpf(inv_stack_scale, ex) : 1.f, nb * s, 0.f, 0.f);
   }
 }
 
@@ -292,7 +296,8 @@ int launch_tc_prep(const Plan& p, const float* mc, const TcBuffers& b, cudaStrea
   const int threads = 256;
   const int blocks = (p.M * 32 + threads - 1) / threads;
   tc_prep_kernel<<<blocks, threads, 0, s>>>(p.M, p.splits, p.M * p.splits, b.Qp, mc, b.mc_f16, b.mc_scale, b.mc_hi,
-                                             b.mc_lo, b.rowsum);
+                                             b.mc_lo, b.rowsum, b.blkinfo, b.f16 ? 1 : 0, 1.f / b.stack_scale,
+                                             (float)p.nb);
   return (int)cudaGetLastError();
 }
 

@@ -44,7 +44,11 @@ constexpr uint32_t kOffBhi = kQTile;               // S~_i high part
 constexpr uint32_t kOffZt = kOffBhi + kBTile;      // z~_i as columns 0 (hi) and 1 (lo)
 constexpr uint32_t kOffBlo = kOffZt + kBTile;      // S~_i low part (MALA)
 constexpr uint32_t kOffV = kOffBlo + kBTile;       // v~_i, 64 floats (MALA)
+constexpr uint32_t kOffAux = kOffV + 256;          // rows z~_i, v~_i of Mixed, bf16 hi (256 B)
+constexpr uint32_t kOffAuxLo = kOffAux + 256;      // same, low residuals
+constexpr uint32_t kOffInfo = kOffAuxLo + 256;     // float4 {output scale, n~_i, 0, 0}
 constexpr uint32_t kStageBytes = kOffV + 1024;
+static_assert(kOffInfo + 16 <= kStageBytes, "stage layout");
 constexpr uint32_t kBars = kStages * kStageBytes;
 constexpr uint32_t kSmemBytes = kBars + 256 + 1024;
 constexpr uint32_t kAccStride = 128;               // TMEM columns per stage (80 used)
@@ -55,11 +59,8 @@ static_assert(kStageBytes % 1024 == 0, "stage alignment");
 struct OutArgs {
   CUtensorMap tmQ, tmO;        // 5D (64, Wg, Hg, T, BH), box (64, cw, ch, ct, 1)
   CUtensorMap tmB_hi, tmB_lo;  // 3D (64, R/64, BH*M), box (64, 64, 1)
-  const __nv_bfloat16* mixed_hi;
-  const __nv_bfloat16* mixed_lo;
-  const float* rowsum;
-  const float* col_scale;      // fp16 mixing: Mixed holds S~_i / (2^e_i 2^s); else nullptr
-  float inv_stack_scale;       // 2^s
+  CUtensorMap tmA_hi, tmA_lo;  // same view, box (64, 2, 1), no swizzle: rows z~_i, v~_i
+  const float4* blkinfo;       // per query block {output scale, n~_i, 0, 0}
   int units;
   int use_lo;
   ChunkShape c;
@@ -119,7 +120,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_output_kernel(const __grid_con
       // ---------------------------------------------------------- producer
       const uint64_t pol_q = policy_evict_first();
       const uint64_t pol_b = policy_evict_last();
-      const uint32_t bytes = (uint32_t)rows * 128u + kBTile * (a.use_lo ? 2u : 1u);
+      const uint32_t bytes = (uint32_t)rows * 128u + kBTile * (a.use_lo ? 2u : 1u) + 512u + 16u;
       int stage = 0;
       uint32_t phase = 0;
       for (int w = blockIdx.x; w < a.units; w += gridDim.x) {
@@ -137,6 +138,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_output_kernel(const __grid_con
         tma_load_5d(st, &a.tmQ, full(stage), 0, x0, y0, t0, u, pol_q);
         tma_load_3d(st + kOffBhi, &a.tmB_hi, full(stage), 0, 0, u * p.M + i, pol_b);
         if (a.use_lo) tma_load_3d(st + kOffBlo, &a.tmB_lo, full(stage), 0, 0, u * p.M + i, pol_b);
+        tma_load_3d(st + kOffAux, &a.tmA_hi, full(stage), 0, p.d, u * p.M + i, pol_b);
+        tma_load_3d(st + kOffAuxLo, &a.tmA_lo, full(stage), 0, p.d, u * p.M + i, pol_b);
+        bulk_load(st + kOffInfo, a.blkinfo + i, 16u, full(stage));
         if (++stage == kStages) {
           stage = 0;
           phase ^= 1u;
@@ -178,23 +182,20 @@ __global__ void __launch_bounds__(kThreads, 1) tc_output_kernel(const __grid_con
     int stage = 0;
     uint32_t phase = 0;
     for (int w = blockIdx.x; w < a.units; w += gridDim.x) {
-      const int u = w / per_head;
-      const int i = (w % per_head) / nck;
-      // threads 0..63: z~_i[k] (hi, lo); threads 64..127: v~_i[c] (hi + lo)
-      const size_t aux = ((size_t)u * p.M + i) * p.R + (size_t)p.d * p.d + (t & 127);
-      __nv_bfloat16 zh = __float2bfloat16_rn(0.f), zl = zh;
-      if (t < 128) {
-        zh = a.mixed_hi[aux];
-        zl = a.mixed_lo[aux];
-      }
       const bool ok = mbar_wait(full(stage), phase, a.err, 0x303, abort_flag);
       if (!named_all(2, kXfThreads, ok)) break;
       uint8_t* st = gb + stage * kStageBytes;
-      if (t < 64) {
-        *reinterpret_cast<__nv_bfloat16*>(st + kOffZt + sw128_offset(t, 0)) = zh;
-        *reinterpret_cast<__nv_bfloat16*>(st + kOffZt + sw128_offset(t, 1)) = zl;
-      } else if (t < 128) {
-        reinterpret_cast<float*>(st + kOffV)[t - 64] = __bfloat162float(zh) + __bfloat162float(zl);
+      // threads 0..63: z~_i[k] (hi, lo) into columns 0, 1 of the z~ operand;
+      // threads 64..127: v~_i[c] = hi + lo as float for the MALA epilogue
+      if (t < 128) {
+        const __nv_bfloat16 zh = reinterpret_cast<const __nv_bfloat16*>(st + kOffAux)[t];
+        const __nv_bfloat16 zl = reinterpret_cast<const __nv_bfloat16*>(st + kOffAuxLo)[t];
+        if (t < 64) {
+          *reinterpret_cast<__nv_bfloat16*>(st + kOffZt + sw128_offset(t, 0)) = zh;
+          *reinterpret_cast<__nv_bfloat16*>(st + kOffZt + sw128_offset(t, 1)) = zl;
+        } else {
+          reinterpret_cast<float*>(st + kOffV)[t - 64] = __bfloat162float(zh) + __bfloat162float(zl);
+        }
       }
       if (row < rows) {
         uint8_t* rp = st + row * 128;
@@ -244,13 +245,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_output_kernel(const __grid_con
       uint8_t* st = gb + stage * kStageBytes;
       if (t < rows) {
         const float s = s0 + s1;
-        const float cs = a.col_scale ? a.col_scale[i] * a.inv_stack_scale : 1.f;
-        float scale = cs, gamma = 0.f;
+        const float4 info = *reinterpret_cast<const float4*>(st + kOffInfo);
+        float scale = info.x, gamma = 0.f;
         if (p.norm == MHLA_NORM_DIVISIVE) {
-          scale = cs * __frcp_rn(s);
+          scale = info.x * __frcp_rn(s);
         } else if (p.norm == MHLA_NORM_MALA) {
           scale = 1.f + __frcp_rn(s);                       // beta
-          gamma = s / ((float)p.nb * a.rowsum[i]);
+          gamma = s / info.y;                               // s / n~_i
         }
         const float* vs = reinterpret_cast<const float*>(st + kOffV) + 32 * h;
         uint8_t* rp = st + t * 128;
@@ -317,11 +318,10 @@ int launch_tc_output(const Plan& p, const ChunkShape& c, const void* q, const Tc
   const uint32_t box3[3] = {64, 64, 1};
   if ((e = encode_tmap_bf16(&a.tmB_hi, b.mixed_hi, 3, dims3, str3, box3)) != 0) return e;
   if ((e = encode_tmap_bf16(&a.tmB_lo, b.mixed_lo, 3, dims3, str3, box3)) != 0) return e;
-  a.mixed_hi = b.mixed_hi;
-  a.mixed_lo = b.mixed_lo;
-  a.rowsum = b.rowsum;
-  a.col_scale = b.f16 ? b.mc_scale : nullptr;
-  a.inv_stack_scale = 1.f / b.stack_scale;
+  const uint32_t boxA[3] = {64, 2, 1};
+  if ((e = encode_tmap_plain(&a.tmA_hi, b.mixed_hi, 3, dims3, str3, boxA)) != 0) return e;
+  if ((e = encode_tmap_plain(&a.tmA_lo, b.mixed_lo, 3, dims3, str3, boxA)) != 0) return e;
+  a.blkinfo = b.blkinfo;
   a.units = p.BH * p.M * c.per_block;
   a.use_lo = p.norm == MHLA_NORM_MALA;
   a.c = c;
