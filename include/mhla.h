@@ -141,6 +141,25 @@ mhla_status mhla_forward(const void* q, const void* k, const void* v, const floa
                          const mhla_params* p, void* out, void* workspace,
                          size_t workspace_bytes, void* stream);
 
+/* Allocation-free variant of mhla_forward for callers that cannot allocate
+ * device memory when they call (allocator callbacks and out-of-memory
+ * handlers, plugin hosts that forbid cudaMalloc after start-up, real-time
+ * loops that must not touch the allocator).  The pages have no counterpart:
+ * it is the same forward pass, with its scratch memory taken from a 32 MiB
+ * static device array inside this library instead of a caller workspace.
+ *   q, k, v, mc, p, out, stream   as for mhla_forward
+ * Allocates nothing: no cudaMalloc, cudaMallocAsync or cudaFree.  Problems
+ * whose mhla_workspace_bytes(p) exceeds 32 MiB return MHLA_ERR_WORKSPACE and
+ * enqueue nothing.  The first call on a device (that device current) looks up
+ * the array's device address with cudaGetSymbolAddress; make that first call
+ * before any stream capture.  Every GPU that loads the library holds the
+ * array until the process exits.  All calls on a device share the one array,
+ * so calls whose work overlaps on the GPU (different streams, or different
+ * host threads) race and must be serialised by the caller.  Nothing in the
+ * array has to start at zero: each call overwrites every byte it reads. */
+mhla_status mhla_forward_noalloc(const void* q, const void* k, const void* v, const float* mc,
+                                 const mhla_params* p, void* out, void* stream);
+
 /* Device buffer mhla_forward_host needs: room for Q, K, V, Mc, out and the
  * workspace, each 256-byte aligned. */
 mhla_status mhla_host_buffer_bytes(const mhla_params* p, size_t* bytes);

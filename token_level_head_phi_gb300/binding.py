@@ -78,6 +78,8 @@ SIGNATURES = [
     ("mhla_forward", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                     ctypes.POINTER(MhlaParams), ctypes.c_void_p, ctypes.c_void_p,
                                     ctypes.c_size_t, ctypes.c_void_p]),
+    ("mhla_forward_noalloc", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                            ctypes.POINTER(MhlaParams), ctypes.c_void_p, ctypes.c_void_p]),
     ("mhla_host_buffer_bytes", ctypes.c_int, [ctypes.POINTER(MhlaParams), ctypes.POINTER(ctypes.c_size_t)]),
     ("mhla_forward_host", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                          ctypes.POINTER(MhlaParams), ctypes.c_void_p, ctypes.c_void_p,
@@ -204,6 +206,25 @@ def mhla_forward_raw(q_ptr: int, k_ptr: int, v_ptr: int, mc_ptr: int, p: MhlaPar
     """Direct call with raw device pointers; returns the status code."""
     return load().mhla_forward(q_ptr, k_ptr, v_ptr, mc_ptr, ctypes.byref(p), out_ptr, ws_ptr, ws_bytes,
                                stream_handle)
+
+
+def mhla_forward_noalloc(q, k, v, mc, grid, block, norm: str = "divisive", feature_map: str = "elu1",
+                         variant: str = "auto", out=None, stream=None):
+    """mhla_forward without any device allocation by the library: its scratch
+    is a static 32 MiB device array (see include/mhla.h).  For callers that
+    cannot allocate at call time; ``out`` must be given by such callers (when
+    it is None this wrapper allocates it with torch, for convenience)."""
+    import torch
+    p = _params_for(q, grid, block, feature_map, norm, variant)
+    if out is None:
+        out = torch.empty_like(q)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    status = load().mhla_forward_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), mc.data_ptr(), ctypes.byref(p),
+                                         out.data_ptr(), handle)
+    _check(status, "mhla_forward_noalloc")
+    return out
 
 
 def mhla_forward_host(q, k, v, mc, grid, block, norm: str = "divisive", feature_map: str = "elu1",
