@@ -177,10 +177,16 @@ def traffic_table():
     return table
 
 
+KERNEL_HEADERS = ["token_level_head_phi_gb300/csrc/tc_common.cuh", "token_level_head_phi_gb300/csrc/common.cuh",
+                  "token_level_head_phi_gb300/csrc/plan.h", "token_level_head_phi_gb300/csrc/tc_host.h"]
+
+
 def source_hash(relpath: str) -> str:
+    """Hash of a kernel's source file and the headers every kernel includes."""
     h = hashlib.sha256()
-    with open(os.path.join(ROOT, relpath), "rb") as fh:
-        h.update(fh.read())
+    for path in [relpath] + KERNEL_HEADERS:
+        with open(os.path.join(ROOT, path), "rb") as fh:
+            h.update(fh.read())
     return h.hexdigest()[:12]
 
 
