@@ -324,6 +324,22 @@ __device__ __forceinline__ float phi_map(float x, int fmap) {
   return fmap == MHLA_FEATURE_IDENTITY ? x : phi_elu1_fast(x);
 }
 
+// phi = ELU+1 of two bf16 values, returned as bf16x2 rounded to nearest:
+// max(x, 0) and min(x, 0) are exact in bf16x2 arithmetic, exp runs in
+// float32 on the min part and is rounded once, and the final bf16x2 add is
+// exact because one of its two terms is zero (x <= 0) or exp(0) = 1 (x > 0,
+// where x + 1 is rounded once) -- the same result as rounding the float32
+// value max(x, 0) + exp(min(x, 0)).
+__device__ __forceinline__ uint32_t phi2_elu1_bf16(uint32_t w) {
+  const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(&w);
+  const __nv_bfloat162 zero = __float2bfloat162_rn(0.f);
+  const __nv_bfloat162 mx = __hmax2(x, zero);
+  const float2 mn = __bfloat1622float2(__hmin2(x, zero));
+  const __nv_bfloat162 e = __floats2bfloat162_rn(__expf(mn.x), __expf(mn.y));
+  const __nv_bfloat162 r = __hadd2(mx, e);
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+
 // Two bf16 (one 32-bit word) -> float2, exact.
 __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w) {
   return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));

@@ -204,10 +204,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc_output_kernel(const __grid_con
           const uint32_t off = ((4 * half + j + row) & 7) << 4;
           uint4 x = *reinterpret_cast<uint4*>(rp + off);
           uint32_t* xp = &x.x;
+          if (p.fmap == MHLA_FEATURE_ELU1) {
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const float2 f = bf16x2_to_float2(xp[q]);
-            xp[q] = pack_bf16x2(phi_map(f.x, p.fmap), phi_map(f.y, p.fmap));
+            for (int q = 0; q < 4; ++q) xp[q] = phi2_elu1_bf16(xp[q]);
+          } else {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const float2 f = bf16x2_to_float2(xp[q]);
+              xp[q] = pack_bf16x2(phi_map(f.x, p.fmap), phi_map(f.y, p.fmap));
+            }
           }
           *reinterpret_cast<uint4*>(rp + off) = x;
         }

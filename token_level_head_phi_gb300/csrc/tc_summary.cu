@@ -109,6 +109,11 @@ template <bool kLo>
 __device__ __forceinline__ void phi_chunk(uint4& x, uint4& lo, int fmap) {
   uint32_t* xp = &x.x;
   uint32_t* lp = &lo.x;
+  if (!kLo && fmap == MHLA_FEATURE_ELU1) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) xp[q] = phi2_elu1_bf16(xp[q]);
+    return;
+  }
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     const float2 f = bf16x2_to_float2(xp[q]);
@@ -327,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_summary_kernel(const __grid_co
       named_sync(1, kEpiThreads);
       if (e < 2) {
         // row r of S_b and z_b[r]
-        bool overflow = false;
+        float amax = 0.f;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           const float* src = j < 4 ? &s0[8 * j] : &s1[8 * (j - 4)];
@@ -337,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_summary_kernel(const __grid_co
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               const float x0 = src[2 * q] * a.stack_scale, x1 = src[2 * q + 1] * a.stack_scale;
-              overflow |= fabsf(x0) > 65504.f || fabsf(x1) > 65504.f;
+              amax = fmaxf(amax, fmaxf(fabsf(x0), fabsf(x1)));
               __half2 h = __floats2half2_rn(x0, x1);
               hp[q] = *reinterpret_cast<uint32_t*>(&h);
             }
@@ -348,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_summary_kernel(const __grid_co
           *reinterpret_cast<uint4*>(st_hi + off) = hv;
           if (kLo) *reinterpret_cast<uint4*>(st_lo + off) = lv;
         }
-        if (overflow) report_error(a.err, MHLA_ERR_OVERFLOW, 0x106);
+        if (!(amax <= 65504.f)) report_error(a.err, MHLA_ERR_OVERFLOW, 0x106);
         const __nv_bfloat16 zh = __float2bfloat16_rn(zval);
         *reinterpret_cast<__nv_bfloat16*>(st_hi + 8192 + sw128_offset(0, r)) = zh;
         *reinterpret_cast<__nv_bfloat16*>(st_lo + 8192 + sw128_offset(0, r)) =
