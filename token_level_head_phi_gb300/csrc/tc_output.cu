@@ -34,7 +34,7 @@ namespace {
 
 using namespace tc;
 
-constexpr int kStages = 4;
+constexpr int kStages = 5;
 constexpr int kThreads = 640;
 constexpr int kXfThreads = 256;                    // warps 4..11
 constexpr int kEpiThreads = 256;                   // warps 12..19
@@ -51,7 +51,8 @@ constexpr uint32_t kStageBytes = kOffV + 1024;
 static_assert(kOffInfo + 16 <= kStageBytes, "stage layout");
 constexpr uint32_t kBars = kStages * kStageBytes;
 constexpr uint32_t kSmemBytes = kBars + 256 + 1024;
-constexpr uint32_t kAccStride = 128;               // TMEM columns per stage (80 used)
+constexpr int kAccSlots = 4;                       // TMEM accumulators (128 columns each, 80 used)
+constexpr uint32_t kAccStride = 128;
 constexpr uint32_t kTmemCols = 512;
 
 static_assert(kStageBytes % 1024 == 0, "stage alignment");
@@ -77,8 +78,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_output_kernel(const __grid_con
   auto tready = [&](int s) { return bars + 8u * (kStages + s); };
   auto mmadone = [&](int s) { return bars + 8u * (2 * kStages + s); };
   auto empty = [&](int s) { return bars + 8u * (3 * kStages + s); };
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gb + kBars + 8 * (4 * kStages));
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(gb + kBars + 8 * (4 * kStages) + 8);
+  auto accempty = [&](int x) { return bars + 8u * (4 * kStages + x); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gb + kBars + 8 * (4 * kStages + kAccSlots));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gb + kBars + 8 * (4 * kStages + kAccSlots) + 8);
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -97,6 +99,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_output_kernel(const __grid_con
       mbar_init(mmadone(s), 1);
       mbar_init(empty(s), 1);
     }
+    for (int x = 0; x < kAccSlots; ++x) mbar_init(accempty(x), 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -152,13 +155,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_output_kernel(const __grid_con
       // --------------------------------------------------------------- MMA
       const uint32_t idesc80 = idesc_bf16_f32(128, 80, false, true);
       const uint32_t idesc64 = idesc_bf16_f32(128, 64, false, true);
-      int stage = 0;
-      uint32_t phase = 0;
+      int stage = 0, slot = 0;
+      uint32_t phase = 0, slotph = 0;
       for (int w = blockIdx.x; w < a.units; w += gridDim.x) {
         if (!mbar_wait(tready(stage), phase, a.err, 0x302, abort_flag)) break;
+        if (!mbar_wait(accempty(slot), slotph ^ 1u, a.err, 0x306, abort_flag)) break;
         tc_fence_after();
         const uint32_t st = base + (uint32_t)stage * kStageBytes;
-        const uint32_t d = tmem + (uint32_t)stage * kAccStride;
+        const uint32_t d = tmem + (uint32_t)slot * kAccStride;
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
           const uint64_t ad = sdesc_sw128(st + (uint32_t)ks * 32u, 0u, 1024u);
@@ -171,6 +175,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_output_kernel(const __grid_con
         if (++stage == kStages) {
           stage = 0;
           phase ^= 1u;
+        }
+        if (++slot == kAccSlots) {
+          slot = 0;
+          slotph ^= 1u;
         }
       }
     }
@@ -230,7 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_output_kernel(const __grid_con
     const int h = (warp - 12) >> 2;     // output features 32h .. 32h+31
     const int t = 32 * q4 + lane;       // token row = TMEM lane
     const int et = threadIdx.x - 384;
-    int stage = 0, prev = -1;
+    int stage = 0, prev = -1, slot = 0;
     uint32_t phase = 0;
     for (int w = blockIdx.x; w < a.units; w += gridDim.x) {
       const int u = w / per_head;
@@ -243,7 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_output_kernel(const __grid_con
       if (!named_all(3, kEpiThreads, ok)) break;
       tc_fence_after();
       float o[32], s0, s1;
-      const uint32_t taddr = tmem + (uint32_t)stage * kAccStride + ((uint32_t)(32 * q4) << 16);
+      const uint32_t taddr = tmem + (uint32_t)slot * kAccStride + ((uint32_t)(32 * q4) << 16);
       tmem_ld32(taddr + 32u * h, o);
       tmem_ld2(taddr + 64u, s0, s1);
       tmem_wait_ld();
@@ -280,6 +288,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_output_kernel(const __grid_con
       fence_proxy_async();
       tc_fence_before();
       named_sync(3, kEpiThreads);
+      if (et == 0) mbar_arrive(accempty(slot));  // every epilogue thread has read the accumulator
+      if (++slot == kAccSlots) slot = 0;
       if (et == 0) {
         const int bx = i % p.Mw, by = (i / p.Mw) % p.Mh, bz = i / (p.Mw * p.Mh);
         const int x0 = bx * p.bw + (c % a.c.ncx) * a.c.cw;

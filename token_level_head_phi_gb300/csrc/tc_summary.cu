@@ -53,12 +53,13 @@ constexpr int kN = 80;                                  // MMA N: 64 value featu
 // tile per stage (MALA); the stage count shrinks to keep everything resident.
 template <bool kLo>
 struct Layout {
-  static constexpr int kStages = kLo ? 3 : 4;
+  static constexpr int kStages = kLo ? 3 : 5;
+  static constexpr int kStagingBufs = kLo ? 2 : 1;
   static constexpr uint32_t kStageBytes = (kLo ? 3 : 2) * kTile;  // K, V [, K lo]
   static constexpr uint32_t kOnesA = kStages * kStageBytes;         // ones tile of A (rows 64..127)
   static constexpr uint32_t kOnesB = kOnesA + kTile;                // ones tile of B (cols 64..79)
-  static constexpr uint32_t kStaging = kOnesB + kTile;              // 2 staging buffers
-  static constexpr uint32_t kBars = kStaging + 2 * kStagingBuf;
+  static constexpr uint32_t kStaging = kOnesB + kTile;              // staging buffers
+  static constexpr uint32_t kBars = kStaging + kStagingBufs * kStagingBuf;
   static constexpr uint32_t kSmemBytes = kBars + 256 + 1024;        // + barriers + alignment slack
 };
 
@@ -326,9 +327,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_summary_kernel(const __grid_co
         accph ^= 1u;
       }
 
-      uint8_t* st_hi = gb + L::kStaging + (it & 1) * kStagingBuf;
+      uint8_t* st_hi = gb + L::kStaging + (it % L::kStagingBufs) * kStagingBuf;
       uint8_t* st_lo = st_hi + kStagePart;
-      if (et == 0) bulk_wait_read<1>();
+      if (et == 0) {
+        // the store that last read this staging buffer has finished reading it
+        if (L::kStagingBufs == 2) bulk_wait_read<1>();
+        else bulk_wait_read<0>();
+      }
       named_sync(1, kEpiThreads);
       if (e < 2) {
         // row r of S_b and z_b[r]
