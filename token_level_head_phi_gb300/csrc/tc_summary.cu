@@ -19,7 +19,7 @@
 // Persistent, warp-specialised CTA (one per SM, 512 threads):
 //   warp 0       TMA producer (K and V tiles of one token chunk per stage)
 //   warp 1       TMEM allocation + MMA issue (one elected thread)
-//   warps 4-6    epilogue: TMEM rows 0..95 -> S_b as fp16 (scaled by
+//   warps 4-6, 16-17  epilogue: TMEM rows 0..64 -> S_b as fp16 (scaled by
 //                2^-ceil(log2 n), DIVISIVE/NONE) or bf16 hi + lo (MALA),
 //                z_b and v_b as bf16 hi + lo -> swizzled staging tiles ->
 //                TMA stores into the summary stacks
@@ -40,8 +40,8 @@ namespace {
 
 using namespace tc;
 
-constexpr int kThreads = 512;
-constexpr int kEpiThreads = 96;                         // warps 4..6
+constexpr int kThreads = 640;
+constexpr int kEpiThreads = 160;                        // warps 4, 5, 6, 16, 17
 constexpr int kXfThreads = 256;                         // warps 8..15
 constexpr uint32_t kTile = 128 * 128;                   // 128 rows of 128 bytes
 constexpr uint32_t kStagePart = 8192 + 1024;            // staging: S 8 KB + zv 1 KB
@@ -267,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_summary_kernel(const __grid_co
         }
       }
     }
-  } else if (warp >= 8) {
+  } else if (warp >= 8 && warp < 16) {
     // ------------------------------------------------ phi(K) transform
     // thread t: row t/2, chunks 4*(t%2) .. +3 at physical positions rotated
     // by the row so that 8 consecutive threads hit 8 distinct bank groups
@@ -301,10 +301,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_summary_kernel(const __grid_co
         }
       }
     }
-  } else if (warp >= 4 && warp < 7) {
+  } else if (warp == 4 || warp == 5 || warp == 6 || warp == 16 || warp == 17) {
     // ------------------------------------------------------------ epilogue
-    const int e = warp - 4;
-    const int et = threadIdx.x - 128;
+    // warps 4/16 -> rows 0..31, 5/17 -> rows 32..63 (columns 0..31 / 32..63),
+    // warp 6 -> row 64 (v_b)
+    const int e = warp & 3;                   // TMEM lane quarter
+    const int h = warp >= 16 ? 1 : 0;         // column half of S_b
+    const int et = warp < 16 ? threadIdx.x - 128 : 96 + threadIdx.x - 512;
     const int r = 32 * e + lane;  // TMEM lane = row of D
     int acc = 0, it = 0;
     uint32_t accph = 0;
@@ -316,8 +319,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_summary_kernel(const __grid_co
       tc_fence_after();
       const uint32_t taddr = tmem + (uint32_t)acc * 128u + ((uint32_t)(32 * e) << 16);
       float s0[32], s1[32], zval = 0.f, znext;
-      tmem_ld32(taddr, s0);
-      tmem_ld32(taddr + 32u, s1);
+      tmem_ld32(taddr + 32u * h, s0);
+      if (e == 2) tmem_ld32(taddr + 32u, s1);
       tmem_ld2(taddr + 64u, zval, znext);
       tmem_wait_ld();
       tc_fence_before();
@@ -336,11 +339,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_summary_kernel(const __grid_co
       }
       named_sync(1, kEpiThreads);
       if (e < 2) {
-        // row r of S_b and z_b[r]
+        // row r of S_b (columns 32h .. 32h+31) and, for h = 0, z_b[r]
         float amax = 0.f;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float* src = j < 4 ? &s0[8 * j] : &s1[8 * (j - 4)];
+        for (int jj = 0; jj < 4; ++jj) {
+          const int j = 4 * h + jj;
+          const float* src = &s0[8 * jj];
           uint4 hv, lv;
           if (a.f16) {
             uint32_t* hp = &hv.x;
@@ -359,10 +363,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_summary_kernel(const __grid_co
           if (kLo) *reinterpret_cast<uint4*>(st_lo + off) = lv;
         }
         if (!(amax <= 65504.f)) report_error(a.err, MHLA_ERR_OVERFLOW, 0x106);
-        const __nv_bfloat16 zh = __float2bfloat16_rn(zval);
-        *reinterpret_cast<__nv_bfloat16*>(st_hi + 8192 + sw128_offset(0, r)) = zh;
-        *reinterpret_cast<__nv_bfloat16*>(st_lo + 8192 + sw128_offset(0, r)) =
-            __float2bfloat16_rn(zval - __bfloat162float(zh));
+        if (h == 0) {
+          const __nv_bfloat16 zh = __float2bfloat16_rn(zval);
+          *reinterpret_cast<__nv_bfloat16*>(st_hi + 8192 + sw128_offset(0, r)) = zh;
+          *reinterpret_cast<__nv_bfloat16*>(st_lo + 8192 + sw128_offset(0, r)) =
+              __float2bfloat16_rn(zval - __bfloat162float(zh));
+        }
       } else if (lane == 0) {
         // row 64 of D: v_b (every row 64..127 holds the same values; the
         // low-residual MMA of MALA adds them twice)
