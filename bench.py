@@ -150,7 +150,7 @@ def phase_bytes(w: wl.Workload, info, variant: int):
         mc = 4 * M * M
     else:
         mala = w.norm == "mala"
-        stack = U * rows * (d * d * 2 * (2 if mala else 1) + 2 * d * 2 * 2)
+        stack = U * rows * R * 2 * (2 if mala else 1)
         mixed_w = U * M * (R * 2 + (R if mala else 2 * d) * 2)
         mixed_r = U * M * (d * d * 2 * (2 if mala else 1) + 2 * d * 2 * 2)
         mc = 4 * M * M

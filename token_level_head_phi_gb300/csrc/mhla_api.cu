@@ -152,18 +152,13 @@ mhla_status make_plan(const mhla_params* prm, Plan* p) {
     off = align_up(off + sizeof(float) * (size_t)p->M);
   } else {
     const size_t rows = (size_t)p->BH * p->M * p->splits;
-    const size_t stack_s = 2 * rows * d * d;
-    const size_t stack_aux = 2 * rows * 2 * d;
+    const size_t stack = 2 * rows * p->R;
     const size_t mixed = 2 * (size_t)p->BH * p->M * p->R;
     const size_t mcq = 2 * (size_t)p->M * p->Qp;
     p->off_stack = off;
-    off = align_up(off + stack_s);
+    off = align_up(off + stack);
     p->off_stack_lo = off;
-    if (p->norm == MHLA_NORM_MALA) off = align_up(off + stack_s);
-    p->off_aux_hi = off;
-    off = align_up(off + stack_aux);
-    p->off_aux_lo = off;
-    off = align_up(off + stack_aux);
+    if (p->norm == MHLA_NORM_MALA) off = align_up(off + stack);
     p->off_mixed = off;
     off = align_up(off + mixed);
     p->off_mixed_lo = off;
@@ -180,7 +175,7 @@ mhla_status make_plan(const mhla_params* prm, Plan* p) {
     off = align_up(off + sizeof(float) * (size_t)p->M);
     p->off_blkinfo = off;
     off = align_up(off + 16 * (size_t)p->M);
-    p->kernels = 5;
+    p->kernels = 4;
   }
   p->off_aux = off;
   p->ws_total = off;
@@ -208,10 +203,8 @@ mhla_status run_plan(const Plan& plan, const void* q, const void* k, const void*
   int e;
   if (p.variant == MHLA_VARIANT_MULTIPASS) {
     TcBuffers b;
-    b.stack_s = ws + p.off_stack;
-    b.stack_s_lo = p.norm == MHLA_NORM_MALA ? reinterpret_cast<__nv_bfloat16*>(ws + p.off_stack_lo) : nullptr;
-    b.aux_hi = reinterpret_cast<__nv_bfloat16*>(ws + p.off_aux_hi);
-    b.aux_lo = reinterpret_cast<__nv_bfloat16*>(ws + p.off_aux_lo);
+    b.stack = ws + p.off_stack;
+    b.stack_lo = p.norm == MHLA_NORM_MALA ? reinterpret_cast<__nv_bfloat16*>(ws + p.off_stack_lo) : nullptr;
     b.mixed_hi = reinterpret_cast<__nv_bfloat16*>(ws + p.off_mixed);
     b.mixed_lo = reinterpret_cast<__nv_bfloat16*>(ws + p.off_mixed_lo);
     b.mc_f16 = reinterpret_cast<__half*>(ws + p.off_mc_f16);
@@ -227,8 +220,7 @@ mhla_status run_plan(const Plan& plan, const void* q, const void* k, const void*
     if ((e = launch_tc_prep(p, mc, b, s)) != 0) return cuda_fail((cudaError_t)e);
     if ((e = launch_tc_summary(p, p.chunk, k, v, b, s)) != 0) return cuda_fail((cudaError_t)e);
     record_event(1, s);
-    if ((e = launch_tc_mix(p, b, false, s)) != 0) return cuda_fail((cudaError_t)e);
-    if ((e = launch_tc_mix(p, b, true, s)) != 0) return cuda_fail((cudaError_t)e);
+    if ((e = launch_tc_mix(p, b, s)) != 0) return cuda_fail((cudaError_t)e);
     record_event(2, s);
     if ((e = launch_tc_output(p, p.chunk, q, b, out, s)) != 0) return cuda_fail((cudaError_t)e);
     record_event(3, s);

@@ -48,7 +48,7 @@ struct Plan {
   size_t ws_total;
   size_t off_stack, off_mixed, off_rowsum, off_aux;
   // tensor-core path buffers
-  size_t off_stack_lo, off_aux_hi, off_aux_lo, off_mixed_lo;
+  size_t off_stack_lo, off_mixed_lo;
   size_t off_mc_f16, off_mc_scale, off_mc_hi, off_mc_lo, off_blkinfo;
   int Qp;
   int f16_mix;        // S part of the mixing in fp16 (DIVISIVE and NONE)

@@ -37,14 +37,13 @@ int num_sms();
 ChunkShape choose_chunk(const Plan& p);
 
 // Workspace pointers of the tensor-core path.  Stack rows are block pieces
-// (Q = M * splits per head).
+// (Q = M * splits per head), each a record of R = d*d + 2d values: S_b
+// (row-major over (k, c)), z_b, v_b.
 struct TcBuffers {
-  void* stack_s;             // [BH][Q][d*d] S_b: fp16 scaled by stack_scale, or bf16 (MALA)
-  __nv_bfloat16* stack_s_lo; // [BH][Q][d*d] low bf16 residual of S_b (MALA only, else nullptr)
-  __nv_bfloat16* aux_hi;     // [BH][Q][2d]  z_b, v_b (bf16 high parts)
-  __nv_bfloat16* aux_lo;     // [BH][Q][2d]  low residuals
-  __nv_bfloat16* mixed_hi;   // [BH][M][R]   S~_i, z~_i, v~_i high parts
-  __nv_bfloat16* mixed_lo;   // [BH][M][R]   low residuals (S~ part for MALA only)
+  void* stack;               // [BH][Q][R]: fp16(x * stack_scale) (DIVISIVE/NONE) or bf16 high part (MALA)
+  __nv_bfloat16* stack_lo;   // [BH][Q][R] low bf16 residual (MALA only, else nullptr)
+  __nv_bfloat16* mixed_hi;   // [BH][M][R] S~_i, z~_i, v~_i high parts
+  __nv_bfloat16* mixed_lo;   // [BH][M][R] low residuals (S~ part for MALA only)
   __half* mc_f16;            // [M][Qp] Mc[i][q / splits] * 2^-e_i in fp16
   float* mc_scale;           // [M] 2^e_i (power of two with max_b |Mc[i][b]| <= 2^e_i)
   __nv_bfloat16* mc_hi;      // [M][Qp] bf16(Mc[i][q / splits])
@@ -52,15 +51,14 @@ struct TcBuffers {
   float* rowsum;             // [M] sum_b (hi + lo)(Mc[i][b])
   float4* blkinfo;           // [M] {scale the output step applies to S~_i, n~_i, 0, 0}
   int Qp;                    // padded row pitch of the Mc copies
-  bool f16;                  // S part of the stack in fp16 (DIVISIVE and NONE)
+  bool f16;                  // fp16 stack and mixing (DIVISIVE and NONE)
   float stack_scale;         // 2^-ceil(log2(tokens per piece))
 };
 
 int launch_tc_prep(const Plan& p, const float* mc, const TcBuffers& b, cudaStream_t s);
 int launch_tc_summary(const Plan& p, const ChunkShape& c, const void* k, const void* v, const TcBuffers& b,
                       cudaStream_t s);
-// Mixing of the S part (fp16 or split bf16) and of the z/v part (split bf16).
-int launch_tc_mix(const Plan& p, const TcBuffers& b, bool aux_part, cudaStream_t s);
+int launch_tc_mix(const Plan& p, const TcBuffers& b, cudaStream_t s);
 int launch_tc_output(const Plan& p, const ChunkShape& c, const void* q, const TcBuffers& b, void* out,
                      cudaStream_t s);
 

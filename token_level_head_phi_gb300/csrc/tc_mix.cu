@@ -10,10 +10,10 @@
 //   A = X^T  : MN-major (r contiguous), two 64-wide atoms per 128-row tile
 //   B = McExp: K-major (q contiguous), N = up to 256 query blocks per tile
 // Two precisions:
-//   kF16  (S part, DIVISIVE/NONE): X = fp16(S * 2^-s), B = fp16(Mc * 2^-e_i);
-//         one MMA per K step, D rescaled by 2^(s + e_i) in the epilogue.
-//   split (z/v part always, S part for MALA): X and Mc as bf16 high + low
-//         parts, D = Xh Mh + Xh Ml + Xl Mh.
+//   kF16  (DIVISIVE/NONE): X = fp16(x * 2^-s), B = fp16(Mc * 2^-e_i); one MMA
+//         per K step; Mixed keeps the factor 2^-(s + e_i), which the output
+//         step multiplies back.
+//   split (MALA): X and Mc as bf16 high + low parts, D = Xh Mh + Xh Ml + Xl Mh.
 // The epilogue writes Mixed as bf16 (plus the low residual where the output
 // step needs it): 32 query blocks x 128 r at a time, transposed through a
 // shared-memory tile and stored by TMA.  In the fp16 case Mixed holds
@@ -197,6 +197,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_mix_kernel(const __grid_consta
       const int rem = w % per_head;
       const int r0 = a.r_off + (rem / a.itiles) * 128;
       const int i0 = (rem % a.itiles) * a.NT;
+      const bool lo = a.write_lo || r0 >= p.d * p.d;  // z~, v~ always carry their low residual
       ok = mbar_wait(accfull(acc), accph, a.err, 0x204, abort_flag);
       if (!(ok = named_all(1 + g, 128, ok))) break;
       tc_fence_after();
@@ -212,14 +213,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_mix_kernel(const __grid_consta
         for (int j = 0; j < 32; ++j) {
           const __nv_bfloat16 h = __float2bfloat16_rn(v[j]);
           reinterpret_cast<__nv_bfloat16*>(stg)[j * 128 + rl] = h;
-          if (a.write_lo)
+          if (lo)
             reinterpret_cast<__nv_bfloat16*>(stg + 8192)[j * 128 + rl] = __float2bfloat16_rn(v[j] - __bfloat162float(h));
         }
         fence_proxy_async();
         named_sync(1 + g, 128);
         if (gt == 0) {
           tma_store_3d(&a.tmO, stg_addr, r0, i0 + c0, u);
-          if (a.write_lo) tma_store_3d(&a.tmO_lo, stg_addr + 8192, r0, i0 + c0, u);
+          if (lo) tma_store_3d(&a.tmO_lo, stg_addr + 8192, r0, i0 + c0, u);
           bulk_commit();
         }
       }
@@ -301,14 +302,14 @@ int launch_tc_prep(const Plan& p, const float* mc, const TcBuffers& b, cudaStrea
   return (int)cudaGetLastError();
 }
 
-int launch_tc_mix(const Plan& p, const TcBuffers& b, bool aux_part, cudaStream_t s) {
+int launch_tc_mix(const Plan& p, const TcBuffers& b, cudaStream_t s) {
   MixArgs a;
   memset(&a, 0, sizeof(a));
   const int Q = p.M * p.splits;
-  const bool f16 = b.f16 && !aux_part;
-  const int W = aux_part ? 2 * p.d : p.d * p.d;
-  const void* src = aux_part ? (const void*)b.aux_hi : b.stack_s;
-  const void* src_lo = aux_part ? (const void*)b.aux_lo : (const void*)b.stack_s_lo;
+  const bool f16 = b.f16;
+  const int W = p.R;
+  const void* src = b.stack;
+  const void* src_lo = b.stack_lo;
   const uint64_t dimsA[3] = {(uint64_t)W, (uint64_t)Q, (uint64_t)p.BH};
   const uint64_t strA[2] = {2ull * W, 2ull * W * Q};
   const uint32_t boxA[3] = {64, 64, 1};
@@ -341,8 +342,8 @@ int launch_tc_mix(const Plan& p, const TcBuffers& b, bool aux_part, cudaStream_t
   a.rtiles = W / 128;
   a.kchunks = (Q + 63) / 64;
   a.units = p.BH * a.rtiles * a.itiles;
-  a.r_off = aux_part ? p.d * p.d : 0;
-  a.write_lo = aux_part || p.norm == MHLA_NORM_MALA;
+  a.r_off = 0;
+  a.write_lo = p.norm == MHLA_NORM_MALA;
   const uint32_t btile = (uint32_t)NT * 128u;
   if (f16) {
     a.off_b = kATile;

@@ -19,10 +19,10 @@
 // Persistent, warp-specialised CTA (one per SM, 512 threads):
 //   warp 0       TMA producer (K and V tiles of one token chunk per stage)
 //   warp 1       TMEM allocation + MMA issue (one elected thread)
-//   warps 4-6, 16-17  epilogue: TMEM rows 0..64 -> S_b as fp16 (scaled by
-//                2^-ceil(log2 n), DIVISIVE/NONE) or bf16 hi + lo (MALA),
-//                z_b and v_b as bf16 hi + lo -> swizzled staging tiles ->
-//                TMA stores into the summary stacks
+//   warps 4-6, 16-17  epilogue: TMEM rows 0..64 -> the record (S_b, z_b,
+//                v_b) as fp16 scaled by 2^-ceil(log2 n) (DIVISIVE/NONE) or as
+//                bf16 high + low parts (MALA) -> swizzled staging tiles ->
+//                TMA stores into the summary stack
 //   warps 8-15   phi(K) transform, two threads per token row
 // Each CTA walks work units (head, block, piece) with a static stride; long
 // blocks are cut into pieces whose partial summaries the mixing step adds.
@@ -65,11 +65,10 @@ struct Layout {
 
 struct SummaryArgs {
   CUtensorMap tmK, tmV;              // 5D (64, Wg, Hg, T, BH), box (64, cw, ch, ct, 1)
-  CUtensorMap tmS, tmS_lo;           // 2D view (64, BH*Q*64) of the S stack, box (64, 64)
-  CUtensorMap tmZV_hi, tmZV_lo;      // 2D view (64, BH*Q*2) of the z/v stack, box (64, 2)
+  CUtensorMap tmS, tmS_lo;           // 2D view (64, BH*Q*66) of the stack, box (64, 64): S_b rows
+  CUtensorMap tmZV, tmZV_lo;         // same view, box (64, 2): the z_b and v_b rows
   int units, splits, cpp;            // work units, pieces per block, chunks per piece
-  int f16;                           // S stored as fp16(S * stack_scale); else bf16 (+ lo)
-  float stack_scale;
+  float stack_scale;                 // fp16 stack: values are stored times this power of two
   ChunkShape c;
   unsigned int* err;
 };
@@ -346,49 +345,71 @@ __global__ void __launch_bounds__(kThreads, 1) tc_summary_kernel(const __grid_co
           const int j = 4 * h + jj;
           const float* src = &s0[8 * jj];
           uint4 hv, lv;
-          if (a.f16) {
+          if (!kLo) {
             uint32_t* hp = &hv.x;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               const float x0 = src[2 * q] * a.stack_scale, x1 = src[2 * q + 1] * a.stack_scale;
               amax = fmaxf(amax, fmaxf(fabsf(x0), fabsf(x1)));
-              __half2 h = __floats2half2_rn(x0, x1);
-              hp[q] = *reinterpret_cast<uint32_t*>(&h);
+              __half2 hh = __floats2half2_rn(x0, x1);
+              hp[q] = *reinterpret_cast<uint32_t*>(&hh);
             }
           } else {
-            split8(src, hv, lv, 1.f, kLo);
+            split8(src, hv, lv, 1.f, true);
           }
           const uint32_t off = (uint32_t)r * 128u + ((uint32_t)((j ^ (r & 7)) & 7) << 4);
           *reinterpret_cast<uint4*>(st_hi + off) = hv;
           if (kLo) *reinterpret_cast<uint4*>(st_lo + off) = lv;
         }
-        if (!(amax <= 65504.f)) report_error(a.err, MHLA_ERR_OVERFLOW, 0x106);
         if (h == 0) {
-          const __nv_bfloat16 zh = __float2bfloat16_rn(zval);
-          *reinterpret_cast<__nv_bfloat16*>(st_hi + 8192 + sw128_offset(0, r)) = zh;
-          *reinterpret_cast<__nv_bfloat16*>(st_lo + 8192 + sw128_offset(0, r)) =
-              __float2bfloat16_rn(zval - __bfloat162float(zh));
+          if (!kLo) {
+            const float zs = zval * a.stack_scale;
+            amax = fmaxf(amax, fabsf(zs));
+            *reinterpret_cast<__half*>(st_hi + 8192 + sw128_offset(0, r)) = __float2half_rn(zs);
+          } else {
+            const __nv_bfloat16 zh = __float2bfloat16_rn(zval);
+            *reinterpret_cast<__nv_bfloat16*>(st_hi + 8192 + sw128_offset(0, r)) = zh;
+            *reinterpret_cast<__nv_bfloat16*>(st_lo + 8192 + sw128_offset(0, r)) =
+                __float2bfloat16_rn(zval - __bfloat162float(zh));
+          }
         }
+        if (!(amax <= 65504.f)) report_error(a.err, MHLA_ERR_OVERFLOW, 0x106);
       } else if (lane == 0) {
         // row 64 of D: v_b (every row 64..127 holds the same values; the
         // low-residual MMA of MALA adds them twice)
+        float amax = 0.f;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
+          const float* src = j < 4 ? &s0[8 * j] : &s1[8 * (j - 4)];
           uint4 hv, lv;
-          split8(j < 4 ? &s0[8 * j] : &s1[8 * (j - 4)], hv, lv, kLo ? 0.5f : 1.f, true);
+          if (!kLo) {
+            uint32_t* hp = &hv.x;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const float x0 = src[2 * q] * a.stack_scale, x1 = src[2 * q + 1] * a.stack_scale;
+              amax = fmaxf(amax, fmaxf(fabsf(x0), fabsf(x1)));
+              __half2 hh = __floats2half2_rn(x0, x1);
+              hp[q] = *reinterpret_cast<uint32_t*>(&hh);
+            }
+          } else {
+            split8(src, hv, lv, 0.5f, true);
+          }
           const uint32_t off = 128u + ((uint32_t)((j ^ 1) & 7) << 4);
           *reinterpret_cast<uint4*>(st_hi + 8192 + off) = hv;
-          *reinterpret_cast<uint4*>(st_lo + 8192 + off) = lv;
+          if (kLo) *reinterpret_cast<uint4*>(st_lo + 8192 + off) = lv;
         }
+        if (!(amax <= 65504.f)) report_error(a.err, MHLA_ERR_OVERFLOW, 0x107);
       }
       fence_proxy_async();
       named_sync(1, kEpiThreads);
       if (et == 0) {
         const int srow = (uc.u * p.M + uc.b) * a.splits + (uc.c0 / a.cpp);
-        tma_store_2d(&a.tmS, smem_u32(st_hi), 0, srow * 64);
-        if (kLo) tma_store_2d(&a.tmS_lo, smem_u32(st_lo), 0, srow * 64);
-        tma_store_2d(&a.tmZV_hi, smem_u32(st_hi + 8192), 0, srow * 2);
-        tma_store_2d(&a.tmZV_lo, smem_u32(st_lo + 8192), 0, srow * 2);
+        tma_store_2d(&a.tmS, smem_u32(st_hi), 0, srow * 66);
+        tma_store_2d(&a.tmZV, smem_u32(st_hi + 8192), 0, srow * 66 + 64);
+        if (kLo) {
+          tma_store_2d(&a.tmS_lo, smem_u32(st_lo), 0, srow * 66);
+          tma_store_2d(&a.tmZV_lo, smem_u32(st_lo + 8192), 0, srow * 66 + 64);
+        }
         bulk_commit();
       }
     }
@@ -423,19 +444,17 @@ int launch_tc_summary(const Plan& p, const ChunkShape& c, const void* k, const v
   int e;
   if ((e = encode_tmap_bf16(&a.tmK, k, 5, dims5, str5, box5)) != 0) return e;
   if ((e = encode_tmap_bf16(&a.tmV, v, 5, dims5, str5, box5)) != 0) return e;
-  const uint64_t stack_rows = (uint64_t)p.BH * p.M * p.splits;
-  const uint64_t dimsS[2] = {64, stack_rows * 64};
-  const uint64_t dimsA[2] = {64, stack_rows * 2};
+  const uint64_t stack_rows = (uint64_t)p.BH * p.M * p.splits * 66ull;
+  const uint64_t dims2[2] = {64, stack_rows};
   const uint64_t str2[1] = {128};
   const uint32_t boxS[2] = {64, 64};
   const uint32_t boxZV[2] = {64, 2};
-  const bool lo = b.stack_s_lo != nullptr;  // MALA: phi(K) and S carry low residuals
-  if ((e = encode_tmap(&a.tmS, b.stack_s, 2, dimsS, str2, boxS, b.f16)) != 0) return e;
-  if ((e = encode_tmap_bf16(&a.tmS_lo, lo ? (const void*)b.stack_s_lo : b.stack_s, 2, dimsS, str2, boxS)) != 0)
-    return e;
-  if ((e = encode_tmap_bf16(&a.tmZV_hi, b.aux_hi, 2, dimsA, str2, boxZV)) != 0) return e;
-  if ((e = encode_tmap_bf16(&a.tmZV_lo, b.aux_lo, 2, dimsA, str2, boxZV)) != 0) return e;
-  a.f16 = b.f16;
+  const bool lo = b.stack_lo != nullptr;  // MALA: phi(K) and the stack carry low residuals
+  const void* lo_base = lo ? (const void*)b.stack_lo : b.stack;
+  if ((e = encode_tmap(&a.tmS, b.stack, 2, dims2, str2, boxS, b.f16)) != 0) return e;
+  if ((e = encode_tmap(&a.tmZV, b.stack, 2, dims2, str2, boxZV, b.f16)) != 0) return e;
+  if ((e = encode_tmap_bf16(&a.tmS_lo, lo_base, 2, dims2, str2, boxS)) != 0) return e;
+  if ((e = encode_tmap_bf16(&a.tmZV_lo, lo_base, 2, dims2, str2, boxZV)) != 0) return e;
   a.stack_scale = b.stack_scale;
   a.splits = p.splits;
   a.cpp = p.cpp;
