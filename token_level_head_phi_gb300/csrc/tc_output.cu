@@ -259,9 +259,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_output_kernel(const __grid_con
       if (t < rows) {
         const float s = s0 + s1;
         const float4 info = *reinterpret_cast<const float4*>(st + kOffInfo);
+        // info.x undoes the fp16 mixing's power-of-two scale; under DIVISIVE
+        // numerator and denominator carry the same scale, which cancels
         float scale = info.x, gamma = 0.f;
         if (p.norm == MHLA_NORM_DIVISIVE) {
-          scale = info.x * __frcp_rn(s);
+          scale = __frcp_rn(s);
         } else if (p.norm == MHLA_NORM_MALA) {
           scale = 1.f + __frcp_rn(s);                       // beta
           gamma = s / info.y;                               // s / n~_i
