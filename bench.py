@@ -1,7 +1,7 @@
 """Benchmark of the MHLA forward pass on GB300 (one JSON line on stdout).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-                    [--variant auto|simt|multipass] [--impl mine|reference]
+                    [--variant auto|simt|multipass|fused] [--impl mine|reference]
                     [--all-workloads] [--no-cpu-baseline]
 
 A step is one full forward (block summaries, mixing, output) over one batch
@@ -154,6 +154,11 @@ def phase_bytes(w: wl.Workload, info, variant: int):
         mixed_w = U * M * (R * 2 + (R if mala else 2 * d) * 2)
         mixed_r = U * M * (d * d * 2 * (2 if mala else 1) + 2 * d * 2 * 2)
         mc = 4 * M * M
+    if variant == mb.VARIANT_FUSED:
+        # prep: Mc in, its copies out; the fused kernel: Q, K, V in and O out
+        # (the stack and mixed rings stay in L2)
+        mcq = M * ((M * info.summary_splits + 7) // 8 * 8) * 2
+        return {"summary": mc + 3 * mcq, "mix": 0, "output": 4 * io}
     return {"summary": 2 * io + stack, "mix": stack + mixed_w + mc, "output": io + mixed_r + io}
 
 
@@ -178,7 +183,9 @@ def traffic_table():
 
 
 KERNEL_HEADERS = ["token_level_head_phi_gb300/csrc/tc_common.cuh", "token_level_head_phi_gb300/csrc/common.cuh",
-                  "token_level_head_phi_gb300/csrc/plan.h", "token_level_head_phi_gb300/csrc/tc_host.h"]
+                  "token_level_head_phi_gb300/csrc/plan.h", "token_level_head_phi_gb300/csrc/tc_host.h",
+                  "token_level_head_phi_gb300/csrc/tc_summary.cuh", "token_level_head_phi_gb300/csrc/tc_mix.cuh",
+                  "token_level_head_phi_gb300/csrc/tc_output.cuh"]
 
 
 def source_hash(relpath: str) -> str:
@@ -197,6 +204,8 @@ PHASE_KERNEL = {  # variant -> phase -> (kernel name in ncu, source file)
     2: {"summary": ("tc_summary_kernel", "token_level_head_phi_gb300/csrc/tc_summary.cu"),
         "mix": ("tc_mix_kernel", "token_level_head_phi_gb300/csrc/tc_mix.cu"),
         "output": ("tc_output_kernel", "token_level_head_phi_gb300/csrc/tc_output.cu")},
+    3: {"summary": ("tc_prep_kernel", "token_level_head_phi_gb300/csrc/tc_mix.cu"),
+        "output": ("tc_fused_kernel", "token_level_head_phi_gb300/csrc/tc_fused.cu")},
 }
 
 
@@ -317,7 +326,7 @@ def run_mine(args, w: wl.Workload, world: int, rank: int, local: int, dist):
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": w.dtype, "data": "synthetic (seeded normals, locality-biased Mc; no dataset, no weights)",
         "config": dict(wl.describe(w), variant=mb.mhla_plan(p).variant,
-                       variant_name={1: "simt", 2: "multipass"}.get(info.variant, str(info.variant)),
+                       variant_name={1: "simt", 2: "multipass", 3: "fused"}.get(info.variant, str(info.variant)),
                        l2="no flush: inputs exceed L2" if flush is None else "L2 flushed (256 MB write) between steps, outside per-step events",
                        parallelism=f"replicas{world}" if world > 1 else "single GPU"),
         "roofline": {"bound": "hbm", "kernel": kname, "phase": dom, "achieved": achieved, "peak": hbm, "unit": "GB/s",
@@ -441,7 +450,7 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=wl.BENCH_WORKLOAD, choices=sorted(wl.WORKLOADS))
-    ap.add_argument("--variant", default="auto", choices=["auto", "simt", "multipass"])
+    ap.add_argument("--variant", default="auto", choices=["auto", "simt", "multipass", "fused"])
     ap.add_argument("--impl", default="mine", choices=["mine", "reference"])
     ap.add_argument("--all-workloads", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -470,7 +479,8 @@ def main():
     if args.all_workloads:
         extra = {}
         for name in sorted(wl.WORKLOADS):
-            if name == w.name or wl.WORKLOADS[name].head_dim != 64 and args.variant == "multipass":
+            ww = wl.WORKLOADS[name]
+            if name == w.name or (ww.head_dim != 64 or ww.dtype != "bf16") and args.variant in ("multipass", "fused"):
                 continue
             sub = argparse.Namespace(**vars(args))
             sub.steps = max(10, min(args.steps, 50))

@@ -86,11 +86,20 @@ typedef enum mhla_norm { MHLA_NORM_DIVISIVE = 0, MHLA_NORM_MALA = 1, MHLA_NORM_N
  *            that still leaves the fp16 range (a single token with
  *            |phi(K)[k] V[c]| >= 65504) is recorded on the device as
  *            MHLA_ERR_OVERFLOW (see mhla_device_status); MALA and SIMT have
- *            no such limit. */
+ *            no such limit.
+ * FUSED:     the MULTIPASS kernels (same arithmetic, same results) as three
+ *            groups of CTAs in one cooperative launch that work through the
+ *            heads concurrently; the stack and the mixed summaries live in
+ *            a ring of a few heads that stays in L2, so less workspace.
+ *            Needs a device with cooperative launch; the split of the SMs
+ *            between the groups follows a work estimate, and the
+ *            environment variable MHLA_FUSED_GROUPS="s,x,o" (CTA counts)
+ *            overrides it for tuning. */
 typedef enum mhla_variant {
   MHLA_VARIANT_AUTO = 0,
   MHLA_VARIANT_SIMT = 1,
-  MHLA_VARIANT_MULTIPASS = 2
+  MHLA_VARIANT_MULTIPASS = 2,
+  MHLA_VARIANT_FUSED = 3
 } mhla_variant;
 
 typedef struct mhla_params {

@@ -177,10 +177,11 @@ def test_auto_picks_tensor_cores_for_bf16_d64(lib):
     assert mb.mhla_plan(p).variant == mb.VARIANT_SIMT
 
 
-def test_multipass_rejects_unsupported(lib):
+@pytest.mark.parametrize("variant", ["multipass", "fused"])
+def test_tensor_core_variants_reject_unsupported(lib, variant):
     info = mb.MhlaPlanInfo()
     for dtype, d in (("f32", 64), ("bf16", 32), ("bf16", 128)):
-        p = mb.make_params(1, 1, d, (1, 8, 8), (1, 4, 4), dtype, variant="multipass")
+        p = mb.make_params(1, 1, d, (1, 8, 8), (1, 4, 4), dtype, variant=variant)
         assert lib.mhla_plan(ctypes.byref(p), ctypes.byref(info)) == mb.MHLA_ERR_UNSUPPORTED
 
 
@@ -189,3 +190,18 @@ def test_multipass_splits_long_blocks(lib):
     info = mb.mhla_plan(_params(w, variant="multipass"))
     assert info.summary_splits > 1
     assert mb.mhla_plan(_params(wl.WORKLOADS["video_16x64x64"], variant="multipass")).summary_splits == 1
+
+
+@pytest.mark.parametrize("name", ["deit_t", "video_16x64x64", "seq_32k", "seq_32k_mala", "seq_32k_m1"])
+def test_fused_plan(lib, name):
+    """The fused launch is the prep kernel plus one cooperative kernel; its
+    ring of intermediates never needs more workspace than the multi-pass
+    buffers, and needs less once the heads outnumber the ring."""
+    w = wl.WORKLOADS[name]
+    fused = mb.mhla_plan(_params(w, variant="fused"))
+    multi = mb.mhla_plan(_params(w, variant="multipass"))
+    assert fused.variant == mb.VARIANT_FUSED and fused.kernels_per_call == 2
+    assert fused.summary_splits == multi.summary_splits
+    assert fused.workspace_bytes <= multi.workspace_bytes + 3 * 4 * w.units + 256
+    if name == "video_16x64x64":
+        assert fused.workspace_bytes < multi.workspace_bytes / 4

@@ -21,7 +21,7 @@ from helpers import TOL, download, parity, run_gpu, upload
 
 pytestmark = pytest.mark.gpu
 
-VARIANTS = ["simt", "multipass"]
+VARIANTS = ["simt", "multipass", "fused"]
 
 FULL = {  # workload -> units the oracle checks (None = all)
     "tiny_f32": None,
@@ -40,7 +40,7 @@ def _tc_supported(dtype, d):
 
 
 def _skip_unsupported(variant, dtype, d):
-    if variant == "multipass" and not _tc_supported(dtype, d):
+    if variant in ("multipass", "fused") and not _tc_supported(dtype, d):
         pytest.skip("tensor-core path covers bf16 with d = 64")
 
 
@@ -110,7 +110,7 @@ def test_mc_with_zero_entries(variant):
 
 @pytest.mark.parametrize("variant", VARIANTS)
 def test_linear_decay_mc_and_identity_map(variant):
-    dtype = "bf16" if variant == "multipass" else "f32"
+    dtype = "f32" if variant == "simt" else "bf16"
     w = wl.random_small(8, (1, 12, 12), (1, 4, 4), 64, 1, 2, dtype, mc="linear_decay")
     vals, dev = wl.all_inputs(w)
     vals = [np.abs(a) + 0.1 for a in vals]  # positive features for phi(x) = x
@@ -188,3 +188,44 @@ def test_phase_events_recorded():
         mb.mhla_set_phase_events(None)
     times = [ev[0].elapsed_time(ev[i]) for i in range(1, mb.NUM_PHASE_EVENTS)]
     assert all(t >= 0 for t in times) and times == sorted(times)
+
+
+def _run_variant(w, tensors, mc, norm, variant):
+    torch = pytest.importorskip("torch")
+    o = run_gpu(w, tensors, mc, norm, variant)
+    return o.view(torch.int16).cpu().numpy()
+
+
+@pytest.mark.parametrize("name", ["deit_t", "image_64x64", "video_16x64x64", "seq_32k", "seq_32k_mala",
+                                  "seq_32k_m1", "seq_32k_m1_mala"])
+def test_fused_bitwise_equals_multipass(name):
+    w = wl.WORKLOADS[name]
+    vals, dev = wl.all_inputs(w)
+    tensors = upload(w, dev)
+    mc = wl.make_mc(w)
+    a = _run_variant(w, tensors, mc, w.norm, "multipass")
+    b = _run_variant(w, tensors, mc, w.norm, "fused")
+    np.testing.assert_array_equal(a, b)
+
+
+# CTA counts of the (summary, mixing, output) groups: one CTA each, lopsided
+# splits either way, and far more streaming than mixing CTAs
+GROUP_SPLITS = ["1,1,1", "7,1,2", "1,9,1", "2,3,40", "60,2,60"]
+
+
+@pytest.mark.parametrize("groups", GROUP_SPLITS)
+@pytest.mark.parametrize("norm", ["divisive", "mala"])
+def test_fused_group_splits(groups, norm, monkeypatch):
+    w = wl.random_small(77, (1, 16, 16), (1, 4, 8), 64, 4, 6, "bf16")
+    vals, dev = wl.all_inputs(w)
+    tensors = upload(w, dev)
+    mc = wl.make_mc(w)
+    ref = _run_variant(w, tensors, mc, norm, "multipass")
+    monkeypatch.setenv("MHLA_FUSED_GROUPS", groups)
+    got = _run_variant(w, tensors, mc, norm, "fused")
+    np.testing.assert_array_equal(ref, got)
+    o = download(run_gpu(w, tensors, mc, norm, "fused")).reshape(w.units, w.n_tokens, w.head_dim)
+    for u in (0, w.units - 1):
+        b, h = divmod(u, w.heads)
+        want = orc.mhla_head64(vals[0][b, h], vals[1][b, h], vals[2][b, h], mc, w.grid, w.block, "elu1", norm)
+        assert orc.relative_max_error(o[u], want) <= TOL["bf16"]

@@ -35,11 +35,12 @@ NORM_NONE = 2
 VARIANT_AUTO = 0
 VARIANT_SIMT = 1
 VARIANT_MULTIPASS = 2
+VARIANT_FUSED = 3
 NUM_PHASE_EVENTS = 4
 
 NORMS = {"divisive": NORM_DIVISIVE, "mala": NORM_MALA, "none": NORM_NONE}
 FEATURE_MAPS = {"elu1": FEATURE_ELU1, "identity": FEATURE_IDENTITY}
-VARIANTS = {"auto": VARIANT_AUTO, "simt": VARIANT_SIMT, "multipass": VARIANT_MULTIPASS}
+VARIANTS = {"auto": VARIANT_AUTO, "simt": VARIANT_SIMT, "multipass": VARIANT_MULTIPASS, "fused": VARIANT_FUSED}
 DTYPES = {"bf16": DTYPE_BF16, "f32": DTYPE_F32}
 
 

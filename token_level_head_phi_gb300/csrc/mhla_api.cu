@@ -31,6 +31,11 @@ unsigned int* g_err_ptr[kMaxDevices] = {};
 
 constexpr size_t kAlign = 256;
 constexpr int kSimtSplitLen = 1024;
+// Fused launch: the stack and mixed-summary rings take at most this many
+// bytes (well inside the 126 MB L2, which also carries the Q/K/V/O streams)
+// and hold at most kFusedMaxRing heads.
+constexpr size_t kFusedRingBytes = 48ull << 20;
+constexpr size_t kFusedMaxRing = 16;
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
@@ -74,7 +79,7 @@ mhla_status make_plan(const mhla_params* prm, Plan* p) {
   if (prm->norm != MHLA_NORM_DIVISIVE && prm->norm != MHLA_NORM_MALA && prm->norm != MHLA_NORM_NONE)
     return MHLA_ERR_INVALID_ARG;
   if (prm->variant != MHLA_VARIANT_AUTO && prm->variant != MHLA_VARIANT_SIMT &&
-      prm->variant != MHLA_VARIANT_MULTIPASS)
+      prm->variant != MHLA_VARIANT_MULTIPASS && prm->variant != MHLA_VARIANT_FUSED)
     return MHLA_ERR_INVALID_ARG;
 
   const int64_t N64 = (int64_t)prm->grid[0] * prm->grid[1] * prm->grid[2];
@@ -107,7 +112,7 @@ mhla_status make_plan(const mhla_params* prm, Plan* p) {
   const bool tc_ok = prm->dtype == MHLA_DTYPE_BF16 && d == kTcHeadDim;
   int variant = prm->variant;
   if (variant == MHLA_VARIANT_AUTO) variant = tc_ok ? MHLA_VARIANT_MULTIPASS : MHLA_VARIANT_SIMT;
-  if (variant == MHLA_VARIANT_MULTIPASS && !tc_ok) return MHLA_ERR_UNSUPPORTED;
+  if ((variant == MHLA_VARIANT_MULTIPASS || variant == MHLA_VARIANT_FUSED) && !tc_ok) return MHLA_ERR_UNSUPPORTED;
   p->variant = variant;
   p->R = d * d + 2 * d;
   p->kernels = 4;
@@ -151,9 +156,20 @@ mhla_status make_plan(const mhla_params* prm, Plan* p) {
     p->off_rowsum = off;
     off = align_up(off + sizeof(float) * (size_t)p->M);
   } else {
-    const size_t rows = (size_t)p->BH * p->M * p->splits;
+    // fused: a ring of heads small enough to stay in L2 (at least two, so
+    // that consecutive heads overlap)
+    const size_t per_head = 2 * (size_t)p->M * p->splits * p->R * (p->norm == MHLA_NORM_MALA ? 2 : 1) +
+                            4 * (size_t)p->M * p->R;
+    p->slots = p->BH;
+    if (variant == MHLA_VARIANT_FUSED) {
+      size_t ring = kFusedRingBytes / per_head;
+      if (ring < 2) ring = 2;
+      if (ring > kFusedMaxRing) ring = kFusedMaxRing;
+      if (ring < (size_t)p->slots) p->slots = (int)ring;
+    }
+    const size_t rows = (size_t)p->slots * p->M * p->splits;
     const size_t stack = 2 * rows * p->R;
-    const size_t mixed = 2 * (size_t)p->BH * p->M * p->R;
+    const size_t mixed = 2 * (size_t)p->slots * p->M * p->R;
     const size_t mcq = 2 * (size_t)p->M * p->Qp;
     p->off_stack = off;
     off = align_up(off + stack);
@@ -176,6 +192,11 @@ mhla_status make_plan(const mhla_params* prm, Plan* p) {
     p->off_blkinfo = off;
     off = align_up(off + 16 * (size_t)p->M);
     p->kernels = 4;
+    if (variant == MHLA_VARIANT_FUSED) {
+      p->off_flow = off;
+      off = align_up(off + 3 * sizeof(unsigned int) * (size_t)p->BH);
+      p->kernels = 2;
+    }
   }
   p->off_aux = off;
   p->ws_total = off;
@@ -201,7 +222,8 @@ mhla_status run_plan(const Plan& plan, const void* q, const void* k, const void*
   mhla_status st = device_error_ptr(&p.err);
   if (st != MHLA_OK) return st;
   int e;
-  if (p.variant == MHLA_VARIANT_MULTIPASS) {
+  if (p.variant == MHLA_VARIANT_MULTIPASS || p.variant == MHLA_VARIANT_FUSED) {
+    const bool fused = p.variant == MHLA_VARIANT_FUSED;
     TcBuffers b;
     b.stack = ws + p.off_stack;
     b.stack_lo = p.norm == MHLA_NORM_MALA ? reinterpret_cast<__nv_bfloat16*>(ws + p.off_stack_lo) : nullptr;
@@ -216,7 +238,17 @@ mhla_status run_plan(const Plan& plan, const void* q, const void* k, const void*
     b.Qp = p.Qp;
     b.f16 = p.f16_mix != 0;
     b.stack_scale = b.f16 ? p.stack_scale : 1.f;
+    b.slots = p.slots;
+    b.flow = fused ? reinterpret_cast<unsigned int*>(ws + p.off_flow) : nullptr;
     record_event(0, s);
+    if (fused) {
+      if ((e = launch_tc_prep(p, mc, b, s)) != 0) return cuda_fail((cudaError_t)e);
+      record_event(1, s);
+      record_event(2, s);
+      if ((e = launch_tc_fused(p, p.chunk, q, k, v, b, out, s)) != 0) return cuda_fail((cudaError_t)e);
+      record_event(3, s);
+      return MHLA_OK;
+    }
     if ((e = launch_tc_prep(p, mc, b, s)) != 0) return cuda_fail((cudaError_t)e);
     if ((e = launch_tc_summary(p, p.chunk, k, v, b, s)) != 0) return cuda_fail((cudaError_t)e);
     record_event(1, s);

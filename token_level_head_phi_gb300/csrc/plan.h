@@ -51,6 +51,8 @@ struct Plan {
   size_t off_stack_lo, off_mixed_lo;
   size_t off_mc_f16, off_mc_scale, off_mc_hi, off_mc_lo, off_blkinfo;
   int Qp;
+  int slots;          // heads the stack and mixed buffers hold (BH, or the fused ring)
+  size_t off_flow;    // fused launch: [3][BH] progress counters
   int f16_mix;        // S part of the mixing in fp16 (DIVISIVE and NONE)
   float stack_scale;  // 2^-ceil(log2(tokens per piece))
   // device error word (code, detail), set by kernels whose bounded waits

@@ -55,6 +55,16 @@ __device__ __forceinline__ void fence_barrier_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 
+__device__ __forceinline__ void mbar_arrive(uint32_t bar);
+
+// One arrival for the whole (converged) warp, after every lane's earlier
+// shared-memory writes and fences: barriers that wait for warps count
+// warps, not threads.
+__device__ __forceinline__ void mbar_arrive_warp(uint32_t bar) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
@@ -117,6 +127,67 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigne
       return false;
     }
   }
+}
+
+// ------------------------------------------------ cross-CTA work flow
+
+// Where a CTA sits in a (possibly fused) launch and how it hands work to
+// other CTAs.  A standalone launch uses cta = blockIdx.x, ncta = gridDim.x,
+// one intermediate slot per head and no counters.  The fused launch gives
+// each CTA group its own range, keeps the intermediates of `ring` heads in
+// reused slots, and orders producer and consumer groups through per-head
+// counters in global memory.
+struct FlowCtl {
+  int cta, ncta;              // index of this CTA in its group, group size
+  int ring;                   // slots of the stack / mixed rings (0: one slot per head)
+  unsigned int* s_done;       // per head: summary units whose stack rows are written
+  unsigned int* x_done;       // per head: mixing epilogue groups whose rows are written
+  unsigned int* o_done;       // per head: output units that have read their S~_i
+  unsigned int need_s, need_x, need_o;
+};
+
+__device__ __forceinline__ int flow_slot(const FlowCtl& f, int u) { return f.ring ? u % f.ring : u; }
+
+// Waits (bounded) until *ctr >= need, then orders the caller's later TMA
+// reads after the writes the counter publishes.
+__device__ __forceinline__ bool flow_wait(const unsigned int* ctr, unsigned int need, unsigned int* err,
+                                          unsigned int where, volatile int* abort_flag) {
+  const unsigned long long t0 = globaltimer();
+  unsigned int ns = 64;
+  for (;;) {
+    unsigned int v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+    if (v >= need) {
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      return true;
+    }
+    if (abort_flag && *abort_flag) return false;
+    if (globaltimer() - t0 > kWaitLimitNs) {
+      report_timeout(err, where);
+      if (abort_flag) *abort_flag = 1;
+      return false;
+    }
+    __nanosleep(ns);
+    if (ns < 2048) ns <<= 1;
+  }
+}
+
+// Publishes the caller's completed TMA stores (waited for with bulk_wait)
+// and counts n more finished pieces of work.
+__device__ __forceinline__ void flow_signal(unsigned int* ctr, unsigned int n) {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  __threadfence();
+  atomicAdd(ctr, n);
+}
+
+// Whether unit w is the last one of its head that this CTA takes (units are
+// numbered head-major, per_head to a head, and a CTA takes every ncta-th).
+// Counters are bumped once per head and CTA, at that unit, and waits are
+// done once per head: a global-memory round trip per unit would throttle
+// the producers.
+__device__ __forceinline__ bool flow_head_ends(const FlowCtl& f, int w, int units, int per_head) {
+  const int wn = w + f.ncta;
+  return wn >= units || wn / per_head != w / per_head;
 }
 
 // Named barrier over `nthreads` threads (a multiple of 32) with id 1..15.

@@ -39,11 +39,14 @@ ChunkShape choose_chunk(const Plan& p);
 // Workspace pointers of the tensor-core path.  Stack rows are block pieces
 // (Q = M * splits per head), each a record of R = d*d + 2d values: S_b
 // (row-major over (k, c)), z_b, v_b.
+// The stack and the mixed summaries hold `slots` heads: every head (slots =
+// BH) for the multi-pass launches, a ring of heads reused in turn for the
+// fused launch.
 struct TcBuffers {
-  void* stack;               // [BH][Q][R]: fp16(x * stack_scale) (DIVISIVE/NONE) or bf16 high part (MALA)
-  __nv_bfloat16* stack_lo;   // [BH][Q][R] low bf16 residual (MALA only, else nullptr)
-  __nv_bfloat16* mixed_hi;   // [BH][M][R] S~_i, z~_i, v~_i high parts
-  __nv_bfloat16* mixed_lo;   // [BH][M][R] low residuals (S~ part for MALA only)
+  void* stack;               // [slots][Q][R]: fp16(x * stack_scale) (DIVISIVE/NONE) or bf16 high part (MALA)
+  __nv_bfloat16* stack_lo;   // [slots][Q][R] low bf16 residual (MALA only, else nullptr)
+  __nv_bfloat16* mixed_hi;   // [slots][M][R] S~_i, z~_i, v~_i high parts
+  __nv_bfloat16* mixed_lo;   // [slots][M][R] low residuals (S~ part for MALA only)
   __half* mc_f16;            // [M][Qp] Mc[i][q / splits] * 2^-e_i in fp16
   float* mc_scale;           // [M] 2^e_i (power of two with max_b |Mc[i][b]| <= 2^e_i)
   __nv_bfloat16* mc_hi;      // [M][Qp] bf16(Mc[i][q / splits])
@@ -53,6 +56,8 @@ struct TcBuffers {
   int Qp;                    // padded row pitch of the Mc copies
   bool f16;                  // fp16 stack and mixing (DIVISIVE and NONE)
   float stack_scale;         // 2^-ceil(log2(tokens per piece))
+  int slots;                 // heads the stack and mixed buffers hold
+  unsigned int* flow;        // fused launch: [3][BH] progress counters, zeroed by the prep kernel
 };
 
 int launch_tc_prep(const Plan& p, const float* mc, const TcBuffers& b, cudaStream_t s);
@@ -61,5 +66,8 @@ int launch_tc_summary(const Plan& p, const ChunkShape& c, const void* k, const v
 int launch_tc_mix(const Plan& p, const TcBuffers& b, cudaStream_t s);
 int launch_tc_output(const Plan& p, const ChunkShape& c, const void* q, const TcBuffers& b, void* out,
                      cudaStream_t s);
+// Summary, mixing and output in one cooperative launch (after launch_tc_prep).
+int launch_tc_fused(const Plan& p, const ChunkShape& c, const void* q, const void* k, const void* v,
+                    const TcBuffers& b, void* out, cudaStream_t s);
 
 }  // namespace mhla

@@ -1,425 +1,25 @@
-// Block summaries on the tensor cores (head dimension 64, bf16 inputs).
-//
-// For every block b of every head ("MHLA: Restoring Expressivity of Linear
-// Attention via Token-Level Multi-Head", overall framework):
-//   S_b = sum_{j in b} phi(K_j) V_j^T,  z_b = sum_{j in b} phi(K_j),
-//   v_b = sum_{j in b} V_j  (the last one feeds the MALA normalisation).
-// All three come out of ONE 128x80 tcgen05 MMA per 16 tokens:
-//   A = [phi(K_b)^T ; 1^T]  (rows 0..63 features of phi(K), rows 64..127 ones)
-//   B = [V_b | 1]           (cols 0..63 features of V, cols 64..79 ones)
-//   D = A B:  D[k][c] = S_b[k][c], D[k][64] = z_b[k], D[64][c] = v_b[c].
-// Both operands are MN-major: the token tile arrives by TMA exactly as it
-// lies in memory ([token][feature], 128-byte rows, 128-byte swizzle) and the
-// ones tiles sit at a fixed shared-memory offset reached through the
-// descriptor's leading-byte offset.  phi = ELU+1 is applied in place to the
-// K tile by the transform warps; padding rows stay zero.  For MALA the low
-// bf16 residual of phi(K) goes through a second MMA (its ones rows add v_b a
-// second time, which the epilogue halves).
-//
-// Persistent, warp-specialised CTA (one per SM, 512 threads):
-//   warp 0       TMA producer (K and V tiles of one token chunk per stage)
-//   warp 1       TMEM allocation + MMA issue (one elected thread)
-//   warps 4-6, 16-17  epilogue: TMEM rows 0..64 -> the record (S_b, z_b,
-//                v_b) as fp16 scaled by 2^-ceil(log2 n) (DIVISIVE/NONE) or as
-//                bf16 high + low parts (MALA) -> swizzled staging tiles ->
-//                TMA stores into the summary stack
-//   warps 8-15   phi(K) transform, two threads per token row
-// Each CTA walks work units (head, block, piece) with a static stride; long
-// blocks are cut into pieces whose partial summaries the mixing step adds.
+// Standalone launch of the block-summary kernel (body in tc_summary.cuh).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <cstring>
 
-#include "common.cuh"
-#include "tc_common.cuh"
-#include "tc_host.h"
+#include "tc_summary.cuh"
 
 namespace mhla {
 namespace {
 
 using namespace tc;
-
-constexpr int kThreads = 640;
-constexpr int kEpiThreads = 160;                        // warps 4, 5, 6, 16, 17
-constexpr int kXfThreads = 256;                         // warps 8..15
-constexpr uint32_t kTile = 128 * 128;                   // 128 rows of 128 bytes
-constexpr uint32_t kStagePart = 8192 + 1024;            // staging: S 8 KB + zv 1 KB
-constexpr uint32_t kStagingBuf = 2 * kStagePart;        // hi and lo
-constexpr uint32_t kTmemCols = 256;                     // two 128-column accumulators
-constexpr int kN = 80;                                  // MMA N: 64 value features + 16 ones
-
-// Shared-memory layout.  kLo adds the low bf16 residual of phi(K) as a third
-// tile per stage (MALA); the stage count shrinks to keep everything resident.
-template <bool kLo>
-struct Layout {
-  static constexpr int kStages = kLo ? 3 : 5;
-  static constexpr int kStagingBufs = kLo ? 2 : 1;
-  static constexpr uint32_t kStageBytes = (kLo ? 3 : 2) * kTile;  // K, V [, K lo]
-  static constexpr uint32_t kOnesA = kStages * kStageBytes;         // ones tile of A (rows 64..127)
-  static constexpr uint32_t kOnesB = kOnesA + kTile;                // ones tile of B (cols 64..79)
-  static constexpr uint32_t kStaging = kOnesB + kTile;              // staging buffers
-  static constexpr uint32_t kBars = kStaging + kStagingBufs * kStagingBuf;
-  static constexpr uint32_t kSmemBytes = kBars + 256 + 1024;        // + barriers + alignment slack
-};
-
-struct SummaryArgs {
-  CUtensorMap tmK, tmV;              // 5D (64, Wg, Hg, T, BH), box (64, cw, ch, ct, 1)
-  CUtensorMap tmS, tmS_lo;           // 2D view (64, BH*Q*66) of the stack, box (64, 64): S_b rows
-  CUtensorMap tmZV, tmZV_lo;         // same view, box (64, 2): the z_b and v_b rows
-  int units, splits, cpp;            // work units, pieces per block, chunks per piece
-  float stack_scale;                 // fp16 stack: values are stored times this power of two
-  ChunkShape c;
-  unsigned int* err;
-};
-
-struct UnitCoord {
-  int u, b, c0, c1;
-};
-
-__device__ __forceinline__ UnitCoord unit_coord(const Plan& p, const SummaryArgs& a, int w) {
-  UnitCoord r;
-  const int per_head = p.M * a.splits;
-  r.u = w / per_head;
-  const int rem = w % per_head;
-  r.b = rem / a.splits;
-  const int s = rem % a.splits;
-  r.c0 = s * a.cpp;
-  r.c1 = min(a.c.per_block, r.c0 + a.cpp);
-  return r;
-}
-
-// Grid origin of chunk `c` of block `b`.
-__device__ __forceinline__ void chunk_origin(const Plan& p, const ChunkShape& ch, int b, int c, int& x0, int& y0,
-                                             int& t0) {
-  const int bx = b % p.Mw;
-  const int by = (b / p.Mw) % p.Mh;
-  const int bz = b / (p.Mw * p.Mh);
-  const int cx = c % ch.ncx;
-  const int cy = (c / ch.ncx) % ch.ncy;
-  const int cz = c / (ch.ncx * ch.ncy);
-  x0 = bx * p.bw + cx * ch.cw;
-  y0 = by * p.bh + cy * ch.ch;
-  t0 = bz * p.bt + cz * ch.ct;
-}
-
-// phi of 8 bf16 (one 16-byte chunk), rounded to bf16; optionally also the
-// low bf16 residual.
-template <bool kLo>
-__device__ __forceinline__ void phi_chunk(uint4& x, uint4& lo, int fmap) {
-  uint32_t* xp = &x.x;
-  uint32_t* lp = &lo.x;
-  if (!kLo && fmap == MHLA_FEATURE_ELU1) {
-#pragma unroll
-    for (int q = 0; q < 4; ++q) xp[q] = phi2_elu1_bf16(xp[q]);
-    return;
-  }
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const float2 f = bf16x2_to_float2(xp[q]);
-    const float a = phi_map(f.x, fmap), b = phi_map(f.y, fmap);
-    xp[q] = pack_bf16x2(a, b);
-    if (kLo) {
-      const float2 g = bf16x2_to_float2(xp[q]);
-      lp[q] = pack_bf16x2(a - g.x, b - g.y);
-    }
-  }
-}
-
-// 8 floats (times scale) -> 8 bf16 (hi) and optionally their low residuals.
-__device__ __forceinline__ void split8(const float* src, uint4& hv, uint4& lv, float scale, bool want_lo) {
-  uint32_t* hp = &hv.x;
-  uint32_t* lp = &lv.x;
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const float x0 = src[2 * q] * scale, x1 = src[2 * q + 1] * scale;
-    hp[q] = pack_bf16x2(x0, x1);
-    if (want_lo) {
-      const float2 g = bf16x2_to_float2(hp[q]);
-      lp[q] = pack_bf16x2(x0 - g.x, x1 - g.y);
-    }
-  }
-}
+using sm::Layout;
+using sm::SummaryArgs;
+using sm::kThreads;
 
 template <bool kLo>
 __global__ void __launch_bounds__(kThreads, 1) tc_summary_kernel(const __grid_constant__ SummaryArgs a, const Plan p) {
-  using L = Layout<kLo>;
-  constexpr int kStages = L::kStages;
-  constexpr uint32_t kStageBytes = L::kStageBytes;
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw = smem_u32(smem_raw);
-  const uint32_t base = (raw + 1023u) & ~1023u;
-  uint8_t* gb = smem_raw + (base - raw);
-  const uint32_t bars = base + L::kBars;
-  auto full = [&](int s) { return bars + 8u * s; };
-  auto kready = [&](int s) { return bars + 8u * (kStages + s); };
-  auto empty = [&](int s) { return bars + 8u * (2 * kStages + s); };
-  auto accfull = [&](int x) { return bars + 8u * (3 * kStages + x); };
-  auto accempty = [&](int x) { return bars + 8u * (3 * kStages + 2 + x); };
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gb + L::kBars + 8 * (3 * kStages + 4));
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(gb + L::kBars + 8 * (3 * kStages + 4) + 8);
-
-  const int warp = threadIdx.x / 32;
-  const int lane = threadIdx.x % 32;
-  const int rows = a.c.rows;
-
-  // Stage tiles start zeroed (padding rows must stay zero); the ones tiles
-  // hold 1.0 in every valid row.
-  for (uint32_t off = threadIdx.x * 16u; off < L::kStaging; off += kThreads * 16u) {
-    uint4 val = make_uint4(0u, 0u, 0u, 0u);
-    if (off >= L::kOnesA && ((off - L::kOnesA) % kTile) / 128u < (uint32_t)rows)
-      val = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
-    *reinterpret_cast<uint4*>(gb + off) = val;
-  }
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(full(s), 1);
-      mbar_init(kready(s), kXfThreads);
-      mbar_init(empty(s), 1);
-    }
-    for (int x = 0; x < 2; ++x) {
-      mbar_init(accfull(x), 1);
-      mbar_init(accempty(x), kEpiThreads);
-    }
-    *abort_flag = 0;
-    fence_barrier_init();
-  }
-  if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&a.tmK);
-    tma_prefetch_desc(&a.tmV);
-  }
-  if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
-    tmem_relinquish();
-  }
-  fence_proxy_async();
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-
-  if (warp == 0) {
-    // ---------------------------------------------------------- producer
-    if (lane == 0) {
-      const uint64_t pol = policy_evict_first();
-      const uint32_t bytes = 2u * (uint32_t)rows * 128u;
-      int stage = 0;
-      uint32_t phase = 0;
-      bool ok = true;
-      for (int w = blockIdx.x; w < a.units && ok; w += gridDim.x) {
-        const UnitCoord uc = unit_coord(p, a, w);
-        for (int c = uc.c0; c < uc.c1; ++c) {
-          if (!(ok = mbar_wait(empty(stage), phase ^ 1u, a.err, 0x101, abort_flag))) break;
-          int x0, y0, t0;
-          chunk_origin(p, a.c, uc.b, c, x0, y0, t0);
-          const uint32_t kt = base + (uint32_t)stage * kStageBytes;
-          mbar_arrive_expect_tx(full(stage), bytes);
-          tma_load_5d(kt, &a.tmK, full(stage), 0, x0, y0, t0, uc.u, pol);
-          tma_load_5d(kt + kTile, &a.tmV, full(stage), 0, x0, y0, t0, uc.u, pol);
-          if (++stage == kStages) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-      }
-    }
-  } else if (warp == 1) {
-    // --------------------------------------------------------------- MMA
-    if (lane == 0) {
-      const uint32_t idesc = idesc_bf16_f32(128, kN, true, true);
-      const int ksteps = a.c.rows_pad / 16;
-      int stage = 0, acc = 0;
-      uint32_t phase = 0, accph = 0;
-      bool ok = true;
-      for (int w = blockIdx.x; w < a.units && ok; w += gridDim.x) {
-        const UnitCoord uc = unit_coord(p, a, w);
-        if (!(ok = mbar_wait(accempty(acc), accph ^ 1u, a.err, 0x102, abort_flag))) break;
-        tc_fence_after();
-        const uint32_t d = tmem + (uint32_t)acc * 128u;
-        for (int c = uc.c0; c < uc.c1; ++c) {
-          if (!(ok = mbar_wait(kready(stage), phase, a.err, 0x103, abort_flag))) break;
-          tc_fence_after();
-          const uint32_t kt = base + (uint32_t)stage * kStageBytes;
-          const uint32_t vt = kt + kTile;
-          const uint32_t lbo_a = base + L::kOnesA - kt;
-          const uint32_t lbo_b = base + L::kOnesB - vt;
-          for (int ks = 0; ks < ksteps; ++ks) {
-            const uint64_t bd = sdesc_sw128(vt + (uint32_t)ks * 2048u, lbo_b, 1024u);
-            umma_bf16(d, sdesc_sw128(kt + (uint32_t)ks * 2048u, lbo_a, 1024u), bd, idesc,
-                      (c > uc.c0 || ks > 0) ? 1u : 0u);
-            if (kLo) {
-              const uint32_t klo = kt + 2 * kTile;
-              umma_bf16(d, sdesc_sw128(klo + (uint32_t)ks * 2048u, base + L::kOnesA - klo, 1024u), bd, idesc, 1u);
-            }
-          }
-          umma_commit(empty(stage));
-          if (++stage == kStages) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-        if (!ok) break;
-        umma_commit(accfull(acc));
-        if (++acc == 2) {
-          acc = 0;
-          accph ^= 1u;
-        }
-      }
-    }
-  } else if (warp >= 8 && warp < 16) {
-    // ------------------------------------------------ phi(K) transform
-    // thread t: row t/2, chunks 4*(t%2) .. +3 at physical positions rotated
-    // by the row so that 8 consecutive threads hit 8 distinct bank groups
-    const int t = threadIdx.x - 256;
-    const int row = t >> 1;
-    const int half = t & 1;
-    int stage = 0;
-    uint32_t phase = 0;
-    bool ok = true;
-    for (int w = blockIdx.x; w < a.units && ok; w += gridDim.x) {
-      const UnitCoord uc = unit_coord(p, a, w);
-      for (int c = uc.c0; c < uc.c1; ++c) {
-        if (!(ok = mbar_wait(full(stage), phase, a.err, 0x104, abort_flag))) break;
-        if (row < rows) {
-          uint8_t* rp = gb + stage * kStageBytes + row * 128;
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint32_t off = ((4 * half + j + row) & 7) << 4;
-            uint4 x = *reinterpret_cast<uint4*>(rp + off);
-            uint4 lo;
-            phi_chunk<kLo>(x, lo, p.fmap);
-            *reinterpret_cast<uint4*>(rp + off) = x;
-            if (kLo) *reinterpret_cast<uint4*>(rp + 2 * kTile + off) = lo;
-          }
-        }
-        fence_proxy_async();
-        mbar_arrive(kready(stage));
-        if (++stage == kStages) {
-          stage = 0;
-          phase ^= 1u;
-        }
-      }
-    }
-  } else if (warp == 4 || warp == 5 || warp == 6 || warp == 16 || warp == 17) {
-    // ------------------------------------------------------------ epilogue
-    // warps 4/16 -> rows 0..31, 5/17 -> rows 32..63 (columns 0..31 / 32..63),
-    // warp 6 -> row 64 (v_b)
-    const int e = warp & 3;                   // TMEM lane quarter
-    const int h = warp >= 16 ? 1 : 0;         // column half of S_b
-    const int et = warp < 16 ? threadIdx.x - 128 : 96 + threadIdx.x - 512;
-    const int r = 32 * e + lane;  // TMEM lane = row of D
-    int acc = 0, it = 0;
-    uint32_t accph = 0;
-    bool ok = true;
-    for (int w = blockIdx.x; w < a.units && ok; w += gridDim.x, ++it) {
-      const UnitCoord uc = unit_coord(p, a, w);
-      ok = mbar_wait(accfull(acc), accph, a.err, 0x105, abort_flag);
-      if (!(ok = named_all(1, kEpiThreads, ok))) break;
-      tc_fence_after();
-      const uint32_t taddr = tmem + (uint32_t)acc * 128u + ((uint32_t)(32 * e) << 16);
-      float s0[32], s1[32], zval = 0.f, znext;
-      tmem_ld32(taddr + 32u * h, s0);
-      if (e == 2) tmem_ld32(taddr + 32u, s1);
-      tmem_ld2(taddr + 64u, zval, znext);
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(accempty(acc));
-      if (++acc == 2) {
-        acc = 0;
-        accph ^= 1u;
-      }
-
-      uint8_t* st_hi = gb + L::kStaging + (it % L::kStagingBufs) * kStagingBuf;
-      uint8_t* st_lo = st_hi + kStagePart;
-      if (et == 0) {
-        // the store that last read this staging buffer has finished reading it
-        if (L::kStagingBufs == 2) bulk_wait_read<1>();
-        else bulk_wait_read<0>();
-      }
-      named_sync(1, kEpiThreads);
-      if (e < 2) {
-        // row r of S_b (columns 32h .. 32h+31) and, for h = 0, z_b[r]
-        float amax = 0.f;
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          const int j = 4 * h + jj;
-          const float* src = &s0[8 * jj];
-          uint4 hv, lv;
-          if (!kLo) {
-            uint32_t* hp = &hv.x;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const float x0 = src[2 * q] * a.stack_scale, x1 = src[2 * q + 1] * a.stack_scale;
-              amax = fmaxf(amax, fmaxf(fabsf(x0), fabsf(x1)));
-              __half2 hh = __floats2half2_rn(x0, x1);
-              hp[q] = *reinterpret_cast<uint32_t*>(&hh);
-            }
-          } else {
-            split8(src, hv, lv, 1.f, true);
-          }
-          const uint32_t off = (uint32_t)r * 128u + ((uint32_t)((j ^ (r & 7)) & 7) << 4);
-          *reinterpret_cast<uint4*>(st_hi + off) = hv;
-          if (kLo) *reinterpret_cast<uint4*>(st_lo + off) = lv;
-        }
-        if (h == 0) {
-          if (!kLo) {
-            const float zs = zval * a.stack_scale;
-            amax = fmaxf(amax, fabsf(zs));
-            *reinterpret_cast<__half*>(st_hi + 8192 + sw128_offset(0, r)) = __float2half_rn(zs);
-          } else {
-            const __nv_bfloat16 zh = __float2bfloat16_rn(zval);
-            *reinterpret_cast<__nv_bfloat16*>(st_hi + 8192 + sw128_offset(0, r)) = zh;
-            *reinterpret_cast<__nv_bfloat16*>(st_lo + 8192 + sw128_offset(0, r)) =
-                __float2bfloat16_rn(zval - __bfloat162float(zh));
-          }
-        }
-        if (!(amax <= 65504.f)) report_error(a.err, MHLA_ERR_OVERFLOW, 0x106);
-      } else if (lane == 0) {
-        // row 64 of D: v_b (every row 64..127 holds the same values; the
-        // low-residual MMA of MALA adds them twice)
-        float amax = 0.f;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float* src = j < 4 ? &s0[8 * j] : &s1[8 * (j - 4)];
-          uint4 hv, lv;
-          if (!kLo) {
-            uint32_t* hp = &hv.x;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const float x0 = src[2 * q] * a.stack_scale, x1 = src[2 * q + 1] * a.stack_scale;
-              amax = fmaxf(amax, fmaxf(fabsf(x0), fabsf(x1)));
-              __half2 hh = __floats2half2_rn(x0, x1);
-              hp[q] = *reinterpret_cast<uint32_t*>(&hh);
-            }
-          } else {
-            split8(src, hv, lv, 0.5f, true);
-          }
-          const uint32_t off = 128u + ((uint32_t)((j ^ 1) & 7) << 4);
-          *reinterpret_cast<uint4*>(st_hi + 8192 + off) = hv;
-          if (kLo) *reinterpret_cast<uint4*>(st_lo + 8192 + off) = lv;
-        }
-        if (!(amax <= 65504.f)) report_error(a.err, MHLA_ERR_OVERFLOW, 0x107);
-      }
-      fence_proxy_async();
-      named_sync(1, kEpiThreads);
-      if (et == 0) {
-        const int srow = (uc.u * p.M + uc.b) * a.splits + (uc.c0 / a.cpp);
-        tma_store_2d(&a.tmS, smem_u32(st_hi), 0, srow * 66);
-        tma_store_2d(&a.tmZV, smem_u32(st_hi + 8192), 0, srow * 66 + 64);
-        if (kLo) {
-          tma_store_2d(&a.tmS_lo, smem_u32(st_lo), 0, srow * 66);
-          tma_store_2d(&a.tmZV_lo, smem_u32(st_lo + 8192), 0, srow * 66 + 64);
-        }
-        bulk_commit();
-      }
-    }
-    if (et == 0) bulk_wait<0>();
-  }
-  __syncwarp();
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+  FlowCtl f = {};
+  f.cta = blockIdx.x;
+  f.ncta = gridDim.x;
+  sm::summary_body<kLo>(a, p, f);
 }
 
 template <bool kLo>
@@ -434,9 +34,9 @@ int launch_variant(const SummaryArgs& a, const Plan& p, cudaStream_t s) {
 
 }  // namespace
 
-int launch_tc_summary(const Plan& p, const ChunkShape& c, const void* k, const void* v, const TcBuffers& b,
-                      cudaStream_t s) {
-  SummaryArgs a;
+int build_summary_args(const Plan& p, const ChunkShape& c, const void* k, const void* v, const TcBuffers& b,
+                       int slots, sm::SummaryArgs* out) {
+  SummaryArgs& a = *out;
   memset(&a, 0, sizeof(a));
   const uint64_t dims5[5] = {64, (uint64_t)p.Wg, (uint64_t)p.Hg, (uint64_t)p.T, (uint64_t)p.BH};
   const uint64_t str5[4] = {128, 128ull * p.Wg, 128ull * p.Wg * p.Hg, 128ull * p.N};
@@ -444,7 +44,8 @@ int launch_tc_summary(const Plan& p, const ChunkShape& c, const void* k, const v
   int e;
   if ((e = encode_tmap_bf16(&a.tmK, k, 5, dims5, str5, box5)) != 0) return e;
   if ((e = encode_tmap_bf16(&a.tmV, v, 5, dims5, str5, box5)) != 0) return e;
-  const uint64_t stack_rows = (uint64_t)p.BH * p.M * p.splits * 66ull;
+  // the stack holds `slots` heads: every head (standalone) or a ring (fused)
+  const uint64_t stack_rows = (uint64_t)slots * p.M * p.splits * 66ull;
   const uint64_t dims2[2] = {64, stack_rows};
   const uint64_t str2[1] = {128};
   const uint32_t boxS[2] = {64, 64};
@@ -461,7 +62,17 @@ int launch_tc_summary(const Plan& p, const ChunkShape& c, const void* k, const v
   a.units = p.BH * p.M * p.splits;
   a.c = c;
   a.err = p.err;
-  return lo ? launch_variant<true>(a, p, s) : launch_variant<false>(a, p, s);
+  return 0;
+}
+
+uint32_t summary_smem_bytes(bool lo) { return lo ? Layout<true>::kSmemBytes : Layout<false>::kSmemBytes; }
+
+int launch_tc_summary(const Plan& p, const ChunkShape& c, const void* k, const void* v, const TcBuffers& b,
+                      cudaStream_t s) {
+  SummaryArgs a;
+  int e = build_summary_args(p, c, k, v, b, b.slots, &a);
+  if (e != 0) return e;
+  return b.stack_lo ? launch_variant<true>(a, p, s) : launch_variant<false>(a, p, s);
 }
 
 }  // namespace mhla
