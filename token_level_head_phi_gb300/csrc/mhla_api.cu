@@ -104,6 +104,8 @@ mhla_status make_plan(const mhla_params* prm, Plan* p) {
   const int64_t M64 = (int64_t)p->Mt * p->Mh * p->Mw;
   if (M64 > 65536) return MHLA_ERR_UNSUPPORTED;
   p->M = (int)M64;
+  p->f_mw = make_fastdiv((uint32_t)p->Mw);
+  p->f_mwh = make_fastdiv((uint32_t)(p->Mw * p->Mh));
   p->nb = p->bt * p->bh * p->bw;
   p->dtype = prm->dtype;
   p->fmap = prm->feature_map;

@@ -11,7 +11,41 @@
 
 #include "mhla.h"
 
+#ifndef __CUDACC__
+#define __host__
+#define __device__
+#endif
+
 namespace mhla {
+
+// Unsigned division by a divisor fixed when the plan is made, by one
+// multiply-high, an add and a shift (T. Granlund, P. Montgomery, "Division
+// by invariant integers using multiplication", PLDI 1994, section 4): for
+// 1 <= d < 2^31, s = ceil(log2 d) and m = floor(2^32 (2^s - d) / d) + 1,
+// n / d = (hi32(m n) + n) >> s for every 32-bit n.  Work-unit and grid
+// indices are split this way once per unit on the device, where an
+// integer division would otherwise cost a few dozen dependent instructions.
+struct FastDiv {
+  uint32_t d, m, s;
+};
+
+inline FastDiv make_fastdiv(uint32_t d) {
+  FastDiv f;
+  f.d = d < 1 ? 1 : d;
+  f.s = 0;
+  while ((1ull << f.s) < f.d) ++f.s;
+  f.m = (uint32_t)((((1ull << f.s) - f.d) << 32) / f.d + 1);
+  return f;
+}
+
+__host__ __device__ inline uint32_t fdiv(uint32_t n, const FastDiv& f) {
+#ifdef __CUDA_ARCH__
+  const uint32_t hi = __umulhi(n, f.m);
+#else
+  const uint32_t hi = (uint32_t)(((uint64_t)n * f.m) >> 32);
+#endif
+  return (uint32_t)(((uint64_t)hi + n) >> f.s);
+}
 
 // Token tile ("chunk") of the tensor-core path: a (ct, ch, cw) sub-box of a
 // block with ct*ch*cw <= 128 rows that tiles the block exactly.
@@ -21,6 +55,7 @@ struct ChunkShape {
   int per_block;      // ncx * ncy * nct
   int rows;           // ct * ch * cw
   int rows_pad;       // rows rounded up to 16 (MMA K granularity)
+  FastDiv f_ncx, f_ncxy;  // divisions by ncx and ncx * ncy
 };
 
 struct Plan {
@@ -55,10 +90,25 @@ struct Plan {
   size_t off_flow;    // fused launch: [3][BH] progress counters
   int f16_mix;        // S part of the mixing in fp16 (DIVISIVE and NONE)
   float stack_scale;  // 2^-ceil(log2(tokens per piece))
+  // divisions by Mw and Mw * Mh (block index -> block grid coordinates)
+  FastDiv f_mw, f_mwh;
   // device error word (code, detail), set by kernels whose bounded waits
   // expire
   unsigned int* err;
 };
+
+// Grid origin (x0, y0, t0) of chunk c of block b: the block's corner plus the
+// chunk's offset inside it (chunks tile the block in raster order).
+__host__ __device__ inline void chunk_origin(const Plan& p, const ChunkShape& ch, uint32_t b, uint32_t c, int& x0,
+                                             int& y0, int& t0) {
+  const uint32_t bq = fdiv(b, p.f_mw), bz = fdiv(b, p.f_mwh);
+  const uint32_t bx = b - bq * (uint32_t)p.Mw, by = bq - bz * (uint32_t)p.Mh;
+  const uint32_t cq = fdiv(c, ch.f_ncx), cz = fdiv(c, ch.f_ncxy);
+  const uint32_t cx = c - cq * (uint32_t)ch.ncx, cy = cq - cz * (uint32_t)ch.ncy;
+  x0 = (int)(bx * p.bw + cx * ch.cw);
+  y0 = (int)(by * p.bh + cy * ch.ch);
+  t0 = (int)(bz * p.bt + cz * ch.ct);
+}
 
 // Global token index (within one head) of local token l of block b.  Local
 // tokens run in raster order over the (bt, bh, bw) box; blocks in raster

@@ -297,6 +297,17 @@ __device__ __forceinline__ void bulk_store(void* gdst, uint32_t src, uint32_t by
                : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared (L2 only), and an arrival on
+// `bar` once this thread's earlier copies have landed (the barrier's
+// expected count is raised by one when the arrival is registered, so it
+// needs no extra count at init).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
 template <int N>

@@ -75,7 +75,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fused_kernel(const __grid_cons
   } else {
     f.cta = cta - a.n_s - a.n_x;
     f.ncta = a.n_o;
-    ot::output_body(a.o, p, f);
+    ot::output_body<kMala>(a.o, p, f);
   }
 }
 
@@ -136,7 +136,7 @@ int launch_variant(FusedArgs& a, const Plan& p, cudaStream_t s) {
   auto kern = tc_fused_kernel<kMala>;
   uint32_t smem = summary_smem_bytes(kMala);
   if (mix_smem_bytes() > smem) smem = mix_smem_bytes();
-  if (output_smem_bytes() > smem) smem = output_smem_bytes();
+  if (output_smem_bytes(kMala) > smem) smem = output_smem_bytes(kMala);
   cudaError_t ce = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (ce != cudaSuccess) return (int)ce;
   int dev = 0, coop = 0, per_sm = 0;

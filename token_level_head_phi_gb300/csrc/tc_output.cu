@@ -11,14 +11,24 @@ namespace {
 
 using namespace tc;
 using ot::OutArgs;
-using ot::kSmemBytes;
 using ot::kThreads;
 
+template <bool kLo>
 __global__ void __launch_bounds__(ot::kThreads, 1) tc_output_kernel(const __grid_constant__ ot::OutArgs a, const Plan p) {
   FlowCtl f = {};
   f.cta = blockIdx.x;
   f.ncta = gridDim.x;
-  ot::output_body(a, p, f);
+  ot::output_body<kLo>(a, p, f);
+}
+
+template <bool kLo>
+int launch_variant(const OutArgs& a, const Plan& p, cudaStream_t s) {
+  const uint32_t smem = output_smem_bytes(kLo);
+  cudaError_t ce = cudaFuncSetAttribute(tc_output_kernel<kLo>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (ce != cudaSuccess) return (int)ce;
+  const int grid = a.units < num_sms() ? a.units : num_sms();
+  tc_output_kernel<kLo><<<grid, kThreads, smem, s>>>(a, p);
+  return (int)cudaGetLastError();
 }
 
 }  // namespace
@@ -38,12 +48,13 @@ int build_output_args(const Plan& p, const ChunkShape& c, const void* q, const T
   const uint32_t box3[3] = {64, 64, 1};
   if ((e = encode_tmap_bf16(&a.tmB_hi, b.mixed_hi, 3, dims3, str3, box3)) != 0) return e;
   if ((e = encode_tmap_bf16(&a.tmB_lo, b.mixed_lo, 3, dims3, str3, box3)) != 0) return e;
-  const uint32_t boxA[3] = {64, 2, 1};
-  if ((e = encode_tmap_plain(&a.tmA_hi, b.mixed_hi, 3, dims3, str3, boxA)) != 0) return e;
-  if ((e = encode_tmap_plain(&a.tmA_lo, b.mixed_lo, 3, dims3, str3, boxA)) != 0) return e;
   a.blkinfo = b.blkinfo;
+  a.mixed_hi = b.mixed_hi;
+  a.mixed_lo = b.mixed_lo;
+  a.R = p.R;
   a.units = p.BH * p.M * c.per_block;
-  a.use_lo = p.norm == MHLA_NORM_MALA;
+  a.f_head = make_fastdiv((uint32_t)(p.M * c.per_block));
+  a.f_nck = make_fastdiv((uint32_t)c.per_block);
   a.c = c;
   a.err = p.err;
   return 0;
@@ -54,11 +65,7 @@ int launch_tc_output(const Plan& p, const ChunkShape& c, const void* q, const Tc
   OutArgs a;
   int e = build_output_args(p, c, q, b, out, b.slots, &a);
   if (e != 0) return e;
-  cudaError_t ce = cudaFuncSetAttribute(tc_output_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-  if (ce != cudaSuccess) return (int)ce;
-  const int grid = a.units < num_sms() ? a.units : num_sms();
-  tc_output_kernel<<<grid, kThreads, kSmemBytes, s>>>(a, p);
-  return (int)cudaGetLastError();
+  return p.norm == MHLA_NORM_MALA ? launch_variant<true>(a, p, s) : launch_variant<false>(a, p, s);
 }
 
 }  // namespace mhla

@@ -3,23 +3,27 @@
 // 2; "Rectifying Magnitude Neglect in Linear Attention", key designs).
 //
 // For a token tile of query block i (up to 128 tokens, gathered by one TMA box
-// from the token grid) one tcgen05 MMA of N = 80 yields numerators and
-// denominators together:
-//     D = phi(Q_tile) [S~_i | z~_i]   (M = 128 tokens, K = 64, N = 64 + 16)
-//     D[t][c] = phi(q_t)^T S~_i[:, c],  s_t = D[t][64] + D[t][65]
-// where the second B atom holds z~_i in two columns (high and low bf16
-// parts) and zeros elsewhere.  The epilogue forms
+// from the token grid) two tcgen05 MMAs per K step yield numerators and
+// denominators side by side in one TMEM accumulator:
+//     D[:, 0:64]  = phi(Q_tile) S~_i     (M = 128 tokens, K = 64, N = 64)
+//     D[:, 64:80] = phi(Q_tile) Z         (N = 16; Z = [z~_i hi, z~_i lo, 0...])
+//     s_t = D[t][64] + D[t][65]
+// The epilogue forms
 //   DIVISIVE o = D / s,  NONE o = D,
 //   MALA     o = (1 + 1/s) D - (s / n~_i) v~_i,   n~_i = n_b sum_b Mc[i, b]
 // writes the bf16 result over the Q tile in shared memory, and one TMA store
 // scatters it back to the grid positions of the tile.
 //   A = phi(Q) tile: K-major (features contiguous), as TMA delivered it
 //   B = S~_i: MN-major ([k][c], c contiguous), loaded by TMA from the mixed
-//       stack (bf16 high part; MALA adds the low residual as a second MMA)
-// Persistent, warp-specialised CTA (640 threads): warp 0 TMA producer,
-// warp 1 TMEM + MMA, warps 4-11 phi(Q) (two threads per token row) and the
-// z~/v~ operands, warps 12-19 epilogue (two warps per TMEM lane quarter,
-// 32 output features each).
+//       stack (bf16 high part; MALA adds the low residual as a third MMA)
+//   Z: K-major, 16 rows of 64 k (2 KB), rows 0 and 1 written per unit
+// Two rings of shared-memory stages: Q tiles (16 KB, streamed from HBM, the
+// deep one: it sets how many bytes are in flight) and the per-block operands
+// S~_i, Z, z~_i / v~_i rows and the output scale (read from L2, a few stages).
+// Persistent, warp-specialised CTA (640 threads): warp 0 Q producer, warp 1
+// TMEM + MMA, warp 2 block-operand producer, warp 3 Z and v~_i, warps 4-11
+// phi(Q) (two threads per token row), warps 12-19 epilogue (two warps per
+// TMEM lane quarter, 32 output features each).
 #pragma once
 
 #include <cuda_bf16.h>
@@ -34,54 +38,90 @@ namespace ot {
 
 using namespace tc;
 
-constexpr int kStages = 5;
 constexpr int kThreads = 640;
 constexpr int kXfThreads = 256;                    // warps 4..11
 constexpr int kEpiThreads = 256;                   // warps 12..19
 constexpr uint32_t kQTile = 128 * 128;             // Q / O tile
 constexpr uint32_t kBTile = 64 * 128;              // 64 k-rows x 64 columns
-constexpr uint32_t kOffBhi = kQTile;               // S~_i high part
-constexpr uint32_t kOffZt = kOffBhi + kBTile;      // z~_i as columns 0 (hi) and 1 (lo)
-constexpr uint32_t kOffBlo = kOffZt + kBTile;      // S~_i low part (MALA)
-constexpr uint32_t kOffV = kOffBlo + kBTile;       // v~_i, 64 floats (MALA)
-constexpr uint32_t kOffAux = kOffV + 256;          // rows z~_i, v~_i of Mixed, bf16 hi (256 B)
-constexpr uint32_t kOffAuxLo = kOffAux + 256;      // same, low residuals
-constexpr uint32_t kOffInfo = kOffAuxLo + 256;     // float4 {output scale, n~_i, 0, 0}
-constexpr uint32_t kStageBytes = kOffV + 1024;
-static_assert(kOffInfo + 16 <= kStageBytes, "stage layout");
-constexpr uint32_t kBars = kStages * kStageBytes;
-constexpr uint32_t kSmemBytes = kBars + 256 + 1024;
+constexpr int kBStages = 4;
+#ifndef OUT_PEND
+#define OUT_PEND 4
+#endif
+constexpr int kPendStores = OUT_PEND;              // O stores in flight per CTA
 constexpr int kAccSlots = 4;                       // TMEM accumulators (128 columns each, 80 used)
 constexpr uint32_t kAccStride = 128;
 constexpr uint32_t kTmemCols = 512;
 
-static_assert(kStageBytes % 1024 == 0, "stage alignment");
+// Shared-memory layout; kLo (MALA) adds the low residual of S~_i.
+template <bool kLo>
+struct Layout {
+  static constexpr int kQStages = kLo ? 9 : 11;
+  // block-operand stage: S~_i hi [, lo] | Z (16 x 128 B) | misc
+  static constexpr uint32_t kOffBlo = kBTile;
+  static constexpr uint32_t kOffZ = kLo ? 2 * kBTile : kBTile;
+  static constexpr uint32_t kOffMisc = kOffZ + 2048;
+  static constexpr uint32_t kOffV = kOffMisc;               // v~_i, 64 floats (MALA)
+  static constexpr uint32_t kOffAux = kOffMisc + 256;       // rows z~_i, v~_i of Mixed, bf16 hi (256 B)
+  static constexpr uint32_t kOffAuxLo = kOffMisc + 512;     // same, low residuals
+  static constexpr uint32_t kOffInfo = kOffMisc + 768;      // float4 {output scale, n~_i, 0, 0}
+  static constexpr uint32_t kBStageBytes = kOffMisc + 1024;
+  static constexpr uint32_t kBBase = kQStages * kQTile;
+  static constexpr uint32_t kBars = kBBase + kBStages * kBStageBytes;
+  static constexpr int kNumBars = 4 * kQStages + 3 * kBStages + kAccSlots;
+  static constexpr uint32_t kSmemBytes = kBars + 8 * kNumBars + 16 + 1024;
+  static_assert(kBStageBytes % 1024 == 0, "stage alignment");
+};
+
+constexpr uint32_t kSmemBytes =
+    Layout<false>::kSmemBytes > Layout<true>::kSmemBytes ? Layout<false>::kSmemBytes : Layout<true>::kSmemBytes;
+static_assert(kSmemBytes <= 232448, "shared memory");
 
 struct OutArgs {
   CUtensorMap tmQ, tmO;        // 5D (64, Wg, Hg, T, BH), box (64, cw, ch, ct, 1)
-  CUtensorMap tmB_hi, tmB_lo;  // 3D (64, R/64, BH*M), box (64, 64, 1)
-  CUtensorMap tmA_hi, tmA_lo;  // same view, box (64, 2, 1), no swizzle: rows z~_i, v~_i
+  const __nv_bfloat16* mixed_hi;  // records of the mixed summaries (rows z~_i, v~_i read by cp.async)
+  const __nv_bfloat16* mixed_lo;
+  int R;                          // record length
+  CUtensorMap tmB_hi, tmB_lo;  // 3D (64, R/64, slots*M), box (64, 64, 1)
   const float4* blkinfo;       // per query block {output scale, n~_i, 0, 0}
   int units;
-  int use_lo;
   ChunkShape c;
+  FastDiv f_head, f_nck;       // divisions by M * nck and by nck (units per head, per block)
   unsigned int* err;
 };
 
+// Head, query block and chunk of work unit w (head-major, then block, then
+// chunk).
+__device__ __forceinline__ void out_unit(const Plan& p, const OutArgs& a, int w, int& u, int& i, int& c) {
+  const uint32_t uu = fdiv((uint32_t)w, a.f_head);
+  const uint32_t rem = (uint32_t)w - uu * (uint32_t)(p.M * a.c.per_block);
+  const uint32_t ii = fdiv(rem, a.f_nck);
+  u = (int)uu;
+  i = (int)ii;
+  c = (int)(rem - ii * (uint32_t)a.c.per_block);
+}
+
 // The kernel body; `a` must live in kernel parameter space.
+template <bool kLo>
 __device__ __forceinline__ void output_body(const OutArgs& a, const Plan& p, const FlowCtl& f) {
+  using L = Layout<kLo>;
+  constexpr int kQStages = L::kQStages;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gb = smem_raw + (base - raw);
-  const uint32_t bars = base + kBars;
-  auto full = [&](int s) { return bars + 8u * s; };
-  auto tready = [&](int s) { return bars + 8u * (kStages + s); };
-  auto mmadone = [&](int s) { return bars + 8u * (2 * kStages + s); };
-  auto empty = [&](int s) { return bars + 8u * (3 * kStages + s); };
-  auto accempty = [&](int x) { return bars + 8u * (4 * kStages + x); };
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gb + kBars + 8 * (4 * kStages + kAccSlots));
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(gb + kBars + 8 * (4 * kStages + kAccSlots) + 8);
+  const uint32_t bars = base + L::kBars;
+  auto qfull = [&](int s) { return bars + 8u * s; };
+  auto qready = [&](int s) { return bars + 8u * (kQStages + s); };
+  auto qmma = [&](int s) { return bars + 8u * (2 * kQStages + s); };
+  auto qempty = [&](int s) { return bars + 8u * (3 * kQStages + s); };
+  auto bfull = [&](int b) { return bars + 8u * (4 * kQStages + b); };
+  auto bready = [&](int b) { return bars + 8u * (4 * kQStages + kBStages + b); };
+  auto bempty = [&](int b) { return bars + 8u * (4 * kQStages + 2 * kBStages + b); };
+  auto accempty = [&](int x) { return bars + 8u * (4 * kQStages + 3 * kBStages + x); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gb + L::kBars + 8 * L::kNumBars);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gb + L::kBars + 8 * L::kNumBars + 8);
+  auto qst = [&](int s) { return base + (uint32_t)s * kQTile; };
+  auto bst = [&](int b) { return base + L::kBBase + (uint32_t)b * L::kBStageBytes; };
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -89,16 +129,21 @@ __device__ __forceinline__ void output_body(const OutArgs& a, const Plan& p, con
   const int nck = a.c.per_block;
   const int per_head = p.M * nck;
 
-  // z~ tiles: every column except 0 and 1 stays zero
-  for (int s = 0; s < kStages; ++s)
-    for (uint32_t off = threadIdx.x * 16u; off < kBTile; off += kThreads * 16u)
-      *reinterpret_cast<uint4*>(gb + s * kStageBytes + kOffZt + off) = make_uint4(0u, 0u, 0u, 0u);
+  // Z operands: every row except 0 and 1 stays zero
+  for (int b = 0; b < kBStages; ++b)
+    for (uint32_t off = threadIdx.x * 16u; off < 2048u; off += kThreads * 16u)
+      *reinterpret_cast<uint4*>(gb + L::kBBase + b * L::kBStageBytes + L::kOffZ + off) = make_uint4(0u, 0u, 0u, 0u);
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(full(s), 1);
-      mbar_init(tready(s), kXfThreads / 32);
-      mbar_init(mmadone(s), 1);
-      mbar_init(empty(s), 1);
+    for (int s = 0; s < kQStages; ++s) {
+      mbar_init(qfull(s), 1);
+      mbar_init(qready(s), kXfThreads / 32);
+      mbar_init(qmma(s), 1);
+      mbar_init(qempty(s), 1);
+    }
+    for (int b = 0; b < kBStages; ++b) {
+      mbar_init(bfull(b), 1);
+      mbar_init(bready(b), 1);
+      mbar_init(bempty(b), 1);
     }
     for (int x = 0; x < kAccSlots; ++x) mbar_init(accempty(x), 1);
     *abort_flag = 0;
@@ -107,8 +152,8 @@ __device__ __forceinline__ void output_body(const OutArgs& a, const Plan& p, con
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&a.tmQ);
     tma_prefetch_desc(&a.tmO);
-    tma_prefetch_desc(&a.tmB_hi);
   }
+  if (warp == 2 && lane == 0) tma_prefetch_desc(&a.tmB_hi);
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
@@ -121,65 +166,115 @@ __device__ __forceinline__ void output_body(const OutArgs& a, const Plan& p, con
 
   if (warp == 0) {
     if (lane == 0) {
-      // ---------------------------------------------------------- producer
+      // -------------------------------------------------------- Q producer
       const uint64_t pol_q = policy_evict_first();
-      const uint64_t pol_b = policy_evict_last();
-      const uint32_t bytes = (uint32_t)rows * 128u + kBTile * (a.use_lo ? 2u : 1u) + 512u + 16u;
-      int stage = 0, ready_u = -1;
-      uint32_t phase = 0;
+      const uint32_t bytes = (uint32_t)rows * 128u;
+      int s = 0;
+      uint32_t ph = 0;
       for (int w = f.cta; w < a.units; w += f.ncta) {
-        const int u = w / per_head;
-        const int rem = w % per_head;
-        const int i = rem / nck;
-        const int c = rem % nck;
-        // fused flow: the mixed summaries of head u are written
-        if (f.x_done && u != ready_u && !flow_wait(&f.x_done[u], f.need_x, a.err, 0x307, abort_flag)) break;
-        ready_u = u;
-        if (!mbar_wait(empty(stage), phase ^ 1u, a.err, 0x301, abort_flag)) break;
-        const int bx = i % p.Mw, by = (i / p.Mw) % p.Mh, bz = i / (p.Mw * p.Mh);
-        const int x0 = bx * p.bw + (c % a.c.ncx) * a.c.cw;
-        const int y0 = by * p.bh + ((c / a.c.ncx) % a.c.ncy) * a.c.ch;
-        const int t0 = bz * p.bt + (c / (a.c.ncx * a.c.ncy)) * a.c.ct;
-        const uint32_t st = base + (uint32_t)stage * kStageBytes;
-        mbar_arrive_expect_tx(full(stage), bytes);
-        tma_load_5d(st, &a.tmQ, full(stage), 0, x0, y0, t0, u, pol_q);
-        const int rec = flow_slot(f, u) * p.M + i;  // record of S~_i in the mixed summaries
-        tma_load_3d(st + kOffBhi, &a.tmB_hi, full(stage), 0, 0, rec, pol_b);
-        if (a.use_lo) tma_load_3d(st + kOffBlo, &a.tmB_lo, full(stage), 0, 0, rec, pol_b);
-        tma_load_3d(st + kOffAux, &a.tmA_hi, full(stage), 0, p.d, rec, pol_b);
-        tma_load_3d(st + kOffAuxLo, &a.tmA_lo, full(stage), 0, p.d, rec, pol_b);
-        bulk_load(st + kOffInfo, a.blkinfo + i, 16u, full(stage));
-        if (++stage == kStages) {
-          stage = 0;
-          phase ^= 1u;
+        int u, i, c, x0, y0, t0;
+        out_unit(p, a, w, u, i, c);
+        if (!mbar_wait(qempty(s), ph ^ 1u, a.err, 0x301, abort_flag)) break;
+        chunk_origin(p, a.c, (uint32_t)i, (uint32_t)c, x0, y0, t0);
+        mbar_arrive_expect_tx(qfull(s), bytes);
+        tma_load_5d(qst(s), &a.tmQ, qfull(s), 0, x0, y0, t0, u, pol_q);
+        if (++s == kQStages) {
+          s = 0;
+          ph ^= 1u;
         }
+      }
+    }
+  } else if (warp == 2) {
+    // ---------------------------------------------- block-operand producer
+    // lane 0: S~_i (hi [, lo]) by TMA; every lane: one 16-byte piece of the
+    // z~_i / v~_i rows (hi: lanes 0-15, lo: 16-31) and lane 0 the block info,
+    // by cp.async (small copies are cheaper outside the TMA engine)
+    const uint64_t pol_b = policy_evict_last();
+    const uint32_t bytes = kBTile * (kLo ? 2u : 1u);
+    int b = 0, ready_u = -1;
+    uint32_t ph = 0;
+    for (int w = f.cta; w < a.units; w += f.ncta) {
+      int u, i, c;
+      out_unit(p, a, w, u, i, c);
+      bool ok = true;
+      if (lane == 0) {
+        // fused flow: the mixed summaries of head u are written
+        if (f.x_done && u != ready_u) ok = flow_wait(&f.x_done[u], f.need_x, a.err, 0x307, abort_flag);
+        ok = ok && mbar_wait(bempty(b), ph ^ 1u, a.err, 0x308, abort_flag);
+      }
+      if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+      ready_u = u;
+      const uint32_t st = bst(b);
+      const int rec = flow_slot(f, u) * p.M + i;  // record of S~_i in the mixed summaries
+      const __nv_bfloat16* src = (lane < 16 ? a.mixed_hi : a.mixed_lo) + (size_t)rec * a.R + 64 * 64 + (lane & 15) * 8;
+      cp_async16(st + (lane < 16 ? L::kOffAux : L::kOffAuxLo) + (lane & 15) * 16, src);
+      if (lane == 0) cp_async16(st + L::kOffInfo, a.blkinfo + i);
+      cp_async_arrive(bfull(b));
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bfull(b), bytes);
+        tma_load_3d(st, &a.tmB_hi, bfull(b), 0, 0, rec, pol_b);
+        if (kLo) tma_load_3d(st + L::kOffBlo, &a.tmB_lo, bfull(b), 0, 0, rec, pol_b);
+      }
+      if (++b == kBStages) {
+        b = 0;
+        ph ^= 1u;
+      }
+    }
+  } else if (warp == 3) {
+    // ---------------------------- Z (z~_i hi, lo as rows 0, 1) and v~_i
+    int b = 0;
+    uint32_t ph = 0;
+    for (int w = f.cta; w < a.units; w += f.ncta) {
+      const bool ok = mbar_wait(bfull(b), ph, a.err, 0x309, abort_flag);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      uint8_t* st = gb + L::kBBase + b * L::kBStageBytes;
+      const __nv_bfloat16* aux = reinterpret_cast<const __nv_bfloat16*>(st + L::kOffAux);
+      const __nv_bfloat16* auxlo = reinterpret_cast<const __nv_bfloat16*>(st + L::kOffAuxLo);
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int k = lane + 32 * j;
+        *reinterpret_cast<__nv_bfloat16*>(st + L::kOffZ + sw128_offset(0, k)) = aux[k];
+        *reinterpret_cast<__nv_bfloat16*>(st + L::kOffZ + sw128_offset(1, k)) = auxlo[k];
+        reinterpret_cast<float*>(st + L::kOffV)[k] = __bfloat162float(aux[64 + k]) + __bfloat162float(auxlo[64 + k]);
+      }
+      fence_proxy_async();
+      mbar_arrive_warp(bready(b));
+      if (++b == kBStages) {
+        b = 0;
+        ph ^= 1u;
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       // --------------------------------------------------------------- MMA
-      const uint32_t idesc80 = idesc_bf16_f32(128, 80, false, true);
       const uint32_t idesc64 = idesc_bf16_f32(128, 64, false, true);
-      int stage = 0, slot = 0;
-      uint32_t phase = 0, slotph = 0;
+      const uint32_t idesc16 = idesc_bf16_f32(128, 16, false, false);
+      int s = 0, b = 0, slot = 0;
+      uint32_t ph = 0, bph = 0, slotph = 0;
       for (int w = f.cta; w < a.units; w += f.ncta) {
-        if (!mbar_wait(tready(stage), phase, a.err, 0x302, abort_flag)) break;
+        if (!mbar_wait(qready(s), ph, a.err, 0x302, abort_flag)) break;
+        if (!mbar_wait(bready(b), bph, a.err, 0x30a, abort_flag)) break;
         if (!mbar_wait(accempty(slot), slotph ^ 1u, a.err, 0x306, abort_flag)) break;
         tc_fence_after();
-        const uint32_t st = base + (uint32_t)stage * kStageBytes;
+        const uint32_t qs = qst(s), bs = bst(b);
         const uint32_t d = tmem + (uint32_t)slot * kAccStride;
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
-          const uint64_t ad = sdesc_sw128(st + (uint32_t)ks * 32u, 0u, 1024u);
-          umma_bf16(d, ad, sdesc_sw128(st + kOffBhi + (uint32_t)ks * 2048u, kOffZt - kOffBhi, 1024u), idesc80,
-                    ks > 0 ? 1u : 0u);
-          if (a.use_lo)
-            umma_bf16(d, ad, sdesc_sw128(st + kOffBlo + (uint32_t)ks * 2048u, kBTile, 1024u), idesc64, 1u);
+          const uint64_t ad = sdesc_sw128(qs + (uint32_t)ks * 32u, 0u, 1024u);
+          const uint32_t acc = ks > 0 ? 1u : 0u;
+          umma_bf16(d, ad, sdesc_sw128(bs + (uint32_t)ks * 2048u, kBTile, 1024u), idesc64, acc);
+          umma_bf16(d + 64u, ad, sdesc_sw128(bs + L::kOffZ + (uint32_t)ks * 32u, 0u, 1024u), idesc16, acc);
+          if (kLo) umma_bf16(d, ad, sdesc_sw128(bs + L::kOffBlo + (uint32_t)ks * 2048u, kBTile, 1024u), idesc64, 1u);
         }
-        umma_commit(mmadone(stage));
-        if (++stage == kStages) {
-          stage = 0;
-          phase ^= 1u;
+        umma_commit(qmma(s));
+        if (++s == kQStages) {
+          s = 0;
+          ph ^= 1u;
+        }
+        if (++b == kBStages) {
+          b = 0;
+          bph ^= 1u;
         }
         if (++slot == kAccSlots) {
           slot = 0;
@@ -188,34 +283,24 @@ __device__ __forceinline__ void output_body(const OutArgs& a, const Plan& p, con
       }
     }
   } else if (warp >= 4 && warp < 12) {
-    // ----------------------------------- phi(Q) and the z~_i / v~_i operands
+    // -------------------------------------------------------------- phi(Q)
     const int t = threadIdx.x - 128;
     const int row = t >> 1;
     const int half = t & 1;
-    int stage = 0;
-    uint32_t phase = 0;
+    int s = 0;
+    uint32_t ph = 0;
     for (int w = f.cta; w < a.units; w += f.ncta) {
-      const bool ok = mbar_wait(full(stage), phase, a.err, 0x303, abort_flag);
+      const bool ok = mbar_wait(qfull(s), ph, a.err, 0x303, abort_flag);
       if (!named_all(2, kXfThreads, ok)) break;
-      uint8_t* st = gb + stage * kStageBytes;
-      // threads 0..63: z~_i[k] (hi, lo) into columns 0, 1 of the z~ operand;
-      // threads 64..127: v~_i[c] = hi + lo as float for the MALA epilogue
-      if (t < 128) {
-        const __nv_bfloat16 zh = reinterpret_cast<const __nv_bfloat16*>(st + kOffAux)[t];
-        const __nv_bfloat16 zl = reinterpret_cast<const __nv_bfloat16*>(st + kOffAuxLo)[t];
-        if (t < 64) {
-          *reinterpret_cast<__nv_bfloat16*>(st + kOffZt + sw128_offset(t, 0)) = zh;
-          *reinterpret_cast<__nv_bfloat16*>(st + kOffZt + sw128_offset(t, 1)) = zl;
-        } else {
-          reinterpret_cast<float*>(st + kOffV)[t - 64] = __bfloat162float(zh) + __bfloat162float(zl);
-        }
-      }
       if (row < rows) {
-        uint8_t* rp = st + row * 128;
+        uint8_t* rp = gb + s * kQTile + row * 128;
+        uint4 xs[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) xs[j] = *reinterpret_cast<const uint4*>(rp + (((4 * half + j + row) & 7) << 4));
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const uint32_t off = ((4 * half + j + row) & 7) << 4;
-          uint4 x = *reinterpret_cast<uint4*>(rp + off);
+          uint4 x = xs[j];
           uint32_t* xp = &x.x;
           if (p.fmap == MHLA_FEATURE_ELU1) {
 #pragma unroll
@@ -223,18 +308,18 @@ __device__ __forceinline__ void output_body(const OutArgs& a, const Plan& p, con
           } else {
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-              const float2 f = bf16x2_to_float2(xp[q]);
-              xp[q] = pack_bf16x2(phi_map(f.x, p.fmap), phi_map(f.y, p.fmap));
+              const float2 fv = bf16x2_to_float2(xp[q]);
+              xp[q] = pack_bf16x2(phi_map(fv.x, p.fmap), phi_map(fv.y, p.fmap));
             }
           }
           *reinterpret_cast<uint4*>(rp + off) = x;
         }
       }
       fence_proxy_async();
-      mbar_arrive_warp(tready(stage));
-      if (++stage == kStages) {
-        stage = 0;
-        phase ^= 1u;
+      mbar_arrive_warp(qready(s));
+      if (++s == kQStages) {
+        s = 0;
+        ph ^= 1u;
       }
     }
   } else if (warp >= 12) {
@@ -243,17 +328,15 @@ __device__ __forceinline__ void output_body(const OutArgs& a, const Plan& p, con
     const int h = (warp - 12) >> 2;     // output features 32h .. 32h+31
     const int t = 32 * q4 + lane;       // token row = TMEM lane
     const int et = threadIdx.x - 384;
-    int stage = 0, prev = -1, slot = 0;
-    uint32_t phase = 0;
+    int s = 0, b = 0, n_out = 0, slot = 0;
+    uint32_t ph = 0, bph = 0;
     unsigned int batch = 0;
     for (int w = f.cta; w < a.units; w += f.ncta) {
-      const int u = w / per_head;
-      const int rem = w % per_head;
-      const int i = rem / nck;
-      const int c = rem % nck;
-      bool ok = mbar_wait(mmadone(stage), phase, a.err, 0x304, abort_flag);
-      // the transform's shared-memory writes (v~)
-      ok = ok && mbar_wait(tready(stage), phase, a.err, 0x305, abort_flag);
+      int u, i, c;
+      out_unit(p, a, w, u, i, c);
+      bool ok = mbar_wait(qmma(s), ph, a.err, 0x304, abort_flag);
+      // the block operands (v~_i floats written by warp 3)
+      ok = ok && mbar_wait(bready(b), bph, a.err, 0x305, abort_flag);
       if (!named_all(3, kEpiThreads, ok)) break;
       tc_fence_after();
       float o[32], s0, s1;
@@ -261,21 +344,21 @@ __device__ __forceinline__ void output_body(const OutArgs& a, const Plan& p, con
       tmem_ld32(taddr + 32u * h, o);
       tmem_ld2(taddr + 64u, s0, s1);
       tmem_wait_ld();
-      uint8_t* st = gb + stage * kStageBytes;
       if (t < rows) {
-        const float s = s0 + s1;
-        const float4 info = *reinterpret_cast<const float4*>(st + kOffInfo);
+        const uint8_t* bp = gb + L::kBBase + b * L::kBStageBytes;
+        const float sden = s0 + s1;
+        const float4 info = *reinterpret_cast<const float4*>(bp + L::kOffInfo);
         // info.x undoes the fp16 mixing's power-of-two scale; under DIVISIVE
         // numerator and denominator carry the same scale, which cancels
         float scale = info.x, gamma = 0.f;
         if (p.norm == MHLA_NORM_DIVISIVE) {
-          scale = __frcp_rn(s);
+          scale = __frcp_rn(sden);
         } else if (p.norm == MHLA_NORM_MALA) {
-          scale = 1.f + __frcp_rn(s);                       // beta
-          gamma = s / info.y;                               // s / n~_i
+          scale = 1.f + __frcp_rn(sden);                    // beta
+          gamma = sden / info.y;                            // s / n~_i
         }
-        const float* vs = reinterpret_cast<const float*>(st + kOffV) + 32 * h;
-        uint8_t* rp = st + t * 128;
+        const float* vs = reinterpret_cast<const float*>(bp + L::kOffV) + 32 * h;
+        uint8_t* rp = gb + s * kQTile + t * 128;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           uint4 x;
@@ -296,14 +379,13 @@ __device__ __forceinline__ void output_body(const OutArgs& a, const Plan& p, con
       fence_proxy_async();
       tc_fence_before();
       named_sync(3, kEpiThreads);
-      if (et == 0) mbar_arrive(accempty(slot));  // every epilogue thread has read the accumulator
-      if (++slot == kAccSlots) slot = 0;
       if (et == 0) {
-        const int bx = i % p.Mw, by = (i / p.Mw) % p.Mh, bz = i / (p.Mw * p.Mh);
-        const int x0 = bx * p.bw + (c % a.c.ncx) * a.c.cw;
-        const int y0 = by * p.bh + ((c / a.c.ncx) % a.c.ncy) * a.c.ch;
-        const int t0 = bz * p.bt + (c / (a.c.ncx * a.c.ncy)) * a.c.ct;
-        tma_store_5d(&a.tmO, base + (uint32_t)stage * kStageBytes, 0, x0, y0, t0, u);
+        // every epilogue thread has read the accumulator and the block operands
+        mbar_arrive(accempty(slot));
+        mbar_arrive(bempty(b));
+        int x0, y0, t0;
+        chunk_origin(p, a.c, (uint32_t)i, (uint32_t)c, x0, y0, t0);
+        tma_store_5d(&a.tmO, qst(s), 0, x0, y0, t0, u);
         bulk_commit();
         // this CTA's units of head u have read their S~_i (the slot may be
         // reused once every unit has)
@@ -311,15 +393,21 @@ __device__ __forceinline__ void output_body(const OutArgs& a, const Plan& p, con
           flow_signal(&f.o_done[u], batch);
           batch = 0;
         }
-        // the previous tile's store has finished reading its stage: release it
-        bulk_wait_read<1>();
-        if (prev >= 0) mbar_arrive(empty(prev));
+        // release the stage of the store kPendStores - 1 units back once it
+        // has been read (later stores may still be queued behind Q loads)
+        bulk_wait_read<kPendStores - 1>();
+        if (n_out >= kPendStores - 1) mbar_arrive(qempty((s + kQStages - (kPendStores - 1)) % kQStages));
       }
-      prev = stage;
-      if (++stage == kStages) {
-        stage = 0;
-        phase ^= 1u;
+      ++n_out;
+      if (++s == kQStages) {
+        s = 0;
+        ph ^= 1u;
       }
+      if (++b == kBStages) {
+        b = 0;
+        bph ^= 1u;
+      }
+      if (++slot == kAccSlots) slot = 0;
     }
     if (et == 0) bulk_wait<0>();
   }
@@ -336,6 +424,6 @@ __device__ __forceinline__ void output_body(const OutArgs& a, const Plan& p, con
 // summaries hold `slots` heads.
 int build_output_args(const Plan& p, const ChunkShape& c, const void* q, const TcBuffers& b, void* out, int slots,
                       ot::OutArgs* args);
-constexpr uint32_t output_smem_bytes() { return ot::kSmemBytes; }
+constexpr uint32_t output_smem_bytes(bool lo) { return lo ? ot::Layout<true>::kSmemBytes : ot::Layout<false>::kSmemBytes; }
 
 }  // namespace mhla

@@ -60,6 +60,8 @@ int build_summary_args(const Plan& p, const ChunkShape& c, const void* k, const 
   a.splits = p.splits;
   a.cpp = p.cpp;
   a.units = p.BH * p.M * p.splits;
+  a.f_head = make_fastdiv((uint32_t)(p.M * p.splits));
+  a.f_splits = make_fastdiv((uint32_t)p.splits);
   a.c = c;
   a.err = p.err;
   return 0;

@@ -9,20 +9,22 @@
 //   B = [V_b | 1]           (cols 0..63 features of V, cols 64..79 ones)
 //   D = A B:  D[k][c] = S_b[k][c], D[k][64] = z_b[k], D[64][c] = v_b[c].
 // Both operands are MN-major: the token tile arrives by TMA exactly as it
-// lies in memory ([token][feature], 128-byte rows, 128-byte swizzle) and the
-// ones tiles sit at a fixed shared-memory offset reached through the
-// descriptor's leading-byte offset.  phi = ELU+1 is applied in place to the
+// lies in memory ([token][feature], 128-byte rows, 128-byte swizzle).  The
+// second M atom of A and the second N atom of B (the ones) are reached
+// through the descriptors' leading-byte offset; since one MMA reads only 16
+// token rows of each atom, that offset is set per K step so that both land
+// on the same 16-row (2 KB) tile of ones.  phi = ELU+1 is applied in place to the
 // K tile by the transform warps; padding rows stay zero.  For MALA the low
 // bf16 residual of phi(K) goes through a second MMA (its ones rows add v_b a
 // second time, which the epilogue halves).
 //
-// Persistent, warp-specialised CTA (one per SM, 512 threads):
+// Persistent, warp-specialised CTA (one per SM, 640 threads):
 //   warp 0       TMA producer (K and V tiles of one token chunk per stage)
 //   warp 1       TMEM allocation + MMA issue (one elected thread)
 //   warps 4-6, 16-17  epilogue: TMEM rows 0..64 -> the record (S_b, z_b,
 //                v_b) as fp16 scaled by 2^-ceil(log2 n) (DIVISIVE/NONE) or as
-//                bf16 high + low parts (MALA) -> swizzled staging tiles ->
-//                TMA stores into the summary stack
+//                bf16 high + low parts (MALA) -> swizzled staging tiles
+//                (two, used in turn) -> TMA stores into the summary stack
 //   warps 8-15   phi(K) transform, two threads per token row
 // Each CTA walks work units (head, block, piece) with a static stride; long
 // blocks are cut into pieces whose partial summaries the mixing step adds.
@@ -57,11 +59,12 @@ struct Layout {
   static constexpr int kStages = kLo ? 3 : 5;
   static constexpr int kStagingBufs = kLo ? 2 : 1;
   static constexpr uint32_t kStageBytes = (kLo ? 3 : 2) * kTile;  // K, V [, K lo]
-  static constexpr uint32_t kOnesA = kStages * kStageBytes;         // ones tile of A (rows 64..127)
-  static constexpr uint32_t kOnesB = kOnesA + kTile;                // ones tile of B (cols 64..79)
-  static constexpr uint32_t kStaging = kOnesB + kTile;              // staging buffers
-  static constexpr uint32_t kBars = kStaging + kStagingBufs * kStagingBuf;
+  static constexpr uint32_t kOnes = kStages * kStageBytes;          // 16 token rows of ones (2 KB)
+  static constexpr uint32_t kStaging = kOnes + 2048;                // staging buffers
+  static constexpr uint32_t kStagingStride = kLo ? kStagingBuf : kStagePart;
+  static constexpr uint32_t kBars = kStaging + kStagingBufs * kStagingStride;
   static constexpr uint32_t kSmemBytes = kBars + 256 + 1024;        // + barriers + alignment slack
+  static_assert(kStaging % 1024 == 0 && kStagingStride % 1024 == 0 && kSmemBytes <= 232448, "layout");
 };
 
 struct SummaryArgs {
@@ -71,6 +74,7 @@ struct SummaryArgs {
   int units, splits, cpp;            // work units, pieces per block, chunks per piece
   float stack_scale;                 // fp16 stack: values are stored times this power of two
   ChunkShape c;
+  FastDiv f_head, f_splits;          // divisions by M * splits and by splits
   unsigned int* err;
 };
 
@@ -80,28 +84,14 @@ struct UnitCoord {
 
 __device__ __forceinline__ UnitCoord unit_coord(const Plan& p, const SummaryArgs& a, int w) {
   UnitCoord r;
-  const int per_head = p.M * a.splits;
-  r.u = w / per_head;
-  const int rem = w % per_head;
-  r.b = rem / a.splits;
-  const int s = rem % a.splits;
-  r.c0 = s * a.cpp;
+  const uint32_t u = fdiv((uint32_t)w, a.f_head);
+  const uint32_t rem = (uint32_t)w - u * (uint32_t)(p.M * a.splits);
+  const uint32_t b = fdiv(rem, a.f_splits);
+  r.u = (int)u;
+  r.b = (int)b;
+  r.c0 = (int)(rem - b * (uint32_t)a.splits) * a.cpp;
   r.c1 = min(a.c.per_block, r.c0 + a.cpp);
   return r;
-}
-
-// Grid origin of chunk `c` of block `b`.
-__device__ __forceinline__ void chunk_origin(const Plan& p, const ChunkShape& ch, int b, int c, int& x0, int& y0,
-                                             int& t0) {
-  const int bx = b % p.Mw;
-  const int by = (b / p.Mw) % p.Mh;
-  const int bz = b / (p.Mw * p.Mh);
-  const int cx = c % ch.ncx;
-  const int cy = (c / ch.ncx) % ch.ncy;
-  const int cz = c / (ch.ncx * ch.ncy);
-  x0 = bx * p.bw + cx * ch.cw;
-  y0 = by * p.bh + cy * ch.ch;
-  t0 = bz * p.bt + cz * ch.ct;
 }
 
 // phi of 8 bf16 (one 16-byte chunk), rounded to bf16; optionally also the
@@ -166,12 +156,11 @@ __device__ __forceinline__ void summary_body(const SummaryArgs& a, const Plan& p
   const int lane = threadIdx.x % 32;
   const int rows = a.c.rows;
 
-  // Stage tiles start zeroed (padding rows must stay zero); the ones tiles
-  // hold 1.0 in every valid row.
+  // Stage tiles start zeroed (padding rows must stay zero, so they add
+  // nothing against the ones); the ones tile holds 1.0 everywhere.
   for (uint32_t off = threadIdx.x * 16u; off < L::kStaging; off += kThreads * 16u) {
     uint4 val = make_uint4(0u, 0u, 0u, 0u);
-    if (off >= L::kOnesA && ((off - L::kOnesA) % kTile) / 128u < (uint32_t)rows)
-      val = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+    if (off >= L::kOnes) val = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
     *reinterpret_cast<uint4*>(gb + off) = val;
   }
   if (threadIdx.x == 0) {
@@ -250,15 +239,15 @@ __device__ __forceinline__ void summary_body(const SummaryArgs& a, const Plan& p
           tc_fence_after();
           const uint32_t kt = base + (uint32_t)stage * kStageBytes;
           const uint32_t vt = kt + kTile;
-          const uint32_t lbo_a = base + L::kOnesA - kt;
-          const uint32_t lbo_b = base + L::kOnesB - vt;
+          const uint32_t ones = base + L::kOnes;
           for (int ks = 0; ks < ksteps; ++ks) {
-            const uint64_t bd = sdesc_sw128(vt + (uint32_t)ks * 2048u, lbo_b, 1024u);
-            umma_bf16(d, sdesc_sw128(kt + (uint32_t)ks * 2048u, lbo_a, 1024u), bd, idesc,
-                      (c > uc.c0 || ks > 0) ? 1u : 0u);
+            // the second atoms of A and B: the ones tile, whatever the K step
+            const uint32_t ka = kt + (uint32_t)ks * 2048u, va = vt + (uint32_t)ks * 2048u;
+            const uint64_t bd = sdesc_sw128(va, ones - va, 1024u);
+            umma_bf16(d, sdesc_sw128(ka, ones - ka, 1024u), bd, idesc, (c > uc.c0 || ks > 0) ? 1u : 0u);
             if (kLo) {
-              const uint32_t klo = kt + 2 * kTile;
-              umma_bf16(d, sdesc_sw128(klo + (uint32_t)ks * 2048u, base + L::kOnesA - klo, 1024u), bd, idesc, 1u);
+              const uint32_t klo = ka + 2 * kTile;
+              umma_bf16(d, sdesc_sw128(klo, ones - klo, 1024u), bd, idesc, 1u);
             }
           }
           umma_commit(empty(stage));
@@ -291,13 +280,15 @@ __device__ __forceinline__ void summary_body(const SummaryArgs& a, const Plan& p
         if (!(ok = mbar_wait(full(stage), phase, a.err, 0x104, abort_flag))) break;
         if (row < rows) {
           uint8_t* rp = gb + stage * kStageBytes + row * 128;
+          uint4 x[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) x[j] = *reinterpret_cast<const uint4*>(rp + (((4 * half + j + row) & 7) << 4));
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             const uint32_t off = ((4 * half + j + row) & 7) << 4;
-            uint4 x = *reinterpret_cast<uint4*>(rp + off);
             uint4 lo;
-            phi_chunk<kLo>(x, lo, p.fmap);
-            *reinterpret_cast<uint4*>(rp + off) = x;
+            phi_chunk<kLo>(x[j], lo, p.fmap);
+            *reinterpret_cast<uint4*>(rp + off) = x[j];
             if (kLo) *reinterpret_cast<uint4*>(rp + 2 * kTile + off) = lo;
           }
         }
@@ -339,12 +330,11 @@ __device__ __forceinline__ void summary_body(const SummaryArgs& a, const Plan& p
         accph ^= 1u;
       }
 
-      uint8_t* st_hi = gb + L::kStaging + (it % L::kStagingBufs) * kStagingBuf;
+      uint8_t* st_hi = gb + L::kStaging + (it % L::kStagingBufs) * L::kStagingStride;
       uint8_t* st_lo = st_hi + kStagePart;
       if (et == 0) {
         // the store that last read this staging buffer has finished reading it
-        if (L::kStagingBufs == 2) bulk_wait_read<1>();
-        else bulk_wait_read<0>();
+        bulk_wait_read<L::kStagingBufs - 1>();
       }
       named_sync(1, kEpiThreads);
       if (e < 2) {

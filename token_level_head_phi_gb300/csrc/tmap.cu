@@ -80,6 +80,8 @@ ChunkShape choose_chunk(const Plan& p) {
   c.ncy = p.bh / c.ch;
   c.nct = p.bt / c.ct;
   c.per_block = c.ncx * c.ncy * c.nct;
+  c.f_ncx = make_fastdiv((uint32_t)c.ncx);
+  c.f_ncxy = make_fastdiv((uint32_t)(c.ncx * c.ncy));
   c.rows = c.ct * c.ch * c.cw;
   c.rows_pad = (c.rows + 15) / 16 * 16;
   return c;
