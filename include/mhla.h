@@ -199,6 +199,21 @@ mhla_status mhla_device_status(int* code, int* detail);
 #define MHLA_NUM_PHASE_EVENTS 4
 mhla_status mhla_set_phase_events(void* const* events, int n);
 
+/* Testing hooks for the FUSED variant's waits on other CTA groups (the pages
+ * have no counterpart; a wait that cannot end must be testable without
+ * hanging the GPU).
+ *   MHLA_DEBUG_FLOW_WAIT_NS  limit of each such wait, in nanoseconds
+ *                            (value <= 0 restores the default, one second).
+ *   MHLA_DEBUG_FLOW_STALL    value != 0: the output group waits for one more
+ *                            mixing signal per head than will ever arrive, so
+ *                            its wait expires; every CTA then stops early and
+ *                            mhla_device_status reports MHLA_ERR_DEVICE_TIMEOUT
+ *                            (the output is not written).  0 turns it off.
+ * Returns MHLA_ERR_INVALID_ARG for an unknown option.  Process-wide, read at
+ * each launch; not for production use. */
+typedef enum mhla_debug_option { MHLA_DEBUG_FLOW_WAIT_NS = 1, MHLA_DEBUG_FLOW_STALL = 2 } mhla_debug_option;
+mhla_status mhla_set_debug(int option, long long value);
+
 /* Static description of a status code; never NULL. */
 const char* mhla_status_string(mhla_status s);
 

@@ -205,3 +205,11 @@ def test_fused_plan(lib, name):
     assert fused.workspace_bytes <= multi.workspace_bytes + 3 * 4 * w.units + 256
     if name == "video_16x64x64":
         assert fused.workspace_bytes < multi.workspace_bytes / 4
+
+
+def test_debug_options(lib):
+    assert lib.mhla_set_debug(0, 0) == mb.MHLA_ERR_INVALID_ARG
+    assert lib.mhla_set_debug(99, 1) == mb.MHLA_ERR_INVALID_ARG
+    for opt in (mb.DEBUG_FLOW_WAIT_NS, mb.DEBUG_FLOW_STALL):
+        assert lib.mhla_set_debug(opt, 5) == mb.MHLA_OK
+        assert lib.mhla_set_debug(opt, 0) == mb.MHLA_OK

@@ -229,3 +229,34 @@ def test_fused_group_splits(groups, norm, monkeypatch):
         b, h = divmod(u, w.heads)
         want = orc.mhla_head64(vals[0][b, h], vals[1][b, h], vals[2][b, h], mc, w.grid, w.block, "elu1", norm)
         assert orc.relative_max_error(o[u], want) <= TOL["bf16"]
+
+
+def test_fused_wait_expires_and_reports():
+    """A wait on another CTA group that can never end (the output group asks
+    for one mixing signal too many) expires after a short limit, every CTA
+    stops, the device status reads MHLA_ERR_DEVICE_TIMEOUT, and the next call
+    runs normally."""
+    torch = pytest.importorskip("torch")
+    w = wl.random_small(31, (1, 16, 16), (1, 4, 8), 64, 2, 3, "bf16")
+    vals, dev = wl.all_inputs(w)
+    q, k, v = upload(w, dev)
+    mc = wl.make_mc(w)
+    mct = torch.from_numpy(mc).cuda()
+    out = torch.zeros_like(q)
+    mb.mhla_set_debug(mb.DEBUG_FLOW_WAIT_NS, 20_000_000)
+    mb.mhla_set_debug(mb.DEBUG_FLOW_STALL, 1)
+    try:
+        mb.mhla_forward(q, k, v, mct, w.grid, w.block, variant="fused", out=out)
+        code, detail = mb.mhla_device_status()
+    finally:
+        mb.mhla_set_debug(mb.DEBUG_FLOW_STALL, 0)
+        mb.mhla_set_debug(mb.DEBUG_FLOW_WAIT_NS, 0)
+    assert code == mb.MHLA_ERR_DEVICE_TIMEOUT, (code, detail)
+    o = download(run_gpu(w, (q, k, v), mc, "divisive", "fused")).reshape(w.units, w.n_tokens, w.head_dim)
+    for u in (0, w.units - 1):
+        assert orc.relative_max_error(o[u], oracle_unit_divisive(w, vals, u, mc)) <= TOL["bf16"]
+
+
+def oracle_unit_divisive(w, vals, unit, mc):
+    b, h = divmod(unit, w.heads)
+    return orc.mhla_head64(vals[0][b, h], vals[1][b, h], vals[2][b, h], mc, w.grid, w.block)

@@ -90,6 +90,7 @@ SIGNATURES = [
     ("mhla_status_string", ctypes.c_char_p, [ctypes.c_int]),
     ("mhla_last_error_string", ctypes.c_char_p, []),
     ("mhla_abi_version", ctypes.c_int, []),
+    ("mhla_set_debug", ctypes.c_int, [ctypes.c_int, ctypes.c_longlong]),
 ]
 
 
@@ -277,6 +278,15 @@ def mhla_set_phase_events(events) -> None:
 
 def mhla_status_string(status: int) -> str:
     return load().mhla_status_string(status).decode()
+
+
+DEBUG_FLOW_WAIT_NS = 1
+DEBUG_FLOW_STALL = 2
+
+
+def mhla_set_debug(option: int, value: int) -> None:
+    """Testing hooks of the fused launch's waits (see mhla.h)."""
+    _check(load().mhla_set_debug(int(option), int(value)), "mhla_set_debug")
 
 
 def mhla_abi_version() -> int:

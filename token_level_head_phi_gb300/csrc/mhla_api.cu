@@ -5,6 +5,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 #include <string>
 
@@ -13,6 +14,13 @@
 #include "tc_host.h"
 
 namespace mhla {
+
+// Testing hooks of the fused launch (mhla_set_debug).
+std::atomic<unsigned long long> g_debug_flow_wait_ns{0};
+std::atomic<unsigned int> g_debug_flow_stall{0};
+unsigned long long debug_flow_wait_ns() { return g_debug_flow_wait_ns.load(); }
+unsigned int debug_flow_stall() { return g_debug_flow_stall.load(); }
+
 namespace {
 
 thread_local std::string g_last_error;
@@ -401,6 +409,19 @@ mhla_status mhla_device_status(int* code, int* detail) {
   if (code) *code = (int)h[0];
   if (detail) *detail = (int)h[1];
   return MHLA_OK;
+}
+
+mhla_status mhla_set_debug(int option, long long value) {
+  switch (option) {
+    case MHLA_DEBUG_FLOW_WAIT_NS:
+      mhla::g_debug_flow_wait_ns.store(value > 0 ? (unsigned long long)value : 0ull);
+      return MHLA_OK;
+    case MHLA_DEBUG_FLOW_STALL:
+      mhla::g_debug_flow_stall.store(value != 0 ? 1u : 0u);
+      return MHLA_OK;
+    default:
+      return MHLA_ERR_INVALID_ARG;
+  }
 }
 
 mhla_status mhla_set_phase_events(void* const* events, int n) {

@@ -129,6 +129,28 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigne
   }
 }
 
+// Before a producer's CTA exits (normally or after an abort): waits, bounded
+// and regardless of the abort flag, for the last loads it issued (the i-th
+// load went to stage i % stages with parity (i / stages) & 1; the stage's
+// full barrier sits at full0 + 8 * stage), so that no copy into shared
+// memory is still in flight when the CTA's memory is released.
+__device__ __forceinline__ void drain_loads(uint32_t full0, int stages, long long issued, unsigned int* err,
+                                            unsigned int where) {
+  const long long first = issued > stages ? issued - stages : 0;
+  for (long long i = first; i < issued; ++i) {
+    const uint32_t bar = full0 + 8u * (uint32_t)(i % stages);
+    const uint32_t parity = (uint32_t)((i / stages) & 1);
+    if (mbar_try_wait(bar, parity)) continue;
+    const unsigned long long t0 = globaltimer();
+    while (!mbar_try_wait_sleep(bar, parity, 20000u)) {
+      if (globaltimer() - t0 > kWaitLimitNs) {
+        report_timeout(err, where);
+        return;
+      }
+    }
+  }
+}
+
 // ------------------------------------------------ cross-CTA work flow
 
 // Where a CTA sits in a (possibly fused) launch and how it hands work to
@@ -144,6 +166,8 @@ struct FlowCtl {
   unsigned int* x_done;       // per head: mixing epilogue groups whose rows are written
   unsigned int* o_done;       // per head: output units that have read their S~_i
   unsigned int need_s, need_x, need_o;
+  unsigned long long wait_ns;  // limit of each counter wait (0: kWaitLimitNs)
+  unsigned int stall;          // testing: extra count the output's waits demand (never reached)
 };
 
 __device__ __forceinline__ int flow_slot(const FlowCtl& f, int u) { return f.ring ? u % f.ring : u; }
@@ -151,7 +175,9 @@ __device__ __forceinline__ int flow_slot(const FlowCtl& f, int u) { return f.rin
 // Waits (bounded) until *ctr >= need, then orders the caller's later TMA
 // reads after the writes the counter publishes.
 __device__ __forceinline__ bool flow_wait(const unsigned int* ctr, unsigned int need, unsigned int* err,
-                                          unsigned int where, volatile int* abort_flag) {
+                                          unsigned int where, volatile int* abort_flag,
+                                          unsigned long long limit_ns) {
+  if (limit_ns == 0) limit_ns = kWaitLimitNs;
   const unsigned long long t0 = globaltimer();
   unsigned int ns = 64;
   for (;;) {
@@ -162,7 +188,7 @@ __device__ __forceinline__ bool flow_wait(const unsigned int* ctr, unsigned int 
       return true;
     }
     if (abort_flag && *abort_flag) return false;
-    if (globaltimer() - t0 > kWaitLimitNs) {
+    if (globaltimer() - t0 > limit_ns) {
       report_timeout(err, where);
       if (abort_flag) *abort_flag = 1;
       return false;

@@ -51,6 +51,8 @@ struct FusedArgs {
   int BH;
   unsigned int* flow;  // s_done [BH] | x_done [BH] | o_done [BH]
   unsigned int need_s, need_x, need_o;
+  unsigned long long wait_ns;  // limit of each counter wait (0: default)
+  unsigned int stall;          // testing: the output waits for a signal that never comes
 };
 
 template <bool kMala>
@@ -63,6 +65,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fused_kernel(const __grid_cons
   f.need_s = a.need_s;
   f.need_x = a.need_x;
   f.need_o = a.need_o;
+  f.wait_ns = a.wait_ns;
+  f.stall = a.stall;
   const int cta = blockIdx.x;
   if (cta < a.n_s) {
     f.cta = cta;
@@ -186,6 +190,8 @@ int launch_tc_fused(const Plan& p, const ChunkShape& c, const void* q, const voi
   a.need_s = (unsigned)(p.M * p.splits);
   a.need_x = (unsigned)(mx::kEpiGroups * a.x.rtiles * a.x.itiles);
   a.need_o = (unsigned)(p.M * c.per_block);
+  a.wait_ns = debug_flow_wait_ns();
+  a.stall = debug_flow_stall();
   return p.norm == MHLA_NORM_MALA ? launch_variant<true>(a, p, s) : launch_variant<false>(a, p, s);
 }
 

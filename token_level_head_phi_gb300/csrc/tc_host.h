@@ -66,6 +66,12 @@ int launch_tc_summary(const Plan& p, const ChunkShape& c, const void* k, const v
 int launch_tc_mix(const Plan& p, const TcBuffers& b, cudaStream_t s);
 int launch_tc_output(const Plan& p, const ChunkShape& c, const void* q, const TcBuffers& b, void* out,
                      cudaStream_t s);
+// Testing hooks set by mhla_set_debug: limit of the fused launch's counter
+// waits (0: default) and whether the output group demands one signal more
+// than will come.
+unsigned long long debug_flow_wait_ns();
+unsigned int debug_flow_stall();
+
 // Summary, mixing and output in one cooperative launch (after launch_tc_prep).
 int launch_tc_fused(const Plan& p, const ChunkShape& c, const void* q, const void* k, const void* v,
                     const TcBuffers& b, void* out, cudaStream_t s);

@@ -112,6 +112,7 @@ __device__ __forceinline__ void mix_body(const MixArgs& a, const Plan& p, const 
       const uint32_t bytes = kF16 ? kATile + (uint32_t)a.NT * 128u : 2u * kATile + 2u * (uint32_t)a.NT * 128u;
       int stage = 0, ready_u = -1;
       uint32_t phase = 0;
+      long long issued = 0;
       bool ok = true;
       for (int w = f.cta; w < a.units && ok; w += f.ncta) {
         const int u = w / per_head;
@@ -122,9 +123,9 @@ __device__ __forceinline__ void mix_body(const MixArgs& a, const Plan& p, const 
         // fused flow: every summary of head u is written, and the mixed slot
         // is no longer read by the outputs of the head that last used it
         if (f.s_done && u != ready_u) {
-          if (!(ok = flow_wait(&f.s_done[u], f.need_s, a.err, 0x205, abort_flag))) break;
+          if (!(ok = flow_wait(&f.s_done[u], f.need_s, a.err, 0x205, abort_flag, f.wait_ns))) break;
           if (f.ring && u >= f.ring &&
-              !(ok = flow_wait(&f.o_done[u - f.ring], f.need_o, a.err, 0x206, abort_flag)))
+              !(ok = flow_wait(&f.o_done[u - f.ring], f.need_o, a.err, 0x206, abort_flag, f.wait_ns)))
             break;
           ready_u = u;
         }
@@ -140,12 +141,14 @@ __device__ __forceinline__ void mix_body(const MixArgs& a, const Plan& p, const 
             tma_load_3d(st + a.off_alo + kAtom, &a.tmA_lo, full(stage), r0 + 64, kc * 64, ss, pol_a);
             tma_load_2d(st + a.off_blo, &a.tmB_lo, full(stage), kc * 64, i0, pol_b);
           }
+          ++issued;
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
           }
         }
       }
+      drain_loads(full(0), kStages, issued, a.err, 0x207);
     }
   } else if (warp == 1) {
     if (lane == 0) {

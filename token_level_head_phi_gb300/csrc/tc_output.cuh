@@ -44,10 +44,7 @@ constexpr int kEpiThreads = 256;                   // warps 12..19
 constexpr uint32_t kQTile = 128 * 128;             // Q / O tile
 constexpr uint32_t kBTile = 64 * 128;              // 64 k-rows x 64 columns
 constexpr int kBStages = 4;
-#ifndef OUT_PEND
-#define OUT_PEND 4
-#endif
-constexpr int kPendStores = OUT_PEND;              // O stores in flight per CTA
+constexpr int kPendStores = 4;                     // O stores in flight per CTA
 constexpr int kAccSlots = 4;                       // TMEM accumulators (128 columns each, 80 used)
 constexpr uint32_t kAccStride = 128;
 constexpr uint32_t kTmemCols = 512;
@@ -171,6 +168,7 @@ __device__ __forceinline__ void output_body(const OutArgs& a, const Plan& p, con
       const uint32_t bytes = (uint32_t)rows * 128u;
       int s = 0;
       uint32_t ph = 0;
+      long long issued = 0;
       for (int w = f.cta; w < a.units; w += f.ncta) {
         int u, i, c, x0, y0, t0;
         out_unit(p, a, w, u, i, c);
@@ -178,11 +176,13 @@ __device__ __forceinline__ void output_body(const OutArgs& a, const Plan& p, con
         chunk_origin(p, a.c, (uint32_t)i, (uint32_t)c, x0, y0, t0);
         mbar_arrive_expect_tx(qfull(s), bytes);
         tma_load_5d(qst(s), &a.tmQ, qfull(s), 0, x0, y0, t0, u, pol_q);
+        ++issued;
         if (++s == kQStages) {
           s = 0;
           ph ^= 1u;
         }
       }
+      drain_loads(qfull(0), kQStages, issued, a.err, 0x30b);
     }
   } else if (warp == 2) {
     // ---------------------------------------------- block-operand producer
@@ -193,13 +193,14 @@ __device__ __forceinline__ void output_body(const OutArgs& a, const Plan& p, con
     const uint32_t bytes = kBTile * (kLo ? 2u : 1u);
     int b = 0, ready_u = -1;
     uint32_t ph = 0;
+    long long issued = 0;
     for (int w = f.cta; w < a.units; w += f.ncta) {
       int u, i, c;
       out_unit(p, a, w, u, i, c);
       bool ok = true;
       if (lane == 0) {
         // fused flow: the mixed summaries of head u are written
-        if (f.x_done && u != ready_u) ok = flow_wait(&f.x_done[u], f.need_x, a.err, 0x307, abort_flag);
+        if (f.x_done && u != ready_u) ok = flow_wait(&f.x_done[u], f.need_x + f.stall, a.err, 0x307, abort_flag, f.wait_ns);
         ok = ok && mbar_wait(bempty(b), ph ^ 1u, a.err, 0x308, abort_flag);
       }
       if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
@@ -216,11 +217,15 @@ __device__ __forceinline__ void output_body(const OutArgs& a, const Plan& p, con
         tma_load_3d(st, &a.tmB_hi, bfull(b), 0, 0, rec, pol_b);
         if (kLo) tma_load_3d(st + L::kOffBlo, &a.tmB_lo, bfull(b), 0, 0, rec, pol_b);
       }
+      ++issued;
       if (++b == kBStages) {
         b = 0;
         ph ^= 1u;
       }
     }
+    // the barrier completes only once this lane's cp.async copies and the
+    // TMA bytes have landed
+    if (lane == 0) drain_loads(bfull(0), kBStages, issued, a.err, 0x30c);
   } else if (warp == 3) {
     // ---------------------------- Z (z~_i hi, lo as rows 0, 1) and v~_i
     int b = 0;
@@ -291,7 +296,7 @@ __device__ __forceinline__ void output_body(const OutArgs& a, const Plan& p, con
     uint32_t ph = 0;
     for (int w = f.cta; w < a.units; w += f.ncta) {
       const bool ok = mbar_wait(qfull(s), ph, a.err, 0x303, abort_flag);
-      if (!named_all(2, kXfThreads, ok)) break;
+      if (!__all_sync(0xffffffffu, ok)) break;
       if (row < rows) {
         uint8_t* rp = gb + s * kQTile + row * 128;
         uint4 xs[4];

@@ -197,13 +197,14 @@ __device__ __forceinline__ void summary_body(const SummaryArgs& a, const Plan& p
       const uint32_t bytes = 2u * (uint32_t)rows * 128u;
       int stage = 0, ready_u = -1;
       uint32_t phase = 0;
+      long long issued = 0;
       bool ok = true;
       for (int w = f.cta; w < a.units && ok; w += f.ncta) {
         const UnitCoord uc = unit_coord(p, a, w);
         // fused flow: the stack slot of this head is free once the mixing of
         // the head that last used it has read it
         if (f.x_done && f.ring && uc.u >= f.ring && uc.u != ready_u &&
-            !(ok = flow_wait(&f.x_done[uc.u - f.ring], f.need_x, a.err, 0x108, abort_flag)))
+            !(ok = flow_wait(&f.x_done[uc.u - f.ring], f.need_x, a.err, 0x108, abort_flag, f.wait_ns)))
           break;
         ready_u = uc.u;
         for (int c = uc.c0; c < uc.c1; ++c) {
@@ -214,12 +215,14 @@ __device__ __forceinline__ void summary_body(const SummaryArgs& a, const Plan& p
           mbar_arrive_expect_tx(full(stage), bytes);
           tma_load_5d(kt, &a.tmK, full(stage), 0, x0, y0, t0, uc.u, pol);
           tma_load_5d(kt + kTile, &a.tmV, full(stage), 0, x0, y0, t0, uc.u, pol);
+          ++issued;
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
           }
         }
       }
+      drain_loads(full(0), kStages, issued, a.err, 0x109);
     }
   } else if (warp == 1) {
     // --------------------------------------------------------------- MMA
