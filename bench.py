@@ -260,10 +260,12 @@ def run_mine(args, w: wl.Workload, world: int, rank: int, local: int, dist):
     if code != 0:
         raise RuntimeError(f"device status {code} during warm-up (detail {detail})")
 
-    # timed region: K steps, per-step phase events, no flush when inputs exceed L2
+    # timed region: K steps back to back (the kernels of consecutive launches
+    # may overlap their set-up with the previous kernel's tail), no flush
+    # when inputs exceed L2; with a flush, per-step events bracket each step
     K = args.steps
-    ev_sets = [[torch.cuda.Event(enable_timing=True) for _ in range(mb.NUM_PHASE_EVENTS)] for _ in range(K)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     sampler = ClockSampler(local) if rank == 0 else None
     if dist is not None:
         dist.barrier()
@@ -275,10 +277,11 @@ def run_mine(args, w: wl.Workload, world: int, rank: int, local: int, dist):
     for i in range(K):
         if flush is not None:
             flush.zero_()
-        mb.mhla_set_phase_events(ev_sets[i])
+            step_ev[i][0].record(stream)
         step()
+        if flush is not None:
+            step_ev[i][1].record(stream)
     end.record(stream)
-    mb.mhla_set_phase_events(None)
     torch.cuda.synchronize()
     t1 = time.time()
     if dist is not None:
@@ -287,16 +290,26 @@ def run_mine(args, w: wl.Workload, world: int, rank: int, local: int, dist):
     code, detail = mb.mhla_device_status()
     if code != 0:
         raise RuntimeError(f"device status {code} in timed region (detail {detail})")
+    if flush is None:
+        total_ms = start.elapsed_time(end)
+    else:
+        total_ms = sum(a.elapsed_time(b) for a, b in step_ev)
 
+    # per-phase breakdown (for the dominant kernel's roofline): a separate
+    # run with events between the kernels, which serialise them
+    KP = max(10, min(K, 50))
+    ev_sets = [[torch.cuda.Event(enable_timing=True) for _ in range(mb.NUM_PHASE_EVENTS)] for _ in range(KP)]
+    for i in range(KP):
+        if flush is not None:
+            flush.zero_()
+        mb.mhla_set_phase_events(ev_sets[i])
+        step()
+    mb.mhla_set_phase_events(None)
+    torch.cuda.synchronize()
     phase_ms = {ph: [] for ph in PHASES}
     for evs in ev_sets:
         for j, ph in enumerate(PHASES):
             phase_ms[ph].append(evs[j].elapsed_time(evs[j + 1]))
-    step_ms = [evs[0].elapsed_time(evs[-1]) for evs in ev_sets]
-    if flush is None:
-        total_ms = start.elapsed_time(end)
-    else:
-        total_ms = sum(step_ms)
     local_ms = torch.tensor([total_ms], dtype=torch.float64, device=dev)
     if dist is not None:
         dist.all_reduce(local_ms, op=dist.ReduceOp.MAX)

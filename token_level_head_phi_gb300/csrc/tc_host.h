@@ -60,6 +60,24 @@ struct TcBuffers {
   unsigned int* flow;        // fused launch: [3][BH] progress counters, zeroed by the prep kernel
 };
 
+// Launch with programmatic stream serialization (the kernel's body calls
+// pdl_wait before it reads its predecessor's results).
+template <typename... KArgs, typename... Args>
+int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
+  return e != cudaSuccess ? (int)e : (int)cudaGetLastError();
+}
+
 int launch_tc_prep(const Plan& p, const float* mc, const TcBuffers& b, cudaStream_t s);
 int launch_tc_summary(const Plan& p, const ChunkShape& c, const void* k, const void* v, const TcBuffers& b,
                       cudaStream_t s);

@@ -29,6 +29,9 @@ __global__ void tc_prep_kernel(int M, int splits, int Q, int Qp, const float* __
                                __nv_bfloat16* __restrict__ mc_hi, __nv_bfloat16* __restrict__ mc_lo,
                                float* __restrict__ rowsum, float4* __restrict__ blkinfo, int f16,
                                float inv_stack_scale, float nb, unsigned int* __restrict__ flow, int nflow) {
+  // the previous call's kernels may still read what this one writes
+  pdl_wait();
+  pdl_launch_dependents();
   // the progress counters of a fused launch start at zero
   for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < nflow; t += gridDim.x * blockDim.x) flow[t] = 0u;
   const int i = (blockIdx.x * blockDim.x + threadIdx.x) / 32;
@@ -78,8 +81,7 @@ int launch_variant(const MixArgs& a, const Plan& p, cudaStream_t s) {
   cudaError_t ce = cudaFuncSetAttribute(tc_mix_kernel<kF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (ce != cudaSuccess) return (int)ce;
   const int grid = a.units < num_sms() ? a.units : num_sms();
-  tc_mix_kernel<kF16><<<grid, kThreads, kSmemBytes, s>>>(a, p);
-  return (int)cudaGetLastError();
+  return launch_pdl(tc_mix_kernel<kF16>, dim3(grid), dim3(kThreads), kSmemBytes, s, a, p);
 }
 
 }  // namespace
@@ -87,10 +89,9 @@ int launch_variant(const MixArgs& a, const Plan& p, cudaStream_t s) {
 int launch_tc_prep(const Plan& p, const float* mc, const TcBuffers& b, cudaStream_t s) {
   const int threads = 256;
   const int blocks = (p.M * 32 + threads - 1) / threads;
-  tc_prep_kernel<<<blocks, threads, 0, s>>>(p.M, p.splits, p.M * p.splits, b.Qp, mc, b.mc_f16, b.mc_scale, b.mc_hi,
-                                             b.mc_lo, b.rowsum, b.blkinfo, b.f16 ? 1 : 0, 1.f / b.stack_scale,
-                                             (float)p.nb, b.flow, b.flow ? 3 * p.BH : 0);
-  return (int)cudaGetLastError();
+  return launch_pdl(tc_prep_kernel, dim3(blocks), dim3(threads), 0, s, p.M, p.splits, p.M * p.splits, b.Qp, mc,
+                    b.mc_f16, b.mc_scale, b.mc_hi, b.mc_lo, b.rowsum, b.blkinfo, b.f16 ? 1 : 0, 1.f / b.stack_scale,
+                    (float)p.nb, b.flow, b.flow ? 3 * p.BH : 0);
 }
 
 int build_mix_args(const Plan& p, const TcBuffers& b, int slots, mx::MixArgs* out) {
@@ -101,12 +102,15 @@ int build_mix_args(const Plan& p, const TcBuffers& b, int slots, mx::MixArgs* ou
   const int W = p.R;
   const void* src = b.stack;
   const void* src_lo = b.stack_lo;
-  const uint64_t dimsA[3] = {(uint64_t)W, (uint64_t)Q, (uint64_t)slots};
-  const uint64_t strA[2] = {2ull * W, 2ull * W * Q};
-  const uint32_t boxA[3] = {64, 64, 1};
+  // A tile of the stack: 64 pieces (q) x 128 record entries (r) as two
+  // 64-wide atoms, one box: dimensions (r within atom, q, atom, slot), so
+  // the box lands as [atom][q][64 r]
+  const uint64_t dimsA[4] = {64, (uint64_t)Q, (uint64_t)(W / 64), (uint64_t)slots};
+  const uint64_t strA[3] = {2ull * W, 128, 2ull * W * Q};
+  const uint32_t boxA[4] = {64, 64, 2, 1};
   int e;
-  if ((e = encode_tmap(&a.tmA, src, 3, dimsA, strA, boxA, f16)) != 0) return e;
-  if ((e = encode_tmap_bf16(&a.tmA_lo, src_lo ? src_lo : src, 3, dimsA, strA, boxA)) != 0) return e;
+  if ((e = encode_tmap(&a.tmA, src, 4, dimsA, strA, boxA, f16)) != 0) return e;
+  if ((e = encode_tmap_bf16(&a.tmA_lo, src_lo ? src_lo : src, 4, dimsA, strA, boxA)) != 0) return e;
   // query-block tile: a multiple of 64 so that each epilogue group stores
   // whole 32-row boxes that never reach into the next tile
   const int nt_max = f16 ? 256 : 128;

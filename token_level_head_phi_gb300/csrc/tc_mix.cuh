@@ -48,7 +48,7 @@ constexpr uint32_t kSmemBytes = kBars + 256 + 1024;
 constexpr uint32_t kTmemCols = 512;                 // two accumulators of up to 256 columns
 
 struct MixArgs {
-  CUtensorMap tmA, tmA_lo;     // 3D (W, Q, BH), box (64, 64, 1)
+  CUtensorMap tmA, tmA_lo;     // 4D (64, Q, W / 64, slots), box (64, 64, 2, 1): two r atoms
   CUtensorMap tmB, tmB_lo;     // 2D (Q, M),     box (64, NT)
   CUtensorMap tmO, tmO_lo;     // 3D (R, M, BH) view of Mixed, box (128, 32, 1), no swizzle
   int Q, NT, itiles, rtiles, kchunks, units;
@@ -103,6 +103,7 @@ __device__ __forceinline__ void mix_body(const MixArgs& a, const Plan& p, const 
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int per_head = a.rtiles * a.itiles;
+  pdl_launch_dependents();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -114,6 +115,8 @@ __device__ __forceinline__ void mix_body(const MixArgs& a, const Plan& p, const 
       uint32_t phase = 0;
       long long issued = 0;
       bool ok = true;
+      // the stack and the Mc copies come from the preceding kernels
+      pdl_wait();
       for (int w = f.cta; w < a.units && ok; w += f.ncta) {
         const int u = w / per_head;
         const int rem = w % per_head;
@@ -133,12 +136,10 @@ __device__ __forceinline__ void mix_body(const MixArgs& a, const Plan& p, const 
           if (!(ok = mbar_wait(empty(stage), phase ^ 1u, a.err, 0x201, abort_flag))) break;
           const uint32_t st = base + (uint32_t)stage * a.stage_bytes;
           mbar_arrive_expect_tx(full(stage), bytes);
-          tma_load_3d(st, &a.tmA, full(stage), r0, kc * 64, ss, pol_a);
-          tma_load_3d(st + kAtom, &a.tmA, full(stage), r0 + 64, kc * 64, ss, pol_a);
+          tma_load_4d(st, &a.tmA, full(stage), 0, kc * 64, r0 / 64, ss, pol_a);
           tma_load_2d(st + a.off_b, &a.tmB, full(stage), kc * 64, i0, pol_b);
           if (!kF16) {
-            tma_load_3d(st + a.off_alo, &a.tmA_lo, full(stage), r0, kc * 64, ss, pol_a);
-            tma_load_3d(st + a.off_alo + kAtom, &a.tmA_lo, full(stage), r0 + 64, kc * 64, ss, pol_a);
+            tma_load_4d(st + a.off_alo, &a.tmA_lo, full(stage), 0, kc * 64, r0 / 64, ss, pol_a);
             tma_load_2d(st + a.off_blo, &a.tmB_lo, full(stage), kc * 64, i0, pol_b);
           }
           ++issued;

@@ -27,8 +27,7 @@ int launch_variant(const OutArgs& a, const Plan& p, cudaStream_t s) {
   cudaError_t ce = cudaFuncSetAttribute(tc_output_kernel<kLo>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (ce != cudaSuccess) return (int)ce;
   const int grid = a.units < num_sms() ? a.units : num_sms();
-  tc_output_kernel<kLo><<<grid, kThreads, smem, s>>>(a, p);
-  return (int)cudaGetLastError();
+  return launch_pdl(tc_output_kernel<kLo>, dim3(grid), dim3(kThreads), smem, s, a, p);
 }
 
 }  // namespace

@@ -3,11 +3,12 @@
 // 2; "Rectifying Magnitude Neglect in Linear Attention", key designs).
 //
 // For a token tile of query block i (up to 128 tokens, gathered by one TMA box
-// from the token grid) two tcgen05 MMAs per K step yield numerators and
-// denominators side by side in one TMEM accumulator:
-//     D[:, 0:64]  = phi(Q_tile) S~_i     (M = 128 tokens, K = 64, N = 64)
-//     D[:, 64:80] = phi(Q_tile) Z         (N = 16; Z = [z~_i hi, z~_i lo, 0...])
-//     s_t = D[t][64] + D[t][65]
+// from the token grid) one tcgen05 MMA of N = 80 per K step yields numerators
+// and denominators together:
+//     D = phi(Q_tile) [S~_i | Z]   (M = 128 tokens, K = 64, N = 64 + 16)
+//     D[t][c] = phi(q_t)^T S~_i[:, c],  s_t = D[t][64] + D[t][65]
+// where Z, the second N atom of B, holds z~_i in two columns (high and low
+// bf16 parts) and zeros elsewhere.
 // The epilogue forms
 //   DIVISIVE o = D / s,  NONE o = D,
 //   MALA     o = (1 + 1/s) D - (s / n~_i) v~_i,   n~_i = n_b sum_b Mc[i, b]
@@ -16,7 +17,7 @@
 //   A = phi(Q) tile: K-major (features contiguous), as TMA delivered it
 //   B = S~_i: MN-major ([k][c], c contiguous), loaded by TMA from the mixed
 //       stack (bf16 high part; MALA adds the low residual as a third MMA)
-//   Z: K-major, 16 rows of 64 k (2 KB), rows 0 and 1 written per unit
+//   Z: MN-major like S~_i (8 KB), columns 0 and 1 written per unit
 // Two rings of shared-memory stages: Q tiles (16 KB, streamed from HBM, the
 // deep one: it sets how many bytes are in flight) and the per-block operands
 // S~_i, Z, z~_i / v~_i rows and the output scale (read from L2, a few stages).
@@ -52,11 +53,11 @@ constexpr uint32_t kTmemCols = 512;
 // Shared-memory layout; kLo (MALA) adds the low residual of S~_i.
 template <bool kLo>
 struct Layout {
-  static constexpr int kQStages = kLo ? 9 : 11;
-  // block-operand stage: S~_i hi [, lo] | Z (16 x 128 B) | misc
+  static constexpr int kQStages = kLo ? 7 : 9;
+  // block-operand stage: S~_i hi [, lo] | Z (the second N atom of B) | misc
   static constexpr uint32_t kOffBlo = kBTile;
   static constexpr uint32_t kOffZ = kLo ? 2 * kBTile : kBTile;
-  static constexpr uint32_t kOffMisc = kOffZ + 2048;
+  static constexpr uint32_t kOffMisc = kOffZ + kBTile;
   static constexpr uint32_t kOffV = kOffMisc;               // v~_i, 64 floats (MALA)
   static constexpr uint32_t kOffAux = kOffMisc + 256;       // rows z~_i, v~_i of Mixed, bf16 hi (256 B)
   static constexpr uint32_t kOffAuxLo = kOffMisc + 512;     // same, low residuals
@@ -128,7 +129,7 @@ __device__ __forceinline__ void output_body(const OutArgs& a, const Plan& p, con
 
   // Z operands: every row except 0 and 1 stays zero
   for (int b = 0; b < kBStages; ++b)
-    for (uint32_t off = threadIdx.x * 16u; off < 2048u; off += kThreads * 16u)
+    for (uint32_t off = threadIdx.x * 16u; off < kBTile; off += kThreads * 16u)
       *reinterpret_cast<uint4*>(gb + L::kBBase + b * L::kBStageBytes + L::kOffZ + off) = make_uint4(0u, 0u, 0u, 0u);
   if (threadIdx.x == 0) {
     for (int s = 0; s < kQStages; ++s) {
@@ -160,10 +161,12 @@ __device__ __forceinline__ void output_body(const OutArgs& a, const Plan& p, con
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_launch_dependents();
 
   if (warp == 0) {
     if (lane == 0) {
       // -------------------------------------------------------- Q producer
+      // (Q is an input: its loads need not wait for the mixing kernel)
       const uint64_t pol_q = policy_evict_first();
       const uint32_t bytes = (uint32_t)rows * 128u;
       int s = 0;
@@ -194,6 +197,9 @@ __device__ __forceinline__ void output_body(const OutArgs& a, const Plan& p, con
     int b = 0, ready_u = -1;
     uint32_t ph = 0;
     long long issued = 0;
+    // the mixed summaries and the block info come from the preceding kernels
+    if (lane == 0) pdl_wait();
+    __syncwarp();
     for (int w = f.cta; w < a.units; w += f.ncta) {
       int u, i, c;
       out_unit(p, a, w, u, i, c);
@@ -239,8 +245,8 @@ __device__ __forceinline__ void output_body(const OutArgs& a, const Plan& p, con
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
         const int k = lane + 32 * j;
-        *reinterpret_cast<__nv_bfloat16*>(st + L::kOffZ + sw128_offset(0, k)) = aux[k];
-        *reinterpret_cast<__nv_bfloat16*>(st + L::kOffZ + sw128_offset(1, k)) = auxlo[k];
+        *reinterpret_cast<__nv_bfloat16*>(st + L::kOffZ + sw128_offset(k, 0)) = aux[k];
+        *reinterpret_cast<__nv_bfloat16*>(st + L::kOffZ + sw128_offset(k, 1)) = auxlo[k];
         reinterpret_cast<float*>(st + L::kOffV)[k] = __bfloat162float(aux[64 + k]) + __bfloat162float(auxlo[64 + k]);
       }
       fence_proxy_async();
@@ -253,8 +259,8 @@ __device__ __forceinline__ void output_body(const OutArgs& a, const Plan& p, con
   } else if (warp == 1) {
     if (lane == 0) {
       // --------------------------------------------------------------- MMA
+      const uint32_t idesc80 = idesc_bf16_f32(128, 80, false, true);
       const uint32_t idesc64 = idesc_bf16_f32(128, 64, false, true);
-      const uint32_t idesc16 = idesc_bf16_f32(128, 16, false, false);
       int s = 0, b = 0, slot = 0;
       uint32_t ph = 0, bph = 0, slotph = 0;
       for (int w = f.cta; w < a.units; w += f.ncta) {
@@ -268,8 +274,7 @@ __device__ __forceinline__ void output_body(const OutArgs& a, const Plan& p, con
         for (int ks = 0; ks < 4; ++ks) {
           const uint64_t ad = sdesc_sw128(qs + (uint32_t)ks * 32u, 0u, 1024u);
           const uint32_t acc = ks > 0 ? 1u : 0u;
-          umma_bf16(d, ad, sdesc_sw128(bs + (uint32_t)ks * 2048u, kBTile, 1024u), idesc64, acc);
-          umma_bf16(d + 64u, ad, sdesc_sw128(bs + L::kOffZ + (uint32_t)ks * 32u, 0u, 1024u), idesc16, acc);
+          umma_bf16(d, ad, sdesc_sw128(bs + (uint32_t)ks * 2048u, L::kOffZ, 1024u), idesc80, acc);
           if (kLo) umma_bf16(d, ad, sdesc_sw128(bs + L::kOffBlo + (uint32_t)ks * 2048u, kBTile, 1024u), idesc64, 1u);
         }
         umma_commit(qmma(s));

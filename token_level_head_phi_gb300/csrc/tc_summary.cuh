@@ -189,6 +189,9 @@ __device__ __forceinline__ void summary_body(const SummaryArgs& a, const Plan& p
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // K and V are inputs: nothing to wait for; the next kernel may start its
+  // set-up as SMs free up
+  pdl_launch_dependents();
 
   if (warp == 0) {
     // ---------------------------------------------------------- producer
@@ -430,6 +433,9 @@ __device__ __forceinline__ void summary_body(const SummaryArgs& a, const Plan& p
   tc_fence_before();
   __syncthreads();
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+  // this kernel completes only after its predecessor (the prep kernel, whose
+  // Mc copies the mixing reads) has
+  if (threadIdx.x == 0) pdl_wait();
 }
 
 }  // namespace sm
