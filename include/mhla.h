@@ -173,12 +173,17 @@ mhla_status mhla_forward_noalloc(const void* q, const void* k, const void* v, co
  * workspace, each 256-byte aligned. */
 mhla_status mhla_host_buffer_bytes(const mhla_params* p, size_t* bytes);
 
-/* End-to-end call on HOST arrays: enqueues the host-to-device copies of
- * q, k, v, mc into dev_buffer, the forward pass, and the device-to-host copy
- * of the result into out (all on `stream`), then synchronises `stream` and
- * returns.  Host arrays have the layouts of mhla_forward; page-locked host
- * memory makes the copies asynchronous DMA transfers.  dev_buffer is a
- * device allocation of at least mhla_host_buffer_bytes(p) bytes. */
+/* End-to-end call on HOST arrays: copies q, k, v, mc into dev_buffer, runs
+ * the forward pass and copies the result into out, then synchronises
+ * `stream` and returns.  Large problems are cut into up to 8 groups of
+ * (batch, head) units (at least ~32 MB of each input per group): group g's
+ * inputs are copied in on one library-owned stream while group g-1's kernels
+ * run on `stream` and group g-2's result is copied back on another, ordered
+ * by events; everything starts after the work already queued on `stream`.
+ * Host arrays have the layouts of mhla_forward; page-locked host memory makes
+ * the copies asynchronous DMA transfers.  dev_buffer is a device allocation
+ * of at least mhla_host_buffer_bytes(p) bytes.  Calls on the same device are
+ * serialised (the copy streams are per device). */
 mhla_status mhla_forward_host(const void* q, const void* k, const void* v, const float* mc,
                               const mhla_params* p, void* out, void* dev_buffer,
                               size_t dev_buffer_bytes, void* stream);

@@ -260,3 +260,20 @@ def test_fused_wait_expires_and_reports():
 def oracle_unit_divisive(w, vals, unit, mc):
     b, h = divmod(unit, w.heads)
     return orc.mhla_head64(vals[0][b, h], vals[1][b, h], vals[2][b, h], mc, w.grid, w.block)
+
+
+@pytest.mark.parametrize("name", ["seq_32k", "video_16x64x64"])
+def test_host_entry_pipelined_matches_device_entry(name):
+    """Large problems go through the host entry point in head groups whose
+    copies overlap the kernels; the result is the device entry's, bit for bit."""
+    torch = pytest.importorskip("torch")
+    w = wl.WORKLOADS[name]
+    vals, dev = wl.all_inputs(w)
+    mc = wl.make_mc(w)
+    tensors = upload(w, dev)
+    d_out = run_gpu(w, tensors, mc, w.norm).view(torch.int16).cpu().numpy()
+    del tensors
+    host = [torch.from_numpy(a).view(torch.bfloat16).pin_memory() for a in dev]
+    h_out = torch.empty_like(host[0]).pin_memory()
+    mb.mhla_forward_host(*host, torch.from_numpy(mc), w.grid, w.block, norm=w.norm, out=h_out)
+    np.testing.assert_array_equal(h_out.view(torch.int16).numpy(), d_out)

@@ -71,7 +71,10 @@ mhla_status device_error_ptr(unsigned int** out) {
 }
 
 // Shape and option checks; fills the plan without touching the device.
-mhla_status make_plan(const mhla_params* prm, Plan* p) {
+// split_units: the number of (batch, head) units the split of long blocks is
+// sized for (0: this problem's own); a group of a larger problem passes the
+// whole problem's count so that it sums the same pieces in the same order.
+mhla_status make_plan(const mhla_params* prm, Plan* p, int split_units = 0) {
   if (!prm || !p) return MHLA_ERR_INVALID_ARG;
   std::memset(p, 0, sizeof(*p));
   const int d = prm->head_dim;
@@ -136,7 +139,7 @@ mhla_status make_plan(const mhla_params* prm, Plan* p) {
     // are too few blocks to keep every SM busy for several waves
     p->chunk = choose_chunk(*p);
     const int nck = p->chunk.per_block;
-    const int64_t blocks = (int64_t)p->BH * p->M;
+    const int64_t blocks = (int64_t)(split_units > 0 ? split_units : p->BH) * p->M;
     int splits = 1;
     if (blocks > 0 && blocks < 8LL * kPlanSms)
       splits = (int)((8LL * kPlanSms + blocks - 1) / blocks);
@@ -285,6 +288,61 @@ mhla_status run_plan(const Plan& plan, const void* q, const void* k, const void*
 }  // namespace
 }  // namespace mhla
 
+namespace mhla {
+
+// Head groups of mhla_forward_host: at least ~32 MB of each input tensor per
+// group so the copies stay efficient, at most kMaxHostGroups groups.
+constexpr int kMaxHostGroups = 8;
+struct HostGroups {
+  int n, per;  // groups, units per group (the last group may have fewer)
+};
+
+HostGroups host_groups(const Plan& plan) {
+  const size_t io = (size_t)plan.BH * plan.N * plan.d * elem_bytes(plan.dtype);
+  int n = (int)(io / (32ull << 20));
+  if (n > kMaxHostGroups) n = kMaxHostGroups;
+  if (n > plan.BH) n = plan.BH;
+  if (n < 1) n = 1;
+  HostGroups g;
+  g.per = (plan.BH + n - 1) / n;
+  g.n = (plan.BH + g.per - 1) / g.per;
+  return g;
+}
+
+// The parameters of a group of `units` (batch, head) pairs: one batch of
+// `units` heads (the kernels see only the flattened unit index).
+mhla_params group_params(const mhla_params* p, int units) {
+  mhla_params g = *p;
+  g.batch = 1;
+  g.heads = units;
+  return g;
+}
+
+// Largest workspace any group's plan needs.
+mhla_status host_group_workspace(const mhla_params* p, const Plan& plan, size_t* ws) {
+  const HostGroups hg = host_groups(plan);
+  *ws = 0;
+  const int sizes[2] = {hg.per, plan.BH - (hg.n - 1) * hg.per};
+  for (int i = 0; i < 2; ++i) {
+    Plan gp;
+    mhla_params g = group_params(p, sizes[i]);
+    mhla_status st = make_plan(&g, &gp, plan.BH);
+    if (st != MHLA_OK) return st;
+    if (gp.ws_total > *ws) *ws = gp.ws_total;
+  }
+  return MHLA_OK;
+}
+
+struct HostPipe {
+  bool ready = false;
+  cudaStream_t in = nullptr, out = nullptr;
+  cudaEvent_t ev[3 * kMaxHostGroups + 1] = {};
+};
+HostPipe g_pipe[kMaxDevices];
+std::mutex g_pipe_mu[kMaxDevices];
+
+}  // namespace mhla
+
 using mhla::Plan;
 
 extern "C" {
@@ -355,9 +413,16 @@ mhla_status mhla_host_buffer_bytes(const mhla_params* p, size_t* bytes) {
   Plan plan;
   mhla_status st = mhla::make_plan(p, &plan);
   if (st != MHLA_OK) return st;
+  if (plan.BH == 0) {
+    *bytes = 0;
+    return MHLA_OK;
+  }
+  size_t ws = 0;
+  st = mhla::host_group_workspace(p, plan, &ws);
+  if (st != MHLA_OK) return st;
   const size_t io = mhla::align_up((size_t)plan.BH * plan.N * plan.d * mhla::elem_bytes(plan.dtype));
   const size_t mcb = mhla::align_up(sizeof(float) * (size_t)plan.M * plan.M);
-  *bytes = plan.BH == 0 ? 0 : 4 * io + mcb + plan.ws_total;
+  *bytes = 4 * io + mcb + ws;
   return MHLA_OK;
 }
 
@@ -371,9 +436,10 @@ mhla_status mhla_forward_host(const void* q, const void* k, const void* v, const
   if (!q || !k || !v || !mc || !out || !dev_buffer) return MHLA_ERR_INVALID_ARG;
   if (mhla::misaligned(dev_buffer, 256)) return MHLA_ERR_INVALID_ARG;
   size_t need = 0;
-  mhla_host_buffer_bytes(p, &need);
+  if ((st = mhla_host_buffer_bytes(p, &need)) != MHLA_OK) return st;
   if (dev_buffer_bytes < need) return MHLA_ERR_WORKSPACE;
-  const size_t io_raw = (size_t)plan.BH * plan.N * plan.d * mhla::elem_bytes(plan.dtype);
+  const size_t unit_bytes = (size_t)plan.N * plan.d * mhla::elem_bytes(plan.dtype);
+  const size_t io_raw = (size_t)plan.BH * unit_bytes;
   const size_t io = mhla::align_up(io_raw);
   const size_t mc_raw = sizeof(float) * (size_t)plan.M * plan.M;
   const size_t mcb = mhla::align_up(mc_raw);
@@ -384,15 +450,70 @@ mhla_status mhla_forward_host(const void* q, const void* k, const void* v, const
   char* dmc = dv + io;
   char* dout = dmc + mcb;
   char* ws = dout + io;
+  const mhla::HostGroups hg = mhla::host_groups(plan);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e;
-  if ((e = cudaMemcpyAsync(dq, q, io_raw, cudaMemcpyHostToDevice, s)) != cudaSuccess) return mhla::cuda_fail(e);
-  if ((e = cudaMemcpyAsync(dk, k, io_raw, cudaMemcpyHostToDevice, s)) != cudaSuccess) return mhla::cuda_fail(e);
-  if ((e = cudaMemcpyAsync(dv, v, io_raw, cudaMemcpyHostToDevice, s)) != cudaSuccess) return mhla::cuda_fail(e);
-  if ((e = cudaMemcpyAsync(dmc, mc, mc_raw, cudaMemcpyHostToDevice, s)) != cudaSuccess) return mhla::cuda_fail(e);
-  st = mhla::run_plan(plan, dq, dk, dv, reinterpret_cast<const float*>(dmc), dout, ws, s);
-  if (st != MHLA_OK) return st;
-  if ((e = cudaMemcpyAsync(out, dout, io_raw, cudaMemcpyDeviceToHost, s)) != cudaSuccess) return mhla::cuda_fail(e);
+
+  // One pipeline per device: group g's copies in run on `in` while group
+  // g-1's kernels run on the caller's stream and group g-2's result goes
+  // back on `out` (the two copy directions use separate engines).
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return mhla::cuda_fail(e);
+  if (dev < 0 || dev >= mhla::kMaxDevices) return MHLA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(mhla::g_pipe_mu[dev]);
+  mhla::HostPipe& hp = mhla::g_pipe[dev];
+  if (!hp.ready) {
+    if ((e = cudaStreamCreateWithFlags(&hp.in, cudaStreamNonBlocking)) != cudaSuccess) return mhla::cuda_fail(e);
+    if ((e = cudaStreamCreateWithFlags(&hp.out, cudaStreamNonBlocking)) != cudaSuccess) return mhla::cuda_fail(e);
+    for (int i = 0; i < 3 * mhla::kMaxHostGroups + 1; ++i)
+      if ((e = cudaEventCreateWithFlags(&hp.ev[i], cudaEventDisableTiming)) != cudaSuccess) return mhla::cuda_fail(e);
+    hp.ready = true;
+  }
+  cudaEvent_t ev_start = hp.ev[3 * mhla::kMaxHostGroups];
+  auto fail = [&](cudaError_t err) {
+    cudaStreamSynchronize(hp.in);
+    cudaStreamSynchronize(s);
+    cudaStreamSynchronize(hp.out);
+    return mhla::cuda_fail(err);
+  };
+  // the copies start after the caller's earlier work on its stream
+  if ((e = cudaEventRecord(ev_start, s)) != cudaSuccess) return fail(e);
+  if ((e = cudaStreamWaitEvent(hp.in, ev_start, 0)) != cudaSuccess) return fail(e);
+  if ((e = cudaStreamWaitEvent(hp.out, ev_start, 0)) != cudaSuccess) return fail(e);
+  if ((e = cudaMemcpyAsync(dmc, mc, mc_raw, cudaMemcpyHostToDevice, hp.in)) != cudaSuccess) return fail(e);
+  for (int g = 0; g < hg.n; ++g) {
+    const int u0 = g * hg.per;
+    const int nu = plan.BH - u0 < hg.per ? plan.BH - u0 : hg.per;
+    const size_t off = (size_t)u0 * unit_bytes, len = (size_t)nu * unit_bytes;
+    cudaEvent_t ev_in = hp.ev[3 * g], ev_run = hp.ev[3 * g + 1], ev_out = hp.ev[3 * g + 2];
+    // K and V first: the summaries need them before the output step needs Q
+    if ((e = cudaMemcpyAsync(dk + off, static_cast<const char*>(k) + off, len, cudaMemcpyHostToDevice, hp.in)) != cudaSuccess)
+      return fail(e);
+    if ((e = cudaMemcpyAsync(dv + off, static_cast<const char*>(v) + off, len, cudaMemcpyHostToDevice, hp.in)) != cudaSuccess)
+      return fail(e);
+    if ((e = cudaMemcpyAsync(dq + off, static_cast<const char*>(q) + off, len, cudaMemcpyHostToDevice, hp.in)) != cudaSuccess)
+      return fail(e);
+    if ((e = cudaEventRecord(ev_in, hp.in)) != cudaSuccess) return fail(e);
+    if ((e = cudaStreamWaitEvent(s, ev_in, 0)) != cudaSuccess) return fail(e);
+    Plan gp;
+    mhla_params gprm = mhla::group_params(p, nu);
+    if ((st = mhla::make_plan(&gprm, &gp, plan.BH)) != MHLA_OK) {
+      fail(cudaSuccess);
+      return st;
+    }
+    st = mhla::run_plan(gp, dq + off, dk + off, dv + off, reinterpret_cast<const float*>(dmc), dout + off, ws, s);
+    if (st != MHLA_OK) {
+      fail(cudaSuccess);
+      return st;
+    }
+    if ((e = cudaEventRecord(ev_run, s)) != cudaSuccess) return fail(e);
+    if ((e = cudaStreamWaitEvent(hp.out, ev_run, 0)) != cudaSuccess) return fail(e);
+    if ((e = cudaMemcpyAsync(static_cast<char*>(out) + off, dout + off, len, cudaMemcpyDeviceToHost, hp.out)) != cudaSuccess)
+      return fail(e);
+    if ((e = cudaEventRecord(ev_out, hp.out)) != cudaSuccess) return fail(e);
+  }
+  // the caller's stream ends after the last copy back
+  if ((e = cudaStreamWaitEvent(s, hp.ev[3 * (hg.n - 1) + 2], 0)) != cudaSuccess) return fail(e);
   if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return mhla::cuda_fail(e);
   return MHLA_OK;
 }
