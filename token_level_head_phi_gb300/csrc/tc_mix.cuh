@@ -205,7 +205,8 @@ __device__ __forceinline__ void mix_body(const MixArgs& a, const Plan& p, const 
     const uint32_t stg_addr = base + kStaging + g * kStagingBytes;
     const int half_nt = a.NT / 2;
     int acc = 0;
-    uint32_t accph = 0;
+    uint32_t accph = 0, sbuf = 0;
+    bool prev_both = false;
     unsigned int batch = 0;
     bool ok = true;
     for (int w = f.cta; w < a.units && ok; w += f.ncta) {
@@ -222,23 +223,31 @@ __device__ __forceinline__ void mix_body(const MixArgs& a, const Plan& p, const 
         float v[32];
         tmem_ld32(taddr + (uint32_t)c0, v);
         tmem_wait_ld();
-        // the previous slice's store has finished reading the staging tile
-        if (gt == 0) bulk_wait_read<0>();
+        // Slices without low residuals alternate between the two halves of
+        // the staging area, so a slice waits only for the store before the
+        // previous one; a slice with residuals takes both halves.
+        const uint32_t off = lo ? 0u : sbuf * 8192u;
+        if (gt == 0) {
+          if (lo || prev_both) bulk_wait_read<0>();
+          else bulk_wait_read<1>();
+        }
         named_sync(1 + g, 128);
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
           const __nv_bfloat16 h = __float2bfloat16_rn(v[j]);
-          reinterpret_cast<__nv_bfloat16*>(stg)[j * 128 + rl] = h;
+          reinterpret_cast<__nv_bfloat16*>(stg + off)[j * 128 + rl] = h;
           if (lo)
             reinterpret_cast<__nv_bfloat16*>(stg + 8192)[j * 128 + rl] = __float2bfloat16_rn(v[j] - __bfloat162float(h));
         }
         fence_proxy_async();
         named_sync(1 + g, 128);
         if (gt == 0) {
-          tma_store_3d(&a.tmO, stg_addr, r0, i0 + c0, flow_slot(f, u));
+          tma_store_3d(&a.tmO, stg_addr + off, r0, i0 + c0, flow_slot(f, u));
           if (lo) tma_store_3d(&a.tmO_lo, stg_addr + 8192, r0, i0 + c0, flow_slot(f, u));
           bulk_commit();
         }
+        prev_both = lo;
+        if (!lo) sbuf ^= 1u;
       }
       if (f.x_done && gt == 0 && (++batch, flow_head_ends(f, w, a.units, per_head))) {
         // this group's rows of the head are written: publish them
