@@ -56,6 +56,19 @@ def load_peaks():
         return 6800.0, 1900.0, 1700.0, "fallback"
 
 
+def job_throughput(local_ms: float, steps: int, units_per_step: int, world: int, dist, device):
+    """Whole-job throughput of N replicas: every rank ran `steps` steps of
+    `units_per_step` token-heads in `local_ms`; the job took as long as its
+    slowest rank (max over ranks), and did `world` times the work.  Returns
+    (max ms over ranks, units per second)."""
+    import torch
+    t = torch.tensor([float(local_ms)], dtype=torch.float64, device=device)
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    max_ms = float(t.item())
+    return max_ms, world * units_per_step * steps / (max_ms / 1e3)
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -310,13 +323,8 @@ def run_mine(args, w: wl.Workload, world: int, rank: int, local: int, dist):
     for evs in ev_sets:
         for j, ph in enumerate(PHASES):
             phase_ms[ph].append(evs[j].elapsed_time(evs[j + 1]))
-    local_ms = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-    if dist is not None:
-        dist.all_reduce(local_ms, op=dist.ReduceOp.MAX)
-    max_ms = float(local_ms.item())
+    max_ms, value = job_throughput(total_ms, K, w.units * w.n_tokens, world, dist, dev)
     ms_per_step = max_ms / K
-    units_tokens = w.units * w.n_tokens
-    value = world * units_tokens * K / (max_ms / 1e3)
 
     hbm, tf_burst, tf_sust, peak_kind = load_peaks()
     pbytes = phase_bytes(w, info, info.variant)
