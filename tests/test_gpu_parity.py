@@ -32,6 +32,7 @@ FULL = {  # workload -> units the oracle checks (None = all)
     "seq_32k_mala": [0, 63],
     "seq_32k_m1": [0, 40],
     "seq_32k_m1_mala": [1, 62],
+    "wan_21x30x50": [0, 23],
 }
 
 
@@ -197,7 +198,7 @@ def _run_variant(w, tensors, mc, norm, variant):
 
 
 @pytest.mark.parametrize("name", ["deit_t", "image_64x64", "video_16x64x64", "seq_32k", "seq_32k_mala",
-                                  "seq_32k_m1", "seq_32k_m1_mala"])
+                                  "seq_32k_m1", "seq_32k_m1_mala", "wan_21x30x50"])
 def test_fused_bitwise_equals_multipass(name):
     w = wl.WORKLOADS[name]
     vals, dev = wl.all_inputs(w)

@@ -82,6 +82,10 @@ WORKLOADS: Dict[str, Workload] = {
     "seq_32k_mala": Workload("seq_32k_mala", 4, 16, 64, (1, 1, 32768), (1, 1, 256), "bf16", 1.0, 1004, "exp1d", "mala"),
     "seq_32k_m1": Workload("seq_32k_m1", 4, 16, 64, (1, 1, 32768), (1, 1, 32768), "bf16", 1.0, 1004, "exp1d"),
     "seq_32k_m1_mala": Workload("seq_32k_m1_mala", 4, 16, 64, (1, 1, 32768), (1, 1, 32768), "bf16", 1.0, 1004, "exp1d", "mala"),
+    # video sequence of the length and block count the MHLA page reports for
+    # Wan (31.5k tokens, M = 105): 21 x 30 x 50 grid, 3 x 10 x 10 blocks of 300
+    # tokens (not a multiple of the 128-row tile: three 100-token chunks each)
+    "wan_21x30x50": Workload("wan_21x30x50", 2, 12, 64, (21, 30, 50), (3, 10, 10), "bf16", 1.0, 1005, "euclid_noise"),
 }
 
 BENCH_WORKLOAD = "video_16x64x64"
