@@ -7,6 +7,7 @@
 #include <cstring>
 
 #include "tc_mix.cuh"
+#include "tc_mixt.cuh"
 
 namespace mhla {
 namespace {
@@ -84,7 +85,68 @@ int launch_variant(const MixArgs& a, const Plan& p, cudaStream_t s) {
   return launch_pdl(tc_mix_kernel<kF16>, dim3(grid), dim3(kThreads), kSmemBytes, s, a, p);
 }
 
+template <bool kF16>
+__global__ void __launch_bounds__(mt::kThreads, 1) tc_mixt_kernel(const __grid_constant__ mt::MixTArgs a, const Plan p) {
+  mt::mixt_body<kF16>(a, p);
+}
+
+template <bool kF16>
+int launch_mixt(const mt::MixTArgs& a, const Plan& p, cudaStream_t s) {
+  auto kern = tc_mixt_kernel<kF16>;
+  cudaError_t ce = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)mt::kSmemBytes);
+  if (ce != cudaSuccess) return (int)ce;
+  int grid = a.itiles * a.items;
+  if (grid > num_sms()) grid = num_sms();
+  return launch_pdl(kern, dim3(grid), dim3(mt::kThreads), mt::kSmemBytes, s, a, p);
+}
+
 }  // namespace
+
+bool mixt_supported(const Plan& p, const TcBuffers& b) {
+  const int Q = p.M * p.splits;
+  const int kchunks = (Q + 63) / 64;
+  // Mc (and its low part under MALA) plus two 128-column accumulators fit
+  // the 512 TMEM columns.  Taken for one query-block tile (M <= 128) with the
+  // fp16 mixing: then every stack tile is read once, as in the streaming
+  // kernel, and Mc stays off shared memory (measured: 1D 32k 29 -> 23 us,
+  // 14x14 x 192 heads 60 -> 40 us).  With more tiles each stack tile would be
+  // read once per 128 query blocks instead of once per 256 (video: 66 -> 89
+  // us), and under MALA the two kernels measured the same.
+  return p.R % 128 == 0 && kchunks * 32 * (b.f16 ? 1 : 2) <= 256 && p.M <= 128 && b.f16;
+}
+
+int build_mixt_args(const Plan& p, const TcBuffers& b, mt::MixTArgs* out) {
+  mt::MixTArgs& a = *out;
+  memset(&a, 0, sizeof(a));
+  const int Q = p.M * p.splits;
+  const int W = p.R;
+  const uint64_t dimsX[4] = {64, (uint64_t)Q, (uint64_t)(W / 64), (uint64_t)b.slots};
+  const uint64_t strX[3] = {2ull * W, 128, 2ull * W * Q};
+  const uint32_t boxX[4] = {64, 64, 2, 1};
+  int e;
+  if ((e = encode_tmap(&a.tmX, b.stack, 4, dimsX, strX, boxX, b.f16)) != 0) return e;
+  if ((e = encode_tmap_bf16(&a.tmX_lo, b.stack_lo ? (const void*)b.stack_lo : b.stack, 4, dimsX, strX, boxX)) != 0)
+    return e;
+  const uint64_t dimsO[3] = {(uint64_t)p.R, (uint64_t)p.M, (uint64_t)b.slots};
+  const uint64_t strO[2] = {2ull * p.R, 2ull * p.R * p.M};
+  const uint32_t boxO[3] = {64, 128, 1};
+  if ((e = encode_tmap_bf16(&a.tmO, b.mixed_hi, 3, dimsO, strO, boxO)) != 0) return e;
+  if ((e = encode_tmap_bf16(&a.tmO_lo, b.mixed_lo, 3, dimsO, strO, boxO)) != 0) return e;
+  a.mc = b.f16 ? (const void*)b.mc_f16 : (const void*)b.mc_hi;
+  a.mc_lo = b.mc_lo;
+  a.Q = Q;
+  a.Qp = b.Qp;
+  a.kchunks = (Q + 63) / 64;
+  a.itiles = (p.M + 127) / 128;
+  a.rtiles = W / 128;
+  a.items = b.slots * a.rtiles;
+  a.write_lo = p.norm == MHLA_NORM_MALA;
+  a.stage_bytes = mt::kBTile * (b.f16 ? 1u : 2u);
+  a.stages = (int)(mt::kStageArea / a.stage_bytes);
+  if (a.stages > mt::kMaxStages) a.stages = mt::kMaxStages;
+  a.err = p.err;
+  return 0;
+}
 
 int launch_tc_prep(const Plan& p, const float* mc, const TcBuffers& b, cudaStream_t s) {
   const int threads = 256;
@@ -156,6 +218,12 @@ int build_mix_args(const Plan& p, const TcBuffers& b, int slots, mx::MixArgs* ou
 }
 
 int launch_tc_mix(const Plan& p, const TcBuffers& b, cudaStream_t s) {
+  if (mixt_supported(p, b)) {
+    mt::MixTArgs t;
+    int e = build_mixt_args(p, b, &t);
+    if (e != 0) return e;
+    return b.f16 ? launch_mixt<true>(t, p, s) : launch_mixt<false>(t, p, s);
+  }
   MixArgs a;
   int e = build_mix_args(p, b, b.slots, &a);
   if (e != 0) return e;
