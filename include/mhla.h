@@ -188,6 +188,25 @@ mhla_status mhla_forward_host(const void* q, const void* k, const void* v, const
                               const mhla_params* p, void* out, void* dev_buffer,
                               size_t dev_buffer_bytes, void* stream);
 
+/* Backward pass: the gradients of L = sum(dout * o), o = mhla_forward(q, k, v,
+ * mc), with respect to q, k, v and mc -- the chain rule of the forward steps
+ * ("MHLA: Restoring Expressivity of Linear Attention via Token-Level
+ * Multi-Head": Mc is learned end to end, key design 3; the pages print no
+ * gradient).  Every norm and feature map of the forward; float32 arithmetic
+ * on the CUDA cores for every head dimension and both dtypes (p->variant is
+ * ignored).  The forward summaries are recomputed inside the call.
+ *   dout, dq, dk, dv: [B, H, N, d] in p->dtype, like q; dmc: float32 [M, M],
+ *   overwritten with the sum over every (batch, head).
+ * Device pointers, 16-byte aligned (mc, dmc 4-byte); dq, dk, dv, dmc must
+ * not overlap the inputs or each other.  workspace as for mhla_forward, of
+ * at least mhla_backward_workspace_bytes(p) bytes (NULL with 0 bytes: the
+ * library allocates it on `stream`).  Asynchronous on `stream`.  Returns the
+ * validation errors of mhla_forward, MHLA_ERR_WORKSPACE, MHLA_ERR_CUDA. */
+mhla_status mhla_backward_workspace_bytes(const mhla_params* p, size_t* bytes);
+mhla_status mhla_backward(const void* q, const void* k, const void* v, const float* mc, const void* dout,
+                          const mhla_params* p, void* dq, void* dk, void* dv, float* dmc, void* workspace,
+                          size_t workspace_bytes, void* stream);
+
 /* Reads and clears the device error word of the current device.  Blocks the
  * host until the device is idle.  *code receives MHLA_OK or the first status
  * a kernel recorded (MHLA_ERR_DEVICE_TIMEOUT, MHLA_ERR_OVERFLOW); *detail

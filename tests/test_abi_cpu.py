@@ -213,3 +213,44 @@ def test_debug_options(lib):
     for opt in (mb.DEBUG_FLOW_WAIT_NS, mb.DEBUG_FLOW_STALL):
         assert lib.mhla_set_debug(opt, 5) == mb.MHLA_OK
         assert lib.mhla_set_debug(opt, 0) == mb.MHLA_OK
+
+
+def test_backward_workspace_and_checks(lib):
+    w = wl.WORKLOADS["deit_t"]
+    p = _params(w)
+    d, R = w.head_dim, w.head_dim ** 2 + 2 * w.head_dim
+    info = mb.mhla_plan(_params(w, variant="simt"))
+    rows = w.units * w.n_blocks * info.summary_splits
+    need = mb.mhla_backward_workspace_bytes(p)
+    # per-piece summaries and their gradients, mixed summaries and their gradients
+    assert need >= 4 * (2 * rows * R + rows + 2 * w.units * w.n_blocks * R + w.n_blocks)
+    # the variant does not matter: the backward always runs the float32 kernels
+    assert mb.mhla_backward_workspace_bytes(_params(w, variant="simt")) == need
+    io = w.units * w.n_tokens * d * 2
+    q, k, v, dout = FAKE, FAKE + 2 * io, FAKE + 4 * io, FAKE + 6 * io
+    mc, dq, dk, dv, dmc, ws = FAKE + 8 * io, FAKE + 10 * io, FAKE + 12 * io, FAKE + 14 * io, FAKE + 16 * io, \
+        FAKE + 18 * io
+    f = lib.mhla_backward
+    P = ctypes.byref(p)
+    assert f(q, k, v, mc, dout, None, dq, dk, dv, dmc, ws, need, None) == mb.MHLA_ERR_INVALID_ARG
+    assert f(q, k, v, mc, None, P, dq, dk, dv, dmc, ws, need, None) == mb.MHLA_ERR_INVALID_ARG
+    assert f(q, k, v, mc, dout, P, dq, dk, dv, None, ws, need, None) == mb.MHLA_ERR_INVALID_ARG
+    assert f(q, k, v, mc, dout + 2, P, dq, dk, dv, dmc, ws, need, None) == mb.MHLA_ERR_INVALID_ARG
+    assert f(q, k, v, mc, dout, P, dq, dk + 8, dv, dmc, ws, need, None) == mb.MHLA_ERR_INVALID_ARG
+    assert f(q, k, v, mc, dout, P, dq, dk, dv, dmc + 2, ws, need, None) == mb.MHLA_ERR_INVALID_ARG
+    # gradients aliasing an input or each other
+    assert f(q, k, v, mc, dout, P, q + 256, dk, dv, dmc, ws, need, None) == mb.MHLA_ERR_INVALID_ARG
+    assert f(q, k, v, mc, dout, P, dq, dq + 256, dv, dmc, ws, need, None) == mb.MHLA_ERR_INVALID_ARG
+    assert f(q, k, v, mc, dout, P, dq, dk, dv, dv + 256, ws, need, None) == mb.MHLA_ERR_INVALID_ARG
+    assert f(q, k, v, mc, dout, P, dq, dk, dv, mc, ws, need, None) == mb.MHLA_ERR_INVALID_ARG
+    # workspace
+    assert f(q, k, v, mc, dout, P, dq, dk, dv, dmc, ws, need - 1, None) == mb.MHLA_ERR_WORKSPACE
+    assert f(q, k, v, mc, dout, P, dq, dk, dv, dmc, None, need, None) == mb.MHLA_ERR_INVALID_ARG
+    assert f(q, k, v, mc, dout, P, dq, dk, dv, dmc, ws + 16, need, None) == mb.MHLA_ERR_INVALID_ARG
+    # invalid shapes fail before any pointer is looked at; empty problems are no-ops
+    bad = mb.make_params(1, 1, 48, w.grid, w.block)
+    assert f(None, None, None, None, None, ctypes.byref(bad), None, None, None, None, None, 0, None) == \
+        mb.MHLA_ERR_INVALID_ARG
+    empty = mb.make_params(0, 3, 64, w.grid, w.block)
+    assert mb.mhla_backward_workspace_bytes(empty) == 0
+    assert f(None, None, None, None, None, ctypes.byref(empty), None, None, None, None, None, 0, None) == mb.MHLA_OK

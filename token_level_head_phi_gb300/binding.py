@@ -91,6 +91,9 @@ SIGNATURES = [
     ("mhla_last_error_string", ctypes.c_char_p, []),
     ("mhla_abi_version", ctypes.c_int, []),
     ("mhla_set_debug", ctypes.c_int, [ctypes.c_int, ctypes.c_longlong]),
+    ("mhla_backward_workspace_bytes", ctypes.c_int, [ctypes.POINTER(MhlaParams), ctypes.POINTER(ctypes.c_size_t)]),
+    ("mhla_backward", ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.POINTER(MhlaParams)] + [ctypes.c_void_p] * 5
+     + [ctypes.c_size_t, ctypes.c_void_p]),
 ]
 
 
@@ -201,6 +204,51 @@ def mhla_forward(q, k, v, mc, grid, block, norm: str = "divisive", feature_map: 
                                  out.data_ptr(), workspace.data_ptr(), ws_bytes, handle)
     _check(status, "mhla_forward")
     return out
+
+
+def mhla_backward_workspace_bytes(p: MhlaParams) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load().mhla_backward_workspace_bytes(ctypes.byref(p), ctypes.byref(n)), "mhla_backward_workspace_bytes")
+    return n.value
+
+
+def mhla_backward(q, k, v, mc, dout, grid, block, norm: str = "divisive", feature_map: str = "elu1",
+                  dq=None, dk=None, dv=None, dmc=None, workspace=None, stream=None):
+    """Gradients of sum(dout * mhla_forward(q, k, v, mc)): returns (dq, dk, dv, dmc).
+
+    dq, dk, dv are shaped and typed like q; dmc is float32 [M, M] (summed
+    over every batch and head).  Outputs and workspace are allocated with
+    torch when not given; enqueued on ``stream`` without synchronising.
+    """
+    import torch
+    p = _params_for(q, grid, block, feature_map, norm, "simt")
+    for name, t in (("q", q), ("k", k), ("v", v), ("dout", dout)):
+        if not t.is_cuda or not t.is_contiguous() or t.shape != q.shape or t.dtype != q.dtype:
+            raise ValueError(f"{name} must be a contiguous CUDA tensor shaped and typed like q")
+    if not mc.is_cuda or mc.dtype != torch.float32 or not mc.is_contiguous():
+        raise ValueError("mc must be a contiguous float32 CUDA tensor")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        if not t.is_cuda or not t.is_contiguous() or t.shape != q.shape or t.dtype != q.dtype:
+            raise ValueError(f"{name} must be a contiguous CUDA tensor shaped and typed like q")
+    if dmc is None:
+        dmc = torch.empty_like(mc)
+    elif not dmc.is_cuda or dmc.dtype != torch.float32 or not dmc.is_contiguous() or dmc.shape != mc.shape:
+        raise ValueError("dmc must be a contiguous float32 CUDA tensor shaped like mc")
+    need = mhla_backward_workspace_bytes(p)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    status = load().mhla_backward(q.data_ptr(), k.data_ptr(), v.data_ptr(), mc.data_ptr(), dout.data_ptr(),
+                                  ctypes.byref(p), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), dmc.data_ptr(),
+                                  workspace.data_ptr(), ws_bytes, handle)
+    _check(status, "mhla_backward")
+    return dq, dk, dv, dmc
 
 
 def mhla_forward_raw(q_ptr: int, k_ptr: int, v_ptr: int, mc_ptr: int, p: MhlaParams, out_ptr: int,

@@ -1,0 +1,381 @@
+// Backward pass of the MHLA forward on the CUDA cores (float32 arithmetic,
+// every head dimension, bf16 or float32 tensors): the gradients of
+// sum(dO * o) with respect to Q, K, V and Mc.  The pages say Mc is learned
+// end to end ("MHLA: Restoring Expressivity of Linear Attention via
+// Token-Level Multi-Head", key design 3) but print no gradient; these are the
+// chain rule of the forward steps taken in reverse (token t in query block
+// i = b(t), token j in summary block b):
+//
+//   output:   dnum_t, ds_t from the norm (DIVISIVE dnum = dO/s,
+//             ds = -(dO.o)/s; NONE dnum = dO; MALA below)
+//             dphi(q_t) = S~_i dnum_t + z~_i ds_t
+//             dS~_i = sum_t phi(q_t) dnum_t^T,  dz~_i = sum_t ds_t phi(q_t)
+//   mixing:   dS_b = sum_i Mc[i,b] dS~_i (z, v likewise)
+//             dMc[i,b] = sum over heads of <dS~_i, S_b> + <dz~_i, z_b>
+//                        (+ <dv~_i, v_b> + dn~_i n_b for MALA)
+//   summary:  dphi(k_j) = dS_b v_j + dz_b,  dv_j = dS_b^T phi(k_j) (+ dv_b)
+//   map:      dq = dphi(q) * phi'(q),  dk = dphi(k) * phi'(k)
+// MALA ("Rectifying Magnitude Neglect in Linear Attention", key designs,
+// with the mixed sums): o = beta num - gamma v~_i, beta = 1 + 1/s,
+// gamma = s / n~_i, so dnum = beta dO, ds = -(dO.num)/s^2 - (dO.v~_i)/n~_i,
+// dv~_i = -sum_t gamma_t dO_t, dn~_i = sum_t (dO_t.v~_i) s_t / n~_i^2.
+//
+// Kernels, in launch order after the forward summaries and mixing are
+// recomputed by the float32 forward kernels:
+//   bwd_output   one CTA per (query block piece, head): dq and the piece's
+//                partial dS~, dz~, dv~ (and dn~), kept per piece so the
+//                accumulation order is fixed (no atomics)
+//   bwd_mix      dS_b = sum over query pieces of Mc[i(piece), b] * partials
+//   bwd_mc       dMc = sum over heads of partials-per-block . summaries-per-block
+//   bwd_summary  one CTA per (summary block piece, head): dk, dv
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "backward.h"
+#include "common.cuh"
+
+namespace mhla {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kTile = 32;  // tokens per shared-memory tile
+
+__device__ __forceinline__ float phi_grad(float x, int fmap) {
+  if (fmap == MHLA_FEATURE_IDENTITY) return 1.f;
+  return x > 0.f ? 1.f : expf(x);
+}
+
+// One CTA per (query block piece, head).  Shared memory: S~_i [D][D], z~_i,
+// v~_i, and per tile phi(q) [T][D], dO [T][D], dnum [T][D] and per-token
+// scalars.  Thread e owns entries e, e + 256, ... of the partial dS~.
+template <int D, typename T>
+__global__ void __launch_bounds__(kThreads)
+bwd_output_kernel(Plan p, const T* __restrict__ Q, const T* __restrict__ dO, const float* __restrict__ mixed,
+                  const float* __restrict__ rowsum, T* __restrict__ dQ, float* __restrict__ dmixp,
+                  float* __restrict__ dnp) {
+  constexpr int PER = (D * D + kThreads - 1) / kThreads;
+  extern __shared__ float sm[];
+  float* sS = sm;                  // D*D
+  float* sz = sS + D * D;          // D
+  float* sv = sz + D;              // D
+  float* sq = sv + D;              // kTile*D: phi(q)
+  float* sg = sq + kTile * D;      // kTile*D: dO
+  float* sdn = sg + kTile * D;     // kTile*D: dnum
+  float* sds = sdn + kTile * D;    // kTile: ds
+  float* ssc = sds + kTile;        // kTile: s
+  float* sgam = ssc + kTile;       // kTile: gamma (MALA)
+  float* sdgam = sgam + kTile;     // kTile: dO . v~ (MALA)
+  const int u = blockIdx.y;
+  const int row = blockIdx.x;      // query piece: block i, piece row % splits
+  const int i = row / p.splits;
+  const int l0 = (row % p.splits) * p.split_len;
+  const int l1 = min(p.nb, l0 + p.split_len);
+  const int tid = threadIdx.x;
+  const float* mrow = mixed + ((size_t)u * p.M + i) * p.R;
+  for (int e = tid; e < D * D + 2 * D; e += kThreads) sm[e] = mrow[e];
+  const float ntilde = (float)p.nb * rowsum[i];
+  const size_t base = (size_t)u * p.N * D;
+
+  float acc[PER];
+#pragma unroll
+  for (int j = 0; j < PER; ++j) acc[j] = 0.f;
+  float zacc = 0.f, vacc = 0.f, nacc = 0.f;
+
+  for (int lt = l0; lt < l1; lt += kTile) {
+    const int cnt = min(kTile, l1 - lt);
+    __syncthreads();
+    for (int e = tid; e < kTile * D; e += kThreads) {
+      const int tt = e / D, f = e % D;
+      float qx = 0.f, gx = 0.f;
+      if (tt < cnt) {
+        const size_t off = base + (size_t)block_token(p, i, lt + tt) * D + f;
+        qx = phi_apply(to_f32(Q[off]), p.fmap);
+        gx = to_f32(dO[off]);
+      }
+      sq[e] = qx;
+      sg[e] = gx;
+    }
+    __syncthreads();
+    // per token: s = phi(q).z~ and the dO.v~ of MALA
+    if (tid < kTile) {
+      float s = 0.f, gv = 0.f;
+      for (int k = 0; k < D; ++k) {
+        s = fmaf(sq[tid * D + k], sz[k], s);
+        gv = fmaf(sg[tid * D + k], sv[k], gv);
+      }
+      ssc[tid] = s;
+      sdgam[tid] = gv;
+    }
+    __syncthreads();
+    // dnum[t][c] and the per-token reduction dO.num for ds
+    for (int e = tid; e < kTile * D; e += kThreads) {
+      const int tt = e / D, c = e % D;
+      float num = 0.f;
+      for (int k = 0; k < D; ++k) num = fmaf(sq[tt * D + k], sS[k * D + c], num);
+      const float g = sg[e];
+      const float s = ssc[tt];
+      float dn;
+      if (p.norm == MHLA_NORM_DIVISIVE) dn = g / s;
+      else if (p.norm == MHLA_NORM_MALA) dn = (1.f + 1.f / s) * g;
+      else dn = g;
+      sdn[e] = dn;
+      // g * num replaces g: only the per-token sum dO . num is needed below
+      sg[e] = g * num;
+    }
+    __syncthreads();
+    if (tid < kTile) {
+      float gnum = 0.f;
+      for (int c = 0; c < D; ++c) gnum += sg[tid * D + c];
+      const float s = ssc[tid];
+      float ds = 0.f;
+      if (p.norm == MHLA_NORM_DIVISIVE) {
+        ds = -gnum / (s * s);
+      } else if (p.norm == MHLA_NORM_MALA) {
+        const float dbeta = gnum, dgamma = -sdgam[tid];
+        ds = -dbeta / (s * s) + dgamma / ntilde;
+        sgam[tid] = s / ntilde;
+      }
+      if (tid >= cnt) ds = 0.f;
+      sds[tid] = ds;
+    }
+    __syncthreads();
+    // dq[t][k] = (sum_c S~[k][c] dnum[t][c] + z~[k] ds[t]) * phi'(q)
+    for (int e = tid; e < cnt * D; e += kThreads) {
+      const int tt = e / D, k = e % D;
+      float a = sz[k] * sds[tt];
+      for (int c = 0; c < D; ++c) a = fmaf(sS[k * D + c], sdn[tt * D + c], a);
+      const size_t off = base + (size_t)block_token(p, i, lt + tt) * D + k;
+      dQ[off] = from_f32<T>(a * phi_grad(to_f32(Q[off]), p.fmap));
+    }
+    // partial dS~ += phi(q) dnum^T, dz~ += ds phi(q); MALA: dv~, dn~
+    for (int tt = 0; tt < cnt; ++tt) {
+#pragma unroll
+      for (int j = 0; j < PER; ++j) {
+        const int e = tid + j * kThreads;
+        if (e < D * D) acc[j] = fmaf(sq[tt * D + e / D], sdn[tt * D + e % D], acc[j]);
+      }
+      if (tid < D) {
+        zacc = fmaf(sds[tt], sq[tt * D + tid], zacc);
+      } else if (tid < 2 * D && p.norm == MHLA_NORM_MALA) {
+        // dv~ = -sum_t gamma_t dO_t (the tile's dO was overwritten above)
+        const size_t off = base + (size_t)block_token(p, i, lt + tt) * D + (tid - D);
+        vacc = fmaf(-sgam[tt], to_f32(dO[off]), vacc);
+      }
+      if (tid == 0 && p.norm == MHLA_NORM_MALA)
+        nacc += sdgam[tt] * ssc[tt] / (ntilde * ntilde);  // dn~ = -dgamma s / n~^2, dgamma = -dO.v~
+    }
+  }
+  float* out = dmixp + ((size_t)u * p.M * p.splits + row) * p.R;
+#pragma unroll
+  for (int j = 0; j < PER; ++j) {
+    const int e = tid + j * kThreads;
+    if (e < D * D) out[e] = acc[j];
+  }
+  if (tid < D) out[D * D + tid] = zacc;
+  else if (tid < 2 * D) out[D * D + tid] = vacc;
+  if (tid == 0) dnp[(size_t)u * p.M * p.splits + row] = nacc;
+}
+
+// dstack[u][b][r] = sum_q Mc[q / splits][b] * dmixp[u][q][r]: a tiled SGEMM
+// with Mc transposed (32 summary blocks x 128 record columns per CTA).
+__global__ void __launch_bounds__(kThreads)
+bwd_mix_kernel(Plan p, const float* __restrict__ mc, const float* __restrict__ dmixp, float* __restrict__ dstack) {
+  constexpr int TB = 32, TR = 128, TQ = 16;
+  __shared__ float smc[TB][TQ + 1];
+  __shared__ float sst[TQ][TR];
+  const int u = blockIdx.z;
+  const int b0 = blockIdx.y * TB;
+  const int r0 = blockIdx.x * TR;
+  const int tx = threadIdx.x % 32, ty = threadIdx.x / 32;
+  const int rows = p.M * p.splits;
+  const float* st = dmixp + (size_t)u * rows * p.R;
+  float acc[4][4] = {};
+  for (int q0 = 0; q0 < rows; q0 += TQ) {
+    __syncthreads();
+    for (int e = threadIdx.x; e < TB * TQ; e += kThreads) {
+      const int bb = e / TQ, qq = e % TQ;
+      const int b = b0 + bb, q = q0 + qq;
+      smc[bb][qq] = (b < p.M && q < rows) ? mc[(size_t)(q / p.splits) * p.M + b] : 0.f;
+    }
+    for (int e = threadIdx.x; e < TQ * TR; e += kThreads) {
+      const int qq = e / TR, rr = e % TR;
+      const int q = q0 + qq, r = r0 + rr;
+      sst[qq][rr] = (q < rows && r < p.R) ? st[(size_t)q * p.R + r] : 0.f;
+    }
+    __syncthreads();
+#pragma unroll 4
+    for (int qq = 0; qq < TQ; ++qq) {
+      float a[4], bv[4];
+#pragma unroll
+      for (int m = 0; m < 4; ++m) a[m] = smc[ty * 4 + m][qq];
+#pragma unroll
+      for (int n = 0; n < 4; ++n) bv[n] = sst[qq][tx + 32 * n];
+#pragma unroll
+      for (int m = 0; m < 4; ++m)
+#pragma unroll
+        for (int n = 0; n < 4; ++n) acc[m][n] = fmaf(a[m], bv[n], acc[m][n]);
+    }
+  }
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    const int b = b0 + ty * 4 + m;
+    if (b >= p.M) continue;
+    float* dst = dstack + ((size_t)u * p.M + b) * p.R;
+#pragma unroll
+    for (int n = 0; n < 4; ++n) {
+      const int r = r0 + tx + 32 * n;
+      if (r < p.R) dst[r] = acc[m][n];
+    }
+  }
+}
+
+// dMc[i][b] = sum_u sum_r dX~[u][i][r] X[u][b][r] (+ MALA: n_b sum_u dn~[u][i]),
+// dX~ and X summed over pieces on the fly; one CTA per 16 x 16 tile of dMc,
+// reduced over (u, r) in a fixed order.  The sum is blocked in three levels
+// (32 record entries, one head, all heads): the terms of a DIVISIVE or MALA
+// row cancel to a small fraction of their size, and one running float32
+// sum over all d^2 + 2d entries of every head would carry a rounding error
+// proportional to that count.
+__global__ void __launch_bounds__(kThreads)
+bwd_mc_kernel(Plan p, const float* __restrict__ dmixp, const float* __restrict__ stack,
+              const float* __restrict__ dnp, float* __restrict__ dmc) {
+  constexpr int TI = 16, TK = 32;
+  __shared__ float sa[TI][TK + 1];
+  __shared__ float sb[TI][TK + 1];
+  const int i0 = blockIdx.y * TI, b0 = blockIdx.x * TI;
+  const int ti = threadIdx.x / TI, tb = threadIdx.x % TI;
+  const int rows = p.M * p.splits;
+  float acc = 0.f;
+  for (int u = 0; u < p.BH; ++u) {
+    float acc_u = 0.f;
+    const float* da = dmixp + (size_t)u * rows * p.R;
+    const float* xa = stack + (size_t)u * rows * p.R;
+    for (int r0 = 0; r0 < p.R; r0 += TK) {
+      __syncthreads();
+      for (int e = threadIdx.x; e < TI * TK; e += kThreads) {
+        const int ii = e / TK, rr = e % TK;
+        const int r = r0 + rr;
+        float x = 0.f, y = 0.f;
+        if (r < p.R) {
+          if (i0 + ii < p.M)
+            for (int s = 0; s < p.splits; ++s) x += da[((size_t)(i0 + ii) * p.splits + s) * p.R + r];
+          if (b0 + ii < p.M)
+            for (int s = 0; s < p.splits; ++s) y += xa[((size_t)(b0 + ii) * p.splits + s) * p.R + r];
+        }
+        sa[ii][rr] = x;
+        sb[ii][rr] = y;
+      }
+      __syncthreads();
+      float part = 0.f;
+#pragma unroll 8
+      for (int rr = 0; rr < TK; ++rr) part = fmaf(sa[ti][rr], sb[tb][rr], part);
+      acc_u += part;
+    }
+    acc += acc_u;
+  }
+  const int i = i0 + ti, b = b0 + tb;
+  if (i < p.M && b < p.M) {
+    if (p.norm == MHLA_NORM_MALA) {
+      float dn = 0.f;
+      for (int u = 0; u < p.BH; ++u)
+        for (int s = 0; s < p.splits; ++s) dn += dnp[(size_t)u * rows + (size_t)i * p.splits + s];
+      acc = fmaf((float)p.nb, dn, acc);
+    }
+    dmc[(size_t)i * p.M + b] = acc;
+  }
+}
+
+// One CTA per (summary block piece, head): dS_b, dz_b, dv_b in shared memory;
+// dk_j = (dS_b v_j + dz_b) * phi'(k_j), dv_j = dS_b^T phi(k_j) + dv_b.
+template <int D, typename T>
+__global__ void __launch_bounds__(kThreads)
+bwd_summary_kernel(Plan p, const T* __restrict__ K, const T* __restrict__ V, const float* __restrict__ dstack,
+                   T* __restrict__ dK, T* __restrict__ dV) {
+  extern __shared__ float sm[];
+  float* sS = sm;                  // D*D
+  float* sz = sS + D * D;          // D
+  float* sv = sz + D;              // D
+  float* sk = sv + D;              // kTile*D: phi(k)
+  float* sx = sk + kTile * D;      // kTile*D: v
+  const int u = blockIdx.y;
+  const int row = blockIdx.x;
+  const int b = row / p.splits;
+  const int l0 = (row % p.splits) * p.split_len;
+  const int l1 = min(p.nb, l0 + p.split_len);
+  const int tid = threadIdx.x;
+  const float* drow = dstack + ((size_t)u * p.M + b) * p.R;
+  for (int e = tid; e < D * D + 2 * D; e += kThreads) sm[e] = drow[e];
+  const size_t base = (size_t)u * p.N * D;
+  for (int lt = l0; lt < l1; lt += kTile) {
+    const int cnt = min(kTile, l1 - lt);
+    __syncthreads();
+    for (int e = tid; e < kTile * D; e += kThreads) {
+      const int tt = e / D, f = e % D;
+      float kx = 0.f, vx = 0.f;
+      if (tt < cnt) {
+        const size_t off = base + (size_t)block_token(p, b, lt + tt) * D + f;
+        kx = phi_apply(to_f32(K[off]), p.fmap);
+        vx = to_f32(V[off]);
+      }
+      sk[e] = kx;
+      sx[e] = vx;
+    }
+    __syncthreads();
+    for (int e = tid; e < cnt * D; e += kThreads) {
+      const int tt = e / D, f = e % D;
+      float gk = sz[f], gv = sv[f];
+      for (int m = 0; m < D; ++m) {
+        gk = fmaf(sS[f * D + m], sx[tt * D + m], gk);   // (dS_b v_j)[f]
+        gv = fmaf(sS[m * D + f], sk[tt * D + m], gv);   // (dS_b^T phi(k_j))[f]
+      }
+      const size_t off = base + (size_t)block_token(p, b, lt + tt) * D + f;
+      dK[off] = from_f32<T>(gk * phi_grad(to_f32(K[off]), p.fmap));
+      dV[off] = from_f32<T>(gv);
+    }
+  }
+}
+
+template <int D, typename T>
+int run_d(const Plan& p, const BwdBuffers& w, const void* q, const void* k, const void* v, const void* dout,
+          void* dq, void* dk, void* dv, cudaStream_t s) {
+  const size_t smo = sizeof(float) * (D * D + 2 * D + 3 * kTile * D + 4 * kTile);
+  auto ko = bwd_output_kernel<D, T>;
+  cudaError_t e = cudaFuncSetAttribute(ko, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smo);
+  if (e != cudaSuccess) return (int)e;
+  ko<<<dim3(p.M * p.splits, p.BH), kThreads, smo, s>>>(p, (const T*)q, (const T*)dout, w.mixed, w.rowsum, (T*)dq,
+                                                       w.dmixp, w.dnp);
+  if ((e = cudaGetLastError()) != cudaSuccess) return (int)e;
+  bwd_mix_kernel<<<dim3((p.R + 127) / 128, (p.M + 31) / 32, p.BH), kThreads, 0, s>>>(p, w.mc, w.dmixp, w.dstack);
+  if ((e = cudaGetLastError()) != cudaSuccess) return (int)e;
+  bwd_mc_kernel<<<dim3((p.M + 15) / 16, (p.M + 15) / 16), kThreads, 0, s>>>(p, w.dmixp, w.stack, w.dnp, w.dmc);
+  if ((e = cudaGetLastError()) != cudaSuccess) return (int)e;
+  const size_t sms = sizeof(float) * (D * D + 2 * D + 2 * kTile * D);
+  auto ks = bwd_summary_kernel<D, T>;
+  if ((e = cudaFuncSetAttribute(ks, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sms)) != cudaSuccess)
+    return (int)e;
+  ks<<<dim3(p.M * p.splits, p.BH), kThreads, sms, s>>>(p, (const T*)k, (const T*)v, w.dstack, (T*)dk, (T*)dv);
+  return (int)cudaGetLastError();
+}
+
+template <typename T>
+int run_t(const Plan& p, const BwdBuffers& w, const void* q, const void* k, const void* v, const void* dout,
+          void* dq, void* dk, void* dv, cudaStream_t s) {
+  switch (p.d) {
+    case 16: return run_d<16, T>(p, w, q, k, v, dout, dq, dk, dv, s);
+    case 32: return run_d<32, T>(p, w, q, k, v, dout, dq, dk, dv, s);
+    case 64: return run_d<64, T>(p, w, q, k, v, dout, dq, dk, dv, s);
+    case 128: return run_d<128, T>(p, w, q, k, v, dout, dq, dk, dv, s);
+  }
+  return (int)cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+int launch_backward(const Plan& p, const BwdBuffers& w, const void* q, const void* k, const void* v,
+                    const void* dout, void* dq, void* dk, void* dv, void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (p.dtype == MHLA_DTYPE_F32) return run_t<float>(p, w, q, k, v, dout, dq, dk, dv, s);
+  return run_t<__nv_bfloat16>(p, w, q, k, v, dout, dq, dk, dv, s);
+}
+
+}  // namespace mhla

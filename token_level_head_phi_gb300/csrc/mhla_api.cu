@@ -11,6 +11,7 @@
 
 #include "mhla.h"
 #include "plan.h"
+#include "backward.h"
 #include "tc_host.h"
 
 namespace mhla {
@@ -343,9 +344,115 @@ std::mutex g_pipe_mu[kMaxDevices];
 
 }  // namespace mhla
 
+namespace mhla {
+
+// Backward plan (float32 CUDA-core kernels) and its workspace layout.
+struct BwdLayout {
+  size_t stack, mixed, rowsum, dmixp, dnp, dstack, total;
+};
+
+mhla_status make_bwd_plan(const mhla_params* prm, Plan* plan, BwdLayout* lay) {
+  if (!prm) return MHLA_ERR_INVALID_ARG;
+  mhla_params p = *prm;
+  p.variant = MHLA_VARIANT_SIMT;
+  mhla_status st = make_plan(&p, plan);
+  if (st != MHLA_OK) return st;
+  const size_t rows = (size_t)plan->BH * plan->M * plan->splits;
+  size_t off = 0;
+  lay->stack = off;
+  off = align_up(off + sizeof(float) * rows * plan->R);
+  lay->mixed = off;
+  off = align_up(off + sizeof(float) * (size_t)plan->BH * plan->M * plan->R);
+  lay->rowsum = off;
+  off = align_up(off + sizeof(float) * (size_t)plan->M);
+  lay->dmixp = off;
+  off = align_up(off + sizeof(float) * rows * plan->R);
+  lay->dnp = off;
+  off = align_up(off + sizeof(float) * rows);
+  lay->dstack = off;
+  off = align_up(off + sizeof(float) * (size_t)plan->BH * plan->M * plan->R);
+  lay->total = plan->BH == 0 ? 0 : off;
+  return MHLA_OK;
+}
+
+}  // namespace mhla
+
 using mhla::Plan;
 
 extern "C" {
+
+mhla_status mhla_backward_workspace_bytes(const mhla_params* p, size_t* bytes) {
+  if (!bytes) return MHLA_ERR_INVALID_ARG;
+  Plan plan;
+  mhla::BwdLayout lay;
+  mhla_status st = mhla::make_bwd_plan(p, &plan, &lay);
+  if (st != MHLA_OK) return st;
+  *bytes = lay.total;
+  return MHLA_OK;
+}
+
+mhla_status mhla_backward(const void* q, const void* k, const void* v, const float* mc, const void* dout,
+                          const mhla_params* p, void* dq, void* dk, void* dv, float* dmc, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+  Plan plan;
+  mhla::BwdLayout lay;
+  mhla_status st = mhla::make_bwd_plan(p, &plan, &lay);
+  if (st != MHLA_OK) return st;
+  if (plan.BH == 0) return MHLA_OK;
+  if (!q || !k || !v || !mc || !dout || !dq || !dk || !dv || !dmc) return MHLA_ERR_INVALID_ARG;
+  const void* io_in[4] = {q, k, v, dout};
+  void* io_out[3] = {dq, dk, dv};
+  for (const void* x : io_in)
+    if (mhla::misaligned(x, 16)) return MHLA_ERR_INVALID_ARG;
+  for (const void* x : io_out)
+    if (mhla::misaligned(x, 16)) return MHLA_ERR_INVALID_ARG;
+  if (mhla::misaligned(mc, 4) || mhla::misaligned(dmc, 4)) return MHLA_ERR_INVALID_ARG;
+  const size_t io = (size_t)plan.BH * plan.N * plan.d * mhla::elem_bytes(plan.dtype);
+  const size_t mcb = sizeof(float) * (size_t)plan.M * plan.M;
+  for (int a = 0; a < 3; ++a) {
+    for (const void* x : io_in)
+      if (mhla::overlaps(io_out[a], io, x, io)) return MHLA_ERR_INVALID_ARG;
+    if (mhla::overlaps(io_out[a], io, mc, mcb) || mhla::overlaps(io_out[a], io, dmc, mcb)) return MHLA_ERR_INVALID_ARG;
+    for (int b = a + 1; b < 3; ++b)
+      if (mhla::overlaps(io_out[a], io, io_out[b], io)) return MHLA_ERR_INVALID_ARG;
+  }
+  for (const void* x : io_in)
+    if (mhla::overlaps(dmc, mcb, x, io)) return MHLA_ERR_INVALID_ARG;
+  if (mhla::overlaps(dmc, mcb, mc, mcb)) return MHLA_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  bool owned = false;
+  if (!workspace) {
+    if (workspace_bytes != 0) return MHLA_ERR_INVALID_ARG;
+    cudaError_t e = cudaMallocAsync(&workspace, lay.total, s);
+    if (e != cudaSuccess) return mhla::cuda_fail(e);
+    owned = true;
+  } else {
+    if (workspace_bytes < lay.total) return MHLA_ERR_WORKSPACE;
+    if (mhla::misaligned(workspace, 256)) return MHLA_ERR_INVALID_ARG;
+  }
+  char* ws = static_cast<char*>(workspace);
+  mhla::BwdBuffers w;
+  w.mc = mc;
+  w.stack = reinterpret_cast<float*>(ws + lay.stack);
+  w.mixed = reinterpret_cast<float*>(ws + lay.mixed);
+  w.rowsum = reinterpret_cast<float*>(ws + lay.rowsum);
+  w.dmixp = reinterpret_cast<float*>(ws + lay.dmixp);
+  w.dnp = reinterpret_cast<float*>(ws + lay.dnp);
+  w.dstack = reinterpret_cast<float*>(ws + lay.dstack);
+  w.dmc = dmc;
+  int e;
+  if ((e = mhla::launch_mc_rowsum(plan, mc, w.rowsum, s)) != 0) st = mhla::cuda_fail((cudaError_t)e);
+  else if ((e = mhla::launch_simt_summary(plan, k, v, w.stack, s)) != 0) st = mhla::cuda_fail((cudaError_t)e);
+  else if ((e = mhla::launch_simt_mix(plan, mc, w.stack, w.mixed, s)) != 0) st = mhla::cuda_fail((cudaError_t)e);
+  else if ((e = mhla::launch_backward(plan, w, q, k, v, dout, dq, dk, dv, s)) != 0)
+    st = mhla::cuda_fail((cudaError_t)e);
+  if (owned) {
+    cudaError_t fe = cudaFreeAsync(workspace, s);
+    if (st == MHLA_OK && fe != cudaSuccess) st = mhla::cuda_fail(fe);
+  }
+  return st;
+}
+
 
 mhla_status mhla_plan(const mhla_params* p, mhla_plan_info* info) {
   Plan plan;

@@ -206,6 +206,25 @@ def all_device_inputs(w: Workload):
     return [x.reshape(shape) for x in dev]
 
 
+def output_grad(w: Workload):
+    """Seeded upstream gradient dO [B, H, N, d] for the backward pass (standard
+    normal values, rounded to bf16 for bf16 workloads).
+
+    Returns ``(values, device_array)`` like ``all_inputs``.
+    """
+    U, N, d = w.units, w.n_tokens, w.head_dim
+    vals = np.empty((U, N, d), np.float32)
+    dev = np.empty((U, N, d), np.uint16 if w.dtype == "bf16" else np.float32)
+    for u in range(U):
+        x = np.random.default_rng([w.seed, 1, u]).standard_normal((N, d), dtype=np.float32)
+        if w.dtype == "bf16":
+            dev[u], vals[u] = round_to_bf16(x)
+        else:
+            dev[u] = vals[u] = x
+    shape = (w.batch, w.heads, N, d)
+    return vals.reshape(shape), dev.reshape(shape)
+
+
 def random_small(seed: int, grid, block, d: int, batch: int = 1, heads: int = 1,
                  dtype: str = "f32", scale: float = 1.0, mc: str = "euclid_noise") -> Workload:
     """A small ad-hoc workload for edge-case tests."""
