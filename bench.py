@@ -2,7 +2,7 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
                     [--variant auto|simt|multipass|fused] [--impl mine|reference]
-                    [--all-workloads] [--no-cpu-baseline]
+                    [--all-workloads] [--no-cpu-baseline] [--pass forward|backward]
 
 A step is one full forward (block summaries, mixing, output) over one batch
 of the workload's seeded synthetic inputs, already resident in HBM.  The
@@ -12,6 +12,10 @@ M=512): its 403 MB of inputs exceed the 126 MB L2, so no flush runs between
 timed steps.  With --all-workloads the other workloads are timed too (with an
 L2 flush between steps, outside the per-step events) and listed under
 "workloads".
+
+--pass backward times mhla_backward instead (one step = dQ, dK, dV and dMc of
+the same workload for a seeded dO, the forward summaries recomputed inside);
+its line has the same keys, with the backward's own roofline.
 
 --impl reference times the float64 CPU oracle (the only reference there is)
 on the same workload: each step is one (batch, head) unit.
@@ -398,6 +402,195 @@ def run_e2e(w: wl.Workload, state, steps: int):
             "steps": steps, "ms_per_step": (t1 - t0) * 1e3 / steps}
 
 
+# ------------------------------------------------------------ backward
+
+BWD_METRIC = "MHLA bwd tokens*heads/sec (dQ, dK, dV, dMc; d=64) and % of GB300 HBM/tensor roofline"
+BWD_PHASES = ["recompute", "output", "mix", "mc", "summary"]
+# phase -> (kernel name in ncu, source, engine that bounds it when not HBM)
+BWD_PHASE_KERNEL = {
+    "recompute": ("simt_summary_kernel", "token_level_head_phi_gb300/csrc/simt.cu", "alu"),
+    "output": ("bwd_output_kernel", "token_level_head_phi_gb300/csrc/backward.cu", "alu"),
+    "mix": ("bwd_mix_kernel", "token_level_head_phi_gb300/csrc/backward.cu", "alu"),
+    "mc": ("bwd_mc_kernel", "token_level_head_phi_gb300/csrc/backward.cu", "alu"),
+    "summary": ("bwd_summary_kernel", "token_level_head_phi_gb300/csrc/backward.cu", "alu"),
+}
+FP32_LANES_PER_SM = 128  # FP32 FMA lanes per SM (4 partitions x 32)
+SM_COUNT = 152
+
+
+def bwd_phase_cost(w: wl.Workload, splits: int):
+    """Compulsory bytes and dense FLOPs of each backward phase (float32
+    intermediates: 4 bytes per summary entry)."""
+    el = 2 if w.dtype == "bf16" else 4
+    U, N, d, M = w.units, w.n_tokens, w.head_dim, w.n_blocks
+    R = d * d + 2 * d
+    Q = M * splits
+    io = U * N * d * el
+    stack, mixed, mc = U * Q * R * 4, U * M * R * 4, 4 * M * M
+    nd2, m2 = U * N * d * d, U * M * M * d * d
+    return {
+        "recompute": (2 * io + 2 * stack + mixed + mc, 2 * nd2 + 2 * U * M * Q * R),
+        "output": (2 * io + mixed + io + stack, 6 * nd2),
+        "mix": (stack + mixed + mc, 2 * U * M * Q * R),
+        "mc": (2 * stack + mc, 2 * U * Q * Q * R),
+        "summary": (2 * io + mixed + 2 * io, 4 * nd2),
+    }
+
+
+def run_backward(args, w: wl.Workload, world: int, rank: int, local: int, dist):
+    """One step = one mhla_backward over the workload (the forward summaries
+    and mixing recomputed inside it), inputs and dO resident in HBM."""
+    import torch
+    import token_level_head_phi_gb300.binding as mb
+    from token_level_head_phi_gb300 import build as mbuild
+
+    if rank == 0 or world == 1:
+        mbuild.build()
+    if dist is not None:
+        dist.barrier()
+    mb.load()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    qn, kn, vn = wl.all_device_inputs(w)
+    _, gn = wl.output_grad(w)
+
+    def to_dev(a):
+        t = torch.from_numpy(np.ascontiguousarray(a))
+        if w.dtype == "bf16":
+            t = t.view(torch.bfloat16)
+        return t.to(dev)
+
+    q, k, v, g = to_dev(qn), to_dev(kn), to_dev(vn), to_dev(gn)
+    del qn, kn, vn, gn
+    mc = torch.from_numpy(wl.make_mc(w)).to(dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    dmc = torch.empty_like(mc)
+    p = mb.make_params(w.batch, w.heads, w.head_dim, w.grid, w.block, w.dtype, "elu1", w.norm)
+    splits = mb.mhla_plan(mb.make_params(w.batch, w.heads, w.head_dim, w.grid, w.block, w.dtype, "elu1", w.norm,
+                                         "simt")).summary_splits
+    need = mb.mhla_backward_workspace_bytes(p)
+    ws = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    handle = stream.cuda_stream
+    io_bytes = q.numel() * q.element_size()
+    flush = None
+    if io_bytes * 4 < 2 * L2_BYTES:
+        flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+
+    def step():
+        st = mb.mhla_backward_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), mc.data_ptr(), g.data_ptr(), p,
+                                  dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), dmc.data_ptr(), ws.data_ptr(), need,
+                                  handle)
+        if st != 0:
+            raise mb.MhlaError(st, "mhla_backward")
+
+    for _ in range(args.warmup):
+        if flush is not None:
+            flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    K = args.steps
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    sampler = ClockSampler(local) if rank == 0 else None
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+    t0 = time.time()
+    start.record(stream)
+    for i in range(K):
+        if flush is not None:
+            flush.zero_()
+            step_ev[i][0].record(stream)
+        step()
+        if flush is not None:
+            step_ev[i][1].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    if dist is not None:
+        dist.barrier()
+    clocks = sampler.stop(t0, t1) if sampler else None
+    total_ms = start.elapsed_time(end) if flush is None else sum(a.elapsed_time(b) for a, b in step_ev)
+
+    KP = max(3, min(K, 20))
+    ev_sets = [[torch.cuda.Event(enable_timing=True) for _ in range(mb.NUM_BWD_PHASE_EVENTS)] for _ in range(KP)]
+    for i in range(KP):
+        if flush is not None:
+            flush.zero_()
+        mb.mhla_set_backward_phase_events(ev_sets[i])
+        step()
+    mb.mhla_set_backward_phase_events(None)
+    torch.cuda.synchronize()
+    avg_phase = {ph: statistics.mean(evs[j].elapsed_time(evs[j + 1]) for evs in ev_sets)
+                 for j, ph in enumerate(BWD_PHASES)}
+    max_ms, value = job_throughput(total_ms, K, w.units * w.n_tokens, world, dist, dev)
+    ms_per_step = max_ms / K
+
+    hbm, tf_burst, tf_sust, peak_kind = load_peaks()
+    cost = bwd_phase_cost(w, splits)
+    dom = max(avg_phase, key=avg_phase.get)
+    kname, ksrc, engine = BWD_PHASE_KERNEL[dom]
+    nbytes, nflops = cost[dom]
+    sec = avg_phase[dom] / 1e3
+    sm_mhz = (clocks or {}).get("sm_max_mhz") or 2070.0
+    alu_peak = SM_COUNT * FP32_LANES_PER_SM * 2 * sm_mhz * 1e6 / 1e12  # TFLOP/s
+    peak_flops = alu_peak if engine == "alu" else tf_sust
+    if nbytes / (hbm * 1e9) >= nflops / (peak_flops * 1e12):
+        roof = {"bound": "hbm", "achieved": nbytes / sec / 1e9, "peak": hbm, "unit": "GB/s",
+                "peak_source": peak_kind}
+    else:
+        roof = {"bound": engine, "achieved": nflops / sec / 1e12, "peak": peak_flops, "unit": "TFLOP/s",
+                "peak_source": ("fp32 FMA lanes x 2 x max SM clock: %d x %d x 2 x %.0f MHz"
+                                % (SM_COUNT, FP32_LANES_PER_SM, sm_mhz)) if engine == "alu" else peak_kind}
+    roof.update({"frac": roof["achieved"] / roof["peak"], "kernel": kname, "phase": dom, "traffic": None,
+                 "algorithmic_bytes_per_launch": nbytes, "flops_per_launch": nflops, "avg_launch_ms": avg_phase[dom]})
+    rb, rf = wl.backward_roofline_bytes(w), wl.backward_roofline_flops(w)
+    t_hbm, t_tc = rb / (hbm * 1e9), rf / (tf_sust * 1e12)
+
+    # end to end: pinned host Q, K, V, dO, Mc in, dQ, dK, dV, dMc out, every step
+    hin = [t.cpu().pin_memory() for t in (q, k, v, g, mc)]
+    hout = [torch.empty_like(t, device="cpu").pin_memory() for t in (dq, dk, dv, dmc)]
+    dins, douts = (q, k, v, g, mc), (dq, dk, dv, dmc)
+
+    def e2e_step():
+        for d_, h_ in zip(dins, hin):
+            d_.copy_(h_, non_blocking=True)
+        step()
+        for h_, d_ in zip(hout, douts):
+            h_.copy_(d_, non_blocking=True)
+        torch.cuda.current_stream(dev).synchronize()
+
+    e2e_step()
+    E = max(3, min(args.e2e_steps, 10))
+    te0 = time.perf_counter()
+    for _ in range(E):
+        e2e_step()
+    te1 = time.perf_counter()
+    h2d = sum(t.numel() * t.element_size() for t in hin)
+    d2h = sum(t.numel() * t.element_size() for t in hout)
+
+    return {
+        "metric": BWD_METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic (seeded normals, locality-biased Mc, seeded normal dO)",
+        "config": dict(wl.describe(w), pass_="backward", input_dtype=w.dtype,
+                       l2="no flush: inputs exceed L2" if flush is None else "L2 flushed (256 MB write) between steps, outside per-step events",
+                       parallelism=f"replicas{world}" if world > 1 else "single GPU"),
+        "roofline": roof,
+        "path_roofline": {"bytes": rb, "flops": rf, "t_hbm_us": t_hbm * 1e6, "t_tc_us": t_tc * 1e6,
+                          "bound": "hbm" if t_hbm >= t_tc else "tensor",
+                          "frac": max(t_hbm, t_tc) / (ms_per_step / 1e3)},
+        "phase_ms": avg_phase,
+        "gpu_launches": 7 * K,
+        "clocks": clocks,
+        "e2e": {"value": w.units * w.n_tokens * E / (te1 - te0), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": E, "ms_per_step": (te1 - te0) * 1e3 / E},
+    }
+
+
 # ------------------------------------------------------ oracle baseline
 
 ORACLE_SNIPPET = r"""
@@ -405,17 +598,22 @@ import json, sys, time
 sys.path.insert(0, {root!r})
 from token_level_head_phi_gb300 import workloads as wl
 from oracle import mhla_oracle as orc
+from oracle import mhla_backward_oracle as orb
 w = wl.WORKLOADS[{name!r}]
 mc = wl.make_mc(w)
-budget, max_units, per_step = {budget}, {max_units}, {per_step}
+budget, max_units, per_step, backward = {budget}, {max_units}, {per_step}, {backward}
 times = []
 units = 0
 t_all = time.perf_counter()
 for step in range(max_units):
     u = step % w.units
     q, k, v = wl.head_inputs(w, u)
+    g = wl.head_output_grad(w, u) if backward else None
     t0 = time.perf_counter()
-    orc.mhla_head64(q, k, v, mc, w.grid, w.block, orc.ELU1, w.norm)
+    if backward:
+        orb.mhla_head_backward64(q, k, v, mc, w.grid, w.block, g, orc.ELU1, w.norm)
+    else:
+        orc.mhla_head64(q, k, v, mc, w.grid, w.block, orc.ELU1, w.norm)
     times.append(time.perf_counter() - t0)
     units += 1
     if not per_step and sum(times) >= budget:
@@ -424,13 +622,14 @@ print(json.dumps({{"times": times, "units": units}}))
 """
 
 
-def oracle_run(w: wl.Workload, budget_s: float, max_units: int, per_step: bool):
+def oracle_run(w: wl.Workload, budget_s: float, max_units: int, per_step: bool, backward: bool = False):
     """Runs the oracle in a fresh process (BLAS threads = available cores)."""
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
     env = dict(os.environ)
     for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
         env[var] = str(cores)
-    code = ORACLE_SNIPPET.format(root=ROOT, name=w.name, budget=budget_s, max_units=max_units, per_step=per_step)
+    code = ORACLE_SNIPPET.format(root=ROOT, name=w.name, budget=budget_s, max_units=max_units, per_step=per_step,
+                               backward=backward)
     res = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=1800)
     if res.returncode != 0:
         raise RuntimeError(f"oracle run failed: {res.stderr[-2000:]}")
@@ -438,23 +637,25 @@ def oracle_run(w: wl.Workload, budget_s: float, max_units: int, per_step: bool):
     return d["times"], d["units"], cores
 
 
-def cpu_baseline(w: wl.Workload, budget_s: float = 15.0):
-    times, units, cores = oracle_run(w, budget_s, max_units=10 ** 6, per_step=False)
+def cpu_baseline(w: wl.Workload, budget_s: float = 15.0, backward: bool = False):
+    times, units, cores = oracle_run(w, budget_s, max_units=10 ** 6, per_step=False, backward=backward)
     total = sum(times)
+    what = "backward" if backward else "forward"
     return {"value": units * w.n_tokens / total, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"{units} of {w.units} (batch, head) units of {w.name}, float64 NumPy oracle, "
+            "sample": f"{units} of {w.units} (batch, head) units of {w.name}, float64 NumPy {what} oracle, "
                       f"{total:.1f} s of CPU time; input generation excluded"}
 
 
 def run_reference(args, w: wl.Workload):
     """--impl reference: the float64 oracle, each step one (batch, head) unit."""
     K, W = args.steps, args.warmup
-    times, units, cores = oracle_run(w, 0.0, max_units=W + K, per_step=True)
+    backward = getattr(args, "pass_", "forward") == "backward"
+    times, units, cores = oracle_run(w, 0.0, max_units=W + K, per_step=True, backward=backward)
     timed = times[W:W + K]
     total = sum(timed)
     value = K * w.n_tokens / total
     return {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": K,
+        "impl": "reference", "metric": BWD_METRIC if backward else METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": K,
         "warmup": W, "ms_per_step": total * 1e3 / K, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded normals, locality-biased Mc)",
         "config": dict(wl.describe(w), parallelism="host cores"),
@@ -476,6 +677,7 @@ def main():
     ap.add_argument("--all-workloads", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--pass", dest="pass_", default="forward", choices=["forward", "backward"])
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -493,6 +695,16 @@ def main():
         dist_mod.init_process_group("nccl")
         dist = dist_mod
     import torch
+    if args.pass_ == "backward":
+        result = run_backward(args, w, world, rank, local, dist)
+        if rank == 0 and not args.no_cpu_baseline:
+            result["cpu_baseline"] = cpu_baseline(w, backward=True)
+        if rank == 0:
+            print(json.dumps(result), flush=True)
+        if dist is not None:
+            dist.barrier()
+            dist.destroy_process_group()
+        return
     result, state = run_mine(args, w, world, rank, local, dist)
     result["e2e"] = run_e2e(w, state, args.e2e_steps)
     del state

@@ -223,6 +223,13 @@ mhla_status mhla_device_status(int* code, int* detail);
 #define MHLA_NUM_PHASE_EVENTS 4
 mhla_status mhla_set_phase_events(void* const* events, int n);
 
+/* The same hook for mhla_backward: events[0] before its first kernel, then
+ * after each phase (1: forward summaries and mixing recomputed, 2: output
+ * step gradients dq, dS~, dz~, 3: gradient mixing dS, dz, 4: dMc, 5: dk, dv).
+ * Independent of mhla_set_phase_events; same ownership and rules. */
+#define MHLA_NUM_BWD_PHASE_EVENTS 6
+mhla_status mhla_set_backward_phase_events(void* const* events, int n);
+
 /* Testing hooks for the FUSED variant's waits on other CTA groups (the pages
  * have no counterpart; a wait that cannot end must be testable without
  * hanging the GPU).

@@ -161,6 +161,10 @@ def test_phase_event_hook_checks(lib):
     assert lib.mhla_set_phase_events(arr, 3) == mb.MHLA_ERR_INVALID_ARG
     arr = (ctypes.c_void_p * 4)(1, 2, None, 3)
     assert lib.mhla_set_phase_events(arr, 4) == mb.MHLA_ERR_INVALID_ARG
+    assert lib.mhla_set_backward_phase_events(None, 0) == mb.MHLA_OK
+    assert lib.mhla_set_backward_phase_events(None, mb.NUM_BWD_PHASE_EVENTS) == mb.MHLA_ERR_INVALID_ARG
+    arr = (ctypes.c_void_p * 4)(1, 2, 3, 4)
+    assert lib.mhla_set_backward_phase_events(arr, 4) == mb.MHLA_ERR_INVALID_ARG
 
 
 def test_long_blocks_are_split(lib):

@@ -37,6 +37,7 @@ VARIANT_SIMT = 1
 VARIANT_MULTIPASS = 2
 VARIANT_FUSED = 3
 NUM_PHASE_EVENTS = 4
+NUM_BWD_PHASE_EVENTS = 6
 
 NORMS = {"divisive": NORM_DIVISIVE, "mala": NORM_MALA, "none": NORM_NONE}
 FEATURE_MAPS = {"elu1": FEATURE_ELU1, "identity": FEATURE_IDENTITY}
@@ -91,6 +92,7 @@ SIGNATURES = [
     ("mhla_last_error_string", ctypes.c_char_p, []),
     ("mhla_abi_version", ctypes.c_int, []),
     ("mhla_set_debug", ctypes.c_int, [ctypes.c_int, ctypes.c_longlong]),
+    ("mhla_set_backward_phase_events", ctypes.c_int, [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int]),
     ("mhla_backward_workspace_bytes", ctypes.c_int, [ctypes.POINTER(MhlaParams), ctypes.POINTER(ctypes.c_size_t)]),
     ("mhla_backward", ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.POINTER(MhlaParams)] + [ctypes.c_void_p] * 5
      + [ctypes.c_size_t, ctypes.c_void_p]),
@@ -322,6 +324,25 @@ def mhla_set_phase_events(events) -> None:
             e.record()
     arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
     _check(load().mhla_set_phase_events(arr, len(events)), "mhla_set_phase_events")
+
+
+def mhla_set_backward_phase_events(events) -> None:
+    """The same hook for mhla_backward (NUM_BWD_PHASE_EVENTS events, or None)."""
+    if events is None:
+        _check(load().mhla_set_backward_phase_events(None, 0), "mhla_set_backward_phase_events")
+        return
+    for e in events:
+        if not e.cuda_event:
+            e.record()
+    arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+    _check(load().mhla_set_backward_phase_events(arr, len(events)), "mhla_set_backward_phase_events")
+
+
+def mhla_backward_raw(q_ptr: int, k_ptr: int, v_ptr: int, mc_ptr: int, dout_ptr: int, p: MhlaParams, dq_ptr: int,
+                      dk_ptr: int, dv_ptr: int, dmc_ptr: int, ws_ptr: int, ws_bytes: int, stream_handle: int) -> int:
+    """Direct call with raw device pointers; returns the status code."""
+    return load().mhla_backward(q_ptr, k_ptr, v_ptr, mc_ptr, dout_ptr, ctypes.byref(p), dq_ptr, dk_ptr, dv_ptr,
+                                dmc_ptr, ws_ptr, ws_bytes, stream_handle)
 
 
 def mhla_status_string(status: int) -> str:

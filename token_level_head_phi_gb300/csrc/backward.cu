@@ -337,7 +337,7 @@ bwd_summary_kernel(Plan p, const T* __restrict__ K, const T* __restrict__ V, con
 
 template <int D, typename T>
 int run_d(const Plan& p, const BwdBuffers& w, const void* q, const void* k, const void* v, const void* dout,
-          void* dq, void* dk, void* dv, cudaStream_t s) {
+          void* dq, void* dk, void* dv, cudaStream_t s, PhaseMark mark) {
   const size_t smo = sizeof(float) * (D * D + 2 * D + 3 * kTile * D + 4 * kTile);
   auto ko = bwd_output_kernel<D, T>;
   cudaError_t e = cudaFuncSetAttribute(ko, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smo);
@@ -345,26 +345,31 @@ int run_d(const Plan& p, const BwdBuffers& w, const void* q, const void* k, cons
   ko<<<dim3(p.M * p.splits, p.BH), kThreads, smo, s>>>(p, (const T*)q, (const T*)dout, w.mixed, w.rowsum, (T*)dq,
                                                        w.dmixp, w.dnp);
   if ((e = cudaGetLastError()) != cudaSuccess) return (int)e;
+  if (mark) mark(2, s);
   bwd_mix_kernel<<<dim3((p.R + 127) / 128, (p.M + 31) / 32, p.BH), kThreads, 0, s>>>(p, w.mc, w.dmixp, w.dstack);
   if ((e = cudaGetLastError()) != cudaSuccess) return (int)e;
+  if (mark) mark(3, s);
   bwd_mc_kernel<<<dim3((p.M + 15) / 16, (p.M + 15) / 16), kThreads, 0, s>>>(p, w.dmixp, w.stack, w.dnp, w.dmc);
   if ((e = cudaGetLastError()) != cudaSuccess) return (int)e;
+  if (mark) mark(4, s);
   const size_t sms = sizeof(float) * (D * D + 2 * D + 2 * kTile * D);
   auto ks = bwd_summary_kernel<D, T>;
   if ((e = cudaFuncSetAttribute(ks, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sms)) != cudaSuccess)
     return (int)e;
   ks<<<dim3(p.M * p.splits, p.BH), kThreads, sms, s>>>(p, (const T*)k, (const T*)v, w.dstack, (T*)dk, (T*)dv);
-  return (int)cudaGetLastError();
+  if ((e = cudaGetLastError()) != cudaSuccess) return (int)e;
+  if (mark) mark(5, s);
+  return 0;
 }
 
 template <typename T>
 int run_t(const Plan& p, const BwdBuffers& w, const void* q, const void* k, const void* v, const void* dout,
-          void* dq, void* dk, void* dv, cudaStream_t s) {
+          void* dq, void* dk, void* dv, cudaStream_t s, PhaseMark mark) {
   switch (p.d) {
-    case 16: return run_d<16, T>(p, w, q, k, v, dout, dq, dk, dv, s);
-    case 32: return run_d<32, T>(p, w, q, k, v, dout, dq, dk, dv, s);
-    case 64: return run_d<64, T>(p, w, q, k, v, dout, dq, dk, dv, s);
-    case 128: return run_d<128, T>(p, w, q, k, v, dout, dq, dk, dv, s);
+    case 16: return run_d<16, T>(p, w, q, k, v, dout, dq, dk, dv, s, mark);
+    case 32: return run_d<32, T>(p, w, q, k, v, dout, dq, dk, dv, s, mark);
+    case 64: return run_d<64, T>(p, w, q, k, v, dout, dq, dk, dv, s, mark);
+    case 128: return run_d<128, T>(p, w, q, k, v, dout, dq, dk, dv, s, mark);
   }
   return (int)cudaErrorInvalidValue;
 }
@@ -372,10 +377,10 @@ int run_t(const Plan& p, const BwdBuffers& w, const void* q, const void* k, cons
 }  // namespace
 
 int launch_backward(const Plan& p, const BwdBuffers& w, const void* q, const void* k, const void* v,
-                    const void* dout, void* dq, void* dk, void* dv, void* stream) {
+                    const void* dout, void* dq, void* dk, void* dv, void* stream, PhaseMark mark) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (p.dtype == MHLA_DTYPE_F32) return run_t<float>(p, w, q, k, v, dout, dq, dk, dv, s);
-  return run_t<__nv_bfloat16>(p, w, q, k, v, dout, dq, dk, dv, s);
+  if (p.dtype == MHLA_DTYPE_F32) return run_t<float>(p, w, q, k, v, dout, dq, dk, dv, s, mark);
+  return run_t<__nv_bfloat16>(p, w, q, k, v, dout, dq, dk, dv, s, mark);
 }
 
 }  // namespace mhla

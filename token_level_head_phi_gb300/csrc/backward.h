@@ -17,8 +17,12 @@ struct BwdBuffers {
   float* dmc;          // [M][M] output
 };
 
+// Called after each backward phase with its index (2: output step, 3:
+// gradient mixing, 4: dMc, 5: dk and dv) and the stream.
+using PhaseMark = void (*)(int phase, void* stream);
+
 // dq, dk, dv (q's dtype) and w.dmc from the recomputed forward in w.
 int launch_backward(const Plan& p, const BwdBuffers& w, const void* q, const void* k, const void* v,
-                    const void* dout, void* dq, void* dk, void* dv, void* stream);
+                    const void* dout, void* dq, void* dk, void* dv, void* stream, PhaseMark mark);
 
 }  // namespace mhla

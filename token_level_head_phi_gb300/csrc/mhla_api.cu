@@ -29,6 +29,8 @@ thread_local std::string g_last_error;
 std::mutex g_events_mu;
 cudaEvent_t g_events[MHLA_NUM_PHASE_EVENTS];
 int g_num_events = 0;
+cudaEvent_t g_bwd_events[MHLA_NUM_BWD_PHASE_EVENTS];
+int g_num_bwd_events = 0;
 
 // Device error word: [0] status code, [1] location detail.  Kernels with
 // bounded waits write it when a wait expires.
@@ -228,6 +230,12 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 void record_event(int idx, cudaStream_t s) {
   std::lock_guard<std::mutex> lock(g_events_mu);
   if (g_num_events == MHLA_NUM_PHASE_EVENTS) cudaEventRecord(g_events[idx], s);
+}
+
+void record_bwd_event(int idx, void* stream) {
+  std::lock_guard<std::mutex> lock(g_events_mu);
+  if (g_num_bwd_events == MHLA_NUM_BWD_PHASE_EVENTS)
+    cudaEventRecord(g_bwd_events[idx], static_cast<cudaStream_t>(stream));
 }
 
 mhla_status run_plan(const Plan& plan, const void* q, const void* k, const void* v, const float* mc,
@@ -441,10 +449,12 @@ mhla_status mhla_backward(const void* q, const void* k, const void* v, const flo
   w.dstack = reinterpret_cast<float*>(ws + lay.dstack);
   w.dmc = dmc;
   int e;
+  mhla::record_bwd_event(0, s);
   if ((e = mhla::launch_mc_rowsum(plan, mc, w.rowsum, s)) != 0) st = mhla::cuda_fail((cudaError_t)e);
   else if ((e = mhla::launch_simt_summary(plan, k, v, w.stack, s)) != 0) st = mhla::cuda_fail((cudaError_t)e);
   else if ((e = mhla::launch_simt_mix(plan, mc, w.stack, w.mixed, s)) != 0) st = mhla::cuda_fail((cudaError_t)e);
-  else if ((e = mhla::launch_backward(plan, w, q, k, v, dout, dq, dk, dv, s)) != 0)
+  else if (mhla::record_bwd_event(1, s),
+           (e = mhla::launch_backward(plan, w, q, k, v, dout, dq, dk, dv, s, mhla::record_bwd_event)) != 0)
     st = mhla::cuda_fail((cudaError_t)e);
   if (owned) {
     cudaError_t fe = cudaFreeAsync(workspace, s);
@@ -661,6 +671,18 @@ mhla_status mhla_set_phase_events(void* const* events, int n) {
   }
   for (int i = 0; i < n; ++i) mhla::g_events[i] = static_cast<cudaEvent_t>(events[i]);
   mhla::g_num_events = n;
+  return MHLA_OK;
+}
+
+mhla_status mhla_set_backward_phase_events(void* const* events, int n) {
+  if (n != 0 && n != MHLA_NUM_BWD_PHASE_EVENTS) return MHLA_ERR_INVALID_ARG;
+  if (n && !events) return MHLA_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(mhla::g_events_mu);
+  for (int i = 0; i < n; ++i) {
+    if (!events[i]) return MHLA_ERR_INVALID_ARG;
+  }
+  for (int i = 0; i < n; ++i) mhla::g_bwd_events[i] = static_cast<cudaEvent_t>(events[i]);
+  mhla::g_num_bwd_events = n;
   return MHLA_OK;
 }
 

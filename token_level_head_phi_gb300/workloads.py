@@ -225,6 +225,12 @@ def output_grad(w: Workload):
     return vals.reshape(shape), dev.reshape(shape)
 
 
+def head_output_grad(w: Workload, unit: int) -> np.ndarray:
+    """dO [N, d] of one unit as the device sees it (the values of output_grad)."""
+    x = np.random.default_rng([w.seed, 1, unit]).standard_normal((w.n_tokens, w.head_dim), dtype=np.float32)
+    return round_to_bf16(x)[1] if w.dtype == "bf16" else x
+
+
 def random_small(seed: int, grid, block, d: int, batch: int = 1, heads: int = 1,
                  dtype: str = "f32", scale: float = 1.0, mc: str = "euclid_noise") -> Workload:
     """A small ad-hoc workload for edge-case tests."""
@@ -241,6 +247,21 @@ def roofline_flops(w: Workload) -> int:
     """Dense FLOPs: 4*N*d^2 (summaries + output) + 2*M^2*d^2 (mixing) per unit."""
     N, d, M = w.n_tokens, w.head_dim, w.n_blocks
     return w.units * (4 * N * d * d + 2 * M * M * d * d)
+
+
+def backward_roofline_bytes(w: Workload) -> int:
+    """Bytes the backward has to move: read Q, K, V, dO and Mc, write dQ, dK,
+    dV and dMc."""
+    el = 2 if w.dtype == "bf16" else 4
+    return 7 * w.units * w.n_tokens * w.head_dim * el + 8 * w.n_blocks ** 2
+
+
+def backward_roofline_flops(w: Workload) -> int:
+    """Dense FLOPs of the backward per unit: the forward summaries and mixing
+    recomputed (2*N*d^2 + 2*M^2*d^2), the output step (phi(q) S~, dq and dS~:
+    6*N*d^2), the gradient mixing and dMc (4*M^2*d^2) and dk, dv (4*N*d^2)."""
+    N, d, M = w.n_tokens, w.head_dim, w.n_blocks
+    return w.units * (12 * N * d * d + 6 * M * M * d * d)
 
 
 def describe(w: Workload) -> dict:
