@@ -192,9 +192,12 @@ mhla_status mhla_forward_host(const void* q, const void* k, const void* v, const
  * mc), with respect to q, k, v and mc -- the chain rule of the forward steps
  * ("MHLA: Restoring Expressivity of Linear Attention via Token-Level
  * Multi-Head": Mc is learned end to end, key design 3; the pages print no
- * gradient).  Every norm and feature map of the forward; float32 arithmetic
- * on the CUDA cores for every head dimension and both dtypes (p->variant is
- * ignored).  The forward summaries are recomputed inside the call.
+ * gradient).  Every norm and feature map of the forward.  p->variant:
+ * MHLA_VARIANT_AUTO takes the tensor cores for bf16 with head_dim 64 (split
+ * bf16 high + low operands, float32 accumulation) and float32 CUDA-core
+ * kernels otherwise; MHLA_VARIANT_SIMT forces the CUDA-core kernels;
+ * MULTIPASS and FUSED ask for the tensor cores (MHLA_ERR_UNSUPPORTED where
+ * they do not apply).  The forward summaries are recomputed inside the call.
  *   dout, dq, dk, dv: [B, H, N, d] in p->dtype, like q; dmc: float32 [M, M],
  *   overwritten with the sum over every (batch, head).
  * Device pointers, 16-byte aligned (mc, dmc 4-byte); dq, dk, dv, dmc must

@@ -36,23 +36,26 @@ def _lib():
     mb.load()
 
 
-def _gpu_backward(w, dev, gdev, mc, norm, fmap):
+def _gpu_backward(w, dev, gdev, mc, norm, fmap, variant="auto"):
     import torch
     q, k, v = upload(w, dev)
     (g,) = upload(w, [gdev])
     mct = torch.from_numpy(np.ascontiguousarray(mc, dtype=np.float32)).cuda()
-    dq, dk, dv, dmc = mb.mhla_backward(q, k, v, mct, g, w.grid, w.block, norm=norm, feature_map=fmap)
+    dq, dk, dv, dmc = mb.mhla_backward(q, k, v, mct, g, w.grid, w.block, norm=norm, feature_map=fmap,
+                                     variant=variant)
     torch.cuda.synchronize()
+    code, detail = mb.mhla_device_status()
+    assert code == 0, f"device status {code} (detail {detail})"
     shape = (w.batch, w.heads, w.n_tokens, w.head_dim)
     return [download(x).reshape(shape) for x in (dq, dk, dv)] + [dmc.cpu().numpy().astype(np.float64)]
 
 
-def backward_parity(w, norm, fmap="elu1", mc=None, inputs=None):
+def backward_parity(w, norm, fmap="elu1", mc=None, inputs=None, variant="auto"):
     """Worst relative error of (dq, dk, dv) and of dMc."""
     vals, dev = inputs if inputs is not None else wl.all_inputs(w)
     gvals, gdev = wl.output_grad(w)
     mc = wl.make_mc(w) if mc is None else mc
-    got = _gpu_backward(w, dev, gdev, mc, norm, fmap)
+    got = _gpu_backward(w, dev, gdev, mc, norm, fmap, variant)
     want = orb.mhla_backward64(vals[0], vals[1], vals[2], np.asarray(mc, np.float64), w.grid, w.block, gvals,
                                fmap, norm)
     for name, x in zip(("dq", "dk", "dv", "dmc"), got):
@@ -62,11 +65,14 @@ def backward_parity(w, norm, fmap="elu1", mc=None, inputs=None):
     return ex, emc
 
 
+@pytest.mark.parametrize("variant", ["auto", "simt"])
 @pytest.mark.parametrize("name,norm", [(n, m) for n in ("tiny_f32", "deit_t") for m in ("divisive", "none", "mala")]
                          + [("image_64x64", "divisive")])
-def test_workload_backward(name, norm):
+def test_workload_backward(name, norm, variant):
     w = wl.WORKLOADS[name]
-    ex, emc = backward_parity(w, norm)
+    if variant == "simt" and w.dtype == "f32":
+        pytest.skip("float32 inputs always take the CUDA-core backward")
+    ex, emc = backward_parity(w, norm, variant=variant)
     assert ex <= TOL_X[w.dtype] and emc <= TOL_MC[w.dtype], f"{name}/{norm}: {ex:.3e} {emc:.3e}"
 
 

@@ -336,51 +336,74 @@ bwd_summary_kernel(Plan p, const T* __restrict__ K, const T* __restrict__ V, con
 }
 
 template <int D, typename T>
-int run_d(const Plan& p, const BwdBuffers& w, const void* q, const void* k, const void* v, const void* dout,
-          void* dq, void* dk, void* dv, cudaStream_t s, PhaseMark mark) {
+int run_output(const Plan& p, const BwdBuffers& w, const void* q, const void* dout, void* dq, cudaStream_t s) {
   const size_t smo = sizeof(float) * (D * D + 2 * D + 3 * kTile * D + 4 * kTile);
   auto ko = bwd_output_kernel<D, T>;
   cudaError_t e = cudaFuncSetAttribute(ko, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smo);
   if (e != cudaSuccess) return (int)e;
   ko<<<dim3(p.M * p.splits, p.BH), kThreads, smo, s>>>(p, (const T*)q, (const T*)dout, w.mixed, w.rowsum, (T*)dq,
                                                        w.dmixp, w.dnp);
-  if ((e = cudaGetLastError()) != cudaSuccess) return (int)e;
-  if (mark) mark(2, s);
-  bwd_mix_kernel<<<dim3((p.R + 127) / 128, (p.M + 31) / 32, p.BH), kThreads, 0, s>>>(p, w.mc, w.dmixp, w.dstack);
-  if ((e = cudaGetLastError()) != cudaSuccess) return (int)e;
-  if (mark) mark(3, s);
-  bwd_mc_kernel<<<dim3((p.M + 15) / 16, (p.M + 15) / 16), kThreads, 0, s>>>(p, w.dmixp, w.stack, w.dnp, w.dmc);
-  if ((e = cudaGetLastError()) != cudaSuccess) return (int)e;
-  if (mark) mark(4, s);
+  return (int)cudaGetLastError();
+}
+
+template <int D, typename T>
+int run_summary(const Plan& p, const BwdBuffers& w, const void* k, const void* v, void* dk, void* dv,
+                cudaStream_t s) {
   const size_t sms = sizeof(float) * (D * D + 2 * D + 2 * kTile * D);
   auto ks = bwd_summary_kernel<D, T>;
-  if ((e = cudaFuncSetAttribute(ks, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sms)) != cudaSuccess)
-    return (int)e;
+  cudaError_t e = cudaFuncSetAttribute(ks, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sms);
+  if (e != cudaSuccess) return (int)e;
   ks<<<dim3(p.M * p.splits, p.BH), kThreads, sms, s>>>(p, (const T*)k, (const T*)v, w.dstack, (T*)dk, (T*)dv);
-  if ((e = cudaGetLastError()) != cudaSuccess) return (int)e;
-  if (mark) mark(5, s);
-  return 0;
+  return (int)cudaGetLastError();
 }
 
 template <typename T>
-int run_t(const Plan& p, const BwdBuffers& w, const void* q, const void* k, const void* v, const void* dout,
-          void* dq, void* dk, void* dv, cudaStream_t s, PhaseMark mark) {
+int output_t(const Plan& p, const BwdBuffers& w, const void* q, const void* dout, void* dq, cudaStream_t s) {
   switch (p.d) {
-    case 16: return run_d<16, T>(p, w, q, k, v, dout, dq, dk, dv, s, mark);
-    case 32: return run_d<32, T>(p, w, q, k, v, dout, dq, dk, dv, s, mark);
-    case 64: return run_d<64, T>(p, w, q, k, v, dout, dq, dk, dv, s, mark);
-    case 128: return run_d<128, T>(p, w, q, k, v, dout, dq, dk, dv, s, mark);
+    case 16: return run_output<16, T>(p, w, q, dout, dq, s);
+    case 32: return run_output<32, T>(p, w, q, dout, dq, s);
+    case 64: return run_output<64, T>(p, w, q, dout, dq, s);
+    case 128: return run_output<128, T>(p, w, q, dout, dq, s);
+  }
+  return (int)cudaErrorInvalidValue;
+}
+
+template <typename T>
+int summary_t(const Plan& p, const BwdBuffers& w, const void* k, const void* v, void* dk, void* dv, cudaStream_t s) {
+  switch (p.d) {
+    case 16: return run_summary<16, T>(p, w, k, v, dk, dv, s);
+    case 32: return run_summary<32, T>(p, w, k, v, dk, dv, s);
+    case 64: return run_summary<64, T>(p, w, k, v, dk, dv, s);
+    case 128: return run_summary<128, T>(p, w, k, v, dk, dv, s);
   }
   return (int)cudaErrorInvalidValue;
 }
 
 }  // namespace
 
-int launch_backward(const Plan& p, const BwdBuffers& w, const void* q, const void* k, const void* v,
-                    const void* dout, void* dq, void* dk, void* dv, void* stream, PhaseMark mark) {
+int launch_bwd_output(const Plan& p, const BwdBuffers& w, const void* q, const void* dout, void* dq, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (p.dtype == MHLA_DTYPE_F32) return run_t<float>(p, w, q, k, v, dout, dq, dk, dv, s, mark);
-  return run_t<__nv_bfloat16>(p, w, q, k, v, dout, dq, dk, dv, s, mark);
+  if (p.dtype == MHLA_DTYPE_F32) return output_t<float>(p, w, q, dout, dq, s);
+  return output_t<__nv_bfloat16>(p, w, q, dout, dq, s);
+}
+
+int launch_bwd_mix(const Plan& p, const BwdBuffers& w, void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  bwd_mix_kernel<<<dim3((p.R + 127) / 128, (p.M + 31) / 32, p.BH), kThreads, 0, s>>>(p, w.mc, w.dmixp, w.dstack);
+  return (int)cudaGetLastError();
+}
+
+int launch_bwd_mc(const Plan& p, const BwdBuffers& w, void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  bwd_mc_kernel<<<dim3((p.M + 15) / 16, (p.M + 15) / 16), kThreads, 0, s>>>(p, w.dmixp, w.stack, w.dnp, w.dmc);
+  return (int)cudaGetLastError();
+}
+
+int launch_bwd_summary(const Plan& p, const BwdBuffers& w, const void* k, const void* v, void* dk, void* dv,
+                       void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (p.dtype == MHLA_DTYPE_F32) return summary_t<float>(p, w, k, v, dk, dv, s);
+  return summary_t<__nv_bfloat16>(p, w, k, v, dk, dv, s);
 }
 
 }  // namespace mhla

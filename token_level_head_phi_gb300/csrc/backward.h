@@ -17,12 +17,16 @@ struct BwdBuffers {
   float* dmc;          // [M][M] output
 };
 
-// Called after each backward phase with its index (2: output step, 3:
-// gradient mixing, 4: dMc, 5: dk and dv) and the stream.
-using PhaseMark = void (*)(int phase, void* stream);
-
-// dq, dk, dv (q's dtype) and w.dmc from the recomputed forward in w.
-int launch_backward(const Plan& p, const BwdBuffers& w, const void* q, const void* k, const void* v,
-                    const void* dout, void* dq, void* dk, void* dv, void* stream, PhaseMark mark);
+// The four steps of the float32 backward after the forward summaries and
+// mixing (w.stack, w.mixed, w.rowsum) are in place, in this order:
+//   output:  dq and per query piece the partial dS~, dz~, dv~ (w.dmixp), dn~ (w.dnp)
+//   mix:     w.dstack = dS_b, dz_b, dv_b (Mc transposed times the partials)
+//   mc:      w.dmc (summed over heads)
+//   summary: dk, dv
+int launch_bwd_output(const Plan& p, const BwdBuffers& w, const void* q, const void* dout, void* dq, void* stream);
+int launch_bwd_mix(const Plan& p, const BwdBuffers& w, void* stream);
+int launch_bwd_mc(const Plan& p, const BwdBuffers& w, void* stream);
+int launch_bwd_summary(const Plan& p, const BwdBuffers& w, const void* k, const void* v, void* dk, void* dv,
+                       void* stream);
 
 }  // namespace mhla

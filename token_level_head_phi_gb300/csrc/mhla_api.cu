@@ -12,6 +12,7 @@
 #include "mhla.h"
 #include "plan.h"
 #include "backward.h"
+#include "tc_bwd.h"
 #include "tc_host.h"
 
 namespace mhla {
@@ -354,33 +355,136 @@ std::mutex g_pipe_mu[kMaxDevices];
 
 namespace mhla {
 
-// Backward plan (float32 CUDA-core kernels) and its workspace layout.
+// Backward plan and its workspace layout.  The tensor-core backward (bf16,
+// d = 64) recomputes the forward records with the forward kernels in split
+// precision (bf16 high + low planes for every part) and keeps its gradient
+// records as planes too; the float32 CUDA-core backward keeps float32
+// records.
 struct BwdLayout {
-  size_t stack, mixed, rowsum, dmixp, dnp, dstack, total;
+  bool tc;
+  size_t stack, mixed, rowsum, dmixp, dnp, dstack;   // float32 records
+  size_t stack_hi, stack_lo, mixed_hi, mixed_lo;     // planes (tensor cores)
+  size_t dmixp_hi, dmixp_lo;
+  size_t mc_f16, mc_hi, mc_lo, mc_scale, blkinfo, partial;
+  size_t total;
 };
 
 mhla_status make_bwd_plan(const mhla_params* prm, Plan* plan, BwdLayout* lay) {
   if (!prm) return MHLA_ERR_INVALID_ARG;
   mhla_params p = *prm;
-  p.variant = MHLA_VARIANT_SIMT;
+  const bool tc_ok = p.dtype == MHLA_DTYPE_BF16 && p.head_dim == kTcHeadDim;
+  if (p.variant == MHLA_VARIANT_AUTO) p.variant = tc_ok ? MHLA_VARIANT_MULTIPASS : MHLA_VARIANT_SIMT;
+  if (p.variant == MHLA_VARIANT_FUSED) p.variant = MHLA_VARIANT_MULTIPASS;
   mhla_status st = make_plan(&p, plan);
   if (st != MHLA_OK) return st;
+  memset(lay, 0, sizeof(*lay));
+  lay->tc = plan->variant == MHLA_VARIANT_MULTIPASS;
   const size_t rows = (size_t)plan->BH * plan->M * plan->splits;
+  const size_t mrows = (size_t)plan->BH * plan->M;
+  const size_t R = (size_t)plan->R;
   size_t off = 0;
-  lay->stack = off;
-  off = align_up(off + sizeof(float) * rows * plan->R);
-  lay->mixed = off;
-  off = align_up(off + sizeof(float) * (size_t)plan->BH * plan->M * plan->R);
-  lay->rowsum = off;
-  off = align_up(off + sizeof(float) * (size_t)plan->M);
-  lay->dmixp = off;
-  off = align_up(off + sizeof(float) * rows * plan->R);
-  lay->dnp = off;
-  off = align_up(off + sizeof(float) * rows);
-  lay->dstack = off;
-  off = align_up(off + sizeof(float) * (size_t)plan->BH * plan->M * plan->R);
+  auto take = [&](size_t& field, size_t bytes) {
+    field = off;
+    off = align_up(off + bytes);
+  };
+  take(lay->stack, sizeof(float) * rows * R);
+  take(lay->mixed, sizeof(float) * mrows * R);
+  take(lay->rowsum, sizeof(float) * plan->M);
+  take(lay->dmixp, sizeof(float) * rows * R);
+  take(lay->dnp, sizeof(float) * rows);
+  take(lay->dstack, sizeof(float) * mrows * R);
+  if (lay->tc) {
+    take(lay->stack_hi, 2 * rows * R);
+    take(lay->stack_lo, 2 * rows * R);
+    take(lay->mixed_hi, 2 * mrows * R);
+    take(lay->mixed_lo, 2 * mrows * R);
+    take(lay->dmixp_hi, 2 * rows * R);
+    take(lay->dmixp_lo, 2 * rows * R);
+    const size_t mcq = 2 * (size_t)plan->M * plan->Qp;
+    take(lay->mc_f16, mcq);
+    take(lay->mc_hi, mcq);
+    take(lay->mc_lo, mcq);
+    take(lay->mc_scale, sizeof(float) * plan->M);
+    take(lay->blkinfo, 16 * (size_t)plan->M);
+    take(lay->partial, tc_bwd_mc_partial_bytes(*plan));
+  }
   lay->total = plan->BH == 0 ? 0 : off;
   return MHLA_OK;
+}
+
+int run_backward(const Plan& plan, const BwdLayout& lay, const void* q, const void* k, const void* v,
+                 const float* mc, const void* dout, void* dq, void* dk, void* dv, float* dmc, char* ws,
+                 cudaStream_t s) {
+  Plan p = plan;
+  if (device_error_ptr(&p.err) != MHLA_OK) return (int)cudaErrorUnknown;
+  auto F = [&](size_t off) { return reinterpret_cast<float*>(ws + off); };
+  auto H = [&](size_t off) { return reinterpret_cast<__nv_bfloat16*>(ws + off); };
+  BwdBuffers w;
+  w.mc = mc;
+  w.stack = F(lay.stack);
+  w.mixed = F(lay.mixed);
+  w.rowsum = F(lay.rowsum);
+  w.dmixp = F(lay.dmixp);
+  w.dnp = F(lay.dnp);
+  w.dstack = F(lay.dstack);
+  w.dmc = dmc;
+  const size_t rows = (size_t)p.BH * p.M * p.splits, mrows = (size_t)p.BH * p.M;
+  int e;
+  record_bwd_event(0, s);
+  if (lay.tc) {
+    // forward records in split precision: the forward kernels with the MALA
+    // precision settings (bf16 high + low planes for every part)
+    Plan pr = p;
+    pr.norm = MHLA_NORM_MALA;
+    pr.f16_mix = 0;
+    TcBuffers b;
+    b.stack = H(lay.stack_hi);
+    b.stack_lo = H(lay.stack_lo);
+    b.mixed_hi = H(lay.mixed_hi);
+    b.mixed_lo = H(lay.mixed_lo);
+    b.mc_f16 = reinterpret_cast<__half*>(ws + lay.mc_f16);
+    b.mc_scale = F(lay.mc_scale);
+    b.mc_hi = H(lay.mc_hi);
+    b.mc_lo = H(lay.mc_lo);
+    b.rowsum = F(lay.rowsum);
+    b.blkinfo = reinterpret_cast<float4*>(ws + lay.blkinfo);
+    b.Qp = p.Qp;
+    b.f16 = false;
+    b.stack_scale = 1.f;
+    b.slots = p.BH;
+    b.flow = nullptr;
+    if ((e = launch_tc_prep(pr, mc, b, s)) != 0) return e;
+    if ((e = launch_tc_summary(pr, pr.chunk, k, v, b, s)) != 0) return e;
+    if ((e = launch_tc_mix(pr, b, s)) != 0) return e;
+    if ((e = launch_planes_to_f32(H(lay.stack_hi), b.stack_lo, w.stack, rows * p.R, s)) != 0) return e;
+    if ((e = launch_planes_to_f32(b.mixed_hi, b.mixed_lo, w.mixed, mrows * p.R, s)) != 0) return e;
+    record_bwd_event(1, s);
+    if ((e = launch_bwd_output(p, w, q, dout, dq, s)) != 0) return e;
+    record_bwd_event(2, s);
+    if ((e = launch_bwd_mix(p, w, s)) != 0) return e;
+    record_bwd_event(3, s);
+    if ((e = launch_f32_to_planes(w.dmixp, H(lay.dmixp_hi), H(lay.dmixp_lo), rows * p.R, s)) != 0) return e;
+    if ((e = launch_tc_bwd_mc(p, H(lay.dmixp_hi), H(lay.dmixp_lo), H(lay.stack_hi), b.stack_lo, w.dnp, F(lay.partial), dmc,
+                              s)) != 0)
+      return e;
+    record_bwd_event(4, s);
+    if ((e = launch_bwd_summary(p, w, k, v, dk, dv, s)) != 0) return e;
+    record_bwd_event(5, s);
+    return 0;
+  }
+  if ((e = launch_mc_rowsum(p, mc, w.rowsum, s)) != 0) return e;
+  if ((e = launch_simt_summary(p, k, v, w.stack, s)) != 0) return e;
+  if ((e = launch_simt_mix(p, mc, w.stack, w.mixed, s)) != 0) return e;
+  record_bwd_event(1, s);
+  if ((e = launch_bwd_output(p, w, q, dout, dq, s)) != 0) return e;
+  record_bwd_event(2, s);
+  if ((e = launch_bwd_mix(p, w, s)) != 0) return e;
+  record_bwd_event(3, s);
+  if ((e = launch_bwd_mc(p, w, s)) != 0) return e;
+  record_bwd_event(4, s);
+  if ((e = launch_bwd_summary(p, w, k, v, dk, dv, s)) != 0) return e;
+  record_bwd_event(5, s);
+  return 0;
 }
 
 }  // namespace mhla
@@ -439,23 +543,8 @@ mhla_status mhla_backward(const void* q, const void* k, const void* v, const flo
     if (mhla::misaligned(workspace, 256)) return MHLA_ERR_INVALID_ARG;
   }
   char* ws = static_cast<char*>(workspace);
-  mhla::BwdBuffers w;
-  w.mc = mc;
-  w.stack = reinterpret_cast<float*>(ws + lay.stack);
-  w.mixed = reinterpret_cast<float*>(ws + lay.mixed);
-  w.rowsum = reinterpret_cast<float*>(ws + lay.rowsum);
-  w.dmixp = reinterpret_cast<float*>(ws + lay.dmixp);
-  w.dnp = reinterpret_cast<float*>(ws + lay.dnp);
-  w.dstack = reinterpret_cast<float*>(ws + lay.dstack);
-  w.dmc = dmc;
-  int e;
-  mhla::record_bwd_event(0, s);
-  if ((e = mhla::launch_mc_rowsum(plan, mc, w.rowsum, s)) != 0) st = mhla::cuda_fail((cudaError_t)e);
-  else if ((e = mhla::launch_simt_summary(plan, k, v, w.stack, s)) != 0) st = mhla::cuda_fail((cudaError_t)e);
-  else if ((e = mhla::launch_simt_mix(plan, mc, w.stack, w.mixed, s)) != 0) st = mhla::cuda_fail((cudaError_t)e);
-  else if (mhla::record_bwd_event(1, s),
-           (e = mhla::launch_backward(plan, w, q, k, v, dout, dq, dk, dv, s, mhla::record_bwd_event)) != 0)
-    st = mhla::cuda_fail((cudaError_t)e);
+  const int e = mhla::run_backward(plan, lay, q, k, v, mc, dout, dq, dk, dv, dmc, ws, s);
+  if (e != 0) st = mhla::cuda_fail((cudaError_t)e);
   if (owned) {
     cudaError_t fe = cudaFreeAsync(workspace, s);
     if (st == MHLA_OK && fe != cudaSuccess) st = mhla::cuda_fail(fe);

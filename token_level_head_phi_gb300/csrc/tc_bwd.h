@@ -1,0 +1,27 @@
+// Interface between the host dispatcher and the tensor-core backward kernels
+// (head dimension 64, bf16 tensors).  Intermediate records are kept as two
+// bf16 planes, high and low parts of a float32 value (hi = bf16(x),
+// lo = bf16(x - hi)), in the record layout of the forward stack: one row of
+// R = d*d + 2d values per (head, block piece) or (head, block).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "tc_host.h"
+
+namespace mhla {
+
+// dMc from the gradient records dX~ (dx planes, [BH][Q][R]) and the forward
+// records X (x planes, [BH][Q][R]), Q = M * splits piece rows; `partial`
+// holds tc_bwd_mc_partial_bytes(p) bytes; dnp [BH][Q] is read for MALA only.
+size_t tc_bwd_mc_partial_bytes(const Plan& p);
+int launch_tc_bwd_mc(const Plan& p, const __nv_bfloat16* dx_hi, const __nv_bfloat16* dx_lo,
+                     const __nv_bfloat16* x_hi, const __nv_bfloat16* x_lo, const float* dnp, float* partial,
+                     float* dmc, cudaStream_t s);
+
+// Conversions between float32 records and hi/lo planes (n values).
+int launch_planes_to_f32(const __nv_bfloat16* hi, const __nv_bfloat16* lo, float* out, size_t n, cudaStream_t s);
+int launch_f32_to_planes(const float* in, __nv_bfloat16* hi, __nv_bfloat16* lo, size_t n, cudaStream_t s);
+
+}  // namespace mhla
