@@ -366,6 +366,8 @@ struct BwdLayout {
   size_t stack_hi, stack_lo, mixed_hi, mixed_lo;     // planes (tensor cores)
   size_t dmixp_hi, dmixp_lo;
   size_t mc_f16, mc_hi, mc_lo, mc_scale, blkinfo, partial;
+  size_t mct, mct_f16, mct_hi, mct_lo, mct_scale, mct_rowsum, mct_blkinfo;  // Mc transposed
+  size_t dx_hi, dx_lo;                                                      // dS_b, dz_b, dv_b planes
   size_t total;
 };
 
@@ -407,6 +409,15 @@ mhla_status make_bwd_plan(const mhla_params* prm, Plan* plan, BwdLayout* lay) {
     take(lay->mc_scale, sizeof(float) * plan->M);
     take(lay->blkinfo, 16 * (size_t)plan->M);
     take(lay->partial, tc_bwd_mc_partial_bytes(*plan));
+    take(lay->mct, sizeof(float) * (size_t)plan->M * plan->M);
+    take(lay->mct_f16, mcq);
+    take(lay->mct_hi, mcq);
+    take(lay->mct_lo, mcq);
+    take(lay->mct_scale, sizeof(float) * plan->M);
+    take(lay->mct_rowsum, sizeof(float) * plan->M);
+    take(lay->mct_blkinfo, 16 * (size_t)plan->M);
+    take(lay->dx_hi, 2 * mrows * R);
+    take(lay->dx_lo, 2 * mrows * R);
   }
   lay->total = plan->BH == 0 ? 0 : off;
   return MHLA_OK;
@@ -460,15 +471,30 @@ int run_backward(const Plan& plan, const BwdLayout& lay, const void* q, const vo
     if ((e = launch_planes_to_f32(b.mixed_hi, b.mixed_lo, w.mixed, mrows * p.R, s)) != 0) return e;
     record_bwd_event(1, s);
     if ((e = launch_bwd_output(p, w, q, dout, dq, s)) != 0) return e;
-    record_bwd_event(2, s);
-    if ((e = launch_bwd_mix(p, w, s)) != 0) return e;
-    record_bwd_event(3, s);
     if ((e = launch_f32_to_planes(w.dmixp, H(lay.dmixp_hi), H(lay.dmixp_lo), rows * p.R, s)) != 0) return e;
+    record_bwd_event(2, s);
+    // gradient mixing dX_b = sum_q Mc[i(q), b] dX~_q: the forward mixing
+    // kernel with Mc transposed
+    TcBuffers bt = b;
+    bt.stack = H(lay.dmixp_hi);
+    bt.stack_lo = H(lay.dmixp_lo);
+    bt.mixed_hi = H(lay.dx_hi);
+    bt.mixed_lo = H(lay.dx_lo);
+    bt.mc_f16 = reinterpret_cast<__half*>(ws + lay.mct_f16);
+    bt.mc_scale = F(lay.mct_scale);
+    bt.mc_hi = H(lay.mct_hi);
+    bt.mc_lo = H(lay.mct_lo);
+    bt.rowsum = F(lay.mct_rowsum);
+    bt.blkinfo = reinterpret_cast<float4*>(ws + lay.mct_blkinfo);
+    if ((e = launch_transpose_mc(mc, F(lay.mct), p.M, s)) != 0) return e;
+    if ((e = launch_tc_prep(pr, F(lay.mct), bt, s)) != 0) return e;
+    if ((e = launch_tc_mix(pr, bt, s)) != 0) return e;
+    record_bwd_event(3, s);
     if ((e = launch_tc_bwd_mc(p, H(lay.dmixp_hi), H(lay.dmixp_lo), H(lay.stack_hi), b.stack_lo, w.dnp, F(lay.partial), dmc,
                               s)) != 0)
       return e;
     record_bwd_event(4, s);
-    if ((e = launch_bwd_summary(p, w, k, v, dk, dv, s)) != 0) return e;
+    if ((e = launch_tc_bwd_summary(p, k, v, H(lay.dx_hi), H(lay.dx_lo), dk, dv, s)) != 0) return e;
     record_bwd_event(5, s);
     return 0;
   }

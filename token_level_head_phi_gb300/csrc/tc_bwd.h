@@ -20,6 +20,14 @@ int launch_tc_bwd_mc(const Plan& p, const __nv_bfloat16* dx_hi, const __nv_bfloa
                      const __nv_bfloat16* x_hi, const __nv_bfloat16* x_lo, const float* dnp, float* partial,
                      float* dmc, cudaStream_t s);
 
+// dK, dV from the gradient records dX_b = (dS_b, dz_b, dv_b) (dx planes,
+// [BH][M][R]) and the K, V tensors ([B, H, N, 64] bf16).
+int launch_tc_bwd_summary(const Plan& p, const void* k, const void* v, const __nv_bfloat16* dx_hi,
+                          const __nv_bfloat16* dx_lo, void* dk, void* dv, cudaStream_t s);
+
+// out[b][i] = in[i][b] for an M x M float32 matrix.
+int launch_transpose_mc(const float* in, float* out, int M, cudaStream_t s);
+
 // Conversions between float32 records and hi/lo planes (n values).
 int launch_planes_to_f32(const __nv_bfloat16* hi, const __nv_bfloat16* lo, float* out, size_t n, cudaStream_t s);
 int launch_f32_to_planes(const float* in, __nv_bfloat16* hi, __nv_bfloat16* lo, size_t n, cudaStream_t s);

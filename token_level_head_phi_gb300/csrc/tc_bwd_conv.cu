@@ -23,12 +23,29 @@ __global__ void f32_to_planes_kernel(const float* __restrict__ in, __nv_bfloat16
   }
 }
 
+__global__ void transpose_kernel(const float* __restrict__ in, float* __restrict__ out, int M) {
+  __shared__ float t[32][33];
+  const int x = blockIdx.x * 32 + threadIdx.x, y0 = blockIdx.y * 32;
+  for (int j = threadIdx.y; j < 32; j += blockDim.y)
+    if (x < M && y0 + j < M) t[j][threadIdx.x] = in[(size_t)(y0 + j) * M + x];
+  __syncthreads();
+  const int ox = y0 + threadIdx.x, oy0 = blockIdx.x * 32;
+  for (int j = threadIdx.y; j < 32; j += blockDim.y)
+    if (ox < M && oy0 + j < M) out[(size_t)(oy0 + j) * M + ox] = t[threadIdx.x][j];
+}
+
 int grid_for(size_t n) {
   const size_t g = (n + 255) / 256;
   return (int)(g < 4096 ? (g < 1 ? 1 : g) : 4096);
 }
 
 }  // namespace
+
+int launch_transpose_mc(const float* in, float* out, int M, cudaStream_t s) {
+  const dim3 grid((M + 31) / 32, (M + 31) / 32);
+  transpose_kernel<<<grid, dim3(32, 8), 0, s>>>(in, out, M);
+  return (int)cudaGetLastError();
+}
 
 int launch_planes_to_f32(const __nv_bfloat16* hi, const __nv_bfloat16* lo, float* out, size_t n, cudaStream_t s) {
   planes_to_f32_kernel<<<grid_for(n), 256, 0, s>>>(hi, lo, out, n);
