@@ -3,10 +3,13 @@ against the float64 backward oracle.
 
 Measure, per gradient: max|gpu - oracle| / max|oracle| over the whole
 tensor.  Tolerances: dq, dk, dv are rounded to the tensors' dtype, so bf16
-gets the forward's 5e-3; dMc is a float32 sum over every head and token and
-gets 5e-4 (bf16 inputs) and 5e-5 (float32): its DIVISIVE rows are
-differences of nearly equal terms (sum_b Mc[i,b] dMc[i,b] = 0), so float32
-rounding of the O(n_b)-term sums is measured on the largest entry.
+gets the forward's 5e-3.  dMc is a float32 sum over every head and token
+whose terms cancel (sum_b Mc[i,b] dMc[i,b] = 0 under DIVISIVE; with one
+block of 1000 tokens over 4 heads the terms are ~60 times the result).  The
+tensor-core path (bf16 inputs) carries its float32 records as bf16 high +
+low pairs (about 2^-17 relative) and drops the low x low product, so its
+dMc gets 2e-3 (2^-16 times that cancellation, with margin); the float32
+CUDA-core path gets 5e-4 with bf16 inputs and 5e-5 with float32 inputs.
 Float32 dq, dk, dv get 2e-5: their DIVISIVE form is a difference of two
 terms of the size of the output (dq = (S~ dO - z~ (dO . o)) / s).
 """
@@ -26,7 +29,8 @@ from helpers import download, upload
 pytestmark = pytest.mark.gpu
 
 TOL_X = {"bf16": 5e-3, "f32": 2e-5}
-TOL_MC = {"bf16": 5e-4, "f32": 5e-5}
+TOL_MC = {"bf16": 2e-3, "f32": 5e-5}
+TOL_MC_SIMT_BF16 = 5e-4
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -73,7 +77,8 @@ def test_workload_backward(name, norm, variant):
     if variant == "simt" and w.dtype == "f32":
         pytest.skip("float32 inputs always take the CUDA-core backward")
     ex, emc = backward_parity(w, norm, variant=variant)
-    assert ex <= TOL_X[w.dtype] and emc <= TOL_MC[w.dtype], f"{name}/{norm}: {ex:.3e} {emc:.3e}"
+    tol_mc = TOL_MC_SIMT_BF16 if (variant == "simt" and w.dtype == "bf16") else TOL_MC[w.dtype]
+    assert ex <= TOL_X[w.dtype] and emc <= tol_mc, f"{name}/{norm}: {ex:.3e} {emc:.3e}"
 
 
 @pytest.mark.parametrize("name", ["seq_32k_mala", "wan_21x30x50"])

@@ -389,13 +389,14 @@ mhla_status make_bwd_plan(const mhla_params* prm, Plan* plan, BwdLayout* lay) {
     field = off;
     off = align_up(off + bytes);
   };
-  take(lay->stack, sizeof(float) * rows * R);
-  take(lay->mixed, sizeof(float) * mrows * R);
   take(lay->rowsum, sizeof(float) * plan->M);
-  take(lay->dmixp, sizeof(float) * rows * R);
   take(lay->dnp, sizeof(float) * rows);
-  take(lay->dstack, sizeof(float) * mrows * R);
-  if (lay->tc) {
+  if (!lay->tc) {
+    take(lay->stack, sizeof(float) * rows * R);
+    take(lay->mixed, sizeof(float) * mrows * R);
+    take(lay->dmixp, sizeof(float) * rows * R);
+    take(lay->dstack, sizeof(float) * mrows * R);
+  } else {
     take(lay->stack_hi, 2 * rows * R);
     take(lay->stack_lo, 2 * rows * R);
     take(lay->mixed_hi, 2 * mrows * R);
@@ -439,7 +440,6 @@ int run_backward(const Plan& plan, const BwdLayout& lay, const void* q, const vo
   w.dnp = F(lay.dnp);
   w.dstack = F(lay.dstack);
   w.dmc = dmc;
-  const size_t rows = (size_t)p.BH * p.M * p.splits, mrows = (size_t)p.BH * p.M;
   int e;
   record_bwd_event(0, s);
   if (lay.tc) {
@@ -467,11 +467,10 @@ int run_backward(const Plan& plan, const BwdLayout& lay, const void* q, const vo
     if ((e = launch_tc_prep(pr, mc, b, s)) != 0) return e;
     if ((e = launch_tc_summary(pr, pr.chunk, k, v, b, s)) != 0) return e;
     if ((e = launch_tc_mix(pr, b, s)) != 0) return e;
-    if ((e = launch_planes_to_f32(H(lay.stack_hi), b.stack_lo, w.stack, rows * p.R, s)) != 0) return e;
-    if ((e = launch_planes_to_f32(b.mixed_hi, b.mixed_lo, w.mixed, mrows * p.R, s)) != 0) return e;
     record_bwd_event(1, s);
-    if ((e = launch_bwd_output(p, w, q, dout, dq, s)) != 0) return e;
-    if ((e = launch_f32_to_planes(w.dmixp, H(lay.dmixp_hi), H(lay.dmixp_lo), rows * p.R, s)) != 0) return e;
+    if ((e = launch_tc_bwd_output(p, q, dout, b.mixed_hi, b.mixed_lo, b.blkinfo, dq, H(lay.dmixp_hi),
+                                  H(lay.dmixp_lo), w.dnp, s)) != 0)
+      return e;
     record_bwd_event(2, s);
     // gradient mixing dX_b = sum_q Mc[i(q), b] dX~_q: the forward mixing
     // kernel with Mc transposed

@@ -25,6 +25,13 @@ int launch_tc_bwd_mc(const Plan& p, const __nv_bfloat16* dx_hi, const __nv_bfloa
 int launch_tc_bwd_summary(const Plan& p, const void* k, const void* v, const __nv_bfloat16* dx_hi,
                           const __nv_bfloat16* dx_lo, void* dk, void* dv, cudaStream_t s);
 
+// dq and the per-piece gradient records dX~ (dS~, dz~, dv~ as dx planes,
+// [BH][Q][R]; dn~ into dnp [BH][Q] for MALA) from Q, dO and the mixed
+// forward records (planes [BH][M][R], blkinfo as the forward prep writes it).
+int launch_tc_bwd_output(const Plan& p, const void* q, const void* dout, const __nv_bfloat16* mixed_hi,
+                         const __nv_bfloat16* mixed_lo, const float4* blkinfo, void* dq, __nv_bfloat16* dx_hi,
+                         __nv_bfloat16* dx_lo, float* dnp, cudaStream_t s);
+
 // out[b][i] = in[i][b] for an M x M float32 matrix.
 int launch_transpose_mc(const float* in, float* out, int M, cudaStream_t s);
 
