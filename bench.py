@@ -408,19 +408,31 @@ BWD_METRIC = "MHLA bwd tokens*heads/sec (dQ, dK, dV, dMc; d=64) and % of GB300 H
 BWD_PHASES = ["recompute", "output", "mix", "mc", "summary"]
 # phase -> (kernel name in ncu, source, engine that bounds it when not HBM)
 BWD_PHASE_KERNEL = {
-    "recompute": ("simt_summary_kernel", "token_level_head_phi_gb300/csrc/simt.cu", "alu"),
-    "output": ("bwd_output_kernel", "token_level_head_phi_gb300/csrc/backward.cu", "alu"),
-    "mix": ("bwd_mix_kernel", "token_level_head_phi_gb300/csrc/backward.cu", "alu"),
-    "mc": ("bwd_mc_kernel", "token_level_head_phi_gb300/csrc/backward.cu", "alu"),
-    "summary": ("bwd_summary_kernel", "token_level_head_phi_gb300/csrc/backward.cu", "alu"),
+    "simt": {
+        "recompute": ("simt_summary_kernel", "token_level_head_phi_gb300/csrc/simt.cu", "alu"),
+        "output": ("bwd_output_kernel", "token_level_head_phi_gb300/csrc/backward.cu", "alu"),
+        "mix": ("bwd_mix_kernel", "token_level_head_phi_gb300/csrc/backward.cu", "alu"),
+        "mc": ("bwd_mc_kernel", "token_level_head_phi_gb300/csrc/backward.cu", "alu"),
+        "summary": ("bwd_summary_kernel", "token_level_head_phi_gb300/csrc/backward.cu", "alu"),
+    },
+    "tc": {
+        "recompute": ("tc_summary_kernel", "token_level_head_phi_gb300/csrc/tc_summary.cu", "tensor"),
+        "output": ("tc_bwd_output_kernel", "token_level_head_phi_gb300/csrc/tc_bwd_output.cu", "tensor"),
+        "mix": ("tc_mix_kernel", "token_level_head_phi_gb300/csrc/tc_mix.cu", "tensor"),
+        "mc": ("tc_bwd_mc_kernel", "token_level_head_phi_gb300/csrc/tc_bwd_mc.cu", "tensor"),
+        "summary": ("tc_bwd_summary_kernel", "token_level_head_phi_gb300/csrc/tc_bwd_summary.cu", "tensor"),
+    },
 }
+BWD_LAUNCHES = {"simt": 7, "tc": 10}
 FP32_LANES_PER_SM = 128  # FP32 FMA lanes per SM (4 partitions x 32)
 SM_COUNT = 152
 
 
 def bwd_phase_cost(w: wl.Workload, splits: int):
-    """Compulsory bytes and dense FLOPs of each backward phase (float32
-    intermediates: 4 bytes per summary entry)."""
+    """Compulsory bytes and dense FLOPs of each backward phase.  Records take
+    4 bytes per entry on both paths (float32, or bf16 high + low planes); the
+    FLOPs are those of the float32 contractions (the tensor cores run each
+    split product three times)."""
     el = 2 if w.dtype == "bf16" else 4
     U, N, d, M = w.units, w.n_tokens, w.head_dim, w.n_blocks
     R = d * d + 2 * d
@@ -466,9 +478,11 @@ def run_backward(args, w: wl.Workload, world: int, rank: int, local: int, dist):
     mc = torch.from_numpy(wl.make_mc(w)).to(dev)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
     dmc = torch.empty_like(mc)
-    p = mb.make_params(w.batch, w.heads, w.head_dim, w.grid, w.block, w.dtype, "elu1", w.norm)
+    path = "tc" if (w.dtype == "bf16" and w.head_dim == 64 and args.variant != "simt") else "simt"
+    variant = "simt" if path == "simt" else "auto"
+    p = mb.make_params(w.batch, w.heads, w.head_dim, w.grid, w.block, w.dtype, "elu1", w.norm, variant)
     splits = mb.mhla_plan(mb.make_params(w.batch, w.heads, w.head_dim, w.grid, w.block, w.dtype, "elu1", w.norm,
-                                         "simt")).summary_splits
+                                         "multipass" if path == "tc" else "simt")).summary_splits
     need = mb.mhla_backward_workspace_bytes(p)
     ws = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
     handle = stream.cuda_stream
@@ -532,7 +546,7 @@ def run_backward(args, w: wl.Workload, world: int, rank: int, local: int, dist):
     hbm, tf_burst, tf_sust, peak_kind = load_peaks()
     cost = bwd_phase_cost(w, splits)
     dom = max(avg_phase, key=avg_phase.get)
-    kname, ksrc, engine = BWD_PHASE_KERNEL[dom]
+    kname, ksrc, engine = BWD_PHASE_KERNEL[path][dom]
     nbytes, nflops = cost[dom]
     sec = avg_phase[dom] / 1e3
     sm_mhz = (clocks or {}).get("sm_max_mhz") or 2070.0
@@ -575,8 +589,10 @@ def run_backward(args, w: wl.Workload, world: int, rank: int, local: int, dist):
     return {
         "metric": BWD_METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f32", "data": "synthetic (seeded normals, locality-biased Mc, seeded normal dO)",
+        "dtype": "bf16" if path == "tc" else "f32",
+        "data": "synthetic (seeded normals, locality-biased Mc, seeded normal dO)",
         "config": dict(wl.describe(w), pass_="backward", input_dtype=w.dtype,
+                       path="tensor cores (split bf16)" if path == "tc" else "CUDA cores (float32)",
                        l2="no flush: inputs exceed L2" if flush is None else "L2 flushed (256 MB write) between steps, outside per-step events",
                        parallelism=f"replicas{world}" if world > 1 else "single GPU"),
         "roofline": roof,
@@ -584,7 +600,7 @@ def run_backward(args, w: wl.Workload, world: int, rank: int, local: int, dist):
                           "bound": "hbm" if t_hbm >= t_tc else "tensor",
                           "frac": max(t_hbm, t_tc) / (ms_per_step / 1e3)},
         "phase_ms": avg_phase,
-        "gpu_launches": 7 * K,
+        "gpu_launches": BWD_LAUNCHES[path] * K,
         "clocks": clocks,
         "e2e": {"value": w.units * w.n_tokens * E / (te1 - te0), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": E, "ms_per_step": (te1 - te0) * 1e3 / E},

@@ -48,8 +48,8 @@ namespace {
 using namespace tc;
 
 constexpr int kThreads = 512;
-constexpr int kXfThreads = 256;                 // warps 4..11
-constexpr int kEpiThreads = 128;                // warps 12..15
+constexpr int kXfThreads = 128;                 // warps 4..7
+constexpr int kEpiThreads = 128;                // warps 8..11 (E1), 12..15 (dq, record)
 constexpr uint32_t kTile = 128 * 128;           // 128 token rows x 64 bf16
 constexpr uint32_t kBTile = 64 * 128;           // 64 rows x 64 bf16
 constexpr int kStages = 2;
@@ -361,11 +361,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_output_kernel(const __grid
         }
       }
     }
-  } else if (warp >= 4 && warp < 12) {
+  } else if (warp >= 4 && warp < 8) {
     // ------------------------------------ phi(Q): P hi in place, P lo aside
-    const int t = threadIdx.x - 128;
-    const int row = t >> 1;
-    const int half = t & 1;
+    const int row = threadIdx.x - 128;
     int s = 0;
     uint32_t ph = 0;
     bool ok = true;
@@ -380,9 +378,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_output_kernel(const __grid
         }
         uint8_t* rp = gb + s * kStageBytes + row * 128;
         if (row < rows) {
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint32_t off = ((4 * half + j + row) & 7) << 4;
+#pragma unroll 2
+          for (int j = 0; j < 8; ++j) {
+            const uint32_t off = ((j + row) & 7) << 4;
             uint4 xv = *reinterpret_cast<const uint4*>(rp + off), lo;
             uint32_t* xp = &xv.x;
             uint32_t* lp = &lo.x;
@@ -400,10 +398,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_output_kernel(const __grid
         } else if (row < rows_pad) {
           // padding rows of the token contraction: zero
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint32_t off = (uint32_t)(4 * half + j) << 4;
-            *reinterpret_cast<uint4*>(rp + off) = make_uint4(0u, 0u, 0u, 0u);
-            *reinterpret_cast<uint4*>(rp + 2 * kTile + off) = make_uint4(0u, 0u, 0u, 0u);
+          for (int j = 0; j < 8; ++j) {
+            *reinterpret_cast<uint4*>(rp + (j << 4)) = make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4*>(rp + 2 * kTile + (j << 4)) = make_uint4(0u, 0u, 0u, 0u);
           }
         }
         fence_proxy_async();
@@ -414,18 +411,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_output_kernel(const __grid
         }
       }
     }
-  } else if (warp >= 12) {
-    // ----------------------------------------------------------- epilogues
+  } else if (warp >= 8 && warp < 12) {
+    // ------------------------------------------------ E1: D1 -> G, G2, W
     const int q4 = warp & 3;
     const int t = 32 * q4 + lane;       // token row = TMEM lane
-    const int et = threadIdx.x - 384;
     uint8_t* g2row = gb + kOffG2 + t * 128 + ((t & 7) << 4);   // logical chunk 0 of row t
     uint8_t* wrow = gb + kOffW + t * 128 + ((t & 7) << 4);
     uint8_t* glo_row = gb + kOffGlo + t * 128;
-    float* scratch = reinterpret_cast<float*>(gb + kScratch);
     int s = 0, x = 0;
     uint32_t ph = 0, bph = 0;
-    long long n = 0, m = 0;
+    long long n = 0;
     bool ok = true;
     for (int w = blockIdx.x; w < a.units && ok; w += gridDim.x) {
       int u, i, c0, c1;
@@ -440,9 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_output_kernel(const __grid
       const float ntil = reinterpret_cast<const float4*>(bp + kOffInfo)->y;
       for (int c = c0; c < c1; ++c) {
         const uint32_t np = (uint32_t)(n & 1);
-        uint8_t* qrow = gb + s * kStageBytes + t * 128;   // P hi -> dq
-        uint8_t* grow = qrow + kTile;                     // dO -> G hi
-        const uint8_t* lrow = qrow + 2 * kTile;           // P lo
+        uint8_t* grow = gb + s * kStageBytes + kTile + t * 128;   // dO -> G hi
         // ------------------------------------------ E1: D1 -> G, G2, W
         ok = mbar_wait(d1full, np, a.err, 0x80e, abort_flag);
         if (!named_all(5, kEpiThreads, ok)) {
@@ -533,9 +526,38 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_output_kernel(const __grid
         fence_proxy_async();
         mbar_arrive_warp(gready);
 
+        ++n;
+        if (++s == kStages) {
+          s = 0;
+          ph ^= 1u;
+        }
+      }
+      if (++x == kBStages) {
+        x = 0;
+        bph ^= 1u;
+      }
+    }
+  } else if (warp >= 12) {
+    // ------------------------------------- dq from D3, records from D2
+    const int q4 = warp & 3;
+    const int t = 32 * q4 + lane;       // token row = TMEM lane
+    const int et = threadIdx.x - 384;
+    float* scratch = reinterpret_cast<float*>(gb + kScratch);
+    int s = 0;
+    uint32_t ph = 0;
+    long long n = 0, m = 0;
+    bool ok = true;
+    for (int w = blockIdx.x; w < a.units && ok; w += gridDim.x) {
+      int u, i, c0, c1;
+      bo_unit(p, a, w, u, i, c0, c1);
+      for (int c = c0; c < c1; ++c) {
+        const uint32_t np = (uint32_t)(n & 1);
+        uint8_t* qrow = gb + s * kStageBytes + t * 128;   // P hi -> dq
+        const uint8_t* lrow = qrow + 2 * kTile;           // P lo
+        const uint32_t ta = tmem + ((uint32_t)(32 * q4) << 16);
         // ------------------------------------------------- E2: D3 -> dq
         ok = mbar_wait(d3full, np, a.err, 0x810, abort_flag);
-        if (!named_all(5, kEpiThreads, ok)) {
+        if (!named_all(6, kEpiThreads, ok)) {
           ok = false;
           break;
         }
@@ -571,7 +593,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_output_kernel(const __grid
         tc_fence_before();
         mbar_arrive_warp(d3empty);
         fence_proxy_async();
-        named_sync(5, kEpiThreads);
+        named_sync(6, kEpiThreads);
         if (et == 0) {
           int x0, y0, t0;
           chunk_origin(p, a.c, (uint32_t)i, (uint32_t)c, x0, y0, t0);
@@ -590,7 +612,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_output_kernel(const __grid
       // ------------------------------------- piece record from D2
       const int d2 = (int)(m & 1);
       ok = mbar_wait(d2full(d2), (uint32_t)((m >> 1) & 1), a.err, 0x811, abort_flag);
-      if (!named_all(5, kEpiThreads, ok)) {
+      if (!named_all(6, kEpiThreads, ok)) {
         ok = false;
         break;
       }
@@ -600,7 +622,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_output_kernel(const __grid
       uint8_t* zv_hi = st_hi + 2 * kBTile;
       uint8_t* zv_lo = zv_hi + 1024;
       if (et == 0) bulk_wait_read<0>();   // the previous record's stores have read the staging
-      named_sync(5, kEpiThreads);
+      named_sync(6, kEpiThreads);
       const uint32_t td = tmem + kColD2 + 128u * (uint32_t)d2 + ((uint32_t)(32 * q4) << 16);
 #pragma unroll 1
       for (int h = 0; h < 2; ++h) {
@@ -635,7 +657,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_output_kernel(const __grid
       tmem_ld16(td + 64u, zc);
       tmem_wait_ld();
       tc_fence_before();
-      named_sync(5, kEpiThreads);
+      named_sync(6, kEpiThreads);
       if (et == 0) mbar_arrive(d2empty(d2));
       if (q4 < 2) {
         // dz~[k] = D2[k][64] + D2[k][65]
@@ -655,7 +677,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_output_kernel(const __grid
         if (lane == 2 && mala) a.dnp[w] = zc[3] + zc[4];
       }
       fence_proxy_async();
-      named_sync(5, kEpiThreads);
+      named_sync(6, kEpiThreads);
       if (et == 0) {
         const int srow = w;   // record row: (u * M + i) * splits + piece
         tma_store_2d(&a.tmS_hi, smem_u32(st_hi), 0, srow * 66);
@@ -665,10 +687,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_output_kernel(const __grid
         bulk_commit();
       }
       ++m;
-      if (++x == kBStages) {
-        x = 0;
-        bph ^= 1u;
-      }
     }
     if (et == 0) bulk_wait<0>();
   }
