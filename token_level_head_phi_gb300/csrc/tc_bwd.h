@@ -35,8 +35,4 @@ int launch_tc_bwd_output(const Plan& p, const void* q, const void* dout, const _
 // out[b][i] = in[i][b] for an M x M float32 matrix.
 int launch_transpose_mc(const float* in, float* out, int M, cudaStream_t s);
 
-// Conversions between float32 records and hi/lo planes (n values).
-int launch_planes_to_f32(const __nv_bfloat16* hi, const __nv_bfloat16* lo, float* out, size_t n, cudaStream_t s);
-int launch_f32_to_planes(const float* in, __nv_bfloat16* hi, __nv_bfloat16* lo, size_t n, cudaStream_t s);
-
 }  // namespace mhla
