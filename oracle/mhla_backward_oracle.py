@@ -29,6 +29,10 @@ formula for them, so they are the plain chain rule of the forward steps:
     summaries:    dphk_j = dS_b v_j + dz_b,  dv_j = dS_b^T phk_j + dv_b
     feature map:  dq = dphq * phi'(q), dk = dphk * phi'(k)
 
+A query whose denominator s is exactly zero has output 0 (the forward
+oracle's rule); its output is then constant and it contributes nothing to
+any gradient.  phi' of ReLU is taken as 0 at x = 0 (a subgradient).
+
 ``mhla_bruteforce_backward64`` differentiates the explicit N x N form instead
 (A[t,j] = Mc[b(t),b(j)] phq_t . phk_j), never forming a summary; tests pin
 both against each other and against finite differences of the forward.
@@ -38,20 +42,25 @@ from __future__ import annotations
 
 import numpy as np
 
-from .mhla_oracle import (DIVISIVE, ELU1, IDENTITY, MALA, NONE, block_of_token, block_summaries,
+from .mhla_oracle import (DIVISIVE, ELU1, EXP, IDENTITY, MALA, NONE, RELU, block_of_token, block_summaries,
                           feature_map, mix)
 
 
 def feature_map_grad(x, kind: str = ELU1) -> np.ndarray:
-    """phi'(x): 1 for x > 0 and exp(x) otherwise (ELU+1, alpha = 1); 1 for IDENTITY.
+    """phi'(x): 1 for x > 0 and exp(x) otherwise (ELU+1, alpha = 1); 1 for
+    IDENTITY; 1 for x > 0 and 0 otherwise (ReLU); exp(x) (exp).
 
-    At x = 0 both sides give 1, so ELU+1 is differentiable everywhere.
+    At x = 0 both sides of ELU+1 give 1, so it is differentiable everywhere.
     """
     x = np.asarray(x, dtype=np.float64)
     if kind == ELU1:
         return np.where(x > 0.0, 1.0, np.exp(np.minimum(x, 0.0)))
     if kind == IDENTITY:
         return np.ones_like(x)
+    if kind == RELU:
+        return np.where(x > 0.0, 1.0, 0.0)
+    if kind == EXP:
+        return np.exp(x)
     raise ValueError(f"unknown feature map {kind!r}")
 
 
@@ -85,17 +94,21 @@ def mhla_head_backward64(q, k, v, mc, grid, block, dout, fmap: str = ELU1, norm:
             ds = np.zeros(pq.shape[0])
         else:
             s = pq @ zt[i]
+            # queries with s = 0 have a constant (zero) output: no gradient
+            live = s != 0.0
+            g = np.where(live[:, None], g, 0.0)
+            inv = np.divide(1.0, s, out=np.zeros_like(s), where=live)
             if norm == DIVISIVE:
-                o = num / s[:, None]
-                dnum = g / s[:, None]
-                ds = -np.sum(g * o, axis=1) / s
+                o = num * inv[:, None]
+                dnum = g * inv[:, None]
+                ds = -np.sum(g * o, axis=1) * inv
             elif norm == MALA:
-                beta = 1.0 + 1.0 / s
+                beta = 1.0 + inv
                 gamma = s / nt[i]
                 dnum = beta[:, None] * g
                 dbeta = np.sum(g * num, axis=1)
                 dgamma = -(g @ vt[i])
-                ds = -dbeta / s ** 2 + dgamma / nt[i]
+                ds = -dbeta * inv ** 2 + dgamma / nt[i]
                 dvt[i] = -(gamma[:, None] * g).sum(axis=0)
                 dnt[i] = -np.sum(dgamma * s) / nt[i] ** 2
             else:
@@ -145,22 +158,26 @@ def mhla_bruteforce_backward64(q, k, v, mc, grid, block, dout, fmap: str = ELU1,
         dW = np.zeros_like(W)
     elif norm == DIVISIVE:
         s = A.sum(axis=1)
-        P = A / s[:, None]
+        live = s != 0.0
+        inv = np.divide(1.0, s, out=np.zeros_like(s), where=live)
+        P = A * inv[:, None]
         o = P @ v
         dv = P.T @ dout
-        dA = (dout @ v.T - np.sum(dout * o, axis=1)[:, None]) / s[:, None]
+        dA = (dout @ v.T - np.sum(dout * o, axis=1)[:, None]) * inv[:, None]
         dW = np.zeros_like(W)
     elif norm == MALA:
         s = A.sum(axis=1)
+        live = s != 0.0
+        inv = np.divide(1.0, s, out=np.zeros_like(s), where=live)
         w = W.sum(axis=1)
-        beta = 1.0 + 1.0 / s
+        beta = 1.0 + inv
         gamma = s / w
-        P = beta[:, None] * A - gamma[:, None] * W
+        P = np.where(live[:, None], beta[:, None] * A - gamma[:, None] * W, 0.0)
         dv = P.T @ dout
-        dP = dout @ v.T
+        dP = np.where(live[:, None], dout @ v.T, 0.0)
         dbeta = np.sum(dP * A, axis=1)
         dgamma = -np.sum(dP * W, axis=1)
-        ds = -dbeta / s ** 2 + dgamma / w
+        ds = -dbeta * inv ** 2 + dgamma / w
         dw = -dgamma * s / w ** 2
         dA = beta[:, None] * dP + ds[:, None]
         dW = -gamma[:, None] * dP + dw[:, None]

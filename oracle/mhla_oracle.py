@@ -34,7 +34,14 @@ Readings taken where the pages are silent (each is listed in the design notes):
     replaced by its Mc-mixed counterpart (sum phi(K)^T V -> S~_i,
     sum phi(K) -> z~_i, sum V -> v~_i, N -> n~_i = sum_b Mc[i,b] n_b); at
     M = 1 with Mc = [[1]] this is the MALA page's formula;
-  * no epsilon in any denominator.
+  * no epsilon in any denominator; where a query's denominator
+    s = phi(q)^T z~_i is exactly zero (possible with ReLU features, or with a
+    zero row of Mc) its output is zero under DIVISIVE and MALA: with
+    nonnegative features and Mc, s = 0 forces phi(q)^T S~_i = 0, so this is
+    the value the customary guard num / (s + eps) takes for every eps > 0;
+  * the MALA page's ablation names ELU+1, ReLU and exp as interchangeable
+    feature maps; ReLU is max(x, 0) and exp is e^x elementwise, evaluated
+    without any shift (inputs whose exponential overflows are the caller's).
 
 Parity pins (tests/test_oracle_pins.py) tie every function here to facts
 outside this file: a hand-derived worked example, the explicit N x N
@@ -56,6 +63,9 @@ NORMS = (DIVISIVE, MALA, NONE)
 
 ELU1 = "elu1"
 IDENTITY = "identity"
+RELU = "relu"
+EXP = "exp"
+FEATURE_MAPS = (ELU1, IDENTITY, RELU, EXP)
 
 
 def feature_map(x, kind: str = ELU1) -> np.ndarray:
@@ -63,7 +73,8 @@ def feature_map(x, kind: str = ELU1) -> np.ndarray:
 
     ELU+1 (alpha = 1): x + 1 for x > 0, exp(x) otherwise -- the positive
     feature map of the MHLA page's background section and one of the maps the
-    MALA page's ablation names.  IDENTITY is phi(x) = x, used only by tests
+    MALA page's ablation names; RELU (max(x, 0)) and EXP (e^x) are the other
+    two maps of that ablation.  IDENTITY is phi(x) = x, used only by tests
     that need exact control of phi (the caller keeps features positive).
     """
     x = np.asarray(x, dtype=np.float64)
@@ -71,6 +82,10 @@ def feature_map(x, kind: str = ELU1) -> np.ndarray:
         return np.where(x > 0.0, x + 1.0, np.exp(np.minimum(x, 0.0)))
     if kind == IDENTITY:
         return x.copy()
+    if kind == RELU:
+        return np.maximum(x, 0.0)
+    if kind == EXP:
+        return np.exp(x)
     raise ValueError(f"unknown feature map {kind!r}")
 
 
@@ -131,6 +146,7 @@ def head_output(phiq: np.ndarray, bidx: np.ndarray, St, zt, vt, nt, norm: str) -
     MALA:     s = phi(q)^T z~_i, beta = 1 + 1/s, gamma = s / n~_i,
               o = beta phi(q)^T S~_i - gamma v~_i  (MALA page, linear form,
               global sums replaced by their mixed counterparts)
+    A query with s = 0 gets o = 0 under DIVISIVE and MALA (module notes).
     """
     out = np.zeros((phiq.shape[0], St.shape[2]))
     for i in range(St.shape[0]):
@@ -141,14 +157,16 @@ def head_output(phiq: np.ndarray, bidx: np.ndarray, St, zt, vt, nt, norm: str) -
             out[rows] = num
             continue
         s = pq @ zt[i]
+        live = s != 0.0
+        inv = np.divide(1.0, s, out=np.zeros_like(s), where=live)
         if norm == DIVISIVE:
-            out[rows] = num / s[:, None]
+            res = num * inv[:, None]
         elif norm == MALA:
-            beta = 1.0 + 1.0 / s
             gamma = s / nt[i]
-            out[rows] = beta[:, None] * num - gamma[:, None] * vt[i][None, :]
+            res = (1.0 + inv)[:, None] * num - gamma[:, None] * vt[i][None, :]
         else:
             raise ValueError(f"unknown norm {norm!r}")
+        out[rows] = np.where(live[:, None], res, 0.0)
     return out
 
 
@@ -208,7 +226,8 @@ def mhla_bruteforce64(q, k, v, mc, grid, block, fmap: str = ELU1, norm: str = DI
         return A @ v
     s = A.sum(axis=1)
     if norm == DIVISIVE:
-        return (A @ v) / s[:, None]
+        live = s != 0.0
+        return np.where(live[:, None], A @ v, 0.0) * np.divide(1.0, s, out=np.zeros_like(s), where=live)[:, None]
     if norm == MALA:
         return mala_scores64(q, k, mc, grid, block, fmap) @ v
     raise ValueError(f"unknown norm {norm!r}")
@@ -225,9 +244,11 @@ def mala_scores64(q, k, mc, grid, block, fmap: str = ELU1) -> np.ndarray:
     W = mc[bidx][:, bidx]
     A = W * (feature_map(q, fmap) @ feature_map(k, fmap).T)
     s = A.sum(axis=1)
-    beta = 1.0 + 1.0 / s
+    live = s != 0.0
+    beta = 1.0 + np.divide(1.0, s, out=np.zeros_like(s), where=live)
     gamma = s / W.sum(axis=1)
-    return beta[:, None] * A - gamma[:, None] * W
+    # a query with s = 0 has a zero score row (module notes)
+    return np.where(live[:, None], beta[:, None] * A - gamma[:, None] * W, 0.0)
 
 
 def rank_bound(grid, block, d: int) -> int:
@@ -256,7 +277,7 @@ def relative_max_error(got, want) -> float:
 
 
 __all__ = [
-    "DIVISIVE", "MALA", "NONE", "NORMS", "ELU1", "IDENTITY", "feature_map",
+    "DIVISIVE", "MALA", "NONE", "NORMS", "ELU1", "IDENTITY", "RELU", "EXP", "FEATURE_MAPS", "feature_map",
     "block_of_token", "block_summaries", "mix", "head_output", "mhla_head64",
     "mhla_forward64", "attention_matrix64", "mhla_bruteforce64", "mala_scores64",
     "rank_bound", "numerical_rank", "relative_max_error",
