@@ -3,6 +3,7 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
                     [--variant auto|simt|multipass|fused] [--impl mine|reference]
                     [--all-workloads] [--no-cpu-baseline] [--pass forward|backward]
+                    [--feature-map elu1|relu|exp]
 
 A step is one full forward (block summaries, mixing, output) over one batch
 of the workload's seeded synthetic inputs, already resident in HBM.  The
@@ -252,7 +253,7 @@ def run_mine(args, w: wl.Workload, world: int, rank: int, local: int, dist):
     q, k, v = to_dev(qn), to_dev(kn), to_dev(vn)
     mc = torch.from_numpy(mcn).to(dev)
     out = torch.empty_like(q)
-    p = mb.make_params(w.batch, w.heads, w.head_dim, w.grid, w.block, w.dtype, "elu1", w.norm, args.variant)
+    p = mb.make_params(w.batch, w.heads, w.head_dim, w.grid, w.block, w.dtype, args.feature_map, w.norm, args.variant)
     info = mb.mhla_plan(p)
     ws = torch.empty(max(info.workspace_bytes, 1), dtype=torch.uint8, device=dev)
     ws_bytes = ws.numel()
@@ -350,7 +351,7 @@ def run_mine(args, w: wl.Workload, world: int, rank: int, local: int, dist):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": w.dtype, "data": "synthetic (seeded normals, locality-biased Mc; no dataset, no weights)",
-        "config": dict(wl.describe(w), variant=mb.mhla_plan(p).variant,
+        "config": dict(wl.describe(w), feature_map=args.feature_map, variant=mb.mhla_plan(p).variant,
                        variant_name={1: "simt", 2: "multipass", 3: "fused"}.get(info.variant, str(info.variant)),
                        l2="no flush: inputs exceed L2" if flush is None else "L2 flushed (256 MB write) between steps, outside per-step events",
                        parallelism=f"replicas{world}" if world > 1 else "single GPU"),
@@ -480,8 +481,8 @@ def run_backward(args, w: wl.Workload, world: int, rank: int, local: int, dist):
     dmc = torch.empty_like(mc)
     path = "tc" if (w.dtype == "bf16" and w.head_dim == 64 and args.variant != "simt") else "simt"
     variant = "simt" if path == "simt" else "auto"
-    p = mb.make_params(w.batch, w.heads, w.head_dim, w.grid, w.block, w.dtype, "elu1", w.norm, variant)
-    splits = mb.mhla_plan(mb.make_params(w.batch, w.heads, w.head_dim, w.grid, w.block, w.dtype, "elu1", w.norm,
+    p = mb.make_params(w.batch, w.heads, w.head_dim, w.grid, w.block, w.dtype, args.feature_map, w.norm, variant)
+    splits = mb.mhla_plan(mb.make_params(w.batch, w.heads, w.head_dim, w.grid, w.block, w.dtype, args.feature_map, w.norm,
                                          "multipass" if path == "tc" else "simt")).summary_splits
     need = mb.mhla_backward_workspace_bytes(p)
     ws = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
@@ -591,7 +592,7 @@ def run_backward(args, w: wl.Workload, world: int, rank: int, local: int, dist):
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if path == "tc" else "f32",
         "data": "synthetic (seeded normals, locality-biased Mc, seeded normal dO)",
-        "config": dict(wl.describe(w), pass_="backward", input_dtype=w.dtype,
+        "config": dict(wl.describe(w), pass_="backward", feature_map=args.feature_map, input_dtype=w.dtype,
                        path="tensor cores (split bf16)" if path == "tc" else "CUDA cores (float32)",
                        l2="no flush: inputs exceed L2" if flush is None else "L2 flushed (256 MB write) between steps, outside per-step events",
                        parallelism=f"replicas{world}" if world > 1 else "single GPU"),
@@ -617,7 +618,7 @@ from oracle import mhla_oracle as orc
 from oracle import mhla_backward_oracle as orb
 w = wl.WORKLOADS[{name!r}]
 mc = wl.make_mc(w)
-budget, max_units, per_step, backward = {budget}, {max_units}, {per_step}, {backward}
+budget, max_units, per_step, backward, fmap = {budget}, {max_units}, {per_step}, {backward}, {fmap!r}
 times = []
 units = 0
 t_all = time.perf_counter()
@@ -627,9 +628,9 @@ for step in range(max_units):
     g = wl.head_output_grad(w, u) if backward else None
     t0 = time.perf_counter()
     if backward:
-        orb.mhla_head_backward64(q, k, v, mc, w.grid, w.block, g, orc.ELU1, w.norm)
+        orb.mhla_head_backward64(q, k, v, mc, w.grid, w.block, g, fmap, w.norm)
     else:
-        orc.mhla_head64(q, k, v, mc, w.grid, w.block, orc.ELU1, w.norm)
+        orc.mhla_head64(q, k, v, mc, w.grid, w.block, fmap, w.norm)
     times.append(time.perf_counter() - t0)
     units += 1
     if not per_step and sum(times) >= budget:
@@ -638,14 +639,15 @@ print(json.dumps({{"times": times, "units": units}}))
 """
 
 
-def oracle_run(w: wl.Workload, budget_s: float, max_units: int, per_step: bool, backward: bool = False):
+def oracle_run(w: wl.Workload, budget_s: float, max_units: int, per_step: bool, backward: bool = False,
+               fmap: str = "elu1"):
     """Runs the oracle in a fresh process (BLAS threads = available cores)."""
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
     env = dict(os.environ)
     for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
         env[var] = str(cores)
     code = ORACLE_SNIPPET.format(root=ROOT, name=w.name, budget=budget_s, max_units=max_units, per_step=per_step,
-                               backward=backward)
+                               backward=backward, fmap=fmap)
     res = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=1800)
     if res.returncode != 0:
         raise RuntimeError(f"oracle run failed: {res.stderr[-2000:]}")
@@ -653,8 +655,8 @@ def oracle_run(w: wl.Workload, budget_s: float, max_units: int, per_step: bool, 
     return d["times"], d["units"], cores
 
 
-def cpu_baseline(w: wl.Workload, budget_s: float = 15.0, backward: bool = False):
-    times, units, cores = oracle_run(w, budget_s, max_units=10 ** 6, per_step=False, backward=backward)
+def cpu_baseline(w: wl.Workload, budget_s: float = 15.0, backward: bool = False, fmap: str = "elu1"):
+    times, units, cores = oracle_run(w, budget_s, max_units=10 ** 6, per_step=False, backward=backward, fmap=fmap)
     total = sum(times)
     what = "backward" if backward else "forward"
     return {"value": units * w.n_tokens / total, "unit": UNIT, "cores": cores, "kind": "oracle",
@@ -666,7 +668,8 @@ def run_reference(args, w: wl.Workload):
     """--impl reference: the float64 oracle, each step one (batch, head) unit."""
     K, W = args.steps, args.warmup
     backward = getattr(args, "pass_", "forward") == "backward"
-    times, units, cores = oracle_run(w, 0.0, max_units=W + K, per_step=True, backward=backward)
+    times, units, cores = oracle_run(w, 0.0, max_units=W + K, per_step=True, backward=backward,
+                                     fmap=getattr(args, "feature_map", "elu1"))
     timed = times[W:W + K]
     total = sum(timed)
     value = K * w.n_tokens / total
@@ -674,7 +677,7 @@ def run_reference(args, w: wl.Workload):
         "impl": "reference", "metric": BWD_METRIC if backward else METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": K,
         "warmup": W, "ms_per_step": total * 1e3 / K, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded normals, locality-biased Mc)",
-        "config": dict(wl.describe(w), parallelism="host cores"),
+        "config": dict(wl.describe(w), feature_map=getattr(args, "feature_map", "elu1"), parallelism="host cores"),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": f"each step one (batch, head) unit of {w.name} ({w.n_tokens} tokens)"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -694,6 +697,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--pass", dest="pass_", default="forward", choices=["forward", "backward"])
+    ap.add_argument("--feature-map", default="elu1", choices=["elu1", "relu", "exp"])
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -714,7 +718,7 @@ def main():
     if args.pass_ == "backward":
         result = run_backward(args, w, world, rank, local, dist)
         if rank == 0 and not args.no_cpu_baseline:
-            result["cpu_baseline"] = cpu_baseline(w, backward=True)
+            result["cpu_baseline"] = cpu_baseline(w, backward=True, fmap=args.feature_map)
         if rank == 0:
             print(json.dumps(result), flush=True)
         if dist is not None:
@@ -740,7 +744,7 @@ def main():
             extra[name]["config"] = r["config"]
         result["workloads"] = extra
     if rank == 0 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(w)
+        result["cpu_baseline"] = cpu_baseline(w, fmap=args.feature_map)
     if rank == 0:
         print(json.dumps(result), flush=True)
     if dist is not None:

@@ -71,7 +71,19 @@ typedef enum mhla_dtype { MHLA_DTYPE_BF16 = 0, MHLA_DTYPE_F32 = 1 } mhla_dtype;
 
 /* ELU1: phi(x) = x + 1 (x > 0), exp(x) (x <= 0).  IDENTITY: phi(x) = x; for
  * tests only, the caller keeps the features positive. */
-typedef enum mhla_feature_map { MHLA_FEATURE_ELU1 = 0, MHLA_FEATURE_IDENTITY = 1 } mhla_feature_map;
+/* Feature map phi applied to Q and K.  ELU1: ELU(x) + 1 (alpha = 1); RELU:
+ * max(x, 0); EXP: e^x, evaluated in float32 without a shift (inputs whose
+ * exponential overflows float32 give inf/NaN) -- the three maps of "Rectifying
+ * Magnitude Neglect in Linear Attention", ablations.  IDENTITY (phi(x) = x) is
+ * for tests that keep features positive.  A query whose denominator
+ * s = phi(q)^T z~_i is exactly zero (ReLU features, or a zero row of Mc) gets
+ * output 0 under DIVISIVE and MALA, and no gradient. */
+typedef enum mhla_feature_map {
+  MHLA_FEATURE_ELU1 = 0,
+  MHLA_FEATURE_IDENTITY = 1,
+  MHLA_FEATURE_RELU = 2,
+  MHLA_FEATURE_EXP = 3
+} mhla_feature_map;
 
 typedef enum mhla_norm { MHLA_NORM_DIVISIVE = 0, MHLA_NORM_MALA = 1, MHLA_NORM_NONE = 2 } mhla_norm;
 

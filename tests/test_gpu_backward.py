@@ -161,3 +161,28 @@ def test_backward_is_deterministic_and_leaves_guards():
         runs.append((big.clone(), dmc.clone()))
     assert torch.equal(runs[0][0].view(torch.int16), runs[1][0].view(torch.int16))
     assert torch.equal(runs[0][1], runs[1][1])
+
+
+@pytest.mark.parametrize("variant", ["auto", "simt"])
+@pytest.mark.parametrize("norm", ["divisive", "none", "mala"])
+@pytest.mark.parametrize("fmap", ["relu", "exp"])
+def test_relu_and_exp_backward(fmap, norm, variant):
+    w = wl.WORKLOADS["deit_t"].with_(batch=4)
+    ex, emc = backward_parity(w, norm, fmap=fmap, variant=variant)
+    tol_mc = TOL_MC_SIMT_BF16 if variant == "simt" else TOL_MC["bf16"]
+    assert ex <= TOL_X["bf16"] and emc <= tol_mc, f"{fmap}/{norm}/{variant}: {ex:.3e} {emc:.3e}"
+
+
+@pytest.mark.parametrize("variant", ["auto", "simt"])
+@pytest.mark.parametrize("norm", ["divisive", "mala"])
+def test_zero_denominator_rows_pass_no_gradient(norm, variant):
+    w = wl.random_small(32, (1, 14, 14), (1, 7, 7), 64, 1, 2, "bf16")
+    vals, _ = wl.all_inputs(w)
+    q, k, v = (np.array(a) for a in vals)
+    q[:, :, 3, :] = -np.abs(q[:, :, 3, :]) - 0.25   # phi(q_3) = 0 under ReLU
+    pairs = [wl.round_to_bf16(a) for a in (q, k, v)]
+    dev = [b for b, _ in pairs]
+    vals = [x for _, x in pairs]
+    ex, emc = backward_parity(w, norm, fmap="relu", inputs=(vals, dev), variant=variant)
+    tol_mc = TOL_MC_SIMT_BF16 if variant == "simt" else TOL_MC["bf16"]
+    assert ex <= TOL_X["bf16"] and emc <= tol_mc, f"{norm}/{variant}: {ex:.3e} {emc:.3e}"

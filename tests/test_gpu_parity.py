@@ -278,3 +278,48 @@ def test_host_entry_pipelined_matches_device_entry(name):
     h_out = torch.empty_like(host[0]).pin_memory()
     mb.mhla_forward_host(*host, torch.from_numpy(mc), w.grid, w.block, norm=w.norm, out=h_out)
     np.testing.assert_array_equal(h_out.view(torch.int16).numpy(), d_out)
+
+
+# ---------------------------------------------------------------- feature maps
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("norm", ["divisive", "none", "mala"])
+@pytest.mark.parametrize("fmap", ["relu", "exp"])
+@pytest.mark.parametrize("name", ["tiny_f32", "deit_t"])
+def test_relu_and_exp_maps(name, fmap, norm, variant):
+    w = wl.WORKLOADS[name]
+    _skip_unsupported(variant, w.dtype, w.head_dim)
+    err = parity(w, norm, variant, units=[0, w.units - 1], fmap=fmap)
+    assert err <= TOL[w.dtype], f"{name}/{fmap}/{norm}/{variant}: rel err {err:.3e}"
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_relu_maps_on_full_video_head(variant):
+    w = wl.WORKLOADS["video_16x64x64"].with_(batch=1, heads=2)
+    err = parity(w, "divisive", variant, fmap="relu")
+    assert err <= TOL[w.dtype], f"{variant}: rel err {err:.3e}"
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("norm", ["divisive", "mala"])
+def test_zero_denominator_rows_are_zero(norm, variant):
+    # ReLU features: a query with every entry negative has phi(q) = 0, and a
+    # query whose only positive feature no key has sees s = 0 too; both
+    # outputs are 0, every other output matches the oracle
+    w = wl.random_small(31, (1, 14, 14), (1, 7, 7), 64, 1, 2, "bf16")
+    vals, _ = wl.all_inputs(w)
+    q, k, v = (np.array(a) for a in vals)
+    q[:, :, 3, :] = -np.abs(q[:, :, 3, :]) - 0.25
+    k[:, :, :, 0] = -np.abs(k[:, :, :, 0]) - 0.25
+    q[:, :, 17, :] = -np.abs(q[:, :, 17, :]) - 0.25
+    q[:, :, 17, 0] = 1.5
+    pairs = [wl.round_to_bf16(a) for a in (q, k, v)]
+    dev = [b for b, _ in pairs]
+    vals = [x for _, x in pairs]
+    mc = wl.make_mc(w)
+    o = download(run_gpu(w, upload(w, dev), mc, norm, variant, "relu")).reshape(w.units, w.n_tokens, w.head_dim)
+    assert np.all(np.isfinite(o))
+    assert np.all(o[:, 3] == 0.0) and np.all(o[:, 17] == 0.0)
+    for u in range(w.units):
+        want = orc.mhla_head64(vals[0][0, u], vals[1][0, u], vals[2][0, u], mc, w.grid, w.block, "relu", norm)
+        assert orc.relative_max_error(o[u], want) <= TOL["bf16"]

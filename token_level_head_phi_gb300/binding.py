@@ -29,6 +29,8 @@ DTYPE_BF16 = 0
 DTYPE_F32 = 1
 FEATURE_ELU1 = 0
 FEATURE_IDENTITY = 1
+FEATURE_RELU = 2
+FEATURE_EXP = 3
 NORM_DIVISIVE = 0
 NORM_MALA = 1
 NORM_NONE = 2
@@ -40,7 +42,7 @@ NUM_PHASE_EVENTS = 4
 NUM_BWD_PHASE_EVENTS = 6
 
 NORMS = {"divisive": NORM_DIVISIVE, "mala": NORM_MALA, "none": NORM_NONE}
-FEATURE_MAPS = {"elu1": FEATURE_ELU1, "identity": FEATURE_IDENTITY}
+FEATURE_MAPS = {"elu1": FEATURE_ELU1, "identity": FEATURE_IDENTITY, "relu": FEATURE_RELU, "exp": FEATURE_EXP}
 VARIANTS = {"auto": VARIANT_AUTO, "simt": VARIANT_SIMT, "multipass": VARIANT_MULTIPASS, "fused": VARIANT_FUSED}
 DTYPES = {"bf16": DTYPE_BF16, "f32": DTYPE_F32}
 

@@ -40,10 +40,7 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kTile = 32;  // tokens per shared-memory tile
 
-__device__ __forceinline__ float phi_grad(float x, int fmap) {
-  if (fmap == MHLA_FEATURE_IDENTITY) return 1.f;
-  return x > 0.f ? 1.f : expf(x);
-}
+__device__ __forceinline__ float phi_grad(float x, int fmap) { return phi_deriv(x, phi_apply(x, fmap), fmap); }
 
 // One CTA per (query block piece, head).  Shared memory: S~_i [D][D], z~_i,
 // v~_i, and per tile phi(q) [T][D], dO [T][D], dnum [T][D] and per-token
@@ -115,8 +112,8 @@ bwd_output_kernel(Plan p, const T* __restrict__ Q, const T* __restrict__ dO, con
       const float g = sg[e];
       const float s = ssc[tt];
       float dn;
-      if (p.norm == MHLA_NORM_DIVISIVE) dn = g / s;
-      else if (p.norm == MHLA_NORM_MALA) dn = (1.f + 1.f / s) * g;
+      if (p.norm == MHLA_NORM_DIVISIVE) dn = s != 0.f ? g / s : 0.f;   // s = 0: constant output
+      else if (p.norm == MHLA_NORM_MALA) dn = s != 0.f ? (1.f + 1.f / s) * g : 0.f;
       else dn = g;
       sdn[e] = dn;
       // g * num replaces g: only the per-token sum dO . num is needed below
@@ -135,7 +132,7 @@ bwd_output_kernel(Plan p, const T* __restrict__ Q, const T* __restrict__ dO, con
         ds = -dbeta / (s * s) + dgamma / ntilde;
         sgam[tid] = s / ntilde;
       }
-      if (tid >= cnt) ds = 0.f;
+      if (tid >= cnt || (p.norm != MHLA_NORM_NONE && s == 0.f)) ds = 0.f;
       sds[tid] = ds;
     }
     __syncthreads();

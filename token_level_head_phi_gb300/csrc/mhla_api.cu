@@ -89,7 +89,7 @@ mhla_status make_plan(const mhla_params* prm, Plan* p, int split_units = 0) {
     if (prm->grid[i] % prm->block[i] != 0) return MHLA_ERR_INVALID_ARG;
   }
   if (prm->dtype != MHLA_DTYPE_BF16 && prm->dtype != MHLA_DTYPE_F32) return MHLA_ERR_INVALID_ARG;
-  if (prm->feature_map != MHLA_FEATURE_ELU1 && prm->feature_map != MHLA_FEATURE_IDENTITY)
+  if (prm->feature_map < MHLA_FEATURE_ELU1 || prm->feature_map > MHLA_FEATURE_EXP)
     return MHLA_ERR_INVALID_ARG;
   if (prm->norm != MHLA_NORM_DIVISIVE && prm->norm != MHLA_NORM_MALA && prm->norm != MHLA_NORM_NONE)
     return MHLA_ERR_INVALID_ARG;

@@ -177,11 +177,11 @@ simt_output_kernel(Plan p, const Tin* __restrict__ Q, const float* __restrict__ 
     float o;
     const float s = ss[tt];
     if (p.norm == MHLA_NORM_DIVISIVE) {
-      o = a / s;
+      o = s != 0.f ? a / s : 0.f;          // s = 0: no key mass, output 0
     } else if (p.norm == MHLA_NORM_MALA) {
       const float beta = 1.f + 1.f / s;
       const float gamma = s / n_mixed;
-      o = beta * a - gamma * sv[c];
+      o = s != 0.f ? beta * a - gamma * sv[c] : 0.f;
     } else {
       o = a;
     }

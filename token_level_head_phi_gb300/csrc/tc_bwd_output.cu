@@ -515,6 +515,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_output_kernel(const __grid
         wgt = gamma / scale;
         e = dgv * sden / (ntil * ntil);
       }
+      if (p.norm != MHLA_NORM_NONE && sden == 0.f) {
+        // no key mass: the output is constant 0 and passes no gradient
+        scale = ds = wgt = e = 0.f;
+      }
       // this G lo / G2 buffer is free once the MMAs of tile n - 2 are done
       ok = mbar_wait(gfree(g), (uint32_t)((it.n >> 1) & 1) ^ 1u, a.err, 0x80f, abort_flag);
       if (!named_all(5, kEpiThreads, ok)) break;
@@ -584,12 +588,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_output_kernel(const __grid
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               const int cc = 8 * j + 2 * q;
-              float d0 = 1.f, d1 = 1.f;
-              if (p.fmap == MHLA_FEATURE_ELU1) {
-                const float2 fh = bf16x2_to_float2(hp[q]), fl = bf16x2_to_float2(lp[q]);
-                d0 = fminf(fh.x + fl.x, 1.f);
-                d1 = fminf(fh.y + fl.y, 1.f);
-              }
+              const float2 fh = bf16x2_to_float2(hp[q]), fl = bf16x2_to_float2(lp[q]);
+              const float d0 = phi_deriv_from_phi(fh.x, fl.x, p.fmap);
+              const float d1 = phi_deriv_from_phi(fh.y, fl.y, p.fmap);
               hp[q] = pack_bf16x2(dq[cc] * d0, dq[cc + 1] * d1);
             }
             *reinterpret_cast<uint4*>(qrow + off) = ph4;

@@ -16,8 +16,8 @@
 //       K-major for D_K, MN-major for D_V; bf16 high + low planes
 //   the bias K step: A = a tile of ones (columns 0 and 1), B = dz_b (K-major,
 //       columns 0, 1 = high, low) or dv_b (MN-major, rows 0, 1 = high, low)
-// phi'(K) = 1 above zero and exp(K) = phi(K) at and below it, so it is
-// min(phi(K), 1) (ELU+1), taken from the two parts of phi(K).  The epilogue
+// phi'(K) comes from the two parts of phi(K): min(phi, 1) for ELU+1 (1 above
+// zero, exp(K) = phi(K) at and below it), [phi > 0] for ReLU, phi for exp.  The epilogue
 // writes dK over the phi(K) tile and dV over the V tile and stores both by
 // TMA to the grid positions of the tile.
 // Persistent, warp-specialised CTA (512 threads): warp 0 K/V producer, warp 1
@@ -366,11 +366,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_summary_kernel(const __gri
             for (int q = 0; q < 4; ++q) {
               const int cc = 8 * j + 2 * q;
               const float2 fh = bf16x2_to_float2(hp[q]), fl = bf16x2_to_float2(lp[q]);
-              float d0 = 1.f, d1 = 1.f;
-              if (p.fmap == MHLA_FEATURE_ELU1) {
-                d0 = fminf(fh.x + fl.x, 1.f);
-                d1 = fminf(fh.y + fl.y, 1.f);
-              }
+              const float d0 = phi_deriv_from_phi(fh.x, fl.x, p.fmap);
+              const float d1 = phi_deriv_from_phi(fh.y, fl.y, p.fmap);
               kp[q] = pack_bf16x2(gk[cc] * d0, gk[cc + 1] * d1);
               vp[q] = pack_bf16x2(gv[cc], gv[cc + 1]);
             }

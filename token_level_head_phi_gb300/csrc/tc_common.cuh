@@ -474,7 +474,20 @@ __device__ __forceinline__ float phi_elu1_fast(float x) {
 }
 
 __device__ __forceinline__ float phi_map(float x, int fmap) {
-  return fmap == MHLA_FEATURE_IDENTITY ? x : phi_elu1_fast(x);
+  if (fmap == MHLA_FEATURE_IDENTITY) return x;
+  if (fmap == MHLA_FEATURE_RELU) return fmaxf(x, 0.f);
+  if (fmap == MHLA_FEATURE_EXP) return __expf(x);
+  return phi_elu1_fast(x);
+}
+
+// phi' from the bf16 high and low parts of phi(x) (x itself is not kept):
+// ELU+1 gives phi > 1 exactly where x > 0 and phi' = min(phi, 1); ReLU gives
+// phi > 0 exactly where x > 0; exp gives phi' = phi.
+__device__ __forceinline__ float phi_deriv_from_phi(float hi, float lo, int fmap) {
+  if (fmap == MHLA_FEATURE_ELU1) return fminf(hi + lo, 1.f);
+  if (fmap == MHLA_FEATURE_RELU) return hi > 0.f ? 1.f : 0.f;
+  if (fmap == MHLA_FEATURE_EXP) return hi + lo;
+  return 1.f;
 }
 
 // phi = ELU+1 of two bf16 values, returned as bf16x2 rounded to nearest:

@@ -362,9 +362,9 @@ __device__ __forceinline__ void output_body(const OutArgs& a, const Plan& p, con
         // numerator and denominator carry the same scale, which cancels
         float scale = info.x, gamma = 0.f;
         if (p.norm == MHLA_NORM_DIVISIVE) {
-          scale = __frcp_rn(sden);
+          scale = sden != 0.f ? __frcp_rn(sden) : 0.f;     // s = 0: no key mass, output 0
         } else if (p.norm == MHLA_NORM_MALA) {
-          scale = 1.f + __frcp_rn(sden);                    // beta
+          scale = sden != 0.f ? 1.f + __frcp_rn(sden) : 0.f;  // beta
           gamma = sden / info.y;                            // s / n~_i
         }
         const float* vs = reinterpret_cast<const float*>(bp + L::kOffV) + 32 * h;
