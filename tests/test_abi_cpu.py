@@ -80,7 +80,8 @@ BAD = [
     dict(grid=(0, 14, 14)),
     dict(batch=-1),
     dict(dtype=7),
-    dict(feature_map=3),
+    dict(feature_map=4),
+    dict(feature_map=-1),
     dict(norm=9),
     dict(variant=11),
 ]
