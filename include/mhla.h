@@ -55,7 +55,7 @@
 extern "C" {
 #endif
 
-#define MHLA_ABI_VERSION 1
+#define MHLA_ABI_VERSION 2
 
 typedef enum mhla_status {
   MHLA_OK = 0,
@@ -124,6 +124,15 @@ typedef struct mhla_params {
   int feature_map;  /* mhla_feature_map                                    */
   int norm;         /* mhla_norm                                           */
   int variant;      /* mhla_variant                                        */
+  int causal;       /* 0: every token sees every block (the method as the
+                     * MHLA page defines it); 1: block-ordered causal form --
+                     * tokens ordered by (block, position inside the block),
+                     * query t sees keys up to itself: earlier blocks through
+                     * the strict lower triangle of Mc, its own block through
+                     * Mc[i, i] and only the tokens up to t.  Forward only, on
+                     * the float32 CUDA-core kernels (AUTO picks them;
+                     * MULTIPASS/FUSED and mhla_backward return
+                     * MHLA_ERR_UNSUPPORTED).                                */
 } mhla_params;
 
 /* What a call with these parameters will run (for tests and benchmarks). */

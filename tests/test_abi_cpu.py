@@ -44,7 +44,7 @@ def test_binding_declares_every_header_function():
 
 
 def test_abi_version_and_strings(lib):
-    assert mb.mhla_abi_version() == 1
+    assert mb.mhla_abi_version() == 2
     for s in range(7):
         assert mb.mhla_status_string(s).startswith("MHLA")
     assert "unknown" in mb.mhla_status_string(42)
@@ -262,3 +262,19 @@ def test_backward_workspace_and_checks(lib):
     empty = mb.make_params(0, 3, 64, w.grid, w.block)
     assert mb.mhla_backward_workspace_bytes(empty) == 0
     assert f(None, None, None, None, None, ctypes.byref(empty), None, None, None, None, None, 0, None) == mb.MHLA_OK
+
+
+def test_causal_plan_and_rejections(lib):
+    w = wl.WORKLOADS["deit_t"]
+    p = mb.make_params(w.batch, w.heads, w.head_dim, w.grid, w.block, causal=True)
+    info = mb.mhla_plan(p)
+    assert info.variant == mb.VARIANT_SIMT and info.kernels_per_call == 5
+    assert info.workspace_bytes >= mb.mhla_workspace_bytes(mb.make_params(
+        w.batch, w.heads, w.head_dim, w.grid, w.block, variant="simt")) + 4 * w.n_blocks ** 2
+    for variant in ("multipass", "fused"):
+        bad = mb.make_params(w.batch, w.heads, w.head_dim, w.grid, w.block, variant=variant, causal=True)
+        assert lib.mhla_plan(ctypes.byref(bad), ctypes.byref(mb.MhlaPlanInfo())) == mb.MHLA_ERR_UNSUPPORTED
+    n = ctypes.c_size_t(0)
+    assert lib.mhla_backward_workspace_bytes(ctypes.byref(p), ctypes.byref(n)) == mb.MHLA_ERR_UNSUPPORTED
+    p.causal = 2
+    assert lib.mhla_plan(ctypes.byref(p), ctypes.byref(mb.MhlaPlanInfo())) == mb.MHLA_ERR_INVALID_ARG

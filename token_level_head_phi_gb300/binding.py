@@ -61,7 +61,7 @@ class MhlaParams(ctypes.Structure):
         ("batch", ctypes.c_int), ("heads", ctypes.c_int), ("head_dim", ctypes.c_int),
         ("grid", ctypes.c_int * 3), ("block", ctypes.c_int * 3),
         ("dtype", ctypes.c_int), ("feature_map", ctypes.c_int), ("norm", ctypes.c_int),
-        ("variant", ctypes.c_int),
+        ("variant", ctypes.c_int), ("causal", ctypes.c_int),
     ]
 
 
@@ -129,7 +129,7 @@ def _check(status: int, where: str):
 
 def make_params(batch: int, heads: int, head_dim: int, grid: Sequence[int], block: Sequence[int],
                 dtype: str = "bf16", feature_map: str = "elu1", norm: str = "divisive",
-                variant: str = "auto") -> MhlaParams:
+                variant: str = "auto", causal: bool = False) -> MhlaParams:
     p = MhlaParams()
     p.batch, p.heads, p.head_dim = int(batch), int(heads), int(head_dim)
     for i in range(3):
@@ -139,6 +139,7 @@ def make_params(batch: int, heads: int, head_dim: int, grid: Sequence[int], bloc
     p.feature_map = FEATURE_MAPS[feature_map] if isinstance(feature_map, str) else int(feature_map)
     p.norm = NORMS[norm] if isinstance(norm, str) else int(norm)
     p.variant = VARIANTS[variant] if isinstance(variant, str) else int(variant)
+    p.causal = int(causal)
     return p
 
 
@@ -169,17 +170,17 @@ def _torch_dtype_name(t) -> str:
     raise TypeError(f"unsupported dtype {t.dtype}; MHLA takes bfloat16 or float32")
 
 
-def _params_for(q, grid, block, feature_map, norm, variant) -> MhlaParams:
+def _params_for(q, grid, block, feature_map, norm, variant, causal=False) -> MhlaParams:
     if q.dim() != 4:
         raise ValueError("q, k, v must be [B, H, N, d]")
     B, H, N, d = q.shape
     if grid[0] * grid[1] * grid[2] != N:
         raise ValueError(f"grid {tuple(grid)} has {grid[0] * grid[1] * grid[2]} tokens, tensors have {N}")
-    return make_params(B, H, d, grid, block, _torch_dtype_name(q), feature_map, norm, variant)
+    return make_params(B, H, d, grid, block, _torch_dtype_name(q), feature_map, norm, variant, causal)
 
 
 def mhla_forward(q, k, v, mc, grid, block, norm: str = "divisive", feature_map: str = "elu1",
-                 variant: str = "auto", out=None, workspace=None, stream=None):
+                 variant: str = "auto", out=None, workspace=None, stream=None, causal: bool = False):
     """MHLA forward on CUDA tensors [B, H, N, d]; returns ``out``.
 
     ``mc`` is a float32 [M, M] CUDA tensor.  ``out`` and ``workspace`` are
@@ -187,7 +188,7 @@ def mhla_forward(q, k, v, mc, grid, block, norm: str = "divisive", feature_map: 
     (default: torch's current stream) and does not synchronise.
     """
     import torch
-    p = _params_for(q, grid, block, feature_map, norm, variant)
+    p = _params_for(q, grid, block, feature_map, norm, variant, causal)
     for name, t in (("q", q), ("k", k), ("v", v)):
         if not t.is_cuda or not t.is_contiguous() or t.shape != q.shape or t.dtype != q.dtype:
             raise ValueError(f"{name} must be a contiguous CUDA tensor shaped and typed like q")
@@ -284,7 +285,7 @@ def mhla_forward_noalloc(q, k, v, mc, grid, block, norm: str = "divisive", featu
 
 
 def mhla_forward_host(q, k, v, mc, grid, block, norm: str = "divisive", feature_map: str = "elu1",
-                      variant: str = "auto", out=None, dev_buffer=None, stream=None):
+                      variant: str = "auto", out=None, dev_buffer=None, stream=None, causal: bool = False):
     """End-to-end call on CPU tensors (pinned for asynchronous copies).
 
     Copies the inputs into ``dev_buffer`` (a CUDA uint8 tensor of at least
@@ -292,7 +293,7 @@ def mhla_forward_host(q, k, v, mc, grid, block, norm: str = "divisive", feature_
     result back into ``out``; returns when ``out`` is complete.
     """
     import torch
-    p = _params_for(q, grid, block, feature_map, norm, variant)
+    p = _params_for(q, grid, block, feature_map, norm, variant, causal)
     for name, t in (("q", q), ("k", k), ("v", v), ("mc", mc)):
         if t.is_cuda or not t.is_contiguous():
             raise ValueError(f"{name} must be a contiguous CPU tensor")

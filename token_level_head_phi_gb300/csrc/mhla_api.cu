@@ -96,6 +96,7 @@ mhla_status make_plan(const mhla_params* prm, Plan* p, int split_units = 0) {
   if (prm->variant != MHLA_VARIANT_AUTO && prm->variant != MHLA_VARIANT_SIMT &&
       prm->variant != MHLA_VARIANT_MULTIPASS && prm->variant != MHLA_VARIANT_FUSED)
     return MHLA_ERR_INVALID_ARG;
+  if (prm->causal != 0 && prm->causal != 1) return MHLA_ERR_INVALID_ARG;
 
   const int64_t N64 = (int64_t)prm->grid[0] * prm->grid[1] * prm->grid[2];
   const int64_t BH64 = (int64_t)prm->batch * prm->heads;
@@ -125,8 +126,9 @@ mhla_status make_plan(const mhla_params* prm, Plan* p, int split_units = 0) {
   p->dtype = prm->dtype;
   p->fmap = prm->feature_map;
   p->norm = prm->norm;
+  p->causal = prm->causal;
 
-  const bool tc_ok = prm->dtype == MHLA_DTYPE_BF16 && d == kTcHeadDim;
+  const bool tc_ok = prm->dtype == MHLA_DTYPE_BF16 && d == kTcHeadDim && !prm->causal;
   int variant = prm->variant;
   if (variant == MHLA_VARIANT_AUTO) variant = tc_ok ? MHLA_VARIANT_MULTIPASS : MHLA_VARIANT_SIMT;
   if ((variant == MHLA_VARIANT_MULTIPASS || variant == MHLA_VARIANT_FUSED) && !tc_ok) return MHLA_ERR_UNSUPPORTED;
@@ -172,6 +174,11 @@ mhla_status make_plan(const mhla_params* prm, Plan* p, int split_units = 0) {
     off = align_up(off + sizeof(float) * (size_t)p->BH * p->M * p->R);
     p->off_rowsum = off;
     off = align_up(off + sizeof(float) * (size_t)p->M);
+    if (p->causal) {
+      p->off_mcl = off;
+      off = align_up(off + sizeof(float) * (size_t)p->M * p->M);
+      p->kernels = 5;
+    }
   } else {
     // fused: a ring of heads small enough to stay in L2 (at least two, so
     // that consecutive heads overlap)
@@ -285,6 +292,19 @@ mhla_status run_plan(const Plan& plan, const void* q, const void* k, const void*
   float* mixed = reinterpret_cast<float*>(ws + p.off_mixed);
   float* rowsum = reinterpret_cast<float*>(ws + p.off_rowsum);
   record_event(0, s);
+  if (p.causal) {
+    float* mcl = reinterpret_cast<float*>(ws + p.off_mcl);
+    if ((e = launch_mc_strict_lower(p, mc, mcl, s)) != 0) return cuda_fail((cudaError_t)e);
+    if ((e = launch_mc_rowsum(p, mcl, rowsum, s)) != 0) return cuda_fail((cudaError_t)e);
+    if ((e = launch_simt_summary(p, k, v, stack, s)) != 0) return cuda_fail((cudaError_t)e);
+    record_event(1, s);
+    if ((e = launch_simt_mix(p, mcl, stack, mixed, s)) != 0) return cuda_fail((cudaError_t)e);
+    record_event(2, s);
+    if ((e = launch_simt_causal_output(p, q, k, v, mixed, rowsum, mc, out, s)) != 0)
+      return cuda_fail((cudaError_t)e);
+    record_event(3, s);
+    return MHLA_OK;
+  }
   if ((e = launch_mc_rowsum(p, mc, rowsum, s)) != 0) return cuda_fail((cudaError_t)e);
   if ((e = launch_simt_summary(p, k, v, stack, s)) != 0) return cuda_fail((cudaError_t)e);
   record_event(1, s);
@@ -373,6 +393,7 @@ struct BwdLayout {
 
 mhla_status make_bwd_plan(const mhla_params* prm, Plan* plan, BwdLayout* lay) {
   if (!prm) return MHLA_ERR_INVALID_ARG;
+  if (prm->causal == 1) return MHLA_ERR_UNSUPPORTED;  // forward only
   mhla_params p = *prm;
   const bool tc_ok = p.dtype == MHLA_DTYPE_BF16 && p.head_dim == kTcHeadDim;
   if (p.variant == MHLA_VARIANT_AUTO) p.variant = tc_ok ? MHLA_VARIANT_MULTIPASS : MHLA_VARIANT_SIMT;

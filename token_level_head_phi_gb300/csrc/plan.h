@@ -67,6 +67,7 @@ struct Plan {
   int N, M, nb;   // tokens, blocks, tokens per block
   // options
   int dtype, fmap, norm, variant;
+  int causal;         // block-ordered causal form (float32 kernels only)
   // long blocks are summarised in `splits` pieces of at most `split_len`
   // tokens each; the mixing step sums the pieces (every piece of block b
   // takes the weight Mc[i, b])
@@ -82,6 +83,7 @@ struct Plan {
   // workspace layout: byte offsets from the 256-aligned base
   size_t ws_total;
   size_t off_stack, off_mixed, off_rowsum, off_aux;
+  size_t off_mcl;     // causal: Mc with its diagonal and upper triangle zeroed
   // tensor-core path buffers
   size_t off_stack_lo, off_mixed_lo;
   size_t off_mc_f16, off_mc_scale, off_mc_hi, off_mc_lo, off_blkinfo;
@@ -132,5 +134,11 @@ int launch_simt_summary(const Plan& p, const void* k, const void* v, float* stac
 int launch_simt_mix(const Plan& p, const float* mc, const float* stack, float* mixed, void* stream);
 int launch_simt_output(const Plan& p, const void* q, const float* mixed, const float* rowsum,
                        void* out, void* stream);
+// Causal form: the strict lower triangle of Mc, and the output step that walks
+// each block in order (mixed = the records mixed with that triangle,
+// rowsum_lower = its row sums).
+int launch_mc_strict_lower(const Plan& p, const float* mc, float* mcl, void* stream);
+int launch_simt_causal_output(const Plan& p, const void* q, const void* k, const void* v, const float* mixed,
+                              const float* rowsum_lower, const float* mc, void* out, void* stream);
 
 }  // namespace mhla
