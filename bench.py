@@ -3,7 +3,7 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
                     [--variant auto|simt|multipass|fused] [--impl mine|reference]
                     [--all-workloads] [--no-cpu-baseline] [--pass forward|backward]
-                    [--feature-map elu1|relu|exp]
+                    [--feature-map elu1|relu|exp] [--causal]
 
 A step is one full forward (block summaries, mixing, output) over one batch
 of the workload's seeded synthetic inputs, already resident in HBM.  The
@@ -253,7 +253,8 @@ def run_mine(args, w: wl.Workload, world: int, rank: int, local: int, dist):
     q, k, v = to_dev(qn), to_dev(kn), to_dev(vn)
     mc = torch.from_numpy(mcn).to(dev)
     out = torch.empty_like(q)
-    p = mb.make_params(w.batch, w.heads, w.head_dim, w.grid, w.block, w.dtype, args.feature_map, w.norm, args.variant)
+    p = mb.make_params(w.batch, w.heads, w.head_dim, w.grid, w.block, w.dtype, args.feature_map, w.norm, args.variant,
+                       args.causal)
     info = mb.mhla_plan(p)
     ws = torch.empty(max(info.workspace_bytes, 1), dtype=torch.uint8, device=dev)
     ws_bytes = ws.numel()
@@ -333,10 +334,15 @@ def run_mine(args, w: wl.Workload, world: int, rank: int, local: int, dist):
 
     hbm, tf_burst, tf_sust, peak_kind = load_peaks()
     pbytes = phase_bytes(w, info, info.variant)
+    if args.causal:
+        # the causal output step also reads K and V (the in-block prefix)
+        pbytes["output"] += 2 * q.numel() * q.element_size()
     avg_phase = {ph: statistics.mean(v) for ph, v in phase_ms.items()}
     dom = max(avg_phase, key=avg_phase.get)
     achieved = pbytes[dom] / (avg_phase[dom] / 1e3) / 1e9
     kname, ksrc = PHASE_KERNEL.get(info.variant, {}).get(dom, (dom, None))
+    if args.causal and dom == "output":
+        kname, ksrc = "causal_output_kernel", "token_level_head_phi_gb300/csrc/simt_causal.cu"
     traffic = None
     tt = traffic_table().get((kname, w.name))
     if tt and ksrc and tt[1] == source_hash(ksrc):
@@ -351,7 +357,8 @@ def run_mine(args, w: wl.Workload, world: int, rank: int, local: int, dist):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": w.dtype, "data": "synthetic (seeded normals, locality-biased Mc; no dataset, no weights)",
-        "config": dict(wl.describe(w), feature_map=args.feature_map, variant=mb.mhla_plan(p).variant,
+        "config": dict(wl.describe(w), feature_map=args.feature_map, causal=bool(args.causal),
+                       variant=mb.mhla_plan(p).variant,
                        variant_name={1: "simt", 2: "multipass", 3: "fused"}.get(info.variant, str(info.variant)),
                        l2="no flush: inputs exceed L2" if flush is None else "L2 flushed (256 MB write) between steps, outside per-step events",
                        parallelism=f"replicas{world}" if world > 1 else "single GPU"),
@@ -698,6 +705,7 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--pass", dest="pass_", default="forward", choices=["forward", "backward"])
     ap.add_argument("--feature-map", default="elu1", choices=["elu1", "relu", "exp"])
+    ap.add_argument("--causal", action="store_true", help="block-ordered causal forward (float32 kernels)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
