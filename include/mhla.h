@@ -114,6 +114,11 @@ typedef enum mhla_variant {
   MHLA_VARIANT_FUSED = 3
 } mhla_variant;
 
+/* Memory layout of q, k, v, out (and dout, dq, dk, dv): BHND = [B, H, N, d]
+ * (each head's tokens contiguous); BNHD = [B, N, H, d] (token-major, as a
+ * fused QKV projection writes it: the H heads of a token are adjacent). */
+typedef enum mhla_layout { MHLA_LAYOUT_BHND = 0, MHLA_LAYOUT_BNHD = 1 } mhla_layout;
+
 typedef struct mhla_params {
   int batch;        /* B >= 0                                              */
   int heads;        /* H >= 0                                              */
@@ -133,6 +138,7 @@ typedef struct mhla_params {
                      * the float32 CUDA-core kernels (AUTO picks them;
                      * MULTIPASS/FUSED and mhla_backward return
                      * MHLA_ERR_UNSUPPORTED).                                */
+  int layout;       /* mhla_layout of the token tensors                    */
 } mhla_params;
 
 /* What a call with these parameters will run (for tests and benchmarks). */

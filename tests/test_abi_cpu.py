@@ -84,6 +84,8 @@ BAD = [
     dict(feature_map=-1),
     dict(norm=9),
     dict(variant=11),
+    dict(layout=2),
+    dict(causal=3),
 ]
 
 

@@ -45,6 +45,9 @@ NORMS = {"divisive": NORM_DIVISIVE, "mala": NORM_MALA, "none": NORM_NONE}
 FEATURE_MAPS = {"elu1": FEATURE_ELU1, "identity": FEATURE_IDENTITY, "relu": FEATURE_RELU, "exp": FEATURE_EXP}
 VARIANTS = {"auto": VARIANT_AUTO, "simt": VARIANT_SIMT, "multipass": VARIANT_MULTIPASS, "fused": VARIANT_FUSED}
 DTYPES = {"bf16": DTYPE_BF16, "f32": DTYPE_F32}
+LAYOUT_BHND = 0
+LAYOUT_BNHD = 1
+LAYOUTS = {"bhnd": LAYOUT_BHND, "bnhd": LAYOUT_BNHD}
 
 
 class MhlaError(RuntimeError):
@@ -61,7 +64,7 @@ class MhlaParams(ctypes.Structure):
         ("batch", ctypes.c_int), ("heads", ctypes.c_int), ("head_dim", ctypes.c_int),
         ("grid", ctypes.c_int * 3), ("block", ctypes.c_int * 3),
         ("dtype", ctypes.c_int), ("feature_map", ctypes.c_int), ("norm", ctypes.c_int),
-        ("variant", ctypes.c_int), ("causal", ctypes.c_int),
+        ("variant", ctypes.c_int), ("causal", ctypes.c_int), ("layout", ctypes.c_int),
     ]
 
 
@@ -129,7 +132,7 @@ def _check(status: int, where: str):
 
 def make_params(batch: int, heads: int, head_dim: int, grid: Sequence[int], block: Sequence[int],
                 dtype: str = "bf16", feature_map: str = "elu1", norm: str = "divisive",
-                variant: str = "auto", causal: bool = False) -> MhlaParams:
+                variant: str = "auto", causal: bool = False, layout: str = "bhnd") -> MhlaParams:
     p = MhlaParams()
     p.batch, p.heads, p.head_dim = int(batch), int(heads), int(head_dim)
     for i in range(3):
@@ -140,6 +143,7 @@ def make_params(batch: int, heads: int, head_dim: int, grid: Sequence[int], bloc
     p.norm = NORMS[norm] if isinstance(norm, str) else int(norm)
     p.variant = VARIANTS[variant] if isinstance(variant, str) else int(variant)
     p.causal = int(causal)
+    p.layout = LAYOUTS[layout] if isinstance(layout, str) else int(layout)
     return p
 
 
@@ -170,17 +174,21 @@ def _torch_dtype_name(t) -> str:
     raise TypeError(f"unsupported dtype {t.dtype}; MHLA takes bfloat16 or float32")
 
 
-def _params_for(q, grid, block, feature_map, norm, variant, causal=False) -> MhlaParams:
+def _params_for(q, grid, block, feature_map, norm, variant, causal=False, layout="bhnd") -> MhlaParams:
     if q.dim() != 4:
-        raise ValueError("q, k, v must be [B, H, N, d]")
-    B, H, N, d = q.shape
+        raise ValueError("q, k, v must be [B, H, N, d] (layout 'bhnd') or [B, N, H, d] (layout 'bnhd')")
+    if layout == "bnhd":
+        B, N, H, d = q.shape
+    else:
+        B, H, N, d = q.shape
     if grid[0] * grid[1] * grid[2] != N:
         raise ValueError(f"grid {tuple(grid)} has {grid[0] * grid[1] * grid[2]} tokens, tensors have {N}")
-    return make_params(B, H, d, grid, block, _torch_dtype_name(q), feature_map, norm, variant, causal)
+    return make_params(B, H, d, grid, block, _torch_dtype_name(q), feature_map, norm, variant, causal, layout)
 
 
 def mhla_forward(q, k, v, mc, grid, block, norm: str = "divisive", feature_map: str = "elu1",
-                 variant: str = "auto", out=None, workspace=None, stream=None, causal: bool = False):
+                 variant: str = "auto", out=None, workspace=None, stream=None, causal: bool = False,
+                 layout: str = "bhnd"):
     """MHLA forward on CUDA tensors [B, H, N, d]; returns ``out``.
 
     ``mc`` is a float32 [M, M] CUDA tensor.  ``out`` and ``workspace`` are
@@ -188,7 +196,7 @@ def mhla_forward(q, k, v, mc, grid, block, norm: str = "divisive", feature_map: 
     (default: torch's current stream) and does not synchronise.
     """
     import torch
-    p = _params_for(q, grid, block, feature_map, norm, variant, causal)
+    p = _params_for(q, grid, block, feature_map, norm, variant, causal, layout)
     for name, t in (("q", q), ("k", k), ("v", v)):
         if not t.is_cuda or not t.is_contiguous() or t.shape != q.shape or t.dtype != q.dtype:
             raise ValueError(f"{name} must be a contiguous CUDA tensor shaped and typed like q")
@@ -218,7 +226,8 @@ def mhla_backward_workspace_bytes(p: MhlaParams) -> int:
 
 
 def mhla_backward(q, k, v, mc, dout, grid, block, norm: str = "divisive", feature_map: str = "elu1",
-                  dq=None, dk=None, dv=None, dmc=None, workspace=None, stream=None, variant: str = "auto"):
+                  dq=None, dk=None, dv=None, dmc=None, workspace=None, stream=None, variant: str = "auto",
+                  layout: str = "bhnd"):
     """Gradients of sum(dout * mhla_forward(q, k, v, mc)): returns (dq, dk, dv, dmc).
 
     dq, dk, dv are shaped and typed like q; dmc is float32 [M, M] (summed
@@ -228,7 +237,7 @@ def mhla_backward(q, k, v, mc, dout, grid, block, norm: str = "divisive", featur
     cores) or "simt" (float32 CUDA cores).
     """
     import torch
-    p = _params_for(q, grid, block, feature_map, norm, variant)
+    p = _params_for(q, grid, block, feature_map, norm, variant, False, layout)
     for name, t in (("q", q), ("k", k), ("v", v), ("dout", dout)):
         if not t.is_cuda or not t.is_contiguous() or t.shape != q.shape or t.dtype != q.dtype:
             raise ValueError(f"{name} must be a contiguous CUDA tensor shaped and typed like q")
@@ -266,13 +275,13 @@ def mhla_forward_raw(q_ptr: int, k_ptr: int, v_ptr: int, mc_ptr: int, p: MhlaPar
 
 
 def mhla_forward_noalloc(q, k, v, mc, grid, block, norm: str = "divisive", feature_map: str = "elu1",
-                         variant: str = "auto", out=None, stream=None):
+                         variant: str = "auto", out=None, stream=None, layout: str = "bhnd"):
     """mhla_forward without any device allocation by the library: its scratch
     is a static 32 MiB device array (see include/mhla.h).  For callers that
     cannot allocate at call time; ``out`` must be given by such callers (when
     it is None this wrapper allocates it with torch, for convenience)."""
     import torch
-    p = _params_for(q, grid, block, feature_map, norm, variant)
+    p = _params_for(q, grid, block, feature_map, norm, variant, False, layout)
     if out is None:
         out = torch.empty_like(q)
     if stream is None:
@@ -285,7 +294,8 @@ def mhla_forward_noalloc(q, k, v, mc, grid, block, norm: str = "divisive", featu
 
 
 def mhla_forward_host(q, k, v, mc, grid, block, norm: str = "divisive", feature_map: str = "elu1",
-                      variant: str = "auto", out=None, dev_buffer=None, stream=None, causal: bool = False):
+                      variant: str = "auto", out=None, dev_buffer=None, stream=None, causal: bool = False,
+                      layout: str = "bhnd"):
     """End-to-end call on CPU tensors (pinned for asynchronous copies).
 
     Copies the inputs into ``dev_buffer`` (a CUDA uint8 tensor of at least
@@ -293,7 +303,7 @@ def mhla_forward_host(q, k, v, mc, grid, block, norm: str = "divisive", feature_
     result back into ``out``; returns when ``out`` is complete.
     """
     import torch
-    p = _params_for(q, grid, block, feature_map, norm, variant, causal)
+    p = _params_for(q, grid, block, feature_map, norm, variant, causal, layout)
     for name, t in (("q", q), ("k", k), ("v", v), ("mc", mc)):
         if t.is_cuda or not t.is_contiguous():
             raise ValueError(f"{name} must be a contiguous CPU tensor")

@@ -71,7 +71,6 @@ bwd_output_kernel(Plan p, const T* __restrict__ Q, const T* __restrict__ dO, con
   const float* mrow = mixed + ((size_t)u * p.M + i) * p.R;
   for (int e = tid; e < D * D + 2 * D; e += kThreads) sm[e] = mrow[e];
   const float ntilde = (float)p.nb * rowsum[i];
-  const size_t base = (size_t)u * p.N * D;
 
   float acc[PER];
 #pragma unroll
@@ -85,7 +84,7 @@ bwd_output_kernel(Plan p, const T* __restrict__ Q, const T* __restrict__ dO, con
       const int tt = e / D, f = e % D;
       float qx = 0.f, gx = 0.f;
       if (tt < cnt) {
-        const size_t off = base + (size_t)block_token(p, i, lt + tt) * D + f;
+        const size_t off = tok_off(p, u, block_token(p, i, lt + tt)) + f;
         qx = phi_apply(to_f32(Q[off]), p.fmap);
         gx = to_f32(dO[off]);
       }
@@ -141,7 +140,7 @@ bwd_output_kernel(Plan p, const T* __restrict__ Q, const T* __restrict__ dO, con
       const int tt = e / D, k = e % D;
       float a = sz[k] * sds[tt];
       for (int c = 0; c < D; ++c) a = fmaf(sS[k * D + c], sdn[tt * D + c], a);
-      const size_t off = base + (size_t)block_token(p, i, lt + tt) * D + k;
+      const size_t off = tok_off(p, u, block_token(p, i, lt + tt)) + k;
       dQ[off] = from_f32<T>(a * phi_grad(to_f32(Q[off]), p.fmap));
     }
     // partial dS~ += phi(q) dnum^T, dz~ += ds phi(q); MALA: dv~, dn~
@@ -155,7 +154,7 @@ bwd_output_kernel(Plan p, const T* __restrict__ Q, const T* __restrict__ dO, con
         zacc = fmaf(sds[tt], sq[tt * D + tid], zacc);
       } else if (tid < 2 * D && p.norm == MHLA_NORM_MALA) {
         // dv~ = -sum_t gamma_t dO_t (the tile's dO was overwritten above)
-        const size_t off = base + (size_t)block_token(p, i, lt + tt) * D + (tid - D);
+        const size_t off = tok_off(p, u, block_token(p, i, lt + tt)) + (tid - D);
         vacc = fmaf(-sgam[tt], to_f32(dO[off]), vacc);
       }
       if (tid == 0 && p.norm == MHLA_NORM_MALA)
@@ -302,7 +301,6 @@ bwd_summary_kernel(Plan p, const T* __restrict__ K, const T* __restrict__ V, con
   const int tid = threadIdx.x;
   const float* drow = dstack + ((size_t)u * p.M + b) * p.R;
   for (int e = tid; e < D * D + 2 * D; e += kThreads) sm[e] = drow[e];
-  const size_t base = (size_t)u * p.N * D;
   for (int lt = l0; lt < l1; lt += kTile) {
     const int cnt = min(kTile, l1 - lt);
     __syncthreads();
@@ -310,7 +308,7 @@ bwd_summary_kernel(Plan p, const T* __restrict__ K, const T* __restrict__ V, con
       const int tt = e / D, f = e % D;
       float kx = 0.f, vx = 0.f;
       if (tt < cnt) {
-        const size_t off = base + (size_t)block_token(p, b, lt + tt) * D + f;
+        const size_t off = tok_off(p, u, block_token(p, b, lt + tt)) + f;
         kx = phi_apply(to_f32(K[off]), p.fmap);
         vx = to_f32(V[off]);
       }
@@ -325,7 +323,7 @@ bwd_summary_kernel(Plan p, const T* __restrict__ K, const T* __restrict__ V, con
         gk = fmaf(sS[f * D + m], sx[tt * D + m], gk);   // (dS_b v_j)[f]
         gv = fmaf(sS[m * D + f], sk[tt * D + m], gv);   // (dS_b^T phi(k_j))[f]
       }
-      const size_t off = base + (size_t)block_token(p, b, lt + tt) * D + f;
+      const size_t off = tok_off(p, u, block_token(p, b, lt + tt)) + f;
       dK[off] = from_f32<T>(gk * phi_grad(to_f32(K[off]), p.fmap));
       dV[off] = from_f32<T>(gv);
     }

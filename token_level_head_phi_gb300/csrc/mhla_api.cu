@@ -97,6 +97,7 @@ mhla_status make_plan(const mhla_params* prm, Plan* p, int split_units = 0) {
       prm->variant != MHLA_VARIANT_MULTIPASS && prm->variant != MHLA_VARIANT_FUSED)
     return MHLA_ERR_INVALID_ARG;
   if (prm->causal != 0 && prm->causal != 1) return MHLA_ERR_INVALID_ARG;
+  if (prm->layout != MHLA_LAYOUT_BHND && prm->layout != MHLA_LAYOUT_BNHD) return MHLA_ERR_INVALID_ARG;
 
   const int64_t N64 = (int64_t)prm->grid[0] * prm->grid[1] * prm->grid[2];
   const int64_t BH64 = (int64_t)prm->batch * prm->heads;
@@ -127,6 +128,8 @@ mhla_status make_plan(const mhla_params* prm, Plan* p, int split_units = 0) {
   p->fmap = prm->feature_map;
   p->norm = prm->norm;
   p->causal = prm->causal;
+  p->layout = prm->layout;
+  p->f_h = make_fastdiv((uint32_t)(p->H > 0 ? p->H : 1));
 
   const bool tc_ok = prm->dtype == MHLA_DTYPE_BF16 && d == kTcHeadDim && !prm->causal;
   int variant = prm->variant;
@@ -335,16 +338,23 @@ HostGroups host_groups(const Plan& plan) {
   if (n < 1) n = 1;
   HostGroups g;
   g.per = (plan.BH + n - 1) / n;
+  // token-major tensors are contiguous per batch only: whole batches per group
+  if (plan.layout == MHLA_LAYOUT_BNHD && plan.H > 0) g.per = (g.per + plan.H - 1) / plan.H * plan.H;
   g.n = (plan.BH + g.per - 1) / g.per;
   return g;
 }
 
 // The parameters of a group of `units` (batch, head) pairs: one batch of
-// `units` heads (the kernels see only the flattened unit index).
+// `units` heads (the kernels see only the flattened unit index), or for
+// token-major tensors units / H batches of H heads.
 mhla_params group_params(const mhla_params* p, int units) {
   mhla_params g = *p;
-  g.batch = 1;
-  g.heads = units;
+  if (p->layout == MHLA_LAYOUT_BNHD && p->heads > 0) {
+    g.batch = units / p->heads;
+  } else {
+    g.batch = 1;
+    g.heads = units;
+  }
   return g;
 }
 

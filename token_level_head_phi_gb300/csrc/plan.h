@@ -68,6 +68,8 @@ struct Plan {
   // options
   int dtype, fmap, norm, variant;
   int causal;         // block-ordered causal form (float32 kernels only)
+  int layout;         // MHLA_LAYOUT_BHND or MHLA_LAYOUT_BNHD for q, k, v, out (and gradients)
+  FastDiv f_h;        // division by H (unit -> batch, head)
   // long blocks are summarised in `splits` pieces of at most `split_len`
   // tokens each; the mixing step sums the pieces (every piece of block b
   // takes the weight Mc[i, b])
@@ -110,6 +112,42 @@ __host__ __device__ inline void chunk_origin(const Plan& p, const ChunkShape& ch
   x0 = (int)(bx * p.bw + cx * ch.cw);
   y0 = (int)(by * p.bh + cy * ch.ch);
   t0 = (int)(bz * p.bt + cz * ch.ct);
+}
+
+// Element offset of feature 0 of token t of unit u = b * H + h in q, k, v
+// and the outputs: [B, H, N, d] (BHND) or [B, N, H, d] (BNHD, token-major as
+// a fused QKV projection writes it).
+__host__ __device__ inline size_t tok_off(const Plan& p, int u, int t) {
+  if (p.layout == MHLA_LAYOUT_BHND) return ((size_t)u * p.N + t) * p.d;
+  const int b = (int)fdiv((uint32_t)u, p.f_h), h = u - b * p.H;
+  return (((size_t)b * p.N + t) * p.H + h) * p.d;
+}
+
+// Coordinates of the token tile of unit u whose corner is grid position
+// (x0, y0, t0), in the 5D tensor maps encode_token_map builds:
+//   BHND: axes (feature, x, y, t, unit)        -> (0, x0, y0, t0, u)
+//   BNHD: axes (feature, head, x, y, batch*T+t) -> (0, h, x0, y0, b T + t0)
+// (token-major: the head axis sits right after the features, and batch and
+// time share one axis because a batch is N = T Hg Wg token rows).
+struct TileCoords {
+  int c[5];
+};
+__host__ __device__ inline TileCoords token_tile_coords(const Plan& p, int u, int x0, int y0, int t0) {
+  TileCoords r;
+  r.c[0] = 0;
+  if (p.layout == MHLA_LAYOUT_BHND) {
+    r.c[1] = x0;
+    r.c[2] = y0;
+    r.c[3] = t0;
+    r.c[4] = u;
+  } else {
+    const int b = (int)fdiv((uint32_t)u, p.f_h);
+    r.c[1] = u - b * p.H;
+    r.c[2] = x0;
+    r.c[3] = y0;
+    r.c[4] = b * p.T + t0;
+  }
+  return r;
 }
 
 // Global token index (within one head) of local token l of block b.  Local

@@ -34,7 +34,6 @@ simt_summary_kernel(Plan p, const Tin* __restrict__ K, const Tin* __restrict__ V
   const int b = row / p.splits;
   const int l0 = (row % p.splits) * p.split_len;
   const int l1 = min(p.nb, l0 + p.split_len);
-  const size_t base = (size_t)u * p.N * D;
   const int tid = threadIdx.x;
 
   float acc[PER];
@@ -49,7 +48,7 @@ simt_summary_kernel(Plan p, const Tin* __restrict__ K, const Tin* __restrict__ V
       const int tt = e / D, f = e % D;
       float kx = 0.f, vx = 0.f;
       if (tt < cnt) {
-        const size_t off = base + (size_t)block_token(p, b, lt + tt) * D + f;
+        const size_t off = tok_off(p, u, block_token(p, b, lt + tt)) + f;
         kx = phi_apply(to_f32(K[off]), p.fmap);
         vx = to_f32(V[off]);
       }
@@ -153,11 +152,10 @@ simt_output_kernel(Plan p, const Tin* __restrict__ Q, const float* __restrict__ 
   const int tid = threadIdx.x;
   const float* mrow = mixed + ((size_t)u * p.M + i) * p.R;
   for (int e = tid; e < D * D + 2 * D; e += kThreads) sm[e] = mrow[e];
-  const size_t base = (size_t)u * p.N * D;
   for (int e = tid; e < TQ * D; e += kThreads) {
     const int tt = e / D, f = e % D;
     float x = 0.f;
-    if (tt < cnt) x = phi_apply(to_f32(Q[base + (size_t)block_token(p, i, l0 + tt) * D + f]), p.fmap);
+    if (tt < cnt) x = phi_apply(to_f32(Q[tok_off(p, u, block_token(p, i, l0 + tt)) + f]), p.fmap);
     sq[e] = x;
   }
   __syncthreads();
@@ -185,7 +183,7 @@ simt_output_kernel(Plan p, const Tin* __restrict__ Q, const float* __restrict__ 
     } else {
       o = a;
     }
-    out[base + (size_t)block_token(p, i, l0 + tt) * D + c] = from_f32<Tin>(o);
+    out[tok_off(p, u, block_token(p, i, l0 + tt)) + c] = from_f32<Tin>(o);
   }
 }
 

@@ -54,7 +54,6 @@ causal_output_kernel(Plan p, const T* __restrict__ Q, const T* __restrict__ K, c
   const float* mrow = mixed + ((size_t)u * p.M + i) * p.R;
   for (int e = tid; e < D * D + 2 * D; e += kThreads) sm[e] = mrow[e];
   float n_state = (float)p.nb * rowsum_lower[i];   // n<_i
-  const size_t base = (size_t)u * p.N * D;
 
   for (int l0 = 0; l0 < p.nb; l0 += kTQ) {
     const int cnt = min(kTQ, p.nb - l0);
@@ -63,7 +62,7 @@ causal_output_kernel(Plan p, const T* __restrict__ Q, const T* __restrict__ K, c
       const int tt = e / D, f = e % D;
       float qx = 0.f, kx = 0.f, vx = 0.f;
       if (tt < cnt) {
-        const size_t off = base + (size_t)block_token(p, i, l0 + tt) * D + f;
+        const size_t off = tok_off(p, u, block_token(p, i, l0 + tt)) + f;
         qx = phi_apply(to_f32(Q[off]), p.fmap);
         kx = phi_apply(to_f32(K[off]), p.fmap);
         vx = to_f32(V[off]);
@@ -109,7 +108,7 @@ causal_output_kernel(Plan p, const T* __restrict__ Q, const T* __restrict__ K, c
         const float vt = sv[c] + w * vloc;
         o = s != 0.f ? (1.f + 1.f / s) * num - (s / ntil) * vt : 0.f;
       }
-      out[base + (size_t)block_token(p, i, l0 + tt) * D + c] = from_f32<T>(o);
+      out[tok_off(p, u, block_token(p, i, l0 + tt)) + c] = from_f32<T>(o);
     }
     __syncthreads();
     // advance the state by the whole tile: S += w sum_j phi(k_j) v_j^T (z, v, n)

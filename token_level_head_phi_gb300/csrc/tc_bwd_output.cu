@@ -242,9 +242,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_output_kernel(const __grid
         if (!mbar_wait(tempty(s), par ^ 1u, a.err, 0x801, abort_flag)) break;
         int x0, y0, t0;
         chunk_origin(p, a.c, (uint32_t)it.i, (uint32_t)it.c, x0, y0, t0);
+        const TileCoords g5 = token_tile_coords(p, it.u, x0, y0, t0);
         mbar_arrive_expect_tx(tfull(s), 2 * bytes);
-        tma_load_5d(tst(s), &a.tmQ, tfull(s), 0, x0, y0, t0, it.u, pol);
-        tma_load_5d(tst(s) + kTile, &a.tmG, tfull(s), 0, x0, y0, t0, it.u, pol);
+        tma_load_5d(tst(s), &a.tmQ, tfull(s), g5.c[0], g5.c[1], g5.c[2], g5.c[3], g5.c[4], pol);
+        tma_load_5d(tst(s) + kTile, &a.tmG, tfull(s), g5.c[0], g5.c[1], g5.c[2], g5.c[3], g5.c[4], pol);
         ++issued;
       }
       drain_loads(tfull(0), kStages, issued, a.err, 0x802);
@@ -604,7 +605,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_output_kernel(const __grid
       if (et == 0) {
         int x0, y0, t0;
         chunk_origin(p, a.c, (uint32_t)it.i, (uint32_t)it.c, x0, y0, t0);
-        tma_store_5d(&a.tmDQ, tst(s), 0, x0, y0, t0, it.u);
+        const TileCoords g5 = token_tile_coords(p, it.u, x0, y0, t0);
+        tma_store_5d(&a.tmDQ, tst(s), g5.c[0], g5.c[1], g5.c[2], g5.c[3], g5.c[4]);
         bulk_commit();
         bulk_wait_read<0>();
         mbar_arrive(tempty(s));
@@ -686,13 +688,10 @@ int launch_tc_bwd_output(const Plan& p, const void* q, const void* dout, const _
   BoArgs a;
   memset(&a, 0, sizeof(a));
   const ChunkShape& c = p.chunk;
-  const uint64_t dims5[5] = {64, (uint64_t)p.Wg, (uint64_t)p.Hg, (uint64_t)p.T, (uint64_t)p.BH};
-  const uint64_t str5[4] = {128, 128ull * p.Wg, 128ull * p.Wg * p.Hg, 128ull * p.N};
-  const uint32_t box5[5] = {64, (uint32_t)c.cw, (uint32_t)c.ch, (uint32_t)c.ct, 1};
   int e;
-  if ((e = encode_tmap_bf16(&a.tmQ, q, 5, dims5, str5, box5)) != 0) return e;
-  if ((e = encode_tmap_bf16(&a.tmG, dout, 5, dims5, str5, box5)) != 0) return e;
-  if ((e = encode_tmap_bf16(&a.tmDQ, dq, 5, dims5, str5, box5)) != 0) return e;
+  if ((e = encode_token_map(&a.tmQ, p, q, c)) != 0) return e;
+  if ((e = encode_token_map(&a.tmG, p, dout, c)) != 0) return e;
+  if ((e = encode_token_map(&a.tmDQ, p, dq, c)) != 0) return e;
   const uint64_t dims3[3] = {64, (uint64_t)(p.R / 64), (uint64_t)p.BH * p.M};
   const uint64_t str3[2] = {128, 2ull * p.R};
   const uint32_t box3[3] = {64, 64, 1};

@@ -170,9 +170,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_summary_kernel(const __gri
         sum_unit(p, a, w, u, b, c);
         if (!mbar_wait(kvempty(s), ph ^ 1u, a.err, 0x701, abort_flag)) break;
         chunk_origin(p, a.c, (uint32_t)b, (uint32_t)c, x0, y0, t0);
+        const TileCoords g5 = token_tile_coords(p, u, x0, y0, t0);
         mbar_arrive_expect_tx(kvfull(s), 2 * bytes);
-        tma_load_5d(kst(s), &a.tmK, kvfull(s), 0, x0, y0, t0, u, pol);
-        tma_load_5d(kst(s) + kTile, &a.tmV, kvfull(s), 0, x0, y0, t0, u, pol);
+        tma_load_5d(kst(s), &a.tmK, kvfull(s), g5.c[0], g5.c[1], g5.c[2], g5.c[3], g5.c[4], pol);
+        tma_load_5d(kst(s) + kTile, &a.tmV, kvfull(s), g5.c[0], g5.c[1], g5.c[2], g5.c[3], g5.c[4], pol);
         ++issued;
         if (++s == kStages) {
           s = 0;
@@ -383,8 +384,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_summary_kernel(const __gri
         mbar_arrive(accempty(acc));
         int x0, y0, t0;
         chunk_origin(p, a.c, (uint32_t)b, (uint32_t)c, x0, y0, t0);
-        tma_store_5d(&a.tmDK, kst(s), 0, x0, y0, t0, u);
-        tma_store_5d(&a.tmDV, kst(s) + kTile, 0, x0, y0, t0, u);
+        const TileCoords g5 = token_tile_coords(p, u, x0, y0, t0);
+        tma_store_5d(&a.tmDK, kst(s), g5.c[0], g5.c[1], g5.c[2], g5.c[3], g5.c[4]);
+        tma_store_5d(&a.tmDV, kst(s) + kTile, g5.c[0], g5.c[1], g5.c[2], g5.c[3], g5.c[4]);
         bulk_commit();
         bulk_wait_read<kPendStores - 1>();
         if (n_out >= kPendStores - 1) mbar_arrive(kvempty((s + kStages - (kPendStores - 1)) % kStages));
@@ -414,14 +416,11 @@ int launch_tc_bwd_summary(const Plan& p, const void* k, const void* v, const __n
   SumArgs a;
   memset(&a, 0, sizeof(a));
   const ChunkShape& c = p.chunk;
-  const uint64_t dims5[5] = {64, (uint64_t)p.Wg, (uint64_t)p.Hg, (uint64_t)p.T, (uint64_t)p.BH};
-  const uint64_t str5[4] = {128, 128ull * p.Wg, 128ull * p.Wg * p.Hg, 128ull * p.N};
-  const uint32_t box5[5] = {64, (uint32_t)c.cw, (uint32_t)c.ch, (uint32_t)c.ct, 1};
   int e;
-  if ((e = encode_tmap_bf16(&a.tmK, k, 5, dims5, str5, box5)) != 0) return e;
-  if ((e = encode_tmap_bf16(&a.tmV, v, 5, dims5, str5, box5)) != 0) return e;
-  if ((e = encode_tmap_bf16(&a.tmDK, dk, 5, dims5, str5, box5)) != 0) return e;
-  if ((e = encode_tmap_bf16(&a.tmDV, dv, 5, dims5, str5, box5)) != 0) return e;
+  if ((e = encode_token_map(&a.tmK, p, k, c)) != 0) return e;
+  if ((e = encode_token_map(&a.tmV, p, v, c)) != 0) return e;
+  if ((e = encode_token_map(&a.tmDK, p, dk, c)) != 0) return e;
+  if ((e = encode_token_map(&a.tmDV, p, dv, c)) != 0) return e;
   const uint64_t dims3[3] = {64, (uint64_t)(p.R / 64), (uint64_t)p.BH * p.M};
   const uint64_t str3[2] = {128, 2ull * p.R};
   const uint32_t box3[3] = {64, 64, 1};

@@ -33,6 +33,10 @@ inline int encode_tmap_bf16(CUtensorMap* map, const void* base, int rank, const 
   return encode_tmap(map, base, rank, dims, strides_bytes, box, false);
 }
 int num_sms();
+// 5D map over q, k, v, an output or a gradient tensor in the plan's layout,
+// box = one token chunk (64, cw, ch, ct, 1); see unit_coords for the
+// coordinates.
+int encode_token_map(CUtensorMap* map, const Plan& p, const void* base, const ChunkShape& c);
 
 ChunkShape choose_chunk(const Plan& p);
 

@@ -36,12 +36,9 @@ int build_output_args(const Plan& p, const ChunkShape& c, const void* q, const T
                       ot::OutArgs* args) {
   OutArgs& a = *args;
   memset(&a, 0, sizeof(a));
-  const uint64_t dims5[5] = {64, (uint64_t)p.Wg, (uint64_t)p.Hg, (uint64_t)p.T, (uint64_t)p.BH};
-  const uint64_t str5[4] = {128, 128ull * p.Wg, 128ull * p.Wg * p.Hg, 128ull * p.N};
-  const uint32_t box5[5] = {64, (uint32_t)c.cw, (uint32_t)c.ch, (uint32_t)c.ct, 1};
   int e;
-  if ((e = encode_tmap_bf16(&a.tmQ, q, 5, dims5, str5, box5)) != 0) return e;
-  if ((e = encode_tmap_bf16(&a.tmO, out, 5, dims5, str5, box5)) != 0) return e;
+  if ((e = encode_token_map(&a.tmQ, p, q, c)) != 0) return e;
+  if ((e = encode_token_map(&a.tmO, p, out, c)) != 0) return e;
   const uint64_t dims3[3] = {64, (uint64_t)(p.R / 64), (uint64_t)slots * p.M};
   const uint64_t str3[2] = {128, 2ull * p.R};
   const uint32_t box3[3] = {64, 64, 1};

@@ -177,8 +177,9 @@ __device__ __forceinline__ void output_body(const OutArgs& a, const Plan& p, con
         out_unit(p, a, w, u, i, c);
         if (!mbar_wait(qempty(s), ph ^ 1u, a.err, 0x301, abort_flag)) break;
         chunk_origin(p, a.c, (uint32_t)i, (uint32_t)c, x0, y0, t0);
+        const TileCoords g5 = token_tile_coords(p, u, x0, y0, t0);
         mbar_arrive_expect_tx(qfull(s), bytes);
-        tma_load_5d(qst(s), &a.tmQ, qfull(s), 0, x0, y0, t0, u, pol_q);
+        tma_load_5d(qst(s), &a.tmQ, qfull(s), g5.c[0], g5.c[1], g5.c[2], g5.c[3], g5.c[4], pol_q);
         ++issued;
         if (++s == kQStages) {
           s = 0;
@@ -395,7 +396,8 @@ __device__ __forceinline__ void output_body(const OutArgs& a, const Plan& p, con
         mbar_arrive(bempty(b));
         int x0, y0, t0;
         chunk_origin(p, a.c, (uint32_t)i, (uint32_t)c, x0, y0, t0);
-        tma_store_5d(&a.tmO, qst(s), 0, x0, y0, t0, u);
+        const TileCoords g5 = token_tile_coords(p, u, x0, y0, t0);
+        tma_store_5d(&a.tmO, qst(s), g5.c[0], g5.c[1], g5.c[2], g5.c[3], g5.c[4]);
         bulk_commit();
         // this CTA's units of head u have read their S~_i (the slot may be
         // reused once every unit has)

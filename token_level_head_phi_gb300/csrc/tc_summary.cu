@@ -37,12 +37,9 @@ int build_summary_args(const Plan& p, const ChunkShape& c, const void* k, const 
                        int slots, sm::SummaryArgs* out) {
   SummaryArgs& a = *out;
   memset(&a, 0, sizeof(a));
-  const uint64_t dims5[5] = {64, (uint64_t)p.Wg, (uint64_t)p.Hg, (uint64_t)p.T, (uint64_t)p.BH};
-  const uint64_t str5[4] = {128, 128ull * p.Wg, 128ull * p.Wg * p.Hg, 128ull * p.N};
-  const uint32_t box5[5] = {64, (uint32_t)c.cw, (uint32_t)c.ch, (uint32_t)c.ct, 1};
   int e;
-  if ((e = encode_tmap_bf16(&a.tmK, k, 5, dims5, str5, box5)) != 0) return e;
-  if ((e = encode_tmap_bf16(&a.tmV, v, 5, dims5, str5, box5)) != 0) return e;
+  if ((e = encode_token_map(&a.tmK, p, k, c)) != 0) return e;
+  if ((e = encode_token_map(&a.tmV, p, v, c)) != 0) return e;
   // the stack holds `slots` heads: every head (standalone) or a ring (fused)
   const uint64_t stack_rows = (uint64_t)slots * p.M * p.splits * 66ull;
   const uint64_t dims2[2] = {64, stack_rows};

@@ -214,10 +214,11 @@ __device__ __forceinline__ void summary_body(const SummaryArgs& a, const Plan& p
           if (!(ok = mbar_wait(empty(stage), phase ^ 1u, a.err, 0x101, abort_flag))) break;
           int x0, y0, t0;
           chunk_origin(p, a.c, uc.b, c, x0, y0, t0);
+          const TileCoords g5 = token_tile_coords(p, uc.u, x0, y0, t0);
           const uint32_t kt = base + (uint32_t)stage * kStageBytes;
           mbar_arrive_expect_tx(full(stage), bytes);
-          tma_load_5d(kt, &a.tmK, full(stage), 0, x0, y0, t0, uc.u, pol);
-          tma_load_5d(kt + kTile, &a.tmV, full(stage), 0, x0, y0, t0, uc.u, pol);
+          tma_load_5d(kt, &a.tmK, full(stage), g5.c[0], g5.c[1], g5.c[2], g5.c[3], g5.c[4], pol);
+          tma_load_5d(kt + kTile, &a.tmV, full(stage), g5.c[0], g5.c[1], g5.c[2], g5.c[3], g5.c[4], pol);
           ++issued;
           if (++stage == kStages) {
             stage = 0;

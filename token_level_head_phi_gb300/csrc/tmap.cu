@@ -66,6 +66,22 @@ int encode_impl(CUtensorMap* map, const void* base, int rank, const uint64_t* di
 }
 }  // namespace
 
+int encode_token_map(CUtensorMap* map, const Plan& p, const void* base, const ChunkShape& c) {
+  const uint32_t box[5] = {64, (uint32_t)c.cw, (uint32_t)c.ch, (uint32_t)c.ct, 1};
+  if (p.layout == MHLA_LAYOUT_BHND) {
+    const uint64_t dims[5] = {64, (uint64_t)p.Wg, (uint64_t)p.Hg, (uint64_t)p.T, (uint64_t)p.BH};
+    const uint64_t str[4] = {128, 128ull * p.Wg, 128ull * p.Wg * p.Hg, 128ull * p.N};
+    return encode_tmap_bf16(map, base, 5, dims, str, box);
+  }
+  // token-major: the head axis (128 bytes) comes right after the features, a
+  // token row is H * 128 bytes, (batch, time) share one axis of Hg * Wg rows
+  const uint32_t box_t[5] = {64, 1, (uint32_t)c.cw, (uint32_t)c.ch, (uint32_t)c.ct};
+  const uint64_t row = 128ull * p.H;
+  const uint64_t dims[5] = {64, (uint64_t)p.H, (uint64_t)p.Wg, (uint64_t)p.Hg, (uint64_t)p.T * p.B};
+  const uint64_t str[4] = {128, row, row * p.Wg, row * p.Wg * p.Hg};
+  return encode_tmap_bf16(map, base, 5, dims, str, box_t);
+}
+
 ChunkShape choose_chunk(const Plan& p) {
   auto largest_divisor = [](int n, int limit) {
     for (int d = limit < n ? limit : n; d >= 1; --d)
