@@ -43,7 +43,7 @@ from __future__ import annotations
 import numpy as np
 
 from .mhla_oracle import (DIVISIVE, ELU1, EXP, IDENTITY, MALA, NONE, RELU, block_of_token, block_summaries,
-                          feature_map, mix)
+                          feature_map, head_mc, mix)
 
 
 def feature_map_grad(x, kind: str = ELU1) -> np.ndarray:
@@ -193,8 +193,9 @@ def mhla_bruteforce_backward64(q, k, v, mc, grid, block, dout, fmap: str = ELU1,
 
 
 def mhla_backward64(q, k, v, mc, grid, block, dout, fmap: str = ELU1, norm: str = DIVISIVE):
-    """Gradients over [B, H, N, d] inputs: dq, dk, dv [B, H, N, d] and dmc [M, M]
-    summed over every (batch, head) (one Mc is shared by all of them)."""
+    """Gradients over [B, H, N, d] inputs: dq, dk, dv [B, H, N, d] and dmc
+    shaped like mc -- [M, M] summed over every (batch, head) when one Mc is
+    shared, [H, M, M] summed over the batch when each head has its own."""
     q = np.asarray(q)
     if q.ndim == 2:
         return mhla_head_backward64(q, k, v, mc, grid, block, dout, fmap, norm)
@@ -205,9 +206,13 @@ def mhla_backward64(q, k, v, mc, grid, block, dout, fmap: str = ELU1, norm: str 
     dmc = np.zeros(np.asarray(mc).shape)
     for bi in range(q.shape[0]):
         for hi in range(q.shape[1]):
-            g = mhla_head_backward64(q[bi, hi], k[bi, hi], v[bi, hi], mc, grid, block, dout[bi, hi], fmap, norm)
+            g = mhla_head_backward64(q[bi, hi], k[bi, hi], v[bi, hi], head_mc(mc, hi), grid, block, dout[bi, hi],
+                                     fmap, norm)
             dq[bi, hi], dk[bi, hi], dv[bi, hi] = g[0], g[1], g[2]
-            dmc += g[3]
+            if dmc.ndim == 3:
+                dmc[hi] += g[3]
+            else:
+                dmc += g[3]
     return dq, dk, dv, dmc
 
 

@@ -32,7 +32,7 @@ from __future__ import annotations
 
 import numpy as np
 
-from .mhla_oracle import (DIVISIVE, ELU1, MALA, NONE, block_of_token, block_summaries, feature_map, mix)
+from .mhla_oracle import (DIVISIVE, ELU1, MALA, NONE, block_of_token, block_summaries, feature_map, head_mc, mix)
 
 
 def causal_mask(grid, block) -> np.ndarray:
@@ -124,7 +124,8 @@ def mhla_causal_forward64(q, k, v, mc, grid, block, fmap: str = ELU1, norm: str 
     out = np.zeros(q.shape, dtype=np.float64)
     for bi in range(q.shape[0]):
         for hi in range(q.shape[1]):
-            out[bi, hi] = mhla_causal_head64(q[bi, hi], k[bi, hi], v[bi, hi], mc, grid, block, fmap, norm)
+            out[bi, hi] = mhla_causal_head64(q[bi, hi], k[bi, hi], v[bi, hi], head_mc(mc, hi), grid, block, fmap,
+                                             norm)
     return out
 
 

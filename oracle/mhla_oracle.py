@@ -185,8 +185,18 @@ def mhla_head64(q, k, v, mc, grid, block, fmap: str = ELU1, norm: str = DIVISIVE
     return head_output(phiq, bidx, St, zt, vt, nt, norm)
 
 
+def head_mc(mc, hi: int) -> np.ndarray:
+    """The mixing matrix of head hi: mc itself when it is [M, M] (one matrix
+    shared by every head), mc[hi] when it is [H, M, M] (one per head, shared
+    over the batch)."""
+    mc = np.asarray(mc)
+    return mc[hi] if mc.ndim == 3 else mc
+
+
 def mhla_forward64(q, k, v, mc, grid, block, fmap: str = ELU1, norm: str = DIVISIVE) -> np.ndarray:
-    """Factored MHLA forward over [B, H, N, d] (or [N, d]) inputs, float64 out."""
+    """Factored MHLA forward over [B, H, N, d] (or [N, d]) inputs, float64 out.
+
+    mc is [M, M] (shared) or [H, M, M] (per head)."""
     q = np.asarray(q)
     if q.ndim == 2:
         return mhla_head64(q, k, v, mc, grid, block, fmap, norm)
@@ -195,7 +205,7 @@ def mhla_forward64(q, k, v, mc, grid, block, fmap: str = ELU1, norm: str = DIVIS
     out = np.zeros(q.shape, dtype=np.float64)
     for bi in range(q.shape[0]):
         for hi in range(q.shape[1]):
-            out[bi, hi] = mhla_head64(q[bi, hi], k[bi, hi], v[bi, hi], mc, grid, block, fmap, norm)
+            out[bi, hi] = mhla_head64(q[bi, hi], k[bi, hi], v[bi, hi], head_mc(mc, hi), grid, block, fmap, norm)
     return out
 
 
@@ -280,5 +290,5 @@ __all__ = [
     "DIVISIVE", "MALA", "NONE", "NORMS", "ELU1", "IDENTITY", "RELU", "EXP", "FEATURE_MAPS", "feature_map",
     "block_of_token", "block_summaries", "mix", "head_output", "mhla_head64",
     "mhla_forward64", "attention_matrix64", "mhla_bruteforce64", "mala_scores64",
-    "rank_bound", "numerical_rank", "relative_max_error",
+    "rank_bound", "numerical_rank", "relative_max_error", "head_mc",
 ]
