@@ -139,6 +139,11 @@ typedef struct mhla_params {
                      * MULTIPASS/FUSED and mhla_backward return
                      * MHLA_ERR_UNSUPPORTED).                                */
   int layout;       /* mhla_layout of the token tensors                    */
+  int mc_per_head;  /* 0: mc is [M, M], shared by every (batch, head);
+                     * 1: mc is [H, M, M], head h mixes with mc[h] (shared over
+                     * the batch) -- mhla_backward's dmc then has the same
+                     * shape, summed over the batch only.  Not with
+                     * MHLA_VARIANT_FUSED (MHLA_ERR_UNSUPPORTED).           */
 } mhla_params;
 
 /* What a call with these parameters will run (for tests and benchmarks). */

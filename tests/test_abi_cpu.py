@@ -86,6 +86,7 @@ BAD = [
     dict(variant=11),
     dict(layout=2),
     dict(causal=3),
+    dict(mc_per_head=2),
 ]
 
 
@@ -280,3 +281,12 @@ def test_causal_plan_and_rejections(lib):
     assert lib.mhla_backward_workspace_bytes(ctypes.byref(p), ctypes.byref(n)) == mb.MHLA_ERR_UNSUPPORTED
     p.causal = 2
     assert lib.mhla_plan(ctypes.byref(p), ctypes.byref(mb.MhlaPlanInfo())) == mb.MHLA_ERR_INVALID_ARG
+
+
+def test_per_head_mc_plan(lib):
+    w = wl.WORKLOADS["image_64x64"]
+    shared = mb.make_params(w.batch, w.heads, w.head_dim, w.grid, w.block)
+    per_head = mb.make_params(w.batch, w.heads, w.head_dim, w.grid, w.block, mc_per_head=True)
+    assert mb.mhla_workspace_bytes(per_head) > mb.mhla_workspace_bytes(shared)
+    fused = mb.make_params(w.batch, w.heads, w.head_dim, w.grid, w.block, variant="fused", mc_per_head=True)
+    assert lib.mhla_plan(ctypes.byref(fused), ctypes.byref(mb.MhlaPlanInfo())) == mb.MHLA_ERR_UNSUPPORTED

@@ -65,6 +65,7 @@ class MhlaParams(ctypes.Structure):
         ("grid", ctypes.c_int * 3), ("block", ctypes.c_int * 3),
         ("dtype", ctypes.c_int), ("feature_map", ctypes.c_int), ("norm", ctypes.c_int),
         ("variant", ctypes.c_int), ("causal", ctypes.c_int), ("layout", ctypes.c_int),
+        ("mc_per_head", ctypes.c_int),
     ]
 
 
@@ -132,7 +133,8 @@ def _check(status: int, where: str):
 
 def make_params(batch: int, heads: int, head_dim: int, grid: Sequence[int], block: Sequence[int],
                 dtype: str = "bf16", feature_map: str = "elu1", norm: str = "divisive",
-                variant: str = "auto", causal: bool = False, layout: str = "bhnd") -> MhlaParams:
+                variant: str = "auto", causal: bool = False, layout: str = "bhnd",
+                mc_per_head: bool = False) -> MhlaParams:
     p = MhlaParams()
     p.batch, p.heads, p.head_dim = int(batch), int(heads), int(head_dim)
     for i in range(3):
@@ -144,6 +146,7 @@ def make_params(batch: int, heads: int, head_dim: int, grid: Sequence[int], bloc
     p.variant = VARIANTS[variant] if isinstance(variant, str) else int(variant)
     p.causal = int(causal)
     p.layout = LAYOUTS[layout] if isinstance(layout, str) else int(layout)
+    p.mc_per_head = int(mc_per_head)
     return p
 
 
@@ -174,6 +177,17 @@ def _torch_dtype_name(t) -> str:
     raise TypeError(f"unsupported dtype {t.dtype}; MHLA takes bfloat16 or float32")
 
 
+def _mc_per_head(mc, p) -> int:
+    """1 when mc is [H, M, M] (one matrix per head), 0 when it is [M, M]."""
+    if mc.dim() == 3:
+        if mc.shape[0] != p.heads:
+            raise ValueError(f"per-head mc must be [H={p.heads}, M, M], got {tuple(mc.shape)}")
+        return 1
+    if mc.dim() != 2:
+        raise ValueError("mc must be [M, M] or [H, M, M]")
+    return 0
+
+
 def _params_for(q, grid, block, feature_map, norm, variant, causal=False, layout="bhnd") -> MhlaParams:
     if q.dim() != 4:
         raise ValueError("q, k, v must be [B, H, N, d] (layout 'bhnd') or [B, N, H, d] (layout 'bnhd')")
@@ -202,6 +216,7 @@ def mhla_forward(q, k, v, mc, grid, block, norm: str = "divisive", feature_map: 
             raise ValueError(f"{name} must be a contiguous CUDA tensor shaped and typed like q")
     if not mc.is_cuda or mc.dtype != torch.float32 or not mc.is_contiguous():
         raise ValueError("mc must be a contiguous float32 CUDA tensor")
+    p.mc_per_head = _mc_per_head(mc, p)
     if out is None:
         out = torch.empty_like(q)
     elif not out.is_cuda or not out.is_contiguous() or out.shape != q.shape or out.dtype != q.dtype:
@@ -243,6 +258,7 @@ def mhla_backward(q, k, v, mc, dout, grid, block, norm: str = "divisive", featur
             raise ValueError(f"{name} must be a contiguous CUDA tensor shaped and typed like q")
     if not mc.is_cuda or mc.dtype != torch.float32 or not mc.is_contiguous():
         raise ValueError("mc must be a contiguous float32 CUDA tensor")
+    p.mc_per_head = _mc_per_head(mc, p)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(q) if dk is None else dk
     dv = torch.empty_like(q) if dv is None else dv
@@ -282,6 +298,7 @@ def mhla_forward_noalloc(q, k, v, mc, grid, block, norm: str = "divisive", featu
     it is None this wrapper allocates it with torch, for convenience)."""
     import torch
     p = _params_for(q, grid, block, feature_map, norm, variant, False, layout)
+    p.mc_per_head = _mc_per_head(mc, p)
     if out is None:
         out = torch.empty_like(q)
     if stream is None:
@@ -304,6 +321,7 @@ def mhla_forward_host(q, k, v, mc, grid, block, norm: str = "divisive", feature_
     """
     import torch
     p = _params_for(q, grid, block, feature_map, norm, variant, causal, layout)
+    p.mc_per_head = _mc_per_head(mc, p)
     for name, t in (("q", q), ("k", k), ("v", v), ("mc", mc)):
         if t.is_cuda or not t.is_contiguous():
             raise ValueError(f"{name} must be a contiguous CPU tensor")

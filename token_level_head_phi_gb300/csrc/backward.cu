@@ -70,7 +70,7 @@ bwd_output_kernel(Plan p, const T* __restrict__ Q, const T* __restrict__ dO, con
   const int tid = threadIdx.x;
   const float* mrow = mixed + ((size_t)u * p.M + i) * p.R;
   for (int e = tid; e < D * D + 2 * D; e += kThreads) sm[e] = mrow[e];
-  const float ntilde = (float)p.nb * rowsum[i];
+  const float ntilde = (float)p.nb * rowsum[mc_index(p, u) * p.M + i];
 
   float acc[PER];
 #pragma unroll
@@ -185,6 +185,7 @@ bwd_mix_kernel(Plan p, const float* __restrict__ mc, const float* __restrict__ d
   const int tx = threadIdx.x % 32, ty = threadIdx.x / 32;
   const int rows = p.M * p.splits;
   const float* st = dmixp + (size_t)u * rows * p.R;
+  mc += (size_t)mc_index(p, u) * p.M * p.M;
   float acc[4][4] = {};
   for (int q0 = 0; q0 < rows; q0 += TQ) {
     __syncthreads();
@@ -226,6 +227,8 @@ bwd_mix_kernel(Plan p, const float* __restrict__ mc, const float* __restrict__ d
 }
 
 // dMc[i][b] = sum_u sum_r dX~[u][i][r] X[u][b][r] (+ MALA: n_b sum_u dn~[u][i]),
+// u over every unit (one shared Mc) or over the units of head blockIdx.z
+// (one Mc per head),
 // dX~ and X summed over pieces on the fly; one CTA per 16 x 16 tile of dMc,
 // reduced over (u, r) in a fixed order.  The sum is blocked in three levels
 // (32 record entries, one head, all heads): the terms of a DIVISIVE or MALA
@@ -241,8 +244,9 @@ bwd_mc_kernel(Plan p, const float* __restrict__ dmixp, const float* __restrict__
   const int i0 = blockIdx.y * TI, b0 = blockIdx.x * TI;
   const int ti = threadIdx.x / TI, tb = threadIdx.x % TI;
   const int rows = p.M * p.splits;
+  const int h = blockIdx.z, ustep = p.mc_heads == 1 ? 1 : p.H;
   float acc = 0.f;
-  for (int u = 0; u < p.BH; ++u) {
+  for (int u = h; u < p.BH; u += ustep) {
     float acc_u = 0.f;
     const float* da = dmixp + (size_t)u * rows * p.R;
     const float* xa = stack + (size_t)u * rows * p.R;
@@ -273,11 +277,11 @@ bwd_mc_kernel(Plan p, const float* __restrict__ dmixp, const float* __restrict__
   if (i < p.M && b < p.M) {
     if (p.norm == MHLA_NORM_MALA) {
       float dn = 0.f;
-      for (int u = 0; u < p.BH; ++u)
+      for (int u = h; u < p.BH; u += ustep)
         for (int s = 0; s < p.splits; ++s) dn += dnp[(size_t)u * rows + (size_t)i * p.splits + s];
       acc = fmaf((float)p.nb, dn, acc);
     }
-    dmc[(size_t)i * p.M + b] = acc;
+    dmc[((size_t)h * p.M + i) * p.M + b] = acc;
   }
 }
 
@@ -390,7 +394,8 @@ int launch_bwd_mix(const Plan& p, const BwdBuffers& w, void* stream) {
 
 int launch_bwd_mc(const Plan& p, const BwdBuffers& w, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  bwd_mc_kernel<<<dim3((p.M + 15) / 16, (p.M + 15) / 16), kThreads, 0, s>>>(p, w.dmixp, w.stack, w.dnp, w.dmc);
+  bwd_mc_kernel<<<dim3((p.M + 15) / 16, (p.M + 15) / 16, p.mc_heads), kThreads, 0, s>>>(p, w.dmixp, w.stack, w.dnp,
+                                                                                        w.dmc);
   return (int)cudaGetLastError();
 }
 

@@ -98,6 +98,9 @@ mhla_status make_plan(const mhla_params* prm, Plan* p, int split_units = 0) {
     return MHLA_ERR_INVALID_ARG;
   if (prm->causal != 0 && prm->causal != 1) return MHLA_ERR_INVALID_ARG;
   if (prm->layout != MHLA_LAYOUT_BHND && prm->layout != MHLA_LAYOUT_BNHD) return MHLA_ERR_INVALID_ARG;
+  if (prm->mc_per_head != 0 && prm->mc_per_head != 1) return MHLA_ERR_INVALID_ARG;
+  // the fused launch keeps one Mc resident per CTA group
+  if (prm->mc_per_head && prm->variant == MHLA_VARIANT_FUSED) return MHLA_ERR_UNSUPPORTED;
 
   const int64_t N64 = (int64_t)prm->grid[0] * prm->grid[1] * prm->grid[2];
   const int64_t BH64 = (int64_t)prm->batch * prm->heads;
@@ -129,6 +132,7 @@ mhla_status make_plan(const mhla_params* prm, Plan* p, int split_units = 0) {
   p->norm = prm->norm;
   p->causal = prm->causal;
   p->layout = prm->layout;
+  p->mc_heads = prm->mc_per_head ? (p->H > 0 ? p->H : 1) : 1;
   p->f_h = make_fastdiv((uint32_t)(p->H > 0 ? p->H : 1));
 
   const bool tc_ok = prm->dtype == MHLA_DTYPE_BF16 && d == kTcHeadDim && !prm->causal;
@@ -176,10 +180,10 @@ mhla_status make_plan(const mhla_params* prm, Plan* p, int split_units = 0) {
     p->off_mixed = off;
     off = align_up(off + sizeof(float) * (size_t)p->BH * p->M * p->R);
     p->off_rowsum = off;
-    off = align_up(off + sizeof(float) * (size_t)p->M);
+    off = align_up(off + sizeof(float) * (size_t)p->M * p->mc_heads);
     if (p->causal) {
       p->off_mcl = off;
-      off = align_up(off + sizeof(float) * (size_t)p->M * p->M);
+      off = align_up(off + sizeof(float) * (size_t)p->M * p->M * p->mc_heads);
       p->kernels = 5;
     }
   } else {
@@ -197,7 +201,7 @@ mhla_status make_plan(const mhla_params* prm, Plan* p, int split_units = 0) {
     const size_t rows = (size_t)p->slots * p->M * p->splits;
     const size_t stack = 2 * rows * p->R;
     const size_t mixed = 2 * (size_t)p->slots * p->M * p->R;
-    const size_t mcq = 2 * (size_t)p->M * p->Qp;
+    const size_t mcq = 2 * (size_t)p->M * p->mc_heads * p->Qp;
     p->off_stack = off;
     off = align_up(off + stack);
     p->off_stack_lo = off;
@@ -213,11 +217,11 @@ mhla_status make_plan(const mhla_params* prm, Plan* p, int split_units = 0) {
     p->off_mc_lo = off;
     off = align_up(off + mcq);
     p->off_mc_scale = off;
-    off = align_up(off + sizeof(float) * (size_t)p->M);
+    off = align_up(off + sizeof(float) * (size_t)p->M * p->mc_heads);
     p->off_rowsum = off;
-    off = align_up(off + sizeof(float) * (size_t)p->M);
+    off = align_up(off + sizeof(float) * (size_t)p->M * p->mc_heads);
     p->off_blkinfo = off;
-    off = align_up(off + 16 * (size_t)p->M);
+    off = align_up(off + 16 * (size_t)p->M * p->mc_heads);
     p->kernels = 4;
     if (variant == MHLA_VARIANT_FUSED) {
       p->off_flow = off;
@@ -338,8 +342,10 @@ HostGroups host_groups(const Plan& plan) {
   if (n < 1) n = 1;
   HostGroups g;
   g.per = (plan.BH + n - 1) / n;
-  // token-major tensors are contiguous per batch only: whole batches per group
-  if (plan.layout == MHLA_LAYOUT_BNHD && plan.H > 0) g.per = (g.per + plan.H - 1) / plan.H * plan.H;
+  // token-major tensors are contiguous per batch only, and per-head mixing
+  // matrices index heads within a batch: whole batches per group
+  if ((plan.layout == MHLA_LAYOUT_BNHD || plan.mc_heads > 1) && plan.H > 0)
+    g.per = (g.per + plan.H - 1) / plan.H * plan.H;
   g.n = (plan.BH + g.per - 1) / g.per;
   return g;
 }
@@ -349,7 +355,7 @@ HostGroups host_groups(const Plan& plan) {
 // token-major tensors units / H batches of H heads.
 mhla_params group_params(const mhla_params* p, int units) {
   mhla_params g = *p;
-  if (p->layout == MHLA_LAYOUT_BNHD && p->heads > 0) {
+  if ((p->layout == MHLA_LAYOUT_BNHD || p->mc_per_head) && p->heads > 0) {
     g.batch = units / p->heads;
   } else {
     g.batch = 1;
@@ -420,7 +426,8 @@ mhla_status make_bwd_plan(const mhla_params* prm, Plan* plan, BwdLayout* lay) {
     field = off;
     off = align_up(off + bytes);
   };
-  take(lay->rowsum, sizeof(float) * plan->M);
+  const size_t mh = (size_t)plan->mc_heads;
+  take(lay->rowsum, sizeof(float) * plan->M * mh);
   take(lay->dnp, sizeof(float) * rows);
   if (!lay->tc) {
     take(lay->stack, sizeof(float) * rows * R);
@@ -434,20 +441,20 @@ mhla_status make_bwd_plan(const mhla_params* prm, Plan* plan, BwdLayout* lay) {
     take(lay->mixed_lo, 2 * mrows * R);
     take(lay->dmixp_hi, 2 * rows * R);
     take(lay->dmixp_lo, 2 * rows * R);
-    const size_t mcq = 2 * (size_t)plan->M * plan->Qp;
+    const size_t mcq = 2 * (size_t)plan->M * mh * plan->Qp;
     take(lay->mc_f16, mcq);
     take(lay->mc_hi, mcq);
     take(lay->mc_lo, mcq);
-    take(lay->mc_scale, sizeof(float) * plan->M);
-    take(lay->blkinfo, 16 * (size_t)plan->M);
+    take(lay->mc_scale, sizeof(float) * plan->M * mh);
+    take(lay->blkinfo, 16 * (size_t)plan->M * mh);
     take(lay->partial, tc_bwd_mc_partial_bytes(*plan));
-    take(lay->mct, sizeof(float) * (size_t)plan->M * plan->M);
+    take(lay->mct, sizeof(float) * (size_t)plan->M * plan->M * mh);
     take(lay->mct_f16, mcq);
     take(lay->mct_hi, mcq);
     take(lay->mct_lo, mcq);
-    take(lay->mct_scale, sizeof(float) * plan->M);
-    take(lay->mct_rowsum, sizeof(float) * plan->M);
-    take(lay->mct_blkinfo, 16 * (size_t)plan->M);
+    take(lay->mct_scale, sizeof(float) * plan->M * mh);
+    take(lay->mct_rowsum, sizeof(float) * plan->M * mh);
+    take(lay->mct_blkinfo, 16 * (size_t)plan->M * mh);
     take(lay->dx_hi, 2 * mrows * R);
     take(lay->dx_lo, 2 * mrows * R);
   }
@@ -516,7 +523,7 @@ int run_backward(const Plan& plan, const BwdLayout& lay, const void* q, const vo
     bt.mc_lo = H(lay.mct_lo);
     bt.rowsum = F(lay.mct_rowsum);
     bt.blkinfo = reinterpret_cast<float4*>(ws + lay.mct_blkinfo);
-    if ((e = launch_transpose_mc(mc, F(lay.mct), p.M, s)) != 0) return e;
+    if ((e = launch_transpose_mc(mc, F(lay.mct), p.M, p.mc_heads, s)) != 0) return e;
     if ((e = launch_tc_prep(pr, F(lay.mct), bt, s)) != 0) return e;
     if ((e = launch_tc_mix(pr, bt, s)) != 0) return e;
     record_bwd_event(3, s);
@@ -576,7 +583,7 @@ mhla_status mhla_backward(const void* q, const void* k, const void* v, const flo
     if (mhla::misaligned(x, 16)) return MHLA_ERR_INVALID_ARG;
   if (mhla::misaligned(mc, 4) || mhla::misaligned(dmc, 4)) return MHLA_ERR_INVALID_ARG;
   const size_t io = (size_t)plan.BH * plan.N * plan.d * mhla::elem_bytes(plan.dtype);
-  const size_t mcb = sizeof(float) * (size_t)plan.M * plan.M;
+  const size_t mcb = sizeof(float) * (size_t)plan.M * plan.M * plan.mc_heads;
   for (int a = 0; a < 3; ++a) {
     for (const void* x : io_in)
       if (mhla::overlaps(io_out[a], io, x, io)) return MHLA_ERR_INVALID_ARG;
@@ -646,7 +653,7 @@ mhla_status mhla_forward(const void* q, const void* k, const void* v, const floa
       mhla::misaligned(out, 16) || mhla::misaligned(mc, 4))
     return MHLA_ERR_INVALID_ARG;
   const size_t io_bytes = (size_t)plan.BH * plan.N * plan.d * mhla::elem_bytes(plan.dtype);
-  const size_t mc_bytes = sizeof(float) * (size_t)plan.M * plan.M;
+  const size_t mc_bytes = sizeof(float) * (size_t)plan.M * plan.M * plan.mc_heads;
   if (mhla::overlaps(out, io_bytes, q, io_bytes) || mhla::overlaps(out, io_bytes, k, io_bytes) ||
       mhla::overlaps(out, io_bytes, v, io_bytes) || mhla::overlaps(out, io_bytes, mc, mc_bytes))
     return MHLA_ERR_INVALID_ARG;
@@ -683,7 +690,7 @@ mhla_status mhla_host_buffer_bytes(const mhla_params* p, size_t* bytes) {
   st = mhla::host_group_workspace(p, plan, &ws);
   if (st != MHLA_OK) return st;
   const size_t io = mhla::align_up((size_t)plan.BH * plan.N * plan.d * mhla::elem_bytes(plan.dtype));
-  const size_t mcb = mhla::align_up(sizeof(float) * (size_t)plan.M * plan.M);
+  const size_t mcb = mhla::align_up(sizeof(float) * (size_t)plan.M * plan.M * plan.mc_heads);
   *bytes = 4 * io + mcb + ws;
   return MHLA_OK;
 }
@@ -703,7 +710,7 @@ mhla_status mhla_forward_host(const void* q, const void* k, const void* v, const
   const size_t unit_bytes = (size_t)plan.N * plan.d * mhla::elem_bytes(plan.dtype);
   const size_t io_raw = (size_t)plan.BH * unit_bytes;
   const size_t io = mhla::align_up(io_raw);
-  const size_t mc_raw = sizeof(float) * (size_t)plan.M * plan.M;
+  const size_t mc_raw = sizeof(float) * (size_t)plan.M * plan.M * plan.mc_heads;
   const size_t mcb = mhla::align_up(mc_raw);
   char* base = static_cast<char*>(dev_buffer);
   char* dq = base;

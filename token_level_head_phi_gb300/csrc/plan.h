@@ -69,6 +69,7 @@ struct Plan {
   int dtype, fmap, norm, variant;
   int causal;         // block-ordered causal form (float32 kernels only)
   int layout;         // MHLA_LAYOUT_BHND or MHLA_LAYOUT_BNHD for q, k, v, out (and gradients)
+  int mc_heads;       // mixing matrices: 1 (shared) or H (one per head, shared over the batch)
   FastDiv f_h;        // division by H (unit -> batch, head)
   // long blocks are summarised in `splits` pieces of at most `split_len`
   // tokens each; the mixing step sums the pieces (every piece of block b
@@ -112,6 +113,14 @@ __host__ __device__ inline void chunk_origin(const Plan& p, const ChunkShape& ch
   x0 = (int)(bx * p.bw + cx * ch.cw);
   y0 = (int)(by * p.bh + cy * ch.ch);
   t0 = (int)(bz * p.bt + cz * ch.ct);
+}
+
+// Which mixing matrix unit u = b * H + h uses (0 when one Mc is shared).
+// Matrix j occupies rows j*M .. j*M + M - 1 of every per-row array
+// (Mc, its copies, row sums, block info).
+__host__ __device__ inline int mc_index(const Plan& p, int u) {
+  if (p.mc_heads == 1) return 0;
+  return u - (int)fdiv((uint32_t)u, p.f_h) * p.H;
 }
 
 // Element offset of feature 0 of token t of unit u = b * H + h in q, k, v

@@ -90,6 +90,7 @@ simt_mix_kernel(Plan p, const float* __restrict__ mc, const float* __restrict__ 
   const int tx = threadIdx.x % 32, ty = threadIdx.x / 32;
   const int rows = p.M * p.splits;
   const float* st = stack + (size_t)u * rows * p.R;
+  mc += (size_t)mc_index(p, u) * p.M * p.M;
   float acc[4][4] = {};
   for (int q0 = 0; q0 < rows; q0 += TQ) {
     __syncthreads();
@@ -166,7 +167,7 @@ simt_output_kernel(Plan p, const Tin* __restrict__ Q, const float* __restrict__ 
     ss[tid] = s;
   }
   __syncthreads();
-  const float n_mixed = (float)p.nb * rowsum[i];
+  const float n_mixed = (float)p.nb * rowsum[mc_index(p, u) * p.M + i];
   for (int e = tid; e < cnt * D; e += kThreads) {
     const int tt = e / D, c = e % D;
     float a = 0.f;
@@ -187,10 +188,11 @@ simt_output_kernel(Plan p, const Tin* __restrict__ Q, const float* __restrict__ 
   }
 }
 
-__global__ void mc_rowsum_kernel(int M, const float* __restrict__ mc, float* __restrict__ rowsum) {
+// Row sums of `rows` rows of length M (every row of every mixing matrix).
+__global__ void mc_rowsum_kernel(int rows, int M, const float* __restrict__ mc, float* __restrict__ rowsum) {
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) / 32;
   const int lane = threadIdx.x % 32;
-  if (warp >= M) return;
+  if (warp >= rows) return;
   float s = 0.f;
   for (int b = lane; b < M; b += 32) s += mc[(size_t)warp * M + b];
 #pragma unroll
@@ -247,8 +249,9 @@ int output_by_d(const Plan& p, const void* q, const float* mixed, const float* r
 
 int launch_mc_rowsum(const Plan& p, const float* mc, float* rowsum, void* stream) {
   const int threads = 256;
-  const int blocks = (p.M * 32 + threads - 1) / threads;
-  mc_rowsum_kernel<<<blocks, threads, 0, (cudaStream_t)stream>>>(p.M, mc, rowsum);
+  const int rows = p.M * p.mc_heads;
+  const int blocks = (rows * 32 + threads - 1) / threads;
+  mc_rowsum_kernel<<<blocks, threads, 0, (cudaStream_t)stream>>>(rows, p.M, mc, rowsum);
   return (int)cudaGetLastError();
 }
 

@@ -24,10 +24,11 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kTQ = 32;
 
-__global__ void strict_lower_kernel(int M, const float* __restrict__ mc, float* __restrict__ mcl) {
-  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx >= M * M) return;
-  const int i = idx / M, b = idx - i * M;
+// mcl = Mc with its diagonal and upper triangle zeroed, for `heads` matrices.
+__global__ void strict_lower_kernel(int heads, int M, const float* __restrict__ mc, float* __restrict__ mcl) {
+  const size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
+  if (idx >= (size_t)heads * M * M) return;
+  const int r = (int)(idx / M), b = (int)(idx % M), i = r % M;
   mcl[idx] = b < i ? mc[idx] : 0.f;
 }
 
@@ -50,10 +51,11 @@ causal_output_kernel(Plan p, const T* __restrict__ Q, const T* __restrict__ K, c
   const int u = blockIdx.y;
   const int i = blockIdx.x;
   const int tid = threadIdx.x;
-  const float w = mc[(size_t)i * p.M + i];
+  const int j = mc_index(p, u);
+  const float w = mc[((size_t)j * p.M + i) * p.M + i];
   const float* mrow = mixed + ((size_t)u * p.M + i) * p.R;
   for (int e = tid; e < D * D + 2 * D; e += kThreads) sm[e] = mrow[e];
-  float n_state = (float)p.nb * rowsum_lower[i];   // n<_i
+  float n_state = (float)p.nb * rowsum_lower[j * p.M + i];   // n<_i
 
   for (int l0 = 0; l0 < p.nb; l0 += kTQ) {
     const int cnt = min(kTQ, p.nb - l0);
@@ -157,8 +159,8 @@ int by_d(const Plan& p, const void* q, const void* k, const void* v, const float
 }  // namespace
 
 int launch_mc_strict_lower(const Plan& p, const float* mc, float* mcl, void* stream) {
-  const int n = p.M * p.M;
-  strict_lower_kernel<<<(n + 255) / 256, 256, 0, (cudaStream_t)stream>>>(p.M, mc, mcl);
+  const size_t n = (size_t)p.mc_heads * p.M * p.M;
+  strict_lower_kernel<<<(unsigned)((n + 255) / 256), 256, 0, (cudaStream_t)stream>>>(p.mc_heads, p.M, mc, mcl);
   return (int)cudaGetLastError();
 }
 

@@ -32,7 +32,7 @@ int launch_tc_bwd_output(const Plan& p, const void* q, const void* dout, const _
                          const __nv_bfloat16* mixed_lo, const float4* blkinfo, void* dq, __nv_bfloat16* dx_hi,
                          __nv_bfloat16* dx_lo, float* dnp, cudaStream_t s);
 
-// out[b][i] = in[i][b] for an M x M float32 matrix.
-int launch_transpose_mc(const float* in, float* out, int M, cudaStream_t s);
+// out[j][b][i] = in[j][i][b] for `count` M x M float32 matrices.
+int launch_transpose_mc(const float* in, float* out, int M, int count, cudaStream_t s);
 
 }  // namespace mhla

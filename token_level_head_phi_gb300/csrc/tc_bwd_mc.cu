@@ -207,15 +207,19 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_mc_kernel(const __grid_con
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-// dmc[i][b] = sum_u sum_{s, s'} partial[u][i*splits + s][b*splits + s']
-//             (+ MALA: n_b sum_u sum_s dnp[u][i*splits + s])
+// dmc[h][i][b] = sum_u sum_{s, s'} partial[u][i*splits + s][b*splits + s']
+//                (+ MALA: n_b sum_u sum_s dnp[u][i*splits + s])
+// with u over every unit (heads == 1, one shared Mc) or over the units of
+// head h (heads == H, one Mc per head).
 __global__ void bwd_mc_reduce_kernel(const float* __restrict__ partial, const float* __restrict__ dnp, int M,
-                                     int splits, int BH, int qp, int Q, float nb, int mala, float* __restrict__ dmc) {
+                                     int splits, int BH, int qp, int Q, float nb, int mala, int heads,
+                                     float* __restrict__ dmc) {
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx >= M * M) return;
-  const int i = idx / M, b = idx - i * M;
+  if (idx >= heads * M * M) return;
+  const int h = idx / (M * M), rem = idx - h * M * M;
+  const int i = rem / M, b = rem - i * M;
   float acc = 0.f;
-  for (int u = 0; u < BH; ++u) {
+  for (int u = h; u < BH; u += heads) {
     const float* pu = partial + (size_t)u * qp * qp;
     float au = 0.f;
     for (int s = 0; s < splits; ++s)
@@ -224,7 +228,7 @@ __global__ void bwd_mc_reduce_kernel(const float* __restrict__ partial, const fl
   }
   if (mala) {
     float dn = 0.f;
-    for (int u = 0; u < BH; ++u)
+    for (int u = h; u < BH; u += heads)
       for (int s = 0; s < splits; ++s) dn += dnp[(size_t)u * Q + i * splits + s];
     acc = fmaf(nb, dn, acc);
   }
@@ -262,9 +266,10 @@ int launch_tc_bwd_mc(const Plan& p, const __nv_bfloat16* dx_hi, const __nv_bfloa
   const int grid = a.items < num_sms() ? a.items : num_sms();
   tc_bwd_mc_kernel<<<grid, kThreads, kSmemBytes, s>>>(a);
   if ((ce = cudaGetLastError()) != cudaSuccess) return (int)ce;
-  const int n = p.M * p.M;
+  const int n = p.M * p.M * p.mc_heads;
   bwd_mc_reduce_kernel<<<(n + 255) / 256, 256, 0, s>>>(partial, dnp, p.M, p.splits, p.BH, a.qt * 128, Q,
-                                                       (float)p.nb, p.norm == MHLA_NORM_MALA ? 1 : 0, dmc);
+                                                       (float)p.nb, p.norm == MHLA_NORM_MALA ? 1 : 0, p.mc_heads,
+                                                       dmc);
   return (int)cudaGetLastError();
 }
 

@@ -266,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_output_kernel(const __grid
       const int rec = it.u * p.M + it.i;
       const __nv_bfloat16* src = (lane < 16 ? a.mixed_hi : a.mixed_lo) + (size_t)rec * a.R + 64 * 64 + (lane & 15) * 8;
       cp_async16(st + kOffAux + (lane < 16 ? 0u : 256u) + (lane & 15) * 16, src);
-      if (lane == 0) cp_async16(st + kOffInfo, a.blkinfo + it.i);
+      if (lane == 0) cp_async16(st + kOffInfo, a.blkinfo + mc_index(p, it.u) * p.M + it.i);
       cp_async_arrive(bfull(x));
       __syncwarp();
       if (lane == 0) {

@@ -25,7 +25,9 @@ using mx::kThreads;
 // One warp per row i of Mc: the fp16 copy scaled by 2^-e_i (largest entry of
 // the row in [0.5, 1]), the bf16 high and low parts, the row scale 2^e_i and
 // the row sum of hi + lo in float32.  Columns are expanded over pieces.
-__global__ void tc_prep_kernel(int M, int splits, int Q, int Qp, const float* __restrict__ mc,
+// `rows` rows of length M: every row of every mixing matrix (one per head
+// when each head has its own).
+__global__ void tc_prep_kernel(int rows, int M, int splits, int Q, int Qp, const float* __restrict__ mc,
                                __half* __restrict__ mc_f16, float* __restrict__ mc_scale,
                                __nv_bfloat16* __restrict__ mc_hi, __nv_bfloat16* __restrict__ mc_lo,
                                float* __restrict__ rowsum, float4* __restrict__ blkinfo, int f16,
@@ -37,7 +39,7 @@ __global__ void tc_prep_kernel(int M, int splits, int Q, int Qp, const float* __
   for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < nflow; t += gridDim.x * blockDim.x) flow[t] = 0u;
   const int i = (blockIdx.x * blockDim.x + threadIdx.x) / 32;
   const int lane = threadIdx.x % 32;
-  if (i >= M) return;
+  if (i >= rows) return;
   const float* row = mc + (size_t)i * M;
   float s = 0.f, amax = 0.f;
   for (int b = lane; b < M; b += 32) {
@@ -112,6 +114,7 @@ bool mixt_supported(const Plan& p, const TcBuffers& b) {
   // 14x14 x 192 heads 60 -> 40 us).  With more tiles each stack tile would be
   // read once per 128 query blocks instead of once per 256 (video: 66 -> 89
   // us), and under MALA the two kernels measured the same.
+  if (p.mc_heads != 1) return false;  // Mc stays resident per CTA: one matrix only
   return p.R % 128 == 0 && kchunks * 32 * (b.f16 ? 1 : 2) <= 256 && p.M <= 128 && b.f16;
 }
 
@@ -150,8 +153,9 @@ int build_mixt_args(const Plan& p, const TcBuffers& b, mt::MixTArgs* out) {
 
 int launch_tc_prep(const Plan& p, const float* mc, const TcBuffers& b, cudaStream_t s) {
   const int threads = 256;
-  const int blocks = (p.M * 32 + threads - 1) / threads;
-  return launch_pdl(tc_prep_kernel, dim3(blocks), dim3(threads), 0, s, p.M, p.splits, p.M * p.splits, b.Qp, mc,
+  const int rows = p.M * p.mc_heads;
+  const int blocks = (rows * 32 + threads - 1) / threads;
+  return launch_pdl(tc_prep_kernel, dim3(blocks), dim3(threads), 0, s, rows, p.M, p.splits, p.M * p.splits, b.Qp, mc,
                     b.mc_f16, b.mc_scale, b.mc_hi, b.mc_lo, b.rowsum, b.blkinfo, b.f16 ? 1 : 0, 1.f / b.stack_scale,
                     (float)p.nb, b.flow, b.flow ? 3 * p.BH : 0);
 }
@@ -178,7 +182,7 @@ int build_mix_args(const Plan& p, const TcBuffers& b, int slots, mx::MixArgs* ou
   const int nt_max = f16 ? 256 : 128;
   int NT = (p.M + 63) / 64 * 64;
   if (NT > nt_max) NT = nt_max;
-  const uint64_t dimsB[2] = {(uint64_t)Q, (uint64_t)p.M};
+  const uint64_t dimsB[2] = {(uint64_t)Q, (uint64_t)p.M * p.mc_heads};
   const uint64_t strB[1] = {2ull * b.Qp};
   const uint32_t boxB[2] = {64, (uint32_t)NT};
   if (f16) {

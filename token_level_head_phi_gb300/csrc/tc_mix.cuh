@@ -137,10 +137,12 @@ __device__ __forceinline__ void mix_body(const MixArgs& a, const Plan& p, const 
           const uint32_t st = base + (uint32_t)stage * a.stage_bytes;
           mbar_arrive_expect_tx(full(stage), bytes);
           tma_load_4d(st, &a.tmA, full(stage), 0, kc * 64, r0 / 64, ss, pol_a);
-          tma_load_2d(st + a.off_b, &a.tmB, full(stage), kc * 64, i0, pol_b);
+          // rows of this head's mixing matrix (one matrix per head, or one shared)
+          const int ib = i0 + mc_index(p, u) * p.M;
+          tma_load_2d(st + a.off_b, &a.tmB, full(stage), kc * 64, ib, pol_b);
           if (!kF16) {
             tma_load_4d(st + a.off_alo, &a.tmA_lo, full(stage), 0, kc * 64, r0 / 64, ss, pol_a);
-            tma_load_2d(st + a.off_blo, &a.tmB_lo, full(stage), kc * 64, i0, pol_b);
+            tma_load_2d(st + a.off_blo, &a.tmB_lo, full(stage), kc * 64, ib, pol_b);
           }
           ++issued;
           if (++stage == kStages) {

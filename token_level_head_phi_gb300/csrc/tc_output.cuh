@@ -216,7 +216,7 @@ __device__ __forceinline__ void output_body(const OutArgs& a, const Plan& p, con
       const int rec = flow_slot(f, u) * p.M + i;  // record of S~_i in the mixed summaries
       const __nv_bfloat16* src = (lane < 16 ? a.mixed_hi : a.mixed_lo) + (size_t)rec * a.R + 64 * 64 + (lane & 15) * 8;
       cp_async16(st + (lane < 16 ? L::kOffAux : L::kOffAuxLo) + (lane & 15) * 16, src);
-      if (lane == 0) cp_async16(st + L::kOffInfo, a.blkinfo + i);
+      if (lane == 0) cp_async16(st + L::kOffInfo, a.blkinfo + mc_index(p, u) * p.M + i);
       cp_async_arrive(bfull(b));
       __syncwarp();
       if (lane == 0) {
