@@ -3,7 +3,7 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
                     [--variant auto|simt|multipass|fused] [--impl mine|reference]
                     [--all-workloads] [--no-cpu-baseline] [--pass forward|backward]
-                    [--feature-map elu1|relu|exp] [--causal] [--layout bhnd|bnhd]
+                    [--feature-map elu1|relu|exp] [--causal] [--layout bhnd|bnhd] [--mc-per-head]
 
 A step is one full forward (block summaries, mixing, output) over one batch
 of the workload's seeded synthetic inputs, already resident in HBM.  The
@@ -254,10 +254,13 @@ def run_mine(args, w: wl.Workload, world: int, rank: int, local: int, dist):
     if args.layout == "bnhd":
         # token-major [B, N, H, d], as a fused QKV projection writes it
         q, k, v = (t.permute(0, 2, 1, 3).contiguous() for t in (q, k, v))
+    if args.mc_per_head:
+        # one matrix per head: the workload's recipe with a different noise seed per head
+        mcn = np.stack([wl.make_mc(w.with_(seed=w.seed + 101 * h)) for h in range(w.heads)]).astype(np.float32)
     mc = torch.from_numpy(mcn).to(dev)
     out = torch.empty_like(q)
     p = mb.make_params(w.batch, w.heads, w.head_dim, w.grid, w.block, w.dtype, args.feature_map, w.norm, args.variant,
-                       args.causal, args.layout)
+                       args.causal, args.layout, args.mc_per_head)
     info = mb.mhla_plan(p)
     ws = torch.empty(max(info.workspace_bytes, 1), dtype=torch.uint8, device=dev)
     ws_bytes = ws.numel()
@@ -361,6 +364,7 @@ def run_mine(args, w: wl.Workload, world: int, rank: int, local: int, dist):
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": w.dtype, "data": "synthetic (seeded normals, locality-biased Mc; no dataset, no weights)",
         "config": dict(wl.describe(w), feature_map=args.feature_map, causal=bool(args.causal), layout=args.layout,
+                       mc_per_head=bool(args.mc_per_head),
                        variant=mb.mhla_plan(p).variant,
                        variant_name={1: "simt", 2: "multipass", 3: "fused"}.get(info.variant, str(info.variant)),
                        l2="no flush: inputs exceed L2" if flush is None else "L2 flushed (256 MB write) between steps, outside per-step events",
@@ -488,13 +492,17 @@ def run_backward(args, w: wl.Workload, world: int, rank: int, local: int, dist):
     del qn, kn, vn, gn
     if args.layout == "bnhd":
         q, k, v, g = (t.permute(0, 2, 1, 3).contiguous() for t in (q, k, v, g))
-    mc = torch.from_numpy(wl.make_mc(w)).to(dev)
+    if args.mc_per_head:
+        mc = torch.from_numpy(np.stack([wl.make_mc(w.with_(seed=w.seed + 101 * h))
+                                        for h in range(w.heads)]).astype(np.float32)).to(dev)
+    else:
+        mc = torch.from_numpy(wl.make_mc(w)).to(dev)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
     dmc = torch.empty_like(mc)
     path = "tc" if (w.dtype == "bf16" and w.head_dim == 64 and args.variant != "simt") else "simt"
     variant = "simt" if path == "simt" else "auto"
     p = mb.make_params(w.batch, w.heads, w.head_dim, w.grid, w.block, w.dtype, args.feature_map, w.norm, variant,
-                       False, args.layout)
+                       False, args.layout, args.mc_per_head)
     splits = mb.mhla_plan(mb.make_params(w.batch, w.heads, w.head_dim, w.grid, w.block, w.dtype, args.feature_map, w.norm,
                                          "multipass" if path == "tc" else "simt")).summary_splits
     need = mb.mhla_backward_workspace_bytes(p)
@@ -606,6 +614,7 @@ def run_backward(args, w: wl.Workload, world: int, rank: int, local: int, dist):
         "dtype": "bf16" if path == "tc" else "f32",
         "data": "synthetic (seeded normals, locality-biased Mc, seeded normal dO)",
         "config": dict(wl.describe(w), pass_="backward", feature_map=args.feature_map, layout=args.layout,
+                       mc_per_head=bool(args.mc_per_head),
                        input_dtype=w.dtype,
                        path="tensor cores (split bf16)" if path == "tc" else "CUDA cores (float32)",
                        l2="no flush: inputs exceed L2" if flush is None else "L2 flushed (256 MB write) between steps, outside per-step events",
@@ -714,6 +723,7 @@ def main():
     ap.add_argument("--feature-map", default="elu1", choices=["elu1", "relu", "exp"])
     ap.add_argument("--causal", action="store_true", help="block-ordered causal forward (float32 kernels)")
     ap.add_argument("--layout", default="bhnd", choices=["bhnd", "bnhd"], help="q/k/v/out memory layout")
+    ap.add_argument("--mc-per-head", action="store_true", help="one mixing matrix per head")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
