@@ -269,13 +269,18 @@ def test_backward_workspace_and_checks(lib):
 
 def test_causal_plan_and_rejections(lib):
     w = wl.WORKLOADS["deit_t"]
+    # bf16, d = 64, DIVISIVE: the tensor-core causal path (mask, prep, summary, mixing, output)
     p = mb.make_params(w.batch, w.heads, w.head_dim, w.grid, w.block, causal=True)
     info = mb.mhla_plan(p)
-    assert info.variant == mb.VARIANT_SIMT and info.kernels_per_call == 5
-    assert info.workspace_bytes >= mb.mhla_workspace_bytes(mb.make_params(
-        w.batch, w.heads, w.head_dim, w.grid, w.block, variant="simt")) + 4 * w.n_blocks ** 2
-    for variant in ("multipass", "fused"):
-        bad = mb.make_params(w.batch, w.heads, w.head_dim, w.grid, w.block, variant=variant, causal=True)
+    assert info.variant == mb.VARIANT_MULTIPASS and info.kernels_per_call == 5
+    # MALA and float32 take the CUDA-core causal kernels
+    mala = mb.make_params(w.batch, w.heads, w.head_dim, w.grid, w.block, norm="mala", causal=True)
+    assert mb.mhla_plan(mala).variant == mb.VARIANT_SIMT
+    f32 = mb.make_params(w.batch, w.heads, w.head_dim, w.grid, w.block, dtype="f32", causal=True)
+    info32 = mb.mhla_plan(f32)
+    assert info32.variant == mb.VARIANT_SIMT and info32.kernels_per_call == 5
+    for variant, norm in (("fused", "divisive"), ("multipass", "mala")):
+        bad = mb.make_params(w.batch, w.heads, w.head_dim, w.grid, w.block, norm=norm, variant=variant, causal=True)
         assert lib.mhla_plan(ctypes.byref(bad), ctypes.byref(mb.MhlaPlanInfo())) == mb.MHLA_ERR_UNSUPPORTED
     n = ctypes.c_size_t(0)
     assert lib.mhla_backward_workspace_bytes(ctypes.byref(p), ctypes.byref(n)) == mb.MHLA_ERR_UNSUPPORTED

@@ -1,5 +1,6 @@
-"""GPU parity of the block-ordered causal form (float32 CUDA-core kernels)
-against the causal float64 oracle; same measure and tolerances as the
+"""GPU parity of the block-ordered causal form against the causal float64
+oracle, on the tensor-core path (bf16, d = 64, DIVISIVE / NONE: AUTO) and
+the float32 CUDA-core kernels (SIMT); same measure and tolerances as the
 non-causal parity tests (max|gpu - oracle| / max|oracle| per unit)."""
 
 import zlib
@@ -24,13 +25,13 @@ def _lib():
     mb.load()
 
 
-def causal_parity(w, norm, fmap="elu1", units=None, mc=None):
+def causal_parity(w, norm, fmap="elu1", units=None, mc=None, variant="auto"):
     import torch
     vals, dev = wl.all_inputs(w)
     mc = wl.make_mc(w) if mc is None else mc
     q, k, v = upload(w, dev)
     mct = torch.from_numpy(np.ascontiguousarray(mc, dtype=np.float32)).cuda()
-    o = mb.mhla_forward(q, k, v, mct, w.grid, w.block, norm=norm, feature_map=fmap, causal=True)
+    o = mb.mhla_forward(q, k, v, mct, w.grid, w.block, norm=norm, feature_map=fmap, causal=True, variant=variant)
     torch.cuda.synchronize()
     code, detail = mb.mhla_device_status()
     assert code == 0, f"device status {code} (detail {detail})"
@@ -44,25 +45,32 @@ def causal_parity(w, norm, fmap="elu1", units=None, mc=None):
     return worst
 
 
+@pytest.mark.parametrize("variant", ["auto", "simt"])
 @pytest.mark.parametrize("norm", ["divisive", "none", "mala"])
 @pytest.mark.parametrize("name", ["tiny_f32", "deit_t"])
-def test_workload_causal(name, norm):
+def test_workload_causal(name, norm, variant):
     w = wl.WORKLOADS[name]
-    err = causal_parity(w, norm, units=[0, w.units - 1])
+    err = causal_parity(w, norm, units=[0, w.units - 1], variant=variant)
     assert err <= TOL[w.dtype], f"{name}/{norm}: {err:.3e}"
 
 
-@pytest.mark.parametrize("norm", ["divisive", "mala"])
-def test_sequence_head_causal(norm):
-    # the 1D language-model shape: 128 blocks of 256 tokens, eight 32-token tiles per block
+@pytest.mark.parametrize("variant", ["auto", "simt"])
+@pytest.mark.parametrize("norm", ["divisive", "none", "mala"])
+def test_sequence_head_causal(norm, variant):
+    # the 1D language-model shape: 128 blocks of 256 tokens (two 128-token
+    # chunks per block on the tensor cores, eight 32-token tiles in float32)
     w = wl.WORKLOADS["seq_32k"].with_(batch=1, heads=2)
-    err = causal_parity(w, norm)
+    err = causal_parity(w, norm, variant=variant)
     assert err <= TOL[w.dtype], f"{norm}: {err:.3e}"
 
 
 EDGE = [
     # grid, block, d, dtype, batch, heads
     ((1, 14, 14), (1, 7, 7), 64, "bf16", 1, 2),        # 49-token blocks: ragged last tile
+    ((4, 16, 16), (2, 8, 8), 64, "bf16", 1, 2),        # video-shaped 128-token blocks (one chunk)
+    ((1, 1, 2100), (1, 1, 300), 64, "bf16", 1, 2),     # 300-token 1D blocks: three 100-token chunks
+    ((3, 10, 10), (3, 10, 10), 64, "bf16", 1, 1),      # one 300-token 3D block: chunks of whole planes
+    ((1, 1, 1000), (1, 1, 1000), 64, "bf16", 1, 1),    # one long block: eight chunks
     ((1, 1, 300), (1, 1, 100), 32, "f32", 1, 2),       # 1D, 100-token blocks
     ((3, 8, 8), (3, 4, 8), 16, "f32", 1, 1),           # 3D blocks
     ((2, 4, 8), (1, 2, 4), 128, "bf16", 1, 1),         # d = 128

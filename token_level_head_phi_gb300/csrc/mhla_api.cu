@@ -13,6 +13,7 @@
 #include "plan.h"
 #include "backward.h"
 #include "tc_bwd.h"
+#include "tc_causal.h"
 #include "tc_host.h"
 
 namespace mhla {
@@ -135,7 +136,14 @@ mhla_status make_plan(const mhla_params* prm, Plan* p, int split_units = 0) {
   p->mc_heads = prm->mc_per_head ? (p->H > 0 ? p->H : 1) : 1;
   p->f_h = make_fastdiv((uint32_t)(p->H > 0 ? p->H : 1));
 
-  const bool tc_ok = prm->dtype == MHLA_DTYPE_BF16 && d == kTcHeadDim && !prm->causal;
+  bool tc_ok = prm->dtype == MHLA_DTYPE_BF16 && d == kTcHeadDim;
+  if (tc_ok && prm->causal) {
+    // the tensor-core causal output step: DIVISIVE / NONE with token chunks
+    // that are contiguous runs of the block's local order; never fused
+    Plan probe = *p;
+    probe.chunk = choose_chunk(probe);
+    tc_ok = tc_causal_supported(probe) && prm->variant != MHLA_VARIANT_FUSED;
+  }
   int variant = prm->variant;
   if (variant == MHLA_VARIANT_AUTO) variant = tc_ok ? MHLA_VARIANT_MULTIPASS : MHLA_VARIANT_SIMT;
   if ((variant == MHLA_VARIANT_MULTIPASS || variant == MHLA_VARIANT_FUSED) && !tc_ok) return MHLA_ERR_UNSUPPORTED;
@@ -162,7 +170,9 @@ mhla_status make_plan(const mhla_params* prm, Plan* p, int split_units = 0) {
     p->splits = (nck + p->cpp - 1) / p->cpp;
     p->split_len = p->cpp * p->chunk.rows;
     p->Qp = (p->M * p->splits + 7) / 8 * 8;
-    p->f16_mix = p->norm != MHLA_NORM_MALA;
+    // the causal output step adds its in-block terms in float32 to the mixed
+    // prefix records: they stay in bf16 high + low planes (no fp16 scaling)
+    p->f16_mix = p->norm != MHLA_NORM_MALA && !p->causal;
     int lg = 0;
     while ((1 << lg) < p->split_len) ++lg;
     p->stack_scale = ldexpf(1.f, -lg);
@@ -205,7 +215,7 @@ mhla_status make_plan(const mhla_params* prm, Plan* p, int split_units = 0) {
     p->off_stack = off;
     off = align_up(off + stack);
     p->off_stack_lo = off;
-    if (p->norm == MHLA_NORM_MALA) off = align_up(off + stack);
+    if (p->norm == MHLA_NORM_MALA || p->causal) off = align_up(off + stack);
     p->off_mixed = off;
     off = align_up(off + mixed);
     p->off_mixed_lo = off;
@@ -227,6 +237,11 @@ mhla_status make_plan(const mhla_params* prm, Plan* p, int split_units = 0) {
       p->off_flow = off;
       off = align_up(off + 3 * sizeof(unsigned int) * (size_t)p->BH);
       p->kernels = 2;
+    }
+    if (p->causal) {
+      p->off_mcl = off;
+      off = align_up(off + sizeof(float) * (size_t)p->M * p->M * p->mc_heads);
+      p->kernels = 5;
     }
   }
   p->off_aux = off;
@@ -263,7 +278,8 @@ mhla_status run_plan(const Plan& plan, const void* q, const void* k, const void*
     const bool fused = p.variant == MHLA_VARIANT_FUSED;
     TcBuffers b;
     b.stack = ws + p.off_stack;
-    b.stack_lo = p.norm == MHLA_NORM_MALA ? reinterpret_cast<__nv_bfloat16*>(ws + p.off_stack_lo) : nullptr;
+    b.stack_lo = (p.norm == MHLA_NORM_MALA || p.causal) ? reinterpret_cast<__nv_bfloat16*>(ws + p.off_stack_lo)
+                                                          : nullptr;
     b.mixed_hi = reinterpret_cast<__nv_bfloat16*>(ws + p.off_mixed);
     b.mixed_lo = reinterpret_cast<__nv_bfloat16*>(ws + p.off_mixed_lo);
     b.mc_f16 = reinterpret_cast<__half*>(ws + p.off_mc_f16);
@@ -283,6 +299,23 @@ mhla_status run_plan(const Plan& plan, const void* q, const void* k, const void*
       record_event(1, s);
       record_event(2, s);
       if ((e = launch_tc_fused(p, p.chunk, q, k, v, b, out, s)) != 0) return cuda_fail((cudaError_t)e);
+      record_event(3, s);
+      return MHLA_OK;
+    }
+    if (p.causal) {
+      // records mixed with the strict lower triangle of Mc, every part in
+      // high + low planes (the MALA precision settings of the forward kernels)
+      Plan pr = p;
+      pr.norm = MHLA_NORM_MALA;
+      float* mcl = reinterpret_cast<float*>(ws + p.off_mcl);
+      if ((e = launch_mc_strict_lower(p, mc, mcl, s)) != 0) return cuda_fail((cudaError_t)e);
+      if ((e = launch_tc_prep(pr, mcl, b, s)) != 0) return cuda_fail((cudaError_t)e);
+      if ((e = launch_tc_summary(pr, pr.chunk, k, v, b, s)) != 0) return cuda_fail((cudaError_t)e);
+      record_event(1, s);
+      if ((e = launch_tc_mix(pr, b, s)) != 0) return cuda_fail((cudaError_t)e);
+      record_event(2, s);
+      if ((e = launch_tc_causal(p, q, k, v, b.mixed_hi, b.mixed_lo, mc, out, s)) != 0)
+        return cuda_fail((cudaError_t)e);
       record_event(3, s);
       return MHLA_OK;
     }
