@@ -134,10 +134,13 @@ typedef struct mhla_params {
                      * tokens ordered by (block, position inside the block),
                      * query t sees keys up to itself: earlier blocks through
                      * the strict lower triangle of Mc, its own block through
-                     * Mc[i, i] and only the tokens up to t.  Forward only, on
-                     * the float32 CUDA-core kernels (AUTO picks them;
-                     * MULTIPASS/FUSED and mhla_backward return
-                     * MHLA_ERR_UNSUPPORTED).                                */
+                     * Mc[i, i] and only the tokens up to t.  Forward only
+                     * (mhla_backward returns MHLA_ERR_UNSUPPORTED).  AUTO
+                     * takes the tensor cores for bf16, d = 64, DIVISIVE or
+                     * NONE when every token chunk is a contiguous run of its
+                     * block's local order, else the float32 kernels;
+                     * MULTIPASS outside that set and FUSED return
+                     * MHLA_ERR_UNSUPPORTED.                                 */
   int layout;       /* mhla_layout of the token tensors                    */
   int mc_per_head;  /* 0: mc is [M, M], shared by every (batch, head);
                      * 1: mc is [H, M, M], head h mixes with mc[h] (shared over
