@@ -186,3 +186,33 @@ def test_zero_denominator_rows_pass_no_gradient(norm, variant):
     ex, emc = backward_parity(w, norm, fmap="relu", inputs=(vals, dev), variant=variant)
     tol_mc = TOL_MC_SIMT_BF16 if variant == "simt" else TOL_MC["bf16"]
     assert ex <= TOL_X["bf16"] and emc <= tol_mc, f"{norm}/{variant}: {ex:.3e} {emc:.3e}"
+
+
+@pytest.mark.parametrize("name", ["seq_32k", "wan_21x30x50"])
+def test_full_size_backward_sampled_units(name):
+    # the full workload in the launch configuration the bench times: dq, dk,
+    # dv of sampled units against the oracle, and dMc through a property that
+    # holds at any size -- under DIVISIVE the output is invariant to scaling a
+    # row of Mc, so sum_b Mc[i,b] dMc[i,b] = 0 for every row i
+    import torch
+    w = wl.WORKLOADS[name]
+    vals, dev = wl.all_inputs(w)
+    gvals, gdev = wl.output_grad(w)
+    mc = wl.make_mc(w)
+    q, k, v = upload(w, dev)
+    (g,) = upload(w, [gdev])
+    dq, dk, dv, dmc = mb.mhla_backward(q, k, v, torch.from_numpy(mc).cuda(), g, w.grid, w.block, norm="divisive")
+    torch.cuda.synchronize()
+    code, detail = mb.mhla_device_status()
+    assert code == 0, (code, detail)
+    got = [download(x).reshape(w.units, w.n_tokens, w.head_dim) for x in (dq, dk, dv)]
+    for u in (0, w.units - 1):
+        b, h = divmod(u, w.heads)
+        want = orb.mhla_head_backward64(vals[0][b, h], vals[1][b, h], vals[2][b, h], mc, w.grid, w.block,
+                                        gvals[b, h], "elu1", "divisive")
+        for x, y in zip(got, want[:3]):
+            assert orc.relative_max_error(x[u], y) <= TOL_X["bf16"], (name, u)
+    dmc = dmc.cpu().numpy().astype(np.float64)
+    terms = mc.astype(np.float64) * dmc
+    assert np.all(np.isfinite(dmc))
+    assert np.max(np.abs(terms.sum(axis=1))) <= 2e-3 * np.max(np.abs(terms).sum(axis=1))
