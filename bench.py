@@ -348,7 +348,8 @@ def run_mine(args, w: wl.Workload, world: int, rank: int, local: int, dist):
     achieved = pbytes[dom] / (avg_phase[dom] / 1e3) / 1e9
     kname, ksrc = PHASE_KERNEL.get(info.variant, {}).get(dom, (dom, None))
     if args.causal and dom == "output":
-        kname, ksrc = "causal_output_kernel", "token_level_head_phi_gb300/csrc/simt_causal.cu"
+        kname, ksrc = (("tc_causal_kernel", "token_level_head_phi_gb300/csrc/tc_causal.cu") if info.variant == 2 else
+                       ("causal_output_kernel", "token_level_head_phi_gb300/csrc/simt_causal.cu"))
     traffic = None
     tt = traffic_table().get((kname, w.name))
     if tt and ksrc and tt[1] == source_hash(ksrc):
@@ -721,7 +722,7 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--pass", dest="pass_", default="forward", choices=["forward", "backward"])
     ap.add_argument("--feature-map", default="elu1", choices=["elu1", "relu", "exp"])
-    ap.add_argument("--causal", action="store_true", help="block-ordered causal forward (float32 kernels)")
+    ap.add_argument("--causal", action="store_true", help="block-ordered causal forward")
     ap.add_argument("--layout", default="bhnd", choices=["bhnd", "bnhd"], help="q/k/v/out memory layout")
     ap.add_argument("--mc-per-head", action="store_true", help="one mixing matrix per head")
     args = ap.parse_args()

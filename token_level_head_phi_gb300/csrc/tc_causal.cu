@@ -4,23 +4,26 @@
 // Query t of block i sees the earlier blocks through the strict lower
 // triangle of Mc and its own block up to itself through w = Mc[i, i] (the
 // block-ordered reading of "MHLA: Restoring Expressivity of Linear Attention
-// via Token-Level Multi-Head", key design 2 and its chunkwise remarks).  One
-// CTA walks the token chunks of one block in order (each chunk a contiguous
-// run of the block's local order); with P = phi(Q_c), F = phi(K_c):
-//   prefix  D_a  = P [S_state | Z_state]            (N = 80: numerator, s)
-//   scores  D_s  = P F^T                             (N = 128)
-//   intra   P~   = w * mask(D_s)  (j <= t; bf16)     rows summed in float32
-//           D_a += P~ V                              (numerator columns)
-//   MALA    D_v  = L V,  L = lower-triangular ones   (in-chunk prefix of V)
-//   state   D_u += F^T [V | 1]  (+ ones rows: sum V) for the next chunk:
-//           S_state = S<_i + w * D_u  (bf16 high + low planes)
-// where S<_i, z<_i, v<_i, n<_i are the records mixed with the strict lower
-// triangle (high + low planes).  Then
-//   s = D_a[64] + D_a[66] + rowsum(P~),  DIVISIVE o = num / s,  NONE o = num,
-//   MALA o = (1 + 1/s) num - (s / n~_t) v~_t,  v~_t = v_state + w D_v[t],
-//   n~_t = n_state + w (t + 1);  s = 0 gives o = 0.
-// Each CTA (128 threads, one row per thread) runs the chunk's phases in turn;
-// two CTAs share an SM so that one's MMAs overlap the other's epilogues.
+// via Token-Level Multi-Head", key design 2 and its chunkwise remarks).  The
+// token chunks of a block (each a contiguous run of the block's local order)
+// are taken in order; with P = phi(Q_c), F = phi(K_c):
+//   prefix  D_a  = P [S_hi | Z] + P S_lo          (N = 80: numerator, s parts)
+//   scores  D_s  = P F^T                          (N = 128)
+//   intra   P~   = w * mask(D_s)  (j <= t; bf16)
+//           D_a += P~ [V | e0]                    (numerator; row sum of P~ in column 64)
+//   state   D_u  = [F | e0]^T [V | e0]  for the next chunk:
+//           S_state = S<_i + w * sum of F^T V, z_state likewise with F^T 1
+//           (bf16 high + low planes; Z holds z_state as high, low columns)
+// where S<_i, z<_i are the records mixed with the strict lower triangle
+// (high + low planes) and e0 is a tile with a one in its first column.  Then
+//   s = D_a[64] + D_a[65],  DIVISIVE o = num / s,  NONE o = num;  s = 0 gives o = 0.
+// Persistent, warp-specialised CTA (512 threads, one per SM): warp 0 loads
+// Q, K, V (two token stages), warp 1 allocates TMEM and issues the MMAs,
+// warp 2 loads each unit's prefix record (two state buffers), warps 4-7
+// apply phi, warps 8-11 write P~, warps 12-15 update the state and write the
+// outputs.  A CTA takes its (head, block) units two at a time and alternates
+// their chunks, so one unit's carried-state chain overlaps the other's; D_a
+// and the output staging tile are double-buffered.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -35,24 +38,27 @@ namespace {
 
 using namespace tc;
 
-constexpr int kThreads = 128;
-constexpr uint32_t kTile = 128 * 128;   // 128 rows x 64 bf16
-constexpr uint32_t kBTile = 64 * 128;   // 64 rows x 64 bf16
+constexpr int kThreads = 512;
+constexpr int kGrpThreads = 128;                 // warps 4-7 (phi), 8-11 (scores), 12-15 (outputs, state)
+constexpr uint32_t kTile = 128 * 128;            // 128 rows x 64 bf16
+constexpr uint32_t kBTile = 64 * 128;            // 64 rows x 64 bf16
+constexpr int kStages = 2;
 // shared memory (offsets from the 1024-aligned base)
-constexpr uint32_t kOffQ = 0;                    // Q -> P -> O
-constexpr uint32_t kOffK = kTile;                // K -> F
-constexpr uint32_t kOffV = 2 * kTile;            // V
-constexpr uint32_t kOffPt = 3 * kTile;           // P~: two K-major atoms (j 0..63, 64..127)
-constexpr uint32_t kOffSt = 5 * kTile;           // state: S hi | S lo | Z (3 x 8 KB)
-constexpr uint32_t kOffOnes = kOffSt + 3 * kBTile;  // 16 rows of ones (bias atoms of the state MMA)
-constexpr uint32_t kOffZst = kOffOnes + 2048;    // z_state, 64 floats
-constexpr uint32_t kOffBars = kOffZst + 256;     // load barrier, MMA barrier, abort flag, TMEM slot
-constexpr uint32_t kSmemBytes = kOffBars + 32 + 1024;
-constexpr uint32_t kTmemCols = 256;
-// TMEM columns: D_a 0..79; D_s 128..255, reused by D_u 128..207 once read
-constexpr uint32_t kColA = 0, kColS = 128, kColU = 128;
-static_assert(kSmemBytes <= 232448 / 2, "two CTAs per SM");
-static_assert(kOffSt % 1024 == 0 && kOffOnes % 1024 == 0, "alignment");
+constexpr uint32_t kStageBytes = 3 * kTile;            // Q -> P | K -> F | V
+constexpr uint32_t kOffPt = kStages * kStageBytes;     // P~: two K-major atoms (j 0..63, 64..127)
+constexpr uint32_t kOffSt = kOffPt + 2 * kTile;        // two state buffers: S hi | S lo | Z
+constexpr uint32_t kStBytes = 3 * kBTile;
+constexpr uint32_t kOffO = kOffSt + 2 * kStBytes;      // two output staging tiles
+constexpr uint32_t kOffE0 = kOffO + 2 * kTile;         // 16 rows x 64, a one in column 0
+constexpr uint32_t kOffBars = kOffE0 + 2048;
+constexpr int kNumBars = 2 * 6 + 10;                   // six paired kinds + ten single slots
+constexpr uint32_t kSmemBytes = kOffBars + 8 * kNumBars + 16 + 1024;
+constexpr uint32_t kTmemCols = 512;
+// TMEM columns: D_a (two, 80 used) at 0 and 128, D_s 256..383, D_u 384..463
+constexpr uint32_t kColS = 256, kColU = 384;
+static_assert(kNumBars == 22, "barrier count");
+static_assert(kSmemBytes <= 232448, "shared memory");
+static_assert(kOffSt % 1024 == 0 && kOffO % 1024 == 0 && kOffE0 % 1024 == 0 && kStBytes % 1024 == 0, "alignment");
 
 struct CausalArgs {
   CUtensorMap tmQ, tmK, tmV, tmO;   // token maps (encode_token_map)
@@ -60,56 +66,135 @@ struct CausalArgs {
   const __nv_bfloat16* mixed_hi;    // prefix-mixed records (z< rows read directly)
   const __nv_bfloat16* mixed_lo;
   const float* mc;                  // Mc (its diagonal weighs the block's own tokens)
-  int R;
+  int R, units;                     // record length, (head, block) units
+  FastDiv f_m;                      // division by M
   ChunkShape c;
   unsigned int* err;
 };
 
-// all threads agree whether a bounded wait succeeded
-__device__ __forceinline__ bool wait_all(uint32_t bar, uint32_t parity, unsigned int* err, unsigned int where,
-                                         volatile int* abort_flag) {
-  const bool ok = mbar_wait(bar, parity, err, where, abort_flag);
-  return !__syncthreads_or(ok ? 0 : 1);
+// The chunks of this CTA in issue order.  Its units k = 0, 1, 2, ... (unit
+// w = blockIdx.x + k * gridDim.x, head u = w / M, block i = w % M) are taken
+// in pairs whose chunks alternate, (k, 0), (k+1, 0), (k, 1), (k+1, 1), ...:
+// each unit's chunks depend on one another through the carried state, the
+// two units of a pair do not.  n counts chunks; state buffer x = k & 1.
+struct ChunkIt {
+  int k0, side, k, w, u, i, c;
+  bool pair, valid;
+  long long n;
+};
+
+__device__ __forceinline__ void ci_set(const CausalArgs& a, const Plan& p, ChunkIt& it) {
+  it.k = it.k0 + it.side;
+  it.w = (int)blockIdx.x + it.k * (int)gridDim.x;
+  it.u = (int)fdiv((uint32_t)it.w, a.f_m);
+  it.i = it.w - it.u * p.M;
 }
 
-// Writes this thread's state rows k (< 64): S = hi + lo split again, and the
-// Z bias row (z hi, z hi, z lo) of the same k.
-__device__ __forceinline__ void put_z_row(uint8_t* gb, int k, float z) {
+__device__ __forceinline__ void ci_pair(const CausalArgs& a, ChunkIt& it) {
+  it.valid = (int)blockIdx.x + it.k0 * (int)gridDim.x < a.units;
+  it.pair = (int)blockIdx.x + (it.k0 + 1) * (int)gridDim.x < a.units;
+}
+
+__device__ __forceinline__ void ci_begin(const CausalArgs& a, const Plan& p, ChunkIt& it) {
+  it.k0 = 0;
+  it.side = 0;
+  it.c = 0;
+  it.n = 0;
+  ci_pair(a, it);
+  if (it.valid) ci_set(a, p, it);
+}
+
+__device__ __forceinline__ void ci_next(const CausalArgs& a, const Plan& p, ChunkIt& it) {
+  ++it.n;
+  if (it.side == 0 && it.pair) {
+    it.side = 1;
+  } else {
+    it.side = 0;
+    if (++it.c == a.c.per_block) {
+      it.c = 0;
+      it.k0 += 2;
+      ci_pair(a, it);
+    }
+  }
+  if (it.valid) ci_set(a, p, it);
+}
+
+__device__ __forceinline__ float diag_weight(const CausalArgs& a, const Plan& p, const ChunkIt& it) {
+  return a.mc[((size_t)mc_index(p, it.u) * p.M + it.i) * p.M + it.i];
+}
+
+// Z bias row k of a state buffer: z split as bf16 high (column 0) + low
+// (column 1); the rest of the tile stays zero.
+__device__ __forceinline__ void put_z_row(uint8_t* zt, int k, float z) {
   const __nv_bfloat16 zh = __float2bfloat16_rn(z);
   const __nv_bfloat16 zl = __float2bfloat16_rn(z - __bfloat162float(zh));
-  uint8_t* zt = gb + kOffSt + 2 * kBTile;
   *reinterpret_cast<__nv_bfloat16*>(zt + sw128_offset(k, 0)) = zh;
-  *reinterpret_cast<__nv_bfloat16*>(zt + sw128_offset(k, 1)) = zh;
-  *reinterpret_cast<__nv_bfloat16*>(zt + sw128_offset(k, 2)) = zl;
+  *reinterpret_cast<__nv_bfloat16*>(zt + sw128_offset(k, 1)) = zl;
 }
 
-__global__ void __launch_bounds__(kThreads, 2) tc_causal_kernel(const __grid_constant__ CausalArgs a, const Plan p) {
+__global__ void __launch_bounds__(kThreads, 1) tc_causal_kernel(const __grid_constant__ CausalArgs a, const Plan p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gb = smem_raw + (base - raw);
-  const uint32_t bar_ld = base + kOffBars, bar_mma = base + kOffBars + 8;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(gb + kOffBars + 16);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gb + kOffBars + 24);
-  float* zst = reinterpret_cast<float*>(gb + kOffZst);
-  const int t = threadIdx.x;
-  const int warp = t / 32;
-  const int u = blockIdx.y, i = blockIdx.x;
-  const int rows = a.c.rows, rows_pad = a.c.rows_pad, nck = a.c.per_block;
-  const float w = a.mc[((size_t)mc_index(p, u) * p.M + i) * p.M + i];
+  const uint32_t bars = base + kOffBars;
+  // paired barriers: slot 2 * kind + index
+  auto bar2 = [&](int kind, int x) { return bars + 8u * (uint32_t)(2 * kind + x); };
+  auto tfull = [&](int s) { return bar2(0, s); };    // Q, K, V landed (tx)
+  auto pready = [&](int s) { return bar2(1, s); };   // P, F written (4 warps)
+  auto tempty = [&](int s) { return bar2(2, s); };   // the stage's MMAs done (commit)
+  auto stfull = [&](int x) { return bar2(3, x); };   // S<, Z< of a unit in place (tx + warp 2)
+  auto stfree = [&](int x) { return bar2(4, x); };   // the unit's last prefix MMA done (commit)
+  auto stupd = [&](int x) { return bar2(5, x); };    // state updated for the next chunk (2 warps)
+  const uint32_t b1 = bars + 8u * 12u;
+  auto afull = [&](int x) { return b1 + 8u * (uint32_t)x; };        // numerator complete (commit)
+  auto afree = [&](int x) { return b1 + 16u + 8u * (uint32_t)x; };  // numerator read (4 warps)
+  const uint32_t sfull = b1 + 32, sfree = b1 + 40, ptready = b1 + 48, ptfree = b1 + 56, ufree = b1 + 64,
+                 mdone = b1 + 72;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gb + kOffBars + 8 * kNumBars);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gb + kOffBars + 8 * kNumBars + 8);
+  auto tst = [&](int s) { return base + (uint32_t)s * kStageBytes; };
+  auto stb = [&](int x) { return base + kOffSt + (uint32_t)x * kStBytes; };
+  auto obuf = [&](int x) { return base + kOffO + (uint32_t)x * kTile; };
 
-  // zero every tile (rows past a chunk stay finite), ones rows for the state MMA
-  for (uint32_t off = t * 16u; off < kOffOnes; off += kThreads * 16u)
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  const int rows = a.c.rows, rows_pad = a.c.rows_pad, nck = a.c.per_block;
+
+  // every tile starts zero (rows and columns past a chunk stay zero), e0 tile
+  for (uint32_t off = threadIdx.x * 16u; off < kOffBars; off += kThreads * 16u)
     *reinterpret_cast<uint4*>(gb + off) = make_uint4(0u, 0u, 0u, 0u);
-  for (uint32_t off = t * 16u; off < 2048u; off += kThreads * 16u)
-    *reinterpret_cast<uint4*>(gb + kOffOnes + off) = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
-  if (t == 0) {
-    mbar_init(bar_ld, 1);
-    mbar_init(bar_mma, 1);
+  __syncthreads();
+  if (threadIdx.x < 16) *reinterpret_cast<__nv_bfloat16*>(gb + kOffE0 + sw128_offset(threadIdx.x, 0)) = __float2bfloat16_rn(1.f);
+  if (threadIdx.x == 0) {
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(tfull(x), 1);
+      mbar_init(pready(x), kGrpThreads / 32);
+      mbar_init(tempty(x), 1);
+      mbar_init(stfull(x), 1);
+      mbar_init(stfree(x), 1);
+      mbar_init(stupd(x), 2);   // warps 12, 13 (state rows 0..63)
+      mbar_init(afull(x), 1);
+      mbar_init(afree(x), kGrpThreads / 32);
+    }
+    mbar_init(sfull, 1);
+    mbar_init(sfree, kGrpThreads / 32);
+    mbar_init(ptready, kGrpThreads / 32);
+    mbar_init(ptfree, 1);
+    mbar_init(ufree, 2);
+    mbar_init(mdone, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 0) {
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&a.tmQ);
+    tma_prefetch_desc(&a.tmK);
+    tma_prefetch_desc(&a.tmV);
+    tma_prefetch_desc(&a.tmO);
+    tma_prefetch_desc(&a.tmS_hi);
+    tma_prefetch_desc(&a.tmS_lo);
+  }
+  if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
@@ -118,218 +203,324 @@ __global__ void __launch_bounds__(kThreads, 2) tc_causal_kernel(const __grid_con
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t ta = tmem + ((uint32_t)(32 * warp) << 16);   // this warp's TMEM lanes
-  uint32_t ph_ld = 0, ph_mma = 0;
-  bool ok = true;
 
-  // ------------------------------------------- prefix record S<_i, z<_i
-  const int rec = u * p.M + i;
-  if (t == 0) {
-    mbar_arrive_expect_tx(bar_ld, 2 * kBTile);
-    tma_load_3d(base + kOffSt, &a.tmS_hi, bar_ld, 0, 0, rec, policy_evict_first());
-    tma_load_3d(base + kOffSt + kBTile, &a.tmS_lo, bar_ld, 0, 0, rec, policy_evict_first());
-  }
-  if (t < 64) {
-    const size_t zo = (size_t)rec * a.R + 64 * 64 + t;
-    zst[t] = __bfloat162float(a.mixed_hi[zo]) + __bfloat162float(a.mixed_lo[zo]);
-    put_z_row(gb, t, zst[t]);
-  }
-  ok = wait_all(bar_ld, ph_ld, a.err, 0x901, abort_flag);
-  ph_ld ^= 1u;
-
-  const uint32_t id_a = idesc_bf16_f32(128, 80, false, true);
-  const uint32_t id_a64 = idesc_bf16_f32(128, 64, false, true);
-  const uint32_t id_s = idesc_bf16_f32(128, 128, false, false);
-  const uint32_t id_v = idesc_bf16_f32(128, 64, false, true);
-  const uint32_t id_u = idesc_bf16_f32(128, 80, true, true);
-  const uint32_t q_s = base + kOffQ, k_s = base + kOffK, v_s = base + kOffV, pt_s = base + kOffPt;
-  const uint32_t sh = base + kOffSt, sl = sh + kBTile, zt = sh + 2 * kBTile, ones = base + kOffOnes;
-
-  for (int c = 0; c < nck && ok; ++c) {
-    int x0, y0, t0;
-    chunk_origin(p, a.c, (uint32_t)i, (uint32_t)c, x0, y0, t0);
-    const TileCoords g5 = token_tile_coords(p, u, x0, y0, t0);
-    // ------------------------------------------------------ loads
-    if (t == 0) {
-      bulk_wait_read<0>();   // the previous chunk's output has left the Q tile
-      const uint32_t bytes = (uint32_t)rows * 128u;
+  if (warp == 0) {
+    if (lane == 0) {
+      // -------------------------------------------- Q, K, V producer
       const uint64_t pol = policy_evict_first();
-      mbar_arrive_expect_tx(bar_ld, 3 * bytes);
-      tma_load_5d(q_s, &a.tmQ, bar_ld, g5.c[0], g5.c[1], g5.c[2], g5.c[3], g5.c[4], pol);
-      tma_load_5d(k_s, &a.tmK, bar_ld, g5.c[0], g5.c[1], g5.c[2], g5.c[3], g5.c[4], pol);
-      tma_load_5d(v_s, &a.tmV, bar_ld, g5.c[0], g5.c[1], g5.c[2], g5.c[3], g5.c[4], pol);
+      const uint32_t bytes = (uint32_t)rows * 128u;
+      long long issued = 0;
+      ChunkIt it;
+      for (ci_begin(a, p, it); it.valid; ci_next(a, p, it)) {
+        const int s = (int)(it.n % kStages);
+        if (!mbar_wait(tempty(s), (uint32_t)((it.n / kStages) & 1) ^ 1u, a.err, 0x911, abort_flag)) break;
+        int x0, y0, t0;
+        chunk_origin(p, a.c, (uint32_t)it.i, (uint32_t)it.c, x0, y0, t0);
+        const TileCoords g5 = token_tile_coords(p, it.u, x0, y0, t0);
+        mbar_arrive_expect_tx(tfull(s), 3 * bytes);
+        tma_load_5d(tst(s), &a.tmQ, tfull(s), g5.c[0], g5.c[1], g5.c[2], g5.c[3], g5.c[4], pol);
+        tma_load_5d(tst(s) + kTile, &a.tmK, tfull(s), g5.c[0], g5.c[1], g5.c[2], g5.c[3], g5.c[4], pol);
+        tma_load_5d(tst(s) + 2 * kTile, &a.tmV, tfull(s), g5.c[0], g5.c[1], g5.c[2], g5.c[3], g5.c[4], pol);
+        ++issued;
+      }
+      drain_loads(tfull(0), kStages, issued, a.err, 0x912);
     }
-    if (!(ok = wait_all(bar_ld, ph_ld, a.err, 0x902, abort_flag))) break;
-    ph_ld ^= 1u;
-    // ---------------------------------------- P = phi(Q), F = phi(K)
-    {
-      uint8_t* qr = gb + kOffQ + t * 128;
-      uint8_t* kr = gb + kOffK + t * 128;
+  } else if (warp == 2) {
+    // --------------------------- prefix records S<_i, z<_i, one per unit
+    long long issued = 0;
+    for (int k = 0; (int)blockIdx.x + k * (int)gridDim.x < a.units; ++k) {
+      const int x = k & 1;
+      bool ok = true;
+      if (lane == 0) ok = mbar_wait(stfree(x), (uint32_t)((k >> 1) & 1) ^ 1u, a.err, 0x913, abort_flag);
+      if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+      const int w = (int)blockIdx.x + k * (int)gridDim.x;
+      const int u = (int)fdiv((uint32_t)w, a.f_m);
+      const size_t rec = (size_t)u * p.M + (size_t)(w - u * p.M);
+      uint8_t* zt = gb + kOffSt + x * kStBytes + 2 * kBTile;
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int kk = lane + 32 * j;
+        const size_t zo = rec * a.R + 64 * 64 + kk;
+        put_z_row(zt, kk, __bfloat162float(a.mixed_hi[zo]) + __bfloat162float(a.mixed_lo[zo]));
+      }
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) {
+        const uint64_t pol = policy_evict_first();
+        mbar_arrive_expect_tx(stfull(x), 2 * kBTile);
+        tma_load_3d(stb(x), &a.tmS_hi, stfull(x), 0, 0, (int)rec, pol);
+        tma_load_3d(stb(x) + kBTile, &a.tmS_lo, stfull(x), 0, 0, (int)rec, pol);
+      }
+      ++issued;
+    }
+    if (lane == 0) drain_loads(stfull(0), 2, issued, a.err, 0x914);
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------------------------------------------------- MMA
+      // Per chunk: the prefix and score MMAs, then (once the scores
+      // epilogue has written P~) the in-chunk numerator and the state MMA.
+      const uint32_t id_a = idesc_bf16_f32(128, 80, false, true);
+      const uint32_t id_a64 = idesc_bf16_f32(128, 64, false, true);
+      const uint32_t id_s = idesc_bf16_f32(128, 128, false, false);
+      const uint32_t id_v = idesc_bf16_f32(128, 80, false, true);
+      const uint32_t id_u = idesc_bf16_f32(128, 80, true, true);
+      const uint32_t pt_s = base + kOffPt, e0 = base + kOffE0;
+      long long nupd0 = 0, nupd1 = 0, nu = 0;   // state updates waited for (buffers 0, 1); D_u uses
+      bool ok = true;
+      auto second_group = [&](int ps, long long pn, bool pmore) -> bool {
+        const uint32_t v_s = tst(ps) + 2 * kTile, k_s = tst(ps) + kTile;
+        if (!mbar_wait(ptready, (uint32_t)(pn & 1), a.err, 0x915, abort_flag)) return false;
+        if (pmore && nu > 0 && !mbar_wait(ufree, (uint32_t)((nu - 1) & 1), a.err, 0x916, abort_flag)) return false;
+        tc_fence_after();
+        const uint32_t DA = tmem + (uint32_t)(pn & 1) * 128u;
+        // D_a += P~ [V | e0]: numerator columns, and the row sum of P~ in column 64
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint32_t ao = (uint32_t)(ks >> 2) * kTile + (uint32_t)(ks & 3) * 32u;
+          const uint32_t va = v_s + (uint32_t)ks * 2048u;
+          umma_bf16(DA, sdesc_sw128(pt_s + ao, 0u, 1024u), sdesc_sw128(va, e0 - va, 1024u), id_v, 1u);
+        }
+        if (pmore) {
+          // D_u = [F | e0]^T [V | e0] over the chunk: rows 0..63 give F^T V and F^T 1
+          for (int kt = 0; kt < rows_pad / 16; ++kt) {
+            const uint32_t fa = k_s + (uint32_t)kt * 2048u, va = v_s + (uint32_t)kt * 2048u;
+            umma_bf16(tmem + kColU, sdesc_sw128(fa, e0 - fa, 1024u), sdesc_sw128(va, e0 - va, 1024u), id_u,
+                      kt > 0 ? 1u : 0u);
+          }
+          ++nu;
+        }
+        umma_commit(tempty(ps));
+        umma_commit(ptfree);
+        umma_commit(afull((int)(pn & 1)));
+        return true;
+      };
+      ChunkIt it;
+      for (ci_begin(a, p, it); it.valid && ok; ci_next(a, p, it)) {
+        const int s = (int)(it.n % kStages), x = it.k & 1, acc = (int)(it.n & 1);
+        if (it.c == 0) {
+          ok = mbar_wait(stfull(x), (uint32_t)((it.k >> 1) & 1), a.err, 0x917, abort_flag);
+        } else {
+          long long& nupd = x ? nupd1 : nupd0;
+          ok = mbar_wait(stupd(x), (uint32_t)(nupd & 1), a.err, 0x918, abort_flag);
+          ++nupd;
+        }
+        ok = ok && mbar_wait(pready(s), (uint32_t)((it.n / kStages) & 1), a.err, 0x919, abort_flag);
+        ok = ok && mbar_wait(afree(acc), (uint32_t)((it.n >> 1) & 1) ^ 1u, a.err, 0x91a, abort_flag);
+        ok = ok && mbar_wait(sfree, (uint32_t)(it.n & 1) ^ 1u, a.err, 0x91b, abort_flag);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t q_s = tst(s), k_s = q_s + kTile;
+        const uint32_t sh = stb(x), sl = sh + kBTile, zt = sh + 2 * kBTile;
+        const uint32_t DA = tmem + (uint32_t)acc * 128u;
+        // D_a = P [S_hi | Z] + P S_lo (prefix), D_s = P F^T (scores)
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          const uint64_t ap = sdesc_sw128(q_s + (uint32_t)ks * 32u, 0u, 1024u);
+          umma_bf16(DA, ap, sdesc_sw128(sh + (uint32_t)ks * 2048u, zt - sh, 1024u), id_a, ks > 0 ? 1u : 0u);
+          umma_bf16(DA, ap, sdesc_sw128(sl + (uint32_t)ks * 2048u, 0u, 1024u), id_a64, 1u);
+          umma_bf16(tmem + kColS, ap, sdesc_sw128(k_s + (uint32_t)ks * 32u, 0u, 1024u), id_s, ks > 0 ? 1u : 0u);
+        }
+        umma_commit(sfull);
+        if (it.c + 1 == nck) umma_commit(stfree(x));   // the unit's state buffer is read for the last time
+        if (!(ok = second_group(s, it.n, it.c + 1 < nck))) break;
+      }
+      // every MMA issued has completed before TMEM is released
+      umma_commit(mdone);
+      mbar_wait(mdone, 0u, a.err, 0x91c);
+    }
+  } else if (warp >= 4 && warp < 8) {
+    // --------------------------------------- P = phi(Q), F = phi(K)
+    const int t = threadIdx.x - 4 * 32;
+    ChunkIt it;
+    for (ci_begin(a, p, it); it.valid; ci_next(a, p, it)) {
+      const int s = (int)(it.n % kStages);
+      const bool ok = mbar_wait(tfull(s), (uint32_t)((it.n / kStages) & 1), a.err, 0x91d, abort_flag);
+      if (!named_all(9, kGrpThreads, ok)) break;
       if (t < rows) {
-#pragma unroll 2
-        for (int j = 0; j < 8; ++j) {
-          const uint32_t off = (uint32_t)(j << 4);
-          uint4 xq = *reinterpret_cast<const uint4*>(qr + off), xk = *reinterpret_cast<const uint4*>(kr + off);
-          uint32_t* pq = &xq.x;
-          uint32_t* pk = &xk.x;
+        // row t of Q, then of K: the whole 128-byte row in registers, its
+        // 16-byte chunks visited as j ^ t so that the eight rows of a
+        // quarter-warp touch eight different bank groups
+        for (int m = 0; m < 2; ++m) {
+          uint4* r = reinterpret_cast<uint4*>(gb + (tst(s) - base) + (uint32_t)m * kTile + t * 128);
+          uint4 xv[8];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 fq = bf16x2_to_float2(pq[e]), fk = bf16x2_to_float2(pk[e]);
-            pq[e] = pack_bf16x2(phi_map(fq.x, p.fmap), phi_map(fq.y, p.fmap));
-            pk[e] = pack_bf16x2(phi_map(fk.x, p.fmap), phi_map(fk.y, p.fmap));
+          for (int j = 0; j < 8; ++j) xv[j] = r[(j ^ t) & 7];
+          if (p.fmap == MHLA_FEATURE_ELU1) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              xv[j].x = phi2_elu1_bf16(xv[j].x);
+              xv[j].y = phi2_elu1_bf16(xv[j].y);
+              xv[j].z = phi2_elu1_bf16(xv[j].z);
+              xv[j].w = phi2_elu1_bf16(xv[j].w);
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              uint32_t* pw = &xv[j].x;
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float2 f = bf16x2_to_float2(pw[e]);
+                pw[e] = pack_bf16x2(phi_map(f.x, p.fmap), phi_map(f.y, p.fmap));
+              }
+            }
           }
-          *reinterpret_cast<uint4*>(qr + off) = xq;
-          *reinterpret_cast<uint4*>(kr + off) = xk;
-        }
-      } else if (t < rows_pad) {
-        for (int j = 0; j < 8; ++j) {
-          *reinterpret_cast<uint4*>(qr + (j << 4)) = make_uint4(0u, 0u, 0u, 0u);
-          *reinterpret_cast<uint4*>(kr + (j << 4)) = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) r[(j ^ t) & 7] = xv[j];
         }
       }
+      fence_proxy_async();
+      mbar_arrive_warp(pready(s));
     }
-    fence_proxy_async();
-    tc_fence_before();
-    __syncthreads();
-    // --------------------------------------------- MMA: prefix, scores
-    if (t == 0) {
+  } else if (warp >= 8 && warp < 12) {
+    // ------------------------------------ P~ = w mask(D_s), j <= t
+    const int e = warp - 8, t = threadIdx.x - 8 * 32;
+    const uint32_t ta = tmem + ((uint32_t)(32 * e) << 16);
+    uint8_t* prow = gb + kOffPt + t * 128;
+    ChunkIt it;
+    for (ci_begin(a, p, it); it.valid; ci_next(a, p, it)) {
+      const float w = diag_weight(a, p, it);
+      bool ok = mbar_wait(sfull, (uint32_t)(it.n & 1), a.err, 0x91e, abort_flag);
+      ok = ok && mbar_wait(ptfree, (uint32_t)(it.n & 1) ^ 1u, a.err, 0x91f, abort_flag);
+      if (!named_all(8, kGrpThreads, ok)) break;
       tc_fence_after();
+      // columns 32h .. 32h + 31 with h > e lie past every row of this warp
+      // and stay zero; two TMEM loads per wait
 #pragma unroll
-      for (int ks = 0; ks < 4; ++ks) {
-        const uint64_t ap = sdesc_sw128(q_s + (uint32_t)ks * 32u, 0u, 1024u);
-        umma_bf16(tmem + kColA, ap, sdesc_sw128(sh + (uint32_t)ks * 2048u, zt - sh, 1024u), id_a, ks > 0 ? 1u : 0u);
-        umma_bf16(tmem + kColA, ap, sdesc_sw128(sl + (uint32_t)ks * 2048u, 0u, 1024u), id_a64, 1u);
-        umma_bf16(tmem + kColS, ap, sdesc_sw128(k_s + (uint32_t)ks * 32u, 0u, 1024u), id_s, ks > 0 ? 1u : 0u);
-      }
-      umma_commit(bar_mma);
-    }
-    if (!(ok = wait_all(bar_mma, ph_mma, a.err, 0x903, abort_flag))) break;
-    ph_mma ^= 1u;
-    tc_fence_after();
-    // ------------------------------ P~ = w mask(D_s), its row sums
-    float rsum = 0.f;
-    {
-      uint8_t* prow = gb + kOffPt + t * 128;
-#pragma unroll 1
-      for (int h = 0; h < 4; ++h) {
-        float sc[32];
-        tmem_ld32(ta + kColS + 32u * h, sc);
+      for (int hp = 0; hp < 2; ++hp) {
+        if (2 * hp > e) break;
+        const bool two = 2 * hp + 1 <= e;
+        float sc[2][32];
+        tmem_ld32(ta + kColS + 64u * hp, sc[0]);
+        if (two) tmem_ld32(ta + kColS + 64u * hp + 32u, sc[1]);
         tmem_wait_ld();
-        uint8_t* atom = prow + (h >> 1) * kTile;   // j 0..63 -> atom 0, 64..127 -> atom 1
+        uint8_t* atom = prow + hp * kTile;   // j 0..63 -> atom 0, 64..127 -> atom 1
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint4 pk;
-          uint32_t* pp = &pk.x;
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int j0 = 32 * h + 8 * q + 2 * e;
-            const float v0 = (j0 <= t && t < rows) ? w * sc[8 * q + 2 * e] : 0.f;
-            const float v1 = (j0 + 1 <= t && t < rows) ? w * sc[8 * q + 2 * e + 1] : 0.f;
-            rsum += v0 + v1;
-            pp[e] = pack_bf16x2(v0, v1);
-          }
-          const int chunk = ((h & 1) * 4 + q);   // logical 16-byte chunk in the atom row
-          *reinterpret_cast<uint4*>(atom + (((chunk ^ t) & 7) << 4)) = pk;
-        }
-      }
-    }
-    fence_proxy_async();
-    tc_fence_before();
-    __syncthreads();
-    // -------------------------------------- MMA: intra, state update
-    const bool more = c + 1 < nck;
-    if (t == 0) {
-      tc_fence_after();
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        const uint32_t ao = (uint32_t)(ks >> 2) * kTile + (uint32_t)(ks & 3) * 32u;
-        umma_bf16(tmem + kColA, sdesc_sw128(pt_s + ao, 0u, 1024u), sdesc_sw128(v_s + (uint32_t)ks * 2048u, 0u, 1024u),
-                  id_v, 1u);
-      }
-      if (more) {
-        // D_u = F^T [V | 1] over this chunk's tokens (the summary's form)
-        for (int kt = 0; kt < rows_pad / 16; ++kt) {
-          const uint32_t fa = k_s + (uint32_t)kt * 2048u, va = v_s + (uint32_t)kt * 2048u;
-          umma_bf16(tmem + kColU, sdesc_sw128(fa, ones - fa, 1024u), sdesc_sw128(va, ones - va, 1024u), id_u,
-                    kt > 0 ? 1u : 0u);
-        }
-      }
-      umma_commit(bar_mma);
-    }
-    if (!(ok = wait_all(bar_mma, ph_mma, a.err, 0x904, abort_flag))) break;
-    ph_mma ^= 1u;
-    tc_fence_after();
-    // ------------------------------------------------------ output
-    {
-      float nm[32], zc[16];
-      tmem_ld16(ta + kColA + 64u, zc);
-      tmem_wait_ld();
-      const float s = zc[0] + zc[2] + rsum;
-      float scale = 1.f;
-      if (p.norm == MHLA_NORM_DIVISIVE) scale = s != 0.f ? 1.f / s : 0.f;
-      uint8_t* orow = gb + kOffQ + t * 128;
-#pragma unroll 1
-      for (int h = 0; h < 2; ++h) {
-        tmem_ld32(ta + kColA + 32u * h, nm);
-        tmem_wait_ld();
-        if (t < rows) {
+        for (int hh = 0; hh < 2; ++hh) {
+          if (hh == 1 && !two) break;
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            uint4 ov;
-            uint32_t* op = &ov.x;
+            uint32_t pk[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) op[e] = pack_bf16x2(nm[8 * q + 2 * e] * scale, nm[8 * q + 2 * e + 1] * scale);
-            *reinterpret_cast<uint4*>(orow + ((((4 * h + q) ^ t) & 7) << 4)) = ov;
+            for (int m = 0; m < 4; ++m) {
+              const int j0 = 64 * hp + 32 * hh + 8 * q + 2 * m;
+              const float v0 = (j0 <= t && t < rows) ? w * sc[hh][8 * q + 2 * m] : 0.f;
+              const float v1 = (j0 + 1 <= t && t < rows) ? w * sc[hh][8 * q + 2 * m + 1] : 0.f;
+              pk[m] = pack_bf16x2(v0, v1);
+            }
+            const int chunk = hh * 4 + q;   // logical 16-byte chunk in the atom row
+            *reinterpret_cast<uint4*>(atom + (((chunk ^ t) & 7) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
           }
         }
       }
+      tc_fence_before();
+      mbar_arrive_warp(sfree);
+      fence_proxy_async();
+      mbar_arrive_warp(ptready);
     }
-    // ------------------------------------ state for the next chunk
-    if (more && warp < 2) {
-      float dv[32], zc[16];
-      uint8_t* shr = gb + kOffSt + t * 128;
-      uint8_t* slr = shr + kBTile;
-#pragma unroll 1
-      for (int h = 0; h < 2; ++h) {
-        tmem_ld32(ta + kColU + 32u * h, dv);
+  } else if (warp >= 12) {
+    // ----------------------- state for the next chunk, then the outputs
+    const int e = warp - 12, t = threadIdx.x - 12 * 32;
+    const uint32_t ta = tmem + ((uint32_t)(32 * e) << 16);
+    float zr0 = 0.f, zr1 = 0.f;   // z state of row t (< 64) for state buffers 0, 1
+    ChunkIt it;
+    for (ci_begin(a, p, it); it.valid; ci_next(a, p, it)) {
+      const int acc = (int)(it.n & 1), x = it.k & 1;
+      const bool upd = it.c + 1 < nck && e < 2;
+      const float w = diag_weight(a, p, it);
+      bool ok = true;
+      float zin = 0.f;
+      if (upd && it.c == 0) {
+        const size_t zo = ((size_t)it.u * p.M + it.i) * a.R + 64 * 64 + t;
+        zin = __bfloat162float(a.mixed_hi[zo]) + __bfloat162float(a.mixed_lo[zo]);
+        ok = mbar_wait(stfull(x), (uint32_t)((it.k >> 1) & 1), a.err, 0x920, abort_flag);
+      }
+      ok = ok && mbar_wait(afull(acc), (uint32_t)((it.n >> 1) & 1), a.err, 0x921, abort_flag);
+      if (t == 0) bulk_wait_read<1>();   // staging tile acc: the store two chunks back has been read
+      if (!named_all(7, kGrpThreads, ok)) break;
+      tc_fence_after();
+      if (upd) {
+        // S_state += w F^T V (bf16 high + low), z_state += w F^T 1
+        float dv[2][32], zc[16];
+        uint8_t* shr = gb + kOffSt + x * kStBytes + t * 128;
+        uint8_t* slr = shr + kBTile;
+        tmem_ld32(ta + kColU, dv[0]);
+        tmem_ld32(ta + kColU + 32u, dv[1]);
+        tmem_ld16(ta + kColU + 64u, zc);
         tmem_wait_ld();
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint32_t off = (uint32_t)((((4 * h + q) ^ t) & 7) << 4);
-          uint4 hv = *reinterpret_cast<const uint4*>(shr + off), lv = *reinterpret_cast<const uint4*>(slr + off);
-          uint32_t* hp = &hv.x;
-          uint32_t* lp = &lv.x;
+        for (int h = 0; h < 2; ++h) {
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 fh = bf16x2_to_float2(hp[e]), fl = bf16x2_to_float2(lp[e]);
-            const float y0 = fh.x + fl.x + w * dv[8 * q + 2 * e], y1 = fh.y + fl.y + w * dv[8 * q + 2 * e + 1];
-            hp[e] = pack_bf16x2(y0, y1);
-            const float2 g = bf16x2_to_float2(hp[e]);
-            lp[e] = pack_bf16x2(y0 - g.x, y1 - g.y);
+          for (int q = 0; q < 4; ++q) {
+            const uint32_t off = (uint32_t)((((4 * h + q) ^ t) & 7) << 4);
+            uint4 hv = *reinterpret_cast<const uint4*>(shr + off), lv = *reinterpret_cast<const uint4*>(slr + off);
+            uint32_t* hp = &hv.x;
+            uint32_t* lp = &lv.x;
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+              const float2 fh = bf16x2_to_float2(hp[m]), fl = bf16x2_to_float2(lp[m]);
+              const float y0 = fh.x + fl.x + w * dv[h][8 * q + 2 * m], y1 = fh.y + fl.y + w * dv[h][8 * q + 2 * m + 1];
+              hp[m] = pack_bf16x2(y0, y1);
+              const float2 g = bf16x2_to_float2(hp[m]);
+              lp[m] = pack_bf16x2(y0 - g.x, y1 - g.y);
+            }
+            *reinterpret_cast<uint4*>(shr + off) = hv;
+            *reinterpret_cast<uint4*>(slr + off) = lv;
           }
-          *reinterpret_cast<uint4*>(shr + off) = hv;
-          *reinterpret_cast<uint4*>(slr + off) = lv;
+        }
+        const float zn = (it.c == 0 ? zin : (x ? zr1 : zr0)) + w * zc[0];
+        if (x) zr1 = zn;
+        else zr0 = zn;
+        put_z_row(gb + kOffSt + x * kStBytes + 2 * kBTile, t, zn);
+        tc_fence_before();
+        fence_proxy_async();
+        mbar_arrive_warp(ufree);
+        mbar_arrive_warp(stupd(x));
+      }
+      {
+        // s = P z_state + rowsum(P~) (columns 64, 65); DIVISIVE o = num / s
+        float nm[2][32], zc[16];
+        const uint32_t DA = ta + (uint32_t)acc * 128u;
+        tmem_ld32(DA, nm[0]);
+        tmem_ld32(DA + 32u, nm[1]);
+        tmem_ld16(DA + 64u, zc);
+        tmem_wait_ld();
+        const float s = zc[0] + zc[1];
+        float scale = 1.f;
+        if (p.norm == MHLA_NORM_DIVISIVE) scale = s != 0.f ? 1.f / s : 0.f;
+        uint8_t* orow = gb + kOffO + acc * kTile + t * 128;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          if (t < rows) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint4 ov;
+              uint32_t* op = &ov.x;
+#pragma unroll
+              for (int m = 0; m < 4; ++m)
+                op[m] = pack_bf16x2(nm[h][8 * q + 2 * m] * scale, nm[h][8 * q + 2 * m + 1] * scale);
+              *reinterpret_cast<uint4*>(orow + ((((4 * h + q) ^ t) & 7) << 4)) = ov;
+            }
+          }
         }
       }
-      tmem_ld16(ta + kColU + 64u, zc);
-      tmem_wait_ld();
-      zst[t] += w * zc[0];
-      put_z_row(gb, t, zst[t]);
-    } else if (more) {
-      // warps 2, 3 hold TMEM lanes 64..127 of D_u (the ones rows): nothing to keep
+      tc_fence_before();
+      mbar_arrive_warp(afree(acc));
+      fence_proxy_async();
+      named_sync(7, kGrpThreads);
+      if (t == 0) {
+        int x0, y0, t0;
+        chunk_origin(p, a.c, (uint32_t)it.i, (uint32_t)it.c, x0, y0, t0);
+        const TileCoords g5 = token_tile_coords(p, it.u, x0, y0, t0);
+        tma_store_5d(&a.tmO, obuf(acc), g5.c[0], g5.c[1], g5.c[2], g5.c[3], g5.c[4]);
+        bulk_commit();
+      }
     }
-    fence_proxy_async();
-    tc_fence_before();
-    __syncthreads();
-    if (t == 0) {
-      tma_store_5d(&a.tmO, q_s, g5.c[0], g5.c[1], g5.c[2], g5.c[3], g5.c[4]);
-      bulk_commit();
-    }
+    if (t == 0) bulk_wait<0>();
   }
-  if (t == 0) bulk_wait<0>();
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
 }  // namespace
@@ -363,11 +554,14 @@ int launch_tc_causal(const Plan& p, const void* q, const void* k, const void* v,
   a.mixed_lo = mixed_lo;
   a.mc = mc;
   a.R = p.R;
+  a.units = p.BH * p.M;
+  a.f_m = make_fastdiv((uint32_t)p.M);
   a.c = c;
   a.err = p.err;
   cudaError_t ce = cudaFuncSetAttribute(tc_causal_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (ce != cudaSuccess) return (int)ce;
-  tc_causal_kernel<<<dim3(p.M, p.BH), kThreads, kSmemBytes, s>>>(a, p);
+  const int grid = a.units < num_sms() ? a.units : num_sms();
+  tc_causal_kernel<<<grid, kThreads, kSmemBytes, s>>>(a, p);
   return (int)cudaGetLastError();
 }
 
