@@ -7,23 +7,26 @@
 // via Token-Level Multi-Head", key design 2 and its chunkwise remarks).  The
 // token chunks of a block (each a contiguous run of the block's local order)
 // are taken in order; with P = phi(Q_c), F = phi(K_c):
-//   prefix  D_a  = P [S_hi | Z] + P S_lo          (N = 80: numerator, s parts)
-//   scores  D_s  = P F^T                          (N = 128)
-//   intra   P~   = w * mask(D_s)  (j <= t; bf16)
-//           D_a += P~ [V | e0]                    (numerator; row sum of P~ in column 64)
+//   prefix  D_a  = P S_hi + P S_lo  |  P Z          (numerator columns | s parts)
+//   scores  D_s  = P F^T                           (N = 128)
+//   intra   P~   = w * mask(D_s)  (j <= t; bf16, kept in TMEM)
+//           D_a += P~ [V | e0]                     (numerator; row sum of P~ in column 64)
 //   state   D_u  = [F | e0]^T [V | e0]  for the next chunk:
 //           S_state = S<_i + w * sum of F^T V, z_state likewise with F^T 1
-//           (bf16 high + low planes; Z holds z_state as high, low columns)
+//           (S as bf16 high + low planes; Z a K-major tile with z_state's
+//           bf16 high part in row 0 and low part in row 1)
 // where S<_i, z<_i are the records mixed with the strict lower triangle
 // (high + low planes) and e0 is a tile with a one in its first column.  Then
 //   s = D_a[64] + D_a[65],  DIVISIVE o = num / s,  NONE o = num;  s = 0 gives o = 0.
 // Persistent, warp-specialised CTA (512 threads, one per SM): warp 0 loads
-// Q, K, V (two token stages), warp 1 allocates TMEM and issues the MMAs,
+// Q, K, V (three token stages), warp 1 allocates TMEM and issues the MMAs,
 // warp 2 loads each unit's prefix record (two state buffers), warps 4-7
 // apply phi, warps 8-11 write P~, warps 12-15 update the state and write the
 // outputs.  A CTA takes its (head, block) units two at a time and alternates
-// their chunks, so one unit's carried-state chain overlaps the other's; D_a
-// and the output staging tile are double-buffered.
+// their chunks, so one unit's carried-state chain overlaps the other's; the
+// MMA warp issues whichever group is ready, so a chunk's prefix and scores
+// run while the previous chunk's scores epilogue works; D_a and the output
+// staging tile are double-buffered.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -42,21 +45,21 @@ constexpr int kThreads = 512;
 constexpr int kGrpThreads = 128;                 // warps 4-7 (phi), 8-11 (scores), 12-15 (outputs, state)
 constexpr uint32_t kTile = 128 * 128;            // 128 rows x 64 bf16
 constexpr uint32_t kBTile = 64 * 128;            // 64 rows x 64 bf16
-constexpr int kStages = 2;
+constexpr int kStages = 3;
 // shared memory (offsets from the 1024-aligned base)
 constexpr uint32_t kStageBytes = 3 * kTile;            // Q -> P | K -> F | V
-constexpr uint32_t kOffPt = kStages * kStageBytes;     // P~: two K-major atoms (j 0..63, 64..127)
-constexpr uint32_t kOffSt = kOffPt + 2 * kTile;        // two state buffers: S hi | S lo | Z
-constexpr uint32_t kStBytes = 3 * kBTile;
+constexpr uint32_t kOffSt = kStages * kStageBytes;     // two state buffers: S hi | S lo | Z (K-major, 16 rows)
+constexpr uint32_t kStBytes = 2 * kBTile + 2048;
 constexpr uint32_t kOffO = kOffSt + 2 * kStBytes;      // two output staging tiles
 constexpr uint32_t kOffE0 = kOffO + 2 * kTile;         // 16 rows x 64, a one in column 0
 constexpr uint32_t kOffBars = kOffE0 + 2048;
-constexpr int kNumBars = 2 * 6 + 10;                   // six paired kinds + ten single slots
+constexpr int kNumBars = 3 * kStages + 5 * 2 + 6;
 constexpr uint32_t kSmemBytes = kOffBars + 8 * kNumBars + 16 + 1024;
 constexpr uint32_t kTmemCols = 512;
-// TMEM columns: D_a (two, 80 used) at 0 and 128, D_s 256..383, D_u 384..463
-constexpr uint32_t kColS = 256, kColU = 384;
-static_assert(kNumBars == 22, "barrier count");
+// TMEM columns: D_a (two, 80 used) at 0 and 96, D_s 192..319, D_u 320..399,
+// P~ 416..479 (bf16 pairs, the A operand of the numerator MMA)
+constexpr uint32_t kColS = 192, kColU = 320, kColP = 416;
+__device__ __forceinline__ uint32_t col_a(int acc) { return acc ? 96u : 0u; }
 static_assert(kSmemBytes <= 232448, "shared memory");
 static_assert(kOffSt % 1024 == 0 && kOffO % 1024 == 0 && kOffE0 % 1024 == 0 && kStBytes % 1024 == 0, "alignment");
 
@@ -123,13 +126,13 @@ __device__ __forceinline__ float diag_weight(const CausalArgs& a, const Plan& p,
   return a.mc[((size_t)mc_index(p, it.u) * p.M + it.i) * p.M + it.i];
 }
 
-// Z bias row k of a state buffer: z split as bf16 high (column 0) + low
-// (column 1); the rest of the tile stays zero.
-__device__ __forceinline__ void put_z_row(uint8_t* zt, int k, float z) {
+// Feature k of the z state in the K-major Z tile: bf16 high part in row 0,
+// low part in row 1 (rows 2..15 stay zero).
+__device__ __forceinline__ void put_z(uint8_t* zt, int k, float z) {
   const __nv_bfloat16 zh = __float2bfloat16_rn(z);
   const __nv_bfloat16 zl = __float2bfloat16_rn(z - __bfloat162float(zh));
-  *reinterpret_cast<__nv_bfloat16*>(zt + sw128_offset(k, 0)) = zh;
-  *reinterpret_cast<__nv_bfloat16*>(zt + sw128_offset(k, 1)) = zl;
+  *reinterpret_cast<__nv_bfloat16*>(zt + sw128_offset(0, k)) = zh;
+  *reinterpret_cast<__nv_bfloat16*>(zt + sw128_offset(1, k)) = zl;
 }
 
 __global__ void __launch_bounds__(kThreads, 1) tc_causal_kernel(const __grid_constant__ CausalArgs a, const Plan p) {
@@ -138,19 +141,18 @@ __global__ void __launch_bounds__(kThreads, 1) tc_causal_kernel(const __grid_con
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gb = smem_raw + (base - raw);
   const uint32_t bars = base + kOffBars;
-  // paired barriers: slot 2 * kind + index
-  auto bar2 = [&](int kind, int x) { return bars + 8u * (uint32_t)(2 * kind + x); };
-  auto tfull = [&](int s) { return bar2(0, s); };    // Q, K, V landed (tx)
-  auto pready = [&](int s) { return bar2(1, s); };   // P, F written (4 warps)
-  auto tempty = [&](int s) { return bar2(2, s); };   // the stage's MMAs done (commit)
-  auto stfull = [&](int x) { return bar2(3, x); };   // S<, Z< of a unit in place (tx + warp 2)
-  auto stfree = [&](int x) { return bar2(4, x); };   // the unit's last prefix MMA done (commit)
-  auto stupd = [&](int x) { return bar2(5, x); };    // state updated for the next chunk (2 warps)
-  const uint32_t b1 = bars + 8u * 12u;
-  auto afull = [&](int x) { return b1 + 8u * (uint32_t)x; };        // numerator complete (commit)
-  auto afree = [&](int x) { return b1 + 16u + 8u * (uint32_t)x; };  // numerator read (4 warps)
-  const uint32_t sfull = b1 + 32, sfree = b1 + 40, ptready = b1 + 48, ptfree = b1 + 56, ufree = b1 + 64,
-                 mdone = b1 + 72;
+  auto tfull = [&](int s) { return bars + 8u * (uint32_t)s; };                 // Q, K, V landed (tx)
+  auto pready = [&](int s) { return bars + 8u * (uint32_t)(kStages + s); };    // P, F written (4 warps)
+  auto tempty = [&](int s) { return bars + 8u * (uint32_t)(2 * kStages + s); };  // the stage's MMAs done
+  const uint32_t b2 = bars + 8u * (uint32_t)(3 * kStages);
+  auto stfull = [&](int x) { return b2 + 8u * (uint32_t)x; };        // S<, Z< of a unit in place (tx)
+  auto stfree = [&](int x) { return b2 + 16u + 8u * (uint32_t)x; };  // the unit's last prefix MMA done
+  auto stupd = [&](int x) { return b2 + 32u + 8u * (uint32_t)x; };   // state updated for the next chunk (2 warps)
+  auto afull = [&](int x) { return b2 + 48u + 8u * (uint32_t)x; };   // numerator complete (commit)
+  auto afree = [&](int x) { return b2 + 64u + 8u * (uint32_t)x; };   // numerator read (4 warps)
+  const uint32_t b1 = b2 + 80u;
+  const uint32_t sfull = b1, sfree = b1 + 8, ptready = b1 + 16, ptfree = b1 + 24, ufree = b1 + 32, mdone = b1 + 40;
+  static_assert(8 * (3 * kStages) + 80 + 48 == 8 * kNumBars, "barrier slots");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gb + kOffBars + 8 * kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gb + kOffBars + 8 * kNumBars + 8);
   auto tst = [&](int s) { return base + (uint32_t)s * kStageBytes; };
@@ -165,12 +167,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc_causal_kernel(const __grid_con
   for (uint32_t off = threadIdx.x * 16u; off < kOffBars; off += kThreads * 16u)
     *reinterpret_cast<uint4*>(gb + off) = make_uint4(0u, 0u, 0u, 0u);
   __syncthreads();
-  if (threadIdx.x < 16) *reinterpret_cast<__nv_bfloat16*>(gb + kOffE0 + sw128_offset(threadIdx.x, 0)) = __float2bfloat16_rn(1.f);
+  if (threadIdx.x < 16)
+    *reinterpret_cast<__nv_bfloat16*>(gb + kOffE0 + sw128_offset(threadIdx.x, 0)) = __float2bfloat16_rn(1.f);
   if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(tfull(s), 1);
+      mbar_init(pready(s), kGrpThreads / 32);
+      mbar_init(tempty(s), 1);
+    }
     for (int x = 0; x < 2; ++x) {
-      mbar_init(tfull(x), 1);
-      mbar_init(pready(x), kGrpThreads / 32);
-      mbar_init(tempty(x), 1);
       mbar_init(stfull(x), 1);
       mbar_init(stfree(x), 1);
       mbar_init(stupd(x), 2);   // warps 12, 13 (state rows 0..63)
@@ -241,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_causal_kernel(const __grid_con
       for (int j = 0; j < 2; ++j) {
         const int kk = lane + 32 * j;
         const size_t zo = rec * a.R + 64 * 64 + kk;
-        put_z_row(zt, kk, __bfloat162float(a.mixed_hi[zo]) + __bfloat162float(a.mixed_lo[zo]));
+        put_z(zt, kk, __bfloat162float(a.mixed_hi[zo]) + __bfloat162float(a.mixed_lo[zo]));
       }
       fence_proxy_async();
       __syncwarp();
@@ -257,72 +262,117 @@ __global__ void __launch_bounds__(kThreads, 1) tc_causal_kernel(const __grid_con
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------------------------------------------------- MMA
-      // Per chunk: the prefix and score MMAs, then (once the scores
-      // epilogue has written P~) the in-chunk numerator and the state MMA.
-      const uint32_t id_a = idesc_bf16_f32(128, 80, false, true);
-      const uint32_t id_a64 = idesc_bf16_f32(128, 64, false, true);
+      // Two groups per chunk: prefix + scores (once its P, F and state are
+      // in place), then numerator + state (once the scores epilogue has
+      // written P~).  Whichever is ready goes first, numerator groups in
+      // chunk order, so a chunk's prefix and scores can run while the
+      // previous chunk's scores epilogue works.
+      const uint32_t id_s64 = idesc_bf16_f32(128, 64, false, true);
+      const uint32_t id_z = idesc_bf16_f32(128, 16, false, false);
       const uint32_t id_s = idesc_bf16_f32(128, 128, false, false);
       const uint32_t id_v = idesc_bf16_f32(128, 80, false, true);
       const uint32_t id_u = idesc_bf16_f32(128, 80, true, true);
-      const uint32_t pt_s = base + kOffPt, e0 = base + kOffE0;
-      long long nupd0 = 0, nupd1 = 0, nu = 0;   // state updates waited for (buffers 0, 1); D_u uses
-      bool ok = true;
-      auto second_group = [&](int ps, long long pn, bool pmore) -> bool {
-        const uint32_t v_s = tst(ps) + 2 * kTile, k_s = tst(ps) + kTile;
-        if (!mbar_wait(ptready, (uint32_t)(pn & 1), a.err, 0x915, abort_flag)) return false;
-        if (pmore && nu > 0 && !mbar_wait(ufree, (uint32_t)((nu - 1) & 1), a.err, 0x916, abort_flag)) return false;
-        tc_fence_after();
-        const uint32_t DA = tmem + (uint32_t)(pn & 1) * 128u;
-        // D_a += P~ [V | e0]: numerator columns, and the row sum of P~ in column 64
+      const uint32_t e0 = base + kOffE0;
+      long long nupd0 = 0, nupd1 = 0, nu = 0;
+      long long qn0 = 0, qn1 = 0;   // chunks waiting for their second group (oldest first)
+      bool qm0 = false, qm1 = false;
+      int nq = 0;
+      unsigned long long idle_since = 0;
+      ChunkIt nx;
+      ci_begin(a, p, nx);
+      while (nx.valid || nq > 0) {
+        bool did = false;
+        if (nq > 0 && mbar_test(ptready, (uint32_t)(qn0 & 1)) &&
+            (!qm0 || nu == 0 || mbar_test(ufree, (uint32_t)((nu - 1) & 1)))) {
+          // D_a += P~ [V | e0] (numerator; row sum of P~ in column 64), and
+          // D_u = [F | e0]^T [V | e0] when another chunk of the unit follows
+          tc_fence_after();
+          const int ps = (int)(qn0 % kStages);
+          const uint32_t k_s = tst(ps) + kTile, v_s = tst(ps) + 2 * kTile;
+          const uint32_t DA = tmem + col_a((int)(qn0 & 1));
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          const uint32_t ao = (uint32_t)(ks >> 2) * kTile + (uint32_t)(ks & 3) * 32u;
-          const uint32_t va = v_s + (uint32_t)ks * 2048u;
-          umma_bf16(DA, sdesc_sw128(pt_s + ao, 0u, 1024u), sdesc_sw128(va, e0 - va, 1024u), id_v, 1u);
-        }
-        if (pmore) {
-          // D_u = [F | e0]^T [V | e0] over the chunk: rows 0..63 give F^T V and F^T 1
-          for (int kt = 0; kt < rows_pad / 16; ++kt) {
-            const uint32_t fa = k_s + (uint32_t)kt * 2048u, va = v_s + (uint32_t)kt * 2048u;
-            umma_bf16(tmem + kColU, sdesc_sw128(fa, e0 - fa, 1024u), sdesc_sw128(va, e0 - va, 1024u), id_u,
-                      kt > 0 ? 1u : 0u);
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t va = v_s + (uint32_t)ks * 2048u;
+            umma_tmem_a(DA, tmem + kColP + (uint32_t)ks * 8u, sdesc_sw128(va, e0 - va, 1024u), id_v, 1u);
           }
-          ++nu;
-        }
-        umma_commit(tempty(ps));
-        umma_commit(ptfree);
-        umma_commit(afull((int)(pn & 1)));
-        return true;
-      };
-      ChunkIt it;
-      for (ci_begin(a, p, it); it.valid && ok; ci_next(a, p, it)) {
-        const int s = (int)(it.n % kStages), x = it.k & 1, acc = (int)(it.n & 1);
-        if (it.c == 0) {
-          ok = mbar_wait(stfull(x), (uint32_t)((it.k >> 1) & 1), a.err, 0x917, abort_flag);
-        } else {
-          long long& nupd = x ? nupd1 : nupd0;
-          ok = mbar_wait(stupd(x), (uint32_t)(nupd & 1), a.err, 0x918, abort_flag);
-          ++nupd;
-        }
-        ok = ok && mbar_wait(pready(s), (uint32_t)((it.n / kStages) & 1), a.err, 0x919, abort_flag);
-        ok = ok && mbar_wait(afree(acc), (uint32_t)((it.n >> 1) & 1) ^ 1u, a.err, 0x91a, abort_flag);
-        ok = ok && mbar_wait(sfree, (uint32_t)(it.n & 1) ^ 1u, a.err, 0x91b, abort_flag);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t q_s = tst(s), k_s = q_s + kTile;
-        const uint32_t sh = stb(x), sl = sh + kBTile, zt = sh + 2 * kBTile;
-        const uint32_t DA = tmem + (uint32_t)acc * 128u;
-        // D_a = P [S_hi | Z] + P S_lo (prefix), D_s = P F^T (scores)
+          if (qm0) {
+            for (int kt = 0; kt < rows_pad / 16; ++kt) {
+              const uint32_t fa = k_s + (uint32_t)kt * 2048u, va = v_s + (uint32_t)kt * 2048u;
+              umma_bf16(tmem + kColU, sdesc_sw128(fa, e0 - fa, 1024u), sdesc_sw128(va, e0 - va, 1024u), id_u,
+                        kt > 0 ? 1u : 0u);
+            }
+            ++nu;
+          }
+          umma_commit(tempty(ps));
+          umma_commit(ptfree);
+          umma_commit(afull((int)(qn0 & 1)));
+          qn0 = qn1;
+          qm0 = qm1;
+          --nq;
+          did = true;
+        } else if (nx.valid && nq < 2) {
+          const int s = (int)(nx.n % kStages), x = nx.k & 1, acc = (int)(nx.n & 1);
+          const long long nupd = x ? nupd1 : nupd0;
+          bool ready = nx.c == 0 ? mbar_test(stfull(x), (uint32_t)((nx.k >> 1) & 1))
+                                 : mbar_test(stupd(x), (uint32_t)(nupd & 1));
+          ready = ready && mbar_test(pready(s), (uint32_t)((nx.n / kStages) & 1)) &&
+                  mbar_test(afree(acc), (uint32_t)((nx.n >> 1) & 1) ^ 1u) &&
+                  mbar_test(sfree, (uint32_t)(nx.n & 1) ^ 1u);
+          if (ready) {
+            if (nx.c > 0) {
+              if (x) ++nupd1;
+              else ++nupd0;
+            }
+            tc_fence_after();
+            // D_a = P S_hi + P S_lo | P Z (prefix), D_s = P F^T (scores)
+            const uint32_t q_s = tst(s), k_s = q_s + kTile;
+            const uint32_t sh = stb(x), sl = sh + kBTile, zt = sh + 2 * kBTile;
+            const uint32_t DA = tmem + col_a(acc);
+            // one shape at a time: scores first (the scores epilogue waits
+            // for them), then the prefix parts
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-          const uint64_t ap = sdesc_sw128(q_s + (uint32_t)ks * 32u, 0u, 1024u);
-          umma_bf16(DA, ap, sdesc_sw128(sh + (uint32_t)ks * 2048u, zt - sh, 1024u), id_a, ks > 0 ? 1u : 0u);
-          umma_bf16(DA, ap, sdesc_sw128(sl + (uint32_t)ks * 2048u, 0u, 1024u), id_a64, 1u);
-          umma_bf16(tmem + kColS, ap, sdesc_sw128(k_s + (uint32_t)ks * 32u, 0u, 1024u), id_s, ks > 0 ? 1u : 0u);
+            for (int ks = 0; ks < 4; ++ks)
+              umma_bf16(tmem + kColS, sdesc_sw128(q_s + (uint32_t)ks * 32u, 0u, 1024u),
+                        sdesc_sw128(k_s + (uint32_t)ks * 32u, 0u, 1024u), id_s, ks > 0 ? 1u : 0u);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+              const uint32_t sp = (ks < 4 ? sh : sl) + (uint32_t)(ks & 3) * 2048u;
+              umma_bf16(DA, sdesc_sw128(q_s + (uint32_t)(ks & 3) * 32u, 0u, 1024u), sdesc_sw128(sp, 0u, 1024u), id_s64,
+                        ks > 0 ? 1u : 0u);
+            }
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+              umma_bf16(DA + 64u, sdesc_sw128(q_s + (uint32_t)ks * 32u, 0u, 1024u),
+                        sdesc_sw128(zt + (uint32_t)ks * 32u, 0u, 1024u), id_z, ks > 0 ? 1u : 0u);
+            umma_commit(sfull);
+            if (nx.c + 1 == nck) umma_commit(stfree(x));   // the unit's state buffer is read for the last time
+            if (nq == 0) {
+              qn0 = nx.n;
+              qm0 = nx.c + 1 < nck;
+            } else {
+              qn1 = nx.n;
+              qm1 = nx.c + 1 < nck;
+            }
+            ++nq;
+            ci_next(a, p, nx);
+            did = true;
+          }
         }
-        umma_commit(sfull);
-        if (it.c + 1 == nck) umma_commit(stfree(x));   // the unit's state buffer is read for the last time
-        if (!(ok = second_group(s, it.n, it.c + 1 < nck))) break;
+        if (did) {
+          idle_since = 0;
+          continue;
+        }
+        // nothing ready: bounded polling
+        if (*abort_flag) break;
+        const unsigned long long now = globaltimer();
+        if (idle_since == 0) {
+          idle_since = now;
+        } else if (now - idle_since > kWaitLimitNs) {
+          report_timeout(a.err, 0x915);
+          *abort_flag = 1;
+          break;
+        }
+        __nanosleep(64);
       }
       // every MMA issued has completed before TMEM is released
       umma_commit(mdone);
@@ -337,17 +387,19 @@ __global__ void __launch_bounds__(kThreads, 1) tc_causal_kernel(const __grid_con
       const bool ok = mbar_wait(tfull(s), (uint32_t)((it.n / kStages) & 1), a.err, 0x91d, abort_flag);
       if (!named_all(9, kGrpThreads, ok)) break;
       if (t < rows) {
-        // row t of Q, then of K: the whole 128-byte row in registers, its
-        // 16-byte chunks visited as j ^ t so that the eight rows of a
-        // quarter-warp touch eight different bank groups
-        for (int m = 0; m < 2; ++m) {
-          uint4* r = reinterpret_cast<uint4*>(gb + (tst(s) - base) + (uint32_t)m * kTile + t * 128);
-          uint4 xv[8];
+        // rows t of Q and of K, four 16-byte chunks at a time, visited as
+        // j ^ t so that the eight rows of a quarter-warp touch eight
+        // different bank groups (a rolled loop keeps this role's code small)
+#pragma unroll 1
+        for (int g = 0; g < 4; ++g) {
+          uint4* r = reinterpret_cast<uint4*>(gb + (tst(s) - base) + (uint32_t)(g >> 1) * kTile + t * 128);
+          const int j0 = 4 * (g & 1);
+          uint4 xv[4];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) xv[j] = r[(j ^ t) & 7];
+          for (int j = 0; j < 4; ++j) xv[j] = r[((j0 + j) ^ t) & 7];
           if (p.fmap == MHLA_FEATURE_ELU1) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
+            for (int j = 0; j < 4; ++j) {
               xv[j].x = phi2_elu1_bf16(xv[j].x);
               xv[j].y = phi2_elu1_bf16(xv[j].y);
               xv[j].z = phi2_elu1_bf16(xv[j].z);
@@ -355,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_causal_kernel(const __grid_con
             }
           } else {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
+            for (int j = 0; j < 4; ++j) {
               uint32_t* pw = &xv[j].x;
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
@@ -365,56 +417,69 @@ __global__ void __launch_bounds__(kThreads, 1) tc_causal_kernel(const __grid_con
             }
           }
 #pragma unroll
-          for (int j = 0; j < 8; ++j) r[(j ^ t) & 7] = xv[j];
+          for (int j = 0; j < 4; ++j) r[((j0 + j) ^ t) & 7] = xv[j];
         }
       }
       fence_proxy_async();
       mbar_arrive_warp(pready(s));
     }
   } else if (warp >= 8 && warp < 12) {
-    // ------------------------------------ P~ = w mask(D_s), j <= t
+    // --------------------------- P~ = w mask(D_s), j <= t, into TMEM
     const int e = warp - 8, t = threadIdx.x - 8 * 32;
     const uint32_t ta = tmem + ((uint32_t)(32 * e) << 16);
-    uint8_t* prow = gb + kOffPt + t * 128;
+    {
+      // token pairs past every row of this warp stay zero from here on
+      uint32_t zero[32];
+#pragma unroll
+      for (int m = 0; m < 32; ++m) zero[m] = 0u;
+      tmem_st32(ta + kColP, zero);
+      tmem_st32(ta + kColP + 32u, zero);
+      tmem_wait_st();
+    }
+    // scores of 32 tokens (part h of the row) -> 16 bf16 pairs of P~; only
+    // the part on the diagonal (h == e) needs the mask j <= t
+    auto pack_part = [&](const float (&sc)[32], int h, float wt, uint32_t* pw) {
+      if (h < e) {
+#pragma unroll
+        for (int m = 0; m < 16; ++m) pw[m] = pack_bf16x2(wt * sc[2 * m], wt * sc[2 * m + 1]);
+      } else {
+        const int d = t - 32 * h;   // 0..31: last token of the part this row sees
+#pragma unroll
+        for (int m = 0; m < 16; ++m)
+          pw[m] = pack_bf16x2(2 * m <= d ? wt * sc[2 * m] : 0.f, 2 * m + 1 <= d ? wt * sc[2 * m + 1] : 0.f);
+      }
+    };
     ChunkIt it;
     for (ci_begin(a, p, it); it.valid; ci_next(a, p, it)) {
       const float w = diag_weight(a, p, it);
+      const float wt = t < rows ? w : 0.f;
       bool ok = mbar_wait(sfull, (uint32_t)(it.n & 1), a.err, 0x91e, abort_flag);
       ok = ok && mbar_wait(ptfree, (uint32_t)(it.n & 1) ^ 1u, a.err, 0x91f, abort_flag);
       if (!named_all(8, kGrpThreads, ok)) break;
       tc_fence_after();
-      // columns 32h .. 32h + 31 with h > e lie past every row of this warp
-      // and stay zero; two TMEM loads per wait
-#pragma unroll
+      // tokens 64 hp .. 64 hp + 63 -> P~ columns 32 hp .. 32 hp + 31; the
+      // tokens past every row of a warp keep their zero columns
+#pragma unroll 1
       for (int hp = 0; hp < 2; ++hp) {
         if (2 * hp > e) break;
-        const bool two = 2 * hp + 1 <= e;
-        float sc[2][32];
-        tmem_ld32(ta + kColS + 64u * hp, sc[0]);
-        if (two) tmem_ld32(ta + kColS + 64u * hp + 32u, sc[1]);
+        uint32_t pw[32];
+        float sc[32];
+        tmem_ld32(ta + kColS + 64u * hp, sc);
         tmem_wait_ld();
-        uint8_t* atom = prow + hp * kTile;   // j 0..63 -> atom 0, 64..127 -> atom 1
+        pack_part(sc, 2 * hp, wt, pw);
+        if (2 * hp + 1 <= e) {
+          tmem_ld32(ta + kColS + 64u * hp + 32u, sc);
+          tmem_wait_ld();
+          pack_part(sc, 2 * hp + 1, wt, pw + 16);
+        } else {
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          if (hh == 1 && !two) break;
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint32_t pk[4];
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-              const int j0 = 64 * hp + 32 * hh + 8 * q + 2 * m;
-              const float v0 = (j0 <= t && t < rows) ? w * sc[hh][8 * q + 2 * m] : 0.f;
-              const float v1 = (j0 + 1 <= t && t < rows) ? w * sc[hh][8 * q + 2 * m + 1] : 0.f;
-              pk[m] = pack_bf16x2(v0, v1);
-            }
-            const int chunk = hh * 4 + q;   // logical 16-byte chunk in the atom row
-            *reinterpret_cast<uint4*>(atom + (((chunk ^ t) & 7) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-          }
+          for (int m = 16; m < 32; ++m) pw[m] = 0u;
         }
+        tmem_st32(ta + kColP + 32u * hp, pw);
       }
+      tmem_wait_st();
       tc_fence_before();
       mbar_arrive_warp(sfree);
-      fence_proxy_async();
       mbar_arrive_warp(ptready);
     }
   } else if (warp >= 12) {
@@ -440,15 +505,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_causal_kernel(const __grid_con
       tc_fence_after();
       if (upd) {
         // S_state += w F^T V (bf16 high + low), z_state += w F^T 1
-        float dv[2][32], zc[16];
+        float dv[32], zc[16];
         uint8_t* shr = gb + kOffSt + x * kStBytes + t * 128;
         uint8_t* slr = shr + kBTile;
-        tmem_ld32(ta + kColU, dv[0]);
-        tmem_ld32(ta + kColU + 32u, dv[1]);
         tmem_ld16(ta + kColU + 64u, zc);
-        tmem_wait_ld();
-#pragma unroll
+#pragma unroll 1
         for (int h = 0; h < 2; ++h) {
+          tmem_ld32(ta + kColU + 32u * h, dv);
+          tmem_wait_ld();
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const uint32_t off = (uint32_t)((((4 * h + q) ^ t) & 7) << 4);
@@ -458,7 +522,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_causal_kernel(const __grid_con
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
               const float2 fh = bf16x2_to_float2(hp[m]), fl = bf16x2_to_float2(lp[m]);
-              const float y0 = fh.x + fl.x + w * dv[h][8 * q + 2 * m], y1 = fh.y + fl.y + w * dv[h][8 * q + 2 * m + 1];
+              const float y0 = fh.x + fl.x + w * dv[8 * q + 2 * m], y1 = fh.y + fl.y + w * dv[8 * q + 2 * m + 1];
               hp[m] = pack_bf16x2(y0, y1);
               const float2 g = bf16x2_to_float2(hp[m]);
               lp[m] = pack_bf16x2(y0 - g.x, y1 - g.y);
@@ -470,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_causal_kernel(const __grid_con
         const float zn = (it.c == 0 ? zin : (x ? zr1 : zr0)) + w * zc[0];
         if (x) zr1 = zn;
         else zr0 = zn;
-        put_z_row(gb + kOffSt + x * kStBytes + 2 * kBTile, t, zn);
+        put_z(gb + kOffSt + x * kStBytes + 2 * kBTile, t, zn);
         tc_fence_before();
         fence_proxy_async();
         mbar_arrive_warp(ufree);
@@ -478,18 +542,18 @@ __global__ void __launch_bounds__(kThreads, 1) tc_causal_kernel(const __grid_con
       }
       {
         // s = P z_state + rowsum(P~) (columns 64, 65); DIVISIVE o = num / s
-        float nm[2][32], zc[16];
-        const uint32_t DA = ta + (uint32_t)acc * 128u;
-        tmem_ld32(DA, nm[0]);
-        tmem_ld32(DA + 32u, nm[1]);
+        float nm[32], zc[16];
+        const uint32_t DA = ta + col_a(acc);
         tmem_ld16(DA + 64u, zc);
         tmem_wait_ld();
         const float s = zc[0] + zc[1];
         float scale = 1.f;
         if (p.norm == MHLA_NORM_DIVISIVE) scale = s != 0.f ? 1.f / s : 0.f;
         uint8_t* orow = gb + kOffO + acc * kTile + t * 128;
-#pragma unroll
+#pragma unroll 1
         for (int h = 0; h < 2; ++h) {
+          tmem_ld32(DA + 32u * h, nm);
+          tmem_wait_ld();
           if (t < rows) {
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
@@ -497,7 +561,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_causal_kernel(const __grid_con
               uint32_t* op = &ov.x;
 #pragma unroll
               for (int m = 0; m < 4; ++m)
-                op[m] = pack_bf16x2(nm[h][8 * q + 2 * m] * scale, nm[h][8 * q + 2 * m + 1] * scale);
+                op[m] = pack_bf16x2(nm[8 * q + 2 * m] * scale, nm[8 * q + 2 * m + 1] * scale);
               *reinterpret_cast<uint4*>(orow + ((((4 * h + q) ^ t) & 7) << 4)) = ov;
             }
           }
