@@ -41,6 +41,20 @@ namespace {
 
 using namespace tc;
 
+// Non-blocking test whether the phase of `bar` with parity `parity` has
+// completed (acquire semantics when it has).
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 constexpr int kThreads = 512;
 constexpr int kGrpThreads = 128;                 // warps 4-7 (phi), 8-11 (scores), 12-15 (outputs, state)
 constexpr uint32_t kTile = 128 * 128;            // 128 rows x 64 bf16

@@ -86,20 +86,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Non-blocking test whether the phase of `bar` with parity `parity` has
-// completed (acquire semantics when it has).
-__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
 // try_wait that lets the hardware suspend the thread for up to `hint_ns`
 // nanoseconds (it resumes as soon as the phase completes), so waiting roles
 // do not spin on the issue slots the working roles need.
