@@ -20,7 +20,8 @@
 //
 // Persistent, warp-specialised CTA (one per SM, 640 threads):
 //   warp 0       TMA producer (K and V tiles of one token chunk per stage)
-//   warp 1       TMEM allocation + MMA issue (one elected thread)
+//   warp 1       TMEM allocation; warps 1, 2 MMA issue (even / odd units,
+//                each through its own ring of stages; one issuer for MALA)
 //   warps 4-6, 16-17  epilogue: TMEM rows 0..64 -> the record (S_b, z_b,
 //                v_b) as fp16 scaled by 2^-ceil(log2 n) (DIVISIVE/NONE) or as
 //                bf16 high + low parts (MALA) -> swizzled staging tiles
@@ -57,6 +58,7 @@ constexpr int kN = 80;                                  // MMA N: 64 value featu
 template <bool kLo>
 struct Layout {
   static constexpr int kStages = kLo ? 3 : 5;
+  static constexpr int kIssuers = kLo ? 1 : 2;                       // MMA-issuing warps (1, 2)
   static constexpr int kStagingBufs = kLo ? 2 : 1;
   static constexpr uint32_t kStageBytes = (kLo ? 3 : 2) * kTile;  // K, V [, K lo]
   static constexpr uint32_t kOnes = kStages * kStageBytes;          // 16 token rows of ones (2 KB)
@@ -149,6 +151,14 @@ __device__ __forceinline__ void summary_body(const SummaryArgs& a, const Plan& p
   auto empty = [&](int s) { return bars + 8u * (2 * kStages + s); };
   auto accfull = [&](int x) { return bars + 8u * (3 * kStages + x); };
   auto accempty = [&](int x) { return bars + 8u * (3 * kStages + 2 + x); };
+  // Stage rings: with two MMA issuers (kIssuers), unit number `it` of this
+  // CTA goes through ring it % kIssuers, the stages j, j + kIssuers, ...; each
+  // ring is filled in order by the producer and drained in order by ONE
+  // issuer, so no waiter ever falls two phases behind a stage's barriers.
+  constexpr int kIssuers = L::kIssuers;
+  auto ring_len = [&](int j) { return (kStages - j + kIssuers - 1) / kIssuers; };
+  auto ring_stage = [&](int j, long long k) { return j + kIssuers * (int)(k % ring_len(j)); };
+  auto ring_phase = [&](int j, long long k) { return (uint32_t)((k / ring_len(j)) & 1); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gb + L::kBars + 8 * (3 * kStages + 4));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gb + L::kBars + 8 * (3 * kStages + 4) + 8);
 
@@ -198,11 +208,10 @@ __device__ __forceinline__ void summary_body(const SummaryArgs& a, const Plan& p
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
       const uint32_t bytes = 2u * (uint32_t)rows * 128u;
-      int stage = 0, ready_u = -1;
-      uint32_t phase = 0;
-      long long issued = 0;
+      int ready_u = -1, it = 0;
+      long long rk0 = 0, rk1 = 0;   // loads issued per ring
       bool ok = true;
-      for (int w = f.cta; w < a.units && ok; w += f.ncta) {
+      for (int w = f.cta; w < a.units && ok; w += f.ncta, ++it) {
         const UnitCoord uc = unit_coord(p, a, w);
         // fused flow: the stack slot of this head is free once the mixing of
         // the head that last used it has read it
@@ -210,8 +219,11 @@ __device__ __forceinline__ void summary_body(const SummaryArgs& a, const Plan& p
             !(ok = flow_wait(&f.x_done[uc.u - f.ring], f.need_x, a.err, 0x108, abort_flag, f.wait_ns)))
           break;
         ready_u = uc.u;
+        const int j = it % kIssuers;
         for (int c = uc.c0; c < uc.c1; ++c) {
-          if (!(ok = mbar_wait(empty(stage), phase ^ 1u, a.err, 0x101, abort_flag))) break;
+          const long long k = j ? rk1 : rk0;
+          const int stage = ring_stage(j, k);
+          if (!(ok = mbar_wait(empty(stage), ring_phase(j, k) ^ 1u, a.err, 0x101, abort_flag))) break;
           int x0, y0, t0;
           chunk_origin(p, a.c, uc.b, c, x0, y0, t0);
           const TileCoords g5 = token_tile_coords(p, uc.u, x0, y0, t0);
@@ -219,30 +231,52 @@ __device__ __forceinline__ void summary_body(const SummaryArgs& a, const Plan& p
           mbar_arrive_expect_tx(full(stage), bytes);
           tma_load_5d(kt, &a.tmK, full(stage), g5.c[0], g5.c[1], g5.c[2], g5.c[3], g5.c[4], pol);
           tma_load_5d(kt + kTile, &a.tmV, full(stage), g5.c[0], g5.c[1], g5.c[2], g5.c[3], g5.c[4], pol);
-          ++issued;
-          if (++stage == kStages) {
-            stage = 0;
-            phase ^= 1u;
+          if (j) ++rk1;
+          else ++rk0;
+        }
+      }
+      // before the CTA's memory is released: the last loads of each ring
+      // have landed (bounded, whatever the abort flag says)
+      for (int j = 0; j < kIssuers; ++j) {
+        const long long n = j ? rk1 : rk0;
+        const long long first = n > ring_len(j) ? n - ring_len(j) : 0;
+        for (long long k = first; k < n; ++k) {
+          const uint32_t bar = full(ring_stage(j, k)), par = ring_phase(j, k);
+          if (mbar_try_wait(bar, par)) continue;
+          const unsigned long long t0 = globaltimer();
+          while (!mbar_try_wait_sleep(bar, par, 20000u)) {
+            if (globaltimer() - t0 > kWaitLimitNs) {
+              report_timeout(a.err, 0x109);
+              break;
+            }
           }
         }
       }
-      drain_loads(full(0), kStages, issued, a.err, 0x109);
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 || warp == 2) {
     // --------------------------------------------------------------- MMA
-    if (lane == 0) {
+    // A tcgen05.mma holds its issuing warp for a fixed time whatever its N,
+    // so with two issuers warp 1 takes this CTA's even units (accumulator 0,
+    // ring 0) and warp 2 the odd ones (accumulator 1, ring 1); with one,
+    // warp 1 takes every unit and alternates the accumulators.
+    const int j = warp - 1;
+    if (lane == 0 && j < kIssuers) {
       const uint32_t idesc = idesc_bf16_f32(128, kN, true, true);
       const int ksteps = a.c.rows_pad / 16;
-      int stage = 0, acc = 0;
-      uint32_t phase = 0, accph = 0;
+      long long rk = 0;       // chunks taken from ring j
+      int it = 0;
+      uint32_t accph = 0;     // bit x: phase of accumulator x
       bool ok = true;
-      for (int w = f.cta; w < a.units && ok; w += f.ncta) {
+      for (int w = f.cta; w < a.units && ok; w += f.ncta, ++it) {
+        if (it % kIssuers != j) continue;
         const UnitCoord uc = unit_coord(p, a, w);
-        if (!(ok = mbar_wait(accempty(acc), accph ^ 1u, a.err, 0x102, abort_flag))) break;
+        const int acc = it & 1;
+        if (!(ok = mbar_wait(accempty(acc), ((accph >> acc) & 1u) ^ 1u, a.err, 0x102, abort_flag))) break;
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)acc * 128u;
         for (int c = uc.c0; c < uc.c1; ++c) {
-          if (!(ok = mbar_wait(kready(stage), phase, a.err, 0x103, abort_flag))) break;
+          const int stage = ring_stage(j, rk);
+          if (!(ok = mbar_wait(kready(stage), ring_phase(j, rk), a.err, 0x103, abort_flag))) break;
           tc_fence_after();
           const uint32_t kt = base + (uint32_t)stage * kStageBytes;
           const uint32_t vt = kt + kTile;
@@ -258,17 +292,11 @@ __device__ __forceinline__ void summary_body(const SummaryArgs& a, const Plan& p
             }
           }
           umma_commit(empty(stage));
-          if (++stage == kStages) {
-            stage = 0;
-            phase ^= 1u;
-          }
+          ++rk;
         }
         if (!ok) break;
         umma_commit(accfull(acc));
-        if (++acc == 2) {
-          acc = 0;
-          accph ^= 1u;
-        }
+        accph ^= 1u << acc;
       }
     }
   } else if (warp >= 8 && warp < 16) {
@@ -278,13 +306,16 @@ __device__ __forceinline__ void summary_body(const SummaryArgs& a, const Plan& p
     const int t = threadIdx.x - 256;
     const int row = t >> 1;
     const int half = t & 1;
-    int stage = 0;
-    uint32_t phase = 0;
+    long long rk0 = 0, rk1 = 0;   // chunks taken from rings 0, 1
+    int it = 0;
     bool ok = true;
-    for (int w = f.cta; w < a.units && ok; w += f.ncta) {
+    for (int w = f.cta; w < a.units && ok; w += f.ncta, ++it) {
       const UnitCoord uc = unit_coord(p, a, w);
+      const int ring = it % kIssuers;
       for (int c = uc.c0; c < uc.c1; ++c) {
-        if (!(ok = mbar_wait(full(stage), phase, a.err, 0x104, abort_flag))) break;
+        const long long k = ring ? rk1 : rk0;
+        const int stage = ring_stage(ring, k);
+        if (!(ok = mbar_wait(full(stage), ring_phase(ring, k), a.err, 0x104, abort_flag))) break;
         if (row < rows) {
           uint8_t* rp = gb + stage * kStageBytes + row * 128;
           uint4 x[4];
@@ -301,10 +332,8 @@ __device__ __forceinline__ void summary_body(const SummaryArgs& a, const Plan& p
         }
         fence_proxy_async();
         mbar_arrive_warp(kready(stage));
-        if (++stage == kStages) {
-          stage = 0;
-          phase ^= 1u;
-        }
+        if (ring) ++rk1;
+        else ++rk0;
       }
     }
   } else if (warp == 4 || warp == 5 || warp == 6 || warp == 16 || warp == 17) {
