@@ -143,7 +143,7 @@ def summary_protocol(units: int, cpp: int, nstages: int, nissuers: int, shared_r
     schedule([producer(), phi(), epilogue()] + [issuer(j) for j in range(nissuers)], rnd)
 
 
-@pytest.mark.parametrize("nstages,nissuers", [(5, 2), (4, 2), (3, 1), (5, 1)])
+@pytest.mark.parametrize("nstages,nissuers", [(6, 2), (5, 2), (4, 2), (3, 1), (5, 1)])
 def test_summary_stage_rings_are_safe(nstages, nissuers):
     for units in (1, 2, 3, 5, 8):
         for cpp in (1, 2, 3, 4):

@@ -57,9 +57,9 @@ constexpr int kN = 80;                                  // MMA N: 64 value featu
 // tile per stage (MALA); the stage count shrinks to keep everything resident.
 template <bool kLo>
 struct Layout {
-  static constexpr int kStages = kLo ? 3 : 5;
+  static constexpr int kStages = kLo ? 3 : 6;
   static constexpr int kIssuers = kLo ? 1 : 2;                       // MMA-issuing warps (1, 2)
-  static constexpr int kStagingBufs = kLo ? 2 : 1;
+  static constexpr int kStagingBufs = 2;
   static constexpr uint32_t kStageBytes = (kLo ? 3 : 2) * kTile;  // K, V [, K lo]
   static constexpr uint32_t kOnes = kStages * kStageBytes;          // 16 token rows of ones (2 KB)
   static constexpr uint32_t kStaging = kOnes + 2048;                // staging buffers
