@@ -21,7 +21,7 @@
 // Persistent, warp-specialised CTA (one per SM, 640 threads):
 //   warp 0       TMA producer (K and V tiles of one token chunk per stage)
 //   warp 1       TMEM allocation; warps 1, 2 MMA issue (even / odd units,
-//                each through its own ring of stages; one issuer for MALA)
+//                each through its own ring of stages)
 //   warps 4-6, 16-17  epilogue: TMEM rows 0..64 -> the record (S_b, z_b,
 //                v_b) as fp16 scaled by 2^-ceil(log2 n) (DIVISIVE/NONE) or as
 //                bf16 high + low parts (MALA) -> swizzled staging tiles
@@ -54,12 +54,13 @@ constexpr uint32_t kTmemCols = 256;                     // two 128-column accumu
 constexpr int kN = 80;                                  // MMA N: 64 value features + 16 ones
 
 // Shared-memory layout.  kLo adds the low bf16 residual of phi(K) as a third
-// tile per stage (MALA); the stage count shrinks to keep everything resident.
+// tile per stage (MALA); the stage count shrinks (and one staging buffer
+// is kept) to keep everything resident.
 template <bool kLo>
 struct Layout {
-  static constexpr int kStages = kLo ? 3 : 6;
-  static constexpr int kIssuers = kLo ? 1 : 2;                       // MMA-issuing warps (1, 2)
-  static constexpr int kStagingBufs = 2;
+  static constexpr int kStages = kLo ? 4 : 6;
+  static constexpr int kIssuers = 2;                                 // MMA-issuing warps (1, 2)
+  static constexpr int kStagingBufs = kLo ? 1 : 2;
   static constexpr uint32_t kStageBytes = (kLo ? 3 : 2) * kTile;  // K, V [, K lo]
   static constexpr uint32_t kOnes = kStages * kStageBytes;          // 16 token rows of ones (2 KB)
   static constexpr uint32_t kStaging = kOnes + 2048;                // staging buffers
