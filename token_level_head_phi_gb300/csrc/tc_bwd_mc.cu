@@ -43,7 +43,7 @@ constexpr int kThreads = 256;
 constexpr uint32_t kTile = 128 * 128;           // 128 rows x 64 bf16, 128-byte swizzle
 constexpr uint32_t kStageBytes = 4 * kTile;     // A hi, A lo, B hi, B lo
 constexpr int kStages = 3;
-constexpr uint32_t kTmemCols = 256;             // two 128-column accumulators
+constexpr uint32_t kTmemCols = 512;             // two 256-column accumulators
 constexpr uint32_t kBars = kStages * kStageBytes;
 constexpr int kNumBars = 2 * kStages + 4;
 constexpr uint32_t kSmemBytes = kBars + 8 * kNumBars + 16 + 1024;
@@ -133,14 +133,18 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_mc_kernel(const __grid_con
   } else if (warp == 1) {
     if (lane == 0) {
       // ------------------------------------------------------------ MMA
+      // B hi and B lo are adjacent 128-row K-major tiles: one N = 256 MMA
+      // takes A hi against both (columns 0..127 and 128..255; the epilogue adds
+      // them), as an MMA costs the same issue time whatever its N
       const uint32_t idesc = idesc_bf16_f32(128, 128, false, false);
+      const uint32_t idesc2 = idesc_bf16_f32(128, 256, false, false);
       int s = 0, acc = 0;
       uint32_t ph = 0, accph = 0;
       bool ok = true;
       for (int w = blockIdx.x; w < a.items && ok; w += gridDim.x) {
         if (!(ok = mbar_wait(accempty(acc), accph ^ 1u, a.err, 0x603, abort_flag))) break;
         tc_fence_after();
-        const uint32_t d = tmem + (uint32_t)acc * 128u;
+        const uint32_t d = tmem + (uint32_t)acc * 256u;
         for (int kc = 0; kc < a.kchunks; ++kc) {
           if (!(ok = mbar_wait(full(s), ph, a.err, 0x604, abort_flag))) break;
           tc_fence_after();
@@ -149,10 +153,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_mc_kernel(const __grid_con
           for (int ks = 0; ks < 4; ++ks) {
             const uint32_t o = (uint32_t)ks * 32u;
             const uint64_t ah = sdesc_sw128(st + o, 0u, 1024u), al = sdesc_sw128(st + kTile + o, 0u, 1024u);
-            const uint64_t bh = sdesc_sw128(st + 2 * kTile + o, 0u, 1024u);
-            const uint64_t bl = sdesc_sw128(st + 3 * kTile + o, 0u, 1024u);
-            umma_bf16(d, ah, bh, idesc, (kc > 0 || ks > 0) ? 1u : 0u);
-            umma_bf16(d, ah, bl, idesc, 1u);
+            const uint64_t bh = sdesc_sw128(st + 2 * kTile + o, 0u, 1024u);   // rows 0..127 hi, 128..255 lo
+            umma_bf16(d, ah, bh, idesc2, (kc > 0 || ks > 0) ? 1u : 0u);
             umma_bf16(d, al, bh, idesc, 1u);
           }
           umma_commit(empty(s));
@@ -182,13 +184,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_mc_kernel(const __grid_con
       const bool ok = mbar_wait(accfull(acc), accph, a.err, 0x605, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
-      const uint32_t taddr = tmem + (uint32_t)acc * 128u + ((uint32_t)(32 * q4) << 16);
+      const uint32_t taddr = tmem + (uint32_t)acc * 256u + ((uint32_t)(32 * q4) << 16);
       float* dst = a.partial + ((size_t)u * qp + (size_t)ti * 128 + row) * qp + (size_t)tb * 128;
 #pragma unroll 1
       for (int j = 0; j < 4; ++j) {
-        float v[32];
+        float v[32], w2[32];
         tmem_ld32(taddr + 32u * j, v);
+        tmem_ld32(taddr + 128u + 32u * j, w2);
         tmem_wait_ld();
+#pragma unroll
+        for (int x = 0; x < 32; ++x) v[x] += w2[x];
 #pragma unroll
         for (int x = 0; x < 8; ++x)
           reinterpret_cast<float4*>(dst + 32 * j)[x] = make_float4(v[4 * x], v[4 * x + 1], v[4 * x + 2], v[4 * x + 3]);
