@@ -60,7 +60,7 @@ extern "C" {
 typedef enum mhla_status {
   MHLA_OK = 0,
   MHLA_ERR_INVALID_ARG = 1,     /* bad pointer, shape, enum or alignment      */
-  MHLA_ERR_UNSUPPORTED = 2,     /* valid request this build cannot run        */
+  MHLA_ERR_UNSUPPORTED = 2,     /* valid request the library does not support */
   MHLA_ERR_WORKSPACE = 3,       /* workspace missing or smaller than required */
   MHLA_ERR_CUDA = 4,            /* a CUDA runtime call failed                  */
   MHLA_ERR_DEVICE_TIMEOUT = 5,  /* a kernel's bounded wait expired             */

@@ -875,7 +875,7 @@ const char* mhla_status_string(mhla_status s) {
   switch (s) {
     case MHLA_OK: return "MHLA_OK";
     case MHLA_ERR_INVALID_ARG: return "MHLA_ERR_INVALID_ARG: invalid pointer, shape, option or alignment";
-    case MHLA_ERR_UNSUPPORTED: return "MHLA_ERR_UNSUPPORTED: valid request this build cannot run";
+    case MHLA_ERR_UNSUPPORTED: return "MHLA_ERR_UNSUPPORTED: valid request the library does not support";
     case MHLA_ERR_WORKSPACE: return "MHLA_ERR_WORKSPACE: workspace missing or too small";
     case MHLA_ERR_CUDA: return "MHLA_ERR_CUDA: a CUDA runtime call failed";
     case MHLA_ERR_DEVICE_TIMEOUT: return "MHLA_ERR_DEVICE_TIMEOUT: a kernel's bounded wait expired";
