@@ -156,7 +156,9 @@ __device__ __forceinline__ void summary_body(const SummaryArgs& a, const Plan& p
   // CTA goes through ring it % kIssuers, the stages j, j + kIssuers, ...; each
   // ring is filled in order by the producer and drained in order by ONE
   // issuer, so no waiter ever falls two phases behind a stage's barriers.
-  constexpr int kIssuers = L::kIssuers;
+  // (one issuer when a unit has more chunks than a ring has stages: its
+  // chunks would wait on their own ring's reuse)
+  const int kIssuers = (L::kIssuers == 2 && a.cpp <= kStages / 2) ? 2 : 1;
   auto ring_len = [&](int j) { return (kStages - j + kIssuers - 1) / kIssuers; };
   auto ring_stage = [&](int j, long long k) { return j + kIssuers * (int)(k % ring_len(j)); };
   auto ring_phase = [&](int j, long long k) { return (uint32_t)((k / ring_len(j)) & 1); };
