@@ -47,7 +47,7 @@ from token_level_head_phi_gb300 import workloads as wl  # noqa: E402
 
 METRIC = "MHLA fwd tokens*heads/sec (d=64) and % of GB300 HBM/tensor roofline"
 UNIT = "tokens*heads/s"
-PHASES = ["summary", "mix", "output"]
+PHASES = ["prep", "summary", "scale", "mix", "output"]
 L2_BYTES = 126 * 1024 * 1024
 
 

@@ -55,7 +55,7 @@
 extern "C" {
 #endif
 
-#define MHLA_ABI_VERSION 2
+#define MHLA_ABI_VERSION 3
 
 typedef enum mhla_status {
   MHLA_OK = 0,
@@ -64,7 +64,7 @@ typedef enum mhla_status {
   MHLA_ERR_WORKSPACE = 3,       /* workspace missing or smaller than required */
   MHLA_ERR_CUDA = 4,            /* a CUDA runtime call failed                  */
   MHLA_ERR_DEVICE_TIMEOUT = 5,  /* a kernel's bounded wait expired             */
-  MHLA_ERR_OVERFLOW = 6         /* an intermediate left the fp16 range (device) */
+  MHLA_ERR_OVERFLOW = 6         /* reserved: no kernel reports it since ABI 3  */
 } mhla_status;
 
 typedef enum mhla_dtype { MHLA_DTYPE_BF16 = 0, MHLA_DTYPE_F32 = 1 } mhla_dtype;
@@ -92,21 +92,26 @@ typedef enum mhla_norm { MHLA_NORM_DIVISIVE = 0, MHLA_NORM_MALA = 1, MHLA_NORM_N
  * MULTIPASS: tcgen05/TMEM tensor-core kernels fed by TMA (bf16, d = 64):
  *            block summaries -> mixing GEMM -> output with fused epilogue.
  *            For the DIVISIVE and NONE norms the mixing multiplies fp16
- *            operands: each block summary is scaled by 2^-ceil(log2 n) (n
- *            tokens per summary piece) and each Mc row by a power of two
- *            that brings its largest entry into [0.5, 1].  A summary entry
- *            that still leaves the fp16 range (a single token with
- *            |phi(K)[k] V[c]| >= 65504) is recorded on the device as
- *            MHLA_ERR_OVERFLOW (see mhla_device_status); MALA and SIMT have
- *            no such limit.
- * FUSED:     the MULTIPASS kernels (same arithmetic, same results) as three
- *            groups of CTAs in one cooperative launch that work through the
- *            heads concurrently; the stack and the mixed summaries live in
- *            a ring of a few heads that stays in L2, so less workspace.
- *            Needs a device with cooperative launch; the split of the SMs
- *            between the groups follows a work estimate, and the
- *            environment variable MHLA_FUSED_GROUPS="s,x,o" (CTA counts)
- *            overrides it for tuning. */
+ *            operands: each block summary's S_b and z_b are stored times
+ *            their own power of two (the part's largest entry lands in
+ *            [2^14, 2^15)), and a small kernel folds those exponents into a
+ *            per-head fp16 copy of Mc whose rows are scaled so that each
+ *            row's largest entry lies in [0.5, 1); the output step applies
+ *            the remaining power of two.  So every finite input stays in
+ *            range: a summary entry keeps full fp16 precision down to 2^-29
+ *            of its part's largest entry, and a mixed term down to 2^-24 of
+ *            its row's largest term.  MALA (and the causal form) mix bf16
+ *            high + low parts, which have the float32 range.
+ * FUSED:     the MULTIPASS kernels as three groups of CTAs in one
+ *            cooperative launch that work through the heads concurrently;
+ *            the stack and the mixed summaries live in a ring of a few heads
+ *            that stays in L2, so less workspace.  Every norm mixes bf16
+ *            high + low parts here (same results as MULTIPASS under MALA;
+ *            within the same tolerance otherwise).  Needs a device with
+ *            cooperative launch; the split of the SMs between the groups
+ *            follows a work estimate, and the environment variable
+ *            MHLA_FUSED_GROUPS="s,x,o" (CTA counts) overrides it for
+ *            tuning. */
 typedef enum mhla_variant {
   MHLA_VARIANT_AUTO = 0,
   MHLA_VARIANT_SIMT = 1,
@@ -247,18 +252,21 @@ mhla_status mhla_backward(const void* q, const void* k, const void* v, const flo
 
 /* Reads and clears the device error word of the current device.  Blocks the
  * host until the device is idle.  *code receives MHLA_OK or the first status
- * a kernel recorded (MHLA_ERR_DEVICE_TIMEOUT, MHLA_ERR_OVERFLOW); *detail
+ * a kernel recorded (MHLA_ERR_DEVICE_TIMEOUT); *detail
  * receives a kernel-specific location code (0 if none).  Either pointer may
  * be NULL. */
 mhla_status mhla_device_status(int* code, int* detail);
 
 /* Timing hook.  With n == MHLA_NUM_PHASE_EVENTS, each later mhla_forward
  * records events[0] before its first kernel and events[i] after phase i
- * (1: block summaries, 2: mixing, 3: output) on its stream; phases a
- * variant does not have record at the same point as the previous one.
- * events are cudaEvent_t handles owned by the caller.  n == 0 turns the hook
- * off.  Process-wide; not meant for concurrent callers. */
-#define MHLA_NUM_PHASE_EVENTS 4
+ * (1: Mc preparation, 2: block summaries, 3: folding the fp16 records'
+ * exponents into Mc, 4: mixing, 5: output) on its stream; phases a variant
+ * does not have record at the same point as the previous one (the fused
+ * launch runs phases 2-5 as one kernel, recorded after phase 5).  Events
+ * between the kernels serialise them.  events are cudaEvent_t handles owned
+ * by the caller.  n == 0 turns the hook off.  Process-wide; not meant for
+ * concurrent callers. */
+#define MHLA_NUM_PHASE_EVENTS 6
 mhla_status mhla_set_phase_events(void* const* events, int n);
 
 /* The same hook for mhla_backward: events[0] before its first kernel, then

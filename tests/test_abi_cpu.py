@@ -44,7 +44,7 @@ def test_binding_declares_every_header_function():
 
 
 def test_abi_version_and_strings(lib):
-    assert mb.mhla_abi_version() == 2
+    assert mb.mhla_abi_version() == 3
     for s in range(7):
         assert mb.mhla_status_string(s).startswith("MHLA")
     assert "unknown" in mb.mhla_status_string(42)
@@ -202,15 +202,18 @@ def test_multipass_splits_long_blocks(lib):
 
 @pytest.mark.parametrize("name", ["deit_t", "video_16x64x64", "seq_32k", "seq_32k_mala", "seq_32k_m1"])
 def test_fused_plan(lib, name):
-    """The fused launch is the prep kernel plus one cooperative kernel; its
-    ring of intermediates never needs more workspace than the multi-pass
-    buffers, and needs less once the heads outnumber the ring."""
+    """The fused launch is the prep kernel plus one cooperative kernel; it
+    keeps split (bf16 high + low) records for every norm, in a ring that never
+    needs more workspace than the multi-pass buffers of the same records
+    (MALA's), and needs less once the heads outnumber the ring."""
     w = wl.WORKLOADS[name]
     fused = mb.mhla_plan(_params(w, variant="fused"))
     multi = mb.mhla_plan(_params(w, variant="multipass"))
+    split = mb.mhla_plan(_params(w, variant="multipass", norm="mala"))
     assert fused.variant == mb.VARIANT_FUSED and fused.kernels_per_call == 2
+    assert multi.kernels_per_call == (4 if w.norm == "mala" else 5)
     assert fused.summary_splits == multi.summary_splits
-    assert fused.workspace_bytes <= multi.workspace_bytes + 3 * 4 * w.units + 256
+    assert fused.workspace_bytes <= split.workspace_bytes + 3 * 4 * w.units + 256
     if name == "video_16x64x64":
         assert fused.workspace_bytes < multi.workspace_bytes / 4
 

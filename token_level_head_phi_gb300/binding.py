@@ -38,7 +38,7 @@ VARIANT_AUTO = 0
 VARIANT_SIMT = 1
 VARIANT_MULTIPASS = 2
 VARIANT_FUSED = 3
-NUM_PHASE_EVENTS = 4
+NUM_PHASE_EVENTS = 6
 NUM_BWD_PHASE_EVENTS = 6
 
 NORMS = {"divisive": NORM_DIVISIVE, "mala": NORM_MALA, "none": NORM_NONE}

@@ -170,12 +170,16 @@ mhla_status make_plan(const mhla_params* prm, Plan* p, int split_units = 0) {
     p->splits = (nck + p->cpp - 1) / p->cpp;
     p->split_len = p->cpp * p->chunk.rows;
     p->Qp = (p->M * p->splits + 7) / 8 * 8;
-    // the causal output step adds its in-block terms in float32 to the mixed
-    // prefix records: they stay in bf16 high + low planes (no fp16 scaling)
-    p->f16_mix = p->norm != MHLA_NORM_MALA && !p->causal;
-    int lg = 0;
-    while ((1 << lg) < p->split_len) ++lg;
-    p->stack_scale = ldexpf(1.f, -lg);
+    // fp16 records and mixing for DIVISIVE and NONE in the multi-pass launch.
+    // MALA cancels its leading terms and needs the split (bf16 high + low)
+    // records and phi(K); so do exponential features, where a few tokens
+    // dominate each feature and the bf16 rounding of phi(K) no longer
+    // averages out; so does the causal output step, which adds its in-block
+    // terms in float32 to the mixed prefix records; the fused launch has no
+    // pass between its summary and mixing groups to fold the records'
+    // exponents into Mc, so it takes the split records too.
+    p->f16_mix = p->norm != MHLA_NORM_MALA && p->fmap != MHLA_FEATURE_EXP && !p->causal &&
+                 variant == MHLA_VARIANT_MULTIPASS;
   }
 
   if (p->BH == 0) {
@@ -199,7 +203,7 @@ mhla_status make_plan(const mhla_params* prm, Plan* p, int split_units = 0) {
   } else {
     // fused: a ring of heads small enough to stay in L2 (at least two, so
     // that consecutive heads overlap)
-    const size_t per_head = 2 * (size_t)p->M * p->splits * p->R * (p->norm == MHLA_NORM_MALA ? 2 : 1) +
+    const size_t per_head = 2 * (size_t)p->M * p->splits * p->R * (p->f16_mix ? 1 : 2) +
                             4 * (size_t)p->M * p->R;
     p->slots = p->BH;
     if (variant == MHLA_VARIANT_FUSED) {
@@ -215,7 +219,7 @@ mhla_status make_plan(const mhla_params* prm, Plan* p, int split_units = 0) {
     p->off_stack = off;
     off = align_up(off + stack);
     p->off_stack_lo = off;
-    if (p->norm == MHLA_NORM_MALA || p->causal) off = align_up(off + stack);
+    if (!p->f16_mix) off = align_up(off + stack);
     p->off_mixed = off;
     off = align_up(off + mixed);
     p->off_mixed_lo = off;
@@ -233,6 +237,15 @@ mhla_status make_plan(const mhla_params* prm, Plan* p, int split_units = 0) {
     p->off_blkinfo = off;
     off = align_up(off + 16 * (size_t)p->M * p->mc_heads);
     p->kernels = 4;
+    if (p->f16_mix) {
+      p->off_rexp = off;
+      off = align_up(off + 8 * rows);
+      p->off_mcx = off;
+      off = align_up(off + 2 * 2 * (size_t)p->slots * p->M * p->Qp);
+      p->off_sinfo = off;
+      off = align_up(off + 16 * (size_t)p->slots * p->M);
+      p->kernels = 5;
+    }
     if (variant == MHLA_VARIANT_FUSED) {
       p->off_flow = off;
       off = align_up(off + 3 * sizeof(unsigned int) * (size_t)p->BH);
@@ -278,8 +291,7 @@ mhla_status run_plan(const Plan& plan, const void* q, const void* k, const void*
     const bool fused = p.variant == MHLA_VARIANT_FUSED;
     TcBuffers b;
     b.stack = ws + p.off_stack;
-    b.stack_lo = (p.norm == MHLA_NORM_MALA || p.causal) ? reinterpret_cast<__nv_bfloat16*>(ws + p.off_stack_lo)
-                                                          : nullptr;
+    b.stack_lo = p.f16_mix ? nullptr : reinterpret_cast<__nv_bfloat16*>(ws + p.off_stack_lo);
     b.mixed_hi = reinterpret_cast<__nv_bfloat16*>(ws + p.off_mixed);
     b.mixed_lo = reinterpret_cast<__nv_bfloat16*>(ws + p.off_mixed_lo);
     b.mc_f16 = reinterpret_cast<__half*>(ws + p.off_mc_f16);
@@ -288,9 +300,11 @@ mhla_status run_plan(const Plan& plan, const void* q, const void* k, const void*
     b.mc_lo = reinterpret_cast<__nv_bfloat16*>(ws + p.off_mc_lo);
     b.rowsum = reinterpret_cast<float*>(ws + p.off_rowsum);
     b.blkinfo = reinterpret_cast<float4*>(ws + p.off_blkinfo);
+    b.rexp = p.f16_mix ? reinterpret_cast<int2*>(ws + p.off_rexp) : nullptr;
+    b.mcx = p.f16_mix ? reinterpret_cast<__half*>(ws + p.off_mcx) : nullptr;
+    b.sinfo = p.f16_mix ? reinterpret_cast<float4*>(ws + p.off_sinfo) : nullptr;
     b.Qp = p.Qp;
     b.f16 = p.f16_mix != 0;
-    b.stack_scale = b.f16 ? p.stack_scale : 1.f;
     b.slots = p.slots;
     b.flow = fused ? reinterpret_cast<unsigned int*>(ws + p.off_flow) : nullptr;
     record_event(0, s);
@@ -298,8 +312,10 @@ mhla_status run_plan(const Plan& plan, const void* q, const void* k, const void*
       if ((e = launch_tc_prep(p, mc, b, s)) != 0) return cuda_fail((cudaError_t)e);
       record_event(1, s);
       record_event(2, s);
-      if ((e = launch_tc_fused(p, p.chunk, q, k, v, b, out, s)) != 0) return cuda_fail((cudaError_t)e);
       record_event(3, s);
+      record_event(4, s);
+      if ((e = launch_tc_fused(p, p.chunk, q, k, v, b, out, s)) != 0) return cuda_fail((cudaError_t)e);
+      record_event(5, s);
       return MHLA_OK;
     }
     if (p.causal) {
@@ -310,22 +326,27 @@ mhla_status run_plan(const Plan& plan, const void* q, const void* k, const void*
       float* mcl = reinterpret_cast<float*>(ws + p.off_mcl);
       if ((e = launch_mc_strict_lower(p, mc, mcl, s)) != 0) return cuda_fail((cudaError_t)e);
       if ((e = launch_tc_prep(pr, mcl, b, s)) != 0) return cuda_fail((cudaError_t)e);
-      if ((e = launch_tc_summary(pr, pr.chunk, k, v, b, s)) != 0) return cuda_fail((cudaError_t)e);
       record_event(1, s);
-      if ((e = launch_tc_mix(pr, b, s)) != 0) return cuda_fail((cudaError_t)e);
+      if ((e = launch_tc_summary(pr, pr.chunk, k, v, b, s)) != 0) return cuda_fail((cudaError_t)e);
       record_event(2, s);
+      record_event(3, s);
+      if ((e = launch_tc_mix(pr, b, s)) != 0) return cuda_fail((cudaError_t)e);
+      record_event(4, s);
       if ((e = launch_tc_causal(p, q, k, v, b.mixed_hi, b.mixed_lo, mc, out, s)) != 0)
         return cuda_fail((cudaError_t)e);
-      record_event(3, s);
+      record_event(5, s);
       return MHLA_OK;
     }
     if ((e = launch_tc_prep(p, mc, b, s)) != 0) return cuda_fail((cudaError_t)e);
-    if ((e = launch_tc_summary(p, p.chunk, k, v, b, s)) != 0) return cuda_fail((cudaError_t)e);
     record_event(1, s);
-    if ((e = launch_tc_mix(p, b, s)) != 0) return cuda_fail((cudaError_t)e);
+    if ((e = launch_tc_summary(p, p.chunk, k, v, b, s)) != 0) return cuda_fail((cudaError_t)e);
     record_event(2, s);
-    if ((e = launch_tc_output(p, p.chunk, q, b, out, s)) != 0) return cuda_fail((cudaError_t)e);
+    if (b.f16 && (e = launch_tc_scale(p, mc, b, s)) != 0) return cuda_fail((cudaError_t)e);
     record_event(3, s);
+    if ((e = launch_tc_mix(p, b, s)) != 0) return cuda_fail((cudaError_t)e);
+    record_event(4, s);
+    if ((e = launch_tc_output(p, p.chunk, q, b, out, s)) != 0) return cuda_fail((cudaError_t)e);
+    record_event(5, s);
     return MHLA_OK;
   }
   float* stack = reinterpret_cast<float*>(ws + p.off_stack);
@@ -336,22 +357,26 @@ mhla_status run_plan(const Plan& plan, const void* q, const void* k, const void*
     float* mcl = reinterpret_cast<float*>(ws + p.off_mcl);
     if ((e = launch_mc_strict_lower(p, mc, mcl, s)) != 0) return cuda_fail((cudaError_t)e);
     if ((e = launch_mc_rowsum(p, mcl, rowsum, s)) != 0) return cuda_fail((cudaError_t)e);
-    if ((e = launch_simt_summary(p, k, v, stack, s)) != 0) return cuda_fail((cudaError_t)e);
     record_event(1, s);
-    if ((e = launch_simt_mix(p, mcl, stack, mixed, s)) != 0) return cuda_fail((cudaError_t)e);
+    if ((e = launch_simt_summary(p, k, v, stack, s)) != 0) return cuda_fail((cudaError_t)e);
     record_event(2, s);
+    record_event(3, s);
+    if ((e = launch_simt_mix(p, mcl, stack, mixed, s)) != 0) return cuda_fail((cudaError_t)e);
+    record_event(4, s);
     if ((e = launch_simt_causal_output(p, q, k, v, mixed, rowsum, mc, out, s)) != 0)
       return cuda_fail((cudaError_t)e);
-    record_event(3, s);
+    record_event(5, s);
     return MHLA_OK;
   }
   if ((e = launch_mc_rowsum(p, mc, rowsum, s)) != 0) return cuda_fail((cudaError_t)e);
-  if ((e = launch_simt_summary(p, k, v, stack, s)) != 0) return cuda_fail((cudaError_t)e);
   record_event(1, s);
-  if ((e = launch_simt_mix(p, mc, stack, mixed, s)) != 0) return cuda_fail((cudaError_t)e);
+  if ((e = launch_simt_summary(p, k, v, stack, s)) != 0) return cuda_fail((cudaError_t)e);
   record_event(2, s);
-  if ((e = launch_simt_output(p, q, mixed, rowsum, out, s)) != 0) return cuda_fail((cudaError_t)e);
   record_event(3, s);
+  if ((e = launch_simt_mix(p, mc, stack, mixed, s)) != 0) return cuda_fail((cudaError_t)e);
+  record_event(4, s);
+  if ((e = launch_simt_output(p, q, mixed, rowsum, out, s)) != 0) return cuda_fail((cudaError_t)e);
+  record_event(5, s);
   return MHLA_OK;
 }
 
@@ -530,9 +555,11 @@ int run_backward(const Plan& plan, const BwdLayout& lay, const void* q, const vo
     b.mc_lo = H(lay.mc_lo);
     b.rowsum = F(lay.rowsum);
     b.blkinfo = reinterpret_cast<float4*>(ws + lay.blkinfo);
+    b.rexp = nullptr;
+    b.mcx = nullptr;
+    b.sinfo = nullptr;
     b.Qp = p.Qp;
     b.f16 = false;
-    b.stack_scale = 1.f;
     b.slots = p.BH;
     b.flow = nullptr;
     if ((e = launch_tc_prep(pr, mc, b, s)) != 0) return e;

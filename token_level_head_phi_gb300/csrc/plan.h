@@ -90,11 +90,13 @@ struct Plan {
   // tensor-core path buffers
   size_t off_stack_lo, off_mixed_lo;
   size_t off_mc_f16, off_mc_scale, off_mc_hi, off_mc_lo, off_blkinfo;
+  // fp16 path: per-record exponents, per-head fp16 Mc copies, per-(head,
+  // block) output scales
+  size_t off_rexp, off_mcx, off_sinfo;
   int Qp;
   int slots;          // heads the stack and mixed buffers hold (BH, or the fused ring)
   size_t off_flow;    // fused launch: [3][BH] progress counters
-  int f16_mix;        // S part of the mixing in fp16 (DIVISIVE and NONE)
-  float stack_scale;  // 2^-ceil(log2(tokens per piece))
+  int f16_mix;        // fp16 records and mixing (DIVISIVE and NONE, multi-pass)
   // divisions by Mw and Mw * Mh (block index -> block grid coordinates)
   FastDiv f_mw, f_mwh;
   // device error word (code, detail), set by kernels whose bounded waits

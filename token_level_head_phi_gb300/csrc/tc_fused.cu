@@ -55,7 +55,10 @@ struct FusedArgs {
   unsigned int stall;          // testing: the output waits for a signal that never comes
 };
 
-template <bool kMala>
+// Every norm mixes split (bf16 high + low) records here: the fp16 records'
+// exponents are folded into Mc by a pass between the summaries and the
+// mixing, which the concurrent groups do not have.
+template <bool kOutLo, bool kQLo>
 __global__ void __launch_bounds__(kThreads, 1) tc_fused_kernel(const __grid_constant__ FusedArgs a, const Plan p) {
   FlowCtl f;
   f.ring = a.ring;
@@ -71,22 +74,22 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fused_kernel(const __grid_cons
   if (cta < a.n_s) {
     f.cta = cta;
     f.ncta = a.n_s;
-    sm::summary_body<kMala>(a.s, p, f);
+    sm::summary_body<true>(a.s, p, f);
   } else if (cta < a.n_s + a.n_x) {
     f.cta = cta - a.n_s;
     f.ncta = a.n_x;
-    mx::mix_body<!kMala>(a.x, p, f);
+    mx::mix_body<false>(a.x, p, f);
   } else {
     f.cta = cta - a.n_s - a.n_x;
     f.ncta = a.n_o;
-    ot::output_body<kMala>(a.o, p, f);
+    ot::output_body<kOutLo, kQLo>(a.o, p, f);
   }
 }
 
 // Costs the group split assumes: a streaming CTA moves about 40 GB/s of
 // Q/K/V/O; a mixing unit (128 r x NT query blocks) takes a fixed ~1.3 us
-// (barriers, epilogue, stores) plus ~0.45 us per 64-deep K step of a
-// 256-wide tile (about 2.5x that for the three bf16 products of MALA).
+// (barriers, epilogue, stores) plus ~1.1 us per 64-deep K step of a
+// 256-wide tile (the three bf16 products of the split records).
 constexpr double kStreamBytesPerSmUs = 40.0e3;
 constexpr double kMixUnitUs = 1.3;
 constexpr double kMixStepUs = 0.45;
@@ -106,7 +109,7 @@ void split_groups(const Plan& p, const FusedArgs& a, int total, int* n) {
     }
   }
   const double stream = (double)p.BH * p.N * p.d * 4.0;  // bytes of K+V, and of Q+O
-  const double step = kMixStepUs * (p.norm == MHLA_NORM_MALA ? 2.5 : 1.0) * a.x.kchunks * a.x.NT / 256.0;
+  const double step = kMixStepUs * 2.5 * a.x.kchunks * a.x.NT / 256.0;
   const double mix = (double)a.x.units * (kMixUnitUs + step);
   const double w[3] = {stream / kStreamBytesPerSmUs, mix, stream / kStreamBytesPerSmUs};
   const int cap[3] = {a.s.units, a.x.units, a.o.units};
@@ -135,12 +138,12 @@ void split_groups(const Plan& p, const FusedArgs& a, int total, int* n) {
   }
 }
 
-template <bool kMala>
+template <bool kOutLo, bool kQLo>
 int launch_variant(FusedArgs& a, const Plan& p, cudaStream_t s) {
-  auto kern = tc_fused_kernel<kMala>;
-  uint32_t smem = summary_smem_bytes(kMala);
+  auto kern = tc_fused_kernel<kOutLo, kQLo>;
+  uint32_t smem = summary_smem_bytes(true);
   if (mix_smem_bytes() > smem) smem = mix_smem_bytes();
-  if (output_smem_bytes(kMala) > smem) smem = output_smem_bytes(kMala);
+  if (output_smem_bytes(kOutLo, kQLo) > smem) smem = output_smem_bytes(kOutLo, kQLo);
   cudaError_t ce = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (ce != cudaSuccess) return (int)ce;
   int dev = 0, coop = 0, per_sm = 0;
@@ -192,7 +195,8 @@ int launch_tc_fused(const Plan& p, const ChunkShape& c, const void* q, const voi
   a.need_o = (unsigned)(p.M * c.per_block);
   a.wait_ns = debug_flow_wait_ns();
   a.stall = debug_flow_stall();
-  return p.norm == MHLA_NORM_MALA ? launch_variant<true>(a, p, s) : launch_variant<false>(a, p, s);
+  if (tc_q_lo(p)) return tc_out_lo(p) ? launch_variant<true, true>(a, p, s) : launch_variant<false, true>(a, p, s);
+  return tc_out_lo(p) ? launch_variant<true, false>(a, p, s) : launch_variant<false, false>(a, p, s);
 }
 
 }  // namespace mhla

@@ -46,23 +46,45 @@ ChunkShape choose_chunk(const Plan& p);
 // The stack and the mixed summaries hold `slots` heads: every head (slots =
 // BH) for the multi-pass launches, a ring of heads reused in turn for the
 // fused launch.
+//
+// Two precisions.  fp16 (DIVISIVE and NONE, multi-pass): record q holds
+// S_b * 2^-eS[q] and z_b * 2^-eZ[q] in fp16 (v_b, which only MALA reads, is
+// stored as zeros), the exponents chosen from the record's own largest
+// entries; the mixing multiplies by per-head fp16 copies of Mc into which
+// those exponents are folded (mcx), and the output step applies a per-(head,
+// block) power of two (sinfo).  Split (MALA, the causal form, the fused
+// launch, the backward's recomputation): every record as bf16 high + low
+// parts, Mc as bf16 high + low parts.
 struct TcBuffers {
-  void* stack;               // [slots][Q][R]: fp16(x * stack_scale) (DIVISIVE/NONE) or bf16 high part (MALA)
-  __nv_bfloat16* stack_lo;   // [slots][Q][R] low bf16 residual (MALA only, else nullptr)
-  __nv_bfloat16* mixed_hi;   // [slots][M][R] S~_i, z~_i, v~_i high parts
+  void* stack;               // [slots][Q][R]: fp16 scaled record (fp16 path) or bf16 high part (split)
+  __nv_bfloat16* stack_lo;   // [slots][Q][R] low bf16 residual (split path, else nullptr)
+  __nv_bfloat16* mixed_hi;   // [slots][M][R] S~_i, z~_i, v~_i high parts (fp16 path: times 2^-ES, 2^-EZ)
   __nv_bfloat16* mixed_lo;   // [slots][M][R] low residuals (S~ part for MALA only)
-  __half* mc_f16;            // [M][Qp] Mc[i][q / splits] * 2^-e_i in fp16
+  __half* mc_f16;            // [M][Qp] Mc[i][q / splits] * 2^-e_i in fp16 (unused by the fp16 path)
   float* mc_scale;           // [M] 2^e_i (power of two with max_b |Mc[i][b]| <= 2^e_i)
   __nv_bfloat16* mc_hi;      // [M][Qp] bf16(Mc[i][q / splits])
   __nv_bfloat16* mc_lo;      // [M][Qp] low bf16 residual of the same
   float* rowsum;             // [M] sum_b (hi + lo)(Mc[i][b])
-  float4* blkinfo;           // [M] {scale the output step applies to S~_i, n~_i, 0, 0}
+  float4* blkinfo;           // [M] {1, n~_i, 0, 0} (split path)
+  int2* rexp;                // fp16 path: [slots][Q] record exponents {eS, eZ}
+  __half* mcx;               // fp16 path: [slots][2][M][Qp] Mc[i][q / splits] 2^(eS[q] - ES[i]) (part 0),
+                             //            the same with eZ, EZ (part 1)
+  float4* sinfo;             // fp16 path: [slots][M] {output scale, 0, 0, 0}
   int Qp;                    // padded row pitch of the Mc copies
-  bool f16;                  // fp16 stack and mixing (DIVISIVE and NONE)
-  float stack_scale;         // 2^-ceil(log2(tokens per piece))
+  bool f16;                  // fp16 records and mixing
   int slots;                 // heads the stack and mixed buffers hold
   unsigned int* flow;        // fused launch: [3][BH] progress counters, zeroed by the prep kernel
 };
+
+// Whether the output step multiplies phi(Q) by the low residual of S~_i too
+// (a second MMA per K step), which the mixing then writes.  MALA cancels its
+// leading terms; exponential features let a few tokens dominate every
+// feature, so the bf16 rounding of S~_i no longer averages out.
+inline bool tc_out_lo(const Plan& p) { return p.norm == MHLA_NORM_MALA || p.fmap == MHLA_FEATURE_EXP; }
+// Whether phi(Q) enters the output step as bf16 high + low parts
+// (exponential features: the rounding of e^q to bf16 does not average out
+// either, and MALA's cancellation amplifies it).
+inline bool tc_q_lo(const Plan& p) { return p.fmap == MHLA_FEATURE_EXP; }
 
 // Launch with programmatic stream serialization (the kernel's body calls
 // pdl_wait before it reads its predecessor's results).
@@ -85,6 +107,9 @@ int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cud
 int launch_tc_prep(const Plan& p, const float* mc, const TcBuffers& b, cudaStream_t s);
 int launch_tc_summary(const Plan& p, const ChunkShape& c, const void* k, const void* v, const TcBuffers& b,
                       cudaStream_t s);
+// fp16 path, between the summaries and the mixing: the per-head Mc copies
+// with the record exponents folded in, and the output scales.
+int launch_tc_scale(const Plan& p, const float* mc, const TcBuffers& b, cudaStream_t s);
 int launch_tc_mix(const Plan& p, const TcBuffers& b, cudaStream_t s);
 int launch_tc_output(const Plan& p, const ChunkShape& c, const void* q, const TcBuffers& b, void* out,
                      cudaStream_t s);

@@ -23,15 +23,16 @@ using mx::kThreads;
 
 // Also zeroes the progress counters of a fused launch.
 // One warp per row i of Mc: the fp16 copy scaled by 2^-e_i (largest entry of
-// the row in [0.5, 1]), the bf16 high and low parts, the row scale 2^e_i and
-// the row sum of hi + lo in float32.  Columns are expanded over pieces.
-// `rows` rows of length M: every row of every mixing matrix (one per head
-// when each head has its own).
+// the row in [0.5, 1]), the bf16 high and low parts, the row scale 2^e_i, the
+// row sum of hi + lo in float32 and the block record {1, n~_i} of the split
+// path's output step.  Columns are expanded over pieces.  `rows` rows of
+// length M: every row of every mixing matrix (one per head when each head has
+// its own).
 __global__ void tc_prep_kernel(int rows, int M, int splits, int Q, int Qp, const float* __restrict__ mc,
                                __half* __restrict__ mc_f16, float* __restrict__ mc_scale,
                                __nv_bfloat16* __restrict__ mc_hi, __nv_bfloat16* __restrict__ mc_lo,
-                               float* __restrict__ rowsum, float4* __restrict__ blkinfo, int f16,
-                               float inv_stack_scale, float nb, unsigned int* __restrict__ flow, int nflow) {
+                               float* __restrict__ rowsum, float4* __restrict__ blkinfo, float nb,
+                               unsigned int* __restrict__ flow, int nflow) {
   // the previous call's kernels may still read what this one writes
   pdl_wait();
   pdl_launch_dependents();
@@ -65,9 +66,7 @@ __global__ void tc_prep_kernel(int rows, int M, int splits, int Q, int Qp, const
   if (lane == 0) {
     rowsum[i] = s;
     mc_scale[i] = ldexpf(1.f, ex);
-    // the fp16 mixing leaves S~_i divided by 2^ex 2^s; the output step
-    // multiplies it back
-    blkinfo[i] = make_float4(f16 ? ldexpf(inv_stack_scale, ex) : 1.f, nb * s, 0.f, 0.f);
+    blkinfo[i] = make_float4(1.f, nb * s, 0.f, 0.f);
   }
 }
 
@@ -87,14 +86,12 @@ int launch_variant(const MixArgs& a, const Plan& p, cudaStream_t s) {
   return launch_pdl(tc_mix_kernel<kF16>, dim3(grid), dim3(kThreads), kSmemBytes, s, a, p);
 }
 
-template <bool kF16>
 __global__ void __launch_bounds__(mt::kThreads, 1) tc_mixt_kernel(const __grid_constant__ mt::MixTArgs a, const Plan p) {
-  mt::mixt_body<kF16>(a, p);
+  mt::mixt_body(a, p);
 }
 
-template <bool kF16>
 int launch_mixt(const mt::MixTArgs& a, const Plan& p, cudaStream_t s) {
-  auto kern = tc_mixt_kernel<kF16>;
+  auto kern = tc_mixt_kernel;
   cudaError_t ce = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)mt::kSmemBytes);
   if (ce != cudaSuccess) return (int)ce;
   int grid = a.itiles * a.items;
@@ -107,15 +104,14 @@ int launch_mixt(const mt::MixTArgs& a, const Plan& p, cudaStream_t s) {
 bool mixt_supported(const Plan& p, const TcBuffers& b) {
   const int Q = p.M * p.splits;
   const int kchunks = (Q + 63) / 64;
-  // Mc (and its low part under MALA) plus two 128-column accumulators fit
-  // the 512 TMEM columns.  Taken for one query-block tile (M <= 128) with the
-  // fp16 mixing: then every stack tile is read once, as in the streaming
-  // kernel, and Mc stays off shared memory (measured: 1D 32k 29 -> 23 us,
-  // 14x14 x 192 heads 60 -> 40 us).  With more tiles each stack tile would be
-  // read once per 128 query blocks instead of once per 256 (video: 66 -> 89
-  // us), and under MALA the two kernels measured the same.
-  if (p.mc_heads != 1) return false;  // Mc stays resident per CTA: one matrix only
-  return p.R % 128 == 0 && kchunks * 32 * (b.f16 ? 1 : 2) <= 256 && p.M <= 128 && b.f16;
+  // The head's two fp16 Mc copies plus two 128-column accumulators fit the
+  // 512 TMEM columns.  Taken for one query-block tile (M <= 128): then every
+  // stack tile is read once, as in the streaming kernel, and Mc stays off
+  // shared memory (measured: 1D 32k 29 -> 23 us, 14x14 x 192 heads 60 -> 40
+  // us).  With more tiles each stack tile would be read once per 128 query
+  // blocks instead of once per 256 (video: 66 -> 89 us); the split precision
+  // of MALA measured the same in both kernels and stays on the streaming one.
+  return b.f16 && p.R % 128 == 0 && 2 * kchunks * 32 <= 256 && p.M <= 128;
 }
 
 int build_mixt_args(const Plan& p, const TcBuffers& b, mt::MixTArgs* out) {
@@ -127,24 +123,20 @@ int build_mixt_args(const Plan& p, const TcBuffers& b, mt::MixTArgs* out) {
   const uint64_t strX[3] = {2ull * W, 128, 2ull * W * Q};
   const uint32_t boxX[4] = {64, 64, 2, 1};
   int e;
-  if ((e = encode_tmap(&a.tmX, b.stack, 4, dimsX, strX, boxX, b.f16)) != 0) return e;
-  if ((e = encode_tmap_bf16(&a.tmX_lo, b.stack_lo ? (const void*)b.stack_lo : b.stack, 4, dimsX, strX, boxX)) != 0)
-    return e;
+  if ((e = encode_tmap(&a.tmX, b.stack, 4, dimsX, strX, boxX, true)) != 0) return e;
   const uint64_t dimsO[3] = {(uint64_t)p.R, (uint64_t)p.M, (uint64_t)b.slots};
   const uint64_t strO[2] = {2ull * p.R, 2ull * p.R * p.M};
   const uint32_t boxO[3] = {64, 128, 1};
   if ((e = encode_tmap_bf16(&a.tmO, b.mixed_hi, 3, dimsO, strO, boxO)) != 0) return e;
   if ((e = encode_tmap_bf16(&a.tmO_lo, b.mixed_lo, 3, dimsO, strO, boxO)) != 0) return e;
-  a.mc = b.f16 ? (const void*)b.mc_f16 : (const void*)b.mc_hi;
-  a.mc_lo = b.mc_lo;
+  a.mcx = b.mcx;
   a.Q = Q;
   a.Qp = b.Qp;
   a.kchunks = (Q + 63) / 64;
   a.itiles = (p.M + 127) / 128;
   a.rtiles = W / 128;
   a.items = b.slots * a.rtiles;
-  a.write_lo = p.norm == MHLA_NORM_MALA;
-  a.stage_bytes = mt::kBTile * (b.f16 ? 1u : 2u);
+  a.stage_bytes = mt::kBTile;
   a.stages = (int)(mt::kStageArea / a.stage_bytes);
   if (a.stages > mt::kMaxStages) a.stages = mt::kMaxStages;
   a.err = p.err;
@@ -156,8 +148,8 @@ int launch_tc_prep(const Plan& p, const float* mc, const TcBuffers& b, cudaStrea
   const int rows = p.M * p.mc_heads;
   const int blocks = (rows * 32 + threads - 1) / threads;
   return launch_pdl(tc_prep_kernel, dim3(blocks), dim3(threads), 0, s, rows, p.M, p.splits, p.M * p.splits, b.Qp, mc,
-                    b.mc_f16, b.mc_scale, b.mc_hi, b.mc_lo, b.rowsum, b.blkinfo, b.f16 ? 1 : 0, 1.f / b.stack_scale,
-                    (float)p.nb, b.flow, b.flow ? 3 * p.BH : 0);
+                    b.mc_f16, b.mc_scale, b.mc_hi, b.mc_lo, b.rowsum, b.blkinfo, (float)p.nb, b.flow,
+                    b.flow ? 3 * p.BH : 0);
 }
 
 int build_mix_args(const Plan& p, const TcBuffers& b, int slots, mx::MixArgs* out) {
@@ -182,12 +174,14 @@ int build_mix_args(const Plan& p, const TcBuffers& b, int slots, mx::MixArgs* ou
   const int nt_max = f16 ? 256 : 128;
   int NT = (p.M + 63) / 64 * 64;
   if (NT > nt_max) NT = nt_max;
-  const uint64_t dimsB[2] = {(uint64_t)Q, (uint64_t)p.M * p.mc_heads};
+  const uint64_t dimsB[2] = {(uint64_t)Q, (uint64_t)p.M * (f16 ? 2 * slots : p.mc_heads)};
   const uint64_t strB[1] = {2ull * b.Qp};
   const uint32_t boxB[2] = {64, (uint32_t)NT};
   if (f16) {
-    if ((e = encode_tmap(&a.tmB, b.mc_f16, 2, dimsB, strB, boxB, true)) != 0) return e;
+    // the per-head copies with the record exponents folded in
+    if ((e = encode_tmap(&a.tmB, b.mcx, 2, dimsB, strB, boxB, true)) != 0) return e;
     a.tmB_lo = a.tmB;
+    a.b_per_slot = 1;
   } else {
     if ((e = encode_tmap_bf16(&a.tmB, b.mc_hi, 2, dimsB, strB, boxB)) != 0) return e;
     if ((e = encode_tmap_bf16(&a.tmB_lo, b.mc_lo, 2, dimsB, strB, boxB)) != 0) return e;
@@ -204,7 +198,7 @@ int build_mix_args(const Plan& p, const TcBuffers& b, int slots, mx::MixArgs* ou
   a.kchunks = (Q + 63) / 64;
   a.units = p.BH * a.rtiles * a.itiles;
   a.r_off = 0;
-  a.write_lo = p.norm == MHLA_NORM_MALA;
+  a.write_lo = tc_out_lo(p);
   const uint32_t btile = (uint32_t)NT * 128u;
   if (f16) {
     a.off_b = kATile;
@@ -226,7 +220,7 @@ int launch_tc_mix(const Plan& p, const TcBuffers& b, cudaStream_t s) {
     mt::MixTArgs t;
     int e = build_mixt_args(p, b, &t);
     if (e != 0) return e;
-    return b.f16 ? launch_mixt<true>(t, p, s) : launch_mixt<false>(t, p, s);
+    return launch_mixt(t, p, s);
   }
   MixArgs a;
   int e = build_mix_args(p, b, b.slots, &a);

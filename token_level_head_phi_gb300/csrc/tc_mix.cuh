@@ -10,14 +10,16 @@
 //   A = X^T  : MN-major (r contiguous), two 64-wide atoms per 128-row tile
 //   B = McExp: K-major (q contiguous), N = up to 256 query blocks per tile
 // Two precisions:
-//   kF16  (DIVISIVE/NONE): X = fp16(x * 2^-s), B = fp16(Mc * 2^-e_i); one MMA
-//         per K step; Mixed keeps the factor 2^-(s + e_i), which the output
-//         step multiplies back.
-//   split (MALA): X and Mc as bf16 high + low parts, D = Xh Mh + Xh Ml + Xl Mh.
+//   kF16  (DIVISIVE/NONE): X = the fp16 records (S_q 2^-eS[q], z_q 2^-eZ[q]),
+//         B = the head's fp16 copy of Mc with those exponents folded in
+//         (McS for the tiles of S rows, McZ for the tile of z and v rows);
+//         one MMA per K step; Mixed holds S~_i 2^-ES[i] and z~_i 2^-EZ[i],
+//         which the output step scales back.
+//   split (MALA, causal, fused): X and Mc as bf16 high + low parts,
+//         D = Xh Mh + Xh Ml + Xl Mh.
 // The epilogue writes Mixed as bf16 (plus the low residual where the output
 // step needs it): 32 query blocks x 128 r at a time, transposed through a
-// shared-memory tile and stored by TMA.  In the fp16 case Mixed holds
-// S~_i / 2^(s + e_i); the output step multiplies the scale back.
+// shared-memory tile and stored by TMA.
 //
 // Also here: the small preparation kernel that builds the Mc copies.
 #pragma once
@@ -49,11 +51,12 @@ constexpr uint32_t kTmemCols = 512;                 // two accumulators of up to
 
 struct MixArgs {
   CUtensorMap tmA, tmA_lo;     // 4D (64, Q, W / 64, slots), box (64, 64, 2, 1): two r atoms
-  CUtensorMap tmB, tmB_lo;     // 2D (Q, M),     box (64, NT)
+  CUtensorMap tmB, tmB_lo;     // 2D (Q, rows), box (64, NT): Mc copies, [mc_heads][M] or [slots][2][M] rows
   CUtensorMap tmO, tmO_lo;     // 3D (R, M, BH) view of Mixed, box (128, 32, 1), no swizzle
   int Q, NT, itiles, rtiles, kchunks, units;
   int r_off;                   // column of Mixed where this part starts
   int write_lo;                // write the low residual of every value
+  int b_per_slot;              // B rows per slot and part (fp16 path) instead of per mixing matrix
   int stages;
   uint32_t stage_bytes, off_alo, off_b, off_blo;
   unsigned int* err;
@@ -137,8 +140,9 @@ __device__ __forceinline__ void mix_body(const MixArgs& a, const Plan& p, const 
           const uint32_t st = base + (uint32_t)stage * a.stage_bytes;
           mbar_arrive_expect_tx(full(stage), bytes);
           tma_load_4d(st, &a.tmA, full(stage), 0, kc * 64, r0 / 64, ss, pol_a);
-          // rows of this head's mixing matrix (one matrix per head, or one shared)
-          const int ib = i0 + mc_index(p, u) * p.M;
+          // rows of this head's mixing matrix: its own fp16 copy for the S
+          // or the z part of the record, or the matrix it shares
+          const int ib = i0 + (a.b_per_slot ? (2 * ss + (r0 >= p.d * p.d ? 1 : 0)) : mc_index(p, u)) * p.M;
           tma_load_2d(st + a.off_b, &a.tmB, full(stage), kc * 64, ib, pol_b);
           if (!kF16) {
             tma_load_4d(st + a.off_alo, &a.tmA_lo, full(stage), 0, kc * 64, r0 / 64, ss, pol_a);

@@ -2,24 +2,23 @@
 // Expressivity of Linear Attention via Token-Level Multi-Head", key design 2:
 // the mixing is one product of Mc with the stack of block summaries).
 //
-// Per head, with the stack X [Q][W] (one row per block piece) and
-// McExp [M][Q] (McExp[i][q] = Mc[i][q / splits]):
-//     Mixed[i][r] = sum_q McExp[i][q] X[q][r]
+// Per head, with the fp16 record stack X [Q][W] (one row per block piece)
+// and the head's two fp16 Mc copies McS, McZ [M][Q] (Mc[i][q / splits] with
+// the records' exponents folded in, built by the scale kernel):
+//     Mixed[i][r] = sum_q Mc{S,Z}[i][q] X[q][r]
 // computed as D[i][r] with M = 128 query blocks and N = 128 record entries:
-//   A = McExp rows i0..i0+127, in TENSOR MEMORY (lane = query block, column c
-//       holds entries 2c, 2c+1 of q), loaded once per CTA: every CTA works
-//       on one query-block tile, so Mc is read from global memory once and
-//       never passes through shared memory again;
+//   A = the head's Mc copies, rows i0..i0+127, in TENSOR MEMORY (lane = query
+//       block, column c holds entries 2c, 2c+1 of q; McS then McZ), loaded by
+//       tcgen05.st when the CTA starts a head -- a CTA takes a contiguous run
+//       of (head, r-tile) items, so it reloads once per head it touches;
 //   B = X^T tile: MN-major (r contiguous), two 64-wide atoms, one 4D TMA box
 //       per 64-deep K step: the only operand traffic through shared memory.
 // Shared memory moves half as many bytes per FLOP as a kernel streaming both
 // operands, which is what bounds the mixing GEMM.  The epilogue reads rows
 // i of D, i.e. rows of the mixed summaries, and stores them without a
 // transposition (swizzled staging, TMA store).
-// Needs Q <= 512 (fp16) or Q <= 256 (MALA: Mc high and low parts) so that Mc
-// and two 128-column accumulators fit the 512 TMEM columns.
-// Precisions as in the streaming kernel: fp16 Mc rows scaled by 2^-e_i and
-// fp16 stack for DIVISIVE/NONE; bf16 hi/lo with three products for MALA.
+// Needs M <= 128 and Q <= 256 so that both copies and two 128-column
+// accumulators fit the 512 TMEM columns.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -50,19 +49,25 @@ constexpr uint32_t kAccCol = 256;                    // accumulators at columns 
 static_assert(kSmemBytes <= 232448, "shared memory");
 
 struct MixTArgs {
-  CUtensorMap tmX, tmX_lo;     // stack: 4D (64, Q, W / 64, slots), box (64, 64, 2, 1)
+  CUtensorMap tmX;             // stack: 4D (64, Q, W / 64, slots), box (64, 64, 2, 1)
   CUtensorMap tmO, tmO_lo;     // mixed: 3D (R, M, slots), box (64, 128, 1), 128-byte swizzle
-  const void* mc;              // [M][Qp] fp16 (scaled rows) or bf16 high part
-  const void* mc_lo;           // [M][Qp] bf16 low part (MALA)
+  const __half* mcx;           // [slots][2][M][Qp] the heads' fp16 Mc copies (S part, z part)
   int Q, Qp, kchunks, itiles, rtiles, items;  // items: (head, r-tile) pairs per query-block tile
-  int write_lo;                // write the low residual of every value (MALA)
   int stages;
-  uint32_t stage_bytes;        // B tile (+ its low part)
+  uint32_t stage_bytes;        // B tile
   unsigned int* err;
 };
 
+// Contiguous range [j0, j1) of the items of this CTA's query-block tile.
+__device__ __forceinline__ void mixt_items(const MixTArgs& a, int& it, int& j0, int& j1) {
+  it = (int)blockIdx.x % a.itiles;
+  const int first = (int)blockIdx.x / a.itiles;
+  const int ncta = ((int)gridDim.x - it + a.itiles - 1) / a.itiles;  // CTAs on this tile
+  j0 = (int)((long long)first * a.items / ncta);
+  j1 = (int)((long long)(first + 1) * a.items / ncta);
+}
+
 // The kernel body; `a` must live in kernel parameter space.
-template <bool kF16>
 __device__ __forceinline__ void mixt_body(const MixTArgs& a, const Plan& p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -80,11 +85,13 @@ __device__ __forceinline__ void mixt_body(const MixTArgs& a, const Plan& p) {
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
-  // this CTA's query-block tile and its share of the (head, r-tile) items
-  const int it = (int)blockIdx.x % a.itiles;
-  const int first = (int)blockIdx.x / a.itiles;
-  const int stride = ((int)gridDim.x - it + a.itiles - 1) / a.itiles;
+  // this CTA's query-block tile and its run of (head, r-tile) items
+  int it, j0, j1;
+  mixt_items(a, it, j0, j1);
   const int i0 = it * 128;
+  // first TMEM column of the part of a record tile starting at row r0
+  const uint32_t zcol = (uint32_t)a.kchunks * 32u;
+  auto a_col = [&](int r0) { return r0 >= p.d * p.d ? zcol : 0u; };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -120,7 +127,7 @@ __device__ __forceinline__ void mixt_body(const MixTArgs& a, const Plan& p) {
       bool ok = true;
       // the stack comes from the preceding kernel
       pdl_wait();
-      for (int j = first; j < a.items && ok; j += stride) {
+      for (int j = j0; j < j1 && ok; ++j) {
         const int u = j / a.rtiles;
         const int r0 = (j % a.rtiles) * 128;
         for (int kc = 0; kc < a.kchunks; ++kc) {
@@ -128,7 +135,6 @@ __device__ __forceinline__ void mixt_body(const MixTArgs& a, const Plan& p) {
           const uint32_t st = base + (uint32_t)stage * a.stage_bytes;
           mbar_arrive_expect_tx(full(stage), a.stage_bytes);
           tma_load_4d(st, &a.tmX, full(stage), 0, kc * 64, r0 / 64, u, pol);
-          if (!kF16) tma_load_4d(st + kBTile, &a.tmX_lo, full(stage), 0, kc * 64, r0 / 64, u, pol);
           ++issued;
           if (++stage == kStages) {
             stage = 0;
@@ -141,16 +147,23 @@ __device__ __forceinline__ void mixt_body(const MixTArgs& a, const Plan& p) {
   } else if (warp == 1) {
     if (lane == 0) {
       // --------------------------------------------------------------- MMA
-      const uint32_t idesc = kF16 ? idesc_f16_f32(128, 128, false, true) : idesc_bf16_f32(128, 128, false, true);
-      const uint32_t a_hi = tmem, a_lo = tmem + (uint32_t)a.kchunks * 32u;
-      int stage = 0, acc = 0;
-      uint32_t phase = 0, accph = 0;
-      bool ok = mbar_wait(mc_ready, 0, a.err, 0x213, abort_flag);
-      tc_fence_after();
-      for (int j = first; j < a.items && ok; j += stride) {
+      const uint32_t idesc = idesc_f16_f32(128, 128, false, true);
+      int stage = 0, acc = 0, cur_u = -1;
+      uint32_t phase = 0, accph = 0, loads = 0;
+      bool ok = true;
+      for (int j = j0; j < j1 && ok; ++j) {
+        const int u = j / a.rtiles;
+        const int r0 = (j % a.rtiles) * 128;
+        if (u != cur_u) {
+          // the A operand of head u is in tensor memory
+          if (!(ok = mbar_wait(mc_ready, loads & 1u, a.err, 0x213, abort_flag))) break;
+          ++loads;
+          cur_u = u;
+        }
         if (!(ok = mbar_wait(accempty(acc), accph ^ 1u, a.err, 0x214, abort_flag))) break;
         tc_fence_after();
         const uint32_t d = tmem + kAccCol + (uint32_t)acc * 128u;
+        const uint32_t a_base = tmem + a_col(r0);
         for (int kc = 0; kc < a.kchunks; ++kc) {
           if (!(ok = mbar_wait(full(stage), phase, a.err, 0x215, abort_flag))) break;
           tc_fence_after();
@@ -159,12 +172,7 @@ __device__ __forceinline__ void mixt_body(const MixTArgs& a, const Plan& p) {
           for (int ks = 0; ks < 4; ++ks) {
             const uint32_t acol = (uint32_t)(kc * 32 + ks * 8);
             const uint64_t bhi = sdesc_sw128(st + (uint32_t)ks * 2048u, kAtom, 1024u);
-            umma_tmem_a(d, a_hi + acol, bhi, idesc, (kc > 0 || ks > 0) ? 1u : 0u);
-            if (!kF16) {
-              const uint64_t blo = sdesc_sw128(st + kBTile + (uint32_t)ks * 2048u, kAtom, 1024u);
-              umma_tmem_a(d, a_lo + acol, bhi, idesc, 1u);
-              umma_tmem_a(d, a_hi + acol, blo, idesc, 1u);
-            }
+            umma_tmem_a(d, a_base + acol, bhi, idesc, (kc > 0 || ks > 0) ? 1u : 0u);
           }
           umma_commit(empty(stage));
           if (++stage == kStages) {
@@ -185,18 +193,17 @@ __device__ __forceinline__ void mixt_body(const MixTArgs& a, const Plan& p) {
     const int g = (warp - 4) >> 2;            // record columns 64g .. 64g+63 of the tile
     const int gt = threadIdx.x - 128 - 128 * g;
     const int row = 32 * q4 + lane;           // query block i0 + row
-    if (g == 0) {
-      // --------------------------------- Mc rows of this tile into TMEM
-      // row i: McExp[i][q] for q < 64 * kchunks (zero past Q and past M),
-      // 16-bit pairs per 32-bit column; the MALA low part follows the high
-      const int i = i0 + row;
-      // the Mc copies come from the prep kernel, which has finished once the
-      // preceding kernel has
-      pdl_wait();
-      for (int part = 0; part < (kF16 ? 1 : 2); ++part) {
-        const uint16_t* src = static_cast<const uint16_t*>(part ? a.mc_lo : a.mc) + (size_t)i * a.Qp;
+    // Group 0 (warps 4-7) also writes the A operand: rows i0..i0+127 of head
+    // u's two Mc copies, McS[i][q] and McZ[i][q] for q < 64 * kchunks (zero
+    // past Q and past M), 16-bit pairs per 32-bit column.  The copies come
+    // from the scale kernel, which has finished once the preceding kernel
+    // (this CTA waits for it) has.
+    const int i = i0 + 32 * q4 + lane;
+    auto load_a = [&](int u) {
+      for (int part = 0; part < 2; ++part) {
+        const uint16_t* src = reinterpret_cast<const uint16_t*>(a.mcx) + (((size_t)u * 2 + part) * p.M + i) * a.Qp;
         for (int c0 = 0; c0 < a.kchunks * 32; c0 += 32) {
-          // 64 entries of q from 2 * c0, eight at a time (the copy's rows are
+          // 64 entries of q from 2 * c0, eight at a time (the copies' rows are
           // zero from Q to the padded pitch Qp, a multiple of 8)
           uint32_t w[32];
 #pragma unroll
@@ -209,12 +216,16 @@ __device__ __forceinline__ void mixt_body(const MixTArgs& a, const Plan& p) {
             w[4 * g8 + 2] = x.z;
             w[4 * g8 + 3] = x.w;
           }
-          tmem_st32(tmem + (uint32_t)(part * a.kchunks * 32 + c0) + ((uint32_t)(32 * q4) << 16), w);
+          tmem_st32(tmem + (uint32_t)part * zcol + (uint32_t)c0 + ((uint32_t)(32 * q4) << 16), w);
         }
       }
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive_warp(mc_ready);
+    };
+    if (g == 0 && j0 < j1) {
+      pdl_wait();
+      load_a(j0 / a.rtiles);
     }
     // ------------------------------------------------------------ epilogue
     uint8_t* stg = gb + kStaging + g * kStagingGroup;
@@ -222,13 +233,16 @@ __device__ __forceinline__ void mixt_body(const MixTArgs& a, const Plan& p) {
     int acc = 0;
     uint32_t accph = 0;
     bool ok = true;
-    for (int j = first; j < a.items && ok; j += stride) {
+    for (int j = j0; j < j1 && ok; ++j) {
       const int u = j / a.rtiles;
       const int r0 = (j % a.rtiles) * 128 + 64 * g;
-      const bool lo = a.write_lo || r0 >= p.d * p.d;  // z~, v~ always carry their low residual
+      const bool lo = r0 >= p.d * p.d;  // z~, v~ always carry their low residual
       ok = mbar_wait(accfull(acc), accph, a.err, 0x216, abort_flag);
       if (!(ok = named_all(1 + g, 128, ok))) break;
       tc_fence_after();
+      // every MMA that read head u's A operand has completed: the next
+      // item's head, if another, takes its place
+      if (g == 0 && j + 1 < j1 && (j + 1) / a.rtiles != u) load_a((j + 1) / a.rtiles);
       float v0[32], v1[32];
       const uint32_t taddr = tmem + kAccCol + (uint32_t)acc * 128u + (uint32_t)(64 * g) + ((uint32_t)(32 * q4) << 16);
       tmem_ld32(taddr, v0);

@@ -13,21 +13,22 @@ using namespace tc;
 using ot::OutArgs;
 using ot::kThreads;
 
-template <bool kLo>
+template <bool kLo, bool kQLo>
 __global__ void __launch_bounds__(ot::kThreads, 1) tc_output_kernel(const __grid_constant__ ot::OutArgs a, const Plan p) {
   FlowCtl f = {};
   f.cta = blockIdx.x;
   f.ncta = gridDim.x;
-  ot::output_body<kLo>(a, p, f);
+  ot::output_body<kLo, kQLo>(a, p, f);
 }
 
-template <bool kLo>
+template <bool kLo, bool kQLo>
 int launch_variant(const OutArgs& a, const Plan& p, cudaStream_t s) {
-  const uint32_t smem = output_smem_bytes(kLo);
-  cudaError_t ce = cudaFuncSetAttribute(tc_output_kernel<kLo>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const uint32_t smem = output_smem_bytes(kLo, kQLo);
+  auto kern = tc_output_kernel<kLo, kQLo>;
+  cudaError_t ce = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (ce != cudaSuccess) return (int)ce;
   const int grid = a.units < num_sms() ? a.units : num_sms();
-  return launch_pdl(tc_output_kernel<kLo>, dim3(grid), dim3(kThreads), smem, s, a, p);
+  return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, s, a, p);
 }
 
 }  // namespace
@@ -44,7 +45,8 @@ int build_output_args(const Plan& p, const ChunkShape& c, const void* q, const T
   const uint32_t box3[3] = {64, 64, 1};
   if ((e = encode_tmap_bf16(&a.tmB_hi, b.mixed_hi, 3, dims3, str3, box3)) != 0) return e;
   if ((e = encode_tmap_bf16(&a.tmB_lo, b.mixed_lo, 3, dims3, str3, box3)) != 0) return e;
-  a.blkinfo = b.blkinfo;
+  a.blkinfo = b.f16 ? b.sinfo : b.blkinfo;
+  a.info_per_slot = b.f16 ? 1 : 0;
   a.mixed_hi = b.mixed_hi;
   a.mixed_lo = b.mixed_lo;
   a.R = p.R;
@@ -61,7 +63,8 @@ int launch_tc_output(const Plan& p, const ChunkShape& c, const void* q, const Tc
   OutArgs a;
   int e = build_output_args(p, c, q, b, out, b.slots, &a);
   if (e != 0) return e;
-  return p.norm == MHLA_NORM_MALA ? launch_variant<true>(a, p, s) : launch_variant<false>(a, p, s);
+  if (tc_q_lo(p)) return tc_out_lo(p) ? launch_variant<true, true>(a, p, s) : launch_variant<false, true>(a, p, s);
+  return tc_out_lo(p) ? launch_variant<true, false>(a, p, s) : launch_variant<false, false>(a, p, s);
 }
 
 }  // namespace mhla

@@ -21,6 +21,8 @@
 // Two rings of shared-memory stages: Q tiles (16 KB, streamed from HBM, the
 // deep one: it sets how many bytes are in flight) and the per-block operands
 // S~_i, Z, z~_i / v~_i rows and the output scale (read from L2, a few stages).
+// With exponential features phi(Q) also goes in as bf16 high + low parts:
+// the low parts through a third, short ring and one more MMA per K step.
 // Persistent, warp-specialised CTA (640 threads): warp 0 Q producer, warp 1
 // TMEM + MMA, warp 2 block-operand producer, warp 3 Z and v~_i, warps 4-11
 // phi(Q) (two threads per token row), warps 12-19 epilogue (two warps per
@@ -50,10 +52,15 @@ constexpr int kAccSlots = 4;                       // TMEM accumulators (128 col
 constexpr uint32_t kAccStride = 128;
 constexpr uint32_t kTmemCols = 512;
 
-// Shared-memory layout; kLo (MALA) adds the low residual of S~_i.
-template <bool kLo>
+// Shared-memory layout; kLo (MALA, exponential features) adds the low
+// residual of S~_i, kQLo (exponential features) a ring of kQLoStages tiles
+// for the low residual of phi(Q), each free again once its tile's MMAs have
+// completed.
+template <bool kLo, bool kQLo>
 struct Layout {
-  static constexpr int kQStages = kLo ? 7 : 9;
+  static constexpr int kQStages = (kLo ? 7 : 9) - (kQLo ? 2 : 0);
+  static constexpr int kQLoStages = kQLo ? 2 : 0;
+  static constexpr uint32_t kQLoBase = kQStages * kQTile;
   // block-operand stage: S~_i hi [, lo] | Z (the second N atom of B) | misc
   static constexpr uint32_t kOffBlo = kBTile;
   static constexpr uint32_t kOffZ = kLo ? 2 * kBTile : kBTile;
@@ -63,16 +70,16 @@ struct Layout {
   static constexpr uint32_t kOffAuxLo = kOffMisc + 512;     // same, low residuals
   static constexpr uint32_t kOffInfo = kOffMisc + 768;      // float4 {output scale, n~_i, 0, 0}
   static constexpr uint32_t kBStageBytes = kOffMisc + 1024;
-  static constexpr uint32_t kBBase = kQStages * kQTile;
+  static constexpr uint32_t kBBase = kQLoBase + kQLoStages * kQTile;
   static constexpr uint32_t kBars = kBBase + kBStages * kBStageBytes;
-  static constexpr int kNumBars = 4 * kQStages + 3 * kBStages + kAccSlots;
+  static constexpr int kNumBars = 4 * kQStages + 3 * kBStages + kAccSlots + kQLoStages;
   static constexpr uint32_t kSmemBytes = kBars + 8 * kNumBars + 16 + 1024;
   static_assert(kBStageBytes % 1024 == 0, "stage alignment");
 };
 
-constexpr uint32_t kSmemBytes =
-    Layout<false>::kSmemBytes > Layout<true>::kSmemBytes ? Layout<false>::kSmemBytes : Layout<true>::kSmemBytes;
-static_assert(kSmemBytes <= 232448, "shared memory");
+static_assert(Layout<false, false>::kSmemBytes <= 232448 && Layout<true, false>::kSmemBytes <= 232448 &&
+                  Layout<false, true>::kSmemBytes <= 232448 && Layout<true, true>::kSmemBytes <= 232448,
+              "shared memory");
 
 struct OutArgs {
   CUtensorMap tmQ, tmO;        // 5D (64, Wg, Hg, T, BH), box (64, cw, ch, ct, 1)
@@ -81,6 +88,7 @@ struct OutArgs {
   int R;                          // record length
   CUtensorMap tmB_hi, tmB_lo;  // 3D (64, R/64, slots*M), box (64, 64, 1)
   const float4* blkinfo;       // per query block {output scale, n~_i, 0, 0}
+  int info_per_slot;           // blkinfo rows per slot (fp16 path) instead of per mixing matrix
   int units;
   ChunkShape c;
   FastDiv f_head, f_nck;       // divisions by M * nck and by nck (units per head, per block)
@@ -99,9 +107,9 @@ __device__ __forceinline__ void out_unit(const Plan& p, const OutArgs& a, int w,
 }
 
 // The kernel body; `a` must live in kernel parameter space.
-template <bool kLo>
+template <bool kLo, bool kQLo>
 __device__ __forceinline__ void output_body(const OutArgs& a, const Plan& p, const FlowCtl& f) {
-  using L = Layout<kLo>;
+  using L = Layout<kLo, kQLo>;
   constexpr int kQStages = L::kQStages;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -116,6 +124,9 @@ __device__ __forceinline__ void output_body(const OutArgs& a, const Plan& p, con
   auto bready = [&](int b) { return bars + 8u * (4 * kQStages + kBStages + b); };
   auto bempty = [&](int b) { return bars + 8u * (4 * kQStages + 2 * kBStages + b); };
   auto accempty = [&](int x) { return bars + 8u * (4 * kQStages + 3 * kBStages + x); };
+  // phi(Q) low-residual tile j is free (its tile's MMAs have completed)
+  auto lofree = [&](int j) { return bars + 8u * (4 * kQStages + 3 * kBStages + kAccSlots + j); };
+  auto qlo = [&](int j) { return base + L::kQLoBase + (uint32_t)j * kQTile; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gb + L::kBars + 8 * L::kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gb + L::kBars + 8 * L::kNumBars + 8);
   auto qst = [&](int s) { return base + (uint32_t)s * kQTile; };
@@ -144,6 +155,7 @@ __device__ __forceinline__ void output_body(const OutArgs& a, const Plan& p, con
       mbar_init(bempty(b), 1);
     }
     for (int x = 0; x < kAccSlots; ++x) mbar_init(accempty(x), 1);
+    for (int j = 0; j < L::kQLoStages; ++j) mbar_init(lofree(j), 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -216,7 +228,8 @@ __device__ __forceinline__ void output_body(const OutArgs& a, const Plan& p, con
       const int rec = flow_slot(f, u) * p.M + i;  // record of S~_i in the mixed summaries
       const __nv_bfloat16* src = (lane < 16 ? a.mixed_hi : a.mixed_lo) + (size_t)rec * a.R + 64 * 64 + (lane & 15) * 8;
       cp_async16(st + (lane < 16 ? L::kOffAux : L::kOffAuxLo) + (lane & 15) * 16, src);
-      if (lane == 0) cp_async16(st + L::kOffInfo, a.blkinfo + mc_index(p, u) * p.M + i);
+      if (lane == 0)
+        cp_async16(st + L::kOffInfo, a.blkinfo + (a.info_per_slot ? flow_slot(f, u) : mc_index(p, u)) * p.M + i);
       cp_async_arrive(bfull(b));
       __syncwarp();
       if (lane == 0) {
@@ -262,7 +275,7 @@ __device__ __forceinline__ void output_body(const OutArgs& a, const Plan& p, con
       // --------------------------------------------------------------- MMA
       const uint32_t idesc80 = idesc_bf16_f32(128, 80, false, true);
       const uint32_t idesc64 = idesc_bf16_f32(128, 64, false, true);
-      int s = 0, b = 0, slot = 0;
+      int s = 0, b = 0, slot = 0, lj = 0;
       uint32_t ph = 0, bph = 0, slotph = 0;
       for (int w = f.cta; w < a.units; w += f.ncta) {
         if (!mbar_wait(qready(s), ph, a.err, 0x302, abort_flag)) break;
@@ -274,9 +287,16 @@ __device__ __forceinline__ void output_body(const OutArgs& a, const Plan& p, con
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
           const uint64_t ad = sdesc_sw128(qs + (uint32_t)ks * 32u, 0u, 1024u);
+          const uint64_t bd = sdesc_sw128(bs + (uint32_t)ks * 2048u, L::kOffZ, 1024u);
           const uint32_t acc = ks > 0 ? 1u : 0u;
-          umma_bf16(d, ad, sdesc_sw128(bs + (uint32_t)ks * 2048u, L::kOffZ, 1024u), idesc80, acc);
+          umma_bf16(d, ad, bd, idesc80, acc);
           if (kLo) umma_bf16(d, ad, sdesc_sw128(bs + L::kOffBlo + (uint32_t)ks * 2048u, kBTile, 1024u), idesc64, 1u);
+          // the low residual of phi(Q) times [S~_i | Z]
+          if (kQLo) umma_bf16(d, sdesc_sw128(qlo(lj) + (uint32_t)ks * 32u, 0u, 1024u), bd, idesc80, 1u);
+        }
+        if (kQLo) {
+          umma_commit(lofree(lj));
+          if (++lj == L::kQLoStages) lj = 0;
         }
         umma_commit(qmma(s));
         if (++s == kQStages) {
@@ -298,33 +318,46 @@ __device__ __forceinline__ void output_body(const OutArgs& a, const Plan& p, con
     const int t = threadIdx.x - 128;
     const int row = t >> 1;
     const int half = t & 1;
-    int s = 0;
-    uint32_t ph = 0;
+    int s = 0, lj = 0;
+    uint32_t ph = 0, lph = 0;
     for (int w = f.cta; w < a.units; w += f.ncta) {
-      const bool ok = mbar_wait(qfull(s), ph, a.err, 0x303, abort_flag);
+      bool ok = mbar_wait(qfull(s), ph, a.err, 0x303, abort_flag);
+      if (kQLo) ok = ok && mbar_wait(lofree(lj), lph ^ 1u, a.err, 0x30d, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) break;
       if (row < rows) {
         uint8_t* rp = gb + s * kQTile + row * 128;
+        uint8_t* lp = gb + L::kQLoBase + lj * kQTile + row * 128;
         uint4 xs[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) xs[j] = *reinterpret_cast<const uint4*>(rp + (((4 * half + j + row) & 7) << 4));
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const uint32_t off = ((4 * half + j + row) & 7) << 4;
-          uint4 x = xs[j];
+          uint4 x = xs[j], lo;
           uint32_t* xp = &x.x;
-          if (p.fmap == MHLA_FEATURE_ELU1) {
+          uint32_t* lop = &lo.x;
+          if (!kQLo && p.fmap == MHLA_FEATURE_ELU1) {
 #pragma unroll
             for (int q = 0; q < 4; ++q) xp[q] = phi2_elu1_bf16(xp[q]);
           } else {
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               const float2 fv = bf16x2_to_float2(xp[q]);
-              xp[q] = pack_bf16x2(phi_map(fv.x, p.fmap), phi_map(fv.y, p.fmap));
+              const float p0 = phi_map(fv.x, p.fmap), p1 = phi_map(fv.y, p.fmap);
+              xp[q] = pack_bf16x2(p0, p1);
+              if (kQLo) {
+                const float2 hv = bf16x2_to_float2(xp[q]);
+                lop[q] = pack_bf16x2(p0 - hv.x, p1 - hv.y);
+              }
             }
           }
           *reinterpret_cast<uint4*>(rp + off) = x;
+          if (kQLo) *reinterpret_cast<uint4*>(lp + off) = lo;
         }
+      }
+      if (kQLo && ++lj == L::kQLoStages) {
+        lj = 0;
+        lph ^= 1u;
       }
       fence_proxy_async();
       mbar_arrive_warp(qready(s));
@@ -359,11 +392,11 @@ __device__ __forceinline__ void output_body(const OutArgs& a, const Plan& p, con
         const uint8_t* bp = gb + L::kBBase + b * L::kBStageBytes;
         const float sden = s0 + s1;
         const float4 info = *reinterpret_cast<const float4*>(bp + L::kOffInfo);
-        // info.x undoes the fp16 mixing's power-of-two scale; under DIVISIVE
-        // numerator and denominator carry the same scale, which cancels
+        // info.x undoes the powers of two of the fp16 records: 2^(ES - EZ)
+        // under DIVISIVE, 2^ES under NONE (1 for split records)
         float scale = info.x, gamma = 0.f;
         if (p.norm == MHLA_NORM_DIVISIVE) {
-          scale = sden != 0.f ? __frcp_rn(sden) : 0.f;     // s = 0: no key mass, output 0
+          scale = sden != 0.f ? info.x * __frcp_rn(sden) : 0.f;  // s = 0: no key mass, output 0
         } else if (p.norm == MHLA_NORM_MALA) {
           scale = sden != 0.f ? 1.f + __frcp_rn(sden) : 0.f;  // beta
           gamma = sden / info.y;                            // s / n~_i
@@ -436,6 +469,9 @@ __device__ __forceinline__ void output_body(const OutArgs& a, const Plan& p, con
 // summaries hold `slots` heads.
 int build_output_args(const Plan& p, const ChunkShape& c, const void* q, const TcBuffers& b, void* out, int slots,
                       ot::OutArgs* args);
-constexpr uint32_t output_smem_bytes(bool lo) { return lo ? ot::Layout<true>::kSmemBytes : ot::Layout<false>::kSmemBytes; }
+constexpr uint32_t output_smem_bytes(bool lo, bool qlo) {
+  return lo ? (qlo ? ot::Layout<true, true>::kSmemBytes : ot::Layout<true, false>::kSmemBytes)
+            : (qlo ? ot::Layout<false, true>::kSmemBytes : ot::Layout<false, false>::kSmemBytes);
+}
 
 }  // namespace mhla

@@ -52,7 +52,7 @@ int build_summary_args(const Plan& p, const ChunkShape& c, const void* k, const 
   if ((e = encode_tmap(&a.tmZV, b.stack, 2, dims2, str2, boxZV, b.f16)) != 0) return e;
   if ((e = encode_tmap_bf16(&a.tmS_lo, lo_base, 2, dims2, str2, boxS)) != 0) return e;
   if ((e = encode_tmap_bf16(&a.tmZV_lo, lo_base, 2, dims2, str2, boxZV)) != 0) return e;
-  a.stack_scale = b.stack_scale;
+  a.rexp = b.rexp;
   a.splits = p.splits;
   a.cpp = p.cpp;
   a.units = p.BH * p.M * p.splits;

@@ -23,9 +23,12 @@
 //   warp 1       TMEM allocation; warps 1, 2 MMA issue (even / odd units,
 //                each through its own ring of stages)
 //   warps 4-6, 16-17  epilogue: TMEM rows 0..64 -> the record (S_b, z_b,
-//                v_b) as fp16 scaled by 2^-ceil(log2 n) (DIVISIVE/NONE) or as
-//                bf16 high + low parts (MALA) -> swizzled staging tiles
-//                (two, used in turn) -> TMA stores into the summary stack
+//                v_b) as fp16 (DIVISIVE/NONE: S_b and z_b each scaled by a
+//                power of two taken from its own largest entry, the two
+//                exponents stored beside the record; v_b, which only MALA
+//                reads, as zeros) or as bf16 high + low parts (split) ->
+//                swizzled staging tiles (two, used in turn) -> TMA stores
+//                into the summary stack
 //   warps 8-15   phi(K) transform, two threads per token row
 // Each CTA walks work units (head, block, piece) with a static stride; long
 // blocks are cut into pieces whose partial summaries the mixing step adds.
@@ -75,7 +78,7 @@ struct SummaryArgs {
   CUtensorMap tmS, tmS_lo;           // 2D view (64, BH*Q*66) of the stack, box (64, 64): S_b rows
   CUtensorMap tmZV, tmZV_lo;         // same view, box (64, 2): the z_b and v_b rows
   int units, splits, cpp;            // work units, pieces per block, chunks per piece
-  float stack_scale;                 // fp16 stack: values are stored times this power of two
+  int2* rexp;                        // fp16 records: [slots * M * splits] exponents {eS, eZ}
   ChunkShape c;
   FastDiv f_head, f_splits;          // divisions by M * splits and by splits
   unsigned int* err;
@@ -119,6 +122,21 @@ __device__ __forceinline__ void phi_chunk(uint4& x, uint4& lo, int fmap) {
     }
   }
 }
+
+// Exponent e of an fp16 record part whose largest magnitude is `amax`: the
+// part is stored times 2^-e, which puts that entry in [2^14, 2^15) -- every
+// entry down to 2^-29 of it stays a normal fp16 number, and no rounding can
+// reach the fp16 limit 65504.  Read from the float's exponent field
+// (amax in [2^k, 2^(k+1)) gives e = k - 14); clamped so that 2^-e is a normal
+// float (a part whose largest entry is below 2^-106 counts as zero).  An
+// infinite entry stays infinite, NaN stays NaN.
+__device__ __forceinline__ int record_exponent(float amax) {
+  const int e = (int)((__float_as_uint(amax) >> 23) & 0xFFu) - 141;
+  return min(max(e, -120), 113);
+}
+
+// 2^-e as a float, for e in [-120, 113].
+__device__ __forceinline__ float pow2_neg(int e) { return __uint_as_float((uint32_t)(127 - e) << 23); }
 
 // 8 floats (times scale) -> 8 bf16 (hi) and optionally their low residuals.
 __device__ __forceinline__ void split8(const float* src, uint4& hv, uint4& lv, float scale, bool want_lo) {
@@ -164,6 +182,9 @@ __device__ __forceinline__ void summary_body(const SummaryArgs& a, const Plan& p
   auto ring_phase = [&](int j, long long k) { return (uint32_t)((k / ring_len(j)) & 1); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gb + L::kBars + 8 * (3 * kStages + 4));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gb + L::kBars + 8 * (3 * kStages + 4) + 8);
+  // epilogue: per-warp maxima of the fp16 record parts (8 floats)
+  float* red = reinterpret_cast<float*>(gb + L::kBars + 192);
+  static_assert(8 * (3 * kStages + 4) + 12 <= 192, "barrier area");
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -371,14 +392,38 @@ __device__ __forceinline__ void summary_body(const SummaryArgs& a, const Plan& p
 
       uint8_t* st_hi = gb + L::kStaging + (it % L::kStagingBufs) * L::kStagingStride;
       uint8_t* st_lo = st_hi + kStagePart;
+      if (!kLo) {
+        // largest magnitudes of this warp's share of S_b and z_b, gathered
+        // in shared memory: red[2e + h] (S_b), red[4 + e] (z_b)
+        float am = 0.f, amz = 0.f;
+        if (e < 2) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) am = fmaxf(am, fabsf(s0[j]));
+          if (h == 0) amz = fabsf(zval);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+          amz = fmaxf(amz, __shfl_xor_sync(0xffffffffu, amz, o));
+        }
+        if (lane == 0 && e < 2) {
+          red[2 * e + h] = am;
+          if (h == 0) red[4 + e] = amz;
+        }
+      }
       if (et == 0) {
         // the store that last read this staging buffer has finished reading it
         bulk_wait_read<L::kStagingBufs - 1>();
       }
       named_sync(1, kEpiThreads);
+      int eS = 0, eZ = 0;
+      if (!kLo) {
+        eS = record_exponent(fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3])));
+        eZ = record_exponent(fmaxf(red[4], red[5]));
+      }
       if (e < 2) {
         // row r of S_b (columns 32h .. 32h+31) and, for h = 0, z_b[r]
-        float amax = 0.f;
+        const float scS = kLo ? 1.f : pow2_neg(eS);
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
           const int j = 4 * h + jj;
@@ -388,9 +433,7 @@ __device__ __forceinline__ void summary_body(const SummaryArgs& a, const Plan& p
             uint32_t* hp = &hv.x;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-              const float x0 = src[2 * q] * a.stack_scale, x1 = src[2 * q + 1] * a.stack_scale;
-              amax = fmaxf(amax, fmaxf(fabsf(x0), fabsf(x1)));
-              __half2 hh = __floats2half2_rn(x0, x1);
+              __half2 hh = __floats2half2_rn(src[2 * q] * scS, src[2 * q + 1] * scS);
               hp[q] = *reinterpret_cast<uint32_t*>(&hh);
             }
           } else {
@@ -402,9 +445,7 @@ __device__ __forceinline__ void summary_body(const SummaryArgs& a, const Plan& p
         }
         if (h == 0) {
           if (!kLo) {
-            const float zs = zval * a.stack_scale;
-            amax = fmaxf(amax, fabsf(zs));
-            *reinterpret_cast<__half*>(st_hi + 8192 + sw128_offset(0, r)) = __float2half_rn(zs);
+            *reinterpret_cast<__half*>(st_hi + 8192 + sw128_offset(0, r)) = __float2half_rn(zval * pow2_neg(eZ));
           } else {
             const __nv_bfloat16 zh = __float2bfloat16_rn(zval);
             *reinterpret_cast<__nv_bfloat16*>(st_hi + 8192 + sw128_offset(0, r)) = zh;
@@ -412,37 +453,25 @@ __device__ __forceinline__ void summary_body(const SummaryArgs& a, const Plan& p
                 __float2bfloat16_rn(zval - __bfloat162float(zh));
           }
         }
-        if (!(amax <= 65504.f)) report_error(a.err, MHLA_ERR_OVERFLOW, 0x106);
       } else if (lane == 0) {
         // row 64 of D: v_b (every row 64..127 holds the same values; the
-        // low-residual MMA of MALA adds them twice)
-        float amax = 0.f;
+        // low-residual MMA of MALA adds them twice).  The fp16 records feed
+        // DIVISIVE and NONE only, which never read v_b: zeros.
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           const float* src = j < 4 ? &s0[8 * j] : &s1[8 * (j - 4)];
-          uint4 hv, lv;
-          if (!kLo) {
-            uint32_t* hp = &hv.x;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const float x0 = src[2 * q] * a.stack_scale, x1 = src[2 * q + 1] * a.stack_scale;
-              amax = fmaxf(amax, fmaxf(fabsf(x0), fabsf(x1)));
-              __half2 hh = __floats2half2_rn(x0, x1);
-              hp[q] = *reinterpret_cast<uint32_t*>(&hh);
-            }
-          } else {
-            split8(src, hv, lv, 0.5f, true);
-          }
+          uint4 hv = make_uint4(0u, 0u, 0u, 0u), lv;
+          if (kLo) split8(src, hv, lv, 0.5f, true);
           const uint32_t off = 128u + ((uint32_t)((j ^ 1) & 7) << 4);
           *reinterpret_cast<uint4*>(st_hi + 8192 + off) = hv;
           if (kLo) *reinterpret_cast<uint4*>(st_lo + 8192 + off) = lv;
         }
-        if (!(amax <= 65504.f)) report_error(a.err, MHLA_ERR_OVERFLOW, 0x107);
       }
       fence_proxy_async();
       named_sync(1, kEpiThreads);
       if (et == 0) {
         const int srow = (flow_slot(f, uc.u) * p.M + uc.b) * a.splits + (uc.c0 / a.cpp);
+        if (!kLo) a.rexp[srow] = make_int2(eS, eZ);
         tma_store_2d(&a.tmS, smem_u32(st_hi), 0, srow * 66);
         tma_store_2d(&a.tmZV, smem_u32(st_hi + 8192), 0, srow * 66 + 64);
         if (kLo) {
