@@ -2,7 +2,7 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
                     [--variant auto|simt|multipass|fused] [--impl mine|reference]
-                    [--all-workloads] [--no-cpu-baseline] [--pass forward|backward]
+                    [--no-per-config] [--no-cpu-baseline] [--pass forward|backward]
                     [--feature-map elu1|relu|exp] [--causal] [--layout bhnd|bnhd] [--mc-per-head]
 
 A step is one full forward (block summaries, mixing, output) over one batch
@@ -10,9 +10,15 @@ of the workload's seeded synthetic inputs, already resident in HBM.  The
 metric is tokens*heads per second (B*H*N / step time).  The default workload
 is the video-shaped 3D grid (B=2, H=16, d=64, 16x64x64 tokens, 2x8x8 blocks,
 M=512): its 403 MB of inputs exceed the 126 MB L2, so no flush runs between
-timed steps.  With --all-workloads the other workloads are timed too (with an
-L2 flush between steps, outside the per-step events) and listed under
-"workloads".
+timed steps.  The default run also times every other configuration (each
+with its own warm-up, an L2 flush between steps where its inputs fit in L2,
+outside the per-step events) and lists them under "per_config".
+
+Rooflines: "roofline" is the dominant kernel of the step, "kernels" every
+kernel, each with the method's own bytes (or FLOPs) per launch divided by the
+kernel's average launch time; "path_roofline" is the whole step against
+max(bytes / HBM, FLOPs / tensor peak) with bytes = read Q, K, V, write O, read
+Mc and FLOPs = 4 N d^2 + 2 M^2 d^2 per unit.
 
 --pass backward times mhla_backward instead (one step = dQ, dK, dV and dMc of
 the same workload for a seeded dO, the forward summaries recomputed inside);
@@ -150,34 +156,83 @@ class ClockSampler:
 
 # ------------------------------------------------------------ my arm
 
-def phase_bytes(w: wl.Workload, info, variant: int):
-    """Compulsory bytes of each phase: its inputs read once, its outputs
-    written once, in the layouts the variant uses (SIMT: float32 stack and
-    mixed summaries; tensor cores: fp16 or bf16 S stack, bf16 hi+lo z/v
-    stack, bf16 mixed summaries with low residuals where the output needs
-    them)."""
+def phase_kernels(w: wl.Workload, info, fmap: str, causal: bool):
+    """Kernel that runs in each phase of one forward (None: the phase is
+    absent from this variant), as ncu names it, with its source file."""
     import token_level_head_phi_gb300.binding as mb
+    C = "token_level_head_phi_gb300/csrc/"
+    if info.variant == mb.VARIANT_SIMT:
+        return {"prep": ("mc_rowsum_kernel", C + "simt.cu"), "summary": ("simt_summary_kernel", C + "simt.cu"),
+                "scale": None, "mix": ("simt_mix_kernel", C + "simt.cu"),
+                "output": ("causal_output_kernel", C + "simt_causal.cu") if causal else
+                ("simt_output_kernel", C + "simt.cu")}
+    if info.variant == mb.VARIANT_FUSED:
+        return {"prep": ("tc_prep_kernel", C + "tc_mix.cu"), "summary": None, "scale": None, "mix": None,
+                "output": ("tc_fused_kernel", C + "tc_fused.cu")}
+    f16 = w.norm != "mala" and fmap != "exp" and not causal
+    q = w.n_blocks * info.summary_splits
+    mixt = f16 and w.n_blocks <= 128 and 2 * ((q + 63) // 64) * 32 <= 256
+    return {"prep": ("tc_prep_kernel", C + "tc_mix.cu"), "summary": ("tc_summary_kernel", C + "tc_summary.cu"),
+            "scale": ("tc_scale_kernel", C + "tc_scale.cu") if f16 else None,
+            "mix": ("tc_mixt_kernel", C + "tc_mix.cu") if mixt else ("tc_mix_kernel", C + "tc_mix.cu"),
+            "output": ("tc_causal_kernel", C + "tc_causal.cu") if causal else ("tc_output_kernel", C + "tc_output.cu")}
+
+
+def kernel_table(w: wl.Workload, info, fmap: str, causal: bool, avg_phase: dict, peaks, sm_mhz=None):
+    """One row per kernel of the forward: its average launch time and, for the
+    kernels that do the method's work, the method's own bytes or FLOPs per
+    launch (read K and V for the summaries; read Q and write O for the output
+    step, plus K and V for the causal one; the mixing's 2 M^2 d^2 FLOPs per
+    unit; Q, K, V, O for the fused launch) against the measured peak, and the
+    ncu DRAM bytes per launch where the committed table has them for the
+    current sources.  Preparation and exponent folding move only
+    intermediates: their time is reported, no fraction."""
+    import token_level_head_phi_gb300.binding as mb
+    hbm, tf_burst, tf_sust, peak_kind = peaks
     el = 2 if w.dtype == "bf16" else 4
-    U, N, d, M = w.units, w.n_tokens, w.head_dim, w.n_blocks
-    R = d * d + 2 * d
-    rows = M * info.summary_splits
-    io = U * N * d * el
-    if variant == mb.VARIANT_SIMT:
-        stack = U * rows * R * 4
-        mixed_w = mixed_r = U * M * R * 4
-        mc = 4 * M * M
-    else:
-        mala = w.norm == "mala"
-        stack = U * rows * R * 2 * (2 if mala else 1)
-        mixed_w = U * M * (R * 2 + (R if mala else 2 * d) * 2)
-        mixed_r = U * M * (d * d * 2 * (2 if mala else 1) + 2 * d * 2 * 2)
-        mc = 4 * M * M
-    if variant == mb.VARIANT_FUSED:
-        # prep: Mc in, its copies out; the fused kernel: Q, K, V in and O out
-        # (the stack and mixed rings stay in L2)
-        mcq = M * ((M * info.summary_splits + 7) // 8 * 8) * 2
-        return {"summary": mc + 3 * mcq, "mix": 0, "output": 4 * io}
-    return {"summary": 2 * io + stack, "mix": stack + mixed_w + mc, "output": io + mixed_r + io}
+    io = w.units * w.n_tokens * w.head_dim * el
+    mix_flops = 2 * w.units * w.n_blocks ** 2 * w.head_dim ** 2
+    kernels = phase_kernels(w, info, fmap, causal)
+    tt = traffic_table()
+    rows = {}
+    for ph, kern in kernels.items():
+        if kern is None:
+            continue
+        name, src = kern
+        ms = avg_phase.get(ph, 0.0)
+        row = {"kernel": name, "avg_launch_ms": ms}
+        if ph == "summary":
+            row.update(bound="hbm", algorithmic_bytes_per_launch=2 * io)
+        elif ph == "output":
+            if name == "tc_fused_kernel":
+                nb = 4 * io + 4 * w.n_blocks ** 2   # the whole forward in one launch
+            else:
+                nb = (4 if causal else 2) * io      # Q in, O out (the causal step also reads K, V)
+            row.update(bound="hbm", algorithmic_bytes_per_launch=nb)
+        elif ph == "mix":
+            row.update(bound="tensor" if info.variant != mb.VARIANT_SIMT else "alu", flops_per_launch=mix_flops)
+        else:
+            row.update(bound="overhead")
+        if ms > 0 and row["bound"] == "hbm":
+            row["achieved"] = row["algorithmic_bytes_per_launch"] / (ms / 1e3) / 1e9
+            row.update(peak=hbm, unit="GB/s", peak_source=peak_kind)
+        elif ms > 0 and row["bound"] == "tensor":
+            row["achieved"] = mix_flops / (ms / 1e3) / 1e12
+            row.update(peak=tf_burst, unit="TFLOP/s", peak_source=peak_kind + " bf16 dense burst (fp16 runs at the same rate)")
+        elif ms > 0 and row["bound"] == "alu":
+            mhz = sm_mhz or 2070.0
+            peak = SM_COUNT * FP32_LANES_PER_SM * 2 * mhz * 1e6 / 1e12
+            row["achieved"] = mix_flops / (ms / 1e3) / 1e12
+            row.update(peak=peak, unit="TFLOP/s",
+                       peak_source="fp32 FMA lanes x 2 x max SM clock: %d x %d x 2 x %.0f MHz" % (SM_COUNT, FP32_LANES_PER_SM, mhz))
+        if "achieved" in row:
+            row["frac"] = row["achieved"] / row["peak"]
+        t = tt.get((name, w.name))
+        row["traffic"] = t[0] if (t and t[1] == source_hash(src)) else None
+        if row["traffic"] is not None and row.get("algorithmic_bytes_per_launch"):
+            row["traffic_over_algorithmic"] = row["traffic"] / row["algorithmic_bytes_per_launch"]
+        rows[ph] = row
+    return rows
 
 
 def traffic_table():
@@ -203,7 +258,7 @@ def traffic_table():
 KERNEL_HEADERS = ["token_level_head_phi_gb300/csrc/tc_common.cuh", "token_level_head_phi_gb300/csrc/common.cuh",
                   "token_level_head_phi_gb300/csrc/plan.h", "token_level_head_phi_gb300/csrc/tc_host.h",
                   "token_level_head_phi_gb300/csrc/tc_summary.cuh", "token_level_head_phi_gb300/csrc/tc_mix.cuh",
-                  "token_level_head_phi_gb300/csrc/tc_output.cuh"]
+                  "token_level_head_phi_gb300/csrc/tc_mixt.cuh", "token_level_head_phi_gb300/csrc/tc_output.cuh"]
 
 
 def source_hash(relpath: str) -> str:
@@ -215,19 +270,7 @@ def source_hash(relpath: str) -> str:
     return h.hexdigest()[:12]
 
 
-PHASE_KERNEL = {  # variant -> phase -> (kernel name in ncu, source file)
-    1: {"summary": ("simt_summary_kernel", "token_level_head_phi_gb300/csrc/simt.cu"),
-        "mix": ("simt_mix_kernel", "token_level_head_phi_gb300/csrc/simt.cu"),
-        "output": ("simt_output_kernel", "token_level_head_phi_gb300/csrc/simt.cu")},
-    2: {"summary": ("tc_summary_kernel", "token_level_head_phi_gb300/csrc/tc_summary.cu"),
-        "mix": ("tc_mix_kernel", "token_level_head_phi_gb300/csrc/tc_mix.cu"),
-        "output": ("tc_output_kernel", "token_level_head_phi_gb300/csrc/tc_output.cu")},
-    3: {"summary": ("tc_prep_kernel", "token_level_head_phi_gb300/csrc/tc_mix.cu"),
-        "output": ("tc_fused_kernel", "token_level_head_phi_gb300/csrc/tc_fused.cu")},
-}
-
-
-def run_mine(args, w: wl.Workload, world: int, rank: int, local: int, dist):
+def run_mine(args, w: wl.Workload, world: int, rank: int, local: int, dist, sample_clocks: bool = True):
     import torch
     import token_level_head_phi_gb300.binding as mb
     from token_level_head_phi_gb300 import build as mbuild
@@ -291,7 +334,7 @@ def run_mine(args, w: wl.Workload, world: int, rank: int, local: int, dist):
     K = args.steps
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    sampler = ClockSampler(local) if rank == 0 else None
+    sampler = ClockSampler(local) if rank == 0 and sample_clocks else None
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
@@ -338,25 +381,19 @@ def run_mine(args, w: wl.Workload, world: int, rank: int, local: int, dist):
     max_ms, value = job_throughput(total_ms, K, w.units * w.n_tokens, world, dist, dev)
     ms_per_step = max_ms / K
 
-    hbm, tf_burst, tf_sust, peak_kind = load_peaks()
-    pbytes = phase_bytes(w, info, info.variant)
-    if args.causal:
-        # the causal output step also reads K and V (the in-block prefix)
-        pbytes["output"] += 2 * q.numel() * q.element_size()
+    peaks = load_peaks()
+    hbm, tf_burst, tf_sust, peak_kind = peaks
     avg_phase = {ph: statistics.mean(v) for ph, v in phase_ms.items()}
-    dom = max(avg_phase, key=avg_phase.get)
-    achieved = pbytes[dom] / (avg_phase[dom] / 1e3) / 1e9
-    kname, ksrc = PHASE_KERNEL.get(info.variant, {}).get(dom, (dom, None))
-    if args.causal and dom == "output":
-        kname, ksrc = (("tc_causal_kernel", "token_level_head_phi_gb300/csrc/tc_causal.cu") if info.variant == 2 else
-                       ("causal_output_kernel", "token_level_head_phi_gb300/csrc/simt_causal.cu"))
-    traffic = None
-    tt = traffic_table().get((kname, w.name))
-    if tt and ksrc and tt[1] == source_hash(ksrc):
-        traffic = tt[0]
+    kernels = kernel_table(w, info, args.feature_map, bool(args.causal), avg_phase, peaks,
+                           (clocks or {}).get("sm_max_mhz"))
+    # the dominant kernel: the longest of those that do the method's work
+    work = {ph: r for ph, r in kernels.items() if r["bound"] != "overhead" and "frac" in r}
+    dom = max(work, key=lambda ph: work[ph]["avg_launch_ms"])
+    roof = dict(work[dom], phase=dom)
     roof_bytes = wl.roofline_bytes(w)
     roof_flops = wl.roofline_flops(w)
     t_hbm = roof_bytes / (hbm * 1e9)
+    # a whole step is a long run of kernels: the sustained tensor peak
     t_tc = roof_flops / (tf_sust * 1e12)
     t_roof = max(t_hbm, t_tc)
 
@@ -366,21 +403,62 @@ def run_mine(args, w: wl.Workload, world: int, rank: int, local: int, dist):
         "dtype": w.dtype, "data": "synthetic (seeded normals, locality-biased Mc; no dataset, no weights)",
         "config": dict(wl.describe(w), feature_map=args.feature_map, causal=bool(args.causal), layout=args.layout,
                        mc_per_head=bool(args.mc_per_head),
-                       variant=mb.mhla_plan(p).variant,
+                       variant=info.variant,
                        variant_name={1: "simt", 2: "multipass", 3: "fused"}.get(info.variant, str(info.variant)),
                        l2="no flush: inputs exceed L2" if flush is None else "L2 flushed (256 MB write) between steps, outside per-step events",
                        parallelism=f"replicas{world}" if world > 1 else "single GPU"),
-        "roofline": {"bound": "hbm", "kernel": kname, "phase": dom, "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                     "frac": achieved / hbm, "traffic": traffic, "peak_source": peak_kind,
-                     "algorithmic_bytes_per_launch": pbytes[dom], "avg_launch_ms": avg_phase[dom]},
+        "roofline": roof,
+        "kernels": kernels,
         "path_roofline": {"bytes": roof_bytes, "flops": roof_flops, "t_hbm_us": t_hbm * 1e6, "t_tc_us": t_tc * 1e6,
                           "bound": "hbm" if t_hbm >= t_tc else "tensor", "frac": t_roof / (ms_per_step / 1e3),
                           "peak_hbm_gbs": hbm, "peak_bf16_tflops_sustained": tf_sust, "peak_source": peak_kind},
         "phase_ms": avg_phase,
+        "phase_note": "per-kernel times from a separate run with events between the kernels (which serialises "
+                      "the launches the timed steps overlap)",
         "gpu_launches": info.kernels_per_call * K,
         "clocks": clocks,
     }
     return result, (q, k, v, mc, out, p, info, stream)
+
+
+# The other configurations of the default run: (label, workload).  The
+# video-shaped workload is the headline line itself.
+PER_CONFIG = [("C0 tiny fp32", "tiny_f32"), ("C1 DeiT-T-shaped", "deit_t"), ("C2 high-res image", "image_64x64"),
+              ("C4 1D 32k divisive", "seq_32k"), ("C4 1D 32k MALA", "seq_32k_mala"),
+              ("C4 1D 32k M=1 divisive", "seq_32k_m1"), ("C4 1D 32k M=1 MALA", "seq_32k_m1_mala"),
+              ("Wan-shaped 3D (21x30x50, 300-token blocks)", "wan_21x30x50")]
+
+
+def run_per_config(args, world, rank, local, dist):
+    """Each other configuration with its own warm-up and timed steps (an L2
+    flush between steps where its inputs fit in L2), as the headline: step
+    time, tokens*heads/s, whole-path roofline fraction and the per-kernel
+    table with the dominant kernel."""
+    import torch
+    out = {}
+    for label, name in PER_CONFIG:
+        w = wl.WORKLOADS[name]
+        if args.variant in ("multipass", "fused") and (w.dtype != "bf16" or w.head_dim != 64):
+            continue  # the tensor-core launches take bf16 with d = 64
+        sub = argparse.Namespace(**vars(args))
+        sub.steps = max(10, min(args.steps, 30))
+        sub.causal = False
+        r, st = run_mine(sub, w, world, rank, local, dist, sample_clocks=False)
+        del st
+        torch.cuda.empty_cache()
+        out[name] = {
+            "label": label, "ms_per_step": r["ms_per_step"], "value": r["value"], "unit": UNIT,
+            "path_roofline_frac": r["path_roofline"]["frac"], "path_bound": r["path_roofline"]["bound"],
+            "t_roofline_us": max(r["path_roofline"]["t_hbm_us"], r["path_roofline"]["t_tc_us"]),
+            "dominant": {k: r["roofline"].get(k) for k in ("kernel", "phase", "bound", "frac", "achieved", "unit",
+                                                           "avg_launch_ms")},
+            "kernels": {ph: {k: v for k, v in row.items() if k in ("kernel", "avg_launch_ms", "bound", "frac",
+                                                                   "traffic_over_algorithmic")}
+                        for ph, row in r["kernels"].items()},
+            "variant_name": r["config"]["variant_name"], "dtype": w.dtype, "norm": w.norm,
+            "steps": sub.steps, "warmup": sub.warmup, "l2": r["config"]["l2"],
+        }
+    return out
 
 
 def run_e2e(w: wl.Workload, state, steps: int):
@@ -529,7 +607,7 @@ def run_backward(args, w: wl.Workload, world: int, rank: int, local: int, dist):
     K = args.steps
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    sampler = ClockSampler(local) if rank == 0 else None
+    sampler = ClockSampler(local) if rank == 0 and sample_clocks else None
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
@@ -717,7 +795,8 @@ def main():
     ap.add_argument("--workload", default=wl.BENCH_WORKLOAD, choices=sorted(wl.WORKLOADS))
     ap.add_argument("--variant", default="auto", choices=["auto", "simt", "multipass", "fused"])
     ap.add_argument("--impl", default="mine", choices=["mine", "reference"])
-    ap.add_argument("--all-workloads", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the other configurations (listed under per_config by default)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--pass", dest="pass_", default="forward", choices=["forward", "backward"])
@@ -756,20 +835,8 @@ def main():
     result["e2e"] = run_e2e(w, state, args.e2e_steps)
     del state
     torch.cuda.empty_cache()
-    if args.all_workloads:
-        extra = {}
-        for name in sorted(wl.WORKLOADS):
-            ww = wl.WORKLOADS[name]
-            if name == w.name or (ww.head_dim != 64 or ww.dtype != "bf16") and args.variant in ("multipass", "fused"):
-                continue
-            sub = argparse.Namespace(**vars(args))
-            sub.steps = max(10, min(args.steps, 50))
-            r, st = run_mine(sub, wl.WORKLOADS[name], world, rank, local, dist)
-            del st
-            torch.cuda.empty_cache()
-            extra[name] = {k: r[k] for k in ("value", "ms_per_step", "phase_ms", "path_roofline", "roofline")}
-            extra[name]["config"] = r["config"]
-        result["workloads"] = extra
+    if not args.no_per_config and args.workload == wl.BENCH_WORKLOAD:
+        result["per_config"] = run_per_config(args, world, rank, local, dist)
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(w, fmap=args.feature_map)
     if rank == 0:

@@ -244,6 +244,8 @@ mhla_status make_plan(const mhla_params* prm, Plan* p, int split_units = 0) {
       off = align_up(off + 2 * 2 * (size_t)p->slots * p->M * p->Qp);
       p->off_sinfo = off;
       off = align_up(off + 16 * (size_t)p->slots * p->M);
+      p->off_mcw = off;
+      off = align_up(off + 4 * (size_t)p->M * p->mc_heads * p->Qp);
       p->kernels = 5;
     }
     if (variant == MHLA_VARIANT_FUSED) {
@@ -303,6 +305,7 @@ mhla_status run_plan(const Plan& plan, const void* q, const void* k, const void*
     b.rexp = p.f16_mix ? reinterpret_cast<int2*>(ws + p.off_rexp) : nullptr;
     b.mcx = p.f16_mix ? reinterpret_cast<__half*>(ws + p.off_mcx) : nullptr;
     b.sinfo = p.f16_mix ? reinterpret_cast<float4*>(ws + p.off_sinfo) : nullptr;
+    b.mcw = p.f16_mix ? reinterpret_cast<uint32_t*>(ws + p.off_mcw) : nullptr;
     b.Qp = p.Qp;
     b.f16 = p.f16_mix != 0;
     b.slots = p.slots;
@@ -341,7 +344,7 @@ mhla_status run_plan(const Plan& plan, const void* q, const void* k, const void*
     record_event(1, s);
     if ((e = launch_tc_summary(p, p.chunk, k, v, b, s)) != 0) return cuda_fail((cudaError_t)e);
     record_event(2, s);
-    if (b.f16 && (e = launch_tc_scale(p, mc, b, s)) != 0) return cuda_fail((cudaError_t)e);
+    if (b.f16 && (e = launch_tc_scale(p, b, s)) != 0) return cuda_fail((cudaError_t)e);
     record_event(3, s);
     if ((e = launch_tc_mix(p, b, s)) != 0) return cuda_fail((cudaError_t)e);
     record_event(4, s);
@@ -558,6 +561,7 @@ int run_backward(const Plan& plan, const BwdLayout& lay, const void* q, const vo
     b.rexp = nullptr;
     b.mcx = nullptr;
     b.sinfo = nullptr;
+    b.mcw = nullptr;
     b.Qp = p.Qp;
     b.f16 = false;
     b.slots = p.BH;

@@ -92,7 +92,7 @@ struct Plan {
   size_t off_mc_f16, off_mc_scale, off_mc_hi, off_mc_lo, off_blkinfo;
   // fp16 path: per-record exponents, per-head fp16 Mc copies, per-(head,
   // block) output scales
-  size_t off_rexp, off_mcx, off_sinfo;
+  size_t off_rexp, off_mcx, off_sinfo, off_mcw;
   int Qp;
   int slots;          // heads the stack and mixed buffers hold (BH, or the fused ring)
   size_t off_flow;    // fused launch: [3][BH] progress counters

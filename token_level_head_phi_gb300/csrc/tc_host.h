@@ -67,6 +67,9 @@ struct TcBuffers {
   float* rowsum;             // [M] sum_b (hi + lo)(Mc[i][b])
   float4* blkinfo;           // [M] {1, n~_i, 0, 0} (split path)
   int2* rexp;                // fp16 path: [slots][Q] record exponents {eS, eZ}
+  uint32_t* mcw;             // fp16 path: [M][Qp] Mc[i][q / splits] as {fp16 bits of its mantissa in
+                             //            [1, 2) (with sign; 0 for a zero entry), int16 exponent x} with
+                             //            Mc = mantissa 2^(x - 1); x = -16384 marks a zero entry
   __half* mcx;               // fp16 path: [slots][2][M][Qp] Mc[i][q / splits] 2^(eS[q] - ES[i]) (part 0),
                              //            the same with eZ, EZ (part 1)
   float4* sinfo;             // fp16 path: [slots][M] {output scale, 0, 0, 0}
@@ -109,7 +112,7 @@ int launch_tc_summary(const Plan& p, const ChunkShape& c, const void* k, const v
                       cudaStream_t s);
 // fp16 path, between the summaries and the mixing: the per-head Mc copies
 // with the record exponents folded in, and the output scales.
-int launch_tc_scale(const Plan& p, const float* mc, const TcBuffers& b, cudaStream_t s);
+int launch_tc_scale(const Plan& p, const TcBuffers& b, cudaStream_t s);
 int launch_tc_mix(const Plan& p, const TcBuffers& b, cudaStream_t s);
 int launch_tc_output(const Plan& p, const ChunkShape& c, const void* q, const TcBuffers& b, void* out,
                      cudaStream_t s);

@@ -21,18 +21,38 @@ using mx::kSmemBytes;
 using mx::kStageArea;
 using mx::kThreads;
 
+// One entry of Mc as the fp16 path's exponent-folding kernel reads it:
+// x = m == 0 ? -16384 : the exponent with |m| = f 2^x, f in [0.5, 1), and the
+// fp16 bits of the mantissa 2f in [1, 2) with m's sign (a mantissa that rounds
+// up to 2 becomes 1 with x + 1), so that m = mantissa 2^(x - 1) up to the
+// fp16 rounding of the mantissa.  (-16384 keeps x + e far below any real
+// exponent sum without leaving the 16-bit range.)
+__device__ __forceinline__ uint32_t mc_word(float m) {
+  if (m == 0.f) return 0xC0000000u;
+  int x = 0;
+  const float f = frexpf(fabsf(m), &x);
+  uint32_t h = __half_as_ushort(__float2half_rn(2.f * f));
+  if (h == 0x4000u) {  // 2.0
+    h = 0x3C00u;       // 1.0
+    ++x;
+  }
+  if (m < 0.f) h |= 0x8000u;
+  return h | ((uint32_t)(x & 0xFFFF) << 16);
+}
+
 // Also zeroes the progress counters of a fused launch.
-// One warp per row i of Mc: the fp16 copy scaled by 2^-e_i (largest entry of
-// the row in [0.5, 1]), the bf16 high and low parts, the row scale 2^e_i, the
-// row sum of hi + lo in float32 and the block record {1, n~_i} of the split
-// path's output step.  Columns are expanded over pieces.  `rows` rows of
-// length M: every row of every mixing matrix (one per head when each head has
-// its own).
+// One warp per row i of Mc.  Split path: the bf16 high and low parts (and an
+// fp16 copy scaled by 2^-e_i, largest entry of the row in [0.5, 1]), the row
+// scale 2^e_i, the row sum of hi + lo in float32 and the block record
+// {1, n~_i} of the output step.  fp16 path: the mantissa-and-exponent words
+// mcw instead of the copies.  Columns are expanded over pieces.  `rows` rows
+// of length M: every row of every mixing matrix (one per head when each head
+// has its own).
 __global__ void tc_prep_kernel(int rows, int M, int splits, int Q, int Qp, const float* __restrict__ mc,
                                __half* __restrict__ mc_f16, float* __restrict__ mc_scale,
                                __nv_bfloat16* __restrict__ mc_hi, __nv_bfloat16* __restrict__ mc_lo,
-                               float* __restrict__ rowsum, float4* __restrict__ blkinfo, float nb,
-                               unsigned int* __restrict__ flow, int nflow) {
+                               uint32_t* __restrict__ mcw, float* __restrict__ rowsum,
+                               float4* __restrict__ blkinfo, float nb, unsigned int* __restrict__ flow, int nflow) {
   // the previous call's kernels may still read what this one writes
   pdl_wait();
   pdl_launch_dependents();
@@ -58,6 +78,10 @@ __global__ void tc_prep_kernel(int rows, int M, int splits, int Q, int Qp, const
   const float down = ldexpf(1.f, -ex);
   for (int q = lane; q < Qp; q += 32) {
     const float x = q < Q ? row[q / splits] : 0.f;
+    if (mcw) {
+      mcw[(size_t)i * Qp + q] = mc_word(x);
+      continue;
+    }
     const __nv_bfloat16 h = __float2bfloat16_rn(x);
     mc_hi[(size_t)i * Qp + q] = h;
     mc_lo[(size_t)i * Qp + q] = __float2bfloat16_rn(x - __bfloat162float(h));
@@ -148,8 +172,8 @@ int launch_tc_prep(const Plan& p, const float* mc, const TcBuffers& b, cudaStrea
   const int rows = p.M * p.mc_heads;
   const int blocks = (rows * 32 + threads - 1) / threads;
   return launch_pdl(tc_prep_kernel, dim3(blocks), dim3(threads), 0, s, rows, p.M, p.splits, p.M * p.splits, b.Qp, mc,
-                    b.mc_f16, b.mc_scale, b.mc_hi, b.mc_lo, b.rowsum, b.blkinfo, (float)p.nb, b.flow,
-                    b.flow ? 3 * p.BH : 0);
+                    b.mc_f16, b.mc_scale, b.mc_hi, b.mc_lo, b.f16 ? b.mcw : nullptr, b.rowsum, b.blkinfo,
+                    (float)p.nb, b.flow, b.flow ? 3 * p.BH : 0);
 }
 
 int build_mix_args(const Plan& p, const TcBuffers& b, int slots, mx::MixArgs* out) {

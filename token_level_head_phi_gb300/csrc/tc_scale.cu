@@ -30,67 +30,120 @@ namespace {
 
 using namespace tc;
 
-constexpr int kRowsPerCta = 8;  // one warp per query block
+constexpr int kWarps = 8;      // one query block (row) per warp
+constexpr int kQChunk = 4096;  // record exponents staged in shared memory at a time (16 KB)
+constexpr uint32_t kZeroWord = 0xC0000000u;  // Mc word of a zero entry (exponent -16384)
 
-// Exponent x of a float m != 0 with |m| = f 2^x, f in [0.5, 1) (read from
-// the exponent field; a subnormal m counts as 2^-126, an over-estimate that
-// only makes its row's entries smaller).
-__device__ __forceinline__ int frexp_exponent(float m) {
-  return (int)((__float_as_uint(m) >> 23) & 0xFFu) - 126;
+// fp16 bits of mantissa 2^(x + e - E - 1) for Mc word w (see mc_word in
+// tc_mix.cu): the mantissa's bits under a new exponent while the result is a
+// normal fp16 number; below that, the subnormal with the mantissa shifted
+// right and rounded to nearest even (2^-24 steps; a result that rounds up to
+// 2^-14 lands on the smallest normal number, as the encoding continues there).
+__device__ __forceinline__ uint32_t place(uint32_t w, int e, int E) {
+  if (w == kZeroWord) return 0u;
+  const int x = (int)(int16_t)(w >> 16);
+  const uint32_t h = w & 0xFFFFu, sign = h & 0x8000u;
+  const int biased = x + e - E + 14;
+  if (biased >= 1) return sign | ((uint32_t)biased << 10) | (h & 0x3FFu);
+  const int sh = 1 - biased;
+  if (sh > 11) return sign;
+  const uint32_t m11 = (h & 0x3FFu) | 0x400u;
+  uint32_t q = m11 >> sh;
+  const uint32_t rem = m11 & ((1u << sh) - 1u), half = 1u << (sh - 1);
+  q += (rem > half || (rem == half && (q & 1u))) ? 1u : 0u;
+  return sign | q;
 }
 
-// Grid (ceil(M / kRowsPerCta), slots); warp w of CTA (x, u) builds row
-// i = x * kRowsPerCta + w of head u's two Mc copies and its output scale.
-__global__ void __launch_bounds__(32 * kRowsPerCta) tc_scale_kernel(const Plan p, int Q, int Qp, int splits,
-                                                                    const float* __restrict__ mc,
-                                                                    const int2* __restrict__ rexp,
-                                                                    __half* __restrict__ mcx,
-                                                                    float4* __restrict__ sinfo) {
+// Both parts of one entry: fp16 bits for the S copy (low half) and the z
+// copy (high half).  e2 packs the record's {eS, eZ} and base2 {14 - ES,
+// 14 - EZ} as 16-bit lanes; the biased exponents x + e - E + 14 of both parts
+// come from two packed adds, and while both are positive (they are at most
+// 14: x + e <= E) the result is the
+// mantissa bits with those exponents placed above them.
+__device__ __forceinline__ uint32_t place2(uint32_t w, uint32_t e2, uint32_t base2, int es, int ez) {
+  if (w == kZeroWord) return 0u;
+  const uint32_t xx = __byte_perm(w, 0u, 0x3232);               // x in both lanes
+  const uint32_t t = __vadd2(__vadd2(e2, xx), base2);           // biased exponents
+  if (__vcmpgts2(t, 0u) == 0xFFFFFFFFu)
+    return (__byte_perm(w, 0u, 0x1010) & 0x83FF83FFu) | (t << 10);
+  return place(w, (int)(int16_t)(e2 & 0xFFFFu), es) | (place(w, (int)(int16_t)(e2 >> 16), ez) << 16);
+}
+
+// Grid (ceil(M / kWarps), slots): warp w of CTA (x, u) builds row
+// i = x * kWarps + w of head u's two Mc copies and its output scale.  The
+// head's record exponents pass through shared memory in chunks of kQChunk,
+// packed {eS, eZ} as 16-bit lanes; each lane reads four consecutive Mc words
+// and four packed exponents (16 bytes each) at a time.
+__global__ void __launch_bounds__(32 * kWarps) tc_scale_kernel(const Plan p, int Q, int Qp,
+                                                               const uint32_t* __restrict__ mcw,
+                                                               const int2* __restrict__ rexp,
+                                                               __half* __restrict__ mcx,
+                                                               float4* __restrict__ sinfo) {
+  __shared__ __align__(16) uint32_t ex_s[kQChunk];
   // the record exponents come from the summary kernel
   pdl_wait();
   pdl_launch_dependents();
   const int lane = threadIdx.x % 32;
   const int u = blockIdx.y;
-  const int i = blockIdx.x * kRowsPerCta + threadIdx.x / 32;
-  if (i >= p.M) return;
-  const float* row = mc + ((size_t)mc_index(p, u) * p.M + i) * p.M;
+  const int i = blockIdx.x * kWarps + threadIdx.x / 32;
+  const bool live = i < p.M;
+  const uint4* row = reinterpret_cast<const uint4*>(mcw + ((size_t)mc_index(p, u) * p.M + (live ? i : 0)) * Qp);
   const int2* ex = rexp + (size_t)u * Q;
-  int es = INT_MIN, ez = INT_MIN;
-  for (int q = lane; q < Q; q += 32) {
-    const float m = row[splits == 1 ? q : q / splits];
-    if (m != 0.f) {
-      const int xm = frexp_exponent(m);
-      const int2 e = ex[q];
-      es = max(es, e.x + xm);
-      ez = max(ez, e.y + xm);
+  auto stage = [&](int c0, int n) {
+    for (int t = threadIdx.x; t < n; t += blockDim.x) {
+      const int2 e = c0 + t < Q ? ex[c0 + t] : make_int2(0, 0);
+      ex_s[t] = ((uint32_t)e.x & 0xFFFFu) | ((uint32_t)e.y << 16);
     }
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    es = max(es, __shfl_xor_sync(0xffffffffu, es, o));
-    ez = max(ez, __shfl_xor_sync(0xffffffffu, ez, o));
-  }
-  // an all-zero row mixes nothing: any exponent (its entries stay zero)
-  if (es == INT_MIN) es = 0;
-  if (ez == INT_MIN) ez = 0;
-  __half2* ds = reinterpret_cast<__half2*>(mcx + (((size_t)u * 2 + 0) * p.M + i) * Qp);
-  __half2* dz = reinterpret_cast<__half2*>(mcx + (((size_t)u * 2 + 1) * p.M + i) * Qp);
-  for (int q2 = lane; 2 * q2 < Qp; q2 += 32) {
-    float s[2] = {0.f, 0.f}, z[2] = {0.f, 0.f};
-#pragma unroll
-    for (int t = 0; t < 2; ++t) {
-      const int q = 2 * q2 + t;
-      if (q < Q) {
-        const float m = row[splits == 1 ? q : q / splits];
-        const int2 e = ex[q];
-        s[t] = ldexpf(m, e.x - es);
-        z[t] = ldexpf(m, e.y - ez);
+  };
+  // row exponents: the largest eS[q] + x(Mc[i][b(q)]) (and eZ) over nonzero
+  // weights, as signed 16-bit lanes (a zero weight adds -16384)
+  uint32_t mx = 0x80008000u;
+  for (int c0 = 0; c0 < Qp; c0 += kQChunk) {
+    const int n = min(kQChunk, Qp - c0);
+    __syncthreads();
+    stage(c0, n);
+    __syncthreads();
+    if (live) {
+#pragma unroll 4
+      for (int q = 4 * lane; q < n; q += 128) {
+        const uint4 w4 = __ldg(row + (c0 + q) / 4);
+        const uint4 e4 = *reinterpret_cast<const uint4*>(ex_s + q);
+        mx = __vmaxs2(mx, __vadd2(e4.x, __byte_perm(w4.x, 0u, 0x3232)));
+        mx = __vmaxs2(mx, __vadd2(e4.y, __byte_perm(w4.y, 0u, 0x3232)));
+        mx = __vmaxs2(mx, __vadd2(e4.z, __byte_perm(w4.z, 0u, 0x3232)));
+        mx = __vmaxs2(mx, __vadd2(e4.w, __byte_perm(w4.w, 0u, 0x3232)));
       }
     }
-    ds[q2] = __floats2half2_rn(s[0], s[1]);
-    dz[q2] = __floats2half2_rn(z[0], z[1]);
   }
-  if (lane == 0) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = __vmaxs2(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  int es = (int)(int16_t)(mx & 0xFFFFu), ez = (int)(int16_t)(mx >> 16);
+  // an all-zero row mixes nothing: any exponent (its entries stay zero)
+  if (es < -8192) es = 0;
+  if (ez < -8192) ez = 0;
+  const uint32_t base2 = ((uint32_t)(14 - es) & 0xFFFFu) | ((uint32_t)(14 - ez) << 16);
+  uint2* ds = reinterpret_cast<uint2*>(mcx + (((size_t)u * 2 + 0) * p.M + i) * Qp);
+  uint2* dz = reinterpret_cast<uint2*>(mcx + (((size_t)u * 2 + 1) * p.M + i) * Qp);
+  for (int c0 = 0; c0 < Qp; c0 += kQChunk) {
+    const int n = min(kQChunk, Qp - c0);
+    if (c0 > 0) {
+      __syncthreads();
+      stage(c0, n);
+    }
+    __syncthreads();
+    if (live) {
+#pragma unroll 4
+      for (int q = 4 * lane; q < n; q += 128) {
+        const uint4 w4 = __ldg(row + (c0 + q) / 4);
+        const uint4 e4 = *reinterpret_cast<const uint4*>(ex_s + q);
+        const uint32_t r0 = place2(w4.x, e4.x, base2, es, ez), r1 = place2(w4.y, e4.y, base2, es, ez);
+        const uint32_t r2 = place2(w4.z, e4.z, base2, es, ez), r3 = place2(w4.w, e4.w, base2, es, ez);
+        ds[(c0 + q) / 4] = make_uint2(__byte_perm(r0, r1, 0x5410), __byte_perm(r2, r3, 0x5410));
+        dz[(c0 + q) / 4] = make_uint2(__byte_perm(r0, r1, 0x7632), __byte_perm(r2, r3, 0x7632));
+      }
+    }
+  }
+  if (live && lane == 0) {
     const float scale = p.norm == MHLA_NORM_DIVISIVE ? exp2f((float)(es - ez)) : exp2f((float)es);
     sinfo[(size_t)u * p.M + i] = make_float4(scale, 0.f, 0.f, 0.f);
   }
@@ -98,9 +151,9 @@ __global__ void __launch_bounds__(32 * kRowsPerCta) tc_scale_kernel(const Plan p
 
 }  // namespace
 
-int launch_tc_scale(const Plan& p, const float* mc, const TcBuffers& b, cudaStream_t s) {
-  const dim3 grid((unsigned)((p.M + kRowsPerCta - 1) / kRowsPerCta), (unsigned)b.slots);
-  return launch_pdl(tc_scale_kernel, grid, dim3(32 * kRowsPerCta), 0, s, p, p.M * p.splits, b.Qp, p.splits, mc,
+int launch_tc_scale(const Plan& p, const TcBuffers& b, cudaStream_t s) {
+  const dim3 grid((unsigned)((p.M + kWarps - 1) / kWarps), (unsigned)b.slots);
+  return launch_pdl(tc_scale_kernel, grid, dim3(32 * kWarps), 0, s, p, p.M * p.splits, b.Qp, (const uint32_t*)b.mcw,
                     (const int2*)b.rexp, b.mcx, b.sinfo);
 }
 

@@ -123,17 +123,32 @@ __device__ __forceinline__ void phi_chunk(uint4& x, uint4& lo, int fmap) {
   }
 }
 
-// Exponent e of an fp16 record part whose largest magnitude is `amax`: the
-// part is stored times 2^-e, which puts that entry in [2^14, 2^15) -- every
-// entry down to 2^-29 of it stays a normal fp16 number, and no rounding can
-// reach the fp16 limit 65504.  Read from the float's exponent field
-// (amax in [2^k, 2^(k+1)) gives e = k - 14); clamped so that 2^-e is a normal
-// float (a part whose largest entry is below 2^-106 counts as zero).  An
-// infinite entry stays infinite, NaN stays NaN.
-__device__ __forceinline__ int record_exponent(float amax) {
-  const int e = (int)((__float_as_uint(amax) >> 23) & 0xFFu) - 141;
+// Exponent e of an fp16 record part whose largest magnitude has the float
+// bits `amax_bits` (sign cleared): the part is stored times 2^-e, which puts
+// that entry in [2^14, 2^15) -- every entry down to 2^-29 of it stays a normal
+// fp16 number, and no rounding can reach the fp16 limit 65504.  Read from the
+// exponent field (amax in [2^k, 2^(k+1)) gives e = k - 14); clamped so that
+// 2^-e is a normal float (a part whose largest entry is below 2^-106 counts
+// as zero).  An infinite entry stays infinite, NaN stays NaN.
+__device__ __forceinline__ int record_exponent(uint32_t amax_bits) {
+  const int e = (int)((amax_bits >> 23) & 0xFFu) - 141;
   return min(max(e, -120), 113);
 }
+
+// Largest |v[j]| of 32 floats as float bits (for non-negative floats the
+// bit patterns order as the values do): a tree of maxima, five deep (|x| is
+// an operand modifier of the max, not an instruction).
+__device__ __forceinline__ uint32_t abs_max_bits32(const float (&v)[32]) {
+  float m[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) m[j] = fmaxf(fabsf(v[2 * j]), fabsf(v[2 * j + 1]));
+#pragma unroll
+  for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+    for (int j = 0; j < w; ++j) m[j] = fmaxf(m[j], m[j + w]);
+  return __float_as_uint(m[0]);
+}
+
 
 // 2^-e as a float, for e in [-120, 113].
 __device__ __forceinline__ float pow2_neg(int e) { return __uint_as_float((uint32_t)(127 - e) << 23); }
@@ -182,8 +197,8 @@ __device__ __forceinline__ void summary_body(const SummaryArgs& a, const Plan& p
   auto ring_phase = [&](int j, long long k) { return (uint32_t)((k / ring_len(j)) & 1); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gb + L::kBars + 8 * (3 * kStages + 4));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gb + L::kBars + 8 * (3 * kStages + 4) + 8);
-  // epilogue: per-warp maxima of the fp16 record parts (8 floats)
-  float* red = reinterpret_cast<float*>(gb + L::kBars + 192);
+  // epilogue: per-warp maxima of the fp16 record parts (float bits)
+  uint32_t* red = reinterpret_cast<uint32_t*>(gb + L::kBars + 192);
   static_assert(8 * (3 * kStages + 4) + 12 <= 192, "barrier area");
 
   const int warp = threadIdx.x / 32;
@@ -392,21 +407,12 @@ __device__ __forceinline__ void summary_body(const SummaryArgs& a, const Plan& p
 
       uint8_t* st_hi = gb + L::kStaging + (it % L::kStagingBufs) * L::kStagingStride;
       uint8_t* st_lo = st_hi + kStagePart;
-      if (!kLo) {
-        // largest magnitudes of this warp's share of S_b and z_b, gathered
-        // in shared memory: red[2e + h] (S_b), red[4 + e] (z_b)
-        float am = 0.f, amz = 0.f;
-        if (e < 2) {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) am = fmaxf(am, fabsf(s0[j]));
-          if (h == 0) amz = fabsf(zval);
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
-          amz = fmaxf(amz, __shfl_xor_sync(0xffffffffu, amz, o));
-        }
-        if (lane == 0 && e < 2) {
+      if (!kLo && e < 2) {
+        // largest magnitudes (float bits) of this warp's share of S_b and
+        // z_b, gathered in shared memory: red[2e + h] (S_b), red[4 + e] (z_b)
+        const uint32_t am = __reduce_max_sync(0xffffffffu, abs_max_bits32(s0));
+        const uint32_t amz = __reduce_max_sync(0xffffffffu, h == 0 ? __float_as_uint(fabsf(zval)) : 0u);
+        if (lane == 0) {
           red[2 * e + h] = am;
           if (h == 0) red[4 + e] = amz;
         }
@@ -418,8 +424,8 @@ __device__ __forceinline__ void summary_body(const SummaryArgs& a, const Plan& p
       named_sync(1, kEpiThreads);
       int eS = 0, eZ = 0;
       if (!kLo) {
-        eS = record_exponent(fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3])));
-        eZ = record_exponent(fmaxf(red[4], red[5]));
+        eS = record_exponent(max(max(red[0], red[1]), max(red[2], red[3])));
+        eZ = record_exponent(max(red[4], red[5]));
       }
       if (e < 2) {
         // row r of S_b (columns 32h .. 32h+31) and, for h = 0, z_b[r]
