@@ -68,8 +68,8 @@ struct TcBuffers {
   float4* blkinfo;           // [M] {1, n~_i, 0, 0} (split path)
   int2* rexp;                // fp16 path: [slots][Q] record exponents {eS, eZ}
   uint32_t* mcw;             // fp16 path: [M][Qp] Mc[i][q / splits] as {fp16 bits of its mantissa in
-                             //            [1, 2) (with sign; 0 for a zero entry), int16 exponent x} with
-                             //            Mc = mantissa 2^(x - 1); x = -16384 marks a zero entry
+                             //            [1, 2) (with sign), x + 8192 in the high 16 bits} with
+                             //            Mc = mantissa 2^(x - 1); 0 for a zero entry
   __half* mcx;               // fp16 path: [slots][2][M][Qp] Mc[i][q / splits] 2^(eS[q] - ES[i]) (part 0),
                              //            the same with eZ, EZ (part 1)
   float4* sinfo;             // fp16 path: [slots][M] {output scale, 0, 0, 0}

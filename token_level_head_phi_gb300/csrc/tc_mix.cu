@@ -21,14 +21,15 @@ using mx::kSmemBytes;
 using mx::kStageArea;
 using mx::kThreads;
 
-// One entry of Mc as the fp16 path's exponent-folding kernel reads it:
-// x = m == 0 ? -16384 : the exponent with |m| = f 2^x, f in [0.5, 1), and the
-// fp16 bits of the mantissa 2f in [1, 2) with m's sign (a mantissa that rounds
-// up to 2 becomes 1 with x + 1), so that m = mantissa 2^(x - 1) up to the
-// fp16 rounding of the mantissa.  (-16384 keeps x + e far below any real
-// exponent sum without leaving the 16-bit range.)
+// One entry of Mc as the fp16 path's exponent-folding kernel reads it: the
+// fp16 bits of the mantissa 2f in [1, 2) of |m| = f 2^x, f in [0.5, 1), with
+// m's sign (a mantissa that rounds up to 2 becomes 1 with x + 1), and above
+// them x + 8192 as an unsigned 16-bit field, so that m = mantissa 2^(x - 1)
+// up to the fp16 rounding of the mantissa; a zero entry is the word 0.  (The
+// bias keeps every exponent sum the folding kernel forms positive and inside
+// its 16-bit lane.)
 __device__ __forceinline__ uint32_t mc_word(float m) {
-  if (m == 0.f) return 0xC0000000u;
+  if (m == 0.f) return 0u;
   int x = 0;
   const float f = frexpf(fabsf(m), &x);
   uint32_t h = __half_as_ushort(__float2half_rn(2.f * f));
@@ -37,7 +38,7 @@ __device__ __forceinline__ uint32_t mc_word(float m) {
     ++x;
   }
   if (m < 0.f) h |= 0x8000u;
-  return h | ((uint32_t)(x & 0xFFFF) << 16);
+  return h | ((uint32_t)(x + 8192) << 16);
 }
 
 // Also zeroes the progress counters of a fused launch.

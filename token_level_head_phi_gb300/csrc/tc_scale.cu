@@ -31,17 +31,21 @@ namespace {
 using namespace tc;
 
 constexpr int kWarps = 8;      // one query block (row) per warp
-constexpr int kQChunk = 4096;  // record exponents staged in shared memory at a time (16 KB)
-constexpr uint32_t kZeroWord = 0xC0000000u;  // Mc word of a zero entry (exponent -16384)
+constexpr int kQChunk = 4096;  // record exponents staged in shared memory at a time (at most 16 KB)
+// Exponents travel as unsigned 16-bit lanes with a bias: record exponents
+// e + kBias, Mc exponents x + kBias (mc_word in tc_mix.cu; the word 0 is a
+// zero entry).  Every sum below then stays in [0, 2^16) per lane, so plain
+// 32-bit adds and masks act on both lanes (S part low, z part high) at once.
+constexpr int kBias = 8192;
 
-// fp16 bits of mantissa 2^(x + e - E - 1) for Mc word w (see mc_word in
-// tc_mix.cu): the mantissa's bits under a new exponent while the result is a
-// normal fp16 number; below that, the subnormal with the mantissa shifted
-// right and rounded to nearest even (2^-24 steps; a result that rounds up to
-// 2^-14 lands on the smallest normal number, as the encoding continues there).
+// fp16 bits of mantissa 2^(x + e - E - 1) for Mc word w (one part): the
+// mantissa's bits under a new exponent while the result is a normal fp16
+// number; below that, the subnormal with the mantissa shifted right and
+// rounded to nearest even (2^-24 steps; a result that rounds up to 2^-14
+// lands on the smallest normal number, as the encoding continues there).
 __device__ __forceinline__ uint32_t place(uint32_t w, int e, int E) {
-  if (w == kZeroWord) return 0u;
-  const int x = (int)(int16_t)(w >> 16);
+  if (w == 0u) return 0u;
+  const int x = (int)(w >> 16) - kBias;
   const uint32_t h = w & 0xFFFFu, sign = h & 0x8000u;
   const int biased = x + e - E + 14;
   if (biased >= 1) return sign | ((uint32_t)biased << 10) | (h & 0x3FFu);
@@ -55,31 +59,30 @@ __device__ __forceinline__ uint32_t place(uint32_t w, int e, int E) {
 }
 
 // Both parts of one entry: fp16 bits for the S copy (low half) and the z
-// copy (high half).  e2 packs the record's {eS, eZ} and base2 {14 - ES,
-// 14 - EZ} as 16-bit lanes; the biased exponents x + e - E + 14 of both parts
-// come from two packed adds, and while both are positive (they are at most
-// 14: x + e <= E) the result is the
-// mantissa bits with those exponents placed above them.
-__device__ __forceinline__ uint32_t place2(uint32_t w, uint32_t e2, uint32_t base2, int es, int ez) {
-  if (w == kZeroWord) return 0u;
-  const uint32_t xx = __byte_perm(w, 0u, 0x3232);               // x in both lanes
-  const uint32_t t = __vadd2(__vadd2(e2, xx), base2);           // biased exponents
-  if (__vcmpgts2(t, 0u) == 0xFFFFFFFFu)
-    return (__byte_perm(w, 0u, 0x1010) & 0x83FF83FFu) | (t << 10);
-  return place(w, (int)(int16_t)(e2 & 0xFFFFu), es) | (place(w, (int)(int16_t)(e2 >> 16), ez) << 16);
+// copy (high half).  e2 = {eS, eZ} + kBias per lane, c2 = {14 - ES, 14 - EZ}
+// + 256 per lane (non-negative), so t = e2 + x + kBias + c2 holds the biased
+// fp16 exponents x + e - E + 14 (at most 14) plus 2 kBias + 256 = 16640, a
+// multiple of 64.  While both lie in [1, 14] the result is the mantissa bits
+// with t's low six bits shifted above them; otherwise each part takes the
+// exact path (a zero entry included).
+__device__ __forceinline__ uint32_t place2(uint32_t w, uint32_t e2, uint32_t c2, int es, int ez) {
+  const uint32_t t = e2 + __byte_perm(w, 0u, 0x3232) + c2;
+  if (((t - 0x41014101u) & 0xFFF0FFF0u) == 0u)
+    return (__byte_perm(w, 0u, 0x1010) & 0x83FF83FFu) | ((t << 10) & 0xFC00FC00u);
+  return place(w, (int)(e2 & 0xFFFFu) - kBias, es) | (place(w, (int)(e2 >> 16) - kBias, ez) << 16);
 }
 
 // Grid (ceil(M / kWarps), slots): warp w of CTA (x, u) builds row
 // i = x * kWarps + w of head u's two Mc copies and its output scale.  The
 // head's record exponents pass through shared memory in chunks of kQChunk,
-// packed {eS, eZ} as 16-bit lanes; each lane reads four consecutive Mc words
-// and four packed exponents (16 bytes each) at a time.
+// packed {eS, eZ} + kBias as 16-bit lanes; each lane reads four consecutive
+// Mc words and four packed exponents (16 bytes each) at a time.
 __global__ void __launch_bounds__(32 * kWarps) tc_scale_kernel(const Plan p, int Q, int Qp,
                                                                const uint32_t* __restrict__ mcw,
                                                                const int2* __restrict__ rexp,
                                                                __half* __restrict__ mcx,
                                                                float4* __restrict__ sinfo) {
-  __shared__ __align__(16) uint32_t ex_s[kQChunk];
+  extern __shared__ __align__(16) uint32_t ex_s[];  // min(Qp, kQChunk) words
   // the record exponents come from the summary kernel
   pdl_wait();
   pdl_launch_dependents();
@@ -92,12 +95,13 @@ __global__ void __launch_bounds__(32 * kWarps) tc_scale_kernel(const Plan p, int
   auto stage = [&](int c0, int n) {
     for (int t = threadIdx.x; t < n; t += blockDim.x) {
       const int2 e = c0 + t < Q ? ex[c0 + t] : make_int2(0, 0);
-      ex_s[t] = ((uint32_t)e.x & 0xFFFFu) | ((uint32_t)e.y << 16);
+      ex_s[t] = (uint32_t)(e.x + kBias) | ((uint32_t)(e.y + kBias) << 16);
     }
   };
   // row exponents: the largest eS[q] + x(Mc[i][b(q)]) (and eZ) over nonzero
-  // weights, as signed 16-bit lanes (a zero weight adds -16384)
-  uint32_t mx = 0x80008000u;
+  // weights, as biased lanes (a zero weight adds only the record's e + kBias,
+  // below every real sum)
+  uint32_t mx = 0u;
   for (int c0 = 0; c0 < Qp; c0 += kQChunk) {
     const int n = min(kQChunk, Qp - c0);
     __syncthreads();
@@ -108,20 +112,20 @@ __global__ void __launch_bounds__(32 * kWarps) tc_scale_kernel(const Plan p, int
       for (int q = 4 * lane; q < n; q += 128) {
         const uint4 w4 = __ldg(row + (c0 + q) / 4);
         const uint4 e4 = *reinterpret_cast<const uint4*>(ex_s + q);
-        mx = __vmaxs2(mx, __vadd2(e4.x, __byte_perm(w4.x, 0u, 0x3232)));
-        mx = __vmaxs2(mx, __vadd2(e4.y, __byte_perm(w4.y, 0u, 0x3232)));
-        mx = __vmaxs2(mx, __vadd2(e4.z, __byte_perm(w4.z, 0u, 0x3232)));
-        mx = __vmaxs2(mx, __vadd2(e4.w, __byte_perm(w4.w, 0u, 0x3232)));
+        mx = __viaddmax_u16x2(e4.x, __byte_perm(w4.x, 0u, 0x3232), mx);
+        mx = __viaddmax_u16x2(e4.y, __byte_perm(w4.y, 0u, 0x3232), mx);
+        mx = __viaddmax_u16x2(e4.z, __byte_perm(w4.z, 0u, 0x3232), mx);
+        mx = __viaddmax_u16x2(e4.w, __byte_perm(w4.w, 0u, 0x3232), mx);
       }
     }
   }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mx = __vmaxs2(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  int es = (int)(int16_t)(mx & 0xFFFFu), ez = (int)(int16_t)(mx >> 16);
+  for (int o = 16; o > 0; o >>= 1) mx = __vimax3_u16x2(mx, __shfl_xor_sync(0xffffffffu, mx, o), 0u);
+  int es = (int)(mx & 0xFFFFu) - 2 * kBias, ez = (int)(mx >> 16) - 2 * kBias;
   // an all-zero row mixes nothing: any exponent (its entries stay zero)
-  if (es < -8192) es = 0;
-  if (ez < -8192) ez = 0;
-  const uint32_t base2 = ((uint32_t)(14 - es) & 0xFFFFu) | ((uint32_t)(14 - ez) << 16);
+  if (es < -kBias / 2) es = 0;
+  if (ez < -kBias / 2) ez = 0;
+  const uint32_t c2 = (uint32_t)(14 - es + 256) | ((uint32_t)(14 - ez + 256) << 16);
   uint2* ds = reinterpret_cast<uint2*>(mcx + (((size_t)u * 2 + 0) * p.M + i) * Qp);
   uint2* dz = reinterpret_cast<uint2*>(mcx + (((size_t)u * 2 + 1) * p.M + i) * Qp);
   for (int c0 = 0; c0 < Qp; c0 += kQChunk) {
@@ -136,8 +140,8 @@ __global__ void __launch_bounds__(32 * kWarps) tc_scale_kernel(const Plan p, int
       for (int q = 4 * lane; q < n; q += 128) {
         const uint4 w4 = __ldg(row + (c0 + q) / 4);
         const uint4 e4 = *reinterpret_cast<const uint4*>(ex_s + q);
-        const uint32_t r0 = place2(w4.x, e4.x, base2, es, ez), r1 = place2(w4.y, e4.y, base2, es, ez);
-        const uint32_t r2 = place2(w4.z, e4.z, base2, es, ez), r3 = place2(w4.w, e4.w, base2, es, ez);
+        const uint32_t r0 = place2(w4.x, e4.x, c2, es, ez), r1 = place2(w4.y, e4.y, c2, es, ez);
+        const uint32_t r2 = place2(w4.z, e4.z, c2, es, ez), r3 = place2(w4.w, e4.w, c2, es, ez);
         ds[(c0 + q) / 4] = make_uint2(__byte_perm(r0, r1, 0x5410), __byte_perm(r2, r3, 0x5410));
         dz[(c0 + q) / 4] = make_uint2(__byte_perm(r0, r1, 0x7632), __byte_perm(r2, r3, 0x7632));
       }
@@ -153,7 +157,8 @@ __global__ void __launch_bounds__(32 * kWarps) tc_scale_kernel(const Plan p, int
 
 int launch_tc_scale(const Plan& p, const TcBuffers& b, cudaStream_t s) {
   const dim3 grid((unsigned)((p.M + kWarps - 1) / kWarps), (unsigned)b.slots);
-  return launch_pdl(tc_scale_kernel, grid, dim3(32 * kWarps), 0, s, p, p.M * p.splits, b.Qp, (const uint32_t*)b.mcw,
+  const size_t smem = 4 * (size_t)(b.Qp < kQChunk ? b.Qp : kQChunk);
+  return launch_pdl(tc_scale_kernel, grid, dim3(32 * kWarps), smem, s, p, p.M * p.splits, b.Qp, (const uint32_t*)b.mcw,
                     (const int2*)b.rexp, b.mcx, b.sinfo);
 }
 

@@ -430,6 +430,7 @@ __device__ __forceinline__ void summary_body(const SummaryArgs& a, const Plan& p
       if (e < 2) {
         // row r of S_b (columns 32h .. 32h+31) and, for h = 0, z_b[r]
         const float scS = kLo ? 1.f : pow2_neg(eS);
+        const float2 sc2 = make_float2(scS, scS);
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
           const int j = 4 * h + jj;
@@ -439,7 +440,9 @@ __device__ __forceinline__ void summary_body(const SummaryArgs& a, const Plan& p
             uint32_t* hp = &hv.x;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-              __half2 hh = __floats2half2_rn(src[2 * q] * scS, src[2 * q + 1] * scS);
+              // two products per instruction (exact: a power of two)
+              const float2 y = __fmul2_rn(make_float2(src[2 * q], src[2 * q + 1]), sc2);
+              __half2 hh = __floats2half2_rn(y.x, y.y);
               hp[q] = *reinterpret_cast<uint32_t*>(&hh);
             }
           } else {
