@@ -199,13 +199,17 @@ mhla_status mhla_forward(const void* q, const void* k, const void* v, const floa
  *   q, k, v, mc, p, out, stream   as for mhla_forward
  * Allocates nothing: no cudaMalloc, cudaMallocAsync or cudaFree.  Problems
  * whose mhla_workspace_bytes(p) exceeds 32 MiB return MHLA_ERR_WORKSPACE and
- * enqueue nothing.  The first call on a device (that device current) looks up
- * the array's device address with cudaGetSymbolAddress; make that first call
- * before any stream capture.  Every GPU that loads the library holds the
- * array until the process exits.  All calls on a device share the one array,
- * so calls whose work overlaps on the GPU (different streams, or different
- * host threads) race and must be serialised by the caller.  Nothing in the
- * array has to start at zero: each call overwrites every byte it reads. */
+ * enqueue nothing.  Each call looks up the array's device address with
+ * cudaGetSymbolAddress for the current device.  The first call on a device
+ * may be the one that loads the library's code there (CUDA loads modules
+ * lazily by default), and loading commits the array's 32 MiB of device
+ * memory at that moment: make a first, small call at start-up, before any
+ * stream capture, if later calls must not depend on free device memory.
+ * Every GPU that loads the library holds the array until the process exits.
+ * All calls on a device share the one array, so calls whose work overlaps on
+ * the GPU (different streams, or different host threads) race and must be
+ * serialised by the caller.  Nothing in the array has to start at zero: each
+ * call overwrites every byte it reads. */
 mhla_status mhla_forward_noalloc(const void* q, const void* k, const void* v, const float* mc,
                                  const mhla_params* p, void* out, void* stream);
 

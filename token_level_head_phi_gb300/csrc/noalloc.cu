@@ -11,12 +11,19 @@
 // memory that every GPU loading this library holds until the process exits.
 //
 // The scratch array is an ordinary __device__ symbol.  Host code only sees a
-// host-side stand-in for it, so its device address is looked up once per
-// device with cudaGetSymbolAddress (on the first call made while that device
-// is current) and handed to the kernels as a plain pointer.
+// host-side stand-in for it, so its device address is looked up with
+// cudaGetSymbolAddress on every call (for the device current at that call,
+// in the context current there; once the library's code is loaded on that
+// device the lookup is a table read and allocates nothing) and handed to the
+// kernels as a plain pointer.
+//
+// First call on a device: with CUDA's lazy module loading (the default since
+// CUDA 12.2) the part of the library that holds the array may be loaded only
+// by that call's lookup, and loading it commits the array's 32 MiB of device
+// memory then.  A caller that will need this entry point where it cannot
+// allocate (an out-of-memory handler, say) should make one small call at
+// start-up, before any stream capture.
 #include <cuda_runtime.h>
-
-#include <mutex>
 
 #include "mhla.h"
 
@@ -28,25 +35,12 @@ constexpr size_t kNoallocScratchBytes = 32ull << 20;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-void* g_scratch_ptr[kMaxDevices] = {};
-
-// Device address of the scratch array on the current device (looked up once
-// per device; the lookup itself allocates nothing).
+// Device address of the scratch array on the current device.
 mhla_status scratch_address(void** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return MHLA_ERR_CUDA;
-  if (dev < 0 || dev >= kMaxDevices) return MHLA_ERR_UNSUPPORTED;
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_scratch_ptr[dev]) {
-    void* ptr = nullptr;
-    e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
-    if (e != cudaSuccess || !ptr) return MHLA_ERR_CUDA;
-    g_scratch_ptr[dev] = ptr;
-  }
-  *out = g_scratch_ptr[dev];
+  void* ptr = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+  if (e != cudaSuccess || !ptr) return MHLA_ERR_CUDA;
+  *out = ptr;
   return MHLA_OK;
 }
 
