@@ -171,10 +171,13 @@ def phase_kernels(w: wl.Workload, info, fmap: str, causal: bool):
                 "output": ("tc_fused_kernel", C + "tc_fused.cu")}
     f16 = w.norm != "mala" and fmap != "exp" and not causal
     q = w.n_blocks * info.summary_splits
+    small = not causal and w.n_blocks <= 16 and q <= 256          # CUDA-core mixing of few blocks
     mixt = f16 and w.n_blocks <= 128 and 2 * ((q + 63) // 64) * 32 <= 256
+    mix = ("tc_mixs_kernel", C + "tc_mixs.cu") if small else \
+        ("tc_mixt_kernel", C + "tc_mix.cu") if mixt else ("tc_mix_kernel", C + "tc_mix.cu")
     return {"prep": ("tc_prep_kernel", C + "tc_mix.cu"), "summary": ("tc_summary_kernel", C + "tc_summary.cu"),
-            "scale": ("tc_scale_kernel", C + "tc_scale.cu") if f16 else None,
-            "mix": ("tc_mixt_kernel", C + "tc_mix.cu") if mixt else ("tc_mix_kernel", C + "tc_mix.cu"),
+            "scale": ("tc_scale_kernel", C + "tc_scale.cu") if f16 and not small else None,
+            "mix": mix,
             "output": ("tc_causal_kernel", C + "tc_causal.cu") if causal else ("tc_output_kernel", C + "tc_output.cu")}
 
 

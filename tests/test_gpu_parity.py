@@ -197,13 +197,15 @@ def _run_variant(w, tensors, mc, norm, variant):
     return o.view(torch.int16).cpu().numpy()
 
 
-@pytest.mark.parametrize("name", ["seq_32k_mala", "seq_32k_m1_mala"])
+@pytest.mark.parametrize("name", ["seq_32k_mala", "image_64x64"])
 def test_fused_bitwise_equals_multipass_mala(name):
     """Under MALA both launches run the same split-precision arithmetic in
-    the same order: the results are bit for bit the same.  (DIVISIVE and NONE
-    mix fp16 records in the multi-pass launch and split records in the fused
-    one; test_workload_parity checks both against the oracle.)"""
-    w = wl.WORKLOADS[name]
+    the same order on the tensor cores: the results are bit for bit the same.
+    (DIVISIVE and NONE mix fp16 records in the multi-pass launch and split
+    records in the fused one, and the multi-pass launch mixes 16 blocks or
+    fewer on the CUDA cores; test_workload_parity checks every one of them
+    against the oracle.)"""
+    w = wl.WORKLOADS[name].with_(norm="mala")
     vals, dev = wl.all_inputs(w)
     tensors = upload(w, dev)
     mc = wl.make_mc(w)

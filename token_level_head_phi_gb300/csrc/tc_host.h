@@ -114,6 +114,14 @@ int launch_tc_summary(const Plan& p, const ChunkShape& c, const void* k, const v
 // with the record exponents folded in, and the output scales.
 int launch_tc_scale(const Plan& p, const TcBuffers& b, cudaStream_t s);
 int launch_tc_mix(const Plan& p, const TcBuffers& b, cudaStream_t s);
+// Mixing of few blocks on the CUDA cores (tc_mixs.cu): M <= kSmallMixMaxM query
+// blocks and Q <= kSmallMixMaxQ records per head, read from the tensor-core
+// records, written as launch_tc_mix writes them (fp16 records need no
+// launch_tc_scale before it).
+constexpr int kSmallMixMaxM = 16;
+constexpr int kSmallMixMaxQ = 256;
+bool small_mix_supported(const Plan& p);
+int launch_tc_mix_small(const Plan& p, const float* mc, const TcBuffers& b, cudaStream_t s);
 int launch_tc_output(const Plan& p, const ChunkShape& c, const void* q, const TcBuffers& b, void* out,
                      cudaStream_t s);
 // Testing hooks set by mhla_set_debug: limit of the fused launch's counter
