@@ -345,11 +345,14 @@ def run_mine(args, w: wl.Workload, world: int, rank: int, local: int, dist, samp
         sampler.start()
     t0 = time.time()
     start.record(stream)
+    host_s = 0.0
     for i in range(K):
         if flush is not None:
             flush.zero_()
             step_ev[i][0].record(stream)
+        h0 = time.perf_counter()
         step()
+        host_s += time.perf_counter() - h0
         if flush is not None:
             step_ev[i][1].record(stream)
     end.record(stream)
@@ -419,6 +422,7 @@ def run_mine(args, w: wl.Workload, world: int, rank: int, local: int, dist, samp
         "phase_note": "per-kernel times from a separate run with events between the kernels (which serialises "
                       "the launches the timed steps overlap)",
         "gpu_launches": info.kernels_per_call * K,
+        "host_us_per_call": host_s / K * 1e6,
         "clocks": clocks,
     }
     return result, (q, k, v, mc, out, p, info, stream)
@@ -459,6 +463,7 @@ def run_per_config(args, world, rank, local, dist):
                                                                    "traffic_over_algorithmic")}
                         for ph, row in r["kernels"].items()},
             "variant_name": r["config"]["variant_name"], "dtype": w.dtype, "norm": w.norm,
+            "host_us_per_call": r["host_us_per_call"],
             "steps": sub.steps, "warmup": sub.warmup, "l2": r["config"]["l2"],
         }
     return out
@@ -618,11 +623,14 @@ def run_backward(args, w: wl.Workload, world: int, rank: int, local: int, dist):
         sampler.start()
     t0 = time.time()
     start.record(stream)
+    host_s = 0.0
     for i in range(K):
         if flush is not None:
             flush.zero_()
             step_ev[i][0].record(stream)
+        h0 = time.perf_counter()
         step()
+        host_s += time.perf_counter() - h0
         if flush is not None:
             step_ev[i][1].record(stream)
     end.record(stream)

@@ -11,8 +11,10 @@ They model the protocols as written in the kernel sources (kept in step by
 hand); they do not run the kernels.
 
 Covered:
-  * the summary kernel's stage rings: with two MMA-issuing warps each unit
-    goes through its issuer's own ring of stages (safe); one ring shared by
+  * the summary kernel's stage rings and accumulators: with two MMA-issuing
+    warps each unit goes through its issuer's own ring of stages and unit it
+    accumulates in TMEM slot it % 4, each issuer alternating two (safe); one
+    ring shared by
     both issuers lets an issuer that skips the other's units wait on a stage
     two phases ahead and read it early (the negative control: the form that
     faulted a backward run on the Wan shape -- the split-precision layout's
@@ -79,13 +81,15 @@ def wait(bar: Bar, q: int):
 
 
 # --------------------------------------------------------------- summary kernel
-def summary_protocol(units: int, cpp: int, nstages: int, nissuers: int, shared_ring: bool, seed: int):
+def summary_protocol(units: int, cpp: int, nstages: int, nissuers: int, shared_ring: bool, seed: int,
+                     nacc: int = 4):
     rnd = random.Random(seed)
     full = [Bar(1) for _ in range(nstages)]
     kready = [Bar(1) for _ in range(nstages)]
     empty = [Bar(1) for _ in range(nstages)]
-    accfull = [Bar(1) for _ in range(2)]
-    accempty = [Bar(1) for _ in range(2)]
+    # unit it accumulates in TMEM slot it % nacc (each issuer alternates its own slots)
+    accfull = [Bar(1) for _ in range(nacc)]
+    accempty = [Bar(1) for _ in range(nacc)]
     content = [None] * nstages
 
     def ring(it):
@@ -118,11 +122,11 @@ def summary_protocol(units: int, cpp: int, nstages: int, nissuers: int, shared_r
             yield True
 
     def issuer(j):
-        uses = [0, 0]
+        uses = [0] * nacc
         for it, c, s, k in walk():
             if it % nissuers != j:
                 continue
-            acc = it % 2
+            acc = it % nacc
             if c == 0:
                 yield from wait(accempty[acc], uses[acc] - 1)
             yield from wait(kready[s], k)
@@ -135,20 +139,21 @@ def summary_protocol(units: int, cpp: int, nstages: int, nissuers: int, shared_r
 
     def epilogue():
         for it in range(units):
-            acc = it % 2
-            yield from wait(accfull[acc], it // 2)
+            acc = it % nacc
+            yield from wait(accfull[acc], it // nacc)
             accempty[acc].arrive()
             yield True
 
     schedule([producer(), phi(), epilogue()] + [issuer(j) for j in range(nissuers)], rnd)
 
 
+@pytest.mark.parametrize("nacc", [2, 4])
 @pytest.mark.parametrize("nstages,nissuers", [(6, 2), (5, 2), (4, 2), (3, 1), (5, 1)])
-def test_summary_stage_rings_are_safe(nstages, nissuers):
-    for units in (1, 2, 3, 5, 8):
+def test_summary_stage_rings_are_safe(nstages, nissuers, nacc):
+    for units in (1, 2, 3, 5, 8, 11):
         for cpp in (1, 2, 3, 4):
             for seed in range(25):
-                summary_protocol(units, cpp, nstages, nissuers, shared_ring=False, seed=seed)
+                summary_protocol(units, cpp, nstages, nissuers, shared_ring=False, seed=seed, nacc=nacc)
 
 
 @pytest.mark.parametrize("nstages,cpp", [(3, 3), (4, 4)])

@@ -338,7 +338,7 @@ template <int D, typename T>
 int run_output(const Plan& p, const BwdBuffers& w, const void* q, const void* dout, void* dq, cudaStream_t s) {
   const size_t smo = sizeof(float) * (D * D + 2 * D + 3 * kTile * D + 4 * kTile);
   auto ko = bwd_output_kernel<D, T>;
-  cudaError_t e = cudaFuncSetAttribute(ko, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smo);
+  cudaError_t e = (cudaError_t)set_max_dynamic_smem((const void*)ko, (int)smo);
   if (e != cudaSuccess) return (int)e;
   ko<<<dim3(p.M * p.splits, p.BH), kThreads, smo, s>>>(p, (const T*)q, (const T*)dout, w.mixed, w.rowsum, (T*)dq,
                                                        w.dmixp, w.dnp);
@@ -350,7 +350,7 @@ int run_summary(const Plan& p, const BwdBuffers& w, const void* k, const void* v
                 cudaStream_t s) {
   const size_t sms = sizeof(float) * (D * D + 2 * D + 2 * kTile * D);
   auto ks = bwd_summary_kernel<D, T>;
-  cudaError_t e = cudaFuncSetAttribute(ks, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sms);
+  cudaError_t e = (cudaError_t)set_max_dynamic_smem((const void*)ks, (int)sms);
   if (e != cudaSuccess) return (int)e;
   ks<<<dim3(p.M * p.splits, p.BH), kThreads, sms, s>>>(p, (const T*)k, (const T*)v, w.dstack, (T*)dk, (T*)dv);
   return (int)cudaGetLastError();

@@ -176,6 +176,11 @@ __host__ __device__ inline int block_token(const Plan& p, int b, int l) {
   return ((bz * p.bt + z) * p.Hg + by * p.bh + y) * p.Wg + bx * p.bw + x;
 }
 
+// cudaFuncSetAttribute(kernel, MaxDynamicSharedMemorySize, bytes), done once
+// per kernel and context (a launch would otherwise pay for it every time);
+// returns a cudaError_t as int.
+int set_max_dynamic_smem(const void* kernel, int bytes);
+
 // Launchers implemented by the kernel translation units.  Each returns the
 // cudaError_t of its launch (as int, to keep this header runtime-free).
 int launch_mc_rowsum(const Plan& p, const float* mc, float* rowsum, void* stream);

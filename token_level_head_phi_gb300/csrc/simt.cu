@@ -213,7 +213,7 @@ int output_dispatch(const Plan& p, const void* q, const float* mixed, const floa
   const size_t smem = sizeof(float) * (D * D + 2 * D + 64 * D + 64);
   auto kern = simt_output_kernel<D, Tin>;
   if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = (cudaError_t)set_max_dynamic_smem((const void*)kern, (int)smem);
     if (e != cudaSuccess) return (int)e;
   }
   const int tiles = (p.nb + 63) / 64;

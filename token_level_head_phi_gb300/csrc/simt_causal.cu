@@ -138,7 +138,7 @@ int run(const Plan& p, const void* q, const void* k, const void* v, const float*
         const float* mc, void* out, cudaStream_t s) {
   const size_t smem = sizeof(float) * (D * D + 2 * D + 3 * kTQ * D + kTQ * kTQ + kTQ);
   auto kern = causal_output_kernel<D, T>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = (cudaError_t)set_max_dynamic_smem((const void*)kern, (int)smem);
   if (e != cudaSuccess) return (int)e;
   kern<<<dim3(p.M, p.BH), kThreads, smem, s>>>(p, (const T*)q, (const T*)k, (const T*)v, mixed, rl, mc, (T*)out);
   return (int)cudaGetLastError();

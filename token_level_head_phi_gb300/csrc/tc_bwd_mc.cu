@@ -266,7 +266,7 @@ int launch_tc_bwd_mc(const Plan& p, const __nv_bfloat16* dx_hi, const __nv_bfloa
   a.items = p.BH * a.qt * a.qt;
   a.partial = partial;
   a.err = p.err;
-  cudaError_t ce = cudaFuncSetAttribute(tc_bwd_mc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  cudaError_t ce = (cudaError_t)set_max_dynamic_smem((const void*)tc_bwd_mc_kernel, (int)kSmemBytes);
   if (ce != cudaSuccess) return (int)ce;
   const int grid = a.items < num_sms() ? a.items : num_sms();
   tc_bwd_mc_kernel<<<grid, kThreads, kSmemBytes, s>>>(a);

@@ -712,7 +712,7 @@ int launch_tc_bwd_output(const Plan& p, const void* q, const void* dout, const _
   a.c = c;
   a.err = p.err;
   cudaError_t ce =
-      cudaFuncSetAttribute(tc_bwd_output_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+      (cudaError_t)set_max_dynamic_smem((const void*)tc_bwd_output_kernel, (int)kSmemBytes);
   if (ce != cudaSuccess) return (int)ce;
   const int grid = a.units < num_sms() ? a.units : num_sms();
   tc_bwd_output_kernel<<<grid, kThreads, kSmemBytes, s>>>(a, p);

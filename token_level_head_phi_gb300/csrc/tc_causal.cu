@@ -636,7 +636,7 @@ int launch_tc_causal(const Plan& p, const void* q, const void* k, const void* v,
   a.f_m = make_fastdiv((uint32_t)p.M);
   a.c = c;
   a.err = p.err;
-  cudaError_t ce = cudaFuncSetAttribute(tc_causal_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  cudaError_t ce = (cudaError_t)set_max_dynamic_smem((const void*)tc_causal_kernel, (int)kSmemBytes);
   if (ce != cudaSuccess) return (int)ce;
   const int grid = a.units < num_sms() ? a.units : num_sms();
   tc_causal_kernel<<<grid, kThreads, kSmemBytes, s>>>(a, p);

@@ -144,7 +144,7 @@ int launch_variant(FusedArgs& a, const Plan& p, cudaStream_t s) {
   uint32_t smem = summary_smem_bytes(true);
   if (mix_smem_bytes() > smem) smem = mix_smem_bytes();
   if (output_smem_bytes(kOutLo, kQLo) > smem) smem = output_smem_bytes(kOutLo, kQLo);
-  cudaError_t ce = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t ce = (cudaError_t)set_max_dynamic_smem((const void*)kern, (int)smem);
   if (ce != cudaSuccess) return (int)ce;
   int dev = 0, coop = 0, per_sm = 0;
   if ((ce = cudaGetDevice(&dev)) != cudaSuccess) return (int)ce;

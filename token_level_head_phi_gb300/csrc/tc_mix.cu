@@ -105,7 +105,7 @@ __global__ void __launch_bounds__(mx::kThreads, 1) tc_mix_kernel(const __grid_co
 
 template <bool kF16>
 int launch_variant(const MixArgs& a, const Plan& p, cudaStream_t s) {
-  cudaError_t ce = cudaFuncSetAttribute(tc_mix_kernel<kF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  cudaError_t ce = (cudaError_t)set_max_dynamic_smem((const void*)tc_mix_kernel<kF16>, (int)kSmemBytes);
   if (ce != cudaSuccess) return (int)ce;
   const int grid = a.units < num_sms() ? a.units : num_sms();
   return launch_pdl(tc_mix_kernel<kF16>, dim3(grid), dim3(kThreads), kSmemBytes, s, a, p);
@@ -117,7 +117,7 @@ __global__ void __launch_bounds__(mt::kThreads, 1) tc_mixt_kernel(const __grid_c
 
 int launch_mixt(const mt::MixTArgs& a, const Plan& p, cudaStream_t s) {
   auto kern = tc_mixt_kernel;
-  cudaError_t ce = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)mt::kSmemBytes);
+  cudaError_t ce = (cudaError_t)set_max_dynamic_smem((const void*)kern, (int)mt::kSmemBytes);
   if (ce != cudaSuccess) return (int)ce;
   int grid = a.itiles * a.items;
   if (grid > num_sms()) grid = num_sms();

@@ -16,7 +16,10 @@
 //         one MMA per K step; Mixed holds S~_i 2^-ES[i] and z~_i 2^-EZ[i],
 //         which the output step scales back.
 //   split (MALA, causal, fused): X and Mc as bf16 high + low parts,
-//         D = Xh Mh + Xh Ml + Xl Mh.
+//         D = Xh Mh + Xh Ml + Xl Mh in two MMAs per K step: Xh [Mh | Ml]
+//         (N = 2 NT: the two B tiles lie back to back in shared memory, so
+//         one descriptor spans both) into accumulator columns [0, 2 NT), and
+//         Xl Mh into [0, NT); the epilogue adds columns c and NT + c.
 // The epilogue writes Mixed as bf16 (plus the low residual where the output
 // step needs it): 32 query blocks x 128 r at a time, transposed through a
 // shared-memory tile and stored by TMA.
@@ -161,6 +164,7 @@ __device__ __forceinline__ void mix_body(const MixArgs& a, const Plan& p, const 
     if (lane == 0) {
       // --------------------------------------------------------------- MMA
       const uint32_t idesc = kF16 ? idesc_f16_f32(128, a.NT, true, false) : idesc_bf16_f32(128, a.NT, true, false);
+      const uint32_t idesc2 = idesc_bf16_f32(128, 2 * a.NT, true, false);  // split: Xh [Mh | Ml]
       int stage = 0, acc = 0;
       uint32_t phase = 0, accph = 0;
       bool ok = true;
@@ -176,11 +180,13 @@ __device__ __forceinline__ void mix_body(const MixArgs& a, const Plan& p, const 
           for (int ks = 0; ks < 4; ++ks) {
             const uint64_t ahi = sdesc_sw128(st + (uint32_t)ks * 2048u, kAtom, 1024u);
             const uint64_t bhi = sdesc_sw128(st + a.off_b + (uint32_t)ks * 32u, 0u, 1024u);
-            umma_bf16(d, ahi, bhi, idesc, (kc > 0 || ks > 0) ? 1u : 0u);
-            if (!kF16) {
+            const uint32_t accum = (kc > 0 || ks > 0) ? 1u : 0u;
+            if (kF16) {
+              umma_bf16(d, ahi, bhi, idesc, accum);
+            } else {
+              // the B descriptor at Mh spans Ml too (off_blo = off_b + NT rows)
               const uint64_t alo = sdesc_sw128(st + a.off_alo + (uint32_t)ks * 2048u, kAtom, 1024u);
-              const uint64_t blo = sdesc_sw128(st + a.off_blo + (uint32_t)ks * 32u, 0u, 1024u);
-              umma_bf16(d, ahi, blo, idesc, 1u);
+              umma_bf16(d, ahi, bhi, idesc2, accum);
               umma_bf16(d, alo, bhi, idesc, 1u);
             }
           }
@@ -228,6 +234,14 @@ __device__ __forceinline__ void mix_body(const MixArgs& a, const Plan& p, const 
       for (int c0 = g * half_nt; c0 < (g + 1) * half_nt; c0 += 32) {
         float v[32];
         tmem_ld32(taddr + (uint32_t)c0, v);
+        if (!kF16) {
+          // split: add the Xh Ml products, NT columns further
+          float v2[32];
+          tmem_ld32(taddr + (uint32_t)(a.NT + c0), v2);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] += v2[j];
+        }
         tmem_wait_ld();
         // Slices without low residuals alternate between the two halves of
         // the staging area, so a slice waits only for the store before the

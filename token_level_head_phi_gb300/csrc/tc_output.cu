@@ -25,7 +25,7 @@ template <bool kLo, bool kQLo>
 int launch_variant(const OutArgs& a, const Plan& p, cudaStream_t s) {
   const uint32_t smem = output_smem_bytes(kLo, kQLo);
   auto kern = tc_output_kernel<kLo, kQLo>;
-  cudaError_t ce = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t ce = (cudaError_t)set_max_dynamic_smem((const void*)kern, (int)smem);
   if (ce != cudaSuccess) return (int)ce;
   const int grid = a.units < num_sms() ? a.units : num_sms();
   return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, s, a, p);

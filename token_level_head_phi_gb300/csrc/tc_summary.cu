@@ -25,7 +25,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_summary_kernel(const __grid_co
 template <bool kLo>
 int launch_variant(const SummaryArgs& a, const Plan& p, cudaStream_t s) {
   const uint32_t smem = Layout<kLo>::kSmemBytes;
-  cudaError_t ce = cudaFuncSetAttribute(tc_summary_kernel<kLo>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t ce = (cudaError_t)set_max_dynamic_smem((const void*)tc_summary_kernel<kLo>, (int)smem);
   if (ce != cudaSuccess) return (int)ce;
   const int grid = a.units < num_sms() ? a.units : num_sms();
   return launch_pdl(tc_summary_kernel<kLo>, dim3(grid), dim3(kThreads), smem, s, a, p);

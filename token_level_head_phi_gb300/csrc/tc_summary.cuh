@@ -21,7 +21,8 @@
 // Persistent, warp-specialised CTA (one per SM, 640 threads):
 //   warp 0       TMA producer (K and V tiles of one token chunk per stage)
 //   warp 1       TMEM allocation; warps 1, 2 MMA issue (even / odd units,
-//                each through its own ring of stages)
+//                each through its own ring of stages and its own two of the
+//                four TMEM accumulators)
 //   warps 4-6, 16-17  epilogue: TMEM rows 0..64 -> the record (S_b, z_b,
 //                v_b) as fp16 (DIVISIVE/NONE: S_b and z_b each scaled by a
 //                power of two taken from its own largest entry, the two
@@ -53,7 +54,8 @@ constexpr int kXfThreads = 256;                         // warps 8..15
 constexpr uint32_t kTile = 128 * 128;                   // 128 rows of 128 bytes
 constexpr uint32_t kStagePart = 8192 + 1024;            // staging: S 8 KB + zv 1 KB
 constexpr uint32_t kStagingBuf = 2 * kStagePart;        // hi and lo
-constexpr uint32_t kTmemCols = 256;                     // two 128-column accumulators
+constexpr int kAccs = 4;                                // TMEM accumulators: unit it uses it % 4
+constexpr uint32_t kTmemCols = 512;                     // four 128-column accumulators (80 columns used)
 constexpr int kN = 80;                                  // MMA N: 64 value features + 16 ones
 
 // Shared-memory layout.  kLo adds the low bf16 residual of phi(K) as a third
@@ -184,7 +186,7 @@ __device__ __forceinline__ void summary_body(const SummaryArgs& a, const Plan& p
   auto kready = [&](int s) { return bars + 8u * (kStages + s); };
   auto empty = [&](int s) { return bars + 8u * (2 * kStages + s); };
   auto accfull = [&](int x) { return bars + 8u * (3 * kStages + x); };
-  auto accempty = [&](int x) { return bars + 8u * (3 * kStages + 2 + x); };
+  auto accempty = [&](int x) { return bars + 8u * (3 * kStages + kAccs + x); };
   // Stage rings: with two MMA issuers (kIssuers), unit number `it` of this
   // CTA goes through ring it % kIssuers, the stages j, j + kIssuers, ...; each
   // ring is filled in order by the producer and drained in order by ONE
@@ -195,11 +197,11 @@ __device__ __forceinline__ void summary_body(const SummaryArgs& a, const Plan& p
   auto ring_len = [&](int j) { return (kStages - j + kIssuers - 1) / kIssuers; };
   auto ring_stage = [&](int j, long long k) { return j + kIssuers * (int)(k % ring_len(j)); };
   auto ring_phase = [&](int j, long long k) { return (uint32_t)((k / ring_len(j)) & 1); };
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gb + L::kBars + 8 * (3 * kStages + 4));
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(gb + L::kBars + 8 * (3 * kStages + 4) + 8);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gb + L::kBars + 8 * (3 * kStages + 2 * kAccs));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gb + L::kBars + 8 * (3 * kStages + 2 * kAccs) + 8);
   // epilogue: per-warp maxima of the fp16 record parts (float bits)
-  uint32_t* red = reinterpret_cast<uint32_t*>(gb + L::kBars + 192);
-  static_assert(8 * (3 * kStages + 4) + 12 <= 192, "barrier area");
+  uint32_t* red = reinterpret_cast<uint32_t*>(gb + L::kBars + 224);
+  static_assert(8 * (3 * kStages + 2 * kAccs) + 12 <= 224 && 224 + 4 * 6 <= 256, "barrier area");
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -218,7 +220,7 @@ __device__ __forceinline__ void summary_body(const SummaryArgs& a, const Plan& p
       mbar_init(kready(s), kXfThreads / 32);
       mbar_init(empty(s), 1);
     }
-    for (int x = 0; x < 2; ++x) {
+    for (int x = 0; x < kAccs; ++x) {
       mbar_init(accfull(x), 1);
       mbar_init(accempty(x), kEpiThreads / 32);
     }
@@ -304,13 +306,15 @@ __device__ __forceinline__ void summary_body(const SummaryArgs& a, const Plan& p
       const int ksteps = a.c.rows_pad / 16;
       long long rk = 0;       // chunks taken from ring j
       int it = 0;
-      uint32_t accph = 0;     // bit x: phase of accumulator x
       bool ok = true;
       for (int w = f.cta; w < a.units && ok; w += f.ncta, ++it) {
         if (it % kIssuers != j) continue;
         const UnitCoord uc = unit_coord(p, a, w);
-        const int acc = it & 1;
-        if (!(ok = mbar_wait(accempty(acc), ((accph >> acc) & 1u) ^ 1u, a.err, 0x102, abort_flag))) break;
+        // unit it accumulates in slot it % 4: each issuer alternates two
+        // slots, so it can start a unit before the epilogue has read the
+        // previous one out of tensor memory
+        const int acc = it & (kAccs - 1);
+        if (!(ok = mbar_wait(accempty(acc), ((uint32_t)(it / kAccs) & 1u) ^ 1u, a.err, 0x102, abort_flag))) break;
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)acc * 128u;
         for (int c = uc.c0; c < uc.c1; ++c) {
@@ -335,7 +339,6 @@ __device__ __forceinline__ void summary_body(const SummaryArgs& a, const Plan& p
         }
         if (!ok) break;
         umma_commit(accfull(acc));
-        accph ^= 1u << acc;
       }
     }
   } else if (warp >= 8 && warp < 16) {
@@ -383,13 +386,13 @@ __device__ __forceinline__ void summary_body(const SummaryArgs& a, const Plan& p
     const int h = warp >= 16 ? 1 : 0;         // column half of S_b
     const int et = warp < 16 ? threadIdx.x - 128 : 96 + threadIdx.x - 512;
     const int r = 32 * e + lane;  // TMEM lane = row of D
-    int acc = 0, it = 0;
+    int it = 0;
     unsigned int batch = 0;
-    uint32_t accph = 0;
     bool ok = true;
     for (int w = f.cta; w < a.units && ok; w += f.ncta, ++it) {
       const UnitCoord uc = unit_coord(p, a, w);
-      ok = mbar_wait(accfull(acc), accph, a.err, 0x105, abort_flag);
+      const int acc = it & (kAccs - 1);
+      ok = mbar_wait(accfull(acc), (uint32_t)(it / kAccs) & 1u, a.err, 0x105, abort_flag);
       if (!(ok = named_all(1, kEpiThreads, ok))) break;
       tc_fence_after();
       const uint32_t taddr = tmem + (uint32_t)acc * 128u + ((uint32_t)(32 * e) << 16);
@@ -400,10 +403,6 @@ __device__ __forceinline__ void summary_body(const SummaryArgs& a, const Plan& p
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive_warp(accempty(acc));
-      if (++acc == 2) {
-        acc = 0;
-        accph ^= 1u;
-      }
 
       uint8_t* st_hi = gb + L::kStaging + (it % L::kStagingBufs) * L::kStagingStride;
       uint8_t* st_lo = st_hi + kStagePart;

@@ -1,10 +1,11 @@
 // Host helpers of the tensor-core path: TMA tensor-map encoding (through the
-// driver entry point, so the library does not link libcuda directly) and the
-// SM count of the current device.
+// driver entry point, so the library does not link libcuda directly) with a
+// cache of encoded maps, and the SM count of the current device.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <cstring>
 #include <mutex>
 
 #include "tc_host.h"
@@ -18,6 +19,34 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 constexpr int kMaxDevices = 64;
 std::mutex g_sm_mu;
 int g_sms[kMaxDevices] = {};
+
+// Encoded maps keyed by everything the encoding reads (base address, rank,
+// extents, strides, box, element type, swizzle): a map is a pure function of
+// its key, so a hit is always valid, whatever happened to the memory in
+// between.  A call encodes up to a dozen maps; a repeated call with the same
+// buffers finds them here instead of re-encoding them.  Direct-mapped.
+struct MapKey {
+  const void* base;
+  uint64_t dims[5], strides[4];
+  uint32_t box[5];
+  int rank, f16, swizzle;
+};
+struct MapEntry {
+  bool used;
+  MapKey key;
+  CUtensorMap map;
+};
+constexpr int kMapCache = 512;
+std::mutex g_map_mu;
+MapEntry g_maps[kMapCache];
+
+uint64_t key_hash(const MapKey& k) {
+  // FNV-1a over the key's bytes
+  const unsigned char* b = reinterpret_cast<const unsigned char*>(&k);
+  uint64_t h = 1469598103934665603ull;
+  for (size_t i = 0; i < sizeof(MapKey); ++i) h = (h ^ b[i]) * 1099511628211ull;
+  return h;
+}
 
 }  // namespace
 
@@ -48,6 +77,25 @@ int encode_impl(CUtensorMap* map, const void* base, int rank, const uint64_t* di
       g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   });
   if (!g_encode) return (int)cudaErrorNotSupported;
+  MapKey key;
+  std::memset(&key, 0, sizeof(key));  // padding bytes take part in the hash and the comparison
+  key.base = base;
+  key.rank = rank;
+  key.f16 = f16 ? 1 : 0;
+  key.swizzle = swizzle ? 1 : 0;
+  for (int i = 0; i < rank; ++i) {
+    key.dims[i] = dims[i];
+    key.box[i] = box[i];
+    if (i + 1 < rank) key.strides[i] = strides_bytes[i];
+  }
+  MapEntry& slot = g_maps[key_hash(key) % kMapCache];
+  {
+    std::lock_guard<std::mutex> lock(g_map_mu);
+    if (slot.used && std::memcmp(&slot.key, &key, sizeof(key)) == 0) {
+      *map = slot.map;
+      return 0;
+    }
+  }
   cuuint64_t gdim[5];
   cuuint64_t gstride[4];
   cuuint32_t bdim[5];
@@ -62,7 +110,12 @@ int encode_impl(CUtensorMap* map, const void* base, int rank, const uint64_t* di
                         gstride, bdim, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? 0 : (int)cudaErrorInvalidValue;
+  if (r != CUDA_SUCCESS) return (int)cudaErrorInvalidValue;
+  std::lock_guard<std::mutex> lock(g_map_mu);
+  slot.used = true;
+  slot.key = key;
+  slot.map = *map;
+  return 0;
 }
 }  // namespace
 
@@ -101,6 +154,47 @@ ChunkShape choose_chunk(const Plan& p) {
   c.rows = c.ct * c.ch * c.cw;
   c.rows_pad = (c.rows + 15) / 16 * 16;
   return c;
+}
+
+// Kernels whose shared-memory limit has been raised, per current context
+// (a device reset or another context starts afresh).  The context is read
+// through the driver entry point, like the tensor-map encoder.
+int set_max_dynamic_smem(const void* kernel, int bytes) {
+  struct Done {
+    const void* kernel;
+    CUcontext ctx;
+    int bytes;
+  };
+  static std::once_flag once;
+  static PFN_cuCtxGetCurrent_v4000 get_ctx = nullptr;
+  static std::mutex mu;
+  static Done done[256];
+  static int n_done = 0;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_ctx = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+  });
+  // no current context yet: the runtime call creates the primary one
+  CUcontext ctx = nullptr;
+  if (!get_ctx || get_ctx(&ctx) != CUDA_SUCCESS || !ctx)
+    return (int)cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  std::lock_guard<std::mutex> lock(mu);
+  int slot = -1;
+  for (int i = 0; i < n_done; ++i) {
+    if (done[i].kernel == kernel && done[i].ctx == ctx) {
+      if (done[i].bytes >= bytes) return 0;
+      slot = i;
+      break;
+    }
+  }
+  const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return (int)e;
+  if (slot < 0) slot = n_done < 256 ? n_done++ : (int)(((uintptr_t)kernel >> 4) % 256);
+  done[slot] = Done{kernel, ctx, bytes};
+  return 0;
 }
 
 int num_sms() {
