@@ -615,7 +615,7 @@ def run_backward(args, w: wl.Workload, world: int, rank: int, local: int, dist):
     K = args.steps
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    sampler = ClockSampler(local) if rank == 0 and sample_clocks else None
+    sampler = ClockSampler(local) if rank == 0 else None
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
@@ -715,6 +715,7 @@ def run_backward(args, w: wl.Workload, world: int, rank: int, local: int, dist):
                           "frac": max(t_hbm, t_tc) / (ms_per_step / 1e3)},
         "phase_ms": avg_phase,
         "gpu_launches": BWD_LAUNCHES[path] * K,
+        "host_us_per_call": host_s / K * 1e6,
         "clocks": clocks,
         "e2e": {"value": w.units * w.n_tokens * E / (te1 - te0), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": E, "ms_per_step": (te1 - te0) * 1e3 / E},

@@ -65,6 +65,8 @@ __global__ void __launch_bounds__(kThreads) tc_mixs_kernel(const Plan p, int Q, 
   float a0[kSmallMixMaxM], a1[kSmallMixMaxM];
 #pragma unroll
   for (int i = 0; i < kSmallMixMaxM; ++i) a0[i] = a1[i] = 0.f;
+  // unrolled so that the loads of several records are in flight together
+#pragma unroll 8
   for (int q = 0; q < Q; ++q) {
     const size_t off = ((size_t)u * Q + q) * R + r;
     float x0, x1;
