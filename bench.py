@@ -517,6 +517,13 @@ BWD_PHASE_KERNEL = {
         "mc": ("bwd_mc_kernel", "token_level_head_phi_gb300/csrc/backward.cu", "alu"),
         "summary": ("bwd_summary_kernel", "token_level_head_phi_gb300/csrc/backward.cu", "alu"),
     },
+    "simt_causal": {
+        "recompute": ("simt_summary_kernel", "token_level_head_phi_gb300/csrc/simt.cu", "alu"),
+        "output": ("causal_bwd_fwd_kernel", "token_level_head_phi_gb300/csrc/simt_causal_bwd.cu", "alu"),
+        "mix": ("bwd_mix_kernel", "token_level_head_phi_gb300/csrc/backward.cu", "alu"),
+        "mc": ("bwd_mc_kernel", "token_level_head_phi_gb300/csrc/backward.cu", "alu"),
+        "summary": ("bwd_summary_kernel", "token_level_head_phi_gb300/csrc/backward.cu", "alu"),
+    },
     "tc": {
         "recompute": ("tc_summary_kernel", "token_level_head_phi_gb300/csrc/tc_summary.cu", "tensor"),
         "output": ("tc_bwd_output_kernel", "token_level_head_phi_gb300/csrc/tc_bwd_output.cu", "tensor"),
@@ -525,16 +532,19 @@ BWD_PHASE_KERNEL = {
         "summary": ("tc_bwd_summary_kernel", "token_level_head_phi_gb300/csrc/tc_bwd_summary.cu", "tensor"),
     },
 }
-BWD_LAUNCHES = {"simt": 7, "tc": 10}
+BWD_LAUNCHES = {"simt": 7, "simt_causal": 9, "tc": 10}
 FP32_LANES_PER_SM = 128  # FP32 FMA lanes per SM (4 partitions x 32)
 SM_COUNT = 152
 
 
-def bwd_phase_cost(w: wl.Workload, splits: int):
+def bwd_phase_cost(w: wl.Workload, splits: int, causal: bool = False):
     """Compulsory bytes and dense FLOPs of each backward phase.  Records take
     4 bytes per entry on both paths (float32, or bf16 high + low planes); the
     FLOPs are those of the float32 contractions (the tensor cores run each
-    split product three times)."""
+    split product three times).  Causal form: the in-block step reads Q, K, V,
+    dO and the prefix records and writes dQ, and runs the per-token state
+    products forwards and backwards (16 d^2 FLOPs per token); the summary
+    step also reads the in-block parts of dK, dV (float32)."""
     el = 2 if w.dtype == "bf16" else 4
     U, N, d, M = w.units, w.n_tokens, w.head_dim, w.n_blocks
     R = d * d + 2 * d
@@ -542,13 +552,17 @@ def bwd_phase_cost(w: wl.Workload, splits: int):
     io = U * N * d * el
     stack, mixed, mc = U * Q * R * 4, U * M * R * 4, 4 * M * M
     nd2, m2 = U * N * d * d, U * M * M * d * d
-    return {
+    cost = {
         "recompute": (2 * io + 2 * stack + mixed + mc, 2 * nd2 + 2 * U * M * Q * R),
         "output": (2 * io + mixed + io + stack, 6 * nd2),
         "mix": (stack + mixed + mc, 2 * U * M * Q * R),
         "mc": (2 * stack + mc, 2 * U * Q * Q * R),
         "summary": (2 * io + mixed + 2 * io, 4 * nd2),
     }
+    if causal:
+        cost["output"] = (5 * io + mixed, 16 * nd2)
+        cost["summary"] = (2 * io + mixed + 2 * io + 2 * U * N * d * 4, 4 * nd2)
+    return cost
 
 
 def run_backward(args, w: wl.Workload, world: int, rank: int, local: int, dist):
@@ -587,9 +601,11 @@ def run_backward(args, w: wl.Workload, world: int, rank: int, local: int, dist):
     dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
     dmc = torch.empty_like(mc)
     path = "tc" if (w.dtype == "bf16" and w.head_dim == 64 and args.variant != "simt") else "simt"
-    variant = "simt" if path == "simt" else "auto"
+    if args.causal:
+        path = "simt_causal"  # the causal form's gradients run on the CUDA cores
+    variant = "auto" if path == "tc" else "simt"
     p = mb.make_params(w.batch, w.heads, w.head_dim, w.grid, w.block, w.dtype, args.feature_map, w.norm, variant,
-                       False, args.layout, args.mc_per_head)
+                       bool(args.causal), args.layout, args.mc_per_head)
     splits = mb.mhla_plan(mb.make_params(w.batch, w.heads, w.head_dim, w.grid, w.block, w.dtype, args.feature_map, w.norm,
                                          "multipass" if path == "tc" else "simt")).summary_splits
     need = mb.mhla_backward_workspace_bytes(p)
@@ -656,7 +672,7 @@ def run_backward(args, w: wl.Workload, world: int, rank: int, local: int, dist):
     ms_per_step = max_ms / K
 
     hbm, tf_burst, tf_sust, peak_kind = load_peaks()
-    cost = bwd_phase_cost(w, splits)
+    cost = bwd_phase_cost(w, splits, bool(args.causal))
     dom = max(avg_phase, key=avg_phase.get)
     kname, ksrc, engine = BWD_PHASE_KERNEL[path][dom]
     nbytes, nflops = cost[dom]
@@ -704,7 +720,7 @@ def run_backward(args, w: wl.Workload, world: int, rank: int, local: int, dist):
         "dtype": "bf16" if path == "tc" else "f32",
         "data": "synthetic (seeded normals, locality-biased Mc, seeded normal dO)",
         "config": dict(wl.describe(w), pass_="backward", feature_map=args.feature_map, layout=args.layout,
-                       mc_per_head=bool(args.mc_per_head),
+                       mc_per_head=bool(args.mc_per_head), causal=bool(args.causal),
                        input_dtype=w.dtype,
                        path="tensor cores (split bf16)" if path == "tc" else "CUDA cores (float32)",
                        l2="no flush: inputs exceed L2" if flush is None else "L2 flushed (256 MB write) between steps, outside per-step events",
@@ -730,9 +746,12 @@ sys.path.insert(0, {root!r})
 from token_level_head_phi_gb300 import workloads as wl
 from oracle import mhla_oracle as orc
 from oracle import mhla_backward_oracle as orb
+from oracle import mhla_causal_oracle as oca
+from oracle import mhla_causal_backward_oracle as ocb
 w = wl.WORKLOADS[{name!r}]
 mc = wl.make_mc(w)
 budget, max_units, per_step, backward, fmap = {budget}, {max_units}, {per_step}, {backward}, {fmap!r}
+causal = {causal}
 times = []
 units = 0
 t_all = time.perf_counter()
@@ -742,9 +761,10 @@ for step in range(max_units):
     g = wl.head_output_grad(w, u) if backward else None
     t0 = time.perf_counter()
     if backward:
-        orb.mhla_head_backward64(q, k, v, mc, w.grid, w.block, g, fmap, w.norm)
+        (ocb.mhla_causal_head_backward64 if causal else orb.mhla_head_backward64)(q, k, v, mc, w.grid, w.block, g,
+                                                                                 fmap, w.norm)
     else:
-        orc.mhla_head64(q, k, v, mc, w.grid, w.block, fmap, w.norm)
+        (oca.mhla_causal_head64 if causal else orc.mhla_head64)(q, k, v, mc, w.grid, w.block, fmap, w.norm)
     times.append(time.perf_counter() - t0)
     units += 1
     if not per_step and sum(times) >= budget:
@@ -754,14 +774,14 @@ print(json.dumps({{"times": times, "units": units}}))
 
 
 def oracle_run(w: wl.Workload, budget_s: float, max_units: int, per_step: bool, backward: bool = False,
-               fmap: str = "elu1"):
+               fmap: str = "elu1", causal: bool = False):
     """Runs the oracle in a fresh process (BLAS threads = available cores)."""
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
     env = dict(os.environ)
     for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
         env[var] = str(cores)
     code = ORACLE_SNIPPET.format(root=ROOT, name=w.name, budget=budget_s, max_units=max_units, per_step=per_step,
-                               backward=backward, fmap=fmap)
+                               backward=backward, fmap=fmap, causal=causal)
     res = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=1800)
     if res.returncode != 0:
         raise RuntimeError(f"oracle run failed: {res.stderr[-2000:]}")
@@ -769,10 +789,12 @@ def oracle_run(w: wl.Workload, budget_s: float, max_units: int, per_step: bool, 
     return d["times"], d["units"], cores
 
 
-def cpu_baseline(w: wl.Workload, budget_s: float = 15.0, backward: bool = False, fmap: str = "elu1"):
-    times, units, cores = oracle_run(w, budget_s, max_units=10 ** 6, per_step=False, backward=backward, fmap=fmap)
+def cpu_baseline(w: wl.Workload, budget_s: float = 15.0, backward: bool = False, fmap: str = "elu1",
+                 causal: bool = False):
+    times, units, cores = oracle_run(w, budget_s, max_units=10 ** 6, per_step=False, backward=backward, fmap=fmap,
+                                     causal=causal)
     total = sum(times)
-    what = "backward" if backward else "forward"
+    what = ("causal " if causal else "") + ("backward" if backward else "forward")
     return {"value": units * w.n_tokens / total, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"{units} of {w.units} (batch, head) units of {w.name}, float64 NumPy {what} oracle, "
                       f"{total:.1f} s of CPU time; input generation excluded"}
@@ -783,7 +805,7 @@ def run_reference(args, w: wl.Workload):
     K, W = args.steps, args.warmup
     backward = getattr(args, "pass_", "forward") == "backward"
     times, units, cores = oracle_run(w, 0.0, max_units=W + K, per_step=True, backward=backward,
-                                     fmap=getattr(args, "feature_map", "elu1"))
+                                     fmap=getattr(args, "feature_map", "elu1"), causal=bool(getattr(args, "causal", 0)))
     timed = times[W:W + K]
     total = sum(timed)
     value = K * w.n_tokens / total
@@ -813,7 +835,7 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--pass", dest="pass_", default="forward", choices=["forward", "backward"])
     ap.add_argument("--feature-map", default="elu1", choices=["elu1", "relu", "exp"])
-    ap.add_argument("--causal", action="store_true", help="block-ordered causal forward")
+    ap.add_argument("--causal", action="store_true", help="block-ordered causal form (forward or backward)")
     ap.add_argument("--layout", default="bhnd", choices=["bhnd", "bnhd"], help="q/k/v/out memory layout")
     ap.add_argument("--mc-per-head", action="store_true", help="one mixing matrix per head")
     args = ap.parse_args()
@@ -836,7 +858,7 @@ def main():
     if args.pass_ == "backward":
         result = run_backward(args, w, world, rank, local, dist)
         if rank == 0 and not args.no_cpu_baseline:
-            result["cpu_baseline"] = cpu_baseline(w, backward=True, fmap=args.feature_map)
+            result["cpu_baseline"] = cpu_baseline(w, backward=True, fmap=args.feature_map, causal=bool(args.causal))
         if rank == 0:
             print(json.dumps(result), flush=True)
         if dist is not None:
@@ -850,7 +872,7 @@ def main():
     if not args.no_per_config and args.workload == wl.BENCH_WORKLOAD:
         result["per_config"] = run_per_config(args, world, rank, local, dist)
     if rank == 0 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(w, fmap=args.feature_map)
+        result["cpu_baseline"] = cpu_baseline(w, fmap=args.feature_map, causal=bool(args.causal))
     if rank == 0:
         print(json.dumps(result), flush=True)
     if dist is not None:

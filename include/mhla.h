@@ -139,8 +139,8 @@ typedef struct mhla_params {
                      * tokens ordered by (block, position inside the block),
                      * query t sees keys up to itself: earlier blocks through
                      * the strict lower triangle of Mc, its own block through
-                     * Mc[i, i] and only the tokens up to t.  Forward only
-                     * (mhla_backward returns MHLA_ERR_UNSUPPORTED).  AUTO
+                     * Mc[i, i] and only the tokens up to t.  mhla_backward
+                     * runs it on the float32 CUDA-core kernels.  AUTO
                      * takes the tensor cores for bf16, d = 64, DIVISIVE or
                      * NONE when every token chunk is a contiguous run of its
                      * block's local order, else the float32 kernels;
@@ -242,6 +242,10 @@ mhla_status mhla_forward_host(const void* q, const void* k, const void* v, const
  * kernels otherwise; MHLA_VARIANT_SIMT forces the CUDA-core kernels;
  * MULTIPASS and FUSED ask for the tensor cores (MHLA_ERR_UNSUPPORTED where
  * they do not apply).  The forward summaries are recomputed inside the call.
+ * p->causal = 1 differentiates the block-ordered causal form on the CUDA
+ * cores (AUTO or SIMT; MULTIPASS and FUSED return MHLA_ERR_UNSUPPORTED):
+ * Mc above its diagonal does not enter that output, and its dmc entries
+ * are 0.
  *   dout, dq, dk, dv: [B, H, N, d] in p->dtype, like q; dmc: float32 [M, M],
  *   overwritten with the sum over every (batch, head).
  * Device pointers, 16-byte aligned (mc, dmc 4-byte); dq, dk, dv, dmc must

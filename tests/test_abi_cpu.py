@@ -288,8 +288,14 @@ def test_causal_plan_and_rejections(lib):
     for variant, norm in (("fused", "divisive"), ("multipass", "mala")):
         bad = mb.make_params(w.batch, w.heads, w.head_dim, w.grid, w.block, norm=norm, variant=variant, causal=True)
         assert lib.mhla_plan(ctypes.byref(bad), ctypes.byref(mb.MhlaPlanInfo())) == mb.MHLA_ERR_UNSUPPORTED
+    # the causal backward runs on the CUDA cores: AUTO and SIMT plan it,
+    # the tensor-core variants are refused
     n = ctypes.c_size_t(0)
-    assert lib.mhla_backward_workspace_bytes(ctypes.byref(p), ctypes.byref(n)) == mb.MHLA_ERR_UNSUPPORTED
+    assert lib.mhla_backward_workspace_bytes(ctypes.byref(p), ctypes.byref(n)) == mb.MHLA_OK and n.value > 0
+    for variant in ("simt", "multipass", "fused"):
+        bq = mb.make_params(w.batch, w.heads, w.head_dim, w.grid, w.block, variant=variant, causal=True)
+        want = mb.MHLA_OK if variant == "simt" else mb.MHLA_ERR_UNSUPPORTED
+        assert lib.mhla_backward_workspace_bytes(ctypes.byref(bq), ctypes.byref(n)) == want
     p.causal = 2
     assert lib.mhla_plan(ctypes.byref(p), ctypes.byref(mb.MhlaPlanInfo())) == mb.MHLA_ERR_INVALID_ARG
 

@@ -242,17 +242,18 @@ def mhla_backward_workspace_bytes(p: MhlaParams) -> int:
 
 def mhla_backward(q, k, v, mc, dout, grid, block, norm: str = "divisive", feature_map: str = "elu1",
                   dq=None, dk=None, dv=None, dmc=None, workspace=None, stream=None, variant: str = "auto",
-                  layout: str = "bhnd"):
+                  layout: str = "bhnd", causal: bool = False):
     """Gradients of sum(dout * mhla_forward(q, k, v, mc)): returns (dq, dk, dv, dmc).
 
     dq, dk, dv are shaped and typed like q; dmc is float32 [M, M] (summed
     over every batch and head).  Outputs and workspace are allocated with
     torch when not given; enqueued on ``stream`` without synchronising.
     ``variant``: "auto" (tensor cores for bf16 with d = 64, else float32 CUDA
-    cores) or "simt" (float32 CUDA cores).
+    cores) or "simt" (float32 CUDA cores).  ``causal``: the block-ordered
+    causal form (float32 CUDA cores).
     """
     import torch
-    p = _params_for(q, grid, block, feature_map, norm, variant, False, layout)
+    p = _params_for(q, grid, block, feature_map, norm, variant, causal, layout)
     for name, t in (("q", q), ("k", k), ("v", v), ("dout", dout)):
         if not t.is_cuda or not t.is_contiguous() or t.shape != q.shape or t.dtype != q.dtype:
             raise ValueError(f"{name} must be a contiguous CUDA tensor shaped and typed like q")

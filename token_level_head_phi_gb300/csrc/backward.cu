@@ -235,9 +235,12 @@ bwd_mix_kernel(Plan p, const float* __restrict__ mc, const float* __restrict__ d
 // row cancel to a small fraction of their size, and one running float32
 // sum over all d^2 + 2d entries of every head would carry a rounding error
 // proportional to that count.
+// Causal form (diag set): only b < i comes from the prefix partials; the
+// diagonal is the sum of the in-block terms, and above it Mc does not enter
+// the output (0).
 __global__ void __launch_bounds__(kThreads)
 bwd_mc_kernel(Plan p, const float* __restrict__ dmixp, const float* __restrict__ stack,
-              const float* __restrict__ dnp, float* __restrict__ dmc) {
+              const float* __restrict__ dnp, const float* __restrict__ diag, float* __restrict__ dmc) {
   constexpr int TI = 16, TK = 32;
   __shared__ float sa[TI][TK + 1];
   __shared__ float sb[TI][TK + 1];
@@ -274,7 +277,12 @@ bwd_mc_kernel(Plan p, const float* __restrict__ dmixp, const float* __restrict__
     acc += acc_u;
   }
   const int i = i0 + ti, b = b0 + tb;
-  if (i < p.M && b < p.M) {
+  if (diag && i < p.M && b < p.M && b >= i) {
+    float t = 0.f;
+    if (b == i)
+      for (int u = h; u < p.BH; u += ustep) t += diag[(size_t)u * p.M + i];
+    dmc[((size_t)h * p.M + i) * p.M + b] = t;
+  } else if (i < p.M && b < p.M) {
     if (p.norm == MHLA_NORM_MALA) {
       float dn = 0.f;
       for (int u = h; u < p.BH; u += ustep)
@@ -286,11 +294,13 @@ bwd_mc_kernel(Plan p, const float* __restrict__ dmixp, const float* __restrict__
 }
 
 // One CTA per (summary block piece, head): dS_b, dz_b, dv_b in shared memory;
-// dk_j = (dS_b v_j + dz_b) * phi'(k_j), dv_j = dS_b^T phi(k_j) + dv_b.
+// dk_j = (dS_b v_j + dz_b) * phi'(k_j), dv_j = dS_b^T phi(k_j) + dv_b (the
+// causal form adds the in-block parts xk, xv before phi').
 template <int D, typename T>
 __global__ void __launch_bounds__(kThreads)
 bwd_summary_kernel(Plan p, const T* __restrict__ K, const T* __restrict__ V, const float* __restrict__ dstack,
-                   T* __restrict__ dK, T* __restrict__ dV) {
+                   const float* __restrict__ xk, const float* __restrict__ xv, T* __restrict__ dK,
+                   T* __restrict__ dV) {
   extern __shared__ float sm[];
   float* sS = sm;                  // D*D
   float* sz = sS + D * D;          // D
@@ -328,6 +338,10 @@ bwd_summary_kernel(Plan p, const T* __restrict__ K, const T* __restrict__ V, con
         gv = fmaf(sS[m * D + f], sk[tt * D + m], gv);   // (dS_b^T phi(k_j))[f]
       }
       const size_t off = tok_off(p, u, block_token(p, b, lt + tt)) + f;
+      if (xk) {
+        gk += xk[off];
+        gv += xv[off];
+      }
       dK[off] = from_f32<T>(gk * phi_grad(to_f32(K[off]), p.fmap));
       dV[off] = from_f32<T>(gv);
     }
@@ -352,7 +366,8 @@ int run_summary(const Plan& p, const BwdBuffers& w, const void* k, const void* v
   auto ks = bwd_summary_kernel<D, T>;
   cudaError_t e = (cudaError_t)set_max_dynamic_smem((const void*)ks, (int)sms);
   if (e != cudaSuccess) return (int)e;
-  ks<<<dim3(p.M * p.splits, p.BH), kThreads, sms, s>>>(p, (const T*)k, (const T*)v, w.dstack, (T*)dk, (T*)dv);
+  ks<<<dim3(p.M * p.splits, p.BH), kThreads, sms, s>>>(p, (const T*)k, (const T*)v, w.dstack, w.xk, w.xv, (T*)dk,
+                                                       (T*)dv);
   return (int)cudaGetLastError();
 }
 
@@ -395,7 +410,7 @@ int launch_bwd_mix(const Plan& p, const BwdBuffers& w, void* stream) {
 int launch_bwd_mc(const Plan& p, const BwdBuffers& w, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   bwd_mc_kernel<<<dim3((p.M + 15) / 16, (p.M + 15) / 16, p.mc_heads), kThreads, 0, s>>>(p, w.dmixp, w.stack, w.dnp,
-                                                                                        w.dmc);
+                                                                                        w.diag, w.dmc);
   return (int)cudaGetLastError();
 }
 

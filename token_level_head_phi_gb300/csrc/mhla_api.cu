@@ -469,14 +469,19 @@ struct BwdLayout {
   size_t mc_f16, mc_hi, mc_lo, mc_scale, blkinfo, partial;
   size_t mct, mct_f16, mct_hi, mct_lo, mct_scale, mct_rowsum, mct_blkinfo;  // Mc transposed
   size_t dx_hi, dx_lo;                                                      // dS_b, dz_b, dv_b planes
+  size_t mcl, tokbuf, xk, xv, diag;                                         // causal form (CUDA cores)
   size_t total;
 };
 
 mhla_status make_bwd_plan(const mhla_params* prm, Plan* plan, BwdLayout* lay) {
   if (!prm) return MHLA_ERR_INVALID_ARG;
-  if (prm->causal == 1) return MHLA_ERR_UNSUPPORTED;  // forward only
   mhla_params p = *prm;
   const bool tc_ok = p.dtype == MHLA_DTYPE_BF16 && p.head_dim == kTcHeadDim;
+  if (p.causal == 1) {
+    // the causal form's gradients run on the CUDA cores only
+    if (p.variant != MHLA_VARIANT_AUTO && p.variant != MHLA_VARIANT_SIMT) return MHLA_ERR_UNSUPPORTED;
+    p.variant = MHLA_VARIANT_SIMT;
+  }
   if (p.variant == MHLA_VARIANT_AUTO) p.variant = tc_ok ? MHLA_VARIANT_MULTIPASS : MHLA_VARIANT_SIMT;
   if (p.variant == MHLA_VARIANT_FUSED) p.variant = MHLA_VARIANT_MULTIPASS;
   mhla_status st = make_plan(&p, plan);
@@ -499,6 +504,14 @@ mhla_status make_bwd_plan(const mhla_params* prm, Plan* plan, BwdLayout* lay) {
     take(lay->mixed, sizeof(float) * mrows * R);
     take(lay->dmixp, sizeof(float) * rows * R);
     take(lay->dstack, sizeof(float) * mrows * R);
+    if (plan->causal) {
+      const size_t toks = (size_t)plan->BH * plan->N;
+      take(lay->mcl, sizeof(float) * (size_t)plan->M * plan->M * mh);
+      take(lay->tokbuf, sizeof(float) * toks * (plan->d + 2));
+      take(lay->xk, sizeof(float) * toks * plan->d);
+      take(lay->xv, sizeof(float) * toks * plan->d);
+      take(lay->diag, sizeof(float) * mrows);
+    }
   } else {
     take(lay->stack_hi, 2 * rows * R);
     take(lay->stack_lo, 2 * rows * R);
@@ -543,6 +556,9 @@ int run_backward(const Plan& plan, const BwdLayout& lay, const void* q, const vo
   w.dnp = F(lay.dnp);
   w.dstack = F(lay.dstack);
   w.dmc = dmc;
+  w.diag = nullptr;
+  w.xk = nullptr;
+  w.xv = nullptr;
   int e;
   record_bwd_event(0, s);
   if (lay.tc) {
@@ -600,6 +616,39 @@ int run_backward(const Plan& plan, const BwdLayout& lay, const void* q, const vo
       return e;
     record_bwd_event(4, s);
     if ((e = launch_tc_bwd_summary(p, k, v, H(lay.dx_hi), H(lay.dx_lo), dk, dv, s)) != 0) return e;
+    record_bwd_event(5, s);
+    return 0;
+  }
+  if (p.causal) {
+    // earlier blocks through Mc's strict lower triangle, the own block token
+    // by token through its diagonal
+    float* mcl = F(lay.mcl);
+    if ((e = launch_mc_strict_lower(p, mc, mcl, s)) != 0) return e;
+    if ((e = launch_mc_rowsum(p, mcl, w.rowsum, s)) != 0) return e;
+    if ((e = launch_simt_summary(p, k, v, w.stack, s)) != 0) return e;
+    if ((e = launch_simt_mix(p, mcl, w.stack, w.mixed, s)) != 0) return e;
+    record_bwd_event(1, s);
+    CausalBwdBuffers c;
+    c.mc = mc;
+    c.mixed = w.mixed;
+    c.rowsum_lower = w.rowsum;
+    c.dmixp = w.dmixp;
+    c.dnp = w.dnp;
+    c.diag = F(lay.diag);
+    c.tokbuf = F(lay.tokbuf);
+    c.xk = F(lay.xk);
+    c.xv = F(lay.xv);
+    if ((e = launch_bwd_causal_block(p, c, q, k, v, dout, dq, s)) != 0) return e;
+    record_bwd_event(2, s);
+    w.mc = mcl;
+    w.diag = c.diag;
+    w.xk = c.xk;
+    w.xv = c.xv;
+    if ((e = launch_bwd_mix(p, w, s)) != 0) return e;
+    record_bwd_event(3, s);
+    if ((e = launch_bwd_mc(p, w, s)) != 0) return e;
+    record_bwd_event(4, s);
+    if ((e = launch_bwd_summary(p, w, k, v, dk, dv, s)) != 0) return e;
     record_bwd_event(5, s);
     return 0;
   }
