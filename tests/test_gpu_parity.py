@@ -96,6 +96,27 @@ def test_edge_shapes(case, norm, variant):
     assert err <= TOL[dtype], f"{case}/{norm}: rel err {err:.3e}"
 
 
+LARGE_M_CASES = [
+    # grid, block, heads: more than 128 query blocks, so the fp16 mixing takes
+    # the streaming tensor-core kernel (256 query blocks per tile)
+    ((1, 1, 2304), (1, 1, 16), 3),      # M = 144: one tile of 256 query blocks, 112 of them padding; Q % 64 = 16
+    ((1, 1, 8192), (1, 1, 32), 2),      # M = 256: one full tile
+    ((1, 1, 4160), (1, 1, 8), 1),       # M = 520: three 256-block tiles, the last with 8 rows
+    ((1, 96, 96), (1, 6, 6), 2),        # 2D, M = 256, 36-token blocks
+    ((4, 48, 48), (2, 4, 4), 1),        # 3D, M = 288
+]
+
+
+@pytest.mark.parametrize("norm", ["divisive", "none"])
+@pytest.mark.parametrize("case", LARGE_M_CASES, ids=lambda c: f"{c[0]}-{c[1]}-h{c[2]}")
+def test_large_m_mixing_shapes(case, norm):
+    grid, block, heads = case
+    w = wl.random_small(zlib.crc32(repr(case).encode()) % 10000, grid, block, 64, 1, heads, "bf16")
+    assert w.n_blocks > 128
+    err = parity(w, norm, "multipass")
+    assert err <= TOL["bf16"], f"{case}/{norm}: rel err {err:.3e}"
+
+
 @pytest.mark.parametrize("variant", VARIANTS)
 def test_mc_with_zero_entries(variant):
     w = wl.random_small(5, (1, 16, 16), (1, 4, 4), 64, 2, 2, "bf16")
