@@ -165,6 +165,14 @@ __device__ __forceinline__ void mix_body(const MixArgs& a, const Plan& p, const 
       // --------------------------------------------------------------- MMA
       const uint32_t idesc = kF16 ? idesc_f16_f32(128, a.NT, true, false) : idesc_bf16_f32(128, a.NT, true, false);
       const uint32_t idesc2 = idesc_bf16_f32(128, 2 * a.NT, true, false);  // split: Xh [Mh | Ml]
+      // Descriptors of stage 0, advanced by adding byte offset / 16 to their
+      // address field (the shared memory window is below 256 KB, so the
+      // field never carries): the issue of each MMA waits for the tensor
+      // pipe, so every instruction on this thread adds to the step time.
+      const uint64_t ad0 = sdesc_sw128(base, kAtom, 1024u);
+      const uint64_t bd0 = sdesc_sw128(base + a.off_b, 0u, 1024u);
+      const uint64_t ld0 = sdesc_sw128(base + a.off_alo, kAtom, 1024u);
+      const uint32_t sstep = a.stage_bytes >> 4;
       int stage = 0, acc = 0;
       uint32_t phase = 0, accph = 0;
       bool ok = true;
@@ -175,19 +183,18 @@ __device__ __forceinline__ void mix_body(const MixArgs& a, const Plan& p, const 
         for (int kc = 0; kc < a.kchunks; ++kc) {
           if (!(ok = mbar_wait(full(stage), phase, a.err, 0x203, abort_flag))) break;
           tc_fence_after();
-          const uint32_t st = base + (uint32_t)stage * a.stage_bytes;
+          const uint64_t so = (uint64_t)((uint32_t)stage * sstep);
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) {
-            const uint64_t ahi = sdesc_sw128(st + (uint32_t)ks * 2048u, kAtom, 1024u);
-            const uint64_t bhi = sdesc_sw128(st + a.off_b + (uint32_t)ks * 32u, 0u, 1024u);
+            const uint64_t ahi = ad0 + so + 128 * ks;  // + 2048 bytes per K step
+            const uint64_t bhi = bd0 + so + 2 * ks;    // + 32 bytes per K step
             const uint32_t accum = (kc > 0 || ks > 0) ? 1u : 0u;
             if (kF16) {
               umma_bf16(d, ahi, bhi, idesc, accum);
             } else {
               // the B descriptor at Mh spans Ml too (off_blo = off_b + NT rows)
-              const uint64_t alo = sdesc_sw128(st + a.off_alo + (uint32_t)ks * 2048u, kAtom, 1024u);
               umma_bf16(d, ahi, bhi, idesc2, accum);
-              umma_bf16(d, alo, bhi, idesc, 1u);
+              umma_bf16(d, ld0 + so + 128 * ks, bhi, idesc, 1u);
             }
           }
           umma_commit(empty(stage));

@@ -148,6 +148,11 @@ __device__ __forceinline__ void mixt_body(const MixTArgs& a, const Plan& p) {
     if (lane == 0) {
       // --------------------------------------------------------------- MMA
       const uint32_t idesc = idesc_f16_f32(128, 128, false, true);
+      // stage 0's B descriptor, advanced by adding byte offset / 16 to its
+      // address field (the issue of each MMA waits for the tensor pipe, so
+      // every instruction on this thread adds to the step time)
+      const uint64_t bd0 = sdesc_sw128(base, kAtom, 1024u);
+      const uint32_t sstep = a.stage_bytes >> 4;
       int stage = 0, acc = 0, cur_u = -1;
       uint32_t phase = 0, accph = 0, loads = 0;
       bool ok = true;
@@ -167,13 +172,12 @@ __device__ __forceinline__ void mixt_body(const MixTArgs& a, const Plan& p) {
         for (int kc = 0; kc < a.kchunks; ++kc) {
           if (!(ok = mbar_wait(full(stage), phase, a.err, 0x215, abort_flag))) break;
           tc_fence_after();
-          const uint32_t st = base + (uint32_t)stage * a.stage_bytes;
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks) {
-            const uint32_t acol = (uint32_t)(kc * 32 + ks * 8);
-            const uint64_t bhi = sdesc_sw128(st + (uint32_t)ks * 2048u, kAtom, 1024u);
-            umma_tmem_a(d, a_base + acol, bhi, idesc, (kc > 0 || ks > 0) ? 1u : 0u);
-          }
+          const uint64_t bd = bd0 + (uint64_t)((uint32_t)stage * sstep);
+          const uint32_t ac = a_base + (uint32_t)kc * 32u;
+          umma_tmem_a(d, ac, bd, idesc, kc > 0 ? 1u : 0u);
+          umma_tmem_a(d, ac + 8u, bd + 128, idesc, 1u);
+          umma_tmem_a(d, ac + 16u, bd + 256, idesc, 1u);
+          umma_tmem_a(d, ac + 24u, bd + 384, idesc, 1u);
           umma_commit(empty(stage));
           if (++stage == kStages) {
             stage = 0;

@@ -284,15 +284,22 @@ __device__ __forceinline__ void output_body(const OutArgs& a, const Plan& p, con
         tc_fence_after();
         const uint32_t qs = qst(s), bs = bst(b);
         const uint32_t d = tmem + (uint32_t)slot * kAccStride;
+        // descriptors of K step 0, advanced by adding byte offset / 16 to the
+        // address field (the issue of each MMA waits for the tensor pipe, so
+        // every instruction on this thread adds to the tile's time)
+        const uint64_t ad0 = sdesc_sw128(qs, 0u, 1024u);
+        const uint64_t bd0 = sdesc_sw128(bs, L::kOffZ, 1024u);
+        const uint64_t bl0 = sdesc_sw128(bs + L::kOffBlo, kBTile, 1024u);
+        const uint64_t ql0 = sdesc_sw128(kQLo ? qlo(lj) : qs, 0u, 1024u);
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
-          const uint64_t ad = sdesc_sw128(qs + (uint32_t)ks * 32u, 0u, 1024u);
-          const uint64_t bd = sdesc_sw128(bs + (uint32_t)ks * 2048u, L::kOffZ, 1024u);
+          const uint64_t ad = ad0 + 2 * ks;     // + 32 bytes per K step
+          const uint64_t bd = bd0 + 128 * ks;   // + 2048 bytes per K step
           const uint32_t acc = ks > 0 ? 1u : 0u;
           umma_bf16(d, ad, bd, idesc80, acc);
-          if (kLo) umma_bf16(d, ad, sdesc_sw128(bs + L::kOffBlo + (uint32_t)ks * 2048u, kBTile, 1024u), idesc64, 1u);
+          if (kLo) umma_bf16(d, ad, bl0 + 128 * ks, idesc64, 1u);
           // the low residual of phi(Q) times [S~_i | Z]
-          if (kQLo) umma_bf16(d, sdesc_sw128(qlo(lj) + (uint32_t)ks * 32u, 0u, 1024u), bd, idesc80, 1u);
+          if (kQLo) umma_bf16(d, ql0 + 2 * ks, bd, idesc80, 1u);
         }
         if (kQLo) {
           umma_commit(lofree(lj));
