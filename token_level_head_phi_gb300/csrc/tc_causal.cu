@@ -287,6 +287,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_causal_kernel(const __grid_con
       const uint32_t id_v = idesc_bf16_f32(128, 80, false, true);
       const uint32_t id_u = idesc_bf16_f32(128, 80, true, true);
       const uint32_t e0 = base + kOffE0;
+      // Descriptors are formed once per group and advanced by adding to their
+      // fields: the address field (byte offset / 16) and, for the operands
+      // whose second atom is the ones tile e0, the leading offset field
+      // (bits 16..29), which shrinks by as much as the address grows.  The
+      // issue of each MMA waits for the tensor pipe, so every instruction on
+      // this thread adds to the chunk's time.
+      const uint64_t e_step = 128ull - (128ull << 16);  // + 2048 bytes, leading offset - 2048 bytes
       long long nupd0 = 0, nupd1 = 0, nu = 0;
       long long qn0 = 0, qn1 = 0;   // chunks waiting for their second group (oldest first)
       bool qm0 = false, qm1 = false;
@@ -304,16 +311,17 @@ __global__ void __launch_bounds__(kThreads, 1) tc_causal_kernel(const __grid_con
           const int ps = (int)(qn0 % kStages);
           const uint32_t k_s = tst(ps) + kTile, v_s = tst(ps) + 2 * kTile;
           const uint32_t DA = tmem + col_a((int)(qn0 & 1));
+          const uint64_t vd0 = sdesc_sw128(v_s, e0 - v_s, 1024u);
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            const uint32_t va = v_s + (uint32_t)ks * 2048u;
-            umma_tmem_a(DA, tmem + kColP + (uint32_t)ks * 8u, sdesc_sw128(va, e0 - va, 1024u), id_v, 1u);
-          }
+          for (int ks = 0; ks < 8; ++ks)
+            umma_tmem_a(DA, tmem + kColP + (uint32_t)ks * 8u, vd0 + (uint64_t)ks * e_step, id_v, 1u);
           if (qm0) {
+            const uint64_t fd0 = sdesc_sw128(k_s, e0 - k_s, 1024u);
+            uint64_t fd = fd0, vd = vd0;
             for (int kt = 0; kt < rows_pad / 16; ++kt) {
-              const uint32_t fa = k_s + (uint32_t)kt * 2048u, va = v_s + (uint32_t)kt * 2048u;
-              umma_bf16(tmem + kColU, sdesc_sw128(fa, e0 - fa, 1024u), sdesc_sw128(va, e0 - va, 1024u), id_u,
-                        kt > 0 ? 1u : 0u);
+              umma_bf16(tmem + kColU, fd, vd, id_u, kt > 0 ? 1u : 0u);
+              fd += e_step;
+              vd += e_step;
             }
             ++nu;
           }
@@ -344,20 +352,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_causal_kernel(const __grid_con
             const uint32_t DA = tmem + col_a(acc);
             // one shape at a time: scores first (the scores epilogue waits
             // for them), then the prefix parts
+            const uint64_t qd = sdesc_sw128(q_s, 0u, 1024u), kd = sdesc_sw128(k_s, 0u, 1024u);
+            const uint64_t shd = sdesc_sw128(sh, 0u, 1024u), sld = sdesc_sw128(sl, 0u, 1024u);
+            const uint64_t zd = sdesc_sw128(zt, 0u, 1024u);
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-              umma_bf16(tmem + kColS, sdesc_sw128(q_s + (uint32_t)ks * 32u, 0u, 1024u),
-                        sdesc_sw128(k_s + (uint32_t)ks * 32u, 0u, 1024u), id_s, ks > 0 ? 1u : 0u);
+            for (int ks = 0; ks < 4; ++ks) umma_bf16(tmem + kColS, qd + 2 * ks, kd + 2 * ks, id_s, ks > 0 ? 1u : 0u);
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-              const uint32_t sp = (ks < 4 ? sh : sl) + (uint32_t)(ks & 3) * 2048u;
-              umma_bf16(DA, sdesc_sw128(q_s + (uint32_t)(ks & 3) * 32u, 0u, 1024u), sdesc_sw128(sp, 0u, 1024u), id_s64,
-                        ks > 0 ? 1u : 0u);
-            }
+            for (int ks = 0; ks < 8; ++ks)
+              umma_bf16(DA, qd + 2 * (ks & 3), (ks < 4 ? shd : sld) + 128 * (ks & 3), id_s64, ks > 0 ? 1u : 0u);
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-              umma_bf16(DA + 64u, sdesc_sw128(q_s + (uint32_t)ks * 32u, 0u, 1024u),
-                        sdesc_sw128(zt + (uint32_t)ks * 32u, 0u, 1024u), id_z, ks > 0 ? 1u : 0u);
+            for (int ks = 0; ks < 4; ++ks) umma_bf16(DA + 64u, qd + 2 * ks, zd + 2 * ks, id_z, ks > 0 ? 1u : 0u);
             umma_commit(sfull);
             if (nx.c + 1 == nck) umma_commit(stfree(x));   // the unit's state buffer is read for the last time
             if (nq == 0) {

@@ -324,15 +324,20 @@ __device__ __forceinline__ void summary_body(const SummaryArgs& a, const Plan& p
           const uint32_t kt = base + (uint32_t)stage * kStageBytes;
           const uint32_t vt = kt + kTile;
           const uint32_t ones = base + L::kOnes;
+          // the second atoms of A and B: the ones tile, whatever the K step.
+          // Descriptors advance by adding to their fields (address + 2048
+          // bytes, leading offset to the ones tile - 2048 bytes per K step):
+          // the issue of each MMA waits for the tensor pipe, so every
+          // instruction on this thread adds to the unit's time.
+          const uint64_t e_step = 128ull - (128ull << 16);
+          uint64_t kd = sdesc_sw128(kt, ones - kt, 1024u), vd = sdesc_sw128(vt, ones - vt, 1024u);
+          uint64_t ld = sdesc_sw128(kt + 2 * kTile, ones - (kt + 2 * kTile), 1024u);
           for (int ks = 0; ks < ksteps; ++ks) {
-            // the second atoms of A and B: the ones tile, whatever the K step
-            const uint32_t ka = kt + (uint32_t)ks * 2048u, va = vt + (uint32_t)ks * 2048u;
-            const uint64_t bd = sdesc_sw128(va, ones - va, 1024u);
-            umma_bf16(d, sdesc_sw128(ka, ones - ka, 1024u), bd, idesc, (c > uc.c0 || ks > 0) ? 1u : 0u);
-            if (kLo) {
-              const uint32_t klo = ka + 2 * kTile;
-              umma_bf16(d, sdesc_sw128(klo, ones - klo, 1024u), bd, idesc, 1u);
-            }
+            umma_bf16(d, kd, vd, idesc, (c > uc.c0 || ks > 0) ? 1u : 0u);
+            if (kLo) umma_bf16(d, ld, vd, idesc, 1u);
+            kd += e_step;
+            vd += e_step;
+            ld += e_step;
           }
           umma_commit(empty(stage));
           ++rk;
