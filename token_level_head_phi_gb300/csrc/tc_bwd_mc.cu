@@ -149,13 +149,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_mc_kernel(const __grid_con
           if (!(ok = mbar_wait(full(s), ph, a.err, 0x604, abort_flag))) break;
           tc_fence_after();
           const uint32_t st = base + (uint32_t)s * kStageBytes;
+          // descriptors of K step 0 advanced by 32 bytes (2 in the address
+          // field) per step: the issuing thread's scalar work adds to every MMA
+          const uint64_t ah0 = sdesc_sw128(st, 0u, 1024u), al0 = sdesc_sw128(st + kTile, 0u, 1024u);
+          const uint64_t bh0 = sdesc_sw128(st + 2 * kTile, 0u, 1024u);   // rows 0..127 hi, 128..255 lo
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) {
-            const uint32_t o = (uint32_t)ks * 32u;
-            const uint64_t ah = sdesc_sw128(st + o, 0u, 1024u), al = sdesc_sw128(st + kTile + o, 0u, 1024u);
-            const uint64_t bh = sdesc_sw128(st + 2 * kTile + o, 0u, 1024u);   // rows 0..127 hi, 128..255 lo
-            umma_bf16(d, ah, bh, idesc2, (kc > 0 || ks > 0) ? 1u : 0u);
-            umma_bf16(d, al, bh, idesc, 1u);
+            umma_bf16(d, ah0 + 2 * ks, bh0 + 2 * ks, idesc2, (kc > 0 || ks > 0) ? 1u : 0u);
+            umma_bf16(d, al0 + 2 * ks, bh0 + 2 * ks, idesc, 1u);
           }
           umma_commit(empty(s));
           if (++s == kStages) {

@@ -307,6 +307,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_output_kernel(const __grid
       const uint32_t id3 = idesc_bf16_f32(128, 64, false, false);
       const uint32_t zero = base + kOffZero;
       const int ksteps2 = rows_pad / 16;
+      // Descriptors are formed once per group and advanced by adding to their
+      // fields (address: byte offset / 16; for operands whose second atom is
+      // the zero tile, the leading offset shrinks as the address grows): the
+      // issue of each MMA waits for the tensor pipe, so every instruction on
+      // this thread adds to the tile's time.
+      const uint64_t e_step = 128ull - (128ull << 16);
       // MMA1 of a tile: D1 = P [S~ | Z]
       auto mma1 = [&](const TileIt& it) -> bool {
         const int s = (int)(it.n % kStages), x = (int)(it.m % kBStages), d = (int)(it.n & 1);
@@ -318,14 +324,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_output_kernel(const __grid
         const uint32_t phi = tst(s), plo = phi + 2 * kTile;
         const uint32_t sh = bst(x), sl = sh + kOffSlo, zt = sh + kOffZ;
         const uint32_t D1 = tmem + col_d1(d);
+        const uint64_t ah0 = sdesc_sw128(phi, 0u, 1024u), al0 = sdesc_sw128(plo, 0u, 1024u);
+        const uint64_t bh0 = sdesc_sw128(sh, zt - sh, 1024u), bl0 = sdesc_sw128(sl, 0u, 1024u);
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
-          const uint64_t ah = sdesc_sw128(phi + (uint32_t)ks * 32u, 0u, 1024u);
-          const uint64_t al = sdesc_sw128(plo + (uint32_t)ks * 32u, 0u, 1024u);
-          const uint64_t bh = sdesc_sw128(sh + (uint32_t)ks * 2048u, zt - sh, 1024u);
+          const uint64_t ah = ah0 + 2 * ks, bh = bh0 + 128 * ks;  // + 32 / + 2048 bytes per K step
           umma_bf16(D1, ah, bh, id1, ks > 0 ? 1u : 0u);
-          umma_bf16(D1, ah, sdesc_sw128(sl + (uint32_t)ks * 2048u, 0u, 1024u), id1s, 1u);
-          umma_bf16(D1, al, bh, id1, 1u);
+          umma_bf16(D1, ah, bl0 + 128 * ks, id1s, 1u);
+          umma_bf16(D1, al0 + 2 * ks, bh, id1, 1u);
         }
         umma_commit(d1full(d));
         return true;
@@ -344,24 +350,27 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_output_kernel(const __grid
         const uint32_t glo = base + kOffGlo + (uint32_t)g * kTile, g2 = base + kOffG2 + (uint32_t)g * kTile;
         const uint32_t sh = bst(x), sl = sh + kOffSlo, zt = sh + kOffZ;
         const uint32_t D2 = tmem + col_d2(d2), D3 = tmem + kColD3;
+        uint64_t aw = sdesc_sw128(phi, g2 - phi, 1024u);    // P hi | G2
+        uint64_t az = sdesc_sw128(plo, zero - plo, 1024u);  // P lo | 0
+        uint64_t bg = sdesc_sw128(gt, g2 - gt, 1024u);      // G hi | G2
+        uint64_t bz = sdesc_sw128(glo, zero - glo, 1024u);  // G lo | 0
         for (int kt = 0; kt < ksteps2; ++kt) {
-          const uint32_t o = (uint32_t)kt * 2048u;
-          const uint64_t aw = sdesc_sw128(phi + o, g2 - phi, 1024u);          // P hi | G2
-          const uint64_t az = sdesc_sw128(plo + o, zero - (plo + o), 1024u);  // P lo | 0
-          const uint64_t bg = sdesc_sw128(gt + o, g2 - gt, 1024u);            // G hi | G2
-          const uint64_t bz = sdesc_sw128(glo + o, zero - (glo + o), 1024u);  // G lo | 0
           umma_bf16(D2, aw, bg, id2, (it.c > it.c0 || kt > 0) ? 1u : 0u);
           umma_bf16(D2, aw, bz, id2, 1u);
           umma_bf16(D2, az, bg, id2, 1u);
+          aw += 128;  // + 2048 bytes; the leading offset to G2 stays
+          bg += 128;
+          az += e_step;
+          bz += e_step;
         }
+        const uint64_t gh0 = sdesc_sw128(gt, 0u, 1024u), gl0 = sdesc_sw128(glo, 0u, 1024u);
+        const uint64_t sh0 = sdesc_sw128(sh, 0u, 1024u), sl0 = sdesc_sw128(sl, 0u, 1024u);
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
-          const uint32_t o = (uint32_t)ks * 32u;
-          const uint64_t ah = sdesc_sw128(gt + o, 0u, 1024u), al = sdesc_sw128(glo + o, 0u, 1024u);
-          const uint64_t bh = sdesc_sw128(sh + o, 0u, 1024u);
+          const uint64_t ah = gh0 + 2 * ks, bh = sh0 + 2 * ks;  // + 32 bytes per K step
           umma_bf16(D3, ah, bh, id3, ks > 0 ? 1u : 0u);
-          umma_bf16(D3, ah, sdesc_sw128(sl + o, 0u, 1024u), id3, 1u);
-          umma_bf16(D3, al, bh, id3, 1u);
+          umma_bf16(D3, ah, sl0 + 2 * ks, id3, 1u);
+          umma_bf16(D3, gl0 + 2 * ks, bh, id3, 1u);
         }
         umma_bf16(D3, sdesc_sw128(g2, 0u, 1024u), sdesc_sw128(zt, 0u, 1024u), id3, 1u);
         umma_commit(gfree(g));

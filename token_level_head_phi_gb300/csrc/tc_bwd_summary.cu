@@ -256,19 +256,23 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_summary_kernel(const __gri
         const uint32_t ks_ = kst(s), phi_hi = ks_, vt = ks_ + kTile, phi_lo = ks_ + 2 * kTile;
         const uint32_t bs = bst(x);
         const uint32_t dK = tmem + (uint32_t)acc * 128u, dV = dK + 64u;
+        // descriptors of K step 0, advanced by adding byte offset / 16 to the
+        // address field (the issue of each MMA waits for the tensor pipe, so
+        // every instruction on this thread adds to the unit's time)
+        const uint64_t v0 = sdesc_sw128(vt, 0u, 1024u), b0 = sdesc_sw128(bs, 0u, 1024u);
+        const uint64_t bl0 = sdesc_sw128(bs + kOffSlo, 0u, 1024u);
+        const uint64_t h0 = sdesc_sw128(phi_hi, 0u, 1024u), l0 = sdesc_sw128(phi_lo, 0u, 1024u);
 #pragma unroll
         for (int k4 = 0; k4 < 4; ++k4) {
-          const uint32_t ka = (uint32_t)k4 * 32u, kb = (uint32_t)k4 * 2048u;
-          // D_K += V dS^T (B K-major: rows k, 16 c per step)
-          const uint64_t av = sdesc_sw128(vt + ka, 0u, 1024u);
-          umma_bf16(dK, av, sdesc_sw128(bs + ka, 0u, 1024u), id_k, k4 > 0 ? 1u : 0u);
-          umma_bf16(dK, av, sdesc_sw128(bs + kOffSlo + ka, 0u, 1024u), id_k, 1u);
-          // D_V += phi(K) dS (B MN-major: 16 k rows per step)
-          const uint64_t ah = sdesc_sw128(phi_hi + ka, 0u, 1024u), al = sdesc_sw128(phi_lo + ka, 0u, 1024u);
-          const uint64_t bh = sdesc_sw128(bs + kb, 0u, 1024u);
+          // D_K += V dS^T (B K-major: rows k, 16 c per step; + 32 bytes per step)
+          const uint64_t av = v0 + 2 * k4;
+          umma_bf16(dK, av, b0 + 2 * k4, id_k, k4 > 0 ? 1u : 0u);
+          umma_bf16(dK, av, bl0 + 2 * k4, id_k, 1u);
+          // D_V += phi(K) dS (B MN-major: 16 k rows per step, + 2048 bytes)
+          const uint64_t ah = h0 + 2 * k4, bh = b0 + 128 * k4;
           umma_bf16(dV, ah, bh, id_v, k4 > 0 ? 1u : 0u);
-          umma_bf16(dV, ah, sdesc_sw128(bs + kOffSlo + kb, 0u, 1024u), id_v, 1u);
-          umma_bf16(dV, al, bh, id_v, 1u);
+          umma_bf16(dV, ah, bl0 + 128 * k4, id_v, 1u);
+          umma_bf16(dV, l0 + 2 * k4, bh, id_v, 1u);
         }
         // bias K step: ones columns 0, 1 against (dz hi, lo) and (dv hi, lo)
         const uint64_t a1 = sdesc_sw128(ones, 0u, 1024u);
