@@ -175,7 +175,8 @@ def phase_kernels(w: wl.Workload, info, fmap: str, causal: bool):
     mixt = f16 and w.n_blocks <= 128 and 2 * ((q + 63) // 64) * 32 <= 256
     mix = ("tc_mixs_kernel", C + "tc_mixs.cu") if small else \
         ("tc_mixt_kernel", C + "tc_mix.cu") if mixt else ("tc_mix_kernel", C + "tc_mix.cu")
-    return {"prep": ("tc_prep_kernel", C + "tc_mix.cu"), "summary": ("tc_summary_kernel", C + "tc_summary.cu"),
+    return {"prep": None if (f16 and small) else ("tc_prep_kernel", C + "tc_mix.cu"),
+            "summary": ("tc_summary_kernel", C + "tc_summary.cu"),
             "scale": ("tc_scale_kernel", C + "tc_scale.cu") if f16 and not small else None,
             "mix": mix,
             "output": ("tc_causal_kernel", C + "tc_causal.cu") if causal else ("tc_output_kernel", C + "tc_output.cu")}

@@ -212,9 +212,12 @@ def test_fused_plan(lib, name):
     split = mb.mhla_plan(_params(w, variant="multipass", norm="mala"))
     assert fused.variant == mb.VARIANT_FUSED and fused.kernels_per_call == 2
     # fp16 records need the exponent-folding kernel unless the mixing of few
-    # blocks (M <= 16) runs on the CUDA cores
+    # blocks (M <= 16) runs on the CUDA cores, which also needs no prep kernel
     small = w.n_blocks <= 16 and w.n_blocks * multi.summary_splits <= 256
-    assert multi.kernels_per_call == (4 if w.norm == "mala" or small else 5)
+    if w.norm == "mala":
+        assert multi.kernels_per_call == 4
+    else:
+        assert multi.kernels_per_call == (3 if small else 5)
     assert fused.summary_splits == multi.summary_splits
     assert fused.workspace_bytes <= split.workspace_bytes + 3 * 4 * w.units + 256
     if name == "video_16x64x64":

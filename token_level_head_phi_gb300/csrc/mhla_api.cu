@@ -247,7 +247,8 @@ mhla_status make_plan(const mhla_params* prm, Plan* p, int split_units = 0) {
       p->off_mcw = off;
       off = align_up(off + 4 * (size_t)p->M * p->mc_heads * p->Qp);
       // few blocks: the CUDA-core mixing reads the record exponents itself
-      p->kernels = small_mix_supported(*p) ? 4 : 5;
+      // few blocks: no prep kernel, no exponent folding
+      p->kernels = small_mix_supported(*p) ? 3 : 5;
     }
     if (variant == MHLA_VARIANT_FUSED) {
       p->off_flow = off;
@@ -341,13 +342,16 @@ mhla_status run_plan(const Plan& plan, const void* q, const void* k, const void*
       record_event(5, s);
       return MHLA_OK;
     }
-    if ((e = launch_tc_prep(p, mc, b, s)) != 0) return cuda_fail((cudaError_t)e);
-    record_event(1, s);
-    if ((e = launch_tc_summary(p, p.chunk, k, v, b, s)) != 0) return cuda_fail((cudaError_t)e);
-    record_event(2, s);
     // few blocks: the mixing runs on the CUDA cores (a tensor-core tile would
     // be almost all padding) and decodes the fp16 records' exponents itself
     const bool small = small_mix_supported(p);
+    // the fp16 records with few blocks need nothing the prep kernel makes
+    // (the small mixing reads Mc itself and writes the output scales)
+    b.no_prep = b.f16 && small;
+    if (!b.no_prep && (e = launch_tc_prep(p, mc, b, s)) != 0) return cuda_fail((cudaError_t)e);
+    record_event(1, s);
+    if ((e = launch_tc_summary(p, p.chunk, k, v, b, s)) != 0) return cuda_fail((cudaError_t)e);
+    record_event(2, s);
     if (b.f16 && !small && (e = launch_tc_scale(p, b, s)) != 0) return cuda_fail((cudaError_t)e);
     record_event(3, s);
     if ((e = small ? launch_tc_mix_small(p, mc, b, s) : launch_tc_mix(p, b, s)) != 0) return cuda_fail((cudaError_t)e);

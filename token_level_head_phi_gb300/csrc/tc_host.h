@@ -77,6 +77,7 @@ struct TcBuffers {
   bool f16;                  // fp16 records and mixing
   int slots;                 // heads the stack and mixed buffers hold
   unsigned int* flow;        // fused launch: [3][BH] progress counters, zeroed by the prep kernel
+  bool no_prep;              // the summary kernel is the call's first kernel
 };
 
 // Whether the output step multiplies phi(Q) by the low residual of S~_i too

@@ -53,6 +53,7 @@ int build_summary_args(const Plan& p, const ChunkShape& c, const void* k, const 
   if ((e = encode_tmap_bf16(&a.tmS_lo, lo_base, 2, dims2, str2, boxS)) != 0) return e;
   if ((e = encode_tmap_bf16(&a.tmZV_lo, lo_base, 2, dims2, str2, boxZV)) != 0) return e;
   a.rexp = b.rexp;
+  a.wait_prev = b.no_prep ? 1 : 0;
   a.splits = p.splits;
   a.cpp = p.cpp;
   a.units = p.BH * p.M * p.splits;

@@ -80,6 +80,7 @@ struct SummaryArgs {
   CUtensorMap tmS, tmS_lo;           // 2D view (64, BH*Q*66) of the stack, box (64, 64): S_b rows
   CUtensorMap tmZV, tmZV_lo;         // same view, box (64, 2): the z_b and v_b rows
   int units, splits, cpp;            // work units, pieces per block, chunks per piece
+  int wait_prev;                     // no prep kernel before this one: wait for the stream's previous work
   int2* rexp;                        // fp16 records: [slots * M * splits] exponents {eS, eZ}
   ChunkShape c;
   FastDiv f_head, f_splits;          // divisions by M * splits and by splits
@@ -240,8 +241,12 @@ __device__ __forceinline__ void summary_body(const SummaryArgs& a, const Plan& p
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // K and V are inputs: nothing to wait for; the next kernel may start its
-  // set-up as SMs free up
+  // First kernel of a call: what came before in the stream (the previous
+  // call, whose kernels read the stack this one writes, or the producer of K
+  // and V) has finished.  After the prep kernel, which waited for it, K and V
+  // are inputs with nothing to wait for.
+  if (a.wait_prev) pdl_wait();
+  // the next kernel may start its set-up as SMs free up
   pdl_launch_dependents();
 
   if (warp == 0) {
