@@ -76,12 +76,19 @@ __device__ __forceinline__ uint32_t place2(uint32_t w, uint32_t e2, uint32_t c2,
 // i = x * kWarps + w of head u's two Mc copies and its output scale.  The
 // head's record exponents pass through shared memory in chunks of kQChunk,
 // packed {eS, eZ} + kBias as 16-bit lanes; each lane reads four consecutive
-// Mc words and four packed exponents (16 bytes each) at a time.
+// Mc words and four packed exponents (16 bytes each) at a time.  For rows of
+// at most kCacheQ records (kCached) a lane loads its Mc words once, while
+// the exponents are being staged, and keeps them in registers for both
+// passes.
+constexpr int kCacheQ = 512;
+
+template <bool kCached>
 __global__ void __launch_bounds__(32 * kWarps) tc_scale_kernel(const Plan p, int Q, int Qp,
                                                                const uint32_t* __restrict__ mcw,
                                                                const int2* __restrict__ rexp,
                                                                __half* __restrict__ mcx,
                                                                float4* __restrict__ sinfo) {
+  constexpr int kIters = kCached ? kCacheQ / 128 : 1;
   extern __shared__ __align__(16) uint32_t ex_s[];  // min(Qp, kQChunk) words
   // the record exponents come from the summary kernel
   pdl_wait();
@@ -98,24 +105,37 @@ __global__ void __launch_bounds__(32 * kWarps) tc_scale_kernel(const Plan p, int
       ex_s[t] = (uint32_t)(e.x + kBias) | ((uint32_t)(e.y + kBias) << 16);
     }
   };
+  auto amax = [](uint32_t mx, const uint4& w4, const uint4& e4) {
+    mx = __viaddmax_u16x2(e4.x, __byte_perm(w4.x, 0u, 0x3232), mx);
+    mx = __viaddmax_u16x2(e4.y, __byte_perm(w4.y, 0u, 0x3232), mx);
+    mx = __viaddmax_u16x2(e4.z, __byte_perm(w4.z, 0u, 0x3232), mx);
+    return __viaddmax_u16x2(e4.w, __byte_perm(w4.w, 0u, 0x3232), mx);
+  };
   // row exponents: the largest eS[q] + x(Mc[i][b(q)]) (and eZ) over nonzero
   // weights, as biased lanes (a zero weight adds only the record's e + kBias,
   // below every real sum)
   uint32_t mx = 0u;
-  for (int c0 = 0; c0 < Qp; c0 += kQChunk) {
-    const int n = min(kQChunk, Qp - c0);
+  uint4 wc[kIters];
+  if (kCached) {
+#pragma unroll
+    for (int k = 0; k < kIters; ++k)
+      if (live && 4 * lane + 128 * k < Qp) wc[k] = __ldg(row + lane + 32 * k);
+    stage(0, Qp);
     __syncthreads();
-    stage(c0, n);
-    __syncthreads();
-    if (live) {
+#pragma unroll
+    for (int k = 0; k < kIters; ++k)
+      if (live && 4 * lane + 128 * k < Qp)
+        mx = amax(mx, wc[k], *reinterpret_cast<const uint4*>(ex_s + 4 * lane + 128 * k));
+  } else {
+    for (int c0 = 0; c0 < Qp; c0 += kQChunk) {
+      const int n = min(kQChunk, Qp - c0);
+      __syncthreads();
+      stage(c0, n);
+      __syncthreads();
+      if (live) {
 #pragma unroll 4
-      for (int q = 4 * lane; q < n; q += 128) {
-        const uint4 w4 = __ldg(row + (c0 + q) / 4);
-        const uint4 e4 = *reinterpret_cast<const uint4*>(ex_s + q);
-        mx = __viaddmax_u16x2(e4.x, __byte_perm(w4.x, 0u, 0x3232), mx);
-        mx = __viaddmax_u16x2(e4.y, __byte_perm(w4.y, 0u, 0x3232), mx);
-        mx = __viaddmax_u16x2(e4.z, __byte_perm(w4.z, 0u, 0x3232), mx);
-        mx = __viaddmax_u16x2(e4.w, __byte_perm(w4.w, 0u, 0x3232), mx);
+        for (int q = 4 * lane; q < n; q += 128)
+          mx = amax(mx, __ldg(row + (c0 + q) / 4), *reinterpret_cast<const uint4*>(ex_s + q));
       }
     }
   }
@@ -128,22 +148,30 @@ __global__ void __launch_bounds__(32 * kWarps) tc_scale_kernel(const Plan p, int
   const uint32_t c2 = (uint32_t)(14 - es + 256) | ((uint32_t)(14 - ez + 256) << 16);
   uint2* ds = reinterpret_cast<uint2*>(mcx + (((size_t)u * 2 + 0) * p.M + i) * Qp);
   uint2* dz = reinterpret_cast<uint2*>(mcx + (((size_t)u * 2 + 1) * p.M + i) * Qp);
-  for (int c0 = 0; c0 < Qp; c0 += kQChunk) {
-    const int n = min(kQChunk, Qp - c0);
-    if (c0 > 0) {
-      __syncthreads();
-      stage(c0, n);
+  auto emit = [&](int q, const uint4& w4, const uint4& e4) {
+    const uint32_t r0 = place2(w4.x, e4.x, c2, es, ez), r1 = place2(w4.y, e4.y, c2, es, ez);
+    const uint32_t r2 = place2(w4.z, e4.z, c2, es, ez), r3 = place2(w4.w, e4.w, c2, es, ez);
+    ds[q / 4] = make_uint2(__byte_perm(r0, r1, 0x5410), __byte_perm(r2, r3, 0x5410));
+    dz[q / 4] = make_uint2(__byte_perm(r0, r1, 0x7632), __byte_perm(r2, r3, 0x7632));
+  };
+  if (kCached) {
+#pragma unroll
+    for (int k = 0; k < kIters; ++k) {
+      const int q = 4 * lane + 128 * k;
+      if (live && q < Qp) emit(q, wc[k], *reinterpret_cast<const uint4*>(ex_s + q));
     }
-    __syncthreads();
-    if (live) {
+  } else {
+    for (int c0 = 0; c0 < Qp; c0 += kQChunk) {
+      const int n = min(kQChunk, Qp - c0);
+      if (c0 > 0) {
+        __syncthreads();
+        stage(c0, n);
+      }
+      __syncthreads();
+      if (live) {
 #pragma unroll 4
-      for (int q = 4 * lane; q < n; q += 128) {
-        const uint4 w4 = __ldg(row + (c0 + q) / 4);
-        const uint4 e4 = *reinterpret_cast<const uint4*>(ex_s + q);
-        const uint32_t r0 = place2(w4.x, e4.x, c2, es, ez), r1 = place2(w4.y, e4.y, c2, es, ez);
-        const uint32_t r2 = place2(w4.z, e4.z, c2, es, ez), r3 = place2(w4.w, e4.w, c2, es, ez);
-        ds[(c0 + q) / 4] = make_uint2(__byte_perm(r0, r1, 0x5410), __byte_perm(r2, r3, 0x5410));
-        dz[(c0 + q) / 4] = make_uint2(__byte_perm(r0, r1, 0x7632), __byte_perm(r2, r3, 0x7632));
+        for (int q = 4 * lane; q < n; q += 128)
+          emit(c0 + q, __ldg(row + (c0 + q) / 4), *reinterpret_cast<const uint4*>(ex_s + q));
       }
     }
   }
@@ -158,7 +186,8 @@ __global__ void __launch_bounds__(32 * kWarps) tc_scale_kernel(const Plan p, int
 int launch_tc_scale(const Plan& p, const TcBuffers& b, cudaStream_t s) {
   const dim3 grid((unsigned)((p.M + kWarps - 1) / kWarps), (unsigned)b.slots);
   const size_t smem = 4 * (size_t)(b.Qp < kQChunk ? b.Qp : kQChunk);
-  return launch_pdl(tc_scale_kernel, grid, dim3(32 * kWarps), smem, s, p, p.M * p.splits, b.Qp, (const uint32_t*)b.mcw,
+  auto kern = b.Qp <= kCacheQ ? tc_scale_kernel<true> : tc_scale_kernel<false>;
+  return launch_pdl(kern, grid, dim3(32 * kWarps), smem, s, p, p.M * p.splits, b.Qp, (const uint32_t*)b.mcw,
                     (const int2*)b.rexp, b.mcx, b.sinfo);
 }
 
