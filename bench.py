@@ -534,6 +534,14 @@ BWD_PHASE_KERNEL = {
     },
 }
 BWD_LAUNCHES = {"simt": 7, "simt_causal": 9, "tc": 10}
+
+
+def simt_mc_reduce_launches(w, mc_heads):
+    """1 when the CUDA-core dMc kernel splits its units over groups (then a
+    reduce kernel follows): fewer tiles than about four CTAs per SM."""
+    tiles = ((w.n_blocks + 15) // 16) ** 2 * mc_heads
+    units = w.units if mc_heads == 1 else w.batch
+    return int(min(-(-608 // tiles), units, 64) > 1)
 FP32_LANES_PER_SM = 128  # FP32 FMA lanes per SM (4 partitions x 32)
 SM_COUNT = 152
 
@@ -731,7 +739,8 @@ def run_backward(args, w: wl.Workload, world: int, rank: int, local: int, dist):
                           "bound": "hbm" if t_hbm >= t_tc else "tensor",
                           "frac": max(t_hbm, t_tc) / (ms_per_step / 1e3)},
         "phase_ms": avg_phase,
-        "gpu_launches": BWD_LAUNCHES[path] * K,
+        "gpu_launches": (BWD_LAUNCHES[path] + (0 if path == "tc" else simt_mc_reduce_launches(
+            w, w.heads if args.mc_per_head else 1))) * K,
         "host_us_per_call": host_s / K * 1e6,
         "clocks": clocks,
         "e2e": {"value": w.units * w.n_tokens * E / (te1 - te0), "unit": UNIT, "h2d_bytes_per_step": h2d,

@@ -238,18 +238,42 @@ bwd_mix_kernel(Plan p, const float* __restrict__ mc, const float* __restrict__ d
 // Causal form (diag set): only b < i comes from the prefix partials; the
 // diagonal is the sum of the in-block terms, and above it Mc does not enter
 // the output (0).
+// With groups > 1 the units of a head are split over blockIdx.z / mc_heads
+// (group g takes every groups-th unit) into partial[g][h][M][M], which
+// bwd_mc_reduce_kernel then sums in group order: a few tiles of dMc over
+// many units would otherwise leave most of the GPU idle.
+__device__ __forceinline__ float mc_assemble(const Plan& p, int h, int ustep, int i, int b, float acc,
+                                             const float* __restrict__ dnp, const float* __restrict__ diag) {
+  const int rows = p.M * p.splits;
+  if (diag && b >= i) {
+    float t = 0.f;
+    if (b == i)
+      for (int u = h; u < p.BH; u += ustep) t += diag[(size_t)u * p.M + i];
+    return t;
+  }
+  if (p.norm == MHLA_NORM_MALA) {
+    float dn = 0.f;
+    for (int u = h; u < p.BH; u += ustep)
+      for (int s = 0; s < p.splits; ++s) dn += dnp[(size_t)u * rows + (size_t)i * p.splits + s];
+    acc = fmaf((float)p.nb, dn, acc);
+  }
+  return acc;
+}
+
 __global__ void __launch_bounds__(kThreads)
 bwd_mc_kernel(Plan p, const float* __restrict__ dmixp, const float* __restrict__ stack,
-              const float* __restrict__ dnp, const float* __restrict__ diag, float* __restrict__ dmc) {
+              const float* __restrict__ dnp, const float* __restrict__ diag, float* __restrict__ dmc, int groups,
+              float* __restrict__ partial) {
   constexpr int TI = 16, TK = 32;
   __shared__ float sa[TI][TK + 1];
   __shared__ float sb[TI][TK + 1];
   const int i0 = blockIdx.y * TI, b0 = blockIdx.x * TI;
   const int ti = threadIdx.x / TI, tb = threadIdx.x % TI;
   const int rows = p.M * p.splits;
-  const int h = blockIdx.z, ustep = p.mc_heads == 1 ? 1 : p.H;
+  const int h = (int)blockIdx.z % p.mc_heads, g = (int)blockIdx.z / p.mc_heads;
+  const int ustep = p.mc_heads == 1 ? 1 : p.H;
   float acc = 0.f;
-  for (int u = h; u < p.BH; u += ustep) {
+  for (int u = h + g * ustep; u < p.BH; u += groups * ustep) {
     float acc_u = 0.f;
     const float* da = dmixp + (size_t)u * rows * p.R;
     const float* xa = stack + (size_t)u * rows * p.R;
@@ -277,20 +301,25 @@ bwd_mc_kernel(Plan p, const float* __restrict__ dmixp, const float* __restrict__
     acc += acc_u;
   }
   const int i = i0 + ti, b = b0 + tb;
-  if (diag && i < p.M && b < p.M && b >= i) {
-    float t = 0.f;
-    if (b == i)
-      for (int u = h; u < p.BH; u += ustep) t += diag[(size_t)u * p.M + i];
-    dmc[((size_t)h * p.M + i) * p.M + b] = t;
-  } else if (i < p.M && b < p.M) {
-    if (p.norm == MHLA_NORM_MALA) {
-      float dn = 0.f;
-      for (int u = h; u < p.BH; u += ustep)
-        for (int s = 0; s < p.splits; ++s) dn += dnp[(size_t)u * rows + (size_t)i * p.splits + s];
-      acc = fmaf((float)p.nb, dn, acc);
-    }
-    dmc[((size_t)h * p.M + i) * p.M + b] = acc;
-  }
+  if (i >= p.M || b >= p.M) return;
+  if (groups > 1)
+    partial[(((size_t)g * p.mc_heads + h) * p.M + i) * p.M + b] = acc;
+  else
+    dmc[((size_t)h * p.M + i) * p.M + b] = mc_assemble(p, h, ustep, i, b, acc, dnp, diag);
+}
+
+// dMc[h][i][b] from the groups' partial sums, in group order.
+__global__ void __launch_bounds__(kThreads)
+bwd_mc_reduce_kernel(Plan p, const float* __restrict__ partial, int groups, const float* __restrict__ dnp,
+                     const float* __restrict__ diag, float* __restrict__ dmc) {
+  const size_t n = (size_t)p.mc_heads * p.M * p.M;
+  const size_t e = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
+  if (e >= n) return;
+  const int h = (int)(e / ((size_t)p.M * p.M));
+  const int i = (int)(e / p.M % p.M), b = (int)(e % p.M);
+  float acc = 0.f;
+  for (int g = 0; g < groups; ++g) acc += partial[(size_t)g * n + e];
+  dmc[e] = mc_assemble(p, h, p.mc_heads == 1 ? 1 : p.H, i, b, acc, dnp, diag);
 }
 
 // One CTA per (summary block piece, head): dS_b, dz_b, dv_b in shared memory;
@@ -407,10 +436,32 @@ int launch_bwd_mix(const Plan& p, const BwdBuffers& w, void* stream) {
   return (int)cudaGetLastError();
 }
 
+int bwd_mc_groups(const Plan& p) {
+  // about four CTAs per SM of a 152-SM GPU, at most one group per unit of a
+  // head and 64 groups
+  const long long tiles = (long long)((p.M + 15) / 16) * ((p.M + 15) / 16) * p.mc_heads;
+  const int units = p.mc_heads == 1 ? p.BH : p.BH / p.H;
+  long long g = (608 + tiles - 1) / tiles;
+  if (g > units) g = units;
+  if (g > 64) g = 64;
+  return g < 1 ? 1 : (int)g;
+}
+
+size_t bwd_mc_partial_bytes(const Plan& p) {
+  const int g = bwd_mc_groups(p);
+  return g > 1 ? sizeof(float) * (size_t)g * p.mc_heads * p.M * p.M : 0;
+}
+
 int launch_bwd_mc(const Plan& p, const BwdBuffers& w, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  bwd_mc_kernel<<<dim3((p.M + 15) / 16, (p.M + 15) / 16, p.mc_heads), kThreads, 0, s>>>(p, w.dmixp, w.stack, w.dnp,
-                                                                                        w.diag, w.dmc);
+  const int groups = bwd_mc_groups(p);
+  bwd_mc_kernel<<<dim3((p.M + 15) / 16, (p.M + 15) / 16, p.mc_heads * groups), kThreads, 0, s>>>(
+      p, w.dmixp, w.stack, w.dnp, w.diag, w.dmc, groups, w.mc_partial);
+  if (groups > 1) {
+    const size_t n = (size_t)p.mc_heads * p.M * p.M;
+    bwd_mc_reduce_kernel<<<(unsigned)((n + kThreads - 1) / kThreads), kThreads, 0, s>>>(p, w.mc_partial, groups,
+                                                                                       w.dnp, w.diag, w.dmc);
+  }
   return (int)cudaGetLastError();
 }
 

@@ -19,6 +19,7 @@ struct BwdBuffers {
   const float* diag;   // [BH][M] in-block term of dMc[i][i]; dMc above the diagonal is 0
   const float* xk;     // [BH][N][d] in-block part of dphi(k) (laid out like K, float32)
   const float* xv;     // [BH][N][d] in-block part of dv
+  float* mc_partial;   // [groups][mc_heads][M][M] partial sums of dMc (bwd_mc_partial_bytes, may be 0)
 };
 
 // Buffers of the causal backward's in-block kernels (simt_causal_bwd.cu).
@@ -43,6 +44,8 @@ struct CausalBwdBuffers {
 int launch_bwd_output(const Plan& p, const BwdBuffers& w, const void* q, const void* dout, void* dq, void* stream);
 int launch_bwd_mix(const Plan& p, const BwdBuffers& w, void* stream);
 int launch_bwd_mc(const Plan& p, const BwdBuffers& w, void* stream);
+// Workspace of the dMc partial sums (0 when one group covers every unit).
+size_t bwd_mc_partial_bytes(const Plan& p);
 int launch_bwd_summary(const Plan& p, const BwdBuffers& w, const void* k, const void* v, void* dk, void* dv,
                        void* stream);
 // Causal form, after the forward summaries and the strict-lower mixing: dq,

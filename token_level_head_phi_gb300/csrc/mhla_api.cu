@@ -474,6 +474,7 @@ struct BwdLayout {
   size_t mct, mct_f16, mct_hi, mct_lo, mct_scale, mct_rowsum, mct_blkinfo;  // Mc transposed
   size_t dx_hi, dx_lo;                                                      // dS_b, dz_b, dv_b planes
   size_t mcl, tokbuf, xk, xv, diag;                                         // causal form (CUDA cores)
+  size_t mc_partial;                                                        // dMc partial sums (CUDA cores)
   size_t total;
 };
 
@@ -508,6 +509,7 @@ mhla_status make_bwd_plan(const mhla_params* prm, Plan* plan, BwdLayout* lay) {
     take(lay->mixed, sizeof(float) * mrows * R);
     take(lay->dmixp, sizeof(float) * rows * R);
     take(lay->dstack, sizeof(float) * mrows * R);
+    take(lay->mc_partial, bwd_mc_partial_bytes(*plan));
     if (plan->causal) {
       const size_t toks = (size_t)plan->BH * plan->N;
       take(lay->mcl, sizeof(float) * (size_t)plan->M * plan->M * mh);
@@ -563,6 +565,7 @@ int run_backward(const Plan& plan, const BwdLayout& lay, const void* q, const vo
   w.diag = nullptr;
   w.xk = nullptr;
   w.xv = nullptr;
+  w.mc_partial = lay.tc ? nullptr : F(lay.mc_partial);
   int e;
   record_bwd_event(0, s);
   if (lay.tc) {

@@ -47,16 +47,18 @@ struct TileTokens {
   static constexpr int value = D <= 64 ? 32 : 16;
 };
 
+// Rows of the D-wide shared arrays are D + 1 floats apart, so that a warp
+// reading one column of D consecutive rows hits 32 different banks.
 template <int D>
 constexpr size_t fwd_smem_floats() {
-  constexpr int TQ = TileTokens<D>::value;
-  return 2 * D * D + 4 * D + 5 * TQ * D + TQ * TQ + 2 * TQ + 2 * kWarps;
+  constexpr int TQ = TileTokens<D>::value, LD = D + 1;
+  return 2 * D * LD + 4 * D + 5 * TQ * LD + TQ * TQ + 2 * TQ + 2 * kWarps;
 }
 
 template <int D>
 constexpr size_t rev_smem_floats() {
-  constexpr int TQ = TileTokens<D>::value;
-  return D * D + 2 * D + 5 * TQ * D + 2 * TQ * TQ + TQ;
+  constexpr int TQ = TileTokens<D>::value, LD = D + 1;
+  return D * LD + 2 * D + 5 * TQ * LD + 2 * TQ * TQ + TQ;
 }
 
 __device__ __forceinline__ float warp_sum(float x) {
@@ -78,21 +80,21 @@ causal_bwd_fwd_kernel(Plan p, const T* __restrict__ Q, const T* __restrict__ K, 
                       const float* __restrict__ rowsum_lower, const float* __restrict__ mc, T* __restrict__ dQ,
                       float* __restrict__ dmixp, float* __restrict__ dnp, float* __restrict__ diag,
                       float* __restrict__ tokbuf) {
-  constexpr int TQ = TileTokens<D>::value;
+  constexpr int TQ = TileTokens<D>::value, LD = D + 1;
   constexpr int PER = (D * D + kThreads - 1) / kThreads;
   extern __shared__ float sm[];
   float* sP = sm;               // Sp_i
-  float* sR = sP + D * D;       // in-block state R (without w)
-  float* zP = sR + D * D;
+  float* sR = sP + D * LD;      // in-block state R (without w)
+  float* zP = sR + D * LD;
   float* vP = zP + D;
   float* zR = vP + D;
   float* vR = zR + D;
   float* sq = vR + D;           // phi(q)
-  float* sk = sq + TQ * D;      // phi(k)
-  float* sx = sk + TQ * D;      // v
-  float* sg = sx + TQ * D;      // dO
-  float* sdn = sg + TQ * D;     // dnum
-  float* sa = sdn + TQ * D;     // TQ*TQ
+  float* sk = sq + TQ * LD;     // phi(k)
+  float* sx = sk + TQ * LD;     // v
+  float* sg = sx + TQ * LD;     // dO
+  float* sdn = sg + TQ * LD;    // dnum
+  float* sa = sdn + TQ * LD;    // TQ*TQ
   float* sds = sa + TQ * TQ;    // ds
   float* sgm = sds + TQ;        // gamma
   float* sdg = sgm + TQ;        // per-warp sums: diagonal term [kWarps], dn~ [kWarps]
@@ -102,8 +104,8 @@ causal_bwd_fwd_kernel(Plan p, const T* __restrict__ Q, const T* __restrict__ K, 
   const float w = mc[((size_t)jm * p.M + i) * p.M + i];
   const float* mrow = mixed + ((size_t)u * p.M + i) * p.R;
   for (int e = tid; e < D * D; e += kThreads) {
-    sP[e] = mrow[e];
-    sR[e] = 0.f;
+    sP[e / D * LD + e % D] = mrow[e];
+    sR[e / D * LD + e % D] = 0.f;
   }
   for (int e = tid; e < D; e += kThreads) {
     zP[e] = mrow[D * D + e];
@@ -133,10 +135,10 @@ causal_bwd_fwd_kernel(Plan p, const T* __restrict__ Q, const T* __restrict__ K, 
         vx = to_f32(V[off]);
         gx = to_f32(dO[off]);
       }
-      sq[e] = qx;
-      sk[e] = kx;
-      sx[e] = vx;
-      sg[e] = gx;
+      sq[tt * LD + f] = qx;
+      sk[tt * LD + f] = kx;
+      sx[tt * LD + f] = vx;
+      sg[tt * LD + f] = gx;
     }
     __syncthreads();
     // masked in-tile scores a[t][j] = phi(q_t) . phi(k_j), j <= t
@@ -144,7 +146,7 @@ causal_bwd_fwd_kernel(Plan p, const T* __restrict__ Q, const T* __restrict__ K, 
       const int tt = e / TQ, jj = e % TQ;
       float a = 0.f;
       if (jj <= tt && tt < cnt)
-        for (int f = 0; f < D; ++f) a = fmaf(sq[tt * D + f], sk[jj * D + f], a);
+        for (int f = 0; f < D; ++f) a = fmaf(sq[tt * LD + f], sk[jj * LD + f], a);
       sa[e] = a;
     }
     __syncthreads();
@@ -152,8 +154,8 @@ causal_bwd_fwd_kernel(Plan p, const T* __restrict__ Q, const T* __restrict__ K, 
     for (int tt = warp; tt < cnt; tt += kWarps) {
       float sp = 0.f, sin = 0.f;
       for (int f = lane; f < D; f += 32) {
-        sp = fmaf(sq[tt * D + f], zP[f], sp);
-        sin = fmaf(sq[tt * D + f], zR[f], sin);
+        sp = fmaf(sq[tt * LD + f], zP[f], sp);
+        sin = fmaf(sq[tt * LD + f], zR[f], sin);
       }
       for (int jj = lane; jj <= tt; jj += 32) sin += sa[tt * TQ + jj];
       sp = warp_sum(sp);
@@ -168,24 +170,24 @@ causal_bwd_fwd_kernel(Plan p, const T* __restrict__ Q, const T* __restrict__ K, 
       for (int c = lane; c < D; c += 32) {
         float ap = 0.f, ar = 0.f, loc = 0.f, vloc = 0.f;
         for (int f = 0; f < D; ++f) {
-          const float x = sq[tt * D + f];
-          ap = fmaf(x, sP[f * D + c], ap);
-          ar = fmaf(x, sR[f * D + c], ar);
+          const float x = sq[tt * LD + f];
+          ap = fmaf(x, sP[f * LD + c], ap);
+          ar = fmaf(x, sR[f * LD + c], ar);
         }
         for (int jj = 0; jj <= tt; ++jj) {
-          loc = fmaf(sa[tt * TQ + jj], sx[jj * D + c], loc);
-          vloc += sx[jj * D + c];
+          loc = fmaf(sa[tt * TQ + jj], sx[jj * LD + c], loc);
+          vloc += sx[jj * LD + c];
         }
         const float ain = ar + loc;                 // phi(q_t)^T R_t, column c
         const float num = fmaf(w, ain, ap);
         const float vin = vR[c] + vloc;             // rv_t
         const float vt = fmaf(w, vin, vP[c]);
-        const float g = sg[tt * D + c];
+        const float g = sg[tt * LD + c];
         gnum = fmaf(g, num, gnum);
         gvt = fmaf(g, vt, gvt);
         gain = fmaf(g, ain, gain);
         gvin = fmaf(g, vin, gvin);
-        sdn[tt * D + c] = coef * g;
+        sdn[tt * LD + c] = coef * g;
       }
       gnum = warp_sum(gnum);
       gvt = warp_sum(gvt);
@@ -215,7 +217,7 @@ causal_bwd_fwd_kernel(Plan p, const T* __restrict__ Q, const T* __restrict__ K, 
       float a = 0.f;
       if (jj <= tt && tt < cnt) {
         a = sds[tt];
-        for (int c = 0; c < D; ++c) a = fmaf(sx[jj * D + c], sdn[tt * D + c], a);
+        for (int c = 0; c < D; ++c) a = fmaf(sx[jj * LD + c], sdn[tt * LD + c], a);
       }
       sa[e] = a;
     }
@@ -224,10 +226,10 @@ causal_bwd_fwd_kernel(Plan p, const T* __restrict__ Q, const T* __restrict__ K, 
     for (int e = tid; e < cnt * D; e += kThreads) {
       const int tt = e / D, k = e % D;
       float a = 0.f;
-      for (int c = 0; c < D; ++c) a = fmaf(fmaf(w, sR[k * D + c], sP[k * D + c]), sdn[tt * D + c], a);
+      for (int c = 0; c < D; ++c) a = fmaf(fmaf(w, sR[k * LD + c], sP[k * LD + c]), sdn[tt * LD + c], a);
       a = fmaf(fmaf(w, zR[k], zP[k]), sds[tt], a);
       float loc = 0.f;
-      for (int jj = 0; jj <= tt; ++jj) loc = fmaf(sa[tt * TQ + jj], sk[jj * D + k], loc);
+      for (int jj = 0; jj <= tt; ++jj) loc = fmaf(sa[tt * TQ + jj], sk[jj * LD + k], loc);
       a = fmaf(w, loc, a);
       const size_t off = tok_off(p, u, block_token(p, i, l0 + tt)) + k;
       dQ[off] = from_f32<T>(a * phi_grad(to_f32(Q[off]), p.fmap));
@@ -237,15 +239,15 @@ causal_bwd_fwd_kernel(Plan p, const T* __restrict__ Q, const T* __restrict__ K, 
 #pragma unroll
       for (int m = 0; m < PER; ++m) {
         const int e = tid + m * kThreads;
-        if (e < D * D) acc[m] = fmaf(sq[tt * D + e / D], sdn[tt * D + e % D], acc[m]);
+        if (e < D * D) acc[m] = fmaf(sq[tt * LD + e / D], sdn[tt * LD + e % D], acc[m]);
       }
-      if (tid < D) zacc = fmaf(sds[tt], sq[tt * D + tid], zacc);
-      else if (tid < 2 * D && mala) vacc = fmaf(-sgm[tt], sg[tt * D + tid - D], vacc);
+      if (tid < D) zacc = fmaf(sds[tt], sq[tt * LD + tid], zacc);
+      else if (tid < 2 * D && mala) vacc = fmaf(-sgm[tt], sg[tt * LD + tid - D], vacc);
     }
     // per token for the reverse walk: dnum (D), ds, gamma
     for (int e = tid; e < cnt * (D + 2); e += kThreads) {
       const int tt = e / (D + 2), c = e % (D + 2);
-      const float x = c < D ? sdn[tt * D + c] : (c == D ? sds[tt] : sgm[tt]);
+      const float x = c < D ? sdn[tt * LD + c] : (c == D ? sds[tt] : sgm[tt]);
       tokbuf[((size_t)u * p.N + block_token(p, i, l0 + tt)) * (D + 2) + c] = x;
     }
     __syncthreads();
@@ -253,16 +255,16 @@ causal_bwd_fwd_kernel(Plan p, const T* __restrict__ Q, const T* __restrict__ K, 
     for (int e = tid; e < D * D; e += kThreads) {
       const int f = e / D, c = e % D;
       float a = 0.f;
-      for (int jj = 0; jj < cnt; ++jj) a = fmaf(sk[jj * D + f], sx[jj * D + c], a);
-      sR[e] += a;
+      for (int jj = 0; jj < cnt; ++jj) a = fmaf(sk[jj * LD + f], sx[jj * LD + c], a);
+      sR[f * LD + c] += a;
     }
     if (tid < D) {
       float a = 0.f;
-      for (int jj = 0; jj < cnt; ++jj) a += sk[jj * D + tid];
+      for (int jj = 0; jj < cnt; ++jj) a += sk[jj * LD + tid];
       zR[tid] += a;
     } else if (tid < 2 * D) {
       float a = 0.f;
-      for (int jj = 0; jj < cnt; ++jj) a += sx[jj * D + tid - D];
+      for (int jj = 0; jj < cnt; ++jj) a += sx[jj * LD + tid - D];
       vR[tid - D] += a;
     }
     rn += (float)cnt;
@@ -307,25 +309,25 @@ __global__ void __launch_bounds__(kThreads)
 causal_bwd_rev_kernel(Plan p, const T* __restrict__ Q, const T* __restrict__ K, const T* __restrict__ V,
                       const T* __restrict__ dO, const float* __restrict__ mc, const float* __restrict__ tokbuf,
                       float* __restrict__ xk, float* __restrict__ xv) {
-  constexpr int TQ = TileTokens<D>::value;
+  constexpr int TQ = TileTokens<D>::value, LD = D + 1;
   constexpr int PER = (D * D + kThreads - 1) / kThreads;
   extern __shared__ float sm[];
   float* GS = sm;
-  float* Gz = GS + D * D;
+  float* Gz = GS + D * LD;
   float* Gv = Gz + D;
   float* sq = Gv + D;
-  float* sk = sq + TQ * D;
-  float* sx = sk + TQ * D;
-  float* sdn = sx + TQ * D;
-  float* sgv = sdn + TQ * D;
-  float* sE = sgv + TQ * D;
+  float* sk = sq + TQ * LD;
+  float* sx = sk + TQ * LD;
+  float* sdn = sx + TQ * LD;
+  float* sgv = sdn + TQ * LD;
+  float* sE = sgv + TQ * LD;
   float* sPm = sE + TQ * TQ;
   float* sds = sPm + TQ * TQ;
   const int u = blockIdx.y, i = blockIdx.x, tid = threadIdx.x;
   const int jm = mc_index(p, u);
   const float w = mc[((size_t)jm * p.M + i) * p.M + i];
   const bool mala = p.norm == MHLA_NORM_MALA;
-  for (int e = tid; e < D * D + 2 * D; e += kThreads) sm[e] = 0.f;
+  for (int e = tid; e < D * LD + 2 * D; e += kThreads) sm[e] = 0.f;
   float acc[PER];
 #pragma unroll
   for (int m = 0; m < PER; ++m) acc[m] = 0.f;
@@ -349,11 +351,11 @@ causal_bwd_rev_kernel(Plan p, const T* __restrict__ Q, const T* __restrict__ K, 
       } else if (f == 0) {
         sds[tt] = 0.f;
       }
-      sq[e] = qx;
-      sk[e] = kx;
-      sx[e] = vx;
-      sdn[e] = dn;
-      sgv[e] = gv;
+      sq[tt * LD + f] = qx;
+      sk[tt * LD + f] = kx;
+      sx[tt * LD + f] = vx;
+      sdn[tt * LD + f] = dn;
+      sgv[tt * LD + f] = gv;
     }
     __syncthreads();
     for (int e = tid; e < TQ * TQ; e += kThreads) {
@@ -362,8 +364,8 @@ causal_bwd_rev_kernel(Plan p, const T* __restrict__ Q, const T* __restrict__ K, 
       if (tt >= jj && tt < cnt) {
         a = sds[tt];
         for (int f = 0; f < D; ++f) {
-          a = fmaf(sdn[tt * D + f], sx[jj * D + f], a);
-          b = fmaf(sq[tt * D + f], sk[jj * D + f], b);
+          a = fmaf(sdn[tt * LD + f], sx[jj * LD + f], a);
+          b = fmaf(sq[tt * LD + f], sk[jj * LD + f], b);
         }
       }
       sE[e] = a;
@@ -376,12 +378,12 @@ causal_bwd_rev_kernel(Plan p, const T* __restrict__ Q, const T* __restrict__ K, 
       const int jj = e / D, f = e % D;
       float gk = Gz[f], gv = Gv[f];
       for (int c = 0; c < D; ++c) {
-        gk = fmaf(GS[f * D + c], sx[jj * D + c], gk);
-        gv = fmaf(GS[c * D + f], sk[jj * D + c], gv);
+        gk = fmaf(GS[f * LD + c], sx[jj * LD + c], gk);
+        gv = fmaf(GS[c * LD + f], sk[jj * LD + c], gv);
       }
       for (int tt = jj; tt < cnt; ++tt) {
-        gk = fmaf(sE[jj * TQ + tt], sq[tt * D + f], gk);
-        gv = fmaf(sPm[jj * TQ + tt], sdn[tt * D + f], gv) + sgv[tt * D + f];
+        gk = fmaf(sE[jj * TQ + tt], sq[tt * LD + f], gk);
+        gv = fmaf(sPm[jj * TQ + tt], sdn[tt * LD + f], gv) + sgv[tt * LD + f];
       }
       const size_t off = tok_off(p, u, block_token(p, i, l0 + jj)) + f;
       xk[off] = w * gk;
@@ -394,23 +396,23 @@ causal_bwd_rev_kernel(Plan p, const T* __restrict__ Q, const T* __restrict__ K, 
       const int e = tid + m * kThreads;
       if (e < D * D) {
         float a = 0.f;
-        for (int tt = 0; tt < cnt; ++tt) a = fmaf(sq[tt * D + e / D], sdn[tt * D + e % D], a);
+        for (int tt = 0; tt < cnt; ++tt) a = fmaf(sq[tt * LD + e / D], sdn[tt * LD + e % D], a);
         acc[m] = a;
       }
     }
     if (tid < D) {
       float a = 0.f;
-      for (int tt = 0; tt < cnt; ++tt) a = fmaf(sds[tt], sq[tt * D + tid], a);
+      for (int tt = 0; tt < cnt; ++tt) a = fmaf(sds[tt], sq[tt * LD + tid], a);
       Gz[tid] += a;
     } else if (tid < 2 * D) {
       float a = 0.f;
-      for (int tt = 0; tt < cnt; ++tt) a += sgv[tt * D + tid - D];
+      for (int tt = 0; tt < cnt; ++tt) a += sgv[tt * LD + tid - D];
       Gv[tid - D] += a;
     }
 #pragma unroll
     for (int m = 0; m < PER; ++m) {
       const int e = tid + m * kThreads;
-      if (e < D * D) GS[e] += acc[m];
+      if (e < D * D) GS[e / D * LD + e % D] += acc[m];
     }
   }
 }
