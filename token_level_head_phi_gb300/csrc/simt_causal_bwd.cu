@@ -42,23 +42,39 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 
+// Tile geometry.  Each step of a kernel is a small product on shared
+// memory, split over the CTA so that a thread keeps a register tile and a
+// warp reads each operand value either as one broadcast or from 16-32
+// different banks (rows of the D-wide arrays are LD = D + 1 floats apart):
+//   token x feature  (TQ x D): 2 x RN per thread, rows t = mg + MG a,
+//                    columns c = nl + NL b (NL threads per row group, all
+//                    in one warp)
+//   token x token    (TQ x TQ): 2 x 2 per thread, rows ti + TH a, columns ji + TH b
+//   feature x feature (D x D): 4 x 4 per thread, rows fi + FQ a, columns ci + FQ b
 template <int D>
-struct TileTokens {
-  static constexpr int value = D <= 64 ? 32 : 16;
+struct Geo {
+  static constexpr int TQ = D <= 64 ? 32 : 16;  // tokens per tile
+  static constexpr int LD = D + 1;
+  static constexpr int MG = TQ / 2;
+  static constexpr int NL = kThreads / MG;
+  static constexpr int RN = D / NL;
+  static constexpr int TH = TQ / 2;
+  static constexpr int FQ = D / 4;
+  static constexpr int FT = (FQ * FQ + kThreads - 1) / kThreads;
+  static_assert(NL <= 32 && 32 % NL == 0 && RN >= 1 && RN * NL == D, "token x feature split");
+  static_assert(TH * TH <= kThreads && 2 * D <= kThreads, "tile split");
 };
 
-// Rows of the D-wide shared arrays are D + 1 floats apart, so that a warp
-// reading one column of D consecutive rows hits 32 different banks.
 template <int D>
 constexpr size_t fwd_smem_floats() {
-  constexpr int TQ = TileTokens<D>::value, LD = D + 1;
-  return 2 * D * LD + 4 * D + 5 * TQ * LD + TQ * TQ + 2 * TQ + 2 * kWarps;
+  using G = Geo<D>;
+  return 2 * D * G::LD + 4 * D + 5 * G::TQ * G::LD + G::TQ * G::TQ + 6 * G::TQ + 4 * kWarps;
 }
 
 template <int D>
 constexpr size_t rev_smem_floats() {
-  constexpr int TQ = TileTokens<D>::value, LD = D + 1;
-  return D * LD + 2 * D + 5 * TQ * LD + 2 * TQ * TQ + TQ;
+  using G = Geo<D>;
+  return D * G::LD + 2 * D + 5 * G::TQ * G::LD + 2 * G::TQ * G::TQ + G::TQ;
 }
 
 __device__ __forceinline__ float warp_sum(float x) {
@@ -67,24 +83,32 @@ __device__ __forceinline__ float warp_sum(float x) {
   return x;
 }
 
+// Sum over the NL threads of a row group (lanes aligned to NL in the warp).
+template <int NL>
+__device__ __forceinline__ float group_sum(float x) {
+#pragma unroll
+  for (int o = NL / 2; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
 __device__ __forceinline__ float phi_grad(float x, int fmap) { return phi_deriv(x, phi_apply(x, fmap), fmap); }
 
-// Shared memory: Sp_i (D*D), R (D*D), zp, vp, rz, rv (D each) | tiles of
-// phi(q), phi(k), v, dO, dnum (TQ*D each) | in-tile scores, later the
-// in-tile dq weights (TQ*TQ) | ds, gamma (TQ) | per-warp sums of the
-// diagonal term and of dn~.
+// Shared memory: C = Sp_i + w R and R (D rows each), zp, vp, rz, rv (D each)
+// | tiles of phi(q), phi(k), v, dO, dnum (TQ rows each) | in-tile scores,
+// later the in-tile dq weights E (TQ*TQ) | per token s, phi(q).rz, n, coef,
+// ds, gamma (TQ each) | per-warp sums of the diagonal term and of dn~.
 template <int D, typename T>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1)
 causal_bwd_fwd_kernel(Plan p, const T* __restrict__ Q, const T* __restrict__ K, const T* __restrict__ V,
                       const T* __restrict__ dO, const float* __restrict__ mixed,
                       const float* __restrict__ rowsum_lower, const float* __restrict__ mc, T* __restrict__ dQ,
                       float* __restrict__ dmixp, float* __restrict__ dnp, float* __restrict__ diag,
                       float* __restrict__ tokbuf) {
-  constexpr int TQ = TileTokens<D>::value, LD = D + 1;
-  constexpr int PER = (D * D + kThreads - 1) / kThreads;
+  using G = Geo<D>;
+  constexpr int TQ = G::TQ, LD = G::LD, MG = G::MG, NL = G::NL, RN = G::RN, TH = G::TH, FQ = G::FQ, FT = G::FT;
   extern __shared__ float sm[];
-  float* sP = sm;               // Sp_i
-  float* sR = sP + D * LD;      // in-block state R (without w)
+  float* sC = sm;               // Sp_i + w R
+  float* sR = sC + D * LD;      // in-block state R (without w)
   float* zP = sR + D * LD;
   float* vP = zP + D;
   float* zR = vP + D;
@@ -95,16 +119,21 @@ causal_bwd_fwd_kernel(Plan p, const T* __restrict__ Q, const T* __restrict__ K, 
   float* sg = sx + TQ * LD;     // dO
   float* sdn = sg + TQ * LD;    // dnum
   float* sa = sdn + TQ * LD;    // TQ*TQ
-  float* sds = sa + TQ * TQ;    // ds
+  float* ss = sa + TQ * TQ;     // s_t
+  float* ssin = ss + TQ;        // phi(q_t) . rz_t
+  float* snt = ssin + TQ;       // n_t
+  float* scf = snt + TQ;        // dnum_t / dO_t
+  float* sds = scf + TQ;        // ds
   float* sgm = sds + TQ;        // gamma
-  float* sdg = sgm + TQ;        // per-warp sums: diagonal term [kWarps], dn~ [kWarps]
+  double* sdg = reinterpret_cast<double*>(sgm + TQ);  // per-warp sums: diagonal term, dn~ [kWarps] each
   const int u = blockIdx.y, i = blockIdx.x;
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const int mg = tid / NL, nl = tid % NL;         // token x feature split
   const int jm = mc_index(p, u);
   const float w = mc[((size_t)jm * p.M + i) * p.M + i];
   const float* mrow = mixed + ((size_t)u * p.M + i) * p.R;
   for (int e = tid; e < D * D; e += kThreads) {
-    sP[e / D * LD + e % D] = mrow[e];
+    sC[e / D * LD + e % D] = mrow[e];
     sR[e / D * LD + e % D] = 0.f;
   }
   for (int e = tid; e < D; e += kThreads) {
@@ -116,10 +145,17 @@ causal_bwd_fwd_kernel(Plan p, const T* __restrict__ Q, const T* __restrict__ K, 
   const float n_pre = (float)p.nb * rowsum_lower[jm * p.M + i];
   const bool mala = p.norm == MHLA_NORM_MALA;
 
-  float acc[PER];
+  float acc[FT][4][4];          // dSp_i, feature x feature tiles
 #pragma unroll
-  for (int m = 0; m < PER; ++m) acc[m] = 0.f;
-  float zacc = 0.f, vacc = 0.f, nacc = 0.f, dacc = 0.f;
+  for (int x = 0; x < FT; ++x)
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int b = 0; b < 4; ++b) acc[x][a][b] = 0.f;
+  float zacc = 0.f, vacc = 0.f;
+  // the diagonal term sums many cancelling per-token terms: formed and
+  // summed in double
+  double nacc = 0.0, dacc = 0.0;
   float rn = 0.f;  // tokens of the block before the tile
 
   for (int l0 = 0; l0 < p.nb; l0 += TQ) {
@@ -142,130 +178,252 @@ causal_bwd_fwd_kernel(Plan p, const T* __restrict__ Q, const T* __restrict__ K, 
     }
     __syncthreads();
     // masked in-tile scores a[t][j] = phi(q_t) . phi(k_j), j <= t
-    for (int e = tid; e < TQ * TQ; e += kThreads) {
-      const int tt = e / TQ, jj = e % TQ;
-      float a = 0.f;
-      if (jj <= tt && tt < cnt)
-        for (int f = 0; f < D; ++f) a = fmaf(sq[tt * LD + f], sk[jj * LD + f], a);
-      sa[e] = a;
+    if (tid < TH * TH) {
+      const int ti = tid / TH, ji = tid % TH;
+      float c2[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+      for (int f = 0; f < D; ++f) {
+        const float q0 = sq[ti * LD + f], q1 = sq[(ti + TH) * LD + f];
+        const float k0 = sk[ji * LD + f], k1 = sk[(ji + TH) * LD + f];
+        c2[0][0] = fmaf(q0, k0, c2[0][0]);
+        c2[0][1] = fmaf(q0, k1, c2[0][1]);
+        c2[1][0] = fmaf(q1, k0, c2[1][0]);
+        c2[1][1] = fmaf(q1, k1, c2[1][1]);
+      }
+#pragma unroll
+      for (int a = 0; a < 2; ++a)
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+          const int tt = ti + TH * a, jj = ji + TH * b;
+          sa[tt * TQ + jj] = (jj <= tt && tt < cnt) ? c2[a][b] : 0.f;
+        }
+    }
+    // phi(q_t)^T C and phi(q_t)^T R, kept in registers for the norm step
+    float ac[2][RN], ar[2][RN];
+#pragma unroll
+    for (int a = 0; a < 2; ++a)
+#pragma unroll
+      for (int b = 0; b < RN; ++b) ac[a][b] = ar[a][b] = 0.f;
+    for (int f = 0; f < D; ++f) {
+      const float x0 = sq[mg * LD + f], x1 = sq[(mg + MG) * LD + f];
+#pragma unroll
+      for (int b = 0; b < RN; ++b) {
+        const float cv = sC[f * LD + nl + NL * b], rv = sR[f * LD + nl + NL * b];
+        ac[0][b] = fmaf(x0, cv, ac[0][b]);
+        ac[1][b] = fmaf(x1, cv, ac[1][b]);
+        ar[0][b] = fmaf(x0, rv, ar[0][b]);
+        ar[1][b] = fmaf(x1, rv, ar[1][b]);
+      }
     }
     __syncthreads();
-    // one warp per query: its state, norm gradients and diagonal term
-    for (int tt = warp; tt < cnt; tt += kWarps) {
+    // per token: s_t, phi(q_t) . rz_t, n_t and dnum_t / dO_t
+    for (int tt = warp; tt < TQ; tt += kWarps) {
       float sp = 0.f, sin = 0.f;
       for (int f = lane; f < D; f += 32) {
         sp = fmaf(sq[tt * LD + f], zP[f], sp);
         sin = fmaf(sq[tt * LD + f], zR[f], sin);
       }
-      for (int jj = lane; jj <= tt; jj += 32) sin += sa[tt * TQ + jj];
+      if (lane < TQ) sin += sa[tt * TQ + lane];
       sp = warp_sum(sp);
-      sin = warp_sum(sin);                      // phi(q_t) . rz_t
-      const float s = fmaf(w, sin, sp);
-      const float rnt = rn + (float)(tt + 1);   // rn_t
-      const float nt = fmaf(w, rnt, n_pre);
-      const bool live = p.norm == MHLA_NORM_NONE || s != 0.f;
-      const float coef =
-          !live ? 0.f : (p.norm == MHLA_NORM_DIVISIVE ? 1.f / s : (mala ? 1.f + 1.f / s : 1.f));  // dnum / dO
-      float gnum = 0.f, gvt = 0.f, gain = 0.f, gvin = 0.f;
-      for (int c = lane; c < D; c += 32) {
-        float ap = 0.f, ar = 0.f, loc = 0.f, vloc = 0.f;
-        for (int f = 0; f < D; ++f) {
-          const float x = sq[tt * LD + f];
-          ap = fmaf(x, sP[f * LD + c], ap);
-          ar = fmaf(x, sR[f * LD + c], ar);
-        }
-        for (int jj = 0; jj <= tt; ++jj) {
-          loc = fmaf(sa[tt * TQ + jj], sx[jj * LD + c], loc);
-          vloc += sx[jj * LD + c];
-        }
-        const float ain = ar + loc;                 // phi(q_t)^T R_t, column c
-        const float num = fmaf(w, ain, ap);
-        const float vin = vR[c] + vloc;             // rv_t
-        const float vt = fmaf(w, vin, vP[c]);
-        const float g = sg[tt * LD + c];
-        gnum = fmaf(g, num, gnum);
-        gvt = fmaf(g, vt, gvt);
-        gain = fmaf(g, ain, gain);
-        gvin = fmaf(g, vin, gvin);
-        sdn[tt * LD + c] = coef * g;
-      }
-      gnum = warp_sum(gnum);
-      gvt = warp_sum(gvt);
-      gain = warp_sum(gain);
-      gvin = warp_sum(gvin);
-      float ds = 0.f, gamma = 0.f, dnt = 0.f;
-      if (live && p.norm == MHLA_NORM_DIVISIVE) {
-        ds = -gnum / (s * s);
-      } else if (live && mala) {
-        const float dgamma = -gvt;
-        ds = -gnum / (s * s) + dgamma / nt;
-        gamma = s / nt;
-        dnt = -dgamma * s / (nt * nt);
-      }
+      sin = warp_sum(sin);
       if (lane == 0) {
-        sds[tt] = ds;
-        sgm[tt] = gamma;
-        // <dS~_t, R_t> + ds_t (phi(q_t) . rz_t) + <dv~_t, rv_t> + dn~_t rn_t
-        dacc += coef * gain + ds * sin - gamma * gvin + dnt * rnt;
-        nacc += dnt;
+        const float s = fmaf(w, sin, sp);
+        const float nt = fmaf(w, rn + (float)(tt + 1), n_pre);
+        const bool live = tt < cnt && (p.norm == MHLA_NORM_NONE || s != 0.f);
+        ss[tt] = s;
+        ssin[tt] = sin;
+        snt[tt] = nt;
+        scf[tt] = !live ? 0.f : (p.norm == MHLA_NORM_DIVISIVE ? 1.f / s : (mala ? 1.f + 1.f / s : 1.f));
+      }
+    }
+    __syncthreads();
+    // phi(q_t)^T R_t's in-tile part sum_{j<=t} a[t][j] v_j and rv_t's sum_{j<=t} v_j;
+    // then the norm gradients of each token
+    {
+      float lo[2][RN], vl[2][RN];
+#pragma unroll
+      for (int a = 0; a < 2; ++a)
+#pragma unroll
+        for (int b = 0; b < RN; ++b) lo[a][b] = vl[a][b] = 0.f;
+      const int t0 = mg, t1 = mg + MG;
+      for (int jj = 0; jj < cnt; ++jj) {
+        const float a0 = sa[t0 * TQ + jj], a1 = sa[t1 * TQ + jj];
+        const float m0 = jj <= t0 ? 1.f : 0.f, m1 = jj <= t1 ? 1.f : 0.f;
+#pragma unroll
+        for (int b = 0; b < RN; ++b) {
+          const float xv = sx[jj * LD + nl + NL * b];
+          lo[0][b] = fmaf(a0, xv, lo[0][b]);
+          lo[1][b] = fmaf(a1, xv, lo[1][b]);
+          vl[0][b] = fmaf(m0, xv, vl[0][b]);
+          vl[1][b] = fmaf(m1, xv, vl[1][b]);
+        }
+      }
+#pragma unroll
+      for (int a = 0; a < 2; ++a) {
+        const int tt = mg + MG * a;
+        const float coef = scf[tt];
+        float gnum = 0.f, gvt = 0.f, gain = 0.f, gvin = 0.f;
+#pragma unroll
+        for (int b = 0; b < RN; ++b) {
+          const int c = nl + NL * b;
+          const float ain = ar[a][b] + lo[a][b];      // phi(q_t)^T R_t, column c
+          const float num = fmaf(w, lo[a][b], ac[a][b]);
+          const float vin = vR[c] + vl[a][b];          // rv_t
+          const float vt = fmaf(w, vin, vP[c]);
+          const float g = sg[tt * LD + c];
+          gnum = fmaf(g, num, gnum);
+          gvt = fmaf(g, vt, gvt);
+          gain = fmaf(g, ain, gain);
+          gvin = fmaf(g, vin, gvin);
+          sdn[tt * LD + c] = coef * g;
+        }
+        gnum = group_sum<NL>(gnum);
+        gvt = group_sum<NL>(gvt);
+        gain = group_sum<NL>(gain);
+        gvin = group_sum<NL>(gvin);
+        if (nl == 0) {
+          const float s = ss[tt], sin = ssin[tt], nt = snt[tt];
+          const float rnt = rn + (float)(tt + 1);
+          const bool live = tt < cnt && (p.norm == MHLA_NORM_NONE || s != 0.f);
+          float ds = 0.f, gamma = 0.f, dnt = 0.f;
+          if (live && p.norm == MHLA_NORM_DIVISIVE) {
+            ds = -gnum / (s * s);
+          } else if (live && mala) {
+            const float dgamma = -gvt;
+            ds = -gnum / (s * s) + dgamma / nt;
+            gamma = s / nt;
+            dnt = -dgamma * s / (nt * nt);
+          }
+          sds[tt] = ds;
+          sgm[tt] = gamma;
+          if (tt < cnt) {
+            // <dS~_t, R_t> + ds_t (phi(q_t) . rz_t) + <dv~_t, rv_t> + dn~_t rn_t
+            dacc += (double)coef * gain + (double)ds * sin - (double)gamma * gvin + (double)dnt * rnt;
+            nacc += dnt;
+          }
+        }
       }
     }
     __syncthreads();
     // in-tile dq weights E[t][j] = v_j . dnum_t + ds_t, j <= t
-    for (int e = tid; e < TQ * TQ; e += kThreads) {
-      const int tt = e / TQ, jj = e % TQ;
-      float a = 0.f;
-      if (jj <= tt && tt < cnt) {
-        a = sds[tt];
-        for (int c = 0; c < D; ++c) a = fmaf(sx[jj * LD + c], sdn[tt * LD + c], a);
+    if (tid < TH * TH) {
+      const int ti = tid / TH, ji = tid % TH;
+      float c2[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+      for (int c = 0; c < D; ++c) {
+        const float d0 = sdn[ti * LD + c], d1 = sdn[(ti + TH) * LD + c];
+        const float x0 = sx[ji * LD + c], x1 = sx[(ji + TH) * LD + c];
+        c2[0][0] = fmaf(d0, x0, c2[0][0]);
+        c2[0][1] = fmaf(d0, x1, c2[0][1]);
+        c2[1][0] = fmaf(d1, x0, c2[1][0]);
+        c2[1][1] = fmaf(d1, x1, c2[1][1]);
       }
-      sa[e] = a;
+#pragma unroll
+      for (int a = 0; a < 2; ++a)
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+          const int tt = ti + TH * a, jj = ji + TH * b;
+          sa[tt * TQ + jj] = (jj <= tt && tt < cnt) ? c2[a][b] + sds[tt] : 0.f;
+        }
     }
     __syncthreads();
-    // dq_t = ((Sp + w R) dnum_t + (zp + w rz) ds_t + w sum_{j<=t} E[t][j] phi(k_j)) phi'(q_t)
-    for (int e = tid; e < cnt * D; e += kThreads) {
-      const int tt = e / D, k = e % D;
-      float a = 0.f;
-      for (int c = 0; c < D; ++c) a = fmaf(fmaf(w, sR[k * LD + c], sP[k * LD + c]), sdn[tt * LD + c], a);
-      a = fmaf(fmaf(w, zR[k], zP[k]), sds[tt], a);
-      float loc = 0.f;
-      for (int jj = 0; jj <= tt; ++jj) loc = fmaf(sa[tt * TQ + jj], sk[jj * LD + k], loc);
-      a = fmaf(w, loc, a);
-      const size_t off = tok_off(p, u, block_token(p, i, l0 + tt)) + k;
-      dQ[off] = from_f32<T>(a * phi_grad(to_f32(Q[off]), p.fmap));
-    }
-    // dSp += phi(q_t) dnum_t^T, dzp += ds_t phi(q_t), dvp += -gamma_t dO_t
-    for (int tt = 0; tt < cnt; ++tt) {
+    // dq_t = (C dnum_t + (zp + w rz) ds_t + w sum_{j<=t} E[t][j] phi(k_j)) phi'(q_t)
+    {
+      float dqa[2][RN], lk[2][RN];
 #pragma unroll
-      for (int m = 0; m < PER; ++m) {
-        const int e = tid + m * kThreads;
-        if (e < D * D) acc[m] = fmaf(sq[tt * LD + e / D], sdn[tt * LD + e % D], acc[m]);
+      for (int a = 0; a < 2; ++a)
+#pragma unroll
+        for (int b = 0; b < RN; ++b) dqa[a][b] = lk[a][b] = 0.f;
+      const int t0 = mg, t1 = mg + MG;
+      for (int c = 0; c < D; ++c) {
+        const float d0 = sdn[t0 * LD + c], d1 = sdn[t1 * LD + c];
+#pragma unroll
+        for (int b = 0; b < RN; ++b) {
+          const float cv = sC[(nl + NL * b) * LD + c];
+          dqa[0][b] = fmaf(d0, cv, dqa[0][b]);
+          dqa[1][b] = fmaf(d1, cv, dqa[1][b]);
+        }
       }
-      if (tid < D) zacc = fmaf(sds[tt], sq[tt * LD + tid], zacc);
-      else if (tid < 2 * D && mala) vacc = fmaf(-sgm[tt], sg[tt * LD + tid - D], vacc);
+      for (int jj = 0; jj < cnt; ++jj) {
+        const float e0 = sa[t0 * TQ + jj], e1 = sa[t1 * TQ + jj];
+#pragma unroll
+        for (int b = 0; b < RN; ++b) {
+          const float kv = sk[jj * LD + nl + NL * b];
+          lk[0][b] = fmaf(e0, kv, lk[0][b]);
+          lk[1][b] = fmaf(e1, kv, lk[1][b]);
+        }
+      }
+#pragma unroll
+      for (int a = 0; a < 2; ++a) {
+        const int tt = mg + MG * a;
+        if (tt >= cnt) continue;
+        const size_t base = tok_off(p, u, block_token(p, i, l0 + tt));
+#pragma unroll
+        for (int b = 0; b < RN; ++b) {
+          const int k = nl + NL * b;
+          const float x = fmaf(w, lk[a][b], fmaf(fmaf(w, zR[k], zP[k]), sds[tt], dqa[a][b]));
+          dQ[base + k] = from_f32<T>(x * phi_grad(to_f32(Q[base + k]), p.fmap));
+        }
+      }
+    }
+    __syncthreads();
+    // dSp += phi(q_t) dnum_t^T and the in-block state R += phi(k_j) v_j^T (C by w times it)
+#pragma unroll
+    for (int x = 0; x < FT; ++x) {
+      const int qd = tid + kThreads * x;
+      if (qd >= FQ * FQ) break;
+      const int fi = qd / FQ, ci = qd % FQ;
+      float st[4][4];
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) st[a][b] = 0.f;
+      for (int tt = 0; tt < cnt; ++tt) {
+        float qa[4], ka[4], db[4], xb[4];
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+          qa[a] = sq[tt * LD + fi + FQ * a];
+          ka[a] = sk[tt * LD + fi + FQ * a];
+          db[a] = sdn[tt * LD + ci + FQ * a];
+          xb[a] = sx[tt * LD + ci + FQ * a];
+        }
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+          for (int b = 0; b < 4; ++b) {
+            acc[x][a][b] = fmaf(qa[a], db[b], acc[x][a][b]);
+            st[a][b] = fmaf(ka[a], xb[b], st[a][b]);
+          }
+      }
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          const int e = (fi + FQ * a) * LD + ci + FQ * b;
+          sR[e] += st[a][b];
+          sC[e] = fmaf(w, st[a][b], sC[e]);
+        }
+    }
+    // dzp += ds_t phi(q_t), dvp += -gamma_t dO_t; rz, rv advance by the tile
+    if (tid < D) {
+      float z = 0.f;
+      for (int tt = 0; tt < cnt; ++tt) {
+        zacc = fmaf(sds[tt], sq[tt * LD + tid], zacc);
+        z += sk[tt * LD + tid];
+      }
+      zR[tid] += z;
+    } else if (tid < 2 * D) {
+      const int c = tid - D;
+      float z = 0.f;
+      for (int tt = 0; tt < cnt; ++tt) {
+        if (mala) vacc = fmaf(-sgm[tt], sg[tt * LD + c], vacc);
+        z += sx[tt * LD + c];
+      }
+      vR[c] += z;
     }
     // per token for the reverse walk: dnum (D), ds, gamma
     for (int e = tid; e < cnt * (D + 2); e += kThreads) {
       const int tt = e / (D + 2), c = e % (D + 2);
       const float x = c < D ? sdn[tt * LD + c] : (c == D ? sds[tt] : sgm[tt]);
       tokbuf[((size_t)u * p.N + block_token(p, i, l0 + tt)) * (D + 2) + c] = x;
-    }
-    __syncthreads();
-    // advance the in-block state by the whole tile
-    for (int e = tid; e < D * D; e += kThreads) {
-      const int f = e / D, c = e % D;
-      float a = 0.f;
-      for (int jj = 0; jj < cnt; ++jj) a = fmaf(sk[jj * LD + f], sx[jj * LD + c], a);
-      sR[f * LD + c] += a;
-    }
-    if (tid < D) {
-      float a = 0.f;
-      for (int jj = 0; jj < cnt; ++jj) a += sk[jj * LD + tid];
-      zR[tid] += a;
-    } else if (tid < 2 * D) {
-      float a = 0.f;
-      for (int jj = 0; jj < cnt; ++jj) a += sx[jj * LD + tid - D];
-      vR[tid - D] += a;
     }
     rn += (float)cnt;
   }
@@ -279,38 +437,48 @@ causal_bwd_fwd_kernel(Plan p, const T* __restrict__ Q, const T* __restrict__ K, 
   }
   float* out = dmixp + row0 * p.R;
 #pragma unroll
-  for (int m = 0; m < PER; ++m) {
-    const int e = tid + m * kThreads;
-    if (e < D * D) out[e] = acc[m];
+  for (int x = 0; x < FT; ++x) {
+    const int qd = tid + kThreads * x;
+    if (qd >= FQ * FQ) break;
+    const int fi = qd / FQ, ci = qd % FQ;
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int b = 0; b < 4; ++b) out[(fi + FQ * a) * D + ci + FQ * b] = acc[x][a][b];
   }
   if (tid < D) out[D * D + tid] = zacc;
   else if (tid < 2 * D) out[D * D + tid] = vacc;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    dacc += __shfl_xor_sync(0xffffffffu, dacc, o);
+    nacc += __shfl_xor_sync(0xffffffffu, nacc, o);
+  }
   if (lane == 0) {
     sdg[warp] = dacc;
     sdg[kWarps + warp] = nacc;
   }
   __syncthreads();
   if (tid == 0) {
-    float t = 0.f, n = 0.f;
+    double t = 0.0, n = 0.0;
     for (int x = 0; x < kWarps; ++x) {
       t += sdg[x];
       n += sdg[kWarps + x];
     }
-    diag[(size_t)u * p.M + i] = t;
-    dnp[row0] = n;
+    diag[(size_t)u * p.M + i] = (float)t;
+    dnp[row0] = (float)n;
   }
 }
 
-// Shared memory: GS (D*D), Gz, Gv (D) | tiles of phi(q), phi(k), v, dnum,
-// dv~ (TQ*D each) | E[j][t] = dnum_t . v_j + ds_t and P[j][t] = phi(q_t) .
-// phi(k_j), t >= j (TQ*TQ each) | ds (TQ).
+// Shared memory: GS (D rows), Gz, Gv (D) | tiles of phi(q), phi(k), v,
+// dnum, dv~ (TQ rows each) | E[j][t] = dnum_t . v_j + ds_t and P[j][t] =
+// phi(q_t) . phi(k_j), t >= j (TQ*TQ each) | ds (TQ).
 template <int D, typename T>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1)
 causal_bwd_rev_kernel(Plan p, const T* __restrict__ Q, const T* __restrict__ K, const T* __restrict__ V,
                       const T* __restrict__ dO, const float* __restrict__ mc, const float* __restrict__ tokbuf,
                       float* __restrict__ xk, float* __restrict__ xv) {
-  constexpr int TQ = TileTokens<D>::value, LD = D + 1;
-  constexpr int PER = (D * D + kThreads - 1) / kThreads;
+  using G = Geo<D>;
+  constexpr int TQ = G::TQ, LD = G::LD, MG = G::MG, NL = G::NL, RN = G::RN, TH = G::TH, FQ = G::FQ, FT = G::FT;
   extern __shared__ float sm[];
   float* GS = sm;
   float* Gz = GS + D * LD;
@@ -324,13 +492,11 @@ causal_bwd_rev_kernel(Plan p, const T* __restrict__ Q, const T* __restrict__ K, 
   float* sPm = sE + TQ * TQ;
   float* sds = sPm + TQ * TQ;
   const int u = blockIdx.y, i = blockIdx.x, tid = threadIdx.x;
+  const int mg = tid / NL, nl = tid % NL;
   const int jm = mc_index(p, u);
   const float w = mc[((size_t)jm * p.M + i) * p.M + i];
   const bool mala = p.norm == MHLA_NORM_MALA;
   for (int e = tid; e < D * LD + 2 * D; e += kThreads) sm[e] = 0.f;
-  float acc[PER];
-#pragma unroll
-  for (int m = 0; m < PER; ++m) acc[m] = 0.f;
 
   for (int l0 = (p.nb - 1) / TQ * TQ; l0 >= 0; l0 -= TQ) {
     const int cnt = min(TQ, p.nb - l0);
@@ -358,47 +524,112 @@ causal_bwd_rev_kernel(Plan p, const T* __restrict__ Q, const T* __restrict__ K, 
       sgv[tt * LD + f] = gv;
     }
     __syncthreads();
-    for (int e = tid; e < TQ * TQ; e += kThreads) {
-      const int jj = e / TQ, tt = e % TQ;
-      float a = 0.f, b = 0.f;
-      if (tt >= jj && tt < cnt) {
-        a = sds[tt];
-        for (int f = 0; f < D; ++f) {
-          a = fmaf(sdn[tt * LD + f], sx[jj * LD + f], a);
-          b = fmaf(sq[tt * LD + f], sk[jj * LD + f], b);
-        }
+    // E[j][t] and P[j][t] for t >= j
+    if (tid < TH * TH) {
+      const int ji = tid / TH, ti = tid % TH;
+      float e2[2][2] = {{0.f, 0.f}, {0.f, 0.f}}, p2[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+      for (int f = 0; f < D; ++f) {
+        const float x0 = sx[ji * LD + f], x1 = sx[(ji + TH) * LD + f];
+        const float k0 = sk[ji * LD + f], k1 = sk[(ji + TH) * LD + f];
+        const float d0 = sdn[ti * LD + f], d1 = sdn[(ti + TH) * LD + f];
+        const float q0 = sq[ti * LD + f], q1 = sq[(ti + TH) * LD + f];
+        e2[0][0] = fmaf(x0, d0, e2[0][0]);
+        e2[0][1] = fmaf(x0, d1, e2[0][1]);
+        e2[1][0] = fmaf(x1, d0, e2[1][0]);
+        e2[1][1] = fmaf(x1, d1, e2[1][1]);
+        p2[0][0] = fmaf(k0, q0, p2[0][0]);
+        p2[0][1] = fmaf(k0, q1, p2[0][1]);
+        p2[1][0] = fmaf(k1, q0, p2[1][0]);
+        p2[1][1] = fmaf(k1, q1, p2[1][1]);
       }
-      sE[e] = a;
-      sPm[e] = b;
+#pragma unroll
+      for (int a = 0; a < 2; ++a)
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+          const int jj = ji + TH * a, tt = ti + TH * b;
+          const bool on = tt >= jj && tt < cnt;
+          sE[jj * TQ + tt] = on ? e2[a][b] + sds[tt] : 0.f;
+          sPm[jj * TQ + tt] = on ? p2[a][b] : 0.f;
+        }
     }
     __syncthreads();
     // in-block parts for token j: w (GS v_j + Gz + sum_{t>=j} E[j][t] phi(q_t)) and
     // w (GS^T phi(k_j) + Gv + sum_{t>=j} (P[j][t] dnum_t + dv~_t))
-    for (int e = tid; e < cnt * D; e += kThreads) {
-      const int jj = e / D, f = e % D;
-      float gk = Gz[f], gv = Gv[f];
+    {
+      float gk[2][RN], gv[2][RN];
+      const int j0 = mg, j1 = mg + MG;
+#pragma unroll
+      for (int b = 0; b < RN; ++b) {
+        gk[0][b] = gk[1][b] = Gz[nl + NL * b];
+        gv[0][b] = gv[1][b] = Gv[nl + NL * b];
+      }
       for (int c = 0; c < D; ++c) {
-        gk = fmaf(GS[f * LD + c], sx[jj * LD + c], gk);
-        gv = fmaf(GS[c * LD + f], sk[jj * LD + c], gv);
+        const float x0 = sx[j0 * LD + c], x1 = sx[j1 * LD + c];
+        const float k0 = sk[j0 * LD + c], k1 = sk[j1 * LD + c];
+#pragma unroll
+        for (int b = 0; b < RN; ++b) {
+          const int f = nl + NL * b;
+          const float gf = GS[f * LD + c], gc = GS[c * LD + f];
+          gk[0][b] = fmaf(gf, x0, gk[0][b]);
+          gk[1][b] = fmaf(gf, x1, gk[1][b]);
+          gv[0][b] = fmaf(gc, k0, gv[0][b]);
+          gv[1][b] = fmaf(gc, k1, gv[1][b]);
+        }
       }
-      for (int tt = jj; tt < cnt; ++tt) {
-        gk = fmaf(sE[jj * TQ + tt], sq[tt * LD + f], gk);
-        gv = fmaf(sPm[jj * TQ + tt], sdn[tt * LD + f], gv) + sgv[tt * LD + f];
+      for (int tt = 0; tt < cnt; ++tt) {
+        const float e0 = sE[j0 * TQ + tt], e1 = sE[j1 * TQ + tt];
+        const float p0 = sPm[j0 * TQ + tt], p1 = sPm[j1 * TQ + tt];
+        const float m0 = tt >= j0 ? 1.f : 0.f, m1 = tt >= j1 ? 1.f : 0.f;
+#pragma unroll
+        for (int b = 0; b < RN; ++b) {
+          const int f = nl + NL * b;
+          const float qv = sq[tt * LD + f], dv = sdn[tt * LD + f], gt = sgv[tt * LD + f];
+          gk[0][b] = fmaf(e0, qv, gk[0][b]);
+          gk[1][b] = fmaf(e1, qv, gk[1][b]);
+          gv[0][b] = fmaf(m0, gt, fmaf(p0, dv, gv[0][b]));
+          gv[1][b] = fmaf(m1, gt, fmaf(p1, dv, gv[1][b]));
+        }
       }
-      const size_t off = tok_off(p, u, block_token(p, i, l0 + jj)) + f;
-      xk[off] = w * gk;
-      xv[off] = w * gv;
+#pragma unroll
+      for (int a = 0; a < 2; ++a) {
+        const int jj = mg + MG * a;
+        if (jj >= cnt) continue;
+        const size_t base = tok_off(p, u, block_token(p, i, l0 + jj));
+#pragma unroll
+        for (int b = 0; b < RN; ++b) {
+          xk[base + nl + NL * b] = w * gk[a][b];
+          xv[base + nl + NL * b] = w * gv[a][b];
+        }
+      }
     }
     __syncthreads();
     // the tile joins the suffix sums
 #pragma unroll
-    for (int m = 0; m < PER; ++m) {
-      const int e = tid + m * kThreads;
-      if (e < D * D) {
-        float a = 0.f;
-        for (int tt = 0; tt < cnt; ++tt) a = fmaf(sq[tt * LD + e / D], sdn[tt * LD + e % D], a);
-        acc[m] = a;
+    for (int x = 0; x < FT; ++x) {
+      const int qd = tid + kThreads * x;
+      if (qd >= FQ * FQ) break;
+      const int fi = qd / FQ, ci = qd % FQ;
+      float st[4][4];
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) st[a][b] = 0.f;
+      for (int tt = 0; tt < cnt; ++tt) {
+        float qa[4], db[4];
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+          qa[a] = sq[tt * LD + fi + FQ * a];
+          db[a] = sdn[tt * LD + ci + FQ * a];
+        }
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+          for (int b = 0; b < 4; ++b) st[a][b] = fmaf(qa[a], db[b], st[a][b]);
       }
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) GS[(fi + FQ * a) * LD + ci + FQ * b] += st[a][b];
     }
     if (tid < D) {
       float a = 0.f;
@@ -408,11 +639,6 @@ causal_bwd_rev_kernel(Plan p, const T* __restrict__ Q, const T* __restrict__ K, 
       float a = 0.f;
       for (int tt = 0; tt < cnt; ++tt) a += sgv[tt * LD + tid - D];
       Gv[tid - D] += a;
-    }
-#pragma unroll
-    for (int m = 0; m < PER; ++m) {
-      const int e = tid + m * kThreads;
-      if (e < D * D) GS[e / D * LD + e % D] += acc[m];
     }
   }
 }
