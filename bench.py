@@ -539,7 +539,7 @@ BWD_LAUNCHES = {"simt": 7, "simt_causal": 9, "tc": 10}
 def simt_mc_reduce_launches(w, mc_heads):
     """1 when the CUDA-core dMc kernel splits its units over groups (then a
     reduce kernel follows): fewer tiles than about four CTAs per SM."""
-    tiles = ((w.n_blocks + 15) // 16) ** 2 * mc_heads
+    tiles = ((w.n_blocks + 63) // 64) ** 2 * mc_heads
     units = w.units if mc_heads == 1 else w.batch
     return int(min(-(-608 // tiles), units, 64) > 1)
 FP32_LANES_PER_SM = 128  # FP32 FMA lanes per SM (4 partitions x 32)

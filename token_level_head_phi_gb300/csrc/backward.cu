@@ -39,6 +39,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kTile = 32;  // tokens per shared-memory tile
+constexpr int kMcTile = 64;  // dMc entries per CTA side
 
 __device__ __forceinline__ float phi_grad(float x, int fmap) { return phi_deriv(x, phi_apply(x, fmap), fmap); }
 
@@ -51,14 +52,15 @@ bwd_output_kernel(Plan p, const T* __restrict__ Q, const T* __restrict__ dO, con
                   const float* __restrict__ rowsum, T* __restrict__ dQ, float* __restrict__ dmixp,
                   float* __restrict__ dnp) {
   constexpr int PER = (D * D + kThreads - 1) / kThreads;
+  constexpr int LD = D + 1;        // row stride: a column of consecutive rows spans 32 banks
   extern __shared__ float sm[];
-  float* sS = sm;                  // D*D
-  float* sz = sS + D * D;          // D
+  float* sS = sm;                  // D rows
+  float* sz = sS + D * LD;         // D
   float* sv = sz + D;              // D
-  float* sq = sv + D;              // kTile*D: phi(q)
-  float* sg = sq + kTile * D;      // kTile*D: dO
-  float* sdn = sg + kTile * D;     // kTile*D: dnum
-  float* sds = sdn + kTile * D;    // kTile: ds
+  float* sq = sv + D;              // kTile rows: phi(q)
+  float* sg = sq + kTile * LD;     // kTile rows: dO
+  float* sdn = sg + kTile * LD;    // kTile rows: dnum
+  float* sds = sdn + kTile * LD;   // kTile: ds
   float* ssc = sds + kTile;        // kTile: s
   float* sgam = ssc + kTile;       // kTile: gamma (MALA)
   float* sdgam = sgam + kTile;     // kTile: dO . v~ (MALA)
@@ -69,7 +71,8 @@ bwd_output_kernel(Plan p, const T* __restrict__ Q, const T* __restrict__ dO, con
   const int l1 = min(p.nb, l0 + p.split_len);
   const int tid = threadIdx.x;
   const float* mrow = mixed + ((size_t)u * p.M + i) * p.R;
-  for (int e = tid; e < D * D + 2 * D; e += kThreads) sm[e] = mrow[e];
+  for (int e = tid; e < D * D; e += kThreads) sS[e / D * LD + e % D] = mrow[e];
+  for (int e = tid; e < 2 * D; e += kThreads) sz[e] = mrow[D * D + e];
   const float ntilde = (float)p.nb * rowsum[mc_index(p, u) * p.M + i];
 
   float acc[PER];
@@ -88,16 +91,16 @@ bwd_output_kernel(Plan p, const T* __restrict__ Q, const T* __restrict__ dO, con
         qx = phi_apply(to_f32(Q[off]), p.fmap);
         gx = to_f32(dO[off]);
       }
-      sq[e] = qx;
-      sg[e] = gx;
+      sq[tt * LD + f] = qx;
+      sg[tt * LD + f] = gx;
     }
     __syncthreads();
     // per token: s = phi(q).z~ and the dO.v~ of MALA
     if (tid < kTile) {
       float s = 0.f, gv = 0.f;
       for (int k = 0; k < D; ++k) {
-        s = fmaf(sq[tid * D + k], sz[k], s);
-        gv = fmaf(sg[tid * D + k], sv[k], gv);
+        s = fmaf(sq[tid * LD + k], sz[k], s);
+        gv = fmaf(sg[tid * LD + k], sv[k], gv);
       }
       ssc[tid] = s;
       sdgam[tid] = gv;
@@ -107,21 +110,21 @@ bwd_output_kernel(Plan p, const T* __restrict__ Q, const T* __restrict__ dO, con
     for (int e = tid; e < kTile * D; e += kThreads) {
       const int tt = e / D, c = e % D;
       float num = 0.f;
-      for (int k = 0; k < D; ++k) num = fmaf(sq[tt * D + k], sS[k * D + c], num);
-      const float g = sg[e];
+      for (int k = 0; k < D; ++k) num = fmaf(sq[tt * LD + k], sS[k * LD + c], num);
+      const float g = sg[tt * LD + c];
       const float s = ssc[tt];
       float dn;
       if (p.norm == MHLA_NORM_DIVISIVE) dn = s != 0.f ? g / s : 0.f;   // s = 0: constant output
       else if (p.norm == MHLA_NORM_MALA) dn = s != 0.f ? (1.f + 1.f / s) * g : 0.f;
       else dn = g;
-      sdn[e] = dn;
+      sdn[tt * LD + c] = dn;
       // g * num replaces g: only the per-token sum dO . num is needed below
-      sg[e] = g * num;
+      sg[tt * LD + c] = g * num;
     }
     __syncthreads();
     if (tid < kTile) {
       float gnum = 0.f;
-      for (int c = 0; c < D; ++c) gnum += sg[tid * D + c];
+      for (int c = 0; c < D; ++c) gnum += sg[tid * LD + c];
       const float s = ssc[tid];
       float ds = 0.f;
       if (p.norm == MHLA_NORM_DIVISIVE) {
@@ -139,7 +142,7 @@ bwd_output_kernel(Plan p, const T* __restrict__ Q, const T* __restrict__ dO, con
     for (int e = tid; e < cnt * D; e += kThreads) {
       const int tt = e / D, k = e % D;
       float a = sz[k] * sds[tt];
-      for (int c = 0; c < D; ++c) a = fmaf(sS[k * D + c], sdn[tt * D + c], a);
+      for (int c = 0; c < D; ++c) a = fmaf(sS[k * LD + c], sdn[tt * LD + c], a);
       const size_t off = tok_off(p, u, block_token(p, i, lt + tt)) + k;
       dQ[off] = from_f32<T>(a * phi_grad(to_f32(Q[off]), p.fmap));
     }
@@ -148,10 +151,10 @@ bwd_output_kernel(Plan p, const T* __restrict__ Q, const T* __restrict__ dO, con
 #pragma unroll
       for (int j = 0; j < PER; ++j) {
         const int e = tid + j * kThreads;
-        if (e < D * D) acc[j] = fmaf(sq[tt * D + e / D], sdn[tt * D + e % D], acc[j]);
+        if (e < D * D) acc[j] = fmaf(sq[tt * LD + e / D], sdn[tt * LD + e % D], acc[j]);
       }
       if (tid < D) {
-        zacc = fmaf(sds[tt], sq[tt * D + tid], zacc);
+        zacc = fmaf(sds[tt], sq[tt * LD + tid], zacc);
       } else if (tid < 2 * D && p.norm == MHLA_NORM_MALA) {
         // dv~ = -sum_t gamma_t dO_t (the tile's dO was overwritten above)
         const size_t off = tok_off(p, u, block_token(p, i, lt + tt)) + (tid - D);
@@ -260,21 +263,34 @@ __device__ __forceinline__ float mc_assemble(const Plan& p, int h, int ustep, in
   return acc;
 }
 
+// 64 x 64 entries of dMc per CTA (4 x 4 per thread, rows ti + 16 a, columns
+// tb + 16 c), the record dimension taken in chunks of 32 through shared
+// memory; each unit's products are summed before they join the total.
 __global__ void __launch_bounds__(kThreads)
 bwd_mc_kernel(Plan p, const float* __restrict__ dmixp, const float* __restrict__ stack,
               const float* __restrict__ dnp, const float* __restrict__ diag, float* __restrict__ dmc, int groups,
               float* __restrict__ partial) {
-  constexpr int TI = 16, TK = 32;
-  __shared__ float sa[TI][TK + 1];
-  __shared__ float sb[TI][TK + 1];
+  constexpr int TI = kMcTile, TK = 32;
+  __shared__ float sa[TK][TI + 1];
+  __shared__ float sb[TK][TI + 1];
   const int i0 = blockIdx.y * TI, b0 = blockIdx.x * TI;
-  const int ti = threadIdx.x / TI, tb = threadIdx.x % TI;
+  const int ti = threadIdx.x / 16, tb = threadIdx.x % 16;
   const int rows = p.M * p.splits;
   const int h = (int)blockIdx.z % p.mc_heads, g = (int)blockIdx.z / p.mc_heads;
   const int ustep = p.mc_heads == 1 ? 1 : p.H;
-  float acc = 0.f;
-  for (int u = h + g * ustep; u < p.BH; u += groups * ustep) {
-    float acc_u = 0.f;
+  float acc[4][4];
+#pragma unroll
+  for (int a = 0; a < 4; ++a)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) acc[a][c] = 0.f;
+  // causal form: a tile on or above the diagonal holds no product term
+  const bool products = !(diag && b0 >= i0 + TI - 1);
+  for (int u = h + g * ustep; products && u < p.BH; u += groups * ustep) {
+    float acc_u[4][4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) acc_u[a][c] = 0.f;
     const float* da = dmixp + (size_t)u * rows * p.R;
     const float* xa = stack + (size_t)u * rows * p.R;
     for (int r0 = 0; r0 < p.R; r0 += TK) {
@@ -289,23 +305,50 @@ bwd_mc_kernel(Plan p, const float* __restrict__ dmixp, const float* __restrict__
           if (b0 + ii < p.M)
             for (int s = 0; s < p.splits; ++s) y += xa[((size_t)(b0 + ii) * p.splits + s) * p.R + r];
         }
-        sa[ii][rr] = x;
-        sb[ii][rr] = y;
+        sa[rr][ii] = x;
+        sb[rr][ii] = y;
       }
       __syncthreads();
-      float part = 0.f;
+      // each chunk's 32 products are summed before they join the unit's sum
+      float part[4][4];
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) part[a][c] = 0.f;
 #pragma unroll 8
-      for (int rr = 0; rr < TK; ++rr) part = fmaf(sa[ti][rr], sb[tb][rr], part);
-      acc_u += part;
+      for (int rr = 0; rr < TK; ++rr) {
+        float av[4], bv[4];
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+          av[a] = sa[rr][ti + 16 * a];
+          bv[a] = sb[rr][tb + 16 * a];
+        }
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) part[a][c] = fmaf(av[a], bv[c], part[a][c]);
+      }
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc_u[a][c] += part[a][c];
     }
-    acc += acc_u;
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) acc[a][c] += acc_u[a][c];
   }
-  const int i = i0 + ti, b = b0 + tb;
-  if (i >= p.M || b >= p.M) return;
-  if (groups > 1)
-    partial[(((size_t)g * p.mc_heads + h) * p.M + i) * p.M + b] = acc;
-  else
-    dmc[((size_t)h * p.M + i) * p.M + b] = mc_assemble(p, h, ustep, i, b, acc, dnp, diag);
+#pragma unroll
+  for (int a = 0; a < 4; ++a)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int i = i0 + ti + 16 * a, b = b0 + tb + 16 * c;
+      if (i >= p.M || b >= p.M) continue;
+      if (groups > 1)
+        partial[(((size_t)g * p.mc_heads + h) * p.M + i) * p.M + b] = acc[a][c];
+      else
+        dmc[((size_t)h * p.M + i) * p.M + b] = mc_assemble(p, h, ustep, i, b, acc[a][c], dnp, diag);
+    }
 }
 
 // dMc[h][i][b] from the groups' partial sums, in group order.
@@ -330,20 +373,25 @@ __global__ void __launch_bounds__(kThreads)
 bwd_summary_kernel(Plan p, const T* __restrict__ K, const T* __restrict__ V, const float* __restrict__ dstack,
                    const float* __restrict__ xk, const float* __restrict__ xv, T* __restrict__ dK,
                    T* __restrict__ dV) {
+  // rows LD = D + 1 floats apart; thread (mg, nl) keeps tokens mg, mg + MG
+  // and features nl + NL * b of the tile in registers
+  constexpr int LD = D + 1, MG = kTile / 2, NL = kThreads / MG, RN = D / NL;
+  static_assert(NL <= 32 && RN * NL == D, "tile split");
   extern __shared__ float sm[];
-  float* sS = sm;                  // D*D
-  float* sz = sS + D * D;          // D
+  float* sS = sm;                  // D rows: dS_b
+  float* sz = sS + D * LD;         // D
   float* sv = sz + D;              // D
-  float* sk = sv + D;              // kTile*D: phi(k)
-  float* sx = sk + kTile * D;      // kTile*D: v
+  float* sk = sv + D;              // kTile rows: phi(k)
+  float* sx = sk + kTile * LD;     // kTile rows: v
   const int u = blockIdx.y;
   const int row = blockIdx.x;
   const int b = row / p.splits;
   const int l0 = (row % p.splits) * p.split_len;
   const int l1 = min(p.nb, l0 + p.split_len);
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, mg = tid / NL, nl = tid % NL;
   const float* drow = dstack + ((size_t)u * p.M + b) * p.R;
-  for (int e = tid; e < D * D + 2 * D; e += kThreads) sm[e] = drow[e];
+  for (int e = tid; e < D * D; e += kThreads) sS[e / D * LD + e % D] = drow[e];
+  for (int e = tid; e < 2 * D; e += kThreads) sz[e] = drow[D * D + e];
   for (int lt = l0; lt < l1; lt += kTile) {
     const int cnt = min(kTile, l1 - lt);
     __syncthreads();
@@ -355,31 +403,52 @@ bwd_summary_kernel(Plan p, const T* __restrict__ K, const T* __restrict__ V, con
         kx = phi_apply(to_f32(K[off]), p.fmap);
         vx = to_f32(V[off]);
       }
-      sk[e] = kx;
-      sx[e] = vx;
+      sk[tt * LD + f] = kx;
+      sx[tt * LD + f] = vx;
     }
     __syncthreads();
-    for (int e = tid; e < cnt * D; e += kThreads) {
-      const int tt = e / D, f = e % D;
-      float gk = sz[f], gv = sv[f];
-      for (int m = 0; m < D; ++m) {
-        gk = fmaf(sS[f * D + m], sx[tt * D + m], gk);   // (dS_b v_j)[f]
-        gv = fmaf(sS[m * D + f], sk[tt * D + m], gv);   // (dS_b^T phi(k_j))[f]
+    float gk[2][RN], gv[2][RN];
+#pragma unroll
+    for (int c = 0; c < RN; ++c) {
+      gk[0][c] = gk[1][c] = sz[nl + NL * c];
+      gv[0][c] = gv[1][c] = sv[nl + NL * c];
+    }
+    for (int m = 0; m < D; ++m) {
+      const float x0 = sx[mg * LD + m], x1 = sx[(mg + MG) * LD + m];
+      const float k0 = sk[mg * LD + m], k1 = sk[(mg + MG) * LD + m];
+#pragma unroll
+      for (int c = 0; c < RN; ++c) {
+        const int f = nl + NL * c;
+        const float sf = sS[f * LD + m], sc = sS[m * LD + f];
+        gk[0][c] = fmaf(sf, x0, gk[0][c]);   // (dS_b v_j)[f]
+        gk[1][c] = fmaf(sf, x1, gk[1][c]);
+        gv[0][c] = fmaf(sc, k0, gv[0][c]);   // (dS_b^T phi(k_j))[f]
+        gv[1][c] = fmaf(sc, k1, gv[1][c]);
       }
-      const size_t off = tok_off(p, u, block_token(p, b, lt + tt)) + f;
-      if (xk) {
-        gk += xk[off];
-        gv += xv[off];
+    }
+#pragma unroll
+    for (int a = 0; a < 2; ++a) {
+      const int tt = mg + MG * a;
+      if (tt >= cnt) continue;
+      const size_t base = tok_off(p, u, block_token(p, b, lt + tt));
+#pragma unroll
+      for (int c = 0; c < RN; ++c) {
+        const size_t off = base + nl + NL * c;
+        float k_ = gk[a][c], v_ = gv[a][c];
+        if (xk) {
+          k_ += xk[off];
+          v_ += xv[off];
+        }
+        dK[off] = from_f32<T>(k_ * phi_grad(to_f32(K[off]), p.fmap));
+        dV[off] = from_f32<T>(v_);
       }
-      dK[off] = from_f32<T>(gk * phi_grad(to_f32(K[off]), p.fmap));
-      dV[off] = from_f32<T>(gv);
     }
   }
 }
 
 template <int D, typename T>
 int run_output(const Plan& p, const BwdBuffers& w, const void* q, const void* dout, void* dq, cudaStream_t s) {
-  const size_t smo = sizeof(float) * (D * D + 2 * D + 3 * kTile * D + 4 * kTile);
+  const size_t smo = sizeof(float) * (D * (D + 1) + 2 * D + 3 * kTile * (D + 1) + 4 * kTile);
   auto ko = bwd_output_kernel<D, T>;
   cudaError_t e = (cudaError_t)set_max_dynamic_smem((const void*)ko, (int)smo);
   if (e != cudaSuccess) return (int)e;
@@ -391,7 +460,7 @@ int run_output(const Plan& p, const BwdBuffers& w, const void* q, const void* do
 template <int D, typename T>
 int run_summary(const Plan& p, const BwdBuffers& w, const void* k, const void* v, void* dk, void* dv,
                 cudaStream_t s) {
-  const size_t sms = sizeof(float) * (D * D + 2 * D + 2 * kTile * D);
+  const size_t sms = sizeof(float) * (D * (D + 1) + 2 * D + 2 * kTile * (D + 1));
   auto ks = bwd_summary_kernel<D, T>;
   cudaError_t e = (cudaError_t)set_max_dynamic_smem((const void*)ks, (int)sms);
   if (e != cudaSuccess) return (int)e;
@@ -439,7 +508,7 @@ int launch_bwd_mix(const Plan& p, const BwdBuffers& w, void* stream) {
 int bwd_mc_groups(const Plan& p) {
   // about four CTAs per SM of a 152-SM GPU, at most one group per unit of a
   // head and 64 groups
-  const long long tiles = (long long)((p.M + 15) / 16) * ((p.M + 15) / 16) * p.mc_heads;
+  const long long tiles = (long long)((p.M + kMcTile - 1) / kMcTile) * ((p.M + kMcTile - 1) / kMcTile) * p.mc_heads;
   const int units = p.mc_heads == 1 ? p.BH : p.BH / p.H;
   long long g = (608 + tiles - 1) / tiles;
   if (g > units) g = units;
@@ -455,7 +524,8 @@ size_t bwd_mc_partial_bytes(const Plan& p) {
 int launch_bwd_mc(const Plan& p, const BwdBuffers& w, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int groups = bwd_mc_groups(p);
-  bwd_mc_kernel<<<dim3((p.M + 15) / 16, (p.M + 15) / 16, p.mc_heads * groups), kThreads, 0, s>>>(
+  const unsigned nt = (unsigned)((p.M + kMcTile - 1) / kMcTile);
+  bwd_mc_kernel<<<dim3(nt, nt, p.mc_heads * groups), kThreads, 0, s>>>(
       p, w.dmixp, w.stack, w.dnp, w.diag, w.dmc, groups, w.mc_partial);
   if (groups > 1) {
     const size_t n = (size_t)p.mc_heads * p.M * p.M;

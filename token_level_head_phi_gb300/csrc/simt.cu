@@ -19,14 +19,17 @@ namespace {
 
 constexpr int kThreads = 256;
 
-// One CTA per (stack row = block piece, head unit).  Thread e owns the
-// entries e, e + 256, ... of the row-major d x d summary.
+// One CTA per (stack row = block piece, head unit).  A thread keeps RT x RT
+// entries of the d x d summary, rows fi + FQ a and columns ci + FQ b, so that
+// one token's phi(k) and v values each serve RT products.
 template <int D, typename Tin>
 __global__ void __launch_bounds__(kThreads)
 simt_summary_kernel(Plan p, const Tin* __restrict__ K, const Tin* __restrict__ V,
                     float* __restrict__ stack) {
   constexpr int TT = 32;
-  constexpr int PER = (D * D + kThreads - 1) / kThreads;
+  constexpr int RT = D * D >= 16 * kThreads ? 4 : (D * D >= 4 * kThreads ? 2 : 1);
+  constexpr int FQ = D / RT;
+  constexpr int FT = (FQ * FQ + kThreads - 1) / kThreads;
   __shared__ float sk[TT * D];
   __shared__ float sv[TT * D];
   const int u = blockIdx.y;
@@ -36,9 +39,13 @@ simt_summary_kernel(Plan p, const Tin* __restrict__ K, const Tin* __restrict__ V
   const int l1 = min(p.nb, l0 + p.split_len);
   const int tid = threadIdx.x;
 
-  float acc[PER];
+  float acc[FT][RT][RT];
 #pragma unroll
-  for (int j = 0; j < PER; ++j) acc[j] = 0.f;
+  for (int x = 0; x < FT; ++x)
+#pragma unroll
+    for (int a = 0; a < RT; ++a)
+#pragma unroll
+      for (int c = 0; c < RT; ++c) acc[x][a][c] = 0.f;
   float zacc = 0.f, vacc = 0.f;
 
   for (int lt = l0; lt < l1; lt += TT) {
@@ -56,21 +63,39 @@ simt_summary_kernel(Plan p, const Tin* __restrict__ K, const Tin* __restrict__ V
       sv[e] = vx;
     }
     __syncthreads();
-    for (int tt = 0; tt < cnt; ++tt) {
 #pragma unroll
-      for (int j = 0; j < PER; ++j) {
-        const int e = tid + j * kThreads;
-        if (e < D * D) acc[j] = fmaf(sk[tt * D + e / D], sv[tt * D + e % D], acc[j]);
+    for (int x = 0; x < FT; ++x) {
+      const int qd = tid + kThreads * x;
+      if (qd >= FQ * FQ) break;
+      const int fi = qd / FQ, ci = qd % FQ;
+      for (int tt = 0; tt < cnt; ++tt) {
+        float ka[RT], vb[RT];
+#pragma unroll
+        for (int a = 0; a < RT; ++a) {
+          ka[a] = sk[tt * D + fi + FQ * a];
+          vb[a] = sv[tt * D + ci + FQ * a];
+        }
+#pragma unroll
+        for (int a = 0; a < RT; ++a)
+#pragma unroll
+          for (int c = 0; c < RT; ++c) acc[x][a][c] = fmaf(ka[a], vb[c], acc[x][a][c]);
       }
+    }
+    for (int tt = 0; tt < cnt; ++tt) {
       if (tid < D) zacc += sk[tt * D + tid];
       else if (tid < 2 * D) vacc += sv[tt * D + tid - D];
     }
   }
   float* out = stack + ((size_t)u * p.M * p.splits + row) * p.R;
 #pragma unroll
-  for (int j = 0; j < PER; ++j) {
-    const int e = tid + j * kThreads;
-    if (e < D * D) out[e] = acc[j];
+  for (int x = 0; x < FT; ++x) {
+    const int qd = tid + kThreads * x;
+    if (qd >= FQ * FQ) break;
+    const int fi = qd / FQ, ci = qd % FQ;
+#pragma unroll
+    for (int a = 0; a < RT; ++a)
+#pragma unroll
+      for (int c = 0; c < RT; ++c) out[(fi + FQ * a) * D + ci + FQ * c] = acc[x][a][c];
   }
   if (tid < D) out[D * D + tid] = zacc;
   else if (tid < 2 * D) out[D * D + tid] = vacc;
