@@ -30,7 +30,7 @@ struct CausalBwdBuffers {
   float* dmixp;               // [BH][M * splits][R] out: dSp_i, dzp_i, dvp_i in the block's first piece row
   float* dnp;                 // [BH][M * splits] out: dnp_i (MALA), likewise
   float* diag;                // [BH][M] out: in-block term of dMc[i][i]
-  float* tokbuf;              // [BH][N][d + 2] scratch: dnum_t, ds_t, gamma_t
+  float* tokbuf;              // [BH][N][d + 4] scratch: dnum_t, ds_t, gamma_t (16-byte rows)
   float* xk;                  // [BH][N][d] out: in-block part of dphi(k)
   float* xv;                  // [BH][N][d] out: in-block part of dv
 };

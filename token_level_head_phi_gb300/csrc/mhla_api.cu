@@ -513,7 +513,7 @@ mhla_status make_bwd_plan(const mhla_params* prm, Plan* plan, BwdLayout* lay) {
     if (plan->causal) {
       const size_t toks = (size_t)plan->BH * plan->N;
       take(lay->mcl, sizeof(float) * (size_t)plan->M * plan->M * mh);
-      take(lay->tokbuf, sizeof(float) * toks * (plan->d + 2));
+      take(lay->tokbuf, sizeof(float) * toks * (plan->d + 4));
       take(lay->xk, sizeof(float) * toks * plan->d);
       take(lay->xv, sizeof(float) * toks * plan->d);
       take(lay->diag, sizeof(float) * mrows);

@@ -65,10 +65,28 @@ struct Geo {
   static_assert(TH * TH <= kThreads && 2 * D <= kThreads, "tile split");
 };
 
+// Token rows of the per-token buffer the forward walk leaves for the reverse
+// walk: dnum (D), ds, gamma and two floats of padding (16-byte rows).
+template <int D>
+struct TokRow {
+  static constexpr int value = D + 4;
+};
+
 template <int D>
 constexpr size_t fwd_smem_floats() {
   using G = Geo<D>;
   return 2 * D * G::LD + 4 * D + 5 * G::TQ * G::LD + G::TQ * G::TQ + 6 * G::TQ + 4 * kWarps;
+}
+
+// Bytes of the raw tiles in front of the float arrays: four token arrays
+// (forward walk) or four token arrays and the per-token rows (reverse walk).
+template <int D, typename T>
+__host__ __device__ constexpr size_t fwd_raw_bytes() {
+  return 4 * (size_t)Geo<D>::TQ * D * sizeof(T);
+}
+template <int D, typename T>
+__host__ __device__ constexpr size_t rev_raw_bytes() {
+  return 4 * (size_t)Geo<D>::TQ * D * sizeof(T) + (size_t)Geo<D>::TQ * TokRow<D>::value * sizeof(float);
 }
 
 template <int D>
@@ -93,6 +111,31 @@ __device__ __forceinline__ float group_sum(float x) {
 
 __device__ __forceinline__ float phi_grad(float x, int fmap) { return phi_deriv(x, phi_apply(x, fmap), fmap); }
 
+// Asynchronous 16-byte copies global -> shared: the next tile's raw rows
+// land while the current tile is worked on.
+__device__ __forceinline__ void cpa16(void* dst, const void* src) {
+  const uint32_t d = (uint32_t)__cvta_generic_to_shared(dst);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(d), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cpa_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void cpa_wait_all() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
+
+// Copies the raw rows of tile l0 (cnt tokens of block i, unit u) of the
+// first n of the token arrays s0..s3 into raw[a][TQ][D] (rows at or past
+// cnt are left as they are).
+template <int D, int TQ, typename T>
+__device__ __forceinline__ void prefetch_rows(const Plan& p, int u, int i, int l0, int cnt, const T* s0,
+                                              const T* s1, const T* s2, const T* s3, int n, T* raw) {
+  constexpr int CH = D * (int)sizeof(T) / 16;   // 16-byte pieces per row
+  constexpr int EPC = 16 / (int)sizeof(T);      // elements per piece
+  for (int e = threadIdx.x; e < n * TQ * CH; e += kThreads) {
+    const int a = e / (TQ * CH), r = e % (TQ * CH), tt = r / CH, ch = r % CH;
+    const T* src = a == 0 ? s0 : (a == 1 ? s1 : (a == 2 ? s2 : s3));
+    if (tt < cnt)
+      cpa16(raw + ((size_t)a * TQ + tt) * D + ch * EPC, src + tok_off(p, u, block_token(p, i, l0 + tt)) + ch * EPC);
+  }
+}
+
 // Shared memory: C = Sp_i + w R and R (D rows each), zp, vp, rz, rv (D each)
 // | tiles of phi(q), phi(k), v, dO, dnum (TQ rows each) | in-tile scores,
 // later the in-tile dq weights E (TQ*TQ) | per token s, phi(q).rz, n, coef,
@@ -106,7 +149,9 @@ causal_bwd_fwd_kernel(Plan p, const T* __restrict__ Q, const T* __restrict__ K, 
                       float* __restrict__ tokbuf) {
   using G = Geo<D>;
   constexpr int TQ = G::TQ, LD = G::LD, MG = G::MG, NL = G::NL, RN = G::RN, TH = G::TH, FQ = G::FQ, FT = G::FT;
-  extern __shared__ float sm[];
+  extern __shared__ __align__(16) unsigned char smraw[];
+  T* raw = reinterpret_cast<T*>(smraw);   // Q, K, V, dO rows of the next tile [4][TQ][D]
+  float* sm = reinterpret_cast<float*>(smraw + fwd_raw_bytes<D, T>());
   float* sC = sm;               // Sp_i + w R
   float* sR = sC + D * LD;      // in-block state R (without w)
   float* zP = sR + D * LD;
@@ -158,18 +203,20 @@ causal_bwd_fwd_kernel(Plan p, const T* __restrict__ Q, const T* __restrict__ K, 
   double nacc = 0.0, dacc = 0.0;
   float rn = 0.f;  // tokens of the block before the tile
 
+  prefetch_rows<D, TQ>(p, u, i, 0, min(TQ, p.nb), Q, K, V, dO, 4, raw);
+  cpa_commit();
   for (int l0 = 0; l0 < p.nb; l0 += TQ) {
     const int cnt = min(TQ, p.nb - l0);
+    cpa_wait_all();
     __syncthreads();
     for (int e = tid; e < TQ * D; e += kThreads) {
       const int tt = e / D, f = e % D;
       float qx = 0.f, kx = 0.f, vx = 0.f, gx = 0.f;
       if (tt < cnt) {
-        const size_t off = tok_off(p, u, block_token(p, i, l0 + tt)) + f;
-        qx = phi_apply(to_f32(Q[off]), p.fmap);
-        kx = phi_apply(to_f32(K[off]), p.fmap);
-        vx = to_f32(V[off]);
-        gx = to_f32(dO[off]);
+        qx = phi_apply(to_f32(raw[e]), p.fmap);
+        kx = phi_apply(to_f32(raw[TQ * D + e]), p.fmap);
+        vx = to_f32(raw[2 * TQ * D + e]);
+        gx = to_f32(raw[3 * TQ * D + e]);
       }
       sq[tt * LD + f] = qx;
       sk[tt * LD + f] = kx;
@@ -177,6 +224,8 @@ causal_bwd_fwd_kernel(Plan p, const T* __restrict__ Q, const T* __restrict__ K, 
       sg[tt * LD + f] = gx;
     }
     __syncthreads();
+    if (l0 + TQ < p.nb) prefetch_rows<D, TQ>(p, u, i, l0 + TQ, min(TQ, p.nb - l0 - TQ), Q, K, V, dO, 4, raw);
+    cpa_commit();
     // masked in-tile scores a[t][j] = phi(q_t) . phi(k_j), j <= t
     if (tid < TH * TH) {
       const int ti = tid / TH, ji = tid % TH;
@@ -423,7 +472,7 @@ causal_bwd_fwd_kernel(Plan p, const T* __restrict__ Q, const T* __restrict__ K, 
     for (int e = tid; e < cnt * (D + 2); e += kThreads) {
       const int tt = e / (D + 2), c = e % (D + 2);
       const float x = c < D ? sdn[tt * LD + c] : (c == D ? sds[tt] : sgm[tt]);
-      tokbuf[((size_t)u * p.N + block_token(p, i, l0 + tt)) * (D + 2) + c] = x;
+      tokbuf[((size_t)u * p.N + block_token(p, i, l0 + tt)) * TokRow<D>::value + c] = x;
     }
     rn += (float)cnt;
   }
@@ -479,7 +528,10 @@ causal_bwd_rev_kernel(Plan p, const T* __restrict__ Q, const T* __restrict__ K, 
                       float* __restrict__ xk, float* __restrict__ xv) {
   using G = Geo<D>;
   constexpr int TQ = G::TQ, LD = G::LD, MG = G::MG, NL = G::NL, RN = G::RN, TH = G::TH, FQ = G::FQ, FT = G::FT;
-  extern __shared__ float sm[];
+  extern __shared__ __align__(16) unsigned char smraw[];
+  T* raw = reinterpret_cast<T*>(smraw);   // Q, K, V, dO rows of the next tile [4][TQ][D]
+  float* rtok = reinterpret_cast<float*>(smraw + 4 * (size_t)TQ * D * sizeof(T));  // [TQ][TokRow]
+  float* sm = reinterpret_cast<float*>(smraw + rev_raw_bytes<D, T>());
   float* GS = sm;
   float* Gz = GS + D * LD;
   float* Gv = Gz + D;
@@ -498,21 +550,34 @@ causal_bwd_rev_kernel(Plan p, const T* __restrict__ Q, const T* __restrict__ K, 
   const bool mala = p.norm == MHLA_NORM_MALA;
   for (int e = tid; e < D * LD + 2 * D; e += kThreads) sm[e] = 0.f;
 
+  constexpr int TR = TokRow<D>::value;
+  const int narr = mala ? 4 : 3;
+  // raw rows of tile l0: the token arrays and the forward walk's per-token rows
+  auto prefetch = [&](int l0n) {
+    const int cntn = min(TQ, p.nb - l0n);
+    prefetch_rows<D, TQ>(p, u, i, l0n, cntn, Q, K, V, dO, narr, raw);
+    for (int e = tid; e < TQ * (TR / 4); e += kThreads) {
+      const int tt = e / (TR / 4), ch = e % (TR / 4);
+      if (tt < cntn)
+        cpa16(rtok + tt * TR + 4 * ch, tokbuf + ((size_t)u * p.N + block_token(p, i, l0n + tt)) * TR + 4 * ch);
+    }
+    cpa_commit();
+  };
+  prefetch((p.nb - 1) / TQ * TQ);
   for (int l0 = (p.nb - 1) / TQ * TQ; l0 >= 0; l0 -= TQ) {
     const int cnt = min(TQ, p.nb - l0);
+    cpa_wait_all();
     __syncthreads();
     for (int e = tid; e < TQ * D; e += kThreads) {
       const int tt = e / D, f = e % D;
       float qx = 0.f, kx = 0.f, vx = 0.f, dn = 0.f, gv = 0.f;
       if (tt < cnt) {
-        const int tok = block_token(p, i, l0 + tt);
-        const size_t off = tok_off(p, u, tok) + f;
-        const float* tb = tokbuf + ((size_t)u * p.N + tok) * (D + 2);
-        qx = phi_apply(to_f32(Q[off]), p.fmap);
-        kx = phi_apply(to_f32(K[off]), p.fmap);
-        vx = to_f32(V[off]);
+        const float* tb = rtok + tt * TR;
+        qx = phi_apply(to_f32(raw[e]), p.fmap);
+        kx = phi_apply(to_f32(raw[TQ * D + e]), p.fmap);
+        vx = to_f32(raw[2 * TQ * D + e]);
         dn = tb[f];
-        if (mala) gv = -tb[D + 1] * to_f32(dO[off]);
+        if (mala) gv = -tb[D + 1] * to_f32(raw[3 * TQ * D + e]);
         if (f == 0) sds[tt] = tb[D];
       } else if (f == 0) {
         sds[tt] = 0.f;
@@ -524,6 +589,7 @@ causal_bwd_rev_kernel(Plan p, const T* __restrict__ Q, const T* __restrict__ K, 
       sgv[tt * LD + f] = gv;
     }
     __syncthreads();
+    if (l0 >= TQ) prefetch(l0 - TQ);
     // E[j][t] and P[j][t] for t >= j
     if (tid < TH * TH) {
       const int ji = tid / TH, ti = tid % TH;
@@ -646,8 +712,8 @@ causal_bwd_rev_kernel(Plan p, const T* __restrict__ Q, const T* __restrict__ K, 
 template <int D, typename T>
 int run(const Plan& p, const CausalBwdBuffers& c, const void* q, const void* k, const void* v, const void* dout,
         void* dq, cudaStream_t s) {
-  const size_t smf = sizeof(float) * fwd_smem_floats<D>();
-  const size_t smr = sizeof(float) * rev_smem_floats<D>();
+  const size_t smf = fwd_raw_bytes<D, T>() + sizeof(float) * fwd_smem_floats<D>();
+  const size_t smr = rev_raw_bytes<D, T>() + sizeof(float) * rev_smem_floats<D>();
   auto kf = causal_bwd_fwd_kernel<D, T>;
   auto kr = causal_bwd_rev_kernel<D, T>;
   cudaError_t e = (cudaError_t)set_max_dynamic_smem((const void*)kf, (int)smf);
