@@ -9,10 +9,11 @@
 // Multi-Head", key design 2 with its chunkwise, streaming remarks; the pages
 // define no causal form, this is the block-ordered reading).  The mixing
 // kernel forms S<_i with the masked copy of Mc that launch_mc_strict_lower
-// writes.  One CTA per (block, head) walks the block in 32-token tiles: the
-// tile's own causal part is a masked 32 x 32 score matrix, the part before it
-// is the running state S<_i + Mc[i,i] (sum of the earlier tiles), kept in
-// shared memory and advanced after each tile.
+// writes.  One CTA per (block, head) walks the block in 32-token tiles (16 at
+// d = 128): the tile's own causal part is a masked score matrix, the part
+// before it is the running state S<_i + Mc[i,i] (sum of the earlier tiles),
+// kept in shared memory and advanced after each tile; the next tile's rows
+// arrive by asynchronous copies while the current one is worked on.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -22,7 +23,7 @@ namespace mhla {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kTQ = 32;
+constexpr int kWarps = kThreads / 32;
 
 // mcl = Mc with its diagonal and upper triangle zeroed, for `heads` matrices.
 __global__ void strict_lower_kernel(int heads, int M, const float* __restrict__ mc, float* __restrict__ mcl) {
@@ -32,101 +33,243 @@ __global__ void strict_lower_kernel(int heads, int M, const float* __restrict__ 
   mcl[idx] = b < i ? mc[idx] : 0.f;
 }
 
-// Shared memory: state S (D*D), z (D), v (D) | phi(q), phi(k), v tiles
-// (kTQ*D each) | scores (kTQ*kTQ) | per-token s (kTQ).
+// Tile geometry: every step is a small product on shared-memory tiles whose
+// rows are LD = D + 1 floats apart (a warp reading one column of consecutive
+// rows hits 32 banks), split so that a thread keeps a register tile:
+//   token x feature   (TQ x D): 2 x RN, rows mg + MG a, columns nl + NL b
+//   token x token     (TQ x TQ): 2 x 2, rows ti + TH a, columns ji + TH b
+//   feature x feature (D x D): 4 x 4, rows fi + FQ a, columns ci + FQ b
+template <int D>
+struct Geo {
+  static constexpr int TQ = D <= 64 ? 32 : 16;
+  static constexpr int LD = D + 1;
+  static constexpr int MG = TQ / 2;
+  static constexpr int NL = kThreads / MG;
+  static constexpr int RN = D / NL;
+  static constexpr int TH = TQ / 2;
+  static constexpr int FQ = D / 4;
+  static constexpr int FT = (FQ * FQ + kThreads - 1) / kThreads;
+  static_assert(NL <= 32 && 32 % NL == 0 && RN >= 1 && RN * NL == D, "token x feature split");
+  static_assert(TH * TH <= kThreads && 2 * D <= kThreads, "tile split");
+};
+
 template <int D, typename T>
-__global__ void __launch_bounds__(kThreads)
+__host__ __device__ constexpr size_t raw_bytes() {
+  return 3 * (size_t)Geo<D>::TQ * D * sizeof(T);
+}
+
+template <int D>
+constexpr size_t smem_floats() {
+  using G = Geo<D>;
+  return D * G::LD + 2 * D + 3 * G::TQ * G::LD + G::TQ * G::TQ + G::TQ;
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+// Asynchronous 16-byte copies global -> shared (the next tile's raw rows).
+__device__ __forceinline__ void cpa16(void* dst, const void* src) {
+  const uint32_t d = (uint32_t)__cvta_generic_to_shared(dst);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(d), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cpa_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void cpa_wait_all() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
+
+// Raw Q, K, V rows of tile l0 (cnt tokens of block i, unit u) into raw[3][TQ][D].
+template <int D, int TQ, typename T>
+__device__ __forceinline__ void prefetch_rows(const Plan& p, int u, int i, int l0, int cnt, const T* q, const T* k,
+                                              const T* v, T* raw) {
+  constexpr int CH = D * (int)sizeof(T) / 16;
+  constexpr int EPC = 16 / (int)sizeof(T);
+  for (int e = threadIdx.x; e < 3 * TQ * CH; e += kThreads) {
+    const int a = e / (TQ * CH), r = e % (TQ * CH), tt = r / CH, ch = r % CH;
+    const T* src = a == 0 ? q : (a == 1 ? k : v);
+    if (tt < cnt)
+      cpa16(raw + ((size_t)a * TQ + tt) * D + ch * EPC, src + tok_off(p, u, block_token(p, i, l0 + tt)) + ch * EPC);
+  }
+  cpa_commit();
+}
+
+// Shared memory: raw Q, K, V rows of the next tile | state S (D rows), z, v
+// (D each) | phi(q), phi(k), v tiles (TQ rows each) | scores (TQ*TQ) |
+// per-token s (TQ).
+template <int D, typename T>
+__global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1)
 causal_output_kernel(Plan p, const T* __restrict__ Q, const T* __restrict__ K, const T* __restrict__ V,
                      const float* __restrict__ mixed, const float* __restrict__ rowsum_lower,
                      const float* __restrict__ mc, T* __restrict__ out) {
-  extern __shared__ float sm[];
-  float* sS = sm;                   // D*D
-  float* sz = sS + D * D;           // D
+  using G = Geo<D>;
+  constexpr int TQ = G::TQ, LD = G::LD, MG = G::MG, NL = G::NL, RN = G::RN, TH = G::TH, FQ = G::FQ, FT = G::FT;
+  extern __shared__ __align__(16) unsigned char smraw[];
+  T* raw = reinterpret_cast<T*>(smraw);
+  float* sm = reinterpret_cast<float*>(smraw + raw_bytes<D, T>());
+  float* sS = sm;                   // D rows
+  float* sz = sS + D * LD;          // D
   float* sv = sz + D;               // D
-  float* sq = sv + D;               // kTQ*D
-  float* sk = sq + kTQ * D;         // kTQ*D
-  float* sx = sk + kTQ * D;         // kTQ*D (values)
-  float* sa = sx + kTQ * D;         // kTQ*kTQ
-  float* ss = sa + kTQ * kTQ;       // kTQ
+  float* sq = sv + D;               // TQ rows
+  float* sk = sq + TQ * LD;         // TQ rows
+  float* sx = sk + TQ * LD;         // TQ rows (values)
+  float* sa = sx + TQ * LD;         // TQ*TQ
+  float* ss = sa + TQ * TQ;         // TQ
   const int u = blockIdx.y;
   const int i = blockIdx.x;
-  const int tid = threadIdx.x;
-  const int j = mc_index(p, u);
-  const float w = mc[((size_t)j * p.M + i) * p.M + i];
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const int mg = tid / NL, nl = tid % NL;
+  const int jm = mc_index(p, u);
+  const float w = mc[((size_t)jm * p.M + i) * p.M + i];
+  prefetch_rows<D, TQ>(p, u, i, 0, min(TQ, p.nb), Q, K, V, raw);
   const float* mrow = mixed + ((size_t)u * p.M + i) * p.R;
-  for (int e = tid; e < D * D + 2 * D; e += kThreads) sm[e] = mrow[e];
-  float n_state = (float)p.nb * rowsum_lower[j * p.M + i];   // n<_i
+  for (int e = tid; e < D * D; e += kThreads) sS[e / D * LD + e % D] = mrow[e];
+  for (int e = tid; e < 2 * D; e += kThreads) sz[e] = mrow[D * D + e];
+  float n_state = (float)p.nb * rowsum_lower[jm * p.M + i];   // n<_i
 
-  for (int l0 = 0; l0 < p.nb; l0 += kTQ) {
-    const int cnt = min(kTQ, p.nb - l0);
+  for (int l0 = 0; l0 < p.nb; l0 += TQ) {
+    const int cnt = min(TQ, p.nb - l0);
+    cpa_wait_all();
     __syncthreads();
-    for (int e = tid; e < kTQ * D; e += kThreads) {
+    for (int e = tid; e < TQ * D; e += kThreads) {
       const int tt = e / D, f = e % D;
       float qx = 0.f, kx = 0.f, vx = 0.f;
       if (tt < cnt) {
-        const size_t off = tok_off(p, u, block_token(p, i, l0 + tt)) + f;
-        qx = phi_apply(to_f32(Q[off]), p.fmap);
-        kx = phi_apply(to_f32(K[off]), p.fmap);
-        vx = to_f32(V[off]);
+        qx = phi_apply(to_f32(raw[e]), p.fmap);
+        kx = phi_apply(to_f32(raw[TQ * D + e]), p.fmap);
+        vx = to_f32(raw[2 * TQ * D + e]);
       }
-      sq[e] = qx;
-      sk[e] = kx;
-      sx[e] = vx;
+      sq[tt * LD + f] = qx;
+      sk[tt * LD + f] = kx;
+      sx[tt * LD + f] = vx;
     }
     __syncthreads();
+    if (l0 + TQ < p.nb) prefetch_rows<D, TQ>(p, u, i, l0 + TQ, min(TQ, p.nb - l0 - TQ), Q, K, V, raw);
     // masked in-tile scores a[t][j] = phi(q_t) . phi(k_j), j <= t
-    for (int e = tid; e < kTQ * kTQ; e += kThreads) {
-      const int tt = e / kTQ, j = e % kTQ;
-      float a = 0.f;
-      if (j <= tt && tt < cnt) {
-        for (int f = 0; f < D; ++f) a = fmaf(sq[tt * D + f], sk[j * D + f], a);
+    if (tid < TH * TH) {
+      const int ti = tid / TH, ji = tid % TH;
+      float c2[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+      for (int f = 0; f < D; ++f) {
+        const float q0 = sq[ti * LD + f], q1 = sq[(ti + TH) * LD + f];
+        const float k0 = sk[ji * LD + f], k1 = sk[(ji + TH) * LD + f];
+        c2[0][0] = fmaf(q0, k0, c2[0][0]);
+        c2[0][1] = fmaf(q0, k1, c2[0][1]);
+        c2[1][0] = fmaf(q1, k0, c2[1][0]);
+        c2[1][1] = fmaf(q1, k1, c2[1][1]);
       }
-      sa[e] = a;
+#pragma unroll
+      for (int a = 0; a < 2; ++a)
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+          const int tt = ti + TH * a, jj = ji + TH * b;
+          sa[tt * TQ + jj] = (jj <= tt && tt < cnt) ? c2[a][b] : 0.f;
+        }
+    }
+    // phi(q_t)^T S_state, kept in registers
+    float num[2][RN];
+#pragma unroll
+    for (int a = 0; a < 2; ++a)
+#pragma unroll
+      for (int b = 0; b < RN; ++b) num[a][b] = 0.f;
+    for (int f = 0; f < D; ++f) {
+      const float x0 = sq[mg * LD + f], x1 = sq[(mg + MG) * LD + f];
+#pragma unroll
+      for (int b = 0; b < RN; ++b) {
+        const float sv_ = sS[f * LD + nl + NL * b];
+        num[0][b] = fmaf(x0, sv_, num[0][b]);
+        num[1][b] = fmaf(x1, sv_, num[1][b]);
+      }
     }
     __syncthreads();
     // denominators s_t = phi(q_t) . z_state + w sum_{j <= t} a[t][j]
-    if (tid < kTQ) {
-      float s = 0.f, r = 0.f;
-      for (int f = 0; f < D; ++f) s = fmaf(sq[tid * D + f], sz[f], s);
-      for (int j = 0; j <= tid; ++j) r += sa[tid * kTQ + j];
-      ss[tid] = fmaf(w, r, s);
+    for (int tt = warp; tt < TQ; tt += kWarps) {
+      float s = 0.f;
+      for (int f = lane; f < D; f += 32) s = fmaf(sq[tt * LD + f], sz[f], s);
+      const float r = warp_sum(lane < TQ ? sa[tt * TQ + lane] : 0.f);
+      s = warp_sum(s);
+      if (lane == 0) ss[tt] = fmaf(w, r, s);
     }
     __syncthreads();
-    for (int e = tid; e < cnt * D; e += kThreads) {
-      const int tt = e / D, c = e % D;
-      float num = 0.f, loc = 0.f, vloc = 0.f;
-      for (int f = 0; f < D; ++f) num = fmaf(sq[tt * D + f], sS[f * D + c], num);
-      for (int j = 0; j <= tt; ++j) {
-        loc = fmaf(sa[tt * kTQ + j], sx[j * D + c], loc);
-        vloc += sx[j * D + c];
+    // in-tile part sum_{j<=t} a[t][j] v_j (and sum_{j<=t} v_j), then the norm
+    {
+      float lo[2][RN], vl[2][RN];
+#pragma unroll
+      for (int a = 0; a < 2; ++a)
+#pragma unroll
+        for (int b = 0; b < RN; ++b) lo[a][b] = vl[a][b] = 0.f;
+      const int t0 = mg, t1 = mg + MG;
+      for (int jj = 0; jj < cnt; ++jj) {
+        const float a0 = sa[t0 * TQ + jj], a1 = sa[t1 * TQ + jj];
+        const float m0 = jj <= t0 ? 1.f : 0.f, m1 = jj <= t1 ? 1.f : 0.f;
+#pragma unroll
+        for (int b = 0; b < RN; ++b) {
+          const float xv = sx[jj * LD + nl + NL * b];
+          lo[0][b] = fmaf(a0, xv, lo[0][b]);
+          lo[1][b] = fmaf(a1, xv, lo[1][b]);
+          vl[0][b] = fmaf(m0, xv, vl[0][b]);
+          vl[1][b] = fmaf(m1, xv, vl[1][b]);
+        }
       }
-      num = fmaf(w, loc, num);
-      const float s = ss[tt];
-      float o = num;
-      if (p.norm == MHLA_NORM_DIVISIVE) {
-        o = s != 0.f ? num / s : 0.f;
-      } else if (p.norm == MHLA_NORM_MALA) {
-        const float ntil = n_state + w * (float)(tt + 1);
-        const float vt = sv[c] + w * vloc;
-        o = s != 0.f ? (1.f + 1.f / s) * num - (s / ntil) * vt : 0.f;
+#pragma unroll
+      for (int a = 0; a < 2; ++a) {
+        const int tt = mg + MG * a;
+        if (tt >= cnt) continue;
+        const float s = ss[tt];
+        const size_t base = tok_off(p, u, block_token(p, i, l0 + tt));
+#pragma unroll
+        for (int b = 0; b < RN; ++b) {
+          const int c = nl + NL * b;
+          const float nm = fmaf(w, lo[a][b], num[a][b]);
+          float o = nm;
+          if (p.norm == MHLA_NORM_DIVISIVE) {
+            o = s != 0.f ? nm / s : 0.f;
+          } else if (p.norm == MHLA_NORM_MALA) {
+            const float ntil = n_state + w * (float)(tt + 1);
+            const float vt = sv[c] + w * vl[a][b];
+            o = s != 0.f ? (1.f + 1.f / s) * nm - (s / ntil) * vt : 0.f;
+          }
+          out[base + c] = from_f32<T>(o);
+        }
       }
-      out[tok_off(p, u, block_token(p, i, l0 + tt)) + c] = from_f32<T>(o);
     }
     __syncthreads();
     // advance the state by the whole tile: S += w sum_j phi(k_j) v_j^T (z, v, n)
-    for (int e = tid; e < D * D; e += kThreads) {
-      const int f = e / D, c = e % D;
-      float acc = 0.f;
-      for (int j = 0; j < cnt; ++j) acc = fmaf(sk[j * D + f], sx[j * D + c], acc);
-      sS[e] = fmaf(w, acc, sS[e]);
+#pragma unroll
+    for (int x = 0; x < FT; ++x) {
+      const int qd = tid + kThreads * x;
+      if (qd >= FQ * FQ) break;
+      const int fi = qd / FQ, ci = qd % FQ;
+      float st[4][4];
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) st[a][b] = 0.f;
+      for (int jj = 0; jj < cnt; ++jj) {
+        float ka[4], xb[4];
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+          ka[a] = sk[jj * LD + fi + FQ * a];
+          xb[a] = sx[jj * LD + ci + FQ * a];
+        }
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+          for (int b = 0; b < 4; ++b) st[a][b] = fmaf(ka[a], xb[b], st[a][b]);
+      }
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          const int e = (fi + FQ * a) * LD + ci + FQ * b;
+          sS[e] = fmaf(w, st[a][b], sS[e]);
+        }
     }
     if (tid < D) {
       float a = 0.f;
-      for (int j = 0; j < cnt; ++j) a += sk[j * D + tid];
+      for (int jj = 0; jj < cnt; ++jj) a += sk[jj * LD + tid];
       sz[tid] = fmaf(w, a, sz[tid]);
     } else if (tid < 2 * D) {
       float a = 0.f;
-      for (int j = 0; j < cnt; ++j) a += sx[j * D + tid - D];
+      for (int jj = 0; jj < cnt; ++jj) a += sx[jj * LD + tid - D];
       sv[tid - D] = fmaf(w, a, sv[tid - D]);
     }
     n_state = fmaf(w, (float)cnt, n_state);
@@ -136,7 +279,7 @@ causal_output_kernel(Plan p, const T* __restrict__ Q, const T* __restrict__ K, c
 template <int D, typename T>
 int run(const Plan& p, const void* q, const void* k, const void* v, const float* mixed, const float* rl,
         const float* mc, void* out, cudaStream_t s) {
-  const size_t smem = sizeof(float) * (D * D + 2 * D + 3 * kTQ * D + kTQ * kTQ + kTQ);
+  const size_t smem = raw_bytes<D, T>() + sizeof(float) * smem_floats<D>();
   auto kern = causal_output_kernel<D, T>;
   cudaError_t e = (cudaError_t)set_max_dynamic_smem((const void*)kern, (int)smem);
   if (e != cudaSuccess) return (int)e;
