@@ -19,9 +19,26 @@ namespace {
 
 constexpr int kThreads = 256;
 
+// RT consecutive floats of shared memory (16- or 8-byte aligned for RT = 4, 2).
+template <int RT>
+__device__ __forceinline__ void lds_vec(const float* src, float (&x)[RT]) {
+  if constexpr (RT == 4) {
+    const float4 t = *reinterpret_cast<const float4*>(src);
+    x[0] = t.x; x[1] = t.y; x[2] = t.z; x[3] = t.w;
+  } else if constexpr (RT == 2) {
+    const float2 t = *reinterpret_cast<const float2*>(src);
+    x[0] = t.x; x[1] = t.y;
+  } else {
+    x[0] = src[0];
+  }
+}
+
 // One CTA per (stack row = block piece, head unit).  A thread keeps RT x RT
-// entries of the d x d summary, rows fi + FQ a and columns ci + FQ b, so that
-// one token's phi(k) and v values each serve RT products.
+// entries of the d x d summary, rows RT fi + a and columns RT ci + b, and
+// reads each token's RT phi(k) and RT v values as one vector; the next tile's
+// K and V values are loaded into registers while the current tile is
+// multiplied.  z_b and v_b: each thread sums its own feature (tid % D) over
+// its tokens, and the threads of a feature are summed at the end.
 template <int D, typename Tin>
 __global__ void __launch_bounds__(kThreads)
 simt_summary_kernel(Plan p, const Tin* __restrict__ K, const Tin* __restrict__ V,
@@ -30,8 +47,10 @@ simt_summary_kernel(Plan p, const Tin* __restrict__ K, const Tin* __restrict__ V
   constexpr int RT = D * D >= 16 * kThreads ? 4 : (D * D >= 4 * kThreads ? 2 : 1);
   constexpr int FQ = D / RT;
   constexpr int FT = (FQ * FQ + kThreads - 1) / kThreads;
-  __shared__ float sk[TT * D];
-  __shared__ float sv[TT * D];
+  constexpr int PT = TT * D / kThreads;   // values of each array a thread loads per tile
+  static_assert(kThreads % D == 0 && PT >= 1, "token split");
+  __shared__ __align__(16) float sk[TT * D];
+  __shared__ __align__(16) float sv[TT * D];
   const int u = blockIdx.y;
   const int row = blockIdx.x;
   const int b = row / p.splits;
@@ -46,23 +65,37 @@ simt_summary_kernel(Plan p, const Tin* __restrict__ K, const Tin* __restrict__ V
     for (int a = 0; a < RT; ++a)
 #pragma unroll
       for (int c = 0; c < RT; ++c) acc[x][a][c] = 0.f;
-  float zacc = 0.f, vacc = 0.f;
-
+  float zp = 0.f, vp = 0.f;   // feature tid % D, over this thread's tokens
+  Tin rk[PT], rv[PT];
+  auto fetch = [&](int lt) {
+    const int cnt = min(TT, l1 - lt);
+#pragma unroll
+    for (int m = 0; m < PT; ++m) {
+      const int e = tid + m * kThreads, tt = e / D;
+      if (tt < cnt) {
+        const size_t off = tok_off(p, u, block_token(p, b, lt + tt)) + e % D;
+        rk[m] = K[off];
+        rv[m] = V[off];
+      }
+    }
+  };
+  if (l0 < l1) fetch(l0);
   for (int lt = l0; lt < l1; lt += TT) {
     const int cnt = min(TT, l1 - lt);
     __syncthreads();
-    for (int e = tid; e < TT * D; e += kThreads) {
-      const int tt = e / D, f = e % D;
-      float kx = 0.f, vx = 0.f;
-      if (tt < cnt) {
-        const size_t off = tok_off(p, u, block_token(p, b, lt + tt)) + f;
-        kx = phi_apply(to_f32(K[off]), p.fmap);
-        vx = to_f32(V[off]);
-      }
+#pragma unroll
+    for (int m = 0; m < PT; ++m) {
+      const int e = tid + m * kThreads;
+      const bool in = e / D < cnt;
+      const float kx = in ? phi_apply(to_f32(rk[m]), p.fmap) : 0.f;
+      const float vx = in ? to_f32(rv[m]) : 0.f;
       sk[e] = kx;
       sv[e] = vx;
+      zp += kx;
+      vp += vx;
     }
     __syncthreads();
+    if (lt + TT < l1) fetch(lt + TT);
 #pragma unroll
     for (int x = 0; x < FT; ++x) {
       const int qd = tid + kThreads * x;
@@ -70,20 +103,13 @@ simt_summary_kernel(Plan p, const Tin* __restrict__ K, const Tin* __restrict__ V
       const int fi = qd / FQ, ci = qd % FQ;
       for (int tt = 0; tt < cnt; ++tt) {
         float ka[RT], vb[RT];
-#pragma unroll
-        for (int a = 0; a < RT; ++a) {
-          ka[a] = sk[tt * D + fi + FQ * a];
-          vb[a] = sv[tt * D + ci + FQ * a];
-        }
+        lds_vec<RT>(sk + tt * D + RT * fi, ka);
+        lds_vec<RT>(sv + tt * D + RT * ci, vb);
 #pragma unroll
         for (int a = 0; a < RT; ++a)
 #pragma unroll
           for (int c = 0; c < RT; ++c) acc[x][a][c] = fmaf(ka[a], vb[c], acc[x][a][c]);
       }
-    }
-    for (int tt = 0; tt < cnt; ++tt) {
-      if (tid < D) zacc += sk[tt * D + tid];
-      else if (tid < 2 * D) vacc += sv[tt * D + tid - D];
     }
   }
   float* out = stack + ((size_t)u * p.M * p.splits + row) * p.R;
@@ -95,10 +121,21 @@ simt_summary_kernel(Plan p, const Tin* __restrict__ K, const Tin* __restrict__ V
 #pragma unroll
     for (int a = 0; a < RT; ++a)
 #pragma unroll
-      for (int c = 0; c < RT; ++c) out[(fi + FQ * a) * D + ci + FQ * c] = acc[x][a][c];
+      for (int c = 0; c < RT; ++c) out[(RT * fi + a) * D + RT * ci + c] = acc[x][a][c];
   }
-  if (tid < D) out[D * D + tid] = zacc;
-  else if (tid < 2 * D) out[D * D + tid] = vacc;
+  __syncthreads();
+  sk[tid] = zp;
+  sv[tid] = vp;
+  __syncthreads();
+  if (tid < D) {
+    float z = 0.f, v = 0.f;
+    for (int g = 0; g < kThreads / D; ++g) {
+      z += sk[tid + D * g];
+      v += sv[tid + D * g];
+    }
+    out[D * D + tid] = z;
+    out[D * D + D + tid] = v;
+  }
 }
 
 // mixed[u][i][r] = sum_row Mc[i][row / splits] * stack[u][row][r]: a plain
