@@ -34,15 +34,18 @@ __global__ void strict_lower_kernel(int heads, int M, const float* __restrict__ 
 }
 
 // Tile geometry: every step is a small product on shared-memory tiles whose
-// rows are LD = D + 1 floats apart (a warp reading one column of consecutive
-// rows hits 32 banks), split so that a thread keeps a register tile:
-//   token x feature   (TQ x D): 2 x RN, rows mg + MG a, columns nl + NL b
+// rows are LD = D + 4 floats apart (16-byte rows, so a thread reads up to
+// four consecutive values as one vector; 8 consecutive rows start in 8
+// different 16-byte bank groups), split so that a thread keeps a register
+// tile:
+//   token x feature   (TQ x D): 2 x RN, rows mg + MG a, columns RN nl + b
 //   token x token     (TQ x TQ): 2 x 2, rows ti + TH a, columns ji + TH b
-//   feature x feature (D x D): 4 x 4, rows fi + FQ a, columns ci + FQ b
+//                     (the feature sum taken four features at a time)
+//   feature x feature (D x D): 4 x 4, rows 4 fi + a, columns 4 ci + b
 template <int D>
 struct Geo {
   static constexpr int TQ = D <= 64 ? 32 : 16;
-  static constexpr int LD = D + 1;
+  static constexpr int LD = D + 4;
   static constexpr int MG = TQ / 2;
   static constexpr int NL = kThreads / MG;
   static constexpr int RN = D / NL;
@@ -62,6 +65,20 @@ template <int D>
 constexpr size_t smem_floats() {
   using G = Geo<D>;
   return D * G::LD + 2 * D + 3 * G::TQ * G::LD + G::TQ * G::TQ + G::TQ;
+}
+
+// RT consecutive floats of shared memory as one vector (RT = 4, 2 or 1).
+template <int RT>
+__device__ __forceinline__ void lds_vec(const float* src, float (&x)[RT]) {
+  if constexpr (RT == 4) {
+    const float4 t = *reinterpret_cast<const float4*>(src);
+    x[0] = t.x; x[1] = t.y; x[2] = t.z; x[3] = t.w;
+  } else if constexpr (RT == 2) {
+    const float2 t = *reinterpret_cast<const float2*>(src);
+    x[0] = t.x; x[1] = t.y;
+  } else {
+    x[0] = src[0];
+  }
 }
 
 __device__ __forceinline__ float warp_sum(float x) {
@@ -148,13 +165,19 @@ causal_output_kernel(Plan p, const T* __restrict__ Q, const T* __restrict__ K, c
     if (tid < TH * TH) {
       const int ti = tid / TH, ji = tid % TH;
       float c2[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
-      for (int f = 0; f < D; ++f) {
-        const float q0 = sq[ti * LD + f], q1 = sq[(ti + TH) * LD + f];
-        const float k0 = sk[ji * LD + f], k1 = sk[(ji + TH) * LD + f];
-        c2[0][0] = fmaf(q0, k0, c2[0][0]);
-        c2[0][1] = fmaf(q0, k1, c2[0][1]);
-        c2[1][0] = fmaf(q1, k0, c2[1][0]);
-        c2[1][1] = fmaf(q1, k1, c2[1][1]);
+      for (int f = 0; f < D; f += 4) {
+        float q0[4], q1[4], k0[4], k1[4];
+        lds_vec<4>(sq + ti * LD + f, q0);
+        lds_vec<4>(sq + (ti + TH) * LD + f, q1);
+        lds_vec<4>(sk + ji * LD + f, k0);
+        lds_vec<4>(sk + (ji + TH) * LD + f, k1);
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+          c2[0][0] = fmaf(q0[x], k0[x], c2[0][0]);
+          c2[0][1] = fmaf(q0[x], k1[x], c2[0][1]);
+          c2[1][0] = fmaf(q1[x], k0[x], c2[1][0]);
+          c2[1][1] = fmaf(q1[x], k1[x], c2[1][1]);
+        }
       }
 #pragma unroll
       for (int a = 0; a < 2; ++a)
@@ -172,11 +195,12 @@ causal_output_kernel(Plan p, const T* __restrict__ Q, const T* __restrict__ K, c
       for (int b = 0; b < RN; ++b) num[a][b] = 0.f;
     for (int f = 0; f < D; ++f) {
       const float x0 = sq[mg * LD + f], x1 = sq[(mg + MG) * LD + f];
+      float cv[RN];
+      lds_vec<RN>(sS + f * LD + RN * nl, cv);
 #pragma unroll
       for (int b = 0; b < RN; ++b) {
-        const float sv_ = sS[f * LD + nl + NL * b];
-        num[0][b] = fmaf(x0, sv_, num[0][b]);
-        num[1][b] = fmaf(x1, sv_, num[1][b]);
+        num[0][b] = fmaf(x0, cv[b], num[0][b]);
+        num[1][b] = fmaf(x1, cv[b], num[1][b]);
       }
     }
     __syncthreads();
@@ -200,13 +224,14 @@ causal_output_kernel(Plan p, const T* __restrict__ Q, const T* __restrict__ K, c
       for (int jj = 0; jj < cnt; ++jj) {
         const float a0 = sa[t0 * TQ + jj], a1 = sa[t1 * TQ + jj];
         const float m0 = jj <= t0 ? 1.f : 0.f, m1 = jj <= t1 ? 1.f : 0.f;
+        float xv[RN];
+        lds_vec<RN>(sx + jj * LD + RN * nl, xv);
 #pragma unroll
         for (int b = 0; b < RN; ++b) {
-          const float xv = sx[jj * LD + nl + NL * b];
-          lo[0][b] = fmaf(a0, xv, lo[0][b]);
-          lo[1][b] = fmaf(a1, xv, lo[1][b]);
-          vl[0][b] = fmaf(m0, xv, vl[0][b]);
-          vl[1][b] = fmaf(m1, xv, vl[1][b]);
+          lo[0][b] = fmaf(a0, xv[b], lo[0][b]);
+          lo[1][b] = fmaf(a1, xv[b], lo[1][b]);
+          vl[0][b] = fmaf(m0, xv[b], vl[0][b]);
+          vl[1][b] = fmaf(m1, xv[b], vl[1][b]);
         }
       }
 #pragma unroll
@@ -217,7 +242,7 @@ causal_output_kernel(Plan p, const T* __restrict__ Q, const T* __restrict__ K, c
         const size_t base = tok_off(p, u, block_token(p, i, l0 + tt));
 #pragma unroll
         for (int b = 0; b < RN; ++b) {
-          const int c = nl + NL * b;
+          const int c = RN * nl + b;
           const float nm = fmaf(w, lo[a][b], num[a][b]);
           float o = nm;
           if (p.norm == MHLA_NORM_DIVISIVE) {
@@ -245,11 +270,8 @@ causal_output_kernel(Plan p, const T* __restrict__ Q, const T* __restrict__ K, c
         for (int b = 0; b < 4; ++b) st[a][b] = 0.f;
       for (int jj = 0; jj < cnt; ++jj) {
         float ka[4], xb[4];
-#pragma unroll
-        for (int a = 0; a < 4; ++a) {
-          ka[a] = sk[jj * LD + fi + FQ * a];
-          xb[a] = sx[jj * LD + ci + FQ * a];
-        }
+        lds_vec<4>(sk + jj * LD + 4 * fi, ka);
+        lds_vec<4>(sx + jj * LD + 4 * ci, xb);
 #pragma unroll
         for (int a = 0; a < 4; ++a)
 #pragma unroll
@@ -259,7 +281,7 @@ causal_output_kernel(Plan p, const T* __restrict__ Q, const T* __restrict__ K, c
       for (int a = 0; a < 4; ++a)
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
-          const int e = (fi + FQ * a) * LD + ci + FQ * b;
+          const int e = (4 * fi + a) * LD + 4 * ci + b;
           sS[e] = fmaf(w, st[a][b], sS[e]);
         }
     }
