@@ -369,6 +369,20 @@ def run_mine(args, w: wl.Workload, world: int, rank: int, local: int, dist, samp
         total_ms = start.elapsed_time(end)
     else:
         total_ms = sum(a.elapsed_time(b) for a, b in step_ev)
+    # inputs that fit in L2: the same steps back to back without the flush
+    # (warm L2), reported beside the cold-L2 number
+    warm = None
+    if flush is not None:
+        wa, wb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        step()
+        wa.record(stream)
+        for _ in range(K):
+            step()
+        wb.record(stream)
+        torch.cuda.synchronize()
+        wms = wa.elapsed_time(wb) / K
+        warm = {"ms_per_step": wms, "value": w.units * w.n_tokens / (wms / 1e3), "unit": UNIT,
+                "l2": "warm: no flush, steps back to back"}
 
     # per-phase breakdown (for the dominant kernel's roofline): a separate
     # run with events between the kernels, which serialise them
@@ -420,6 +434,7 @@ def run_mine(args, w: wl.Workload, world: int, rank: int, local: int, dist, samp
                           "bound": "hbm" if t_hbm >= t_tc else "tensor", "frac": t_roof / (ms_per_step / 1e3),
                           "peak_hbm_gbs": hbm, "peak_bf16_tflops_sustained": tf_sust, "peak_source": peak_kind},
         "phase_ms": avg_phase,
+        "warm_l2": warm,
         "phase_note": "per-kernel times from a separate run with events between the kernels (which serialises "
                       "the launches the timed steps overlap)",
         "gpu_launches": info.kernels_per_call * K,
@@ -466,6 +481,7 @@ def run_per_config(args, world, rank, local, dist):
             "variant_name": r["config"]["variant_name"], "dtype": w.dtype, "norm": w.norm,
             "host_us_per_call": r["host_us_per_call"],
             "steps": sub.steps, "warmup": sub.warmup, "l2": r["config"]["l2"],
+            "warm_l2": r.get("warm_l2"),
         }
     return out
 
@@ -784,9 +800,12 @@ print(json.dumps({{"times": times, "units": units}}))
 
 
 def oracle_run(w: wl.Workload, budget_s: float, max_units: int, per_step: bool, backward: bool = False,
-               fmap: str = "elu1", causal: bool = False):
-    """Runs the oracle in a fresh process (BLAS threads = available cores)."""
+               fmap: str = "elu1", causal: bool = False, threads: int = 0):
+    """Runs the oracle in a fresh process (BLAS threads = available cores,
+    or `threads`)."""
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    if threads > 0:
+        cores = threads
     env = dict(os.environ)
     for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
         env[var] = str(cores)
@@ -805,9 +824,14 @@ def cpu_baseline(w: wl.Workload, budget_s: float = 15.0, backward: bool = False,
                                      causal=causal)
     total = sum(times)
     what = ("causal " if causal else "") + ("backward" if backward else "forward")
+    # the same oracle on one BLAS thread, on a shorter sample
+    t1, u1, _ = oracle_run(w, budget_s / 3, max_units=10 ** 6, per_step=False, backward=backward, fmap=fmap,
+                           causal=causal, threads=1)
     return {"value": units * w.n_tokens / total, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"{units} of {w.units} (batch, head) units of {w.name}, float64 NumPy {what} oracle, "
-                      f"{total:.1f} s of CPU time; input generation excluded"}
+                      f"{total:.1f} s of CPU time; input generation excluded",
+            "one_thread": {"value": u1 * w.n_tokens / sum(t1), "unit": UNIT, "cores": 1,
+                           "sample": f"{u1} units, {sum(t1):.1f} s"}}
 
 
 def run_reference(args, w: wl.Workload):
