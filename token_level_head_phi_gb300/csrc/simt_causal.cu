@@ -114,7 +114,7 @@ __device__ __forceinline__ void prefetch_rows(const Plan& p, int u, int i, int l
 // (D each) | phi(q), phi(k), v tiles (TQ rows each) | scores (TQ*TQ) |
 // per-token s (TQ).
 template <int D, typename T>
-__global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1)
+__global__ void __launch_bounds__(kThreads, D <= 64 ? 3 : 1)
 causal_output_kernel(Plan p, const T* __restrict__ Q, const T* __restrict__ K, const T* __restrict__ V,
                      const float* __restrict__ mixed, const float* __restrict__ rowsum_lower,
                      const float* __restrict__ mc, T* __restrict__ out) {
